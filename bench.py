@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Benchmark of position-independent KV stitching on GB300.
+
+One step = one pass of the whole path over one batch: compose the request(s)
+and build the block table (host, C ABI), upload the table, and one pic_stitch
+launch (gather + delta-RoPE + paged scatter + recompute list).  Inputs are
+resident in HBM when the timed region starts; the pool and the cache are
+both larger than L2 (no flush needed).  Prints ONE JSON line on rank 0.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+build) on the same workload, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+WORKLOAD_TEXT = {
+    "llama31_8b_rag": "Llama-3.1-8B shapes: 32 layers, 8 KV heads x 128, bf16, RoPE theta 5e5 + llama3 "
+                      "scaling (neox); 128-token system prompt + 10 x 1024-token chunks in seeded "
+                      "permutation; paged block 16; batch 1; recompute first 4 tokens of non-leading chunks",
+    "tiny_gqa": "1 layer, 8 KV heads x 128, theta 1e4 neox, 32-token prefix + 4 x 256 chunks, block 16",
+    "qwen3_8b_batch": "Qwen3-8B shapes: 36 layers, 8 KV heads x 128, theta 1e6; 8 requests x 32,768 tokens "
+                      "from a 64-chunk pool (lengths U[128,4096]), per-request random order; block 16",
+    "deepseek_v3_mla": "DeepSeek-V3 MLA shapes: 61 layers, 512 latent + 64 rope (interleaved), theta 1e4; "
+                       "65,536 tokens of 16-128-token chunks behind a 32-token leading chunk; block 16",
+    "serving_stress": "Llama-3.1-8B shapes; 64 requests x 16,384 tokens, Zipf(1.1) reuse of a 256-chunk "
+                      "pool with log-uniform lengths 64-8192; block 16",
+}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def bytes_per_token_layer(model, mode):
+    row = model.num_kv_heads * model.head_dim * 2
+    if mode == "inplace":
+        return 2 * row                       # K read + K write
+    return 4 * row if model.kind == "gqa" else 2 * row   # pool read + cache write (K and V)
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "position_independent_kv_stitch_gb300", "csrc", "pic_kernels.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, mode):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(f"{workload}/{mode}")
+        if e and e.get("kernel_source_sha256_16") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1].split()[0]))
+                    mx.append(float(parts[2].split()[0]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle
+
+def run_oracle_sample(wl, pool_k_bits, pool_v_bits, layers):
+    """The oracle as it stands, on the given pool layers of every request."""
+    import oracle
+    m = wl.model
+    theta = oracle.model_inv_freq(m.rope_dim, m.rope_theta, m.llama3)
+    pairing = oracle.NEOX_HALF if m.pairing == "neox" else oracle.INTERLEAVED
+    chunks = [oracle.Chunk(off, n, 0) for off, n in zip(wl.pool_offsets, wl.chunk_lens)]
+    nb = sum(-(-t // m.block_size) for t in wl.request_tokens)
+    pool = oracle.BlockPool(nb)
+    plans, tables = [], []
+    for req in wl.requests:
+        segs = oracle.compose(chunks, [c for c, _ in req], take=[t for _, t in req])
+        total = segs[-1].dst_pos + segs[-1].length
+        tables.append(pool.allocate(oracle.blocks_needed(total, m.block_size)))
+        plans.append(segs)
+        oracle.recompute_positions(segs, wl.k_nonleading, wl.k_leading)
+    oracle.stitch_paged(pool_k_bits, pool_v_bits, plans, tables, nb, m.block_size, theta, pairing,
+                        m.rope_offset, m.rope_dim, layers=layers)
+
+
+def host_pool_bits(wl, which, layers):
+    """bf16 bits of the given pool layers, drawn on the host (the oracle's own inputs)."""
+    import torch
+    t = W.make_pool(W.Workload(wl.name, W.Model(**{**wl.model.__dict__, "num_layers": len(layers)}),
+                               wl.chunk_lens, wl.requests, wl.k_nonleading, wl.k_leading), which, "cpu")
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """Oracle GB/s on a bounded sample: whole requests, as many layers as fit
+    in about budget_s seconds of one host core."""
+    m = wl.model
+    kb = host_pool_bits(wl, "k", [0])
+    vb = host_pool_bits(wl, "v", [0]) if m.kind == "gqa" else None
+    t0 = time.perf_counter()
+    run_oracle_sample(wl, kb, vb, [0])
+    t1 = time.perf_counter() - t0
+    n = int(max(1, min(m.num_layers - 1, budget_s / max(t1, 1e-3) - 1)))
+    kb = np.repeat(kb, n, axis=0)
+    vb = np.repeat(vb, n, axis=0) if vb is not None else None
+    t0 = time.perf_counter()
+    run_oracle_sample(wl, kb, vb, list(range(n)))
+    el = time.perf_counter() - t0
+    tl = sum(wl.request_tokens) * n
+    gbs = tl * bytes_per_token_layer(m, "stitch") / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} layer(s) x all {sum(wl.request_tokens)} tokens of the workload "
+                      f"({tl} token-layers, {el:.1f} s, fp64 numpy, single thread)",
+            "tokens_layers_per_s": tl / el}
+
+
+def run_reference(args, wl):
+    """Reference arm: the fp64 oracle timed on the host, one layer of the whole
+    workload per step."""
+    m = wl.model
+    kb = host_pool_bits(wl, "k", [0])
+    vb = host_pool_bits(wl, "v", [0]) if m.kind == "gqa" else None
+    for _ in range(args.warmup):
+        run_oracle_sample(wl, kb, vb, [0])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run_oracle_sample(wl, kb, vb, [0])
+        times.append(time.perf_counter() - t0)
+    el = sum(times)
+    tl = sum(wl.request_tokens) * args.steps
+    gbs = tl * bytes_per_token_layer(m, "stitch") / el / 1e9
+    line = {
+        "impl": "reference", "metric": "stitched KV GB/s", "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {WORKLOAD_TEXT.get(wl.name, '')}",
+                   "step": "one layer of every request (bounded sample)"},
+        "tokens_layers_per_s": tl / el,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"1 layer x {sum(wl.request_tokens)} tokens per step"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU arm
+
+class Rig:
+    """Everything one rank needs to run steps of a workload through the C ABI."""
+
+    def __init__(self, wl, device, mode):
+        import torch
+        from position_independent_kv_stitch_gb300 import pic
+        self.torch, self.pic = torch, pic
+        self.wl, self.m, self.dev, self.mode = wl, wl.model, device, mode
+        m = wl.model
+        self.bs = m.block_size
+        self.nb = sum(-(-t // self.bs) for t in wl.request_tokens)
+        self.max_blocks = max(-(-t // self.bs) for t in wl.request_tokens)
+        self.ctx = pic.create_from_spec(pic.model_spec_from(m), self.nb)
+        self.ids = [pic.pic_register_chunk(self.ctx, W.chunk_key(wl.name, c), off, n)[0]
+                    for c, (off, n) in enumerate(zip(wl.pool_offsets, wl.chunk_lens))]
+        self.k_pool = W.make_pool(wl, "k", device=device)
+        self.v_pool = W.make_pool(wl, "v", device=device) if m.kind == "gqa" else None
+        shape = (m.num_layers, self.nb, self.bs) + tuple(m.row_shape)
+        self.k_cache = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=device) if m.kind == "gqa" else None
+        plans, bt = self.plan()
+        self.n_rec = sum(pic.pic_plan_info(p)["num_recompute"] for p in plans)
+        self.ws_bytes = pic.pic_workspace_bytes(self.ctx, plans)
+        self.free(plans)
+        self.ridx = torch.empty(max(1, self.n_rec), dtype=torch.int32, device=device)
+        self.indptr = torch.empty(len(wl.requests) + 1, dtype=torch.int32, device=device)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.d_bt = torch.empty((len(wl.requests), self.max_blocks), dtype=torch.int32, device=device)
+        self.bt_pinned = [torch.empty_like(self.d_bt, device="cpu").pin_memory() for _ in range(2)]
+        self.bt_events = [None, None]
+        self.slot = 0
+        self.shift_segs = None
+        if mode == "inplace":
+            self.shift_segs = self._shift_segments()
+            self.ws_shift = torch.empty(pic.pic_rerotate_workspace_bytes(self.ctx, self.shift_segs),
+                                        dtype=torch.uint8, device=device)
+
+    def _shift_segments(self):
+        plans, bt = self.plan()
+        segs = []
+        for r, plan in enumerate(plans):
+            for j in range(self.pic.pic_plan_info(plan)["num_segments"]):
+                s = self.pic.pic_plan_segment(plan, j)
+                new = self.wl.new_pos[r][j] if self.wl.new_pos else s["dst_pos"] + 100003
+                segs.append((r, s["dst_pos"], s["num_tokens"], new - s["dst_pos"]))
+        self.d_bt.copy_(self.torch.from_numpy(bt))
+        self._kept_plans = plans
+        return segs
+
+    def plan(self):
+        pic, wl = self.pic, self.wl
+        plans, tables = [], []
+        for req in wl.requests:
+            plan, bt = pic.pic_build_block_table(self.ctx, [self.ids[c] for c, _ in req], self.max_blocks,
+                                                 take_tokens=[t for _, t in req],
+                                                 k_nonleading=wl.k_nonleading, k_leading=wl.k_leading)
+            plans.append(plan)
+            tables.append(bt)
+        return plans, np.stack(tables)
+
+    def free(self, plans):
+        for p in plans:
+            self.pic.pic_free_request(self.ctx, p)
+
+    def upload_tables(self, bt):
+        s = self.slot
+        if self.bt_events[s] is not None:
+            self.bt_events[s].synchronize()
+        self.bt_pinned[s].numpy()[...] = bt
+        self.d_bt.copy_(self.bt_pinned[s], non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record()
+        self.bt_events[s] = ev
+        self.slot ^= 1
+
+    def step(self, kernel_events=None):
+        """One step: plan + table upload + one launch; returns nothing."""
+        if self.mode == "inplace":
+            if kernel_events:
+                kernel_events[0].record()
+            self.pic.pic_rerotate_inplace(self.ctx, self.k_cache, self.d_bt, self.shift_segs, self.ws_shift)
+            if kernel_events:
+                kernel_events[1].record()
+            return
+        plans, bt = self.plan()
+        self.upload_tables(bt)
+        if kernel_events:
+            kernel_events[0].record()
+        self.pic.pic_stitch(self.ctx, plans, self.k_pool, self.v_pool, self.k_cache, self.v_cache, self.d_bt,
+                            self.ridx, self.indptr, self.ws)
+        if kernel_events:
+            kernel_events[1].record()
+        self.free(plans)
+
+    def check_status(self):
+        ws = self.ws_shift if self.mode == "inplace" else self.ws
+        self.pic.pic_query_device_status(self.ctx, ws)
+
+
+def run_e2e(rig, steps, warmup):
+    """Same metric end to end through the public API: every step copies the
+    pool from pinned host memory to the GPU, plans, stitches, and reads the
+    stitched caches and the recompute list back into pinned host memory."""
+    torch = rig.torch
+    hk = rig.k_pool.cpu().pin_memory()
+    hv = rig.v_pool.cpu().pin_memory() if rig.v_pool is not None else None
+    ok = torch.empty_like(rig.k_cache, device="cpu").pin_memory()
+    ov = torch.empty_like(rig.v_cache, device="cpu").pin_memory() if rig.v_cache is not None else None
+    oi = torch.empty_like(rig.ridx, device="cpu").pin_memory()
+    op = torch.empty_like(rig.indptr, device="cpu").pin_memory()
+
+    def one():
+        rig.k_pool.copy_(hk, non_blocking=True)
+        if hv is not None:
+            rig.v_pool.copy_(hv, non_blocking=True)
+        rig.step()
+        ok.copy_(rig.k_cache, non_blocking=True)
+        if ov is not None:
+            ov.copy_(rig.v_cache, non_blocking=True)
+        oi.copy_(rig.ridx, non_blocking=True)
+        op.copy_(rig.indptr, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = hk.numel() * 2 + (hv.numel() * 2 if hv is not None else 0) + rig.d_bt.numel() * 4 + rig.ws_bytes
+    d2h = ok.numel() * 2 + (ov.numel() * 2 if ov is not None else 0) + oi.numel() * 4 + op.numel() * 4
+    return ms, h2d, d2h
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pic", choices=["pic", "reference"])
+    ap.add_argument("--workload", default="llama31_8b_rag", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--mode", default="stitch", choices=["stitch", "inplace"])
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small profiling captures only)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = W.WORKLOADS[args.workload]()
+    if args.layers:
+        wl = W.Workload(wl.name, W.Model(**{**wl.model.__dict__, "num_layers": args.layers}), wl.chunk_lens,
+                        wl.requests, wl.k_nonleading, wl.k_leading, wl.new_pos)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from position_independent_kv_stitch_gb300 import pic
+    pic.load()  # fails loudly when libpic is not built
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    rig = Rig(wl, dev, args.mode)
+    for _ in range(args.warmup):
+        rig.step()
+    torch.cuda.synchronize()
+    rig.check_status()
+
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        rig.step(kev[i])
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    rig.check_status()
+    ms = t0.elapsed_time(t1) / args.steps
+    kms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    tl = wl.token_layers
+    bpt = bytes_per_token_layer(wl.model, args.mode)
+    algo_bytes = tl * bpt
+    peak, peak_kind = measured_peak()
+    value = world * algo_bytes / (ms * 1e-3) / 1e9
+    achieved = algo_bytes / (kms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name, args.mode)
+
+    e2e = None
+    if not args.no_e2e and args.mode == "stitch":
+        ems, h2d, d2h = run_e2e(rig, max(3, min(args.steps, 10)), 3)
+        if world > 1:
+            tt = torch.tensor([ems], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": world * algo_bytes / (ems * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(wl)
+
+    kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
+             "inplace": "k_rotate_rows<in place>"}[args.mode]
+    line = {
+        "metric": "stitched KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {WORKLOAD_TEXT.get(wl.name, '')}"
+                   + (f" [layers overridden to {args.layers}]" if args.layers else ""), "mode": args.mode,
+                   "token_layers_per_step_per_gpu": tl, "algorithmic_bytes_per_step_per_gpu": algo_bytes,
+                   "bytes_per_token_layer": bpt, "requests_per_gpu": len(wl.requests),
+                   "l2": "no flush: pool and cache are each larger than the 129 MB L2",
+                   "parallelism": f"replicas x{world} (independent requests per GPU, no collective)"},
+        "tokens_layers_per_s": world * tl / (ms * 1e-3),
+        "pct_hbm_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
+                     "launch_ms": kms},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    pic.pic_destroy(rig.ctx)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,331 @@
+/*
+ * pic.h -- C ABI of the position-independent KV stitching library (libpic).
+ *
+ * What the library does.  Each document chunk's KV cache is computed once, at
+ * virtual offset 0, and kept in a chunk pool in GPU memory.  A request lists
+ * chunks in any order; the library places them at their new absolute
+ * positions in the request's paged KV cache.  On the way, the RoPE part of
+ * every cached key is re-rotated by the chunk's position shift
+ * delta = dst_pos - base_pos, using R(a + b) = R(a) R(b); values (GQA) and
+ * the MLA latent are copied bit for bit.  The same pass writes the list of
+ * token positions to recompute (the first k tokens of each chunk).
+ *
+ * Sources (pages, cited by title and section):
+ *   [EPIC]     "EPIC Guide: Position-Independent Caching for LLM Serving"
+ *              (aifetchly blog, on EPIC, ICML 2025).
+ *   [Irminsul] "Irminsul: MLA-Native Position-Independent Caching for Agentic
+ *              LLM Serving" (gist.science explainer), Technical Summary.
+ *   [SemPIC]   "SemPIC: Learning Semantic Position-Independent KV Caches"
+ *              (agihunt summary), cache-hit serving paragraph.
+ *
+ * Conventions for every function:
+ *   - Ownership: the caller owns every device buffer (pools, caches, block
+ *     tables, index outputs, workspaces).  The library never allocates device
+ *     memory.  It owns its host-side registry, block allocator and pic_plan
+ *     objects.
+ *   - Streams: all device work is enqueued on the caller's stream and is
+ *     asynchronous; host arguments may be reused as soon as a call returns.
+ *   - Errors: every call returns a pic_status; on failure nothing was
+ *     enqueued and pic_last_error() describes the cause.  CUDA launch
+ *     failures are PIC_ERR_CUDA.  Errors a kernel finds on the device (a
+ *     block-table entry outside the cache) skip the faulty write and raise a
+ *     status word in the workspace, read by pic_query_device_status().
+ *     Kernels never trap and never wait on anything, so they cannot hang.
+ *   - Layouts (bf16 elements, row = one token of one layer):
+ *       GQA key/value row: [num_kv_heads][head_dim], RoPE over all of head_dim.
+ *       MLA row: [latent_dim + rope_dim] with the rope key last ([Irminsul]
+ *       2.1: 512-d cKV latent, 64-d k_r).
+ *       Pool:  [num_layers] x (layer stride) of [pool_tokens][row].
+ *       Cache: [num_layers] x (layer stride) of [num_cache_blocks][block_size][row].
+ *     Base pointers and layer strides must be multiples of 16 bytes.
+ *   - Positions are int32; |delta| must be below 2^24.
+ */
+#ifndef PIC_H
+#define PIC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* pic_stream_t;
+
+#define PIC_ABI_VERSION 1
+#define PIC_KEY_BYTES 32
+#define PIC_MAX_ABS_DELTA ((1 << 24) - 1)
+
+typedef enum pic_status {
+  PIC_OK = 0,
+  PIC_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum, bad plan      */
+  PIC_ERR_UNKNOWN_CHUNK = 2, /* chunk id or key not in the registry                  */
+  PIC_ERR_KEY_CONFLICT = 3,  /* key already registered with another length/base_pos  */
+  PIC_ERR_OUT_OF_BLOCKS = 4, /* block allocator cannot cover the request             */
+  PIC_ERR_CAPACITY = 5,      /* an output or workspace buffer is too small           */
+  PIC_ERR_RANGE = 6,         /* position, delta or token range out of bounds         */
+  PIC_ERR_ALIGNMENT = 7,     /* pointer or stride not a multiple of 16 bytes         */
+  PIC_ERR_CUDA = 8,          /* a CUDA runtime call or launch failed                 */
+  PIC_ERR_DEVICE_CHECK = 9,  /* a kernel found a bad block-table entry               */
+  PIC_ERR_UNSUPPORTED = 10   /* geometry this build has no kernel for                */
+} pic_status;
+
+enum { PIC_KIND_GQA = 0, PIC_KIND_MLA = 1 };
+/* NEOX_HALF pairs dims (i, i + d/2); INTERLEAVED pairs (2i, 2i + 1), the
+ * layout [EPIC] "Mathematical Foundations" 1. prints. */
+enum { PIC_PAIRING_NEOX_HALF = 0, PIC_PAIRING_INTERLEAVED = 1 };
+enum { PIC_SCALING_NONE = 0, PIC_SCALING_LLAMA3 = 1 };
+
+/* Device status word bits (pic_query_device_status). */
+#define PIC_DEV_BAD_BLOCK 0x1u /* a block-table entry was < 0 or >= num_cache_blocks */
+
+/*
+ * Model geometry and RoPE settings.
+ *   GQA: num_kv_heads >= 1, head_dim in {64, 128, 256}, rope_dim == head_dim,
+ *        rope_offset == 0.
+ *   MLA: num_kv_heads == 1, head_dim == latent + rope (576), rope_dim == 64,
+ *        rope_offset == 512.
+ * Frequencies: theta_i = rope_theta^(-2i/rope_dim) ([EPIC] "Mathematical
+ * Foundations" 1.), optionally with Llama-3.1 scaling (not on the pages;
+ * the public rule), or exactly the rope_dim/2 values in inv_freq when that
+ * pointer is non-NULL (copied at pic_create; any other RoPE scaling scheme can
+ * be supplied this way).
+ */
+typedef struct pic_model_desc {
+  int32_t kind;              /* PIC_KIND_GQA or PIC_KIND_MLA                       */
+  int32_t num_layers;        /* >= 1                                               */
+  int32_t num_kv_heads;      /* GQA: heads per row; MLA: 1                         */
+  int32_t head_dim;          /* GQA: dims per head; MLA: row width                 */
+  int32_t rope_dim;          /* dims rotated per head (even)                       */
+  int32_t rope_offset;       /* first rotated dim inside a head                    */
+  int32_t pairing;           /* PIC_PAIRING_*                                      */
+  int32_t block_size;        /* tokens per paged block, 1 .. 256                   */
+  int32_t scaling;           /* PIC_SCALING_*                                      */
+  int32_t llama3_orig_max_pos;
+  double rope_theta;
+  double llama3_factor;
+  double llama3_low_freq_factor;
+  double llama3_high_freq_factor;
+  const double* inv_freq;    /* optional: rope_dim/2 frequencies (radians/token)   */
+} pic_model_desc;
+
+typedef struct pic_ctx pic_ctx;
+typedef struct pic_plan pic_plan;
+
+/*
+ * One request: the prompt's chunks in order ([EPIC] "Algorithmic
+ * Architecture" 2. Modular Prompt Composer).
+ *   chunk_ids    n_chunks registered ids; a chunk may appear more than once
+ *                (each occurrence is its own segment).
+ *   take_tokens  NULL = whole chunks; else tokens taken from the start of
+ *                each chunk (0 .. num_tokens).
+ *   dst_pos      NULL = chunk j starts where chunk j-1 ended, the first at
+ *                start_pos; else the absolute position of each chunk's first
+ *                token, non-decreasing and non-overlapping (the "offset" of
+ *                [EPIC] "Production Deployment Playbook" 2.).  Gaps hold
+ *                inline tokens the caller computes itself.
+ *   total_tokens logical length the block table must cover; 0 = the end of
+ *                the last chunk.  Must not be smaller than that end.
+ *   k_nonleading tokens recomputed at the start of every chunk not at
+ *                position 0 (LegoLink pseudo-sinks; [EPIC] uses 4).
+ *   k_leading    tokens recomputed at the start of a chunk at position 0
+ *                ([Irminsul] 2.2 First-Chunk Carve-Out uses 32).
+ */
+typedef struct pic_request_desc {
+  const int32_t* chunk_ids;
+  const int32_t* take_tokens;
+  const int32_t* dst_pos;
+  int32_t n_chunks;
+  int32_t start_pos;
+  int32_t total_tokens;
+  int32_t k_nonleading;
+  int32_t k_leading;
+} pic_request_desc;
+
+/* One in-place shift: rows [start_pos, start_pos + num_tokens) of block-table
+ * row `req` are rotated by `delta`. */
+typedef struct pic_shift_seg {
+  int32_t req;
+  int32_t start_pos;
+  int32_t num_tokens;
+  int32_t delta;
+} pic_shift_seg;
+
+/* ---------------------------------------------------------------- context */
+
+/* Creates a context for one model and a paged cache of num_cache_blocks
+ * blocks (the allocator's range; the caller's cache tensors must hold at
+ * least that many blocks per layer).  Validates the geometry
+ * (PIC_ERR_UNSUPPORTED for shapes without a kernel).  Does not touch the GPU;
+ * the device of the first launch is used for every later launch.
+ * *out is set on success, left untouched otherwise. */
+pic_status pic_create(const pic_model_desc* model, int32_t num_cache_blocks, pic_ctx** out);
+
+/* Frees the context, its registry and every plan still alive. NULL is a no-op. */
+void pic_destroy(pic_ctx* ctx);
+
+/* Last error message of ctx (or of the calling thread when ctx is NULL);
+ * valid until the next call on the same ctx / thread.  Never NULL. */
+const char* pic_last_error(const pic_ctx* ctx);
+
+const char* pic_status_string(pic_status status);
+int32_t pic_abi_version(void);
+
+/* --------------------------------------------------------------- registry */
+
+/*
+ * Content-addressed chunk registry ([EPIC] "Algorithmic Architecture" 1.
+ * Content-Addressed Chunk Registry; [Irminsul] 2.2 Registry Lookup:
+ * hash -> (cKV, k_r, base_pos)).  key is PIC_KEY_BYTES opaque bytes (a
+ * SHA-256 digest, or a zero-padded xxHash64).  The chunk's rows are pool
+ * token rows [pool_token_offset, pool_token_offset + num_tokens) of every
+ * layer; base_pos is the position they were computed at (0 = offset 0).
+ * Registering a known key with the same num_tokens and base_pos returns its
+ * id with *is_new = 0 (the pool offset of the first registration is kept);
+ * with another num_tokens or base_pos it fails with PIC_ERR_KEY_CONFLICT.
+ */
+pic_status pic_register_chunk(pic_ctx* ctx, const uint8_t* key, int64_t pool_token_offset,
+                              int32_t num_tokens, int32_t base_pos, int32_t* chunk_id,
+                              int32_t* is_new);
+
+/* Registry lookup by key: PIC_ERR_UNKNOWN_CHUNK on a miss. */
+pic_status pic_lookup_chunk(const pic_ctx* ctx, const uint8_t* key, int32_t* chunk_id);
+
+/* Reads back a registry entry. */
+pic_status pic_chunk_info(const pic_ctx* ctx, int32_t chunk_id, int64_t* pool_token_offset,
+                          int32_t* num_tokens, int32_t* base_pos);
+
+/* Removes a chunk from the registry.  Plans already built keep working (they
+ * hold copies of the entry); the id is never reused. */
+pic_status pic_unregister_chunk(pic_ctx* ctx, int32_t chunk_id);
+
+/* ---------------------------------------------------------- plan + table */
+
+/*
+ * Composes one request and allocates its paged blocks.
+ *   Segments: dst_pos as described in pic_request_desc, delta = dst_pos -
+ *   base_pos ([Irminsul] 2.2 delta-Rotation Rule; [SemPIC] "assign final
+ *   logical positions, re-rotate the RoPE keys").
+ *   Blocks: ceil(total / block_size) blocks covering positions [0, total),
+ *   taken lowest free id first, in logical order (one deterministic choice;
+ *   the pages fix none).  block_table_out[0 .. max_blocks) receives the ids,
+ *   -1 past the last one.
+ * On success *plan_out owns the blocks until pic_free_request.  Fails with
+ * PIC_ERR_CAPACITY if max_blocks is too small, PIC_ERR_OUT_OF_BLOCKS if the
+ * allocator is exhausted (nothing is allocated then).
+ */
+pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* request,
+                                 int32_t* block_table_out, int32_t max_blocks,
+                                 pic_plan** plan_out);
+
+/* Returns the plan's blocks to the allocator and frees the plan. */
+pic_status pic_free_request(pic_ctx* ctx, pic_plan* plan);
+
+/* Sizes of a plan (any pointer may be NULL). */
+pic_status pic_plan_info(const pic_plan* plan, int32_t* total_tokens, int32_t* num_blocks,
+                         int32_t* num_segments, int32_t* num_recompute);
+
+/* Segment j of a plan: where it reads, where it lands and its shift. */
+pic_status pic_plan_segment(const pic_plan* plan, int32_t j, int32_t* chunk_id,
+                            int64_t* src_token, int32_t* num_tokens, int32_t* dst_pos,
+                            int32_t* delta);
+
+/* ---------------------------------------------------------------- stitch */
+
+/* Workspace bytes pic_stitch needs for this batch of plans (device memory,
+ * 256-byte aligned, owned by the caller). */
+size_t pic_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req);
+
+/*
+ * The hot path: for every layer l, plan r, segment, and token t of it,
+ *   K_cache[l][bt[r][p / bs]][p % bs] = R(delta) K_pool[l][src + t]   (rope dims)
+ *   V_cache[l][...same slot...]       = V_pool[l][src + t]           (bit copy)
+ * with p = dst_pos + t ([EPIC] "Mathematical Foundations" 2. The In-Place
+ * Shift Transformation: k_target = R_dp k_cached, "Values ... completely
+ * untouched"; runtime figure: chunks land in PagedAttention blocks).  For MLA
+ * (v_pool = v_cache = NULL) the latent dims are copied and only the rope
+ * dims rotated ([Irminsul] 2.1-2.2).  delta == 0 is a pure bit copy.
+ * Rotation arithmetic: fp32, one round-to-nearest-even to bf16.
+ * The same launch writes the recompute list as CSR: d_recompute_indptr
+ * [n_req + 1] and d_recompute_idx [count] (ascending positions per request;
+ * the rule is pic_recompute_indices').
+ *   d_block_tables  device int32 [n_req][max_blocks]; row r is plans[r]'s
+ *                   table (as pic_build_block_table returned it).
+ *   d_recompute_*   may both be NULL when no index output is wanted.
+ *   recompute_capacity  elements available in d_recompute_idx.
+ *   d_workspace     >= pic_workspace_bytes(...) bytes of device memory.
+ * Rows of the cache outside the plans' chunks are not touched.  Plans must
+ * not write the same cache slot twice (distinct plans own distinct blocks).
+ */
+pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                      const void* k_pool, const void* v_pool, int64_t pool_layer_stride_bytes,
+                      void* k_cache, void* v_cache, int64_t cache_layer_stride_bytes,
+                      const int32_t* d_block_tables, int32_t max_blocks,
+                      int32_t* d_recompute_idx, int32_t* d_recompute_indptr,
+                      int64_t recompute_capacity, void* d_workspace, size_t workspace_bytes,
+                      pic_stream_t stream);
+
+/* ------------------------------------------------------- in-place shift */
+
+size_t pic_rerotate_workspace_bytes(const pic_ctx* ctx, const pic_shift_seg* segs,
+                                    int32_t n_segs);
+
+/*
+ * Re-rotates keys already in the paged cache, in place ([EPIC] runtime
+ * figure, step 2 "Fast In-Place RoPE Key Rotation"; "Mathematical
+ * Foundations" 2.): for each seg, each position p in [start_pos,
+ * start_pos + num_tokens), the key row at bt[req][p / bs], p % bs becomes
+ * R(delta) of itself (rope dims only; values and MLA latents untouched).
+ *   d_block_tables  device int32 [n_tables][max_blocks].
+ *   segs            host array; a cache row must not appear twice (the
+ *                   rotations would race).  delta == 0 segments are skipped.
+ * Note: if blocks are shared between requests, every sharer sees the
+ * rotation.
+ */
+pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_layer_stride_bytes,
+                                const int32_t* d_block_tables, int32_t n_tables,
+                                int32_t max_blocks, const pic_shift_seg* segs, int32_t n_segs,
+                                void* d_workspace, size_t workspace_bytes, pic_stream_t stream);
+
+/* ------------------------------------------------------ recompute list */
+
+/*
+ * Host twin of the index list pic_stitch writes.  For each plan, ascending:
+ * a segment at position 0 contributes its first min(k_leading, len) positions,
+ * every other segment its first min(k_nonleading, len) positions ([EPIC]
+ * LegoLink "1. Identifying and Neutralizing Pseudo-Sinks": sink tokens at each
+ * chunk start, global token 0 protected; [Irminsul] 2.2 First-Chunk
+ * Carve-Out).  idx_out / indptr_out are host arrays (indptr_out has n_req + 1
+ * entries); *count receives the total even when capacity is too small
+ * (PIC_ERR_CAPACITY, nothing written to idx_out then).  idx_out may be NULL to
+ * query the count.
+ */
+pic_status pic_recompute_indices(const pic_plan* const* plans, int32_t n_req, int32_t* idx_out,
+                                 int32_t* indptr_out, int64_t capacity, int64_t* count);
+
+/* ---------------------------------------------------------- diagnostics */
+
+/*
+ * Synchronizes `stream`, then reads and clears nothing: returns the device
+ * status word the last launch that used d_workspace left (0 = clean) in
+ * *status_out, and PIC_ERR_DEVICE_CHECK when it is non-zero.
+ */
+pic_status pic_query_device_status(pic_ctx* ctx, const void* d_workspace, pic_stream_t stream,
+                                   uint32_t* status_out);
+
+/*
+ * The cos/sin the kernels use, for testing the angle arithmetic: for each of
+ * the n shifts in d_deltas (device int32), writes rope_dim/2 (cos, sin) float
+ * pairs of delta * theta_i to d_out (device float [n][rope_dim/2][2]).
+ * d_workspace: >= 4096 bytes.
+ */
+pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n, float* d_out,
+                               void* d_workspace, size_t workspace_bytes, pic_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PIC_H */

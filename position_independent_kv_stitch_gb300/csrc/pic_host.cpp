@@ -1,0 +1,887 @@
+// Host side of libpic: the C ABI declared in include/pic.h.
+//
+// Holds the content-addressed chunk registry, the prompt composer, the paged
+// block allocator and the recompute-list rule, validates every call, builds
+// the flat run list each launch consumes and enqueues it on the caller's
+// stream.  Sources: "EPIC Guide: Position-Independent Caching for LLM
+// Serving" (runtime: chunk registry, prompt composer, PagedAttention block
+// pool; LegoLink sink tokens), "Irminsul: MLA-Native Position-Independent
+// Caching for Agentic LLM Serving" (registry entry (cKV, k_r, base_pos),
+// delta = p_target - p_source, first-chunk carve-out).
+#include "pic.h"
+
+#include <algorithm>
+#include <cstdarg>
+#include <array>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+#include <new>
+#include <set>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "pic_internal.h"
+
+using pic::RunDesc;
+using pic::WsHeader;
+
+namespace {
+
+constexpr double kPi = 3.14159265358979323846;
+
+thread_local std::string g_thread_error;
+
+struct KeyHash {
+  size_t operator()(const std::array<uint8_t, PIC_KEY_BYTES>& k) const {
+    uint64_t h = 0xcbf29ce484222325ull;  // FNV-1a over the key bytes
+    for (uint8_t b : k) {
+      h ^= b;
+      h *= 0x100000001b3ull;
+    }
+    return static_cast<size_t>(h);
+  }
+};
+
+struct ChunkEntry {
+  std::array<uint8_t, PIC_KEY_BYTES> key;
+  int64_t pool_token_offset;
+  int32_t num_tokens;
+  int32_t base_pos;
+  bool live;
+};
+
+struct Segment {
+  int32_t chunk_id;
+  int64_t src_tok;
+  int32_t num_tokens;
+  int32_t dst_pos;
+  int32_t delta;
+  int32_t n_recompute;  // first n_recompute positions of the segment
+};
+
+// Paged blocks [0, n): lowest free id first (one deterministic choice).
+class BlockAllocator {
+ public:
+  explicit BlockAllocator(int32_t n) : n_(n), words_((n + 63) / 64, 0), free_count_(n) {}
+
+  int32_t free_count() const { return free_count_; }
+
+  // Takes the `count` lowest free ids; false (nothing taken) if too few are free.
+  bool allocate(int32_t count, std::vector<int32_t>& out) {
+    out.clear();
+    if (count > free_count_) return false;
+    out.reserve(count);
+    int32_t b = hint_;
+    while (static_cast<int32_t>(out.size()) < count) {
+      b = first_free_from(b);
+      out.push_back(b);
+      ++b;
+    }
+    for (int32_t id : out) words_[id >> 6] |= 1ull << (id & 63);
+    free_count_ -= count;
+    hint_ = first_free_from(hint_);
+    return true;
+  }
+
+  void release(const std::vector<int32_t>& ids) {
+    for (int32_t id : ids) {
+      words_[id >> 6] &= ~(1ull << (id & 63));
+      hint_ = std::min(hint_, id);
+    }
+    free_count_ += static_cast<int32_t>(ids.size());
+  }
+
+ private:
+  int32_t first_free_from(int32_t b) const {
+    while (b < n_) {
+      const uint64_t w = words_[b >> 6];
+      if (w == ~0ull) {
+        b = ((b >> 6) + 1) << 6;
+        continue;
+      }
+      if (!(w >> (b & 63) & 1ull)) return b;
+      ++b;
+    }
+    return n_;
+  }
+
+  int32_t n_;
+  std::vector<uint64_t> words_;
+  int32_t free_count_;
+  int32_t hint_ = 0;  // no free block below this id
+};
+
+int vectorized_bytes_ok(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct pic_plan {
+  pic_ctx* owner;
+  std::vector<Segment> segs;
+  std::vector<int32_t> blocks;
+  int32_t total_tokens;
+  int32_t n_recompute;
+};
+
+// Pinned host staging buffers for workspace images.  A pageable source would
+// make cudaMemcpyAsync wait for the stream first; pinned buffers let the next
+// call be planned and enqueued while the previous kernel runs.  Each buffer
+// records an event after its upload and is reused only once that has fired.
+struct StagingSlot {
+  uint8_t* host = nullptr;
+  size_t cap = 0;
+  cudaEvent_t uploaded = nullptr;
+};
+constexpr int kStagingSlots = 4;
+
+struct pic_ctx {
+  pic_model_desc model;
+  std::vector<double> theta;          // radians per position, rope_dim/2
+  std::vector<float2> freq_turns;     // theta_i / (2 pi) as hi + lo floats
+  int32_t num_cache_blocks;
+  std::vector<ChunkEntry> chunks;
+  std::unordered_map<std::array<uint8_t, PIC_KEY_BYTES>, int32_t, KeyHash> by_key;
+  BlockAllocator alloc;
+  std::set<pic_plan*> plans;
+  std::string err;
+  StagingSlot staging[kStagingSlots];
+  int staging_next = 0;
+  int staging_device = -1;
+  pic_ctx(int32_t nb) : num_cache_blocks(nb), alloc(nb) {}
+};
+
+namespace {
+
+pic_status fail(pic_ctx* ctx, pic_status st, const char* fmt, ...) __attribute__((format(printf, 3, 4)));
+pic_status fail(pic_ctx* ctx, pic_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (ctx) ctx->err = buf;
+  else g_thread_error = buf;
+  return st;
+}
+
+pic_status ok(pic_ctx* ctx) {
+  if (ctx) ctx->err.clear();
+  else g_thread_error.clear();
+  return PIC_OK;
+}
+
+pic_status cuda_fail(pic_ctx* ctx, cudaError_t e, const char* what) {
+  return fail(ctx, PIC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int64_t row_bytes_of(const pic_model_desc& m) {
+  return static_cast<int64_t>(m.num_kv_heads) * m.head_dim * 2;
+}
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+};
+
+pic_status current_device(pic_ctx* ctx, DeviceInfo& di) {
+  cudaError_t e = cudaGetDevice(&di.device);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, di.device);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaDeviceGetAttribute");
+  return PIC_OK;
+}
+
+bool plan_valid(const pic_ctx* ctx, const pic_plan* p) {
+  return p != nullptr && ctx->plans.count(const_cast<pic_plan*>(p)) != 0;
+}
+
+// Splits one token range of a request into runs that stay inside one block.
+void append_runs(std::vector<RunDesc>& runs, int64_t src_tok, int32_t dst_pos, int32_t n,
+                 int32_t req, int32_t delta, int32_t bs, int32_t idx_off, int32_t idx_count) {
+  int32_t t = 0;
+  bool first = true;
+  while (t < n) {
+    const int32_t pos = dst_pos + t;
+    const int32_t row = pos % bs;
+    const int32_t cnt = std::min(bs - row, n - t);
+    RunDesc r;
+    r.src_tok = static_cast<int32_t>(src_tok + t);
+    r.dst_pos = pos;
+    r.req = req;
+    r.ntok = cnt;
+    r.delta = delta;
+    r.idx_off = idx_off;
+    r.idx_count = first ? idx_count : 0;
+    r.idx_start = dst_pos;
+    runs.push_back(r);
+    first = false;
+    t += cnt;
+  }
+}
+
+// Layers per unit: enough units per resident CTA (~16) for an even finish,
+// as few as that allows so the per-unit cos/sin work is amortised.
+void choose_layer_groups(int64_t n_runs, int32_t L, int64_t resident, int32_t& lg_size,
+                         int32_t& n_lgroups) {
+  const int64_t want_units = std::max<int64_t>(1, resident * 16);
+  int64_t lg = (n_runs * L) / want_units;
+  lg = std::max<int64_t>(1, std::min<int64_t>(lg, L));
+  lg_size = static_cast<int32_t>(lg);
+  n_lgroups = (L + lg_size - 1) / lg_size;
+}
+
+struct WsLayout {
+  size_t freq_off, indptr_off, runs_off, total;
+};
+
+WsLayout ws_layout(size_t half, size_t n_indptr, size_t n_runs) {
+  WsLayout w;
+  w.freq_off = pic::align_up(sizeof(WsHeader), pic::kWsAlign);
+  w.indptr_off = pic::align_up(w.freq_off + half * sizeof(float2), pic::kWsAlign);
+  w.runs_off = pic::align_up(w.indptr_off + n_indptr * sizeof(int32_t), pic::kWsAlign);
+  w.total = pic::align_up(w.runs_off + n_runs * sizeof(RunDesc), pic::kWsAlign);
+  return w;
+}
+
+size_t count_stitch_runs(const pic_plan* const* plans, int32_t n_req, int32_t bs) {
+  size_t n = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    for (const Segment& s : plans[r]->segs) {
+      if (s.num_tokens <= 0) continue;
+      const int32_t first_row = s.dst_pos % bs;
+      n += static_cast<size_t>((first_row + s.num_tokens + bs - 1) / bs);
+    }
+  }
+  return n;
+}
+
+size_t count_shift_runs(const pic_shift_seg* segs, int32_t n, int32_t bs) {
+  size_t runs = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (segs[i].num_tokens <= 0 || segs[i].delta == 0 || segs[i].start_pos < 0) continue;
+    runs += static_cast<size_t>((segs[i].start_pos % bs + segs[i].num_tokens + bs - 1) / bs);
+  }
+  return runs;
+}
+
+void release_staging(pic_ctx* ctx) {
+  for (StagingSlot& sl : ctx->staging) {
+    if (sl.uploaded) {
+      cudaEventSynchronize(sl.uploaded);
+      cudaEventDestroy(sl.uploaded);
+    }
+    if (sl.host) cudaFreeHost(sl.host);
+    sl = StagingSlot{};
+  }
+  ctx->staging_device = -1;
+}
+
+// A zeroed pinned buffer of `bytes` for the next upload on `device`.
+pic_status acquire_staging(pic_ctx* ctx, int device, size_t bytes, StagingSlot** out) {
+  if (ctx->staging_device != device) {
+    release_staging(ctx);
+    ctx->staging_device = device;
+  }
+  StagingSlot& sl = ctx->staging[ctx->staging_next];
+  ctx->staging_next = (ctx->staging_next + 1) % kStagingSlots;
+  cudaError_t e;
+  if (sl.uploaded) {
+    e = cudaEventSynchronize(sl.uploaded);  // the last upload from this buffer is done
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "staging event");
+  } else {
+    e = cudaEventCreateWithFlags(&sl.uploaded, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaEventCreate");
+  }
+  if (sl.cap < bytes) {
+    if (sl.host) cudaFreeHost(sl.host);
+    sl.host = nullptr;
+    sl.cap = 0;
+    const size_t cap = std::max<size_t>(bytes + bytes / 2, 64 * 1024);
+    e = cudaHostAlloc(reinterpret_cast<void**>(&sl.host), cap, cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaHostAlloc (staging)");
+    sl.cap = cap;
+  }
+  std::memset(sl.host, 0, bytes);
+  *out = &sl;
+  return PIC_OK;
+}
+
+// Enqueues the upload of a staged image and marks the slot busy until it lands.
+pic_status upload_staging(pic_ctx* ctx, StagingSlot* sl, void* d_ws, size_t bytes, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(d_ws, sl->host, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace upload");
+  e = cudaEventRecord(sl->uploaded, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaEventRecord");
+  return PIC_OK;
+}
+
+void fill_freq(const pic_ctx* ctx, uint8_t* base, const WsLayout& w) {
+  std::memcpy(base + w.freq_off, ctx->freq_turns.data(), ctx->freq_turns.size() * sizeof(float2));
+}
+
+}  // namespace
+
+// ======================================================================= API
+
+extern "C" {
+
+int32_t pic_abi_version(void) { return PIC_ABI_VERSION; }
+
+const char* pic_status_string(pic_status s) {
+  switch (s) {
+    case PIC_OK: return "PIC_OK";
+    case PIC_ERR_INVALID_ARG: return "PIC_ERR_INVALID_ARG";
+    case PIC_ERR_UNKNOWN_CHUNK: return "PIC_ERR_UNKNOWN_CHUNK";
+    case PIC_ERR_KEY_CONFLICT: return "PIC_ERR_KEY_CONFLICT";
+    case PIC_ERR_OUT_OF_BLOCKS: return "PIC_ERR_OUT_OF_BLOCKS";
+    case PIC_ERR_CAPACITY: return "PIC_ERR_CAPACITY";
+    case PIC_ERR_RANGE: return "PIC_ERR_RANGE";
+    case PIC_ERR_ALIGNMENT: return "PIC_ERR_ALIGNMENT";
+    case PIC_ERR_CUDA: return "PIC_ERR_CUDA";
+    case PIC_ERR_DEVICE_CHECK: return "PIC_ERR_DEVICE_CHECK";
+    case PIC_ERR_UNSUPPORTED: return "PIC_ERR_UNSUPPORTED";
+  }
+  return "PIC_ERR_?";
+}
+
+const char* pic_last_error(const pic_ctx* ctx) {
+  return ctx ? ctx->err.c_str() : g_thread_error.c_str();
+}
+
+pic_status pic_create(const pic_model_desc* m, int32_t num_cache_blocks, pic_ctx** out) {
+  if (!m || !out) return fail(nullptr, PIC_ERR_INVALID_ARG, "pic_create: null argument");
+  if (num_cache_blocks < 0) return fail(nullptr, PIC_ERR_INVALID_ARG, "num_cache_blocks < 0");
+  if (m->num_layers < 1) return fail(nullptr, PIC_ERR_INVALID_ARG, "num_layers must be >= 1");
+  if (m->block_size < 1 || m->block_size > 256)
+    return fail(nullptr, PIC_ERR_INVALID_ARG, "block_size must be in [1, 256]");
+  if (m->pairing != PIC_PAIRING_NEOX_HALF && m->pairing != PIC_PAIRING_INTERLEAVED)
+    return fail(nullptr, PIC_ERR_INVALID_ARG, "unknown pairing %d", m->pairing);
+  if (m->kind == PIC_KIND_GQA) {
+    if (m->num_kv_heads < 1) return fail(nullptr, PIC_ERR_INVALID_ARG, "num_kv_heads must be >= 1");
+    if (m->head_dim != 64 && m->head_dim != 128 && m->head_dim != 256)
+      return fail(nullptr, PIC_ERR_UNSUPPORTED, "GQA head_dim %d has no kernel (64, 128, 256)", m->head_dim);
+    if (m->rope_dim != m->head_dim || m->rope_offset != 0)
+      return fail(nullptr, PIC_ERR_UNSUPPORTED, "GQA keys are rotated over the whole head (rope_dim == head_dim, rope_offset 0)");
+  } else if (m->kind == PIC_KIND_MLA) {
+    if (m->num_kv_heads != 1 || m->head_dim != 576 || m->rope_dim != 64 || m->rope_offset != 512)
+      return fail(nullptr, PIC_ERR_UNSUPPORTED, "MLA rows must be 512 latent + 64 rope (num_kv_heads 1, head_dim 576)");
+  } else {
+    return fail(nullptr, PIC_ERR_INVALID_ARG, "unknown kind %d", m->kind);
+  }
+  const int32_t half = m->rope_dim / 2;
+  std::vector<double> theta(half);
+  if (m->inv_freq) {
+    for (int32_t i = 0; i < half; ++i) {
+      if (!std::isfinite(m->inv_freq[i]) || m->inv_freq[i] < 0)
+        return fail(nullptr, PIC_ERR_INVALID_ARG, "inv_freq[%d] is not a finite non-negative number", i);
+      theta[i] = m->inv_freq[i];
+    }
+  } else {
+    if (!(m->rope_theta > 1.0) || !std::isfinite(m->rope_theta))
+      return fail(nullptr, PIC_ERR_INVALID_ARG, "rope_theta must be > 1");
+    // theta_i = b^(-2i/d): EPIC Guide, "Mathematical Foundations", 1.
+    for (int32_t i = 0; i < half; ++i)
+      theta[i] = std::pow(m->rope_theta, -2.0 * static_cast<double>(i) / m->rope_dim);
+    if (m->scaling == PIC_SCALING_LLAMA3) {
+      // Llama-3.1 rescaling (public rule; not on the pages).
+      const double orig = m->llama3_orig_max_pos, lo = m->llama3_low_freq_factor,
+                   hi = m->llama3_high_freq_factor, factor = m->llama3_factor;
+      if (!(orig > 0 && lo > 0 && hi > lo && factor > 0))
+        return fail(nullptr, PIC_ERR_INVALID_ARG, "bad llama3 scaling parameters");
+      const double low_wavelen = orig / lo, high_wavelen = orig / hi;
+      for (int32_t i = 0; i < half; ++i) {
+        const double wavelen = 2.0 * kPi / theta[i];
+        if (wavelen < high_wavelen) continue;
+        if (wavelen > low_wavelen) {
+          theta[i] = theta[i] / factor;
+        } else {
+          const double s = (orig / wavelen - lo) / (hi - lo);
+          theta[i] = (1.0 - s) * theta[i] / factor + s * theta[i];
+        }
+      }
+    } else if (m->scaling != PIC_SCALING_NONE) {
+      return fail(nullptr, PIC_ERR_INVALID_ARG, "unknown scaling %d", m->scaling);
+    }
+  }
+  pic_ctx* ctx = new (std::nothrow) pic_ctx(num_cache_blocks);
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "out of host memory");
+  ctx->model = *m;
+  ctx->model.inv_freq = nullptr;
+  ctx->theta = theta;
+  ctx->freq_turns.resize(half);
+  for (int32_t i = 0; i < half; ++i) {
+    const double f = theta[i] / (2.0 * kPi);
+    const float fh = static_cast<float>(f);
+    ctx->freq_turns[i] = make_float2(fh, static_cast<float>(f - static_cast<double>(fh)));
+  }
+  *out = ctx;
+  return ok(nullptr);
+}
+
+void pic_destroy(pic_ctx* ctx) {
+  if (!ctx) return;
+  release_staging(ctx);
+  for (pic_plan* p : ctx->plans) delete p;
+  delete ctx;
+}
+
+// ------------------------------------------------------------------ registry
+
+pic_status pic_register_chunk(pic_ctx* ctx, const uint8_t* key, int64_t pool_token_offset,
+                              int32_t num_tokens, int32_t base_pos, int32_t* chunk_id,
+                              int32_t* is_new) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (!key || !chunk_id) return fail(ctx, PIC_ERR_INVALID_ARG, "null key or chunk_id");
+  if (num_tokens < 0 || pool_token_offset < 0 || base_pos < 0)
+    return fail(ctx, PIC_ERR_RANGE, "negative offset, length or base_pos");
+  if (pool_token_offset + num_tokens > std::numeric_limits<int32_t>::max())
+    return fail(ctx, PIC_ERR_RANGE, "pool rows beyond 2^31 tokens");
+  std::array<uint8_t, PIC_KEY_BYTES> k;
+  std::memcpy(k.data(), key, PIC_KEY_BYTES);
+  auto it = ctx->by_key.find(k);
+  if (it != ctx->by_key.end()) {
+    const ChunkEntry& e = ctx->chunks[it->second];
+    if (e.num_tokens != num_tokens || e.base_pos != base_pos)
+      return fail(ctx, PIC_ERR_KEY_CONFLICT,
+                  "key already registered as chunk %d with %d tokens at base %d", it->second,
+                  e.num_tokens, e.base_pos);
+    *chunk_id = it->second;
+    if (is_new) *is_new = 0;
+    return ok(ctx);
+  }
+  const int32_t id = static_cast<int32_t>(ctx->chunks.size());
+  ctx->chunks.push_back(ChunkEntry{k, pool_token_offset, num_tokens, base_pos, true});
+  ctx->by_key.emplace(k, id);
+  *chunk_id = id;
+  if (is_new) *is_new = 1;
+  return ok(ctx);
+}
+
+pic_status pic_lookup_chunk(const pic_ctx* cctx, const uint8_t* key, int32_t* chunk_id) {
+  pic_ctx* ctx = const_cast<pic_ctx*>(cctx);
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (!key || !chunk_id) return fail(ctx, PIC_ERR_INVALID_ARG, "null key or chunk_id");
+  std::array<uint8_t, PIC_KEY_BYTES> k;
+  std::memcpy(k.data(), key, PIC_KEY_BYTES);
+  auto it = ctx->by_key.find(k);
+  if (it == ctx->by_key.end()) return fail(ctx, PIC_ERR_UNKNOWN_CHUNK, "key not registered");
+  *chunk_id = it->second;
+  return ok(ctx);
+}
+
+pic_status pic_chunk_info(const pic_ctx* cctx, int32_t id, int64_t* pool_token_offset,
+                          int32_t* num_tokens, int32_t* base_pos) {
+  pic_ctx* ctx = const_cast<pic_ctx*>(cctx);
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (id < 0 || id >= static_cast<int32_t>(ctx->chunks.size()) || !ctx->chunks[id].live)
+    return fail(ctx, PIC_ERR_UNKNOWN_CHUNK, "no chunk %d", id);
+  const ChunkEntry& e = ctx->chunks[id];
+  if (pool_token_offset) *pool_token_offset = e.pool_token_offset;
+  if (num_tokens) *num_tokens = e.num_tokens;
+  if (base_pos) *base_pos = e.base_pos;
+  return ok(ctx);
+}
+
+pic_status pic_unregister_chunk(pic_ctx* ctx, int32_t id) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (id < 0 || id >= static_cast<int32_t>(ctx->chunks.size()) || !ctx->chunks[id].live)
+    return fail(ctx, PIC_ERR_UNKNOWN_CHUNK, "no chunk %d", id);
+  ctx->chunks[id].live = false;
+  ctx->by_key.erase(ctx->chunks[id].key);
+  return ok(ctx);
+}
+
+// ------------------------------------------------------------- plan + table
+
+pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32_t* bt_out,
+                                 int32_t max_blocks, pic_plan** plan_out) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (!rq || !plan_out) return fail(ctx, PIC_ERR_INVALID_ARG, "null request or plan_out");
+  if (rq->n_chunks < 0 || (rq->n_chunks > 0 && !rq->chunk_ids))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "bad chunk list");
+  if (rq->k_nonleading < 0 || rq->k_leading < 0 || rq->start_pos < 0 || rq->total_tokens < 0)
+    return fail(ctx, PIC_ERR_RANGE, "negative k, start_pos or total_tokens");
+  if (max_blocks < 0 || (max_blocks > 0 && !bt_out))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "bad block table output");
+
+  // Compose: EPIC Guide, "Algorithmic Architecture" 2. Modular Prompt Composer.
+  std::vector<Segment> segs;
+  segs.reserve(rq->n_chunks);
+  int64_t pos = rq->start_pos;
+  int64_t prev_end = -1;
+  int64_t n_recompute = 0;
+  for (int32_t j = 0; j < rq->n_chunks; ++j) {
+    const int32_t id = rq->chunk_ids[j];
+    if (id < 0 || id >= static_cast<int32_t>(ctx->chunks.size()) || !ctx->chunks[id].live)
+      return fail(ctx, PIC_ERR_UNKNOWN_CHUNK, "chunk %d (position %d in the request) is not registered", id, j);
+    const ChunkEntry& e = ctx->chunks[id];
+    const int32_t n = rq->take_tokens ? rq->take_tokens[j] : e.num_tokens;
+    if (n < 0 || n > e.num_tokens)
+      return fail(ctx, PIC_ERR_RANGE, "take_tokens[%d] = %d outside [0, %d]", j, n, e.num_tokens);
+    const int64_t p = rq->dst_pos ? rq->dst_pos[j] : pos;
+    if (p < 0 || (prev_end >= 0 && p < prev_end))
+      return fail(ctx, PIC_ERR_RANGE, "chunk %d at position %lld overlaps the previous chunk (ends %lld)", j,
+                  static_cast<long long>(p), static_cast<long long>(prev_end));
+    if (p + n > std::numeric_limits<int32_t>::max())
+      return fail(ctx, PIC_ERR_RANGE, "positions beyond int32");
+    // delta = p_target - p_source (Irminsul, 2.2 delta-Rotation Rule)
+    const int64_t delta = p - e.base_pos;
+    if (delta > PIC_MAX_ABS_DELTA || delta < -PIC_MAX_ABS_DELTA)
+      return fail(ctx, PIC_ERR_RANGE, "|delta| of chunk %d exceeds 2^24 - 1", j);
+    // recompute count: LegoLink sinks of non-leading chunks; Irminsul carve-out at position 0
+    const int32_t k = (p == 0) ? rq->k_leading : rq->k_nonleading;
+    const int32_t nr = std::min(k, n);
+    segs.push_back(Segment{id, e.pool_token_offset, n, static_cast<int32_t>(p), static_cast<int32_t>(delta), nr});
+    n_recompute += nr;
+    pos = p + n;
+    prev_end = pos;
+  }
+  const int64_t end = segs.empty() ? rq->start_pos : pos;
+  if (rq->total_tokens > 0 && rq->total_tokens < end)
+    return fail(ctx, PIC_ERR_RANGE, "total_tokens %d is before the end of the last chunk (%lld)",
+                rq->total_tokens, static_cast<long long>(end));
+  const int64_t total = rq->total_tokens > 0 ? rq->total_tokens : end;
+  const int64_t bs = ctx->model.block_size;
+  const int64_t nblocks = (total + bs - 1) / bs;
+  if (nblocks > max_blocks)
+    return fail(ctx, PIC_ERR_CAPACITY, "request needs %lld blocks, table holds %d",
+                static_cast<long long>(nblocks), max_blocks);
+  if (n_recompute > std::numeric_limits<int32_t>::max())
+    return fail(ctx, PIC_ERR_RANGE, "recompute list too long");
+
+  pic_plan* plan = new (std::nothrow) pic_plan();
+  if (!plan) return fail(ctx, PIC_ERR_INVALID_ARG, "out of host memory");
+  if (!ctx->alloc.allocate(static_cast<int32_t>(nblocks), plan->blocks)) {
+    delete plan;
+    return fail(ctx, PIC_ERR_OUT_OF_BLOCKS, "request needs %lld blocks, %d free",
+                static_cast<long long>(nblocks), ctx->alloc.free_count());
+  }
+  plan->owner = ctx;
+  plan->segs = std::move(segs);
+  plan->total_tokens = static_cast<int32_t>(total);
+  plan->n_recompute = static_cast<int32_t>(n_recompute);
+  for (int32_t i = 0; i < max_blocks; ++i)
+    bt_out[i] = i < static_cast<int32_t>(plan->blocks.size()) ? plan->blocks[i] : -1;
+  ctx->plans.insert(plan);
+  *plan_out = plan;
+  return ok(ctx);
+}
+
+pic_status pic_free_request(pic_ctx* ctx, pic_plan* plan) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (!plan_valid(ctx, plan)) return fail(ctx, PIC_ERR_INVALID_ARG, "plan does not belong to this context");
+  ctx->alloc.release(plan->blocks);
+  ctx->plans.erase(plan);
+  delete plan;
+  return ok(ctx);
+}
+
+pic_status pic_plan_info(const pic_plan* p, int32_t* total_tokens, int32_t* num_blocks,
+                         int32_t* num_segments, int32_t* num_recompute) {
+  if (!p) return fail(nullptr, PIC_ERR_INVALID_ARG, "null plan");
+  if (total_tokens) *total_tokens = p->total_tokens;
+  if (num_blocks) *num_blocks = static_cast<int32_t>(p->blocks.size());
+  if (num_segments) *num_segments = static_cast<int32_t>(p->segs.size());
+  if (num_recompute) *num_recompute = p->n_recompute;
+  return ok(nullptr);
+}
+
+pic_status pic_plan_segment(const pic_plan* p, int32_t j, int32_t* chunk_id, int64_t* src_token,
+                            int32_t* num_tokens, int32_t* dst_pos, int32_t* delta) {
+  if (!p) return fail(nullptr, PIC_ERR_INVALID_ARG, "null plan");
+  if (j < 0 || j >= static_cast<int32_t>(p->segs.size()))
+    return fail(nullptr, PIC_ERR_RANGE, "segment %d out of range", j);
+  const Segment& s = p->segs[j];
+  if (chunk_id) *chunk_id = s.chunk_id;
+  if (src_token) *src_token = s.src_tok;
+  if (num_tokens) *num_tokens = s.num_tokens;
+  if (dst_pos) *dst_pos = s.dst_pos;
+  if (delta) *delta = s.delta;
+  return ok(nullptr);
+}
+
+// -------------------------------------------------------------- recompute
+
+pic_status pic_recompute_indices(const pic_plan* const* plans, int32_t n_req, int32_t* idx_out,
+                                 int32_t* indptr_out, int64_t capacity, int64_t* count) {
+  if (n_req < 0 || (n_req > 0 && !plans)) return fail(nullptr, PIC_ERR_INVALID_ARG, "bad plan list");
+  int64_t total = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    if (!plans[r]) return fail(nullptr, PIC_ERR_INVALID_ARG, "plans[%d] is null", r);
+    total += plans[r]->n_recompute;
+  }
+  if (count) *count = total;
+  if (!idx_out) return ok(nullptr);
+  if (total > capacity) return fail(nullptr, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
+                                    static_cast<long long>(total), static_cast<long long>(capacity));
+  int64_t w = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    if (indptr_out) indptr_out[r] = static_cast<int32_t>(w);
+    for (const Segment& s : plans[r]->segs)
+      for (int32_t t = 0; t < s.n_recompute; ++t) idx_out[w++] = s.dst_pos + t;
+  }
+  if (indptr_out) indptr_out[n_req] = static_cast<int32_t>(w);
+  return ok(nullptr);
+}
+
+// ------------------------------------------------------------------- stitch
+
+size_t pic_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req) {
+  if (!ctx || n_req < 0 || (n_req > 0 && !plans)) return 0;
+  for (int32_t r = 0; r < n_req; ++r)
+    if (!plans[r]) return 0;
+  const size_t runs = count_stitch_runs(plans, n_req, ctx->model.block_size);
+  return ws_layout(ctx->freq_turns.size(), static_cast<size_t>(n_req) + 1, runs).total;
+}
+
+pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                      const void* k_pool, const void* v_pool, int64_t pool_ls, void* k_cache,
+                      void* v_cache, int64_t cache_ls, const int32_t* d_bt, int32_t max_blocks,
+                      int32_t* d_ridx, int32_t* d_indptr, int64_t recompute_capacity,
+                      void* d_ws, size_t ws_bytes, pic_stream_t stream) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  const pic_model_desc& m = ctx->model;
+  if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
+  for (int32_t r = 0; r < n_req; ++r) {
+    if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
+    if (static_cast<int32_t>(plans[r]->blocks.size()) > max_blocks)
+      return fail(ctx, PIC_ERR_CAPACITY, "plans[%d] has %zu blocks, block-table rows hold %d", r,
+                  plans[r]->blocks.size(), max_blocks);
+  }
+  const bool gqa = m.kind == PIC_KIND_GQA;
+  if (!k_pool || !k_cache || !d_bt || !d_ws)
+    return fail(ctx, PIC_ERR_INVALID_ARG, "null pool, cache, block table or workspace");
+  if (gqa && (!v_pool || !v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs v_pool and v_cache");
+  if (!gqa && (v_pool || v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
+  if ((d_ridx == nullptr) != (d_indptr == nullptr))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "pass both recompute outputs or neither");
+  if (!vectorized_bytes_ok(k_pool) || !vectorized_bytes_ok(k_cache) || (gqa && (!vectorized_bytes_ok(v_pool) || !vectorized_bytes_ok(v_cache))) ||
+      (pool_ls & 15) || (cache_ls & 15) || !vectorized_bytes_ok(d_ws))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "pools, caches, layer strides and workspace must be 16-byte aligned");
+  const int64_t row_bytes = row_bytes_of(m);
+  if (pool_ls < 0 || cache_ls < 0 || (m.num_layers > 1 && (pool_ls == 0 || cache_ls == 0)))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "bad layer strides");
+  if (m.num_layers > 1 && cache_ls < static_cast<int64_t>(ctx->num_cache_blocks) * m.block_size * row_bytes)
+    return fail(ctx, PIC_ERR_RANGE, "cache layer stride smaller than num_cache_blocks * block_size rows");
+
+  int64_t n_rec = 0;
+  for (int32_t r = 0; r < n_req; ++r) n_rec += plans[r]->n_recompute;
+  if (d_ridx && n_rec > recompute_capacity)
+    return fail(ctx, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
+                static_cast<long long>(n_rec), static_cast<long long>(recompute_capacity));
+
+  const int32_t bs = m.block_size;
+  const size_t n_runs = count_stitch_runs(plans, n_req, bs);
+  const size_t half = ctx->freq_turns.size();
+  const WsLayout w = ws_layout(half, static_cast<size_t>(n_req) + 1, n_runs);
+  if (ws_bytes < w.total)
+    return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  if (n_runs > static_cast<size_t>(std::numeric_limits<int32_t>::max()))
+    return fail(ctx, PIC_ERR_RANGE, "too many runs");
+
+  DeviceInfo di;
+  pic_status st = current_device(ctx, di);
+  if (st != PIC_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  StagingSlot* sl = nullptr;
+  st = acquire_staging(ctx, di.device, w.total, &sl);
+  if (st != PIC_OK) return st;
+
+  // Workspace image: zeroed header, frequencies, CSR offsets, runs.
+  uint8_t* base = sl->host;
+  fill_freq(ctx, base, w);
+  int32_t* indptr = reinterpret_cast<int32_t*>(base + w.indptr_off);
+  std::vector<RunDesc> runs;
+  runs.reserve(n_runs);
+  int64_t idx = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    indptr[r] = static_cast<int32_t>(idx);
+    for (const Segment& sg : plans[r]->segs) {
+      if (sg.num_tokens > 0)
+        append_runs(runs, sg.src_tok, sg.dst_pos, sg.num_tokens, r, sg.delta, bs,
+                    static_cast<int32_t>(idx), sg.n_recompute);
+      idx += sg.n_recompute;
+    }
+  }
+  indptr[n_req] = static_cast<int32_t>(idx);
+  std::memcpy(base + w.runs_off, runs.data(), runs.size() * sizeof(RunDesc));
+  st = upload_staging(ctx, sl, d_ws, w.total, s);
+  if (st != PIC_OK) return st;
+  cudaError_t e;
+
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  pic::KernelParams p{};
+  p.runs = reinterpret_cast<const RunDesc*>(ws + w.runs_off);
+  p.n_runs = static_cast<int32_t>(n_runs);
+  p.num_layers = m.num_layers;
+  p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
+  p.k_src = static_cast<const uint8_t*>(k_pool);
+  p.v_src = static_cast<const uint8_t*>(v_pool);
+  p.src_layer_stride = pool_ls;
+  p.k_dst = static_cast<uint8_t*>(k_cache);
+  p.v_dst = static_cast<uint8_t*>(v_cache);
+  p.dst_layer_stride = cache_ls;
+  p.block_tables = d_bt;
+  p.max_blocks = max_blocks;
+  p.num_cache_blocks = ctx->num_cache_blocks;
+  p.block_size = bs;
+  p.row_bytes = static_cast<int32_t>(row_bytes);
+  p.ridx = d_ridx;
+  p.indptr_src = reinterpret_cast<const int32_t*>(ws + w.indptr_off);
+  p.indptr_dst = d_indptr;
+  p.n_indptr = n_req + 1;
+  p.header = reinterpret_cast<WsHeader*>(ws);
+
+  const int occ = gqa ? pic::occupancy_stitch_gqa(m.pairing, m.head_dim) : pic::occupancy_stitch_mla(m.pairing);
+  const int64_t resident = static_cast<int64_t>(di.sm_count) * occ;
+  choose_layer_groups(static_cast<int64_t>(n_runs), m.num_layers, resident, p.lg_size, p.n_lgroups);
+  const int64_t units = static_cast<int64_t>(n_runs) * p.n_lgroups;
+  // at least one CTA so the CSR offsets are always written
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
+
+  if (gqa) {
+    p.heads_per_token = m.num_kv_heads;
+    p.head_stride = m.head_dim * 2;
+    p.rope_off_bytes = 0;
+    e = pic::launch_stitch_gqa(p, m.pairing, m.head_dim, grid, s);
+  } else {
+    p.heads_per_token = 1;
+    p.head_stride = static_cast<int32_t>(row_bytes);
+    p.rope_off_bytes = m.rope_offset * 2;
+    e = pic::launch_stitch_mla(p, m.pairing, grid, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
+  return ok(ctx);
+}
+
+// ------------------------------------------------------------ in-place shift
+
+size_t pic_rerotate_workspace_bytes(const pic_ctx* ctx, const pic_shift_seg* segs, int32_t n) {
+  if (!ctx || n < 0 || (n > 0 && !segs)) return 0;
+  return ws_layout(ctx->freq_turns.size(), 0, count_shift_runs(segs, n, ctx->model.block_size)).total;
+}
+
+pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
+                                const int32_t* d_bt, int32_t n_tables, int32_t max_blocks,
+                                const pic_shift_seg* segs, int32_t n_segs, void* d_ws,
+                                size_t ws_bytes, pic_stream_t stream) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  const pic_model_desc& m = ctx->model;
+  if (n_segs < 0 || (n_segs > 0 && !segs)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad segment list");
+  if (!k_cache || !d_bt || !d_ws) return fail(ctx, PIC_ERR_INVALID_ARG, "null cache, block table or workspace");
+  if (n_tables < 0 || max_blocks < 0) return fail(ctx, PIC_ERR_INVALID_ARG, "bad block table shape");
+  if (!vectorized_bytes_ok(k_cache) || (cache_ls & 15) || !vectorized_bytes_ok(d_ws))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "cache, layer stride and workspace must be 16-byte aligned");
+  const int64_t row_bytes = row_bytes_of(m);
+  if (cache_ls < 0 || (m.num_layers > 1 && cache_ls < static_cast<int64_t>(ctx->num_cache_blocks) * m.block_size * row_bytes))
+    return fail(ctx, PIC_ERR_RANGE, "cache layer stride smaller than num_cache_blocks * block_size rows");
+  const int32_t bs = m.block_size;
+  for (int32_t i = 0; i < n_segs; ++i) {
+    const pic_shift_seg& g = segs[i];
+    if (g.req < 0 || g.req >= n_tables) return fail(ctx, PIC_ERR_RANGE, "segs[%d].req %d outside [0, %d)", i, g.req, n_tables);
+    if (g.start_pos < 0 || g.num_tokens < 0) return fail(ctx, PIC_ERR_RANGE, "segs[%d] has a negative range", i);
+    if (static_cast<int64_t>(g.start_pos) + g.num_tokens > static_cast<int64_t>(max_blocks) * bs)
+      return fail(ctx, PIC_ERR_RANGE, "segs[%d] ends past the block table", i);
+    if (g.delta > PIC_MAX_ABS_DELTA || g.delta < -PIC_MAX_ABS_DELTA)
+      return fail(ctx, PIC_ERR_RANGE, "segs[%d].delta exceeds 2^24 - 1", i);
+  }
+  const size_t n_runs = count_shift_runs(segs, n_segs, bs);
+  const WsLayout w = ws_layout(ctx->freq_turns.size(), 0, n_runs);
+  if (ws_bytes < w.total) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  if (n_runs > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return fail(ctx, PIC_ERR_RANGE, "too many runs");
+
+  DeviceInfo di;
+  pic_status st = current_device(ctx, di);
+  if (st != PIC_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  StagingSlot* sl = nullptr;
+  st = acquire_staging(ctx, di.device, w.total, &sl);
+  if (st != PIC_OK) return st;
+  uint8_t* base = sl->host;
+  fill_freq(ctx, base, w);
+  std::vector<RunDesc> runs;
+  runs.reserve(n_runs);
+  for (int32_t i = 0; i < n_segs; ++i) {
+    const pic_shift_seg& g = segs[i];
+    if (g.num_tokens <= 0 || g.delta == 0) continue;  // R_0 = I: nothing to do
+    append_runs(runs, 0, g.start_pos, g.num_tokens, g.req, g.delta, bs, 0, 0);
+  }
+  std::memcpy(base + w.runs_off, runs.data(), runs.size() * sizeof(RunDesc));
+  st = upload_staging(ctx, sl, d_ws, w.total, s);
+  if (st != PIC_OK) return st;
+  cudaError_t e;
+  if (n_runs == 0) return ok(ctx);
+
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  pic::KernelParams p{};
+  p.runs = reinterpret_cast<const RunDesc*>(ws + w.runs_off);
+  p.n_runs = static_cast<int32_t>(n_runs);
+  p.num_layers = m.num_layers;
+  p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
+  p.k_dst = static_cast<uint8_t*>(k_cache);
+  p.dst_layer_stride = cache_ls;
+  p.block_tables = d_bt;
+  p.max_blocks = max_blocks;
+  p.num_cache_blocks = ctx->num_cache_blocks;
+  p.block_size = bs;
+  p.row_bytes = static_cast<int32_t>(row_bytes);
+  p.header = reinterpret_cast<WsHeader*>(ws);
+  if (m.kind == PIC_KIND_GQA) {
+    p.heads_per_token = m.num_kv_heads;
+    p.head_stride = m.head_dim * 2;
+    p.rope_off_bytes = 0;
+  } else {
+    p.heads_per_token = 1;
+    p.head_stride = static_cast<int32_t>(row_bytes);
+    p.rope_off_bytes = m.rope_offset * 2;
+  }
+  const int occ = pic::occupancy_rerotate(m.pairing, m.rope_dim);
+  const int64_t resident = static_cast<int64_t>(di.sm_count) * occ;
+  choose_layer_groups(static_cast<int64_t>(n_runs), m.num_layers, resident, p.lg_size, p.n_lgroups);
+  const int64_t units = static_cast<int64_t>(n_runs) * p.n_lgroups;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
+  e = pic::launch_rerotate(p, m.pairing, m.rope_dim, grid, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "rerotate launch");
+  return ok(ctx);
+}
+
+// ------------------------------------------------------------- diagnostics
+
+pic_status pic_query_device_status(pic_ctx* ctx, const void* d_ws, pic_stream_t stream,
+                                   uint32_t* status_out) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (!d_ws) return fail(ctx, PIC_ERR_INVALID_ARG, "null workspace");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  WsHeader h;
+  e = cudaMemcpy(&h, d_ws, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
+  if (status_out) *status_out = h.status;
+  if (h.status != 0)
+    return fail(ctx, PIC_ERR_DEVICE_CHECK,
+                "kernel found a block-table entry outside the cache (status 0x%x, table row %u, position %u)",
+                h.status, h.bad_req, h.bad_pos);
+  return ok(ctx);
+}
+
+pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n, float* d_out,
+                               void* d_ws, size_t ws_bytes, pic_stream_t stream) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (n < 0 || (n > 0 && (!d_deltas || !d_out)) || !d_ws)
+    return fail(ctx, PIC_ERR_INVALID_ARG, "bad arguments");
+  const size_t need = ctx->freq_turns.size() * sizeof(float2);
+  if (ws_bytes < need || ws_bytes < 4096) return fail(ctx, PIC_ERR_CAPACITY, "workspace needs 4096 bytes");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(d_ws, ctx->freq_turns.data(), need, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "frequency upload");
+  e = pic::launch_cossin(d_deltas, n, static_cast<const float2*>(d_ws),
+                         static_cast<int32_t>(ctx->freq_turns.size()), d_out, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cos/sin launch");
+  return ok(ctx);
+}
+
+}  // extern "C"

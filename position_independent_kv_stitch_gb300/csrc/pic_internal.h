@@ -1,0 +1,84 @@
+// Internal interface between the host library (pic_host.cpp) and the CUDA
+// kernels (pic_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace pic {
+
+// One run: up to block_size consecutive tokens of one segment that land in
+// one paged block.  Runs are layer-independent; a kernel work unit is a run
+// times a group of consecutive layers.  32 bytes, read once per unit.
+struct alignas(32) RunDesc {
+  int32_t src_tok;    // pool token row of the run's first token (stitch only)
+  int32_t dst_pos;    // absolute position of the run's first token
+  int32_t req;        // block-table row
+  int32_t ntok;       // tokens in the run, 1 .. block_size, all in one block
+  int32_t delta;      // position shift of the segment
+  int32_t idx_off;    // first recompute-list slot this run writes
+  int32_t idx_count;  // recompute positions it writes (segment's first run only)
+  int32_t idx_start;  // first recompute position
+};
+static_assert(sizeof(RunDesc) == 32, "RunDesc layout");
+
+// Workspace layout: [header 256 B][freq table][indptr][runs], each 256-B aligned.
+struct WsHeader {
+  uint32_t status;      // PIC_DEV_* bits raised by kernels
+  uint32_t bad_req;     // a block-table row that held a bad entry (diagnostic)
+  uint32_t bad_pos;     // the position it was asked for
+  uint32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
+
+constexpr size_t kWsAlign = 256;
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+enum Pairing : int { kNeox = 0, kInterleaved = 1 };
+
+struct KernelParams {
+  const RunDesc* runs;
+  int32_t n_runs;
+  int32_t n_lgroups;        // ceil(num_layers / lg_size)
+  int32_t lg_size;          // layers per work unit
+  int32_t num_layers;
+  const float2* freq;       // rope_dim/2 (hi, lo): theta_i / (2 pi) as a float pair
+  const uint8_t* k_src;     // pool (stitch) -- unused in place
+  const uint8_t* v_src;     // value pool (GQA stitch) or null
+  int64_t src_layer_stride;
+  uint8_t* k_dst;           // paged key / MLA cache
+  uint8_t* v_dst;           // paged value cache (GQA stitch) or null
+  int64_t dst_layer_stride;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  int32_t num_cache_blocks;
+  int32_t block_size;
+  int32_t heads_per_token;  // head rows per token (GQA heads; 1 for an MLA row)
+  int32_t head_stride;      // bytes between head rows
+  int32_t row_bytes;        // bytes per token row
+  int32_t rope_off_bytes;   // byte offset of the rope slice inside a head row
+  int32_t* ridx;            // recompute list output (may be null)
+  const int32_t* indptr_src;
+  int32_t* indptr_dst;      // recompute CSR offsets output (may be null)
+  int32_t n_indptr;
+  WsHeader* header;
+};
+
+// Launchers; each returns the launch's cudaError_t.  `grid` is the number of
+// CTAs (persistent, grid-stride over units).
+cudaError_t launch_stitch_gqa(const KernelParams& p, int pairing, int head_dim, int grid,
+                              cudaStream_t stream);
+cudaError_t launch_stitch_mla(const KernelParams& p, int pairing, int grid, cudaStream_t stream);
+cudaError_t launch_rerotate(const KernelParams& p, int pairing, int rope_dim, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_cossin(const int32_t* deltas, int32_t n, const float2* freq, int32_t half,
+                          float* out, cudaStream_t stream);
+
+// Resident CTAs per SM of the kernel the matching launcher would use.
+int occupancy_stitch_gqa(int pairing, int head_dim);
+int occupancy_stitch_mla(int pairing);
+int occupancy_rerotate(int pairing, int rope_dim);
+
+}  // namespace pic

@@ -1,0 +1,392 @@
+// CUDA kernels for position-independent KV stitching on GB300 (sm_103a).
+//
+// The work is a gather / delta-rotate / paged scatter over bf16 rows: it moves
+// bytes and does 6 flops per rotated pair, so HBM bandwidth bounds it and
+// tensor cores have nothing to do.  Design:
+//   * Work unit = one run (<= block_size consecutive tokens of one chunk that
+//     land in one paged block; contiguous in both pool and cache) x one group
+//     of consecutive layers.  A persistent grid strides over the units.
+//   * Every thread owns a fixed slice of each head row (16-byte vectors), so
+//     its RoPE frequencies are fixed: the cos/sin of delta * theta_i are
+//     computed once per unit in registers and reused for every token, head
+//     and layer of the unit (one delta per chunk: EPIC Guide, "Mathematical
+//     Foundations: RoPE In-Place Key Transformation", 2. The In-Place Shift
+//     Transformation -- R_{n+dp} = R_dp R_n).
+//   * Neox half-split pairs (i, i + d/2) live in two vectors d bytes apart; a
+//     thread loads both, so no shuffles are needed.  Interleaved pairs
+//     (2i, 2i+1) sit inside one vector.
+//   * Loads of the pool and stores into the cache are streaming (evict-first):
+//     neither is re-read by this launch.
+//   * Angles: the host gives f_i = theta_i / (2 pi) as a float pair hi + lo.
+//     delta * hi is split exactly into p + e with one FMA (Dekker's
+//     TwoProduct), p's integer part is dropped exactly, the small terms are
+//     added back, and sincospif turns the fraction of a turn into cos/sin.
+//     This keeps |delta| up to 2^24 accurate to ~1e-7 rad, where a plain
+//     float delta * theta would be off by up to ~1e-2 rad at delta ~ 1e5.
+//   * Device errors (a block-table entry outside the cache) skip the write and
+//     raise a bit in the workspace header; no trap, no wait, no spin.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pic_internal.h"
+
+namespace pic {
+namespace {
+
+constexpr unsigned kDevBadBlock = 0x1u;  // matches PIC_DEV_BAD_BLOCK
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ void shift_cossin(int delta, float2 f, float& c, float& s) {
+  const float d = static_cast<float>(delta);   // exact for |delta| < 2^24
+  const float p = __fmul_rn(d, f.x);
+  const float e = __fmaf_rn(d, f.x, -p);       // d * hi == p + e exactly
+  const float r = __fsub_rn(p, rintf(p));      // exact, |r| <= 1/2 turn
+  const float t = __fadd_rn(r, __fmaf_rn(d, f.y, e));
+  sincospif(2.0f * t, &s, &c);                 // cos / sin of 2 pi t
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_stream(uint8_t* p, uint4 v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+__device__ __forceinline__ uint4 ld_plain(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ void st_plain(uint8_t* p, uint4 v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+__device__ __forceinline__ uint32_t& word(uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+}
+
+// Neox pair-vector: a holds x_a of frequencies f0..f0+7, b holds x_b of the same.
+__device__ __forceinline__ void rotate_neox(uint4& a, uint4& b, const float* c, const float* s) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t aw = word(a, w), bw = word(b, w);
+    const float a0 = bf_lo(aw), a1 = bf_hi(aw), b0 = bf_lo(bw), b1 = bf_hi(bw);
+    const float c0 = c[2 * w], s0 = s[2 * w], c1 = c[2 * w + 1], s1 = s[2 * w + 1];
+    word(a, w) = bf_pack(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
+    word(b, w) = bf_pack(a0 * s0 + b0 * c0, a1 * s1 + b1 * c1);
+  }
+}
+
+// Interleaved vector: word w holds the pair (x, y) of frequency f0 + w.
+__device__ __forceinline__ void rotate_interleaved(uint4& v, const float* c, const float* s) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t vw = word(v, w);
+    const float x = bf_lo(vw), y = bf_hi(vw);
+    word(v, w) = bf_pack(x * c[w] - y * s[w], x * s[w] + y * c[w]);
+  }
+}
+
+// Resolves a run's destination block; false (and a raised status bit) when
+// the block table entry does not name a cache block.
+__device__ __forceinline__ bool resolve_block(const KernelParams& P, const RunDesc& r, int& blk,
+                                              int& row0) {
+  const int lb = r.dst_pos / P.block_size;
+  row0 = r.dst_pos - lb * P.block_size;
+  blk = __ldg(P.block_tables + static_cast<int64_t>(r.req) * P.max_blocks + lb);
+  if (blk < 0 || blk >= P.num_cache_blocks) {
+    if (threadIdx.x == 0) {
+      atomicOr(&P.header->status, kDevBadBlock);
+      P.header->bad_req = static_cast<uint32_t>(r.req);
+      P.header->bad_pos = static_cast<uint32_t>(r.dst_pos);
+    }
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void emit_recompute(const KernelParams& P, const RunDesc& r, int lg) {
+  if (P.ridx != nullptr && lg == 0 && r.idx_count > 0) {
+    for (int t = threadIdx.x; t < r.idx_count; t += blockDim.x) P.ridx[r.idx_off + t] = r.idx_start + t;
+  }
+}
+
+__device__ __forceinline__ void emit_indptr(const KernelParams& P) {
+  if (P.indptr_dst != nullptr && blockIdx.x == 0) {
+    for (int t = threadIdx.x; t < P.n_indptr; t += blockDim.x) P.indptr_dst[t] = P.indptr_src[t];
+  }
+}
+
+// ------------------------------------------------ GQA stitch / in-place shift
+//
+// RD = rope dims of a head row (the whole head for GQA).  STITCH: read the
+// pool, write K rotated and V copied into the paged cache.  !STITCH: rotate
+// the cache's key rows in place (values untouched).
+constexpr int kThreads = 256;
+
+template <int PAIRING, int RD, bool STITCH>
+__global__ void __launch_bounds__(kThreads) k_rotate_rows(const KernelParams P) {
+  constexpr bool NEOX = (PAIRING == kNeox);
+  constexpr int VPR = RD / 8;                    // 16-B vectors in the rope slice
+  constexpr int TPR = NEOX ? VPR / 2 : VPR;      // threads per head row
+  constexpr int NF = NEOX ? 8 : 4;               // frequencies per thread
+  constexpr int HSTEP = kThreads / TPR;          // head rows per block sweep
+  constexpr int U = NEOX ? 4 : 8;                // sweeps in flight (16 vectors with V)
+  static_assert(kThreads % TPR == 0, "thread slots must tile the block");
+
+  const int slot = threadIdx.x % TPR;
+  const int hrow0 = threadIdx.x / TPR;
+  const int f0 = slot * NF;
+  const int lo_off = P.rope_off_bytes + slot * 16;
+  const int hi_off = lo_off + RD;                // neox partner: +RD/2 elements
+
+  const int64_t n_units = static_cast<int64_t>(P.n_runs) * P.n_lgroups;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const int lg = static_cast<int>(u / P.n_runs);
+    const RunDesc r = P.runs[u - static_cast<int64_t>(lg) * P.n_runs];
+    if (STITCH) emit_recompute(P, r, lg);
+    int blk, row0;
+    if (!resolve_block(P, r, blk, row0)) continue;
+
+    const bool rot = (r.delta != 0);
+    float c[NF], s[NF];
+    if (rot) {
+#pragma unroll
+      for (int k = 0; k < NF; ++k) shift_cossin(r.delta, __ldg(P.freq + f0 + k), c[k], s[k]);
+    }
+
+    const int64_t dst_off = (static_cast<int64_t>(blk) * P.block_size + row0) * P.row_bytes;
+    const int64_t src_off = STITCH ? static_cast<int64_t>(r.src_tok) * P.row_bytes : dst_off;
+    const int nh = r.ntok * P.heads_per_token;
+    const int l_begin = lg * P.lg_size;
+    const int l_end = min(P.num_layers, l_begin + P.lg_size);
+
+    for (int l = l_begin; l < l_end; ++l) {
+      const uint8_t* ks = (STITCH ? P.k_src + l * P.src_layer_stride : P.k_dst + l * P.dst_layer_stride) + src_off;
+      uint8_t* kd = P.k_dst + l * P.dst_layer_stride + dst_off;
+      const uint8_t* vs = STITCH ? P.v_src + l * P.src_layer_stride + src_off : nullptr;
+      uint8_t* vd = STITCH ? P.v_dst + l * P.dst_layer_stride + dst_off : nullptr;
+
+      for (int h0 = hrow0; h0 < nh; h0 += HSTEP * U) {
+        uint4 ka[U], kb[U], va[U], vb[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int h = h0 + j * HSTEP;
+          if (h < nh) {
+            const int64_t o = static_cast<int64_t>(h) * P.head_stride;
+            if (STITCH) {
+              ka[j] = ld_stream(ks + o + lo_off);
+              if (NEOX) kb[j] = ld_stream(ks + o + hi_off);
+              va[j] = ld_stream(vs + o + lo_off);
+              if (NEOX) vb[j] = ld_stream(vs + o + hi_off);
+            } else {
+              ka[j] = ld_plain(ks + o + lo_off);
+              if (NEOX) kb[j] = ld_plain(ks + o + hi_off);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int h = h0 + j * HSTEP;
+          if (h < nh) {
+            const int64_t o = static_cast<int64_t>(h) * P.head_stride;
+            if (rot) {
+              if (NEOX) rotate_neox(ka[j], kb[j], c, s);
+              else rotate_interleaved(ka[j], c, s);
+            }
+            if (STITCH) {
+              st_stream(kd + o + lo_off, ka[j]);
+              if (NEOX) st_stream(kd + o + hi_off, kb[j]);
+              st_stream(vd + o + lo_off, va[j]);
+              if (NEOX) st_stream(vd + o + hi_off, vb[j]);
+            } else {
+              st_plain(kd + o + lo_off, ka[j]);
+              if (NEOX) st_plain(kd + o + hi_off, kb[j]);
+            }
+          }
+        }
+      }
+    }
+  }
+  if (STITCH) emit_indptr(P);
+}
+
+// ------------------------------------------------------------- MLA stitch
+//
+// Row = 512-d latent (64 vectors, copied) + 64-d rope key (8 vectors,
+// rotated): Irminsul, 2.1 Structural Insight: MLA Decomposition and 2.2
+// "delta-Rotation Rule".  288 threads = 4 rows x 72 vectors, so every thread
+// keeps one column (and one set of frequencies) for the whole kernel.
+constexpr int kMlaRowVecs = 72;
+constexpr int kMlaLatVecs = 64;
+constexpr int kMlaRowsPerSweep = 4;
+constexpr int kMlaThreads = kMlaRowVecs * kMlaRowsPerSweep;  // 288
+
+template <int PAIRING>
+__global__ void __launch_bounds__(kMlaThreads) k_stitch_mla(const KernelParams P) {
+  constexpr bool NEOX = (PAIRING == kNeox);
+  constexpr int NF = NEOX ? 8 : 4;
+  constexpr int U = 4;
+  const int col = threadIdx.x % kMlaRowVecs;
+  const int trow = threadIdx.x / kMlaRowVecs;
+  // rope role: interleaved -> every rope column rotates its own 4 pairs;
+  // neox -> columns 64..67 rotate with partners 68..71, which stay idle.
+  const bool rope_col = col >= kMlaLatVecs;
+  const bool active = !(NEOX && col >= kMlaLatVecs + 4);
+  const int rv = col - kMlaLatVecs;
+  const int f0 = rope_col ? rv * NF : 0;
+
+  const int64_t n_units = static_cast<int64_t>(P.n_runs) * P.n_lgroups;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const int lg = static_cast<int>(u / P.n_runs);
+    const RunDesc r = P.runs[u - static_cast<int64_t>(lg) * P.n_runs];
+    emit_recompute(P, r, lg);
+    int blk, row0;
+    if (!resolve_block(P, r, blk, row0)) continue;
+
+    const bool rot = rope_col && (r.delta != 0);
+    float c[NF], s[NF];
+    if (rot) {
+#pragma unroll
+      for (int k = 0; k < NF; ++k) shift_cossin(r.delta, __ldg(P.freq + f0 + k), c[k], s[k]);
+    }
+    const int64_t dst_off = (static_cast<int64_t>(blk) * P.block_size + row0) * P.row_bytes;
+    const int64_t src_off = static_cast<int64_t>(r.src_tok) * P.row_bytes;
+    const int l_begin = lg * P.lg_size;
+    const int l_end = min(P.num_layers, l_begin + P.lg_size);
+
+    for (int l = l_begin; l < l_end; ++l) {
+      const uint8_t* src = P.k_src + l * P.src_layer_stride + src_off + col * 16;
+      uint8_t* dst = P.k_dst + l * P.dst_layer_stride + dst_off + col * 16;
+      if (!active) continue;
+      for (int r0 = trow; r0 < r.ntok; r0 += kMlaRowsPerSweep * U) {
+        uint4 x[U], y[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int row = r0 + j * kMlaRowsPerSweep;
+          if (row < r.ntok) {
+            x[j] = ld_stream(src + static_cast<int64_t>(row) * P.row_bytes);
+            if (NEOX && rope_col) y[j] = ld_stream(src + static_cast<int64_t>(row) * P.row_bytes + 64);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int row = r0 + j * kMlaRowsPerSweep;
+          if (row < r.ntok) {
+            if (rot) {
+              if (NEOX) rotate_neox(x[j], y[j], c, s);
+              else rotate_interleaved(x[j], c, s);
+            }
+            st_stream(dst + static_cast<int64_t>(row) * P.row_bytes, x[j]);
+            if (NEOX && rope_col) st_stream(dst + static_cast<int64_t>(row) * P.row_bytes + 64, y[j]);
+          }
+        }
+      }
+    }
+  }
+  emit_indptr(P);
+}
+
+// ---------------------------------------------------------- cos/sin probe
+
+__global__ void k_cossin(const int32_t* __restrict__ deltas, int32_t n, const float2* __restrict__ freq,
+                         int32_t half, float* __restrict__ out) {
+  const int64_t total = static_cast<int64_t>(n) * half;
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t j = t / half;
+    const int i = static_cast<int>(t - j * half);
+    float c, s;
+    shift_cossin(deltas[j], freq[i], c, s);
+    out[2 * t] = c;
+    out[2 * t + 1] = s;
+  }
+}
+
+template <typename K>
+int occupancy_of(K kernel, int threads) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- launchers
+
+#define PIC_DISPATCH_RD(RD_, PAIR_, STITCH_, FN)                                   \
+  do {                                                                             \
+    if ((RD_) == 64) { FN(PAIR_, 64, STITCH_); }                                   \
+    else if ((RD_) == 128) { FN(PAIR_, 128, STITCH_); }                            \
+    else if ((RD_) == 256) { FN(PAIR_, 256, STITCH_); }                            \
+    else return cudaErrorInvalidValue;                                             \
+  } while (0)
+
+#define PIC_LAUNCH_ROWS(PAIR_, RD_, STITCH_) \
+  k_rotate_rows<PAIR_, RD_, STITCH_><<<grid, kThreads, 0, stream>>>(p)
+
+#define PIC_OCC_ROWS(PAIR_, RD_, STITCH_) \
+  return occupancy_of(k_rotate_rows<PAIR_, RD_, STITCH_>, kThreads)
+
+cudaError_t launch_stitch_gqa(const KernelParams& p, int pairing, int head_dim, int grid,
+                              cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (pairing == kNeox) PIC_DISPATCH_RD(head_dim, kNeox, true, PIC_LAUNCH_ROWS);
+  else PIC_DISPATCH_RD(head_dim, kInterleaved, true, PIC_LAUNCH_ROWS);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rerotate(const KernelParams& p, int pairing, int rope_dim, int grid,
+                            cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (pairing == kNeox) PIC_DISPATCH_RD(rope_dim, kNeox, false, PIC_LAUNCH_ROWS);
+  else PIC_DISPATCH_RD(rope_dim, kInterleaved, false, PIC_LAUNCH_ROWS);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stitch_mla(const KernelParams& p, int pairing, int grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (pairing == kNeox) k_stitch_mla<kNeox><<<grid, kMlaThreads, 0, stream>>>(p);
+  else k_stitch_mla<kInterleaved><<<grid, kMlaThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cossin(const int32_t* deltas, int32_t n, const float2* freq, int32_t half,
+                          float* out, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(n) * half;
+  if (total <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int grid = static_cast<int>(want < 65535 ? want : 65535);
+  k_cossin<<<grid, threads, 0, stream>>>(deltas, n, freq, half, out);
+  return cudaGetLastError();
+}
+
+int occupancy_stitch_gqa(int pairing, int head_dim) {
+  if (pairing == kNeox) PIC_DISPATCH_RD(head_dim, kNeox, true, PIC_OCC_ROWS);
+  else PIC_DISPATCH_RD(head_dim, kInterleaved, true, PIC_OCC_ROWS);
+  return 1;
+}
+
+int occupancy_rerotate(int pairing, int rope_dim) {
+  if (pairing == kNeox) PIC_DISPATCH_RD(rope_dim, kNeox, false, PIC_OCC_ROWS);
+  else PIC_DISPATCH_RD(rope_dim, kInterleaved, false, PIC_OCC_ROWS);
+  return 1;
+}
+
+int occupancy_stitch_mla(int pairing) {
+  return pairing == kNeox ? occupancy_of(k_stitch_mla<kNeox>, kMlaThreads)
+                          : occupancy_of(k_stitch_mla<kInterleaved>, kMlaThreads);
+}
+
+}  // namespace pic

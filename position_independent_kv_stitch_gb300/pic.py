@@ -1,0 +1,409 @@
+"""Thin Python binding of libpic (include/pic.h): ctypes marshalling only.
+
+Every function keeps its C name.  Device buffers are torch tensors (their
+``data_ptr()`` and strides are passed through); the stream is torch's current
+CUDA stream unless one is given.  Every step of the path runs in libpic's
+kernels; nothing here computes.  A missing or unloadable libpic raises
+immediately -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import _build
+
+PIC_OK = 0
+STATUS_NAMES = {
+    0: "PIC_OK", 1: "PIC_ERR_INVALID_ARG", 2: "PIC_ERR_UNKNOWN_CHUNK", 3: "PIC_ERR_KEY_CONFLICT",
+    4: "PIC_ERR_OUT_OF_BLOCKS", 5: "PIC_ERR_CAPACITY", 6: "PIC_ERR_RANGE", 7: "PIC_ERR_ALIGNMENT",
+    8: "PIC_ERR_CUDA", 9: "PIC_ERR_DEVICE_CHECK", 10: "PIC_ERR_UNSUPPORTED",
+}
+PIC_KIND_GQA, PIC_KIND_MLA = 0, 1
+PIC_PAIRING_NEOX_HALF, PIC_PAIRING_INTERLEAVED = 0, 1
+PIC_SCALING_NONE, PIC_SCALING_LLAMA3 = 0, 1
+PIC_KEY_BYTES = 32
+PIC_DEV_BAD_BLOCK = 0x1
+
+
+class PicError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = STATUS_NAMES.get(status, f"PIC_ERR_{status}")
+        super().__init__(f"{self.status_name}: {message}")
+
+
+class pic_model_desc(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32), ("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("rope_offset", ctypes.c_int32),
+        ("pairing", ctypes.c_int32), ("block_size", ctypes.c_int32), ("scaling", ctypes.c_int32),
+        ("llama3_orig_max_pos", ctypes.c_int32), ("rope_theta", ctypes.c_double),
+        ("llama3_factor", ctypes.c_double), ("llama3_low_freq_factor", ctypes.c_double),
+        ("llama3_high_freq_factor", ctypes.c_double), ("inv_freq", ctypes.POINTER(ctypes.c_double)),
+    ]
+
+
+class pic_request_desc(ctypes.Structure):
+    _fields_ = [
+        ("chunk_ids", ctypes.POINTER(ctypes.c_int32)), ("take_tokens", ctypes.POINTER(ctypes.c_int32)),
+        ("dst_pos", ctypes.POINTER(ctypes.c_int32)), ("n_chunks", ctypes.c_int32),
+        ("start_pos", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+        ("k_nonleading", ctypes.c_int32), ("k_leading", ctypes.c_int32),
+    ]
+
+
+class pic_shift_seg(ctypes.Structure):
+    _fields_ = [("req", ctypes.c_int32), ("start_pos", ctypes.c_int32),
+                ("num_tokens", ctypes.c_int32), ("delta", ctypes.c_int32)]
+
+
+_c_void_p = ctypes.c_void_p
+_i32, _i64, _u32, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
+_P = ctypes.POINTER
+
+_SIGNATURES = {
+    "pic_abi_version": (_i32, []),
+    "pic_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pic_last_error": (ctypes.c_char_p, [_c_void_p]),
+    "pic_create": (ctypes.c_int, [_P(pic_model_desc), _i32, _P(_c_void_p)]),
+    "pic_destroy": (None, [_c_void_p]),
+    "pic_register_chunk": (ctypes.c_int, [_c_void_p, ctypes.c_char_p, _i64, _i32, _i32, _P(_i32), _P(_i32)]),
+    "pic_lookup_chunk": (ctypes.c_int, [_c_void_p, ctypes.c_char_p, _P(_i32)]),
+    "pic_chunk_info": (ctypes.c_int, [_c_void_p, _i32, _P(_i64), _P(_i32), _P(_i32)]),
+    "pic_unregister_chunk": (ctypes.c_int, [_c_void_p, _i32]),
+    "pic_build_block_table": (ctypes.c_int, [_c_void_p, _P(pic_request_desc), _P(_i32), _i32, _P(_c_void_p)]),
+    "pic_free_request": (ctypes.c_int, [_c_void_p, _c_void_p]),
+    "pic_plan_info": (ctypes.c_int, [_c_void_p, _P(_i32), _P(_i32), _P(_i32), _P(_i32)]),
+    "pic_plan_segment": (ctypes.c_int, [_c_void_p, _i32, _P(_i32), _P(_i64), _P(_i32), _P(_i32), _P(_i32)]),
+    "pic_workspace_bytes": (_sz, [_c_void_p, _P(_c_void_p), _i32]),
+    "pic_stitch": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _c_void_p, _c_void_p, _i64,
+                                  _c_void_p, _c_void_p, _i64, _c_void_p, _i32, _c_void_p, _c_void_p,
+                                  _i64, _c_void_p, _sz, _c_void_p]),
+    "pic_rerotate_workspace_bytes": (_sz, [_c_void_p, _P(pic_shift_seg), _i32]),
+    "pic_rerotate_inplace": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _i32, _i32,
+                                            _P(pic_shift_seg), _i32, _c_void_p, _sz, _c_void_p]),
+    "pic_recompute_indices": (ctypes.c_int, [_P(_c_void_p), _i32, _P(_i32), _P(_i32), _i64, _P(_i64)]),
+    "pic_query_device_status": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _P(_u32)]),
+    "pic_rotation_cossin": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _sz, _c_void_p]),
+}
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Loads libpic.so (building it first only when asked); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and (not os.path.exists(_build.LIB_PATH) or _build.is_stale()):
+        _build.build()
+    if not os.path.exists(_build.LIB_PATH):
+        raise ImportError(f"libpic is not built ({_build.LIB_PATH} missing): run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_build.LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(st: int, ctx=None):
+    if st != PIC_OK:
+        msg = load().pic_last_error(ctx)
+        raise PicError(st, msg.decode() if msg else "")
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _i32_array(seq):
+    if seq is None:
+        return None
+    a = (ctypes.c_int32 * len(seq))(*[int(x) for x in seq])
+    return a
+
+
+def _plan_array(plans):
+    arr = (ctypes.c_void_p * max(1, len(plans)))()
+    for i, p in enumerate(plans):
+        arr[i] = p.value if isinstance(p, ctypes.c_void_p) else p
+    return arr
+
+
+# ------------------------------------------------------------------ context
+
+def pic_abi_version() -> int:
+    return load().pic_abi_version()
+
+
+def pic_create(kind, num_layers, num_kv_heads, head_dim, rope_dim, rope_offset, pairing,
+               block_size, rope_theta, num_cache_blocks, llama3=None, inv_freq=None):
+    """Returns an opaque context handle (ctypes.c_void_p)."""
+    d = pic_model_desc()
+    d.kind, d.num_layers, d.num_kv_heads, d.head_dim = kind, num_layers, num_kv_heads, head_dim
+    d.rope_dim, d.rope_offset, d.pairing, d.block_size = rope_dim, rope_offset, pairing, block_size
+    d.rope_theta = float(rope_theta)
+    keep = None
+    if llama3:
+        d.scaling = PIC_SCALING_LLAMA3
+        d.llama3_factor = llama3["factor"]
+        d.llama3_low_freq_factor = llama3["low_freq_factor"]
+        d.llama3_high_freq_factor = llama3["high_freq_factor"]
+        d.llama3_orig_max_pos = int(llama3["orig_max_pos"])
+    if inv_freq is not None:
+        keep = (ctypes.c_double * len(inv_freq))(*[float(x) for x in inv_freq])
+        d.inv_freq = ctypes.cast(keep, ctypes.POINTER(ctypes.c_double))
+    out = ctypes.c_void_p()
+    st = load().pic_create(ctypes.byref(d), int(num_cache_blocks), ctypes.byref(out))
+    _check(st, None)
+    return out
+
+
+def pic_destroy(ctx):
+    load().pic_destroy(ctx)
+
+
+def pic_last_error(ctx=None) -> str:
+    return load().pic_last_error(ctx).decode()
+
+
+# ----------------------------------------------------------------- registry
+
+def pic_register_chunk(ctx, key: bytes, pool_token_offset: int, num_tokens: int, base_pos: int = 0):
+    """Returns (chunk_id, is_new)."""
+    if len(key) != PIC_KEY_BYTES:
+        raise ValueError("key must be 32 bytes")
+    cid, new = ctypes.c_int32(), ctypes.c_int32()
+    _check(load().pic_register_chunk(ctx, key, int(pool_token_offset), int(num_tokens), int(base_pos),
+                                     ctypes.byref(cid), ctypes.byref(new)), ctx)
+    return cid.value, bool(new.value)
+
+
+def pic_lookup_chunk(ctx, key: bytes) -> int:
+    cid = ctypes.c_int32()
+    _check(load().pic_lookup_chunk(ctx, key, ctypes.byref(cid)), ctx)
+    return cid.value
+
+
+def pic_chunk_info(ctx, chunk_id: int):
+    off, n, b = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().pic_chunk_info(ctx, chunk_id, ctypes.byref(off), ctypes.byref(n), ctypes.byref(b)), ctx)
+    return off.value, n.value, b.value
+
+
+def pic_unregister_chunk(ctx, chunk_id: int):
+    _check(load().pic_unregister_chunk(ctx, chunk_id), ctx)
+
+
+# ---------------------------------------------------------------- planning
+
+def pic_build_block_table(ctx, chunk_ids, max_blocks: int, take_tokens=None, dst_pos=None,
+                          start_pos: int = 0, total_tokens: int = 0, k_nonleading: int = 0,
+                          k_leading: int = 0):
+    """Returns (plan handle, block table as numpy int32[max_blocks])."""
+    rq = pic_request_desc()
+    ids = _i32_array(list(chunk_ids))
+    take = _i32_array(take_tokens)
+    pos = _i32_array(dst_pos)
+    rq.chunk_ids = ctypes.cast(ids, _P(_i32)) if ids is not None else None
+    rq.take_tokens = ctypes.cast(take, _P(_i32)) if take is not None else None
+    rq.dst_pos = ctypes.cast(pos, _P(_i32)) if pos is not None else None
+    rq.n_chunks = len(chunk_ids)
+    rq.start_pos, rq.total_tokens = int(start_pos), int(total_tokens)
+    rq.k_nonleading, rq.k_leading = int(k_nonleading), int(k_leading)
+    bt = np.empty(max(0, int(max_blocks)), dtype=np.int32)
+    plan = ctypes.c_void_p()
+    _check(load().pic_build_block_table(ctx, ctypes.byref(rq),
+                                        bt.ctypes.data_as(_P(_i32)) if bt.size else None,
+                                        int(max_blocks), ctypes.byref(plan)), ctx)
+    return plan, bt
+
+
+def pic_free_request(ctx, plan):
+    _check(load().pic_free_request(ctx, plan), ctx)
+
+
+def pic_plan_info(plan):
+    t, b, s, r = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().pic_plan_info(plan, ctypes.byref(t), ctypes.byref(b), ctypes.byref(s), ctypes.byref(r)))
+    return {"total_tokens": t.value, "num_blocks": b.value, "num_segments": s.value, "num_recompute": r.value}
+
+
+def pic_plan_segment(plan, j: int):
+    c, src, n, p, d = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().pic_plan_segment(plan, j, ctypes.byref(c), ctypes.byref(src), ctypes.byref(n),
+                                   ctypes.byref(p), ctypes.byref(d)))
+    return {"chunk_id": c.value, "src_tok": src.value, "num_tokens": n.value, "dst_pos": p.value,
+            "delta": d.value}
+
+
+def pic_recompute_indices(plans):
+    """Host recompute list of a batch: (indptr int32[n+1], idx int32[count])."""
+    arr = _plan_array(plans)
+    count = ctypes.c_int64()
+    _check(load().pic_recompute_indices(arr, len(plans), None, None, 0, ctypes.byref(count)))
+    idx = np.empty(max(1, count.value), dtype=np.int32)
+    indptr = np.empty(len(plans) + 1, dtype=np.int32)
+    _check(load().pic_recompute_indices(arr, len(plans), idx.ctypes.data_as(_P(_i32)),
+                                        indptr.ctypes.data_as(_P(_i32)), count.value, ctypes.byref(count)))
+    return indptr, idx[:count.value]
+
+
+# ------------------------------------------------------------------ stitch
+
+def pic_workspace_bytes(ctx, plans) -> int:
+    return int(load().pic_workspace_bytes(ctx, _plan_array(plans), len(plans)))
+
+
+def _layer_stride_bytes(t):
+    return t.stride(0) * t.element_size() if t is not None else 0
+
+
+def pic_stitch(ctx, plans, k_pool, v_pool, k_cache, v_cache, block_tables, recompute_idx=None,
+               recompute_indptr=None, workspace=None, stream=None):
+    """Enqueues the stitch.  Tensors: pools [L][tokens][...], caches
+    [L][blocks][block_size][...] (bf16, contiguous rows), block_tables int32
+    [n_req][max_blocks] on the device, recompute outputs int32 or None,
+    workspace uint8 with >= pic_workspace_bytes bytes."""
+    arr = _plan_array(plans)
+    _check_device_int32(block_tables, "block_tables")
+    if block_tables.dim() != 2 or (len(plans) > 0 and block_tables.shape[0] < len(plans)):
+        raise ValueError("block_tables must be [n_req][max_blocks] with a row per plan")
+    if recompute_indptr is not None:
+        _check_device_int32(recompute_indptr, "recompute_indptr")
+        _check_device_int32(recompute_idx, "recompute_idx")
+        if recompute_indptr.numel() < len(plans) + 1:
+            raise ValueError("recompute_indptr needs n_req + 1 entries")
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if t is not None and (not t.is_cuda or not _is_bf16(t) or not _rows_contiguous(t)):
+            raise ValueError(f"{name} must be a CUDA bf16 tensor with contiguous rows")
+    pool_ls = _layer_stride_bytes(k_pool)
+    cache_ls = _layer_stride_bytes(k_cache)
+    if v_pool is not None and _layer_stride_bytes(v_pool) != pool_ls:
+        raise ValueError("k_pool and v_pool must share a layer stride")
+    if v_cache is not None and _layer_stride_bytes(v_cache) != cache_ls:
+        raise ValueError("k_cache and v_cache must share a layer stride")
+    cap = recompute_idx.numel() if recompute_idx is not None else 0
+    st = load().pic_stitch(ctx, arr, len(plans), _ptr(k_pool), _ptr(v_pool), pool_ls,
+                           _ptr(k_cache), _ptr(v_cache), cache_ls, _ptr(block_tables),
+                           int(block_tables.shape[1]) if block_tables.dim() == 2 else int(block_tables.numel()),
+                           _ptr(recompute_idx), _ptr(recompute_indptr), cap, _ptr(workspace),
+                           workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                           _stream_handle(stream))
+    _check(st, ctx)
+
+
+def _check_device_int32(t, name):
+    import torch
+    if t is None or not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+
+
+def _rows_contiguous(t):
+    """Everything but the layer axis is dense (the layer stride is passed separately)."""
+    return t[0].is_contiguous() if t.dim() > 1 else t.is_contiguous()
+
+
+def _is_bf16(t):
+    import torch
+    return t.dtype == torch.bfloat16
+
+
+def _shift_array(segs):
+    arr = (pic_shift_seg * max(1, len(segs)))()
+    for i, (req, start, n, delta) in enumerate(segs):
+        arr[i].req, arr[i].start_pos, arr[i].num_tokens, arr[i].delta = int(req), int(start), int(n), int(delta)
+    return arr
+
+
+def pic_rerotate_workspace_bytes(ctx, segs) -> int:
+    return int(load().pic_rerotate_workspace_bytes(ctx, _shift_array(segs), len(segs)))
+
+
+def pic_rerotate_inplace(ctx, k_cache, block_tables, segs, workspace, stream=None):
+    """segs: iterable of (req, start_pos, num_tokens, delta) on the host."""
+    segs = list(segs)
+    arr = _shift_array(segs)
+    _check_device_int32(block_tables, "block_tables")
+    if not k_cache.is_cuda or not _is_bf16(k_cache) or not _rows_contiguous(k_cache):
+        raise ValueError("k_cache must be a CUDA bf16 tensor with contiguous rows")
+    n_tables = int(block_tables.shape[0]) if block_tables.dim() == 2 else 1
+    max_blocks = int(block_tables.shape[-1])
+    st = load().pic_rerotate_inplace(ctx, _ptr(k_cache), _layer_stride_bytes(k_cache), _ptr(block_tables),
+                                     n_tables, max_blocks, arr, len(segs), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, ctx)
+
+
+def pic_query_device_status(ctx, workspace, stream=None) -> int:
+    """Synchronizes the stream; returns the device status word (raises on a
+    non-zero word with PIC_ERR_DEVICE_CHECK)."""
+    out = ctypes.c_uint32()
+    st = load().pic_query_device_status(ctx, _ptr(workspace), _stream_handle(stream), ctypes.byref(out))
+    if st != PIC_OK:
+        raise PicError(st, load().pic_last_error(ctx).decode())
+    return out.value
+
+
+def pic_rotation_cossin(ctx, deltas, out, workspace, stream=None):
+    """deltas: int32 device tensor [n]; out: float32 device tensor [n][rope_dim/2][2]."""
+    st = load().pic_rotation_cossin(ctx, _ptr(deltas), int(deltas.numel()), _ptr(out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, ctx)
+
+
+# ----------------------------------------------------------- convenience
+
+@dataclass
+class ModelSpec:
+    """Geometry + RoPE settings (mirrors pic_model_desc)."""
+    kind: int
+    num_layers: int
+    num_kv_heads: int
+    head_dim: int
+    rope_dim: int
+    rope_offset: int
+    pairing: int
+    block_size: int
+    rope_theta: float
+    llama3: dict | None = None
+    inv_freq: list | None = None
+
+    @property
+    def row_bytes(self) -> int:
+        return self.num_kv_heads * self.head_dim * 2
+
+
+def model_spec_from(model) -> ModelSpec:
+    """ModelSpec from any object with the workload-model attributes."""
+    return ModelSpec(
+        kind=PIC_KIND_GQA if model.kind == "gqa" else PIC_KIND_MLA,
+        num_layers=model.num_layers, num_kv_heads=model.num_kv_heads, head_dim=model.head_dim,
+        rope_dim=model.rope_dim, rope_offset=model.rope_offset,
+        pairing=PIC_PAIRING_NEOX_HALF if model.pairing == "neox" else PIC_PAIRING_INTERLEAVED,
+        block_size=model.block_size, rope_theta=model.rope_theta, llama3=model.llama3)
+
+
+def create_from_spec(spec: ModelSpec, num_cache_blocks: int):
+    return pic_create(spec.kind, spec.num_layers, spec.num_kv_heads, spec.head_dim, spec.rope_dim,
+                      spec.rope_offset, spec.pairing, spec.block_size, spec.rope_theta,
+                      num_cache_blocks, llama3=spec.llama3, inv_freq=spec.inv_freq)
