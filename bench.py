@@ -85,15 +85,18 @@ def recorded_traffic(workload, mode):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons; only samples whose timestamps
+    fall inside the timed region are kept."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, index, period_ms=20):
+        self.index, self.period_ms = index, period_ms
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -101,38 +104,61 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader",
-                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", str(self.period_ms)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            deadline = time.time() + 5.0
+            while time.time() < deadline and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
             return None
+        time.sleep(2 * self.period_ms / 1000.0)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        inside, all_rows = [], []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1].split()[0]))
-                    mx.append(float(parts[2].split()[0]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    row = (ts, float(parts[2].split()[0]), float(parts[3].split()[0]), parts[6:10])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
+                all_rows.append(row)
+                if self.t0 is not None and self.t0 <= ts <= self.t1 + self.period_ms / 1000.0:
+                    inside.append(row)
         os.unlink(self.path)
-        if not sm:
+        rows = inside
+        note = None
+        if not rows and all_rows and self.t0 is not None:
+            rows = [min(all_rows, key=lambda r: abs(r[0] - self.t0))]
+            note = "timed region shorter than the sampling period: nearest sample reported"
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for r in rows:
+            for n, v in zip(self.REASONS, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        out = {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+               "reasons": sorted(reasons), "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
 
 
 # ------------------------------------------------------------------ oracle
@@ -267,6 +293,9 @@ class Rig:
                 segs.append((r, s["dst_pos"], s["num_tokens"], new - s["dst_pos"]))
         self.d_bt.copy_(self.torch.from_numpy(bt))
         self._kept_plans = plans
+        # fill the cache with stitched keys once, so the shift runs on real data
+        self.pic.pic_stitch(self.ctx, plans, self.k_pool, self.v_pool, self.k_cache, self.v_cache, self.d_bt,
+                            self.ridx, self.indptr, self.ws)
         return segs
 
     def plan(self):
@@ -360,7 +389,7 @@ def run_e2e(rig, steps, warmup):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pic", choices=["pic", "reference"])
     ap.add_argument("--workload", default="llama31_8b_rag", choices=sorted(W.WORKLOADS))
@@ -408,11 +437,13 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
     t0.record()
     for i in range(args.steps):
         rig.step(kev[i])
     t1.record()
     torch.cuda.synchronize()
+    clocks.mark_end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
