@@ -267,6 +267,41 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
                       int64_t recompute_capacity, void* d_workspace, size_t workspace_bytes,
                       pic_stream_t stream);
 
+/*
+ * pic_stitch_noalloc -- pic_stitch without a caller workspace.  The pages
+ * have no counterpart to this call; it exists for deployment.
+ *
+ * Some callers cannot allocate device memory where they stitch: an engine
+ * that gave (nearly) all of HBM to its own KV-cache pool, a framework that
+ * hands a plugin only the tensors it reads and writes, or a latency-bound
+ * loop that cannot pay for cudaMalloc / cudaFree (cudaFree synchronizes the
+ * whole device).  This call runs the same kernel and computes the same result
+ * as pic_stitch, with the same arguments minus the workspace; it allocates no
+ * memory of any kind.  Its scratch (run list, frequency table, status word)
+ * is a fixed 4 MiB array of device memory inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - Limit: a batch whose scratch image exceeds 4 MiB (about 130,000 runs of
+ *     up to block_size tokens, i.e. about two million tokens per call at block
+ *     size 16) fails with PIC_ERR_CAPACITY before anything is enqueued; split
+ *     the batch or use pic_stitch.
+ *   - Set-up: the first call on a device (with that device current) looks up
+ *     the array's device address; make that first call before any stream
+ *     capture.
+ *   - Sharing: every call uses the same array and leaves its contents behind;
+ *     each call rewrites what it needs, including a zeroed status word.  Calls
+ *     that overlap on the GPU (different streams) race on it, and calls from
+ *     several host threads at once race on its host image: issue one call at a
+ *     time.
+ *   - d_status: optional device uint32 that receives the device status word
+ *     of this launch (PIC_DEV_* bits, 0 = clean); may be NULL.
+ */
+pic_status pic_stitch_noalloc(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                              const void* k_pool, const void* v_pool, int64_t pool_layer_stride_bytes,
+                              void* k_cache, void* v_cache, int64_t cache_layer_stride_bytes,
+                              const int32_t* d_block_tables, int32_t max_blocks,
+                              int32_t* d_recompute_idx, int32_t* d_recompute_indptr,
+                              int64_t recompute_capacity, uint32_t* d_status, pic_stream_t stream);
+
 /* ------------------------------------------------------- in-place shift */
 
 size_t pic_rerotate_workspace_bytes(const pic_ctx* ctx, const pic_shift_seg* segs,

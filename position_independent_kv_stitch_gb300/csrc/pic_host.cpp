@@ -885,3 +885,163 @@ pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n,
 }
 
 }  // extern "C"
+
+// ===================================================== scratch-backed stitch
+//
+// Used only by the no-alloc entry point.  Same validation, workspace image
+// and launch as pic_stitch, but the image is written straight into a
+// caller-owned host buffer and uploaded with a plain (pageable) copy into a
+// caller-owned device buffer, so nothing is allocated here.
+
+namespace {
+
+pic_status check_stitch_args(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                             const void* k_pool, const void* v_pool, int64_t pool_ls,
+                             const void* k_cache, const void* v_cache, int64_t cache_ls,
+                             const int32_t* d_bt, int32_t max_blocks, const int32_t* d_ridx,
+                             const int32_t* d_indptr, int64_t recompute_capacity,
+                             int64_t* n_rec_out) {
+  const pic_model_desc& m = ctx->model;
+  if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
+  for (int32_t r = 0; r < n_req; ++r) {
+    if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
+    if (static_cast<int32_t>(plans[r]->blocks.size()) > max_blocks)
+      return fail(ctx, PIC_ERR_CAPACITY, "plans[%d] has %zu blocks, block-table rows hold %d", r,
+                  plans[r]->blocks.size(), max_blocks);
+  }
+  const bool gqa = m.kind == PIC_KIND_GQA;
+  if (!k_pool || !k_cache || !d_bt) return fail(ctx, PIC_ERR_INVALID_ARG, "null pool, cache or block table");
+  if (gqa && (!v_pool || !v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs v_pool and v_cache");
+  if (!gqa && (v_pool || v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
+  if ((d_ridx == nullptr) != (d_indptr == nullptr))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "pass both recompute outputs or neither");
+  if (!vectorized_bytes_ok(k_pool) || !vectorized_bytes_ok(k_cache) ||
+      (gqa && (!vectorized_bytes_ok(v_pool) || !vectorized_bytes_ok(v_cache))) || (pool_ls & 15) || (cache_ls & 15))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "pools, caches and layer strides must be 16-byte aligned");
+  const int64_t row_bytes = row_bytes_of(m);
+  if (pool_ls < 0 || cache_ls < 0 || (m.num_layers > 1 && (pool_ls == 0 || cache_ls == 0)))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "bad layer strides");
+  if (m.num_layers > 1 && cache_ls < static_cast<int64_t>(ctx->num_cache_blocks) * m.block_size * row_bytes)
+    return fail(ctx, PIC_ERR_RANGE, "cache layer stride smaller than num_cache_blocks * block_size rows");
+  int64_t n_rec = 0;
+  for (int32_t r = 0; r < n_req; ++r) n_rec += plans[r]->n_recompute;
+  if (d_ridx && n_rec > recompute_capacity)
+    return fail(ctx, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
+                static_cast<long long>(n_rec), static_cast<long long>(recompute_capacity));
+  *n_rec_out = n_rec;
+  return PIC_OK;
+}
+
+}  // namespace
+
+namespace pic {
+
+pic_status set_error(pic_ctx* ctx, pic_status st, const char* msg) { return fail(ctx, st, "%s", msg); }
+
+pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                               const void* k_pool, const void* v_pool, int64_t pool_ls,
+                               void* k_cache, void* v_cache, int64_t cache_ls,
+                               const int32_t* d_bt, int32_t max_blocks, int32_t* d_ridx,
+                               int32_t* d_indptr, int64_t recompute_capacity, void* d_scratch,
+                               size_t scratch_bytes, uint8_t* image, size_t image_bytes,
+                               uint32_t* d_status_out, cudaStream_t s) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  int64_t n_rec = 0;
+  pic_status st = check_stitch_args(ctx, plans, n_req, k_pool, v_pool, pool_ls, k_cache, v_cache, cache_ls,
+                                    d_bt, max_blocks, d_ridx, d_indptr, recompute_capacity, &n_rec);
+  if (st != PIC_OK) return st;
+  const pic_model_desc& m = ctx->model;
+  const int32_t bs = m.block_size;
+  const size_t n_runs = count_stitch_runs(plans, n_req, bs);
+  const WsLayout w = ws_layout(ctx->freq_turns.size(), static_cast<size_t>(n_req) + 1, n_runs);
+  const size_t limit = std::min(scratch_bytes, image_bytes);
+  if (w.total > limit)
+    return fail(ctx, PIC_ERR_CAPACITY,
+                "this batch needs %zu bytes of scratch (%zu runs); the static scratch holds %zu bytes. "
+                "Split the batch or call pic_stitch with a workspace", w.total, n_runs, limit);
+  if (!d_scratch || !image) return fail(ctx, PIC_ERR_INVALID_ARG, "null scratch");
+
+  // Image: zeroed header (the status word must start at 0 on every call),
+  // frequencies, CSR offsets, runs written in place.
+  std::memset(image, 0, w.total);
+  fill_freq(ctx, image, w);
+  int32_t* indptr = reinterpret_cast<int32_t*>(image + w.indptr_off);
+  RunDesc* out = reinterpret_cast<RunDesc*>(image + w.runs_off);
+  size_t k = 0;
+  int64_t idx = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    indptr[r] = static_cast<int32_t>(idx);
+    for (const Segment& sg : plans[r]->segs) {
+      for (int32_t t = 0; t < sg.num_tokens;) {
+        const int32_t pos = sg.dst_pos + t;
+        const int32_t cnt = std::min(bs - pos % bs, sg.num_tokens - t);
+        RunDesc& rd = out[k++];
+        rd.src_tok = static_cast<int32_t>(sg.src_tok + t);
+        rd.dst_pos = pos;
+        rd.req = r;
+        rd.ntok = cnt;
+        rd.delta = sg.delta;
+        rd.idx_off = static_cast<int32_t>(idx);
+        rd.idx_count = t == 0 ? sg.n_recompute : 0;
+        rd.idx_start = sg.dst_pos;
+        t += cnt;
+      }
+      idx += sg.n_recompute;
+    }
+  }
+  indptr[n_req] = static_cast<int32_t>(idx);
+
+  DeviceInfo di;
+  st = current_device(ctx, di);
+  if (st != PIC_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(d_scratch, image, w.total, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "scratch upload");
+
+  uint8_t* ws = static_cast<uint8_t*>(d_scratch);
+  KernelParams p{};
+  p.runs = reinterpret_cast<const RunDesc*>(ws + w.runs_off);
+  p.n_runs = static_cast<int32_t>(n_runs);
+  p.num_layers = m.num_layers;
+  p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
+  p.k_src = static_cast<const uint8_t*>(k_pool);
+  p.v_src = static_cast<const uint8_t*>(v_pool);
+  p.src_layer_stride = pool_ls;
+  p.k_dst = static_cast<uint8_t*>(k_cache);
+  p.v_dst = static_cast<uint8_t*>(v_cache);
+  p.dst_layer_stride = cache_ls;
+  p.block_tables = d_bt;
+  p.max_blocks = max_blocks;
+  p.num_cache_blocks = ctx->num_cache_blocks;
+  p.block_size = bs;
+  p.row_bytes = static_cast<int32_t>(row_bytes_of(m));
+  p.ridx = d_ridx;
+  p.indptr_src = reinterpret_cast<const int32_t*>(ws + w.indptr_off);
+  p.indptr_dst = d_indptr;
+  p.n_indptr = n_req + 1;
+  p.header = reinterpret_cast<WsHeader*>(ws);
+  const bool gqa = m.kind == PIC_KIND_GQA;
+  const int occ = gqa ? occupancy_stitch_gqa(m.pairing, m.head_dim) : occupancy_stitch_mla(m.pairing);
+  const int64_t resident = static_cast<int64_t>(di.sm_count) * occ;
+  choose_layer_groups(static_cast<int64_t>(n_runs), m.num_layers, resident, p.lg_size, p.n_lgroups);
+  const int64_t units = static_cast<int64_t>(n_runs) * p.n_lgroups;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
+  if (gqa) {
+    p.heads_per_token = m.num_kv_heads;
+    p.head_stride = m.head_dim * 2;
+    p.rope_off_bytes = 0;
+    e = launch_stitch_gqa(p, m.pairing, m.head_dim, grid, s);
+  } else {
+    p.heads_per_token = 1;
+    p.head_stride = p.row_bytes;
+    p.rope_off_bytes = m.rope_offset * 2;
+    e = launch_stitch_mla(p, m.pairing, grid, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
+  if (d_status_out) {
+    e = cudaMemcpyAsync(d_status_out, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "status copy");
+  }
+  return ok(ctx);
+}
+
+}  // namespace pic

@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include "pic.h"
+
 namespace pic {
 
 // One run: up to block_size consecutive tokens of one segment that land in
@@ -75,6 +77,22 @@ cudaError_t launch_rerotate(const KernelParams& p, int pairing, int rope_dim, in
                             cudaStream_t stream);
 cudaError_t launch_cossin(const int32_t* deltas, int32_t n, const float2* freq, int32_t half,
                           float* out, cudaStream_t stream);
+
+// Stitch whose workspace image is built in caller-supplied host memory and
+// copied (pageable copy, no pinned staging) into caller-supplied device
+// scratch.  On success it allocates nothing, host or device (only building an
+// error message may touch the heap).  Used by the no-alloc entry point
+// (pic_noalloc.cu), which owns both buffers.
+pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                               const void* k_pool, const void* v_pool, int64_t pool_ls,
+                               void* k_cache, void* v_cache, int64_t cache_ls,
+                               const int32_t* d_bt, int32_t max_blocks, int32_t* d_ridx,
+                               int32_t* d_indptr, int64_t recompute_capacity, void* d_scratch,
+                               size_t scratch_bytes, uint8_t* host_image, size_t host_image_bytes,
+                               uint32_t* d_status_out, cudaStream_t stream);
+
+// Records an error message on ctx (or the calling thread) and returns st.
+pic_status set_error(pic_ctx* ctx, pic_status st, const char* msg);
 
 // Resident CTAs per SM of the kernel the matching launcher would use.
 int occupancy_stitch_gqa(int pairing, int head_dim);

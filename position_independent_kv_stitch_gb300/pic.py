@@ -84,6 +84,9 @@ _SIGNATURES = {
     "pic_stitch": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _c_void_p, _c_void_p, _i64,
                                   _c_void_p, _c_void_p, _i64, _c_void_p, _i32, _c_void_p, _c_void_p,
                                   _i64, _c_void_p, _sz, _c_void_p]),
+    "pic_stitch_noalloc": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _c_void_p, _c_void_p, _i64,
+                                          _c_void_p, _c_void_p, _i64, _c_void_p, _i32, _c_void_p,
+                                          _c_void_p, _i64, _c_void_p, _c_void_p]),
     "pic_rerotate_workspace_bytes": (_sz, [_c_void_p, _P(pic_shift_seg), _i32]),
     "pic_rerotate_inplace": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _i32, _i32,
                                             _P(pic_shift_seg), _i32, _c_void_p, _sz, _c_void_p]),
@@ -309,6 +312,40 @@ def pic_stitch(ctx, plans, k_pool, v_pool, k_cache, v_cache, block_tables, recom
                            _ptr(recompute_idx), _ptr(recompute_indptr), cap, _ptr(workspace),
                            workspace.numel() * workspace.element_size() if workspace is not None else 0,
                            _stream_handle(stream))
+    _check(st, ctx)
+
+
+def pic_stitch_noalloc(ctx, plans, k_pool, v_pool, k_cache, v_cache, block_tables, recompute_idx=None,
+                       recompute_indptr=None, status=None, stream=None):
+    """pic_stitch for callers that cannot allocate device memory: same
+    arguments minus the workspace (the library's own fixed 4 MiB device
+    scratch is used; see include/pic.h).  ``status``: optional CUDA uint32
+    tensor that receives this launch's device status word."""
+    arr = _plan_array(plans)
+    _check_device_int32(block_tables, "block_tables")
+    if block_tables.dim() != 2 or (len(plans) > 0 and block_tables.shape[0] < len(plans)):
+        raise ValueError("block_tables must be [n_req][max_blocks] with a row per plan")
+    if recompute_indptr is not None:
+        _check_device_int32(recompute_indptr, "recompute_indptr")
+        _check_device_int32(recompute_idx, "recompute_idx")
+        if recompute_indptr.numel() < len(plans) + 1:
+            raise ValueError("recompute_indptr needs n_req + 1 entries")
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if t is not None and (not t.is_cuda or not _is_bf16(t) or not _rows_contiguous(t)):
+            raise ValueError(f"{name} must be a CUDA bf16 tensor with contiguous rows")
+    if status is not None and (not status.is_cuda or status.element_size() != 4 or status.numel() < 1):
+        raise ValueError("status must be a CUDA tensor of at least one 32-bit element")
+    pool_ls = _layer_stride_bytes(k_pool)
+    cache_ls = _layer_stride_bytes(k_cache)
+    if v_pool is not None and _layer_stride_bytes(v_pool) != pool_ls:
+        raise ValueError("k_pool and v_pool must share a layer stride")
+    if v_cache is not None and _layer_stride_bytes(v_cache) != cache_ls:
+        raise ValueError("k_cache and v_cache must share a layer stride")
+    cap = recompute_idx.numel() if recompute_idx is not None else 0
+    st = load().pic_stitch_noalloc(ctx, arr, len(plans), _ptr(k_pool), _ptr(v_pool), pool_ls,
+                                   _ptr(k_cache), _ptr(v_cache), cache_ls, _ptr(block_tables),
+                                   int(block_tables.shape[1]), _ptr(recompute_idx), _ptr(recompute_indptr),
+                                   cap, _ptr(status), _stream_handle(stream))
     _check(st, ctx)
 
 

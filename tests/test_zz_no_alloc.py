@@ -1,0 +1,104 @@
+"""pic_stitch_noalloc against pic_stitch, through the C ABI.
+
+pic_stitch_noalloc serves callers that may not allocate device memory where
+they stitch (an engine whose KV-cache pool already owns the HBM, a plugin
+that only receives its input and output tensors, a loop that cannot afford
+cudaMalloc/cudaFree).  It runs the same kernel with the library's own fixed
+device scratch instead of a caller workspace, so its output must match
+pic_stitch's on the same inputs -- checked here on two calls in a row with
+different batches, so the second call also shows that leftovers from the
+first call in the shared scratch do not leak into its result.
+
+This file is named to be collected last: a failure here leaves every other
+test already run.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_util import REL, ABS, bits, f64, sentinel_like
+from position_independent_kv_stitch_gb300 import pic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _setup(wl, bs_blocks_extra=0):
+    m = wl.model
+    bs = m.block_size
+    nb = sum(-(-t // bs) for t in wl.request_tokens) + bs_blocks_extra
+    mb = max(-(-t // bs) for t in wl.request_tokens)
+    ctx = pic.create_from_spec(pic.model_spec_from(m), nb)
+    ids = [pic.pic_register_chunk(ctx, W.chunk_key(wl.name, c), off, n)[0]
+           for c, (off, n) in enumerate(zip(wl.pool_offsets, wl.chunk_lens))]
+    plans, tables = [], []
+    for req in wl.requests:
+        plan, bt = pic.pic_build_block_table(ctx, [ids[c] for c, _ in req], mb, take_tokens=[t for _, t in req],
+                                             k_nonleading=wl.k_nonleading, k_leading=wl.k_leading)
+        plans.append(plan)
+        tables.append(bt)
+    k_pool = W.make_pool(wl, "k", device="cpu").to(DEV)
+    v_pool = W.make_pool(wl, "v", device="cpu").to(DEV) if m.kind == "gqa" else None
+    return ctx, m, nb, plans, torch.from_numpy(np.stack(tables)).to(DEV), k_pool, v_pool
+
+
+def _outputs(m, nb, n_req, n_rec):
+    shape = (m.num_layers, nb, m.block_size) + tuple(m.row_shape)
+    k = sentinel_like(shape, DEV)
+    v = sentinel_like(shape, DEV) if m.kind == "gqa" else None
+    ridx = torch.full((max(1, n_rec),), -7, dtype=torch.int32, device=DEV)
+    indptr = torch.full((n_req + 1,), -7, dtype=torch.int32, device=DEV)
+    return k, v, ridx, indptr
+
+
+def _compare(wl):
+    ctx, m, nb, plans, d_bt, k_pool, v_pool = _setup(wl)
+    try:
+        n_rec = len(pic.pic_recompute_indices(plans)[1])
+        ka, va, ia, pa = _outputs(m, nb, len(plans), n_rec)
+        ws = torch.empty(pic.pic_workspace_bytes(ctx, plans), dtype=torch.uint8, device=DEV)
+        pic.pic_stitch(ctx, plans, k_pool, v_pool, ka, va, d_bt, ia, pa, ws)
+        assert pic.pic_query_device_status(ctx, ws) == 0
+
+        kb, vb, ib, pb = _outputs(m, nb, len(plans), n_rec)
+        status = torch.full((1,), 77, dtype=torch.int32, device=DEV)
+        pic.pic_stitch_noalloc(ctx, plans, k_pool, v_pool, kb, vb, d_bt, ib, pb, status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+
+        want, got = f64(ka), f64(kb)
+        written = ~np.isnan(want)
+        assert np.array_equal(written, ~np.isnan(got))
+        err = np.abs(got[written] - want[written])
+        assert np.all(err <= REL * np.abs(want[written]) + ABS)
+        if va is not None:
+            assert np.array_equal(bits(va), bits(vb))
+        assert torch.equal(ia, ib) and torch.equal(pa, pb)
+    finally:
+        pic.pic_destroy(ctx)
+
+
+def test_noalloc_matches_pic_stitch_two_calls_in_a_row():
+    # call 1: the tiny GQA request; call 2: a two-request ragged MLA batch
+    _compare(W.tiny_gqa())
+    base = W.deepseek_v3_mla(context_tokens=700, num_layers=2)
+    reqs = [base.requests[0], list(reversed(base.requests[0][5:40]))]
+    _compare(W.Workload("noalloc-mla", base.model, base.chunk_lens, reqs, 4, 32))
+
+
+def test_noalloc_rejects_batch_beyond_scratch():
+    m = W.Model("big", "gqa", 1, 1, 64, 64, 0, "neox", 1e4, 1)
+    ctx = pic.create_from_spec(pic.model_spec_from(m), 200000)
+    try:
+        pic.pic_register_chunk(ctx, W.chunk_key("big", 0), 0, 150000)
+        plan, bt = pic.pic_build_block_table(ctx, [0], 150000)   # 150,000 one-token runs > 4 MiB
+        d_bt = torch.from_numpy(bt).to(DEV).view(1, -1)
+        pool = torch.zeros((1, 16, 1, 64), dtype=torch.bfloat16, device=DEV)
+        with pytest.raises(pic.PicError) as e:
+            pic.pic_stitch_noalloc(ctx, [plan], pool, pool, pool, pool, d_bt)
+        assert e.value.status_name == "PIC_ERR_CAPACITY"
+        assert "static scratch" in str(e.value)
+    finally:
+        pic.pic_destroy(ctx)
