@@ -418,6 +418,7 @@ def main():
     import torch
     import torch.distributed as dist
     from position_independent_kv_stitch_gb300 import pic
+    from position_independent_kv_stitch_gb300.sharding import max_over_ranks
     pic.load()  # fails loudly when libpic is not built
     if world > 1:
         dist.init_process_group("nccl")
@@ -450,10 +451,7 @@ def main():
     rig.check_status()
     ms = t0.elapsed_time(t1) / args.steps
     kms = statistics.mean(a.elapsed_time(b) for a, b in kev)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dev)
 
     tl = wl.token_layers
     bpt = bytes_per_token_layer(wl.model, args.mode)
@@ -466,10 +464,7 @@ def main():
     e2e = None
     if not args.no_e2e and args.mode == "stitch":
         ems, h2d, d2h = run_e2e(rig, max(3, min(args.steps, 10)), 3)
-        if world > 1:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = max_over_ranks(ems, dev)
         e2e = {"value": world * algo_bytes / (ems * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ems}
 
