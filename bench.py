@@ -62,10 +62,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("pic_kernels.cu", "pic_kernels_tma.cu", "pic_host.cpp", "pic_internal.h")
+
+
 def kernel_source_hash():
+    """Hash of the kernel and launch-schedule sources a traffic record was taken on."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "position_independent_kv_stitch_gb300", "csrc", "pic_kernels.cu"), "rb") as f:
-        h.update(f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "position_independent_kv_stitch_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -472,8 +477,13 @@ def main():
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl)
 
-    kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
-             "inplace": "k_rotate_rows<in place>"}[args.mode]
+    bulk = pic.pic_kernel_variant(rig.ctx, 0 if args.mode == "stitch" else 1) == pic.PIC_VARIANT_BULK_PIPELINE
+    if bulk:
+        kname = "k_tma_pipeline<" + ("stitch K+V" if wl.model.kind == "gqa" else "stitch MLA rows") \
+            + ">" if args.mode == "stitch" else "k_tma_pipeline<in place>"
+    else:
+        kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
+                 "inplace": "k_rotate_rows<in place>"}[args.mode]
     line = {
         "metric": "stitched KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

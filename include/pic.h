@@ -30,7 +30,8 @@
  *     failures are PIC_ERR_CUDA.  Errors a kernel finds on the device (a
  *     block-table entry outside the cache) skip the faulty write and raise a
  *     status word in the workspace, read by pic_query_device_status().
- *     Kernels never trap and never wait on anything, so they cannot hang.
+ *     Kernels never trap; their only waits (for their own bulk copies) are
+ *     bounded and raise PIC_DEV_TIMEOUT instead of hanging.
  *   - Layouts (bf16 elements, row = one token of one layer):
  *       GQA key/value row: [num_kv_heads][head_dim], RoPE over all of head_dim.
  *       MLA row: [latent_dim + rope_dim] with the rope key last ([Irminsul]
@@ -80,6 +81,7 @@ enum { PIC_SCALING_NONE = 0, PIC_SCALING_LLAMA3 = 1 };
 
 /* Device status word bits (pic_query_device_status). */
 #define PIC_DEV_BAD_BLOCK 0x1u /* a block-table entry was < 0 or >= num_cache_blocks */
+#define PIC_DEV_TIMEOUT 0x2u   /* a bounded wait inside a kernel gave up (never expected) */
 
 /*
  * Model geometry and RoPE settings.
@@ -349,6 +351,18 @@ pic_status pic_recompute_indices(const pic_plan* const* plans, int32_t n_req, in
  */
 pic_status pic_query_device_status(pic_ctx* ctx, const void* d_workspace, pic_stream_t stream,
                                    uint32_t* status_out);
+
+/*
+ * Which kernel a context launches for mode 0 (pic_stitch / pic_stitch_noalloc)
+ * or mode 1 (pic_rerotate_inplace): PIC_VARIANT_REGISTERS (16-byte vector
+ * loads and stores through registers) or PIC_VARIANT_BULK_PIPELINE (bulk
+ * async copies through a shared-memory ring).  The bulk pipeline is used when
+ * one work unit fits a stage, unless the environment variable PIC_KERNEL was
+ * "regs" at pic_create.  Both compute the same result.  -1 on bad arguments.
+ */
+#define PIC_VARIANT_REGISTERS 0
+#define PIC_VARIANT_BULK_PIPELINE 1
+int32_t pic_kernel_variant(const pic_ctx* ctx, int32_t mode);
 
 /*
  * The cos/sin the kernels use, for testing the angle arithmetic: for each of

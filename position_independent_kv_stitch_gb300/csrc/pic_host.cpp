@@ -12,6 +12,7 @@
 
 #include <algorithm>
 #include <cstdarg>
+#include <cstdlib>
 #include <array>
 #include <cmath>
 #include <cstdio>
@@ -147,6 +148,13 @@ struct pic_ctx {
   BlockAllocator alloc;
   std::set<pic_plan*> plans;
   std::string err;
+  // Kernel variant per mode: the bulk-copy pipeline when a unit fits a
+  // shared-memory stage, the register kernel otherwise (or when
+  // PIC_KERNEL=regs is set in the environment at pic_create).
+  bool tma_stitch = false;
+  bool tma_inplace = false;
+  pic::TmaConfig tma_stitch_cfg{};
+  pic::TmaConfig tma_inplace_cfg{};
   StagingSlot staging[kStagingSlots];
   int staging_next = 0;
   int staging_device = -1;
@@ -198,15 +206,16 @@ bool plan_valid(const pic_ctx* ctx, const pic_plan* p) {
   return p != nullptr && ctx->plans.count(const_cast<pic_plan*>(p)) != 0;
 }
 
-// Splits one token range of a request into runs that stay inside one block.
+// Splits one token range of a request into runs that stay inside one block
+// and hold at most `cap` tokens.
 void append_runs(std::vector<RunDesc>& runs, int64_t src_tok, int32_t dst_pos, int32_t n,
-                 int32_t req, int32_t delta, int32_t bs, int32_t idx_off, int32_t idx_count) {
+                 int32_t req, int32_t delta, int32_t bs, int32_t cap, int32_t idx_off, int32_t idx_count) {
   int32_t t = 0;
   bool first = true;
   while (t < n) {
     const int32_t pos = dst_pos + t;
     const int32_t row = pos % bs;
-    const int32_t cnt = std::min(bs - row, n - t);
+    const int32_t cnt = std::min(std::min(bs - row, n - t), cap);
     RunDesc r;
     r.src_tok = static_cast<int32_t>(src_tok + t);
     r.dst_pos = pos;
@@ -220,6 +229,16 @@ void append_runs(std::vector<RunDesc>& runs, int64_t src_tok, int32_t dst_pos, i
     first = false;
     t += cnt;
   }
+}
+
+int64_t runs_in_range(int32_t dst_pos, int32_t n, int32_t bs, int32_t cap) {
+  int64_t runs = 0;
+  for (int32_t t = 0; t < n;) {
+    const int32_t pos = dst_pos + t;
+    t += std::min(std::min(bs - pos % bs, n - t), cap);
+    ++runs;
+  }
+  return runs;
 }
 
 // Layers per unit: enough units per resident CTA (~16) for an even finish,
@@ -246,25 +265,210 @@ WsLayout ws_layout(size_t half, size_t n_indptr, size_t n_runs) {
   return w;
 }
 
-size_t count_stitch_runs(const pic_plan* const* plans, int32_t n_req, int32_t bs) {
+int32_t stitch_cap(const pic_ctx* ctx) {
+  return ctx->tma_stitch ? ctx->tma_stitch_cfg.tile_tokens : ctx->model.block_size;
+}
+int32_t inplace_cap(const pic_ctx* ctx) {
+  return ctx->tma_inplace ? ctx->tma_inplace_cfg.tile_tokens : ctx->model.block_size;
+}
+
+size_t count_stitch_runs(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req) {
+  const int32_t bs = ctx->model.block_size, cap = stitch_cap(ctx);
   size_t n = 0;
-  for (int32_t r = 0; r < n_req; ++r) {
-    for (const Segment& s : plans[r]->segs) {
-      if (s.num_tokens <= 0) continue;
-      const int32_t first_row = s.dst_pos % bs;
-      n += static_cast<size_t>((first_row + s.num_tokens + bs - 1) / bs);
-    }
-  }
+  for (int32_t r = 0; r < n_req; ++r)
+    for (const Segment& s : plans[r]->segs)
+      if (s.num_tokens > 0) n += static_cast<size_t>(runs_in_range(s.dst_pos, s.num_tokens, bs, cap));
   return n;
 }
 
-size_t count_shift_runs(const pic_shift_seg* segs, int32_t n, int32_t bs) {
+size_t count_shift_runs(const pic_ctx* ctx, const pic_shift_seg* segs, int32_t n) {
+  const int32_t bs = ctx->model.block_size, cap = inplace_cap(ctx);
   size_t runs = 0;
   for (int32_t i = 0; i < n; ++i) {
     if (segs[i].num_tokens <= 0 || segs[i].delta == 0 || segs[i].start_pos < 0) continue;
-    runs += static_cast<size_t>((segs[i].start_pos % bs + segs[i].num_tokens + bs - 1) / bs);
+    runs += static_cast<size_t>(runs_in_range(segs[i].start_pos, segs[i].num_tokens, bs, cap));
   }
   return runs;
+}
+
+// Writes the stitch workspace image (frequencies, CSR offsets, runs) into a
+// zeroed host buffer laid out as `w`, with no allocation.
+void build_stitch_image(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, uint8_t* image,
+                        const WsLayout& w) {
+  const int32_t bs = ctx->model.block_size, cap = stitch_cap(ctx);
+  std::memcpy(image + w.freq_off, ctx->freq_turns.data(), ctx->freq_turns.size() * sizeof(float2));
+  int32_t* indptr = reinterpret_cast<int32_t*>(image + w.indptr_off);
+  RunDesc* out = reinterpret_cast<RunDesc*>(image + w.runs_off);
+  size_t k = 0;
+  int64_t idx = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    indptr[r] = static_cast<int32_t>(idx);
+    for (const Segment& sg : plans[r]->segs) {
+      for (int32_t t = 0; t < sg.num_tokens;) {
+        const int32_t pos = sg.dst_pos + t;
+        const int32_t cnt = std::min(std::min(bs - pos % bs, sg.num_tokens - t), cap);
+        RunDesc& rd = out[k++];
+        rd.src_tok = static_cast<int32_t>(sg.src_tok + t);
+        rd.dst_pos = pos;
+        rd.req = r;
+        rd.ntok = cnt;
+        rd.delta = sg.delta;
+        rd.idx_off = static_cast<int32_t>(idx);
+        rd.idx_count = t == 0 ? sg.n_recompute : 0;
+        rd.idx_start = sg.dst_pos;
+        t += cnt;
+      }
+      idx += sg.n_recompute;
+    }
+  }
+  indptr[n_req] = static_cast<int32_t>(idx);
+}
+
+void set_geometry(const pic_ctx* ctx, pic::KernelParams& p) {
+  const pic_model_desc& m = ctx->model;
+  p.num_layers = m.num_layers;
+  p.num_cache_blocks = ctx->num_cache_blocks;
+  p.block_size = m.block_size;
+  p.row_bytes = static_cast<int32_t>(row_bytes_of(m));
+  if (m.kind == PIC_KIND_GQA) {
+    p.heads_per_token = m.num_kv_heads;
+    p.head_stride = m.head_dim * 2;
+    p.rope_off_bytes = 0;
+  } else {
+    p.heads_per_token = 1;
+    p.head_stride = p.row_bytes;
+    p.rope_off_bytes = m.rope_offset * 2;
+  }
+}
+
+// Schedules, measured on GB300 with all five workloads (the choices with the
+// highest sustained HBM throughput):
+//  * register kernels: CTAs stride over units of 2 layers, runs fastest, so
+//    CTAs running together stream neighbouring memory; about 64 KB of loads
+//    in flight per SM is best -- 1 CTA/SM for the stitch (K and V in flight),
+//    2 CTAs/SM for the in-place shift (K only);
+//  * bulk pipeline: strided units of 2 layers for GQA stitches, 4 for GQA
+//    shifts; contiguous units of 4 layers for MLA rows, whose short tiles
+//    need the producer's run lookup reused across a run's layers.
+constexpr int kRegsLayersPerUnit = 2;
+
+void set_layer_groups(pic::KernelParams& p, int32_t L, int lg) {
+  p.lg_size = std::max(1, std::min<int32_t>(lg, L));
+  p.n_lgroups = (L + p.lg_size - 1) / p.lg_size;
+}
+
+int grid_for(const pic::KernelParams& p, int64_t resident) {
+  const int64_t units = static_cast<int64_t>(p.n_runs) * p.n_lgroups;
+  // at least one CTA so the CSR offsets are always written
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
+}
+
+// Picks the kernel for a stitch and launches it on stream s.
+cudaError_t launch_stitch_kernel(const pic_ctx* ctx, pic::KernelParams& p, int sm_count, cudaStream_t s) {
+  const pic_model_desc& m = ctx->model;
+  const bool gqa = m.kind == PIC_KIND_GQA;
+  if (ctx->tma_stitch) {
+    // one CTA per SM (the stages take most of shared memory)
+    set_layer_groups(p, m.num_layers, gqa ? 2 : 4);
+    p.contiguous = gqa ? 0 : 1;
+    return pic::launch_tma(p, ctx->tma_stitch_cfg, gqa ? 0 : 1, m.pairing, m.rope_dim, grid_for(p, sm_count), s);
+  }
+  if (gqa) {
+    set_layer_groups(p, m.num_layers, kRegsLayersPerUnit);
+    p.contiguous = 0;
+    const int cps = std::min(1, pic::occupancy_stitch_gqa(m.pairing, m.head_dim));
+    return pic::launch_stitch_gqa(p, m.pairing, m.head_dim, grid_for(p, static_cast<int64_t>(sm_count) * cps), s);
+  }
+  const int64_t resident = static_cast<int64_t>(sm_count) * pic::occupancy_stitch_mla(m.pairing);
+  choose_layer_groups(static_cast<int64_t>(p.n_runs), m.num_layers, resident, p.lg_size, p.n_lgroups);
+  return pic::launch_stitch_mla(p, m.pairing, grid_for(p, resident), s);
+}
+
+cudaError_t launch_shift_kernel(const pic_ctx* ctx, pic::KernelParams& p, int sm_count, cudaStream_t s) {
+  const pic_model_desc& m = ctx->model;
+  if (ctx->tma_inplace) {
+    set_layer_groups(p, m.num_layers, 4);
+    p.contiguous = 0;
+    return pic::launch_tma(p, ctx->tma_inplace_cfg, 2, m.pairing, m.rope_dim, grid_for(p, sm_count), s);
+  }
+  set_layer_groups(p, m.num_layers, kRegsLayersPerUnit);
+  p.contiguous = 0;
+  const int cps = std::min(2, pic::occupancy_rerotate(m.pairing, m.rope_dim));
+  return pic::launch_rerotate(p, m.pairing, m.rope_dim, grid_for(p, static_cast<int64_t>(sm_count) * cps), s);
+}
+
+// Chooses the bulk-copy pipeline shape for units of `tensors` row tiles, or
+// returns false when the register kernel should be used.
+bool tma_config_for(int64_t row_bytes, int32_t block_size, int tensors, int64_t tile_bytes, pic::TmaConfig& c) {
+  int64_t tile = std::max<int64_t>(1, tile_bytes / row_bytes);
+  tile = std::min<int64_t>(tile, block_size);
+  const int64_t per_tensor = static_cast<int64_t>(pic::align_up(static_cast<size_t>(tile * row_bytes), 128));
+  const int64_t stage = per_tensor * tensors;
+  const int64_t stages = std::min<int64_t>(pic::kTmaMaxStages, static_cast<int64_t>(pic::kTmaStageBudget) / stage);
+  if (stages < 2) return false;
+  c.stages = static_cast<int32_t>(stages);
+  c.stage_bytes = static_cast<int32_t>(stage);
+  c.tile_tokens = static_cast<int32_t>(tile);
+  return true;
+}
+
+// Argument checks shared by pic_stitch and the scratch-backed stitch.
+pic_status check_stitch_args(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                             const void* k_pool, const void* v_pool, int64_t pool_ls,
+                             const void* k_cache, const void* v_cache, int64_t cache_ls,
+                             const int32_t* d_bt, int32_t max_blocks, const int32_t* d_ridx,
+                             const int32_t* d_indptr, int64_t recompute_capacity) {
+  const pic_model_desc& m = ctx->model;
+  if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
+  for (int32_t r = 0; r < n_req; ++r) {
+    if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
+    if (static_cast<int32_t>(plans[r]->blocks.size()) > max_blocks)
+      return fail(ctx, PIC_ERR_CAPACITY, "plans[%d] has %zu blocks, block-table rows hold %d", r,
+                  plans[r]->blocks.size(), max_blocks);
+  }
+  const bool gqa = m.kind == PIC_KIND_GQA;
+  if (!k_pool || !k_cache || !d_bt) return fail(ctx, PIC_ERR_INVALID_ARG, "null pool, cache or block table");
+  if (gqa && (!v_pool || !v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs v_pool and v_cache");
+  if (!gqa && (v_pool || v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
+  if ((d_ridx == nullptr) != (d_indptr == nullptr))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "pass both recompute outputs or neither");
+  if (!vectorized_bytes_ok(k_pool) || !vectorized_bytes_ok(k_cache) ||
+      (gqa && (!vectorized_bytes_ok(v_pool) || !vectorized_bytes_ok(v_cache))) || (pool_ls & 15) || (cache_ls & 15))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "pools, caches and layer strides must be 16-byte aligned");
+  const int64_t row_bytes = row_bytes_of(m);
+  if (pool_ls < 0 || cache_ls < 0 || (m.num_layers > 1 && (pool_ls == 0 || cache_ls == 0)))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "bad layer strides");
+  if (m.num_layers > 1 && cache_ls < static_cast<int64_t>(ctx->num_cache_blocks) * m.block_size * row_bytes)
+    return fail(ctx, PIC_ERR_RANGE, "cache layer stride smaller than num_cache_blocks * block_size rows");
+  int64_t n_rec = 0;
+  for (int32_t r = 0; r < n_req; ++r) n_rec += plans[r]->n_recompute;
+  if (d_ridx && n_rec > recompute_capacity)
+    return fail(ctx, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
+                static_cast<long long>(n_rec), static_cast<long long>(recompute_capacity));
+  return PIC_OK;
+}
+
+void fill_stitch_params(const pic_ctx* ctx, pic::KernelParams& p, uint8_t* ws, const WsLayout& w, size_t n_runs,
+                        int32_t n_req, const void* k_pool, const void* v_pool, int64_t pool_ls, void* k_cache,
+                        void* v_cache, int64_t cache_ls, const int32_t* d_bt, int32_t max_blocks, int32_t* d_ridx,
+                        int32_t* d_indptr) {
+  set_geometry(ctx, p);
+  p.runs = reinterpret_cast<const RunDesc*>(ws + w.runs_off);
+  p.n_runs = static_cast<int32_t>(n_runs);
+  p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
+  p.k_src = static_cast<const uint8_t*>(k_pool);
+  p.v_src = static_cast<const uint8_t*>(v_pool);
+  p.src_layer_stride = pool_ls;
+  p.k_dst = static_cast<uint8_t*>(k_cache);
+  p.v_dst = static_cast<uint8_t*>(v_cache);
+  p.dst_layer_stride = cache_ls;
+  p.block_tables = d_bt;
+  p.max_blocks = max_blocks;
+  p.ridx = d_ridx;
+  p.indptr_src = reinterpret_cast<const int32_t*>(ws + w.indptr_off);
+  p.indptr_dst = d_indptr;
+  p.n_indptr = n_req + 1;
+  p.header = reinterpret_cast<WsHeader*>(ws);
 }
 
 void release_staging(pic_ctx* ctx) {
@@ -409,6 +613,25 @@ pic_status pic_create(const pic_model_desc* m, int32_t num_cache_blocks, pic_ctx
   pic_ctx* ctx = new (std::nothrow) pic_ctx(num_cache_blocks);
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "out of host memory");
   ctx->model = *m;
+  {
+    // Default: the bulk-copy pipeline for MLA rows (it keeps the 512-d latent
+    // out of registers and wins there), the register kernel for GQA rows
+    // (faster there).  PIC_KERNEL=regs or =bulk forces one variant.
+    const char* kv = std::getenv("PIC_KERNEL");
+    const bool regs_only = kv && std::strcmp(kv, "regs") == 0;
+    const bool bulk_all = kv && std::strcmp(kv, "bulk") == 0;
+    const int64_t tile_bytes = pic::kTmaTileBytesPerTensor;
+    const int64_t row = row_bytes_of(*m);
+    if (!regs_only && (bulk_all || m->kind == PIC_KIND_MLA)) {
+      ctx->tma_stitch = tma_config_for(row, m->block_size, m->kind == PIC_KIND_GQA ? 2 : 1, tile_bytes,
+                                       ctx->tma_stitch_cfg);
+    }
+    // An MLA shift touches only the 64-d rope slice of each row: the register
+    // kernel reads just those bytes, whole-row copies would move 9x more.
+    if (bulk_all && m->kind == PIC_KIND_GQA) {
+      ctx->tma_inplace = tma_config_for(row, m->block_size, 1, tile_bytes, ctx->tma_inplace_cfg);
+    }
+  }
   ctx->model.inv_freq = nullptr;
   ctx->theta = theta;
   ctx->freq_turns.resize(half);
@@ -633,7 +856,7 @@ size_t pic_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int
   if (!ctx || n_req < 0 || (n_req > 0 && !plans)) return 0;
   for (int32_t r = 0; r < n_req; ++r)
     if (!plans[r]) return 0;
-  const size_t runs = count_stitch_runs(plans, n_req, ctx->model.block_size);
+  const size_t runs = count_stitch_runs(ctx, plans, n_req);
   return ws_layout(ctx->freq_turns.size(), static_cast<size_t>(n_req) + 1, runs).total;
 }
 
@@ -643,116 +866,33 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
                       int32_t* d_ridx, int32_t* d_indptr, int64_t recompute_capacity,
                       void* d_ws, size_t ws_bytes, pic_stream_t stream) {
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
-  const pic_model_desc& m = ctx->model;
-  if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
-  for (int32_t r = 0; r < n_req; ++r) {
-    if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
-    if (static_cast<int32_t>(plans[r]->blocks.size()) > max_blocks)
-      return fail(ctx, PIC_ERR_CAPACITY, "plans[%d] has %zu blocks, block-table rows hold %d", r,
-                  plans[r]->blocks.size(), max_blocks);
-  }
-  const bool gqa = m.kind == PIC_KIND_GQA;
-  if (!k_pool || !k_cache || !d_bt || !d_ws)
-    return fail(ctx, PIC_ERR_INVALID_ARG, "null pool, cache, block table or workspace");
-  if (gqa && (!v_pool || !v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs v_pool and v_cache");
-  if (!gqa && (v_pool || v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
-  if ((d_ridx == nullptr) != (d_indptr == nullptr))
-    return fail(ctx, PIC_ERR_INVALID_ARG, "pass both recompute outputs or neither");
-  if (!vectorized_bytes_ok(k_pool) || !vectorized_bytes_ok(k_cache) || (gqa && (!vectorized_bytes_ok(v_pool) || !vectorized_bytes_ok(v_cache))) ||
-      (pool_ls & 15) || (cache_ls & 15) || !vectorized_bytes_ok(d_ws))
-    return fail(ctx, PIC_ERR_ALIGNMENT, "pools, caches, layer strides and workspace must be 16-byte aligned");
-  const int64_t row_bytes = row_bytes_of(m);
-  if (pool_ls < 0 || cache_ls < 0 || (m.num_layers > 1 && (pool_ls == 0 || cache_ls == 0)))
-    return fail(ctx, PIC_ERR_INVALID_ARG, "bad layer strides");
-  if (m.num_layers > 1 && cache_ls < static_cast<int64_t>(ctx->num_cache_blocks) * m.block_size * row_bytes)
-    return fail(ctx, PIC_ERR_RANGE, "cache layer stride smaller than num_cache_blocks * block_size rows");
-
-  int64_t n_rec = 0;
-  for (int32_t r = 0; r < n_req; ++r) n_rec += plans[r]->n_recompute;
-  if (d_ridx && n_rec > recompute_capacity)
-    return fail(ctx, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
-                static_cast<long long>(n_rec), static_cast<long long>(recompute_capacity));
-
-  const int32_t bs = m.block_size;
-  const size_t n_runs = count_stitch_runs(plans, n_req, bs);
-  const size_t half = ctx->freq_turns.size();
-  const WsLayout w = ws_layout(half, static_cast<size_t>(n_req) + 1, n_runs);
+  pic_status st = check_stitch_args(ctx, plans, n_req, k_pool, v_pool, pool_ls, k_cache, v_cache, cache_ls,
+                                    d_bt, max_blocks, d_ridx, d_indptr, recompute_capacity);
+  if (st != PIC_OK) return st;
+  if (!d_ws) return fail(ctx, PIC_ERR_INVALID_ARG, "null workspace");
+  if (!vectorized_bytes_ok(d_ws)) return fail(ctx, PIC_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  const size_t n_runs = count_stitch_runs(ctx, plans, n_req);
+  const WsLayout w = ws_layout(ctx->freq_turns.size(), static_cast<size_t>(n_req) + 1, n_runs);
   if (ws_bytes < w.total)
     return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
   if (n_runs > static_cast<size_t>(std::numeric_limits<int32_t>::max()))
     return fail(ctx, PIC_ERR_RANGE, "too many runs");
 
   DeviceInfo di;
-  pic_status st = current_device(ctx, di);
+  st = current_device(ctx, di);
   if (st != PIC_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   StagingSlot* sl = nullptr;
   st = acquire_staging(ctx, di.device, w.total, &sl);
   if (st != PIC_OK) return st;
-
-  // Workspace image: zeroed header, frequencies, CSR offsets, runs.
-  uint8_t* base = sl->host;
-  fill_freq(ctx, base, w);
-  int32_t* indptr = reinterpret_cast<int32_t*>(base + w.indptr_off);
-  std::vector<RunDesc> runs;
-  runs.reserve(n_runs);
-  int64_t idx = 0;
-  for (int32_t r = 0; r < n_req; ++r) {
-    indptr[r] = static_cast<int32_t>(idx);
-    for (const Segment& sg : plans[r]->segs) {
-      if (sg.num_tokens > 0)
-        append_runs(runs, sg.src_tok, sg.dst_pos, sg.num_tokens, r, sg.delta, bs,
-                    static_cast<int32_t>(idx), sg.n_recompute);
-      idx += sg.n_recompute;
-    }
-  }
-  indptr[n_req] = static_cast<int32_t>(idx);
-  std::memcpy(base + w.runs_off, runs.data(), runs.size() * sizeof(RunDesc));
+  build_stitch_image(ctx, plans, n_req, sl->host, w);
   st = upload_staging(ctx, sl, d_ws, w.total, s);
   if (st != PIC_OK) return st;
-  cudaError_t e;
 
-  uint8_t* ws = static_cast<uint8_t*>(d_ws);
   pic::KernelParams p{};
-  p.runs = reinterpret_cast<const RunDesc*>(ws + w.runs_off);
-  p.n_runs = static_cast<int32_t>(n_runs);
-  p.num_layers = m.num_layers;
-  p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
-  p.k_src = static_cast<const uint8_t*>(k_pool);
-  p.v_src = static_cast<const uint8_t*>(v_pool);
-  p.src_layer_stride = pool_ls;
-  p.k_dst = static_cast<uint8_t*>(k_cache);
-  p.v_dst = static_cast<uint8_t*>(v_cache);
-  p.dst_layer_stride = cache_ls;
-  p.block_tables = d_bt;
-  p.max_blocks = max_blocks;
-  p.num_cache_blocks = ctx->num_cache_blocks;
-  p.block_size = bs;
-  p.row_bytes = static_cast<int32_t>(row_bytes);
-  p.ridx = d_ridx;
-  p.indptr_src = reinterpret_cast<const int32_t*>(ws + w.indptr_off);
-  p.indptr_dst = d_indptr;
-  p.n_indptr = n_req + 1;
-  p.header = reinterpret_cast<WsHeader*>(ws);
-
-  const int occ = gqa ? pic::occupancy_stitch_gqa(m.pairing, m.head_dim) : pic::occupancy_stitch_mla(m.pairing);
-  const int64_t resident = static_cast<int64_t>(di.sm_count) * occ;
-  choose_layer_groups(static_cast<int64_t>(n_runs), m.num_layers, resident, p.lg_size, p.n_lgroups);
-  const int64_t units = static_cast<int64_t>(n_runs) * p.n_lgroups;
-  // at least one CTA so the CSR offsets are always written
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
-
-  if (gqa) {
-    p.heads_per_token = m.num_kv_heads;
-    p.head_stride = m.head_dim * 2;
-    p.rope_off_bytes = 0;
-    e = pic::launch_stitch_gqa(p, m.pairing, m.head_dim, grid, s);
-  } else {
-    p.heads_per_token = 1;
-    p.head_stride = static_cast<int32_t>(row_bytes);
-    p.rope_off_bytes = m.rope_offset * 2;
-    e = pic::launch_stitch_mla(p, m.pairing, grid, s);
-  }
+  fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_ws), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
+                     v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
+  const cudaError_t e = launch_stitch_kernel(ctx, p, di.sm_count, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
   return ok(ctx);
 }
@@ -761,7 +901,7 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
 
 size_t pic_rerotate_workspace_bytes(const pic_ctx* ctx, const pic_shift_seg* segs, int32_t n) {
   if (!ctx || n < 0 || (n > 0 && !segs)) return 0;
-  return ws_layout(ctx->freq_turns.size(), 0, count_shift_runs(segs, n, ctx->model.block_size)).total;
+  return ws_layout(ctx->freq_turns.size(), 0, count_shift_runs(ctx, segs, n)).total;
 }
 
 pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
@@ -788,7 +928,7 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
     if (g.delta > PIC_MAX_ABS_DELTA || g.delta < -PIC_MAX_ABS_DELTA)
       return fail(ctx, PIC_ERR_RANGE, "segs[%d].delta exceeds 2^24 - 1", i);
   }
-  const size_t n_runs = count_shift_runs(segs, n_segs, bs);
+  const size_t n_runs = count_shift_runs(ctx, segs, n_segs);
   const WsLayout w = ws_layout(ctx->freq_turns.size(), 0, n_runs);
   if (ws_bytes < w.total) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
   if (n_runs > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return fail(ctx, PIC_ERR_RANGE, "too many runs");
@@ -804,46 +944,29 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
   fill_freq(ctx, base, w);
   std::vector<RunDesc> runs;
   runs.reserve(n_runs);
+  const int32_t cap = inplace_cap(ctx);
   for (int32_t i = 0; i < n_segs; ++i) {
     const pic_shift_seg& g = segs[i];
     if (g.num_tokens <= 0 || g.delta == 0) continue;  // R_0 = I: nothing to do
-    append_runs(runs, 0, g.start_pos, g.num_tokens, g.req, g.delta, bs, 0, 0);
+    append_runs(runs, 0, g.start_pos, g.num_tokens, g.req, g.delta, bs, cap, 0, 0);
   }
   std::memcpy(base + w.runs_off, runs.data(), runs.size() * sizeof(RunDesc));
   st = upload_staging(ctx, sl, d_ws, w.total, s);
   if (st != PIC_OK) return st;
-  cudaError_t e;
   if (n_runs == 0) return ok(ctx);
 
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   pic::KernelParams p{};
+  set_geometry(ctx, p);
   p.runs = reinterpret_cast<const RunDesc*>(ws + w.runs_off);
   p.n_runs = static_cast<int32_t>(n_runs);
-  p.num_layers = m.num_layers;
   p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
   p.k_dst = static_cast<uint8_t*>(k_cache);
   p.dst_layer_stride = cache_ls;
   p.block_tables = d_bt;
   p.max_blocks = max_blocks;
-  p.num_cache_blocks = ctx->num_cache_blocks;
-  p.block_size = bs;
-  p.row_bytes = static_cast<int32_t>(row_bytes);
   p.header = reinterpret_cast<WsHeader*>(ws);
-  if (m.kind == PIC_KIND_GQA) {
-    p.heads_per_token = m.num_kv_heads;
-    p.head_stride = m.head_dim * 2;
-    p.rope_off_bytes = 0;
-  } else {
-    p.heads_per_token = 1;
-    p.head_stride = static_cast<int32_t>(row_bytes);
-    p.rope_off_bytes = m.rope_offset * 2;
-  }
-  const int occ = pic::occupancy_rerotate(m.pairing, m.rope_dim);
-  const int64_t resident = static_cast<int64_t>(di.sm_count) * occ;
-  choose_layer_groups(static_cast<int64_t>(n_runs), m.num_layers, resident, p.lg_size, p.n_lgroups);
-  const int64_t units = static_cast<int64_t>(n_runs) * p.n_lgroups;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
-  e = pic::launch_rerotate(p, m.pairing, m.rope_dim, grid, s);
+  const cudaError_t e = launch_shift_kernel(ctx, p, di.sm_count, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "rerotate launch");
   return ok(ctx);
 }
@@ -863,9 +986,16 @@ pic_status pic_query_device_status(pic_ctx* ctx, const void* d_ws, pic_stream_t 
   if (status_out) *status_out = h.status;
   if (h.status != 0)
     return fail(ctx, PIC_ERR_DEVICE_CHECK,
-                "kernel found a block-table entry outside the cache (status 0x%x, table row %u, position %u)",
+                "kernel reported device status 0x%x (bit 0x1: block-table entry outside the cache, table row %u, "
+                "position %u; bit 0x2: a bounded wait gave up)",
                 h.status, h.bad_req, h.bad_pos);
   return ok(ctx);
+}
+
+int32_t pic_kernel_variant(const pic_ctx* ctx, int32_t mode) {
+  if (!ctx || (mode != 0 && mode != 1)) return -1;
+  const bool bulk = mode == 0 ? ctx->tma_stitch : ctx->tma_inplace;
+  return bulk ? PIC_VARIANT_BULK_PIPELINE : PIC_VARIANT_REGISTERS;
 }
 
 pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n, float* d_out,
@@ -888,51 +1018,10 @@ pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n,
 
 // ===================================================== scratch-backed stitch
 //
-// Used only by the no-alloc entry point.  Same validation, workspace image
-// and launch as pic_stitch, but the image is written straight into a
+// Used only by the no-alloc entry point.  Same checks, workspace image and
+// launch as pic_stitch, but the image is written straight into a
 // caller-owned host buffer and uploaded with a plain (pageable) copy into a
 // caller-owned device buffer, so nothing is allocated here.
-
-namespace {
-
-pic_status check_stitch_args(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
-                             const void* k_pool, const void* v_pool, int64_t pool_ls,
-                             const void* k_cache, const void* v_cache, int64_t cache_ls,
-                             const int32_t* d_bt, int32_t max_blocks, const int32_t* d_ridx,
-                             const int32_t* d_indptr, int64_t recompute_capacity,
-                             int64_t* n_rec_out) {
-  const pic_model_desc& m = ctx->model;
-  if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
-  for (int32_t r = 0; r < n_req; ++r) {
-    if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
-    if (static_cast<int32_t>(plans[r]->blocks.size()) > max_blocks)
-      return fail(ctx, PIC_ERR_CAPACITY, "plans[%d] has %zu blocks, block-table rows hold %d", r,
-                  plans[r]->blocks.size(), max_blocks);
-  }
-  const bool gqa = m.kind == PIC_KIND_GQA;
-  if (!k_pool || !k_cache || !d_bt) return fail(ctx, PIC_ERR_INVALID_ARG, "null pool, cache or block table");
-  if (gqa && (!v_pool || !v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs v_pool and v_cache");
-  if (!gqa && (v_pool || v_cache)) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
-  if ((d_ridx == nullptr) != (d_indptr == nullptr))
-    return fail(ctx, PIC_ERR_INVALID_ARG, "pass both recompute outputs or neither");
-  if (!vectorized_bytes_ok(k_pool) || !vectorized_bytes_ok(k_cache) ||
-      (gqa && (!vectorized_bytes_ok(v_pool) || !vectorized_bytes_ok(v_cache))) || (pool_ls & 15) || (cache_ls & 15))
-    return fail(ctx, PIC_ERR_ALIGNMENT, "pools, caches and layer strides must be 16-byte aligned");
-  const int64_t row_bytes = row_bytes_of(m);
-  if (pool_ls < 0 || cache_ls < 0 || (m.num_layers > 1 && (pool_ls == 0 || cache_ls == 0)))
-    return fail(ctx, PIC_ERR_INVALID_ARG, "bad layer strides");
-  if (m.num_layers > 1 && cache_ls < static_cast<int64_t>(ctx->num_cache_blocks) * m.block_size * row_bytes)
-    return fail(ctx, PIC_ERR_RANGE, "cache layer stride smaller than num_cache_blocks * block_size rows");
-  int64_t n_rec = 0;
-  for (int32_t r = 0; r < n_req; ++r) n_rec += plans[r]->n_recompute;
-  if (d_ridx && n_rec > recompute_capacity)
-    return fail(ctx, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
-                static_cast<long long>(n_rec), static_cast<long long>(recompute_capacity));
-  *n_rec_out = n_rec;
-  return PIC_OK;
-}
-
-}  // namespace
 
 namespace pic {
 
@@ -946,13 +1035,10 @@ pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32
                                size_t scratch_bytes, uint8_t* image, size_t image_bytes,
                                uint32_t* d_status_out, cudaStream_t s) {
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
-  int64_t n_rec = 0;
   pic_status st = check_stitch_args(ctx, plans, n_req, k_pool, v_pool, pool_ls, k_cache, v_cache, cache_ls,
-                                    d_bt, max_blocks, d_ridx, d_indptr, recompute_capacity, &n_rec);
+                                    d_bt, max_blocks, d_ridx, d_indptr, recompute_capacity);
   if (st != PIC_OK) return st;
-  const pic_model_desc& m = ctx->model;
-  const int32_t bs = m.block_size;
-  const size_t n_runs = count_stitch_runs(plans, n_req, bs);
+  const size_t n_runs = count_stitch_runs(ctx, plans, n_req);
   const WsLayout w = ws_layout(ctx->freq_turns.size(), static_cast<size_t>(n_req) + 1, n_runs);
   const size_t limit = std::min(scratch_bytes, image_bytes);
   if (w.total > limit)
@@ -964,81 +1050,20 @@ pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32
   // Image: zeroed header (the status word must start at 0 on every call),
   // frequencies, CSR offsets, runs written in place.
   std::memset(image, 0, w.total);
-  fill_freq(ctx, image, w);
-  int32_t* indptr = reinterpret_cast<int32_t*>(image + w.indptr_off);
-  RunDesc* out = reinterpret_cast<RunDesc*>(image + w.runs_off);
-  size_t k = 0;
-  int64_t idx = 0;
-  for (int32_t r = 0; r < n_req; ++r) {
-    indptr[r] = static_cast<int32_t>(idx);
-    for (const Segment& sg : plans[r]->segs) {
-      for (int32_t t = 0; t < sg.num_tokens;) {
-        const int32_t pos = sg.dst_pos + t;
-        const int32_t cnt = std::min(bs - pos % bs, sg.num_tokens - t);
-        RunDesc& rd = out[k++];
-        rd.src_tok = static_cast<int32_t>(sg.src_tok + t);
-        rd.dst_pos = pos;
-        rd.req = r;
-        rd.ntok = cnt;
-        rd.delta = sg.delta;
-        rd.idx_off = static_cast<int32_t>(idx);
-        rd.idx_count = t == 0 ? sg.n_recompute : 0;
-        rd.idx_start = sg.dst_pos;
-        t += cnt;
-      }
-      idx += sg.n_recompute;
-    }
-  }
-  indptr[n_req] = static_cast<int32_t>(idx);
+  build_stitch_image(ctx, plans, n_req, image, w);
 
   DeviceInfo di;
   st = current_device(ctx, di);
   if (st != PIC_OK) return st;
   cudaError_t e = cudaMemcpyAsync(d_scratch, image, w.total, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "scratch upload");
-
-  uint8_t* ws = static_cast<uint8_t*>(d_scratch);
   KernelParams p{};
-  p.runs = reinterpret_cast<const RunDesc*>(ws + w.runs_off);
-  p.n_runs = static_cast<int32_t>(n_runs);
-  p.num_layers = m.num_layers;
-  p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
-  p.k_src = static_cast<const uint8_t*>(k_pool);
-  p.v_src = static_cast<const uint8_t*>(v_pool);
-  p.src_layer_stride = pool_ls;
-  p.k_dst = static_cast<uint8_t*>(k_cache);
-  p.v_dst = static_cast<uint8_t*>(v_cache);
-  p.dst_layer_stride = cache_ls;
-  p.block_tables = d_bt;
-  p.max_blocks = max_blocks;
-  p.num_cache_blocks = ctx->num_cache_blocks;
-  p.block_size = bs;
-  p.row_bytes = static_cast<int32_t>(row_bytes_of(m));
-  p.ridx = d_ridx;
-  p.indptr_src = reinterpret_cast<const int32_t*>(ws + w.indptr_off);
-  p.indptr_dst = d_indptr;
-  p.n_indptr = n_req + 1;
-  p.header = reinterpret_cast<WsHeader*>(ws);
-  const bool gqa = m.kind == PIC_KIND_GQA;
-  const int occ = gqa ? occupancy_stitch_gqa(m.pairing, m.head_dim) : occupancy_stitch_mla(m.pairing);
-  const int64_t resident = static_cast<int64_t>(di.sm_count) * occ;
-  choose_layer_groups(static_cast<int64_t>(n_runs), m.num_layers, resident, p.lg_size, p.n_lgroups);
-  const int64_t units = static_cast<int64_t>(n_runs) * p.n_lgroups;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
-  if (gqa) {
-    p.heads_per_token = m.num_kv_heads;
-    p.head_stride = m.head_dim * 2;
-    p.rope_off_bytes = 0;
-    e = launch_stitch_gqa(p, m.pairing, m.head_dim, grid, s);
-  } else {
-    p.heads_per_token = 1;
-    p.head_stride = p.row_bytes;
-    p.rope_off_bytes = m.rope_offset * 2;
-    e = launch_stitch_mla(p, m.pairing, grid, s);
-  }
+  fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_scratch), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
+                     v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
+  e = launch_stitch_kernel(ctx, p, di.sm_count, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
   if (d_status_out) {
-    e = cudaMemcpyAsync(d_status_out, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+    e = cudaMemcpyAsync(d_status_out, d_scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "status copy");
   }
   return ok(ctx);

@@ -45,6 +45,8 @@ struct KernelParams {
   int32_t n_runs;
   int32_t n_lgroups;        // ceil(num_layers / lg_size)
   int32_t lg_size;          // layers per work unit
+  int32_t contiguous;       // 1: CTA c owns units [c*U/G, (c+1)*U/G), layer group fastest;
+                            // 0: CTA c takes units c, c+G, ..., run fastest
   int32_t num_layers;
   const float2* freq;       // rope_dim/2 (hi, lo): theta_i / (2 pi) as a float pair
   const uint8_t* k_src;     // pool (stitch) -- unused in place
@@ -67,6 +69,21 @@ struct KernelParams {
   int32_t n_indptr;
   WsHeader* header;
 };
+
+// Shared-memory pipeline shape of the bulk-copy kernels.
+struct TmaConfig {
+  int32_t stages;       // ring depth (>= 2)
+  int32_t stage_bytes;  // bytes per stage (K tile, then V tile when present), multiple of 128
+  int32_t tile_tokens;  // most tokens one unit (run x layer) may hold
+};
+constexpr size_t kTmaStageBudget = 200 * 1024;  // shared memory given to the stages
+constexpr int kTmaMaxStages = 16;
+constexpr int kTmaTileBytesPerTensor = 32 * 1024;
+
+size_t tma_smem_bytes(const TmaConfig& c);
+// mode 0: stitch with values, 1: stitch without values (MLA), 2: in place.
+cudaError_t launch_tma(const KernelParams& p, const TmaConfig& c, int mode, int pairing, int rope_dim,
+                       int grid, cudaStream_t stream);
 
 // Launchers; each returns the launch's cudaError_t.  `grid` is the number of
 // CTAs (persistent, grid-stride over units).

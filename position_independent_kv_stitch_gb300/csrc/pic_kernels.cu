@@ -4,14 +4,16 @@
 // bytes and does 6 flops per rotated pair, so HBM bandwidth bounds it and
 // tensor cores have nothing to do.  Design:
 //   * Work unit = one run (<= block_size consecutive tokens of one chunk that
-//     land in one paged block; contiguous in both pool and cache) x one group
-//     of consecutive layers.  A persistent grid strides over the units.
+//     land in one paged block; contiguous in both pool and cache) x a group
+//     of consecutive layers.  A persistent grid strides over the units with
+//     runs fastest, so CTAs running together stream neighbouring memory and
+//     finish within one unit of each other.
 //   * Every thread owns a fixed slice of each head row (16-byte vectors), so
 //     its RoPE frequencies are fixed: the cos/sin of delta * theta_i are
-//     computed once per unit in registers and reused for every token, head
-//     and layer of the unit (one delta per chunk: EPIC Guide, "Mathematical
-//     Foundations: RoPE In-Place Key Transformation", 2. The In-Place Shift
-//     Transformation -- R_{n+dp} = R_dp R_n).
+//     computed in registers when the delta changes and reused for every
+//     token, head and layer that shares it (one delta per chunk: EPIC Guide,
+//     "Mathematical Foundations: RoPE In-Place Key Transformation", 2. The
+//     In-Place Shift Transformation -- R_{n+dp} = R_dp R_n).
 //   * Neox half-split pairs (i, i + d/2) live in two vectors d bytes apart; a
 //     thread loads both, so no shuffles are needed.  Interleaved pairs
 //     (2i, 2i+1) sit inside one vector.
@@ -132,7 +134,7 @@ __device__ __forceinline__ void emit_indptr(const KernelParams& P) {
 constexpr int kThreads = 256;
 
 template <int PAIRING, int RD, bool STITCH>
-__global__ void __launch_bounds__(kThreads) k_rotate_rows(const KernelParams P) {
+__global__ void __launch_bounds__(kThreads, 2) k_rotate_rows(const KernelParams P) {
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr int VPR = RD / 8;                    // 16-B vectors in the rope slice
   constexpr int TPR = NEOX ? VPR / 2 : VPR;      // threads per head row
@@ -147,29 +149,53 @@ __global__ void __launch_bounds__(kThreads) k_rotate_rows(const KernelParams P) 
   const int lo_off = P.rope_off_bytes + slot * 16;
   const int hi_off = lo_off + RD;                // neox partner: +RD/2 elements
 
+  // Units are run x layer group.  Either each CTA owns a contiguous range of
+  // units (layer group fastest) or CTAs stride over units (run fastest, so
+  // CTAs running at the same time touch neighbouring runs of one layer).
+  // A run's descriptor, block and cos/sin are set up once per change.
   const int64_t n_units = static_cast<int64_t>(P.n_runs) * P.n_lgroups;
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int lg = static_cast<int>(u / P.n_runs);
-    const RunDesc r = P.runs[u - static_cast<int64_t>(lg) * P.n_runs];
-    if (STITCH) emit_recompute(P, r, lg);
-    int blk, row0;
-    if (!resolve_block(P, r, blk, row0)) continue;
-
-    const bool rot = (r.delta != 0);
-    float c[NF], s[NF];
-    if (rot) {
+  const int64_t u_first = P.contiguous ? n_units * blockIdx.x / gridDim.x : blockIdx.x;
+  const int64_t u_last = P.contiguous ? n_units * (blockIdx.x + 1) / gridDim.x : n_units;
+  const int64_t u_step = P.contiguous ? 1 : gridDim.x;
+  int cur_run = -1;
+  RunDesc r{};
+  bool valid = false;
+  int64_t dst_off = 0, src_off = 0;
+  int cached_delta = 0;
+  float c[NF], s[NF];
 #pragma unroll
-      for (int k = 0; k < NF; ++k) shift_cossin(r.delta, __ldg(P.freq + f0 + k), c[k], s[k]);
+  for (int k = 0; k < NF; ++k) { c[k] = 1.0f; s[k] = 0.0f; }
+
+  for (int64_t u = u_first; u < u_last; u += u_step) {
+    int run, lg;
+    if (P.contiguous) {
+      run = static_cast<int>(u / P.n_lgroups);
+      lg = static_cast<int>(u - static_cast<int64_t>(run) * P.n_lgroups);
+    } else {
+      lg = static_cast<int>(u / P.n_runs);
+      run = static_cast<int>(u - static_cast<int64_t>(lg) * P.n_runs);
     }
-
-    const int64_t dst_off = (static_cast<int64_t>(blk) * P.block_size + row0) * P.row_bytes;
-    const int64_t src_off = STITCH ? static_cast<int64_t>(r.src_tok) * P.row_bytes : dst_off;
+    if (run != cur_run) {
+      cur_run = run;
+      r = P.runs[run];
+      int blk, row0;
+      valid = resolve_block(P, r, blk, row0);
+      dst_off = valid ? (static_cast<int64_t>(blk) * P.block_size + row0) * P.row_bytes : 0;
+      src_off = STITCH ? static_cast<int64_t>(r.src_tok) * P.row_bytes : dst_off;
+      if (r.delta != 0 && r.delta != cached_delta) {
+#pragma unroll
+        for (int k = 0; k < NF; ++k) shift_cossin(r.delta, __ldg(P.freq + f0 + k), c[k], s[k]);
+        cached_delta = r.delta;
+      }
+    }
+    if (STITCH) emit_recompute(P, r, lg);
+    if (!valid) continue;
+    const bool rot = (r.delta != 0);
     const int nh = r.ntok * P.heads_per_token;
-    const int l_begin = lg * P.lg_size;
-    const int l_end = min(P.num_layers, l_begin + P.lg_size);
-
-    for (int l = l_begin; l < l_end; ++l) {
-      const uint8_t* ks = (STITCH ? P.k_src + l * P.src_layer_stride : P.k_dst + l * P.dst_layer_stride) + src_off;
+    const int l_end = min(P.num_layers, (lg + 1) * P.lg_size);
+    for (int l = lg * P.lg_size; l < l_end; ++l) {
+      const uint8_t* ks =
+          (STITCH ? P.k_src + l * P.src_layer_stride : P.k_dst + l * P.dst_layer_stride) + src_off;
       uint8_t* kd = P.k_dst + l * P.dst_layer_stride + dst_off;
       const uint8_t* vs = STITCH ? P.v_src + l * P.src_layer_stride + src_off : nullptr;
       uint8_t* vd = STITCH ? P.v_dst + l * P.dst_layer_stride + dst_off : nullptr;

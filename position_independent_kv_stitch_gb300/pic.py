@@ -28,6 +28,8 @@ PIC_PAIRING_NEOX_HALF, PIC_PAIRING_INTERLEAVED = 0, 1
 PIC_SCALING_NONE, PIC_SCALING_LLAMA3 = 0, 1
 PIC_KEY_BYTES = 32
 PIC_DEV_BAD_BLOCK = 0x1
+PIC_DEV_TIMEOUT = 0x2
+PIC_VARIANT_REGISTERS, PIC_VARIANT_BULK_PIPELINE = 0, 1
 
 
 class PicError(RuntimeError):
@@ -92,6 +94,7 @@ _SIGNATURES = {
                                             _P(pic_shift_seg), _i32, _c_void_p, _sz, _c_void_p]),
     "pic_recompute_indices": (ctypes.c_int, [_P(_c_void_p), _i32, _P(_i32), _P(_i32), _i64, _P(_i64)]),
     "pic_query_device_status": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _P(_u32)]),
+    "pic_kernel_variant": (_i32, [_c_void_p, _i32]),
     "pic_rotation_cossin": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _sz, _c_void_p]),
 }
 
@@ -399,6 +402,11 @@ def pic_query_device_status(ctx, workspace, stream=None) -> int:
     if st != PIC_OK:
         raise PicError(st, load().pic_last_error(ctx).decode())
     return out.value
+
+
+def pic_kernel_variant(ctx, mode: int) -> int:
+    """0 = register kernel, 1 = bulk-copy pipeline; mode 0 stitch, 1 in-place shift."""
+    return int(load().pic_kernel_variant(ctx, int(mode)))
 
 
 def pic_rotation_cossin(ctx, deltas, out, workspace, stream=None):

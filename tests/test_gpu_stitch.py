@@ -26,6 +26,14 @@ def _lib():
     torch.cuda.empty_cache()
 
 
+@pytest.fixture(params=["bulk", "regs"])
+def variant(request, monkeypatch):
+    """Runs a test once per kernel variant, forced at pic_create through PIC_KERNEL
+    (the default picks the bulk pipeline for MLA rows, registers for GQA rows)."""
+    monkeypatch.setenv("PIC_KERNEL", request.param)
+    return request.param
+
+
 def _pairs_close(got, want, pairing, rel, abs_=1e-3):
     a, b = oracle.rope_pairs(want.shape[-1], pairing)
     err = np.hypot(got[..., a] - want[..., a], got[..., b] - want[..., b])
@@ -62,10 +70,12 @@ def test_cossin_matches_fp64(rope_dim, base, llama3):
 
 # --------------------------------------------------------- full comparisons
 
-def test_tiny_gqa_full_parity():
+def test_tiny_gqa_full_parity(variant):
     wl = W.tiny_gqa()
     st = Stitched(wl, pool_device="cpu").run()
     try:
+        assert pic.pic_kernel_variant(st.ctx, 0) == (pic.PIC_VARIANT_BULK_PIPELINE if variant == "bulk"
+                                                      else pic.PIC_VARIANT_REGISTERS)
         segs, tables, rec = oracle_side(wl, st.nb)
         assert st.tables[0][:len(tables[0])].tolist() == tables[0]
         want_k, want_v = oracle.stitch_paged(bits(st.k_pool), bits(st.v_pool), segs, tables, st.nb,
@@ -98,7 +108,7 @@ GEOMS = [
 
 
 @pytest.mark.parametrize("pairing,D,H,bs", GEOMS)
-def test_gqa_geometries_ragged(pairing, D, H, bs):
+def test_gqa_geometries_ragged(pairing, D, H, bs, variant):
     """Ragged chunks (1, 15, 17, 33, 100 tokens), a truncated chunk, a repeated
     chunk, two requests in one launch, 3 layers."""
     lens = [1, 15, 17, 33, 100, 64]
@@ -121,7 +131,7 @@ def test_gqa_geometries_ragged(pairing, D, H, bs):
         st.close()
 
 
-def test_explicit_positions_base_pos_and_extreme_delta():
+def test_explicit_positions_base_pos_and_extreme_delta(variant):
     """Chunks cached at a non-zero base position (negative delta up to
     -(2^24 - 4)), explicit positions with inline gaps, a delta-0 chunk (bit
     copy), start after an inline prefix."""
@@ -174,7 +184,7 @@ def test_explicit_positions_base_pos_and_extreme_delta():
         pic.pic_destroy(ctx)
 
 
-def test_empty_batch_and_empty_request():
+def test_empty_batch_and_empty_request(variant):
     m = W.Model("empty", "gqa", 2, 2, 64, 64, 0, "neox", 1e4, 16)
     ctx = pic.create_from_spec(pic.model_spec_from(m), 8)
     try:
@@ -204,7 +214,7 @@ def test_empty_batch_and_empty_request():
         pic.pic_destroy(ctx)
 
 
-def test_bad_block_entry_sets_status_and_skips_write():
+def test_bad_block_entry_sets_status_and_skips_write(variant):
     """A block-table entry outside the cache is caught by the kernel's own
     bounds check: the write is skipped and the status word raised."""
     m = W.Model("bad", "gqa", 1, 1, 64, 64, 0, "neox", 1e4, 16)
@@ -261,7 +271,7 @@ def test_llama31_8b_full_parity_on_three_layers():
 
 
 @pytest.mark.parametrize("pairing", ["interleaved", "neox"])
-def test_mla_parity_small_context(pairing):
+def test_mla_parity_small_context(pairing, variant):
     """MLA rows: latent bit-exact, rope slice rotated; 3 layers, 2,000 tokens of
     16..128-token chunks behind a 32-token leading chunk (carve-out)."""
     base = W.deepseek_v3_mla(context_tokens=2000, num_layers=3)
@@ -371,7 +381,7 @@ def test_qwen3_8b_batch_full_size_sampled():
 
 @pytest.mark.parametrize("kind,pairing", [("gqa", "neox"), ("gqa", "interleaved"), ("mla", "interleaved"),
                                           ("mla", "neox")])
-def test_inplace_parity(kind, pairing):
+def test_inplace_parity(kind, pairing, variant):
     """Random cache contents; listed token ranges rotate by their delta
     (|delta| up to 2^17, negative included), every other row is untouched."""
     L, bs = 3, 16
@@ -438,7 +448,7 @@ def test_serving_stress_full_size_stitch_then_shift():
         torch.cuda.empty_cache()
 
 
-def test_stitch_then_shift_composes_small():
+def test_stitch_then_shift_composes_small(variant):
     """stitch(delta) then shift(delta') equals R(delta + delta') of the pool
     to two bf16 roundings (2 * 2^-8 per RoPE pair), on every row."""
     wl = _custom_workload("compose", "gqa", 2, 2, 128, "neox", 16, [50, 30, 70], [[(2, 70), (0, 50), (1, 30)]])
