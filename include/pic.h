@@ -39,6 +39,12 @@
  *       Pool:  [num_layers] x (layer stride) of [pool_tokens][row].
  *       Cache: [num_layers] x (layer stride) of [num_cache_blocks][block_size][row].
  *     Base pointers and layer strides must be multiples of 16 bytes.
+ *   - Host-resident pools and caches: pool and cache pointers may also be
+ *     pinned host memory (cudaHostAlloc, or memory registered with
+ *     cudaHostRegister): the kernels then stream them over the host link
+ *     directly, with no staging copy (on GB300, NVLink-C2C to Grace memory).
+ *     Pageable host memory is refused with PIC_ERR_INVALID_ARG.  Block tables,
+ *     recompute outputs and workspaces stay in device memory.
  *   - Positions are int32; |delta| must be below 2^24.
  */
 #ifndef PIC_H

@@ -363,11 +363,46 @@ int grid_for(const pic::KernelParams& p, int64_t resident) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(resident, units)));
 }
 
+// Where a buffer lives, for the kernels: 0 device (or managed) memory, 1
+// pinned / registered host memory (reachable over the host link), -1 memory
+// the GPU cannot reach (pageable host memory).
+int residency(const void* p) {
+  if (!p) return 0;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (a.type == cudaMemoryTypeHost) return 1;
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return 0;
+  return -1;
+}
+
+// 1 if any of the buffers is host memory, 0 if all are device memory, -1 if
+// one is unreachable (the error is recorded on ctx).
+int host_buffers(pic_ctx* ctx, const void* const* ptrs, int n) {
+  int any_host = 0;
+  for (int i = 0; i < n; ++i) {
+    const int r = residency(ptrs[i]);
+    if (r < 0) {
+      fail(ctx, PIC_ERR_INVALID_ARG,
+           "a pool or cache buffer is pageable host memory; pin it (cudaHostAlloc / cudaHostRegister) or use "
+           "device memory");
+      return -1;
+    }
+    any_host |= r;
+  }
+  return any_host;
+}
+
 // Picks the kernel for a stitch and launches it on stream s.
-cudaError_t launch_stitch_kernel(const pic_ctx* ctx, pic::KernelParams& p, int sm_count, cudaStream_t s) {
+// Buffers in host memory always go to the register kernels: they stream
+// through the host link with plain loads and stores.
+cudaError_t launch_stitch_kernel(const pic_ctx* ctx, pic::KernelParams& p, int sm_count, cudaStream_t s,
+                                 bool host_io) {
   const pic_model_desc& m = ctx->model;
   const bool gqa = m.kind == PIC_KIND_GQA;
-  if (ctx->tma_stitch) {
+  if (ctx->tma_stitch && !host_io) {
     // one CTA per SM (the stages take most of shared memory)
     set_layer_groups(p, m.num_layers, gqa ? 2 : 4);
     p.contiguous = gqa ? 0 : 1;
@@ -384,9 +419,10 @@ cudaError_t launch_stitch_kernel(const pic_ctx* ctx, pic::KernelParams& p, int s
   return pic::launch_stitch_mla(p, m.pairing, grid_for(p, resident), s);
 }
 
-cudaError_t launch_shift_kernel(const pic_ctx* ctx, pic::KernelParams& p, int sm_count, cudaStream_t s) {
+cudaError_t launch_shift_kernel(const pic_ctx* ctx, pic::KernelParams& p, int sm_count, cudaStream_t s,
+                                bool host_io) {
   const pic_model_desc& m = ctx->model;
-  if (ctx->tma_inplace) {
+  if (ctx->tma_inplace && !host_io) {
     set_layer_groups(p, m.num_layers, 4);
     p.contiguous = 0;
     return pic::launch_tma(p, ctx->tma_inplace_cfg, 2, m.pairing, m.rope_dim, grid_for(p, sm_count), s);
@@ -881,6 +917,9 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
   DeviceInfo di;
   st = current_device(ctx, di);
   if (st != PIC_OK) return st;
+  const void* bufs[4] = {k_pool, v_pool, k_cache, v_cache};
+  const int host_io = host_buffers(ctx, bufs, 4);
+  if (host_io < 0) return PIC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   StagingSlot* sl = nullptr;
   st = acquire_staging(ctx, di.device, w.total, &sl);
@@ -892,7 +931,7 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
   pic::KernelParams p{};
   fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_ws), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
                      v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
-  const cudaError_t e = launch_stitch_kernel(ctx, p, di.sm_count, s);
+  const cudaError_t e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
   return ok(ctx);
 }
@@ -936,6 +975,9 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
   DeviceInfo di;
   pic_status st = current_device(ctx, di);
   if (st != PIC_OK) return st;
+  const void* bufs[1] = {k_cache};
+  const int host_io = host_buffers(ctx, bufs, 1);
+  if (host_io < 0) return PIC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   StagingSlot* sl = nullptr;
   st = acquire_staging(ctx, di.device, w.total, &sl);
@@ -966,7 +1008,7 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
   p.block_tables = d_bt;
   p.max_blocks = max_blocks;
   p.header = reinterpret_cast<WsHeader*>(ws);
-  const cudaError_t e = launch_shift_kernel(ctx, p, di.sm_count, s);
+  const cudaError_t e = launch_shift_kernel(ctx, p, di.sm_count, s, host_io != 0);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "rerotate launch");
   return ok(ctx);
 }
@@ -1055,12 +1097,15 @@ pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32
   DeviceInfo di;
   st = current_device(ctx, di);
   if (st != PIC_OK) return st;
+  const void* bufs[4] = {k_pool, v_pool, k_cache, v_cache};
+  const int host_io = host_buffers(ctx, bufs, 4);
+  if (host_io < 0) return PIC_ERR_INVALID_ARG;
   cudaError_t e = cudaMemcpyAsync(d_scratch, image, w.total, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "scratch upload");
   KernelParams p{};
   fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_scratch), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
                      v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
-  e = launch_stitch_kernel(ctx, p, di.sm_count, s);
+  e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
   if (d_status_out) {
     e = cudaMemcpyAsync(d_status_out, d_scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);

@@ -300,8 +300,7 @@ def pic_stitch(ctx, plans, k_pool, v_pool, k_cache, v_cache, block_tables, recom
         if recompute_indptr.numel() < len(plans) + 1:
             raise ValueError("recompute_indptr needs n_req + 1 entries")
     for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_cache", k_cache), ("v_cache", v_cache)):
-        if t is not None and (not t.is_cuda or not _is_bf16(t) or not _rows_contiguous(t)):
-            raise ValueError(f"{name} must be a CUDA bf16 tensor with contiguous rows")
+        _check_kv_buffer(t, name)
     pool_ls = _layer_stride_bytes(k_pool)
     cache_ls = _layer_stride_bytes(k_cache)
     if v_pool is not None and _layer_stride_bytes(v_pool) != pool_ls:
@@ -334,8 +333,7 @@ def pic_stitch_noalloc(ctx, plans, k_pool, v_pool, k_cache, v_cache, block_table
         if recompute_indptr.numel() < len(plans) + 1:
             raise ValueError("recompute_indptr needs n_req + 1 entries")
     for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_cache", k_cache), ("v_cache", v_cache)):
-        if t is not None and (not t.is_cuda or not _is_bf16(t) or not _rows_contiguous(t)):
-            raise ValueError(f"{name} must be a CUDA bf16 tensor with contiguous rows")
+        _check_kv_buffer(t, name)
     if status is not None and (not status.is_cuda or status.element_size() != 4 or status.numel() < 1):
         raise ValueError("status must be a CUDA tensor of at least one 32-bit element")
     pool_ls = _layer_stride_bytes(k_pool)
@@ -363,6 +361,16 @@ def _rows_contiguous(t):
     return t[0].is_contiguous() if t.dim() > 1 else t.is_contiguous()
 
 
+def _check_kv_buffer(t, name):
+    """Pools and caches: bf16 with contiguous rows, on the GPU or in pinned host memory."""
+    if t is None:
+        return
+    if not _is_bf16(t) or not _rows_contiguous(t):
+        raise ValueError(f"{name} must be a bf16 tensor with contiguous rows")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+
+
 def _is_bf16(t):
     import torch
     return t.dtype == torch.bfloat16
@@ -384,8 +392,7 @@ def pic_rerotate_inplace(ctx, k_cache, block_tables, segs, workspace, stream=Non
     segs = list(segs)
     arr = _shift_array(segs)
     _check_device_int32(block_tables, "block_tables")
-    if not k_cache.is_cuda or not _is_bf16(k_cache) or not _rows_contiguous(k_cache):
-        raise ValueError("k_cache must be a CUDA bf16 tensor with contiguous rows")
+    _check_kv_buffer(k_cache, "k_cache")
     n_tables = int(block_tables.shape[0]) if block_tables.dim() == 2 else 1
     max_blocks = int(block_tables.shape[-1])
     st = load().pic_rerotate_inplace(ctx, _ptr(k_cache), _layer_stride_bytes(k_cache), _ptr(block_tables),
