@@ -268,13 +268,31 @@ class Rig:
                     for c, (off, n) in enumerate(zip(wl.pool_offsets, wl.chunk_lens))]
         self.k_pool = W.make_pool(wl, "k", device=device)
         self.v_pool = W.make_pool(wl, "v", device=device) if m.kind == "gqa" else None
+        self.chunk_blocks = None
+        if mode == "mapped":
+            # chunks resident in cache blocks (after the requests' own blocks)
+            pic.pic_destroy(self.ctx)
+            nblk = [-(-n // self.bs) for n in wl.chunk_lens]
+            first = self.nb
+            self.nb += sum(nblk)
+            self.ctx = pic.create_from_spec(pic.model_spec_from(m), self.nb)
+            self.chunk_blocks = []
+            b = first
+            for n in nblk:
+                self.chunk_blocks.append(list(range(b, b + n)))
+                b += n
         shape = (m.num_layers, self.nb, self.bs) + tuple(m.row_shape)
         self.k_cache = torch.empty(shape, dtype=torch.bfloat16, device=device)
         self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=device) if m.kind == "gqa" else None
-        plans, bt = self.plan()
-        self.n_rec = sum(pic.pic_plan_info(p)["num_recompute"] for p in plans)
-        self.ws_bytes = pic.pic_workspace_bytes(self.ctx, plans)
-        self.free(plans)
+        self.orders = None
+        if mode == "mapped":
+            self._load_chunks_into_blocks()
+        self.ws_bytes = 0
+        for _ in range(2 if self.orders is not None else 1):   # both orders of the mapped mode
+            plans, bt = self.plan()
+            self.n_rec = sum(pic.pic_plan_info(p)["num_recompute"] for p in plans)
+            self.ws_bytes = max(self.ws_bytes, pic.pic_workspace_bytes(self.ctx, plans))
+            self.free(plans)
         self.ridx = torch.empty(max(1, self.n_rec), dtype=torch.int32, device=device)
         self.indptr = torch.empty(len(wl.requests) + 1, dtype=torch.int32, device=device)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
@@ -282,11 +300,36 @@ class Rig:
         self.bt_pinned = [torch.empty_like(self.d_bt, device="cpu").pin_memory() for _ in range(2)]
         self.bt_events = [None, None]
         self.slot = 0
+        self.moved = 0
         self.shift_segs = None
         if mode == "inplace":
             self.shift_segs = self._shift_segments()
             self.ws_shift = torch.empty(pic.pic_rerotate_workspace_bytes(self.ctx, self.shift_segs),
                                         dtype=torch.uint8, device=device)
+
+    def _load_chunks_into_blocks(self):
+        """Writes every pool chunk into its cache blocks (rows 0.. of each) and
+        registers it as block-resident at position 0; requests then alternate
+        between their own chunk order and a second seeded order, so mapped
+        chunks really move every step."""
+        torch, pic, wl = self.torch, self.pic, self.wl
+        bs = self.bs
+        self.ids = []
+        for c, (off, n) in enumerate(zip(wl.pool_offsets, wl.chunk_lens)):
+            blks = self.chunk_blocks[c]
+            for j, b in enumerate(blks):
+                t0, t1 = j * bs, min(n, (j + 1) * bs)
+                self.k_cache[:, b, :t1 - t0] = self.k_pool[:, off + t0:off + t1]
+                if self.v_cache is not None:
+                    self.v_cache[:, b, :t1 - t0] = self.v_pool[:, off + t0:off + t1]
+            self.ids.append(pic.pic_register_chunk_blocks(self.ctx, W.chunk_key(wl.name, c), blks, n, 0)[0])
+        alt = []
+        for r, req in enumerate(wl.requests):
+            head, rest = req[:1], list(req[1:])
+            perm = W.Stream(1, f"mapped/order/{r}").permutation(len(rest))
+            alt.append(head + [rest[i] for i in perm])
+        self.orders = [wl.requests, alt]
+        self.step_no = 0
 
     def _shift_segments(self):
         plans, bt = self.plan()
@@ -306,13 +349,35 @@ class Rig:
     def plan(self):
         pic, wl = self.pic, self.wl
         plans, tables = [], []
-        for req in wl.requests:
+        reqs = wl.requests
+        if self.orders is not None:
+            reqs = self.orders[self.step_no % 2]
+            self.step_no += 1
+        for req in reqs:
             plan, bt = pic.pic_build_block_table(self.ctx, [self.ids[c] for c, _ in req], self.max_blocks,
                                                  take_tokens=[t for _, t in req],
-                                                 k_nonleading=wl.k_nonleading, k_leading=wl.k_leading)
+                                                 k_nonleading=wl.k_nonleading, k_leading=wl.k_leading,
+                                                 alias=self.orders is not None)
             plans.append(plan)
             tables.append(bt)
         return plans, np.stack(tables)
+
+    def moved_bytes(self, plans):
+        """Bytes a stitch of these plans must move: copied rows read + written
+        (K and V), mapped keys read + written when they move, nothing else."""
+        pic = self.pic
+        row = self.m.num_kv_heads * self.m.head_dim * 2
+        tensors = 2 if self.m.kind == "gqa" else 1
+        total = 0
+        for plan in plans:
+            for j in range(pic.pic_plan_info(plan)["num_segments"]):
+                sg = pic.pic_plan_segment(plan, j)
+                mode = pic.pic_plan_segment_mode(plan, j)
+                if mode == pic.PIC_SEG_MAPPED:
+                    total += 0 if sg["delta"] == 0 else 2 * row * sg["num_tokens"]
+                else:
+                    total += 2 * tensors * row * sg["num_tokens"]
+        return total * self.m.num_layers
 
     def free(self, plans):
         for p in plans:
@@ -339,6 +404,8 @@ class Rig:
                 kernel_events[1].record()
             return
         plans, bt = self.plan()
+        if self.orders is not None:
+            self.moved += self.moved_bytes(plans)
         self.upload_tables(bt)
         if kernel_events:
             kernel_events[0].record()
@@ -404,7 +471,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pic", choices=["pic", "reference"])
     ap.add_argument("--workload", default="llama31_8b_rag", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--mode", default="stitch", choices=["stitch", "inplace"])
+    ap.add_argument("--mode", default="stitch", choices=["stitch", "inplace", "mapped"])
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling captures only)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -449,6 +516,7 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rig.moved = 0
     clocks.mark_start()
     t0.record()
     for i in range(args.steps):
@@ -465,8 +533,12 @@ def main():
     ms = max_over_ranks(ms, dev)
 
     tl = wl.token_layers
-    bpt = bytes_per_token_layer(wl.model, args.mode)
-    algo_bytes = tl * bpt
+    if args.mode == "mapped":
+        algo_bytes = rig.moved / args.steps           # bytes actually moved per step
+        bpt = algo_bytes / tl
+    else:
+        bpt = bytes_per_token_layer(wl.model, args.mode)
+        algo_bytes = tl * bpt
     peak, peak_kind = measured_peak()
     value = world * algo_bytes / (ms * 1e-3) / 1e9
     achieved = algo_bytes / (kms * 1e-3) / 1e9
@@ -485,12 +557,13 @@ def main():
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl)
 
-    bulk = pic.pic_kernel_variant(rig.ctx, 0 if args.mode == "stitch" else 1) == pic.PIC_VARIANT_BULK_PIPELINE
+    bulk = pic.pic_kernel_variant(rig.ctx, 1 if args.mode == "inplace" else 0) == pic.PIC_VARIANT_BULK_PIPELINE
     if bulk:
         kname = "k_tma_pipeline<" + ("stitch K+V" if wl.model.kind == "gqa" else "stitch MLA rows") \
-            + ">" if args.mode == "stitch" else "k_tma_pipeline<in place>"
+            + ">" if args.mode != "inplace" else "k_tma_pipeline<in place>"
     else:
         kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
+                 "mapped": "k_rotate_rows<stitch, mapped chunks in place>",
                  "inplace": "k_rotate_rows<in place>"}[args.mode]
     line = {
         "metric": "stitched KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

@@ -61,7 +61,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st* pic_stream_t;
 
-#define PIC_ABI_VERSION 1
+#define PIC_ABI_VERSION 2
 #define PIC_KEY_BYTES 32
 #define PIC_MAX_ABS_DELTA ((1 << 24) - 1)
 
@@ -76,7 +76,8 @@ typedef enum pic_status {
   PIC_ERR_ALIGNMENT = 7,     /* pointer or stride not a multiple of 16 bytes         */
   PIC_ERR_CUDA = 8,          /* a CUDA runtime call or launch failed                 */
   PIC_ERR_DEVICE_CHECK = 9,  /* a kernel found a bad block-table entry               */
-  PIC_ERR_UNSUPPORTED = 10   /* geometry this build has no kernel for                */
+  PIC_ERR_UNSUPPORTED = 10,  /* geometry this build has no kernel for                */
+  PIC_ERR_BUSY = 11          /* chunk is mapped by a live request, or in use         */
 } pic_status;
 
 enum { PIC_KIND_GQA = 0, PIC_KIND_MLA = 1 };
@@ -140,6 +141,9 @@ typedef struct pic_plan pic_plan;
  *                position 0 (LegoLink pseudo-sinks; [EPIC] uses 4).
  *   k_leading    tokens recomputed at the start of a chunk at position 0
  *                ([Irminsul] 2.2 First-Chunk Carve-Out uses 32).
+ *   alias        1: map block-resident chunks into the request instead of
+ *                copying them when allowed (see pic_register_chunk_blocks);
+ *                0: always copy.
  */
 typedef struct pic_request_desc {
   const int32_t* chunk_ids;
@@ -150,6 +154,7 @@ typedef struct pic_request_desc {
   int32_t total_tokens;
   int32_t k_nonleading;
   int32_t k_leading;
+  int32_t alias;
 } pic_request_desc;
 
 /* One in-place shift: rows [start_pos, start_pos + num_tokens) of block-table
@@ -198,15 +203,44 @@ pic_status pic_register_chunk(pic_ctx* ctx, const uint8_t* key, int64_t pool_tok
                               int32_t num_tokens, int32_t base_pos, int32_t* chunk_id,
                               int32_t* is_new);
 
+/*
+ * Registers a chunk whose KV already sits in blocks of the paged cache (for
+ * instance a document prefilled once into the cache): blocks[j], j <
+ * ceil(num_tokens / block_size), holds its tokens [j*bs, (j+1)*bs) in rows
+ * 0.. of the block (the last block partly), keys rotated for position
+ * base_pos.  The blocks must be free in the allocator; they are taken out of
+ * it and belong to the chunk until pic_unregister_chunk.
+ *
+ * Such a chunk can be served to a request without moving its values: the
+ * EPIC runtime ([EPIC] "Algorithmic Architecture", runtime figure step 1
+ * "Virtual Block Mapping" -- the request reuses the chunk's physical blocks --
+ * and step 2, the keys rotated in place by dp).  pic_build_block_table with
+ * alias = 1 maps the chunk's blocks into the request's table when the chunk
+ * starts on a block boundary, is taken whole, occurs once in the request and
+ * no other live request uses it; the stitch then rotates only its keys, in
+ * place, by delta = new position - current position, and the chunk's current
+ * position becomes the new one (pic_chunk_info reports it).  Otherwise its
+ * tokens are copied out of its blocks like a pool chunk.  While a request has
+ * a chunk mapped, no other request may use that chunk (PIC_ERR_BUSY): its
+ * keys are being moved.  Rows of a mapped chunk's last block past its tokens
+ * belong to the request while it lives.
+ */
+pic_status pic_register_chunk_blocks(pic_ctx* ctx, const uint8_t* key, const int32_t* blocks,
+                                     int32_t num_tokens, int32_t base_pos, int32_t* chunk_id,
+                                     int32_t* is_new);
+
 /* Registry lookup by key: PIC_ERR_UNKNOWN_CHUNK on a miss. */
 pic_status pic_lookup_chunk(const pic_ctx* ctx, const uint8_t* key, int32_t* chunk_id);
 
-/* Reads back a registry entry. */
+/* Reads back a registry entry.  For a block-resident chunk, *pool_token_offset
+ * is -1 and *base_pos its current position. */
 pic_status pic_chunk_info(const pic_ctx* ctx, int32_t chunk_id, int64_t* pool_token_offset,
                           int32_t* num_tokens, int32_t* base_pos);
 
-/* Removes a chunk from the registry.  Plans already built keep working (they
- * hold copies of the entry); the id is never reused. */
+/* Removes a chunk from the registry; the id is never reused.  Plans already
+ * built from a pool chunk keep working (they hold copies of the entry).  A
+ * block-resident chunk still used by a live request is refused with
+ * PIC_ERR_BUSY; otherwise its blocks return to the allocator. */
 pic_status pic_unregister_chunk(pic_ctx* ctx, int32_t chunk_id);
 
 /* ---------------------------------------------------------- plan + table */
@@ -228,7 +262,10 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* request,
                                  int32_t* block_table_out, int32_t max_blocks,
                                  pic_plan** plan_out);
 
-/* Returns the plan's blocks to the allocator and frees the plan. */
+/* Returns the plan's fresh blocks to the allocator (mapped chunk blocks stay
+ * with their chunks), releases the chunks it used and frees the plan.  A plan
+ * whose in-place rotations were never enqueued puts its mapped chunks back
+ * at their old positions. */
 pic_status pic_free_request(pic_ctx* ctx, pic_plan* plan);
 
 /* Sizes of a plan (any pointer may be NULL). */
@@ -239,6 +276,14 @@ pic_status pic_plan_info(const pic_plan* plan, int32_t* total_tokens, int32_t* n
 pic_status pic_plan_segment(const pic_plan* plan, int32_t j, int32_t* chunk_id,
                             int64_t* src_token, int32_t* num_tokens, int32_t* dst_pos,
                             int32_t* delta);
+
+/* How segment j is served: PIC_SEG_COPY_POOL, PIC_SEG_COPY_BLOCKS (copied out
+ * of a block-resident chunk) or PIC_SEG_MAPPED (the chunk's blocks mapped,
+ * keys rotated in place); -1 on bad arguments. */
+#define PIC_SEG_COPY_POOL 0
+#define PIC_SEG_COPY_BLOCKS 1
+#define PIC_SEG_MAPPED 2
+int32_t pic_plan_segment_mode(const pic_plan* plan, int32_t j);
 
 /* ---------------------------------------------------------------- stitch */
 
@@ -266,6 +311,9 @@ size_t pic_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int
  *   d_workspace     >= pic_workspace_bytes(...) bytes of device memory.
  * Rows of the cache outside the plans' chunks are not touched.  Plans must
  * not write the same cache slot twice (distinct plans own distinct blocks).
+ * Mapped segments (PIC_SEG_MAPPED) are served in the same launch by rotating
+ * their keys in place; a plan's in-place rotations run once, so a plan with
+ * mapped segments can be stitched only once (PIC_ERR_INVALID_ARG after).
  */
 pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
                       const void* k_pool, const void* v_pool, int64_t pool_layer_stride_bytes,

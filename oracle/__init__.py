@@ -37,6 +37,9 @@ Pin status of each function (what outside fact each is checked against is in
                          carve-out)
 * ``stitch_*`` / ``rerotate_inplace`` pinned end to end against forward RoPE
                          computed at the target position.
+* ``map_request`` / ``apply_mapped`` (virtual block mapping) pinned against the
+                         block ids printed on the EPIC runtime figure and
+                         against forward RoPE at the mapped positions.
 """
 
 from .pic_oracle import (  # noqa: F401
@@ -60,4 +63,10 @@ from .pic_oracle import (  # noqa: F401
     stitch_paged,
     rerotate_inplace,
     expected_row,
+    BlockChunk,
+    MappedSegment,
+    BusyError,
+    map_request,
+    release_request,
+    apply_mapped,
 )

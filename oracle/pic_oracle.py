@@ -349,3 +349,151 @@ def expected_row(k_pool_row_bits, delta: int, theta, pairing: int, rope_offset: 
     """One stitched key row from its pool row: R(delta) on the rope slice."""
     return rotate_rows(bf16_bits_to_f64(k_pool_row_bits), delta, theta, pairing,
                        rope_offset, rope_dim)
+
+
+# ---------------------------------------------------------------------------
+# virtual block mapping (chunks resident in paged blocks)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class BlockChunk:
+    """A chunk whose KV sits in physical blocks of the paged cache: blocks[j]
+    holds its tokens [j*bs, (j+1)*bs) (the last block partly).  cur_pos is the
+    position its keys are currently rotated to (its base position when
+    registered); refs counts live requests that use it, mapped_by the one
+    request that has its blocks mapped (or None)."""
+    blocks: tuple
+    num_tokens: int
+    cur_pos: int = 0
+    refs: int = 0
+    mapped_by: object = None
+
+
+@dataclass(frozen=True)
+class MappedSegment:
+    """One chunk occurrence.  mode 'alias': the chunk's own blocks serve these
+    positions and its keys rotate in place by delta.  mode 'copy': tokens are
+    read from src_rows (pool token rows when src_kind == 'pool', absolute
+    cache rows block*bs + row when 'cache') and written rotated by delta."""
+    chunk: int
+    mode: str
+    src_kind: str
+    length: int
+    dst_pos: int
+    delta: int
+    src_rows: tuple
+
+
+class BusyError(Exception):
+    """A chunk is mapped by a live request and cannot be used by another."""
+
+
+def map_request(chunks, chunk_ids, block_size, pool: BlockPool, req_id, start_pos=0,
+                total_tokens=0, alias=True):
+    """Compose a request whose chunks may sit in paged blocks.
+
+    EPIC Guide, runtime figure: step 1 "Virtual Block Mapping" (the request
+    reuses the chunk's physical blocks) and step 2 (the keys are rotated in
+    place by dp; values untouched).  Rules (readings):
+    a block-resident chunk is mapped when aliasing is on, it starts on a
+    block boundary, it occurs once in the request and no other live request
+    uses it; otherwise it is copied out of its blocks.  A chunk mapped by a
+    live request may not be used by any other (BusyError).  delta is always
+    dst_pos - cur_pos.  Logical blocks not served by a mapped chunk get fresh
+    blocks, lowest id first.  On success the registry state changes: refs of
+    used block chunks +1, mapped chunks record the request and move cur_pos to
+    their new position.  Returns (segments, table, fresh blocks, undo list).
+    """
+    bs = block_size
+    counts = {}
+    for cid in chunk_ids:
+        counts[cid] = counts.get(cid, 0) + 1
+    segs, mapped, pos = [], {}, start_pos
+    for cid in chunk_ids:
+        c = chunks[cid]
+        n = c.num_tokens
+        if isinstance(c, BlockChunk):
+            if c.mapped_by is not None:
+                raise BusyError(cid)
+            delta = pos - c.cur_pos
+            if alias and pos % bs == 0 and counts[cid] == 1 and c.refs == 0:
+                for j, b in enumerate(c.blocks):
+                    mapped[pos // bs + j] = b
+                segs.append(MappedSegment(cid, "alias", "", n, pos, delta, ()))
+            else:
+                rows = tuple(c.blocks[t // bs] * bs + t % bs for t in range(n))
+                segs.append(MappedSegment(cid, "copy", "cache", n, pos, delta, rows))
+        else:
+            rows = tuple(range(c.pool_offset, c.pool_offset + n))
+            segs.append(MappedSegment(cid, "copy", "pool", n, pos, pos - c.base_pos, rows))
+        pos += n
+    total = max(pos, total_tokens)
+    n_logical = blocks_needed(total, bs)
+    need = [j for j in range(n_logical) if j not in mapped]
+    fresh = pool.allocate(len(need))
+    table = [0] * n_logical
+    for j, b in mapped.items():
+        table[j] = b
+    for j, b in zip(need, fresh):
+        table[j] = b
+    undo = []
+    for s in segs:
+        c = chunks[s.chunk]
+        if isinstance(c, BlockChunk):
+            c.refs += 1
+            if s.mode == "alias":
+                undo.append((s.chunk, c.cur_pos))
+                c.mapped_by = req_id
+                c.cur_pos = s.dst_pos
+    return segs, table, fresh, undo
+
+
+def release_request(chunks, segs, fresh, undo, pool: BlockPool, applied: bool):
+    """Free a mapped request: fresh blocks go back, block chunks lose a
+    reference, mapped chunks are released (and, if the request's in-place
+    rotations never ran, return to their old position)."""
+    pool.release(fresh)
+    for s in segs:
+        c = chunks[s.chunk]
+        if isinstance(c, BlockChunk):
+            c.refs -= 1
+            if s.mode == "alias":
+                c.mapped_by = None
+    if not applied:
+        for cid, old in undo:
+            chunks[cid].cur_pos = old
+
+
+def apply_mapped(k_cache_bits, v_cache_bits, k_pool_bits, v_pool_bits, segs, table, block_size,
+                 theta, pairing, rope_offset, rope_dim):
+    """Expected caches after one mapped request runs: K float64 (NaN-free: the
+    whole input cache, updated), V bits.  Every read sees the cache as it was
+    before the request (the rules above keep reads and in-place writes of one
+    launch on different rows).  k_cache_bits: uint16 [L][blocks][bs][*row]."""
+    bs = block_size
+    kc = np.asarray(k_cache_bits).view(np.uint16)
+    k_before = bf16_bits_to_f64(kc)
+    k_out = k_before.copy()
+    L = kc.shape[0]
+    flat_k = k_before.reshape((L, -1) + kc.shape[3:])
+    v_out = flat_v = None
+    if v_cache_bits is not None:
+        vc = np.asarray(v_cache_bits).view(np.uint16)
+        v_out = vc.copy()
+        flat_v = vc.reshape((L, -1) + vc.shape[3:])
+    for s in segs:
+        for t in range(s.length):
+            p = s.dst_pos + t
+            slot, row = table[p // bs], p % bs
+            if s.mode == "alias":
+                src = k_before[:, slot, row]
+            elif s.src_kind == "cache":
+                src = flat_k[:, s.src_rows[t]]
+                if v_out is not None:
+                    v_out[:, slot, row] = flat_v[:, s.src_rows[t]]
+            else:
+                src = bf16_bits_to_f64(np.asarray(k_pool_bits).view(np.uint16)[:, s.src_rows[t]])
+                if v_out is not None:
+                    v_out[:, slot, row] = np.asarray(v_pool_bits).view(np.uint16)[:, s.src_rows[t]]
+            k_out[:, slot, row] = rotate_rows(src, s.delta, theta, pairing, rope_offset, rope_dim)
+    return k_out, v_out

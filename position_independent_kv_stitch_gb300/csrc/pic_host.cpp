@@ -48,19 +48,25 @@ struct KeyHash {
 
 struct ChunkEntry {
   std::array<uint8_t, PIC_KEY_BYTES> key;
-  int64_t pool_token_offset;
+  int64_t pool_token_offset;  // -1 for a block-resident chunk
   int32_t num_tokens;
-  int32_t base_pos;
+  int32_t base_pos;           // block-resident: the position its keys are rotated to now
   bool live;
+  bool in_blocks = false;     // KV sits in blocks of the paged cache
+  std::vector<int32_t> blocks;
+  int32_t refs = 0;           // live plans using this block-resident chunk
+  const void* mapped_by = nullptr;  // the live plan that has its blocks mapped
 };
 
 struct Segment {
   int32_t chunk_id;
-  int64_t src_tok;
+  int64_t src_tok;            // pool chunks: first pool token row; else -1
   int32_t num_tokens;
   int32_t dst_pos;
   int32_t delta;
-  int32_t n_recompute;  // first n_recompute positions of the segment
+  int32_t n_recompute;        // first n_recompute positions of the segment
+  int32_t kind;               // pic::kRunPool / kRunBlocks / kRunInPlace
+  std::vector<int32_t> src_blocks;  // kRunBlocks: the chunk's blocks
 };
 
 // Paged blocks [0, n): lowest free id first (one deterministic choice).
@@ -69,6 +75,14 @@ class BlockAllocator {
   explicit BlockAllocator(int32_t n) : n_(n), words_((n + 63) / 64, 0), free_count_(n) {}
 
   int32_t free_count() const { return free_count_; }
+  bool is_free(int32_t id) const { return id >= 0 && id < n_ && !(words_[id >> 6] >> (id & 63) & 1ull); }
+
+  // Takes specific free ids (the caller checked is_free).
+  void take(const std::vector<int32_t>& ids) {
+    for (int32_t id : ids) words_[id >> 6] |= 1ull << (id & 63);
+    free_count_ -= static_cast<int32_t>(ids.size());
+    hint_ = first_free_from(hint_);
+  }
 
   // Takes the `count` lowest free ids; false (nothing taken) if too few are free.
   bool allocate(int32_t count, std::vector<int32_t>& out) {
@@ -122,9 +136,13 @@ int vectorized_bytes_ok(const void* p) { return (reinterpret_cast<uintptr_t>(p) 
 struct pic_plan {
   pic_ctx* owner;
   std::vector<Segment> segs;
-  std::vector<int32_t> blocks;
+  std::vector<int32_t> table;   // the request's block table (mapped + fresh blocks)
+  std::vector<int32_t> fresh;   // blocks this plan took from the allocator
   int32_t total_tokens;
   int32_t n_recompute;
+  bool has_mapped = false;      // some segment rotates a mapped chunk in place
+  bool applied = false;         // its in-place rotations have been enqueued
+  std::vector<std::pair<int32_t, int32_t>> undo;  // (chunk, position before mapping)
 };
 
 // Pinned host staging buffers for workspace images.  A pageable source would
@@ -206,27 +224,46 @@ bool plan_valid(const pic_ctx* ctx, const pic_plan* p) {
   return p != nullptr && ctx->plans.count(const_cast<pic_plan*>(p)) != 0;
 }
 
-// Splits one token range of a request into runs that stay inside one block
-// and hold at most `cap` tokens.
-void append_runs(std::vector<RunDesc>& runs, int64_t src_tok, int32_t dst_pos, int32_t n,
-                 int32_t req, int32_t delta, int32_t bs, int32_t cap, int32_t idx_off, int32_t idx_count) {
-  int32_t t = 0;
-  bool first = true;
-  while (t < n) {
+// Calls f(t, cnt, src) for each run of a segment: at most `cap` tokens that
+// land in one destination block and, for copies out of a block-resident
+// chunk, come from one of its blocks.  src is the run's first source row
+// (pool token row or absolute cache row; unused in place).  A mapped segment
+// whose keys need no rotation (delta 0) moves nothing: it yields one run of 0
+// tokens when it still has recompute positions to write, else none.
+template <typename F>
+void for_each_run(const Segment& sg, int32_t bs, int32_t cap, F f) {
+  if (sg.num_tokens <= 0) return;
+  if (sg.kind == pic::kRunInPlace && sg.delta == 0) {
+    if (sg.n_recompute > 0) f(0, 0, 0);
+    return;
+  }
+  for (int32_t t = 0; t < sg.num_tokens;) {
+    const int32_t pos = sg.dst_pos + t;
+    int32_t cnt = std::min(std::min(bs - pos % bs, sg.num_tokens - t), cap);
+    int32_t src = 0;
+    if (sg.kind == pic::kRunPool) {
+      src = static_cast<int32_t>(sg.src_tok + t);
+    } else if (sg.kind == pic::kRunBlocks) {
+      cnt = std::min(cnt, bs - t % bs);
+      src = sg.src_blocks[t / bs] * bs + t % bs;
+    }
+    f(t, cnt, src);
+    t += cnt;
+  }
+}
+
+// Runs of an in-place shift segment (source = destination).
+void append_shift_runs(std::vector<RunDesc>& runs, int32_t dst_pos, int32_t n, int32_t req, int32_t delta,
+                       int32_t bs, int32_t cap) {
+  for (int32_t t = 0; t < n;) {
     const int32_t pos = dst_pos + t;
-    const int32_t row = pos % bs;
-    const int32_t cnt = std::min(std::min(bs - row, n - t), cap);
-    RunDesc r;
-    r.src_tok = static_cast<int32_t>(src_tok + t);
+    const int32_t cnt = std::min(std::min(bs - pos % bs, n - t), cap);
+    RunDesc r{};
     r.dst_pos = pos;
     r.req = req;
-    r.ntok = cnt;
+    r.ntok_kind = cnt | (pic::kRunInPlace << 16);
     r.delta = delta;
-    r.idx_off = idx_off;
-    r.idx_count = first ? idx_count : 0;
-    r.idx_start = dst_pos;
     runs.push_back(r);
-    first = false;
     t += cnt;
   }
 }
@@ -276,8 +313,7 @@ size_t count_stitch_runs(const pic_ctx* ctx, const pic_plan* const* plans, int32
   const int32_t bs = ctx->model.block_size, cap = stitch_cap(ctx);
   size_t n = 0;
   for (int32_t r = 0; r < n_req; ++r)
-    for (const Segment& s : plans[r]->segs)
-      if (s.num_tokens > 0) n += static_cast<size_t>(runs_in_range(s.dst_pos, s.num_tokens, bs, cap));
+    for (const Segment& sg : plans[r]->segs) for_each_run(sg, bs, cap, [&](int32_t, int32_t, int32_t) { ++n; });
   return n;
 }
 
@@ -304,20 +340,17 @@ void build_stitch_image(const pic_ctx* ctx, const pic_plan* const* plans, int32_
   for (int32_t r = 0; r < n_req; ++r) {
     indptr[r] = static_cast<int32_t>(idx);
     for (const Segment& sg : plans[r]->segs) {
-      for (int32_t t = 0; t < sg.num_tokens;) {
-        const int32_t pos = sg.dst_pos + t;
-        const int32_t cnt = std::min(std::min(bs - pos % bs, sg.num_tokens - t), cap);
+      for_each_run(sg, bs, cap, [&](int32_t t, int32_t cnt, int32_t src) {
         RunDesc& rd = out[k++];
-        rd.src_tok = static_cast<int32_t>(sg.src_tok + t);
-        rd.dst_pos = pos;
+        rd.src = src;
+        rd.dst_pos = sg.dst_pos + t;
         rd.req = r;
-        rd.ntok = cnt;
+        rd.ntok_kind = cnt | (sg.kind << 16);
         rd.delta = sg.delta;
         rd.idx_off = static_cast<int32_t>(idx);
         rd.idx_count = t == 0 ? sg.n_recompute : 0;
         rd.idx_start = sg.dst_pos;
-        t += cnt;
-      }
+      });
       idx += sg.n_recompute;
     }
   }
@@ -398,8 +431,20 @@ int host_buffers(pic_ctx* ctx, const void* const* ptrs, int n) {
 // Picks the kernel for a stitch and launches it on stream s.
 // Buffers in host memory always go to the register kernels: they stream
 // through the host link with plain loads and stores.
+// True when most tokens of the batch are mapped keys rotated in place (K
+// only, half the bytes in flight per thread of a K+V copy).
+bool mostly_in_place(const pic_plan* const* plans, int32_t n_req) {
+  int64_t in_place = 0, copied = 0;
+  for (int32_t r = 0; r < n_req; ++r)
+    for (const Segment& sg : plans[r]->segs) {
+      if (sg.kind == pic::kRunInPlace) in_place += sg.delta != 0 ? sg.num_tokens : 0;
+      else copied += sg.num_tokens;
+    }
+  return in_place > copied;
+}
+
 cudaError_t launch_stitch_kernel(const pic_ctx* ctx, pic::KernelParams& p, int sm_count, cudaStream_t s,
-                                 bool host_io) {
+                                 bool host_io, bool in_place_heavy) {
   const pic_model_desc& m = ctx->model;
   const bool gqa = m.kind == PIC_KIND_GQA;
   if (ctx->tma_stitch && !host_io) {
@@ -411,7 +456,9 @@ cudaError_t launch_stitch_kernel(const pic_ctx* ctx, pic::KernelParams& p, int s
   if (gqa) {
     set_layer_groups(p, m.num_layers, kRegsLayersPerUnit);
     p.contiguous = 0;
-    const int cps = std::min(1, pic::occupancy_stitch_gqa(m.pairing, m.head_dim));
+    // ~64 KB of loads in flight per SM: one CTA for K+V copies, two when most
+    // runs move keys only (mapped chunks rotated in place)
+    const int cps = std::min(in_place_heavy ? 2 : 1, pic::occupancy_stitch_gqa(m.pairing, m.head_dim));
     return pic::launch_stitch_gqa(p, m.pairing, m.head_dim, grid_for(p, static_cast<int64_t>(sm_count) * cps), s);
   }
   const int64_t resident = static_cast<int64_t>(sm_count) * pic::occupancy_stitch_mla(m.pairing);
@@ -458,9 +505,16 @@ pic_status check_stitch_args(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
   for (int32_t r = 0; r < n_req; ++r) {
     if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
-    if (static_cast<int32_t>(plans[r]->blocks.size()) > max_blocks)
+    if (static_cast<int32_t>(plans[r]->table.size()) > max_blocks)
       return fail(ctx, PIC_ERR_CAPACITY, "plans[%d] has %zu blocks, block-table rows hold %d", r,
-                  plans[r]->blocks.size(), max_blocks);
+                  plans[r]->table.size(), max_blocks);
+    if (plans[r]->has_mapped) {
+      if (plans[r]->applied)
+        return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] maps chunks whose keys were already rotated in place; "
+                    "a plan with mapped chunks is stitched once", r);
+      for (int32_t q = 0; q < r; ++q)
+        if (plans[q] == plans[r]) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] appears twice", r);
+    }
   }
   const bool gqa = m.kind == PIC_KIND_GQA;
   if (!k_pool || !k_cache || !d_bt) return fail(ctx, PIC_ERR_INVALID_ARG, "null pool, cache or block table");
@@ -583,6 +637,7 @@ const char* pic_status_string(pic_status s) {
     case PIC_ERR_CUDA: return "PIC_ERR_CUDA";
     case PIC_ERR_DEVICE_CHECK: return "PIC_ERR_DEVICE_CHECK";
     case PIC_ERR_UNSUPPORTED: return "PIC_ERR_UNSUPPORTED";
+    case PIC_ERR_BUSY: return "PIC_ERR_BUSY";
   }
   return "PIC_ERR_?";
 }
@@ -594,6 +649,8 @@ const char* pic_last_error(const pic_ctx* ctx) {
 pic_status pic_create(const pic_model_desc* m, int32_t num_cache_blocks, pic_ctx** out) {
   if (!m || !out) return fail(nullptr, PIC_ERR_INVALID_ARG, "pic_create: null argument");
   if (num_cache_blocks < 0) return fail(nullptr, PIC_ERR_INVALID_ARG, "num_cache_blocks < 0");
+  if (m && static_cast<int64_t>(num_cache_blocks) * std::max(1, m->block_size) > std::numeric_limits<int32_t>::max())
+    return fail(nullptr, PIC_ERR_RANGE, "num_cache_blocks * block_size must stay below 2^31 rows");
   if (m->num_layers < 1) return fail(nullptr, PIC_ERR_INVALID_ARG, "num_layers must be >= 1");
   if (m->block_size < 1 || m->block_size > 256)
     return fail(nullptr, PIC_ERR_INVALID_ARG, "block_size must be in [1, 256]");
@@ -703,6 +760,8 @@ pic_status pic_register_chunk(pic_ctx* ctx, const uint8_t* key, int64_t pool_tok
   auto it = ctx->by_key.find(k);
   if (it != ctx->by_key.end()) {
     const ChunkEntry& e = ctx->chunks[it->second];
+    if (e.in_blocks)
+      return fail(ctx, PIC_ERR_KEY_CONFLICT, "key already registered as block-resident chunk %d", it->second);
     if (e.num_tokens != num_tokens || e.base_pos != base_pos)
       return fail(ctx, PIC_ERR_KEY_CONFLICT,
                   "key already registered as chunk %d with %d tokens at base %d", it->second,
@@ -713,6 +772,45 @@ pic_status pic_register_chunk(pic_ctx* ctx, const uint8_t* key, int64_t pool_tok
   }
   const int32_t id = static_cast<int32_t>(ctx->chunks.size());
   ctx->chunks.push_back(ChunkEntry{k, pool_token_offset, num_tokens, base_pos, true});
+  ctx->by_key.emplace(k, id);
+  *chunk_id = id;
+  if (is_new) *is_new = 1;
+  return ok(ctx);
+}
+
+pic_status pic_register_chunk_blocks(pic_ctx* ctx, const uint8_t* key, const int32_t* blocks,
+                                     int32_t num_tokens, int32_t base_pos, int32_t* chunk_id, int32_t* is_new) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (!key || !chunk_id || !blocks) return fail(ctx, PIC_ERR_INVALID_ARG, "null key, blocks or chunk_id");
+  if (num_tokens <= 0 || base_pos < 0) return fail(ctx, PIC_ERR_RANGE, "num_tokens must be > 0 and base_pos >= 0");
+  const int32_t bs = ctx->model.block_size;
+  const int32_t nb = (num_tokens + bs - 1) / bs;
+  std::vector<int32_t> ids(blocks, blocks + nb);
+  std::array<uint8_t, PIC_KEY_BYTES> k;
+  std::memcpy(k.data(), key, PIC_KEY_BYTES);
+  auto it = ctx->by_key.find(k);
+  if (it != ctx->by_key.end()) {
+    const ChunkEntry& e = ctx->chunks[it->second];
+    if (!e.in_blocks || e.num_tokens != num_tokens || e.blocks != ids)
+      return fail(ctx, PIC_ERR_KEY_CONFLICT, "key already registered as chunk %d with other tokens or blocks",
+                  it->second);
+    *chunk_id = it->second;
+    if (is_new) *is_new = 0;
+    return ok(ctx);
+  }
+  std::vector<int32_t> sorted = ids;
+  std::sort(sorted.begin(), sorted.end());
+  for (int32_t i = 0; i < nb; ++i) {
+    if (!ctx->alloc.is_free(sorted[i]))
+      return fail(ctx, PIC_ERR_RANGE, "block %d is outside the cache or not free", sorted[i]);
+    if (i > 0 && sorted[i] == sorted[i - 1]) return fail(ctx, PIC_ERR_INVALID_ARG, "block %d listed twice", sorted[i]);
+  }
+  ctx->alloc.take(ids);
+  const int32_t id = static_cast<int32_t>(ctx->chunks.size());
+  ChunkEntry e{k, -1, num_tokens, base_pos, true};
+  e.in_blocks = true;
+  e.blocks = std::move(ids);
+  ctx->chunks.push_back(std::move(e));
   ctx->by_key.emplace(k, id);
   *chunk_id = id;
   if (is_new) *is_new = 1;
@@ -748,6 +846,12 @@ pic_status pic_unregister_chunk(pic_ctx* ctx, int32_t id) {
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
   if (id < 0 || id >= static_cast<int32_t>(ctx->chunks.size()) || !ctx->chunks[id].live)
     return fail(ctx, PIC_ERR_UNKNOWN_CHUNK, "no chunk %d", id);
+  ChunkEntry& ce = ctx->chunks[id];
+  if (ce.in_blocks) {
+    if (ce.refs > 0) return fail(ctx, PIC_ERR_BUSY, "chunk %d is used by %d live request(s)", id, ce.refs);
+    ctx->alloc.release(ce.blocks);
+    ce.blocks.clear();
+  }
   ctx->chunks[id].live = false;
   ctx->by_key.erase(ctx->chunks[id].key);
   return ok(ctx);
@@ -767,6 +871,9 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32
     return fail(ctx, PIC_ERR_INVALID_ARG, "bad block table output");
 
   // Compose: EPIC Guide, "Algorithmic Architecture" 2. Modular Prompt Composer.
+  const int64_t bs = ctx->model.block_size;
+  std::unordered_map<int32_t, int32_t> occurrences;
+  for (int32_t j = 0; j < rq->n_chunks; ++j) ++occurrences[rq->chunk_ids[j]];
   std::vector<Segment> segs;
   segs.reserve(rq->n_chunks);
   int64_t pos = rq->start_pos;
@@ -777,6 +884,8 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32
     if (id < 0 || id >= static_cast<int32_t>(ctx->chunks.size()) || !ctx->chunks[id].live)
       return fail(ctx, PIC_ERR_UNKNOWN_CHUNK, "chunk %d (position %d in the request) is not registered", id, j);
     const ChunkEntry& e = ctx->chunks[id];
+    if (e.in_blocks && e.mapped_by != nullptr)
+      return fail(ctx, PIC_ERR_BUSY, "chunk %d is mapped by a live request; free it first", id);
     const int32_t n = rq->take_tokens ? rq->take_tokens[j] : e.num_tokens;
     if (n < 0 || n > e.num_tokens)
       return fail(ctx, PIC_ERR_RANGE, "take_tokens[%d] = %d outside [0, %d]", j, n, e.num_tokens);
@@ -786,14 +895,25 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32
                   static_cast<long long>(p), static_cast<long long>(prev_end));
     if (p + n > std::numeric_limits<int32_t>::max())
       return fail(ctx, PIC_ERR_RANGE, "positions beyond int32");
-    // delta = p_target - p_source (Irminsul, 2.2 delta-Rotation Rule)
+    // delta = p_target - p_source (Irminsul, 2.2 delta-Rotation Rule); for a
+    // block-resident chunk p_source is where its keys sit now.
     const int64_t delta = p - e.base_pos;
     if (delta > PIC_MAX_ABS_DELTA || delta < -PIC_MAX_ABS_DELTA)
       return fail(ctx, PIC_ERR_RANGE, "|delta| of chunk %d exceeds 2^24 - 1", j);
     // recompute count: LegoLink sinks of non-leading chunks; Irminsul carve-out at position 0
     const int32_t k = (p == 0) ? rq->k_leading : rq->k_nonleading;
     const int32_t nr = std::min(k, n);
-    segs.push_back(Segment{id, e.pool_token_offset, n, static_cast<int32_t>(p), static_cast<int32_t>(delta), nr});
+    Segment sg{id, e.in_blocks ? -1 : e.pool_token_offset, n, static_cast<int32_t>(p), static_cast<int32_t>(delta),
+               nr, pic::kRunPool, {}};
+    if (e.in_blocks) {
+      // EPIC runtime figure, step 1 "Virtual Block Mapping": reuse the chunk's
+      // blocks when it starts on a block boundary, is taken whole, occurs once
+      // here and no other live request uses it; otherwise copy it out.
+      const bool map = rq->alias && p % bs == 0 && n == e.num_tokens && occurrences[id] == 1 && e.refs == 0;
+      sg.kind = map ? pic::kRunInPlace : pic::kRunBlocks;
+      if (!map) sg.src_blocks = e.blocks;
+    }
+    segs.push_back(std::move(sg));
     n_recompute += nr;
     pos = p + n;
     prev_end = pos;
@@ -803,7 +923,6 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32
     return fail(ctx, PIC_ERR_RANGE, "total_tokens %d is before the end of the last chunk (%lld)",
                 rq->total_tokens, static_cast<long long>(end));
   const int64_t total = rq->total_tokens > 0 ? rq->total_tokens : end;
-  const int64_t bs = ctx->model.block_size;
   const int64_t nblocks = (total + bs - 1) / bs;
   if (nblocks > max_blocks)
     return fail(ctx, PIC_ERR_CAPACITY, "request needs %lld blocks, table holds %d",
@@ -811,19 +930,43 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32
   if (n_recompute > std::numeric_limits<int32_t>::max())
     return fail(ctx, PIC_ERR_RANGE, "recompute list too long");
 
+  // Logical blocks served by mapped chunks keep the chunk's blocks; the rest
+  // are fresh, lowest free id first.
+  std::vector<int32_t> table(static_cast<size_t>(nblocks), -1);
+  for (const Segment& sg : segs) {
+    if (sg.kind != pic::kRunInPlace) continue;
+    const ChunkEntry& e = ctx->chunks[sg.chunk_id];
+    for (size_t b = 0; b < e.blocks.size(); ++b) table[sg.dst_pos / bs + b] = e.blocks[b];
+  }
+  int32_t need = 0;
+  for (int32_t v : table) need += v < 0;
   pic_plan* plan = new (std::nothrow) pic_plan();
   if (!plan) return fail(ctx, PIC_ERR_INVALID_ARG, "out of host memory");
-  if (!ctx->alloc.allocate(static_cast<int32_t>(nblocks), plan->blocks)) {
+  if (!ctx->alloc.allocate(need, plan->fresh)) {
     delete plan;
-    return fail(ctx, PIC_ERR_OUT_OF_BLOCKS, "request needs %lld blocks, %d free",
-                static_cast<long long>(nblocks), ctx->alloc.free_count());
+    return fail(ctx, PIC_ERR_OUT_OF_BLOCKS, "request needs %d fresh blocks, %d free", need, ctx->alloc.free_count());
   }
+  for (size_t i = 0, f = 0; i < table.size(); ++i)
+    if (table[i] < 0) table[i] = plan->fresh[f++];
   plan->owner = ctx;
+  plan->table = std::move(table);
   plan->segs = std::move(segs);
   plan->total_tokens = static_cast<int32_t>(total);
   plan->n_recompute = static_cast<int32_t>(n_recompute);
+  // Registry: block-resident chunks gain a user; mapped ones move to their new position.
+  for (const Segment& sg : plan->segs) {
+    ChunkEntry& e = ctx->chunks[sg.chunk_id];
+    if (!e.in_blocks) continue;
+    ++e.refs;
+    if (sg.kind == pic::kRunInPlace) {
+      plan->undo.emplace_back(sg.chunk_id, e.base_pos);
+      plan->has_mapped = true;
+      e.mapped_by = plan;
+      e.base_pos = sg.dst_pos;
+    }
+  }
   for (int32_t i = 0; i < max_blocks; ++i)
-    bt_out[i] = i < static_cast<int32_t>(plan->blocks.size()) ? plan->blocks[i] : -1;
+    bt_out[i] = i < static_cast<int32_t>(plan->table.size()) ? plan->table[i] : -1;
   ctx->plans.insert(plan);
   *plan_out = plan;
   return ok(ctx);
@@ -832,7 +975,15 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32
 pic_status pic_free_request(pic_ctx* ctx, pic_plan* plan) {
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
   if (!plan_valid(ctx, plan)) return fail(ctx, PIC_ERR_INVALID_ARG, "plan does not belong to this context");
-  ctx->alloc.release(plan->blocks);
+  if (!plan->applied)
+    for (const auto& u : plan->undo) ctx->chunks[u.first].base_pos = u.second;  // rotation never enqueued
+  for (const Segment& sg : plan->segs) {
+    ChunkEntry& e = ctx->chunks[sg.chunk_id];
+    if (!e.in_blocks) continue;
+    --e.refs;
+    if (sg.kind == pic::kRunInPlace) e.mapped_by = nullptr;
+  }
+  ctx->alloc.release(plan->fresh);
   ctx->plans.erase(plan);
   delete plan;
   return ok(ctx);
@@ -842,7 +993,7 @@ pic_status pic_plan_info(const pic_plan* p, int32_t* total_tokens, int32_t* num_
                          int32_t* num_segments, int32_t* num_recompute) {
   if (!p) return fail(nullptr, PIC_ERR_INVALID_ARG, "null plan");
   if (total_tokens) *total_tokens = p->total_tokens;
-  if (num_blocks) *num_blocks = static_cast<int32_t>(p->blocks.size());
+  if (num_blocks) *num_blocks = static_cast<int32_t>(p->table.size());
   if (num_segments) *num_segments = static_cast<int32_t>(p->segs.size());
   if (num_recompute) *num_recompute = p->n_recompute;
   return ok(nullptr);
@@ -860,6 +1011,11 @@ pic_status pic_plan_segment(const pic_plan* p, int32_t j, int32_t* chunk_id, int
   if (dst_pos) *dst_pos = s.dst_pos;
   if (delta) *delta = s.delta;
   return ok(nullptr);
+}
+
+int32_t pic_plan_segment_mode(const pic_plan* p, int32_t j) {
+  if (!p || j < 0 || j >= static_cast<int32_t>(p->segs.size())) return -1;
+  return p->segs[j].kind;  // PIC_SEG_* values equal the run kinds
 }
 
 // -------------------------------------------------------------- recompute
@@ -931,8 +1087,9 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
   pic::KernelParams p{};
   fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_ws), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
                      v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
-  const cudaError_t e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0);
+  const cudaError_t e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0, mostly_in_place(plans, n_req));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
+  for (int32_t r = 0; r < n_req; ++r) const_cast<pic_plan*>(plans[r])->applied = true;
   return ok(ctx);
 }
 
@@ -990,7 +1147,7 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
   for (int32_t i = 0; i < n_segs; ++i) {
     const pic_shift_seg& g = segs[i];
     if (g.num_tokens <= 0 || g.delta == 0) continue;  // R_0 = I: nothing to do
-    append_runs(runs, 0, g.start_pos, g.num_tokens, g.req, g.delta, bs, cap, 0, 0);
+    append_shift_runs(runs, g.start_pos, g.num_tokens, g.req, g.delta, bs, cap);
   }
   std::memcpy(base + w.runs_off, runs.data(), runs.size() * sizeof(RunDesc));
   st = upload_staging(ctx, sl, d_ws, w.total, s);
@@ -1105,8 +1262,9 @@ pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32
   KernelParams p{};
   fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_scratch), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
                      v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
-  e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0);
+  e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0, mostly_in_place(plans, n_req));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
+  for (int32_t r = 0; r < n_req; ++r) const_cast<pic_plan*>(plans[r])->applied = true;
   if (d_status_out) {
     e = cudaMemcpyAsync(d_status_out, d_scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "status copy");

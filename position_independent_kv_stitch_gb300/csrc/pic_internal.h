@@ -15,16 +15,25 @@ namespace pic {
 // one paged block.  Runs are layer-independent; a kernel work unit is a run
 // times a group of consecutive layers.  32 bytes, read once per unit.
 struct alignas(32) RunDesc {
-  int32_t src_tok;    // pool token row of the run's first token (stitch only)
+  int32_t src;        // kRunPool: pool token row of the first token; kRunBlocks:
+                      // absolute cache row (block * block_size + row); kRunInPlace: unused
   int32_t dst_pos;    // absolute position of the run's first token
   int32_t req;        // block-table row
-  int32_t ntok;       // tokens in the run, 1 .. block_size, all in one block
+  int32_t ntok_kind;  // tokens in the run (0 .. block_size, low 16 bits) | kind << 16
   int32_t delta;      // position shift of the segment
   int32_t idx_off;    // first recompute-list slot this run writes
   int32_t idx_count;  // recompute positions it writes (segment's first run only)
   int32_t idx_start;  // first recompute position
 };
 static_assert(sizeof(RunDesc) == 32, "RunDesc layout");
+
+// Where a run's source rows are: copied from the chunk pool, copied from the
+// blocks of a block-resident chunk in the cache itself, or the destination
+// rows themselves (a mapped chunk's keys rotated in place; values untouched).
+// A run of 0 tokens only carries recompute positions.
+enum RunKind : int32_t { kRunPool = 0, kRunBlocks = 1, kRunInPlace = 2 };
+__host__ __device__ inline int32_t run_ntok(const RunDesc& r) { return r.ntok_kind & 0xffff; }
+__host__ __device__ inline int32_t run_kind(const RunDesc& r) { return r.ntok_kind >> 16; }
 
 // Workspace layout: [header 256 B][freq table][indptr][runs], each 256-B aligned.
 struct WsHeader {

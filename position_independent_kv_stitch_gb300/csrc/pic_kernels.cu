@@ -159,8 +159,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_rows(const KernelParams 
   const int64_t u_step = P.contiguous ? 1 : gridDim.x;
   int cur_run = -1;
   RunDesc r{};
-  bool valid = false;
-  int64_t dst_off = 0, src_off = 0;
+  bool valid = false, has_v = false;
+  int ntok = 0;
+  int64_t dst_off = 0, src_off = 0, src_ls = 0;
+  const uint8_t* ksrc = nullptr;
+  const uint8_t* vsrc = nullptr;
   int cached_delta = 0;
   float c[NF], s[NF];
 #pragma unroll
@@ -178,10 +181,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_rows(const KernelParams 
     if (run != cur_run) {
       cur_run = run;
       r = P.runs[run];
+      ntok = run_ntok(r);
       int blk, row0;
       valid = resolve_block(P, r, blk, row0);
       dst_off = valid ? (static_cast<int64_t>(blk) * P.block_size + row0) * P.row_bytes : 0;
-      src_off = STITCH ? static_cast<int64_t>(r.src_tok) * P.row_bytes : dst_off;
+      // source rows: the pool, blocks of the cache itself, or the destination (in place)
+      const int kind = STITCH ? run_kind(r) : kRunInPlace;
+      has_v = STITCH && kind != kRunInPlace;
+      if (kind == kRunPool) {
+        ksrc = P.k_src; vsrc = P.v_src; src_ls = P.src_layer_stride;
+        src_off = static_cast<int64_t>(r.src) * P.row_bytes;
+      } else {
+        ksrc = P.k_dst; vsrc = P.v_dst; src_ls = P.dst_layer_stride;
+        src_off = kind == kRunBlocks ? static_cast<int64_t>(r.src) * P.row_bytes : dst_off;
+      }
       if (r.delta != 0 && r.delta != cached_delta) {
 #pragma unroll
         for (int k = 0; k < NF; ++k) shift_cossin(r.delta, __ldg(P.freq + f0 + k), c[k], s[k]);
@@ -191,14 +204,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_rows(const KernelParams 
     if (STITCH) emit_recompute(P, r, lg);
     if (!valid) continue;
     const bool rot = (r.delta != 0);
-    const int nh = r.ntok * P.heads_per_token;
+    const int nh = ntok * P.heads_per_token;
     const int l_end = min(P.num_layers, (lg + 1) * P.lg_size);
     for (int l = lg * P.lg_size; l < l_end; ++l) {
-      const uint8_t* ks =
-          (STITCH ? P.k_src + l * P.src_layer_stride : P.k_dst + l * P.dst_layer_stride) + src_off;
+      const uint8_t* ks = ksrc + l * src_ls + src_off;
       uint8_t* kd = P.k_dst + l * P.dst_layer_stride + dst_off;
-      const uint8_t* vs = STITCH ? P.v_src + l * P.src_layer_stride + src_off : nullptr;
-      uint8_t* vd = STITCH ? P.v_dst + l * P.dst_layer_stride + dst_off : nullptr;
+      const uint8_t* vs = has_v ? vsrc + l * src_ls + src_off : nullptr;
+      uint8_t* vd = has_v ? P.v_dst + l * P.dst_layer_stride + dst_off : nullptr;
 
       for (int h0 = hrow0; h0 < nh; h0 += HSTEP * U) {
         uint4 ka[U], kb[U], va[U], vb[U];
@@ -210,8 +222,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_rows(const KernelParams 
             if (STITCH) {
               ka[j] = ld_stream(ks + o + lo_off);
               if (NEOX) kb[j] = ld_stream(ks + o + hi_off);
-              va[j] = ld_stream(vs + o + lo_off);
-              if (NEOX) vb[j] = ld_stream(vs + o + hi_off);
+              if (has_v) {
+                va[j] = ld_stream(vs + o + lo_off);
+                if (NEOX) vb[j] = ld_stream(vs + o + hi_off);
+              }
             } else {
               ka[j] = ld_plain(ks + o + lo_off);
               if (NEOX) kb[j] = ld_plain(ks + o + hi_off);
@@ -230,8 +244,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_rows(const KernelParams 
             if (STITCH) {
               st_stream(kd + o + lo_off, ka[j]);
               if (NEOX) st_stream(kd + o + hi_off, kb[j]);
-              st_stream(vd + o + lo_off, va[j]);
-              if (NEOX) st_stream(vd + o + hi_off, vb[j]);
+              if (has_v) {
+                st_stream(vd + o + lo_off, va[j]);
+                if (NEOX) st_stream(vd + o + hi_off, vb[j]);
+              }
             } else {
               st_plain(kd + o + lo_off, ka[j]);
               if (NEOX) st_plain(kd + o + hi_off, kb[j]);
@@ -283,21 +299,27 @@ __global__ void __launch_bounds__(kMlaThreads) k_stitch_mla(const KernelParams P
 #pragma unroll
       for (int k = 0; k < NF; ++k) shift_cossin(r.delta, __ldg(P.freq + f0 + k), c[k], s[k]);
     }
+    const int ntok = run_ntok(r);
+    const int kind = run_kind(r);
     const int64_t dst_off = (static_cast<int64_t>(blk) * P.block_size + row0) * P.row_bytes;
-    const int64_t src_off = static_cast<int64_t>(r.src_tok) * P.row_bytes;
+    // source rows: the pool, blocks of the cache itself, or the destination
+    // (in place: only the rope key moves, the latent stays where it is)
+    const uint8_t* sbase = kind == kRunPool ? P.k_src : P.k_dst;
+    const int64_t sls = kind == kRunPool ? P.src_layer_stride : P.dst_layer_stride;
+    const int64_t src_off = kind == kRunInPlace ? dst_off : static_cast<int64_t>(r.src) * P.row_bytes;
+    const bool work = active && !(kind == kRunInPlace && !rope_col);
     const int l_begin = lg * P.lg_size;
     const int l_end = min(P.num_layers, l_begin + P.lg_size);
 
-    for (int l = l_begin; l < l_end; ++l) {
-      const uint8_t* src = P.k_src + l * P.src_layer_stride + src_off + col * 16;
+    for (int l = l_begin; l < l_end && work; ++l) {
+      const uint8_t* src = sbase + l * sls + src_off + col * 16;
       uint8_t* dst = P.k_dst + l * P.dst_layer_stride + dst_off + col * 16;
-      if (!active) continue;
-      for (int r0 = trow; r0 < r.ntok; r0 += kMlaRowsPerSweep * U) {
+      for (int r0 = trow; r0 < ntok; r0 += kMlaRowsPerSweep * U) {
         uint4 x[U], y[U];
 #pragma unroll
         for (int j = 0; j < U; ++j) {
           const int row = r0 + j * kMlaRowsPerSweep;
-          if (row < r.ntok) {
+          if (row < ntok) {
             x[j] = ld_stream(src + static_cast<int64_t>(row) * P.row_bytes);
             if (NEOX && rope_col) y[j] = ld_stream(src + static_cast<int64_t>(row) * P.row_bytes + 64);
           }
@@ -305,7 +327,7 @@ __global__ void __launch_bounds__(kMlaThreads) k_stitch_mla(const KernelParams P
 #pragma unroll
         for (int j = 0; j < U; ++j) {
           const int row = r0 + j * kMlaRowsPerSweep;
-          if (row < r.ntok) {
+          if (row < ntok) {
             if (rot) {
               if (NEOX) rotate_neox(x[j], y[j], c, s);
               else rotate_interleaved(x[j], c, s);

@@ -143,7 +143,7 @@ struct StageMeta {
   int32_t idx_off;
   int32_t idx_count;
   int32_t idx_start;
-  int32_t pad;
+  int32_t has_v;     // the tile carries a value tile too (not for in-place runs)
 };
 
 // MODE 0: GQA/MLA stitch with values (K + V tiles); 1: stitch without values
@@ -249,28 +249,36 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
       cur_l = 0;
       ++k_unit;
     }
+    const int ntok = run_ntok(r);
+    const int kind = INPLACE ? kRunInPlace : run_kind(r);
+    const bool has_v = HAS_V && kind != kRunInPlace;
     StageMeta& m = meta[s];
     m.delta = r.delta;
-    m.ntok = r.ntok;
+    m.ntok = ntok;
     m.valid = valid ? 1 : 0;
     m.layer = l;
     m.idx_off = r.idx_off;
     m.idx_count = r.idx_count;
     m.idx_start = r.idx_start;
+    m.has_v = has_v ? 1 : 0;
     m.dst_k = P.k_dst + l * P.dst_layer_stride + dst_off;
     m.dst_v = HAS_V ? P.v_dst + l * P.dst_layer_stride + dst_off : nullptr;
-    if (!valid) {
+    if (!valid || ntok == 0) {
       mbar_arrive(&bars[s]);  // nothing to copy: complete the phase
       return;
     }
-    const uint32_t bytes = static_cast<uint32_t>(r.ntok) * static_cast<uint32_t>(P.row_bytes);
+    const uint32_t bytes = static_cast<uint32_t>(ntok) * static_cast<uint32_t>(P.row_bytes);
     uint8_t* st = stages + static_cast<size_t>(s) * C.stage_bytes;
-    const uint8_t* src_k =
-        INPLACE ? m.dst_k : P.k_src + l * P.src_layer_stride + static_cast<int64_t>(r.src_tok) * P.row_bytes;
-    mbar_arrive_expect_tx(&bars[s], bytes * (HAS_V ? 2u : 1u));
+    // source rows: the pool, blocks of the cache itself, or the destination (in place)
+    const int64_t src_off = static_cast<int64_t>(r.src) * P.row_bytes;
+    const uint8_t* src_k = kind == kRunInPlace ? m.dst_k
+                           : kind == kRunBlocks ? P.k_dst + l * P.dst_layer_stride + src_off
+                                                : P.k_src + l * P.src_layer_stride + src_off;
+    mbar_arrive_expect_tx(&bars[s], bytes * (has_v ? 2u : 1u));
     bulk_load(st, src_k, bytes, &bars[s]);
-    if (HAS_V) {
-      const uint8_t* src_v = P.v_src + l * P.src_layer_stride + static_cast<int64_t>(r.src_tok) * P.row_bytes;
+    if (has_v) {
+      const uint8_t* src_v = kind == kRunBlocks ? P.v_dst + l * P.dst_layer_stride + src_off
+                                                : P.v_src + l * P.src_layer_stride + src_off;
       bulk_load(st + tensor_bytes, src_v, bytes, &bars[s]);
     }
   };
@@ -327,10 +335,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
     fence_proxy_async_smem();  // make the rotated rows visible to the bulk copy engine
     __syncthreads();
     if (tid == 0) {
-      if (m.valid) {
+      if (m.valid && m.ntok > 0) {
         const uint32_t bytes = static_cast<uint32_t>(m.ntok) * static_cast<uint32_t>(P.row_bytes);
         bulk_store(m.dst_k, st, bytes);
-        if (HAS_V) bulk_store(m.dst_v, st + tensor_bytes, bytes);
+        if (HAS_V && m.has_v) bulk_store(m.dst_v, st + tensor_bytes, bytes);
       }
       bulk_commit();
       bulk_wait_read_1();  // the previous unit's stores have read their stage

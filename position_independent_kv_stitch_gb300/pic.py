@@ -21,7 +21,7 @@ PIC_OK = 0
 STATUS_NAMES = {
     0: "PIC_OK", 1: "PIC_ERR_INVALID_ARG", 2: "PIC_ERR_UNKNOWN_CHUNK", 3: "PIC_ERR_KEY_CONFLICT",
     4: "PIC_ERR_OUT_OF_BLOCKS", 5: "PIC_ERR_CAPACITY", 6: "PIC_ERR_RANGE", 7: "PIC_ERR_ALIGNMENT",
-    8: "PIC_ERR_CUDA", 9: "PIC_ERR_DEVICE_CHECK", 10: "PIC_ERR_UNSUPPORTED",
+    8: "PIC_ERR_CUDA", 9: "PIC_ERR_DEVICE_CHECK", 10: "PIC_ERR_UNSUPPORTED", 11: "PIC_ERR_BUSY",
 }
 PIC_KIND_GQA, PIC_KIND_MLA = 0, 1
 PIC_PAIRING_NEOX_HALF, PIC_PAIRING_INTERLEAVED = 0, 1
@@ -30,6 +30,7 @@ PIC_KEY_BYTES = 32
 PIC_DEV_BAD_BLOCK = 0x1
 PIC_DEV_TIMEOUT = 0x2
 PIC_VARIANT_REGISTERS, PIC_VARIANT_BULK_PIPELINE = 0, 1
+PIC_SEG_COPY_POOL, PIC_SEG_COPY_BLOCKS, PIC_SEG_MAPPED = 0, 1, 2
 
 
 class PicError(RuntimeError):
@@ -55,7 +56,7 @@ class pic_request_desc(ctypes.Structure):
         ("chunk_ids", ctypes.POINTER(ctypes.c_int32)), ("take_tokens", ctypes.POINTER(ctypes.c_int32)),
         ("dst_pos", ctypes.POINTER(ctypes.c_int32)), ("n_chunks", ctypes.c_int32),
         ("start_pos", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
-        ("k_nonleading", ctypes.c_int32), ("k_leading", ctypes.c_int32),
+        ("k_nonleading", ctypes.c_int32), ("k_leading", ctypes.c_int32), ("alias", ctypes.c_int32),
     ]
 
 
@@ -75,6 +76,8 @@ _SIGNATURES = {
     "pic_create": (ctypes.c_int, [_P(pic_model_desc), _i32, _P(_c_void_p)]),
     "pic_destroy": (None, [_c_void_p]),
     "pic_register_chunk": (ctypes.c_int, [_c_void_p, ctypes.c_char_p, _i64, _i32, _i32, _P(_i32), _P(_i32)]),
+    "pic_register_chunk_blocks": (ctypes.c_int, [_c_void_p, ctypes.c_char_p, _P(_i32), _i32, _i32, _P(_i32),
+                                                 _P(_i32)]),
     "pic_lookup_chunk": (ctypes.c_int, [_c_void_p, ctypes.c_char_p, _P(_i32)]),
     "pic_chunk_info": (ctypes.c_int, [_c_void_p, _i32, _P(_i64), _P(_i32), _P(_i32)]),
     "pic_unregister_chunk": (ctypes.c_int, [_c_void_p, _i32]),
@@ -82,6 +85,7 @@ _SIGNATURES = {
     "pic_free_request": (ctypes.c_int, [_c_void_p, _c_void_p]),
     "pic_plan_info": (ctypes.c_int, [_c_void_p, _P(_i32), _P(_i32), _P(_i32), _P(_i32)]),
     "pic_plan_segment": (ctypes.c_int, [_c_void_p, _i32, _P(_i32), _P(_i64), _P(_i32), _P(_i32), _P(_i32)]),
+    "pic_plan_segment_mode": (_i32, [_c_void_p, _i32]),
     "pic_workspace_bytes": (_sz, [_c_void_p, _P(_c_void_p), _i32]),
     "pic_stitch": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _c_void_p, _c_void_p, _i64,
                                   _c_void_p, _c_void_p, _i64, _c_void_p, _i32, _c_void_p, _c_void_p,
@@ -204,6 +208,18 @@ def pic_register_chunk(ctx, key: bytes, pool_token_offset: int, num_tokens: int,
     return cid.value, bool(new.value)
 
 
+def pic_register_chunk_blocks(ctx, key: bytes, blocks, num_tokens: int, base_pos: int = 0):
+    """Registers a chunk whose KV sits in the given paged-cache blocks.
+    Returns (chunk_id, is_new)."""
+    if len(key) != PIC_KEY_BYTES:
+        raise ValueError("key must be 32 bytes")
+    arr = _i32_array(list(blocks))
+    cid, new = ctypes.c_int32(), ctypes.c_int32()
+    _check(load().pic_register_chunk_blocks(ctx, key, ctypes.cast(arr, _P(_i32)), int(num_tokens), int(base_pos),
+                                            ctypes.byref(cid), ctypes.byref(new)), ctx)
+    return cid.value, bool(new.value)
+
+
 def pic_lookup_chunk(ctx, key: bytes) -> int:
     cid = ctypes.c_int32()
     _check(load().pic_lookup_chunk(ctx, key, ctypes.byref(cid)), ctx)
@@ -224,7 +240,7 @@ def pic_unregister_chunk(ctx, chunk_id: int):
 
 def pic_build_block_table(ctx, chunk_ids, max_blocks: int, take_tokens=None, dst_pos=None,
                           start_pos: int = 0, total_tokens: int = 0, k_nonleading: int = 0,
-                          k_leading: int = 0):
+                          k_leading: int = 0, alias: bool = False):
     """Returns (plan handle, block table as numpy int32[max_blocks])."""
     rq = pic_request_desc()
     ids = _i32_array(list(chunk_ids))
@@ -236,6 +252,7 @@ def pic_build_block_table(ctx, chunk_ids, max_blocks: int, take_tokens=None, dst
     rq.n_chunks = len(chunk_ids)
     rq.start_pos, rq.total_tokens = int(start_pos), int(total_tokens)
     rq.k_nonleading, rq.k_leading = int(k_nonleading), int(k_leading)
+    rq.alias = 1 if alias else 0
     bt = np.empty(max(0, int(max_blocks)), dtype=np.int32)
     plan = ctypes.c_void_p()
     _check(load().pic_build_block_table(ctx, ctypes.byref(rq),
@@ -260,6 +277,11 @@ def pic_plan_segment(plan, j: int):
                                    ctypes.byref(p), ctypes.byref(d)))
     return {"chunk_id": c.value, "src_tok": src.value, "num_tokens": n.value, "dst_pos": p.value,
             "delta": d.value}
+
+
+def pic_plan_segment_mode(plan, j: int) -> int:
+    """PIC_SEG_COPY_POOL, PIC_SEG_COPY_BLOCKS or PIC_SEG_MAPPED."""
+    return int(load().pic_plan_segment_mode(plan, int(j)))
 
 
 def pic_recompute_indices(plans):

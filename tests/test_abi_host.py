@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol():
     so = ctypes.CDLL(pic.lib_path())
     missing = [n for n in sorted(declared) if not hasattr(so, n)]
     assert not missing, f"declared but not exported: {missing}"
-    assert pic.pic_abi_version() == 1
+    assert pic.pic_abi_version() == 2
 
 
 def test_binding_covers_every_declared_function():
