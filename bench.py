@@ -302,6 +302,22 @@ class Rig:
         self.slot = 0
         self.moved = 0
         self.shift_segs = None
+        self.attn = None
+        if mode in ("attend", "attend_cache"):
+            hq = 4 * m.num_kv_heads
+            g = torch.Generator(device=device)
+            g.manual_seed(11)
+            q = torch.empty((m.num_layers, len(wl.requests), hq, m.head_dim), dtype=torch.bfloat16, device=device)
+            q.normal_(0.0, 1.0, generator=g)
+            plans, _ = self.plan()
+            aws = pic.pic_attend_workspace_bytes(self.ctx, plans, hq, m.num_layers)
+            self.free(plans)
+            self.attn = {
+                "q": q, "hq": hq, "scale": 1.0 / (m.head_dim ** 0.5),
+                "out": torch.empty((m.num_layers, len(wl.requests), hq, m.head_dim), dtype=torch.float32, device=device),
+                "lse": torch.empty((m.num_layers, len(wl.requests), hq), dtype=torch.float32, device=device),
+                "ws": torch.empty(aws, dtype=torch.uint8, device=device),
+            }
         if mode == "inplace":
             self.shift_segs = self._shift_segments()
             self.ws_shift = torch.empty(pic.pic_rerotate_workspace_bytes(self.ctx, self.shift_segs),
@@ -409,8 +425,14 @@ class Rig:
         self.upload_tables(bt)
         if kernel_events:
             kernel_events[0].record()
-        self.pic.pic_stitch(self.ctx, plans, self.k_pool, self.v_pool, self.k_cache, self.v_cache, self.d_bt,
-                            self.ridx, self.indptr, self.ws)
+        if self.mode != "attend":
+            self.pic.pic_stitch(self.ctx, plans, self.k_pool, self.v_pool, self.k_cache, self.v_cache, self.d_bt,
+                                self.ridx, self.indptr, self.ws)
+        if self.attn is not None:
+            a = self.attn
+            src = self.pic.PIC_ATTEND_FUSED if self.mode == "attend" else self.pic.PIC_ATTEND_CACHE
+            self.pic.pic_attend_decode(self.ctx, plans, src, a["q"], a["scale"], self.k_pool, self.v_pool,
+                                       self.k_cache, self.v_cache, a["out"], a["lse"], a["ws"], sink_bias=-15.0)
         if kernel_events:
             kernel_events[1].record()
         self.free(plans)
@@ -471,7 +493,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pic", choices=["pic", "reference"])
     ap.add_argument("--workload", default="llama31_8b_rag", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--mode", default="stitch", choices=["stitch", "inplace", "mapped"])
+    ap.add_argument("--mode", default="stitch", choices=["stitch", "inplace", "mapped", "attend", "attend_cache"])
+    ap.add_argument("--q-heads", type=int, default=0, help="query heads for the attend modes (default 4 per KV head)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling captures only)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -536,6 +559,12 @@ def main():
     if args.mode == "mapped":
         algo_bytes = rig.moved / args.steps           # bytes actually moved per step
         bpt = algo_bytes / tl
+    elif args.mode in ("attend", "attend_cache"):
+        # attention reads every context K and V row once; the cache path also
+        # stitches first (pool read + cache write)
+        row = wl.model.num_kv_heads * wl.model.head_dim * 2
+        bpt = 2 * row + (4 * row if args.mode == "attend_cache" else 0)
+        algo_bytes = tl * bpt
     else:
         bpt = bytes_per_token_layer(wl.model, args.mode)
         algo_bytes = tl * bpt
@@ -558,12 +587,14 @@ def main():
         cpu = cpu_baseline(wl)
 
     bulk = pic.pic_kernel_variant(rig.ctx, 1 if args.mode == "inplace" else 0) == pic.PIC_VARIANT_BULK_PIPELINE
-    if bulk:
+    if bulk and args.mode not in ("attend", "attend_cache"):
         kname = "k_tma_pipeline<" + ("stitch K+V" if wl.model.kind == "gqa" else "stitch MLA rows") \
             + ">" if args.mode != "inplace" else "k_tma_pipeline<in place>"
     else:
         kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
                  "mapped": "k_rotate_rows<stitch, mapped chunks in place>",
+                 "attend": "k_attend_tiles + k_attend_combine (fused delta-rotation)",
+                 "attend_cache": "k_rotate_rows<stitch> then k_attend_tiles + k_attend_combine",
                  "inplace": "k_rotate_rows<in place>"}[args.mode]
     line = {
         "metric": "stitched KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

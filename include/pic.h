@@ -396,6 +396,49 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_layer
 pic_status pic_recompute_indices(const pic_plan* const* plans, int32_t n_req, int32_t* idx_out,
                                  int32_t* indptr_out, int64_t capacity, int64_t* count);
 
+/* ---------------------------------------------------- decode attention */
+
+#define PIC_ATTEND_FUSED 0 /* chunk tokens read from their sources, keys rotated on load */
+#define PIC_ATTEND_CACHE 1 /* every position read from the request's paged cache          */
+
+/* Workspace bytes of pic_attend_decode for this batch (either source). */
+size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                                  int32_t num_q_heads, int32_t num_layers);
+
+/*
+ * One decode step of grouped-query attention over each request's context,
+ * positions [0, total_tokens) of its plan, for layers [layer_begin,
+ * layer_begin + num_layers):
+ *   s_t = softmax_scale * q . k_t + (sink_bias if t is a pseudo-sink),
+ *   out = sum_t softmax(s)_t v_t,  lse = log sum_t exp(s_t).
+ * PIC_ATTEND_FUSED reads chunk tokens where the chunk lives (pool rows, or the
+ * blocks of a block-resident chunk) and applies R(delta) to each key on the
+ * way from HBM into registers, so the context needs no stitched copy
+ * ([Irminsul] 2.2: the delta-rotation "fused into the FlashMLA kernel",
+ * 4. "fused into the HBM-to-SRAM load path, avoiding extra HBM bandwidth");
+ * positions no chunk covers (inline tokens) and mapped chunks whose rotation
+ * already ran are read from the paged cache through the plan's block table.
+ * PIC_ATTEND_CACHE reads every position from the paged cache (a stitched
+ * context).  A pseudo-sink is one of the first k_nonleading tokens of a chunk
+ * not at position 0, the positions pic_recompute_indices lists for it
+ * ([EPIC] LegoLink "1. Identifying and Neutralizing Pseudo-Sinks"; the listing
+ * adds -15 to those logits); sink_bias 0 disables it.
+ *   q      device bf16 [num_layers][n_req][num_q_heads][head_dim], already
+ *          rotated to the query's position; query head g reads KV head
+ *          g / (num_q_heads / num_kv_heads).
+ *   out    device float [num_layers][n_req][num_q_heads][head_dim].
+ *   lse    device float [num_layers][n_req][num_q_heads] or NULL.
+ * GQA models with head_dim 64 or 128 and 1, 2, 4 or 8 query heads per KV
+ * head; pools and caches in device memory.  The cache's block tables are the
+ * plans' (as pic_build_block_table returned them).
+ */
+pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
+                             const void* q, int32_t num_q_heads, float softmax_scale, float sink_bias,
+                             const void* k_pool, const void* v_pool, int64_t pool_layer_stride_bytes,
+                             const void* k_cache, const void* v_cache, int64_t cache_layer_stride_bytes,
+                             int32_t layer_begin, int32_t num_layers, float* out, float* lse,
+                             void* d_workspace, size_t workspace_bytes, pic_stream_t stream);
+
 /* ---------------------------------------------------------- diagnostics */
 
 /*

@@ -37,6 +37,10 @@ Pin status of each function (what outside fact each is checked against is in
                          carve-out)
 * ``stitch_*`` / ``rerotate_inplace`` pinned end to end against forward RoPE
                          computed at the target position.
+* ``attention_decode`` pinned (uniform scores give the mean value, a dominant
+                         score picks its value, token order does not matter,
+                         shifting query and keys together changes nothing)
+* ``sink_bias``          pinned (the EPIC listing's boundary loop)
 * ``map_request`` / ``apply_mapped`` (virtual block mapping) pinned against the
                          block ids printed on the EPIC runtime figure and
                          against forward RoPE at the mapped positions.
@@ -69,4 +73,6 @@ from .pic_oracle import (  # noqa: F401
     map_request,
     release_request,
     apply_mapped,
+    attention_decode,
+    sink_bias,
 )

@@ -497,3 +497,51 @@ def apply_mapped(k_cache_bits, v_cache_bits, k_pool_bits, v_pool_bits, segs, tab
                     v_out[:, slot, row] = np.asarray(v_pool_bits).view(np.uint16)[:, s.src_rows[t]]
             k_out[:, slot, row] = rotate_rows(src, s.delta, theta, pairing, rope_offset, rope_dim)
     return k_out, v_out
+
+
+# ---------------------------------------------------------------------------
+# decode attention over a stitched context
+# ---------------------------------------------------------------------------
+
+def attention_decode(q, keys, values, scale: float, bias=None):
+    """One decode step of grouped-query attention, in float64.
+
+    q: [Hq][D] (already rotated to the query's position); keys, values:
+    [T][Hkv][D] (keys rotated to their positions); query head g reads KV head
+    g // (Hq / Hkv).  scores = scale * q.k + bias (bias: [T] or None),
+    p = softmax over the T positions, out = sum_t p_t v_t.  Returns
+    (out [Hq][D], log-sum-exp of the scaled scores [Hq]).  The definition of
+    attention the pages rely on (EPIC Guide's listing computes the same
+    softmax(q k^T / sqrt(d)) v in its LegoLink repair).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64)
+    values = np.asarray(values, dtype=np.float64)
+    hq = q.shape[0]
+    hkv = keys.shape[1]
+    group = hq // hkv
+    out = np.empty((hq, values.shape[2]))
+    lse = np.empty(hq)
+    for g in range(hq):
+        h = g // group
+        s = scale * (keys[:, h, :] @ q[g])
+        if bias is not None:
+            s = s + bias
+        m = s.max()
+        e = np.exp(s - m)
+        out[g] = (e[:, None] * values[:, h, :]).sum(axis=0) / e.sum()
+        lse[g] = m + np.log(e.sum())
+    return out, lse
+
+
+def sink_bias(segs, total_tokens: int, k_nonleading: int, bias_value: float):
+    """Per-position logit bias of LegoLink's pseudo-sink suppression: the
+    first k tokens of every chunk not at global position 0 get bias_value
+    (EPIC Guide, LegoLink "1. Identifying and Neutralizing Pseudo-Sinks";
+    the listing subtracts 15 from those logits and leaves boundary 0 alone)."""
+    b = np.zeros(total_tokens)
+    for s in segs:
+        if s.dst_pos == 0:
+            continue
+        b[s.dst_pos:s.dst_pos + min(k_nonleading, s.length)] = bias_value
+    return b

@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libpic.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["pic_host.cpp", "pic_kernels.cu", "pic_kernels_tma.cu", "pic_noalloc.cu"]
+SOURCES = ["pic_host.cpp", "pic_kernels.cu", "pic_kernels_tma.cu", "pic_attention.cu", "pic_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "pic_internal.h"), os.path.join(INCLUDE, "pic.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

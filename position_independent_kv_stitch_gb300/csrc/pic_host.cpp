@@ -616,6 +616,93 @@ void fill_freq(const pic_ctx* ctx, uint8_t* base, const WsLayout& w) {
   std::memcpy(base + w.freq_off, ctx->freq_turns.data(), ctx->freq_turns.size() * sizeof(float2));
 }
 
+// Decode attention: every position [0, total) of each request becomes one
+// token descriptor (where its K/V row is and which delta its key needs), and
+// positions are grouped into tiles of <= kAttnTileTokens tokens with <=
+// kAttnMaxSlots distinct deltas.  fused: chunk tokens are read from their
+// sources (pool rows, block-resident chunk rows) and rotated on load; inline
+// positions and mapped chunks already rotated come from the request's paged
+// cache.  cache: every position from the paged cache, no rotation.
+struct AttnLayout {
+  size_t freq_off, tiles_off, toks_off, reqt_off, partial_off, total;
+  int32_t n_tiles, n_toks;
+};
+
+void attend_tokens(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
+                   int32_t max_slots, std::vector<pic::AttnTile>* tiles, std::vector<pic::AttnTok>* toks,
+                   std::vector<int32_t>* req_tile_begin) {
+  const int32_t bs = ctx->model.block_size;
+  int32_t n_tiles = 0, n_toks = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    const pic_plan* pl = plans[r];
+    if (req_tile_begin) (*req_tile_begin)[r] = n_tiles;
+    // per-position (row, delta, flags) in order
+    std::vector<int32_t> rows(pl->total_tokens), deltas(pl->total_tokens, 0), flags(pl->total_tokens, 0);
+    for (int32_t p = 0; p < pl->total_tokens; ++p) {
+      rows[p] = pl->table[p / bs] * bs + p % bs;
+      flags[p] = pic::kAttnFromCache;
+    }
+    for (const Segment& sg : pl->segs) {
+      for (int32_t t = 0; t < sg.num_tokens; ++t) {
+        const int32_t p = sg.dst_pos + t;
+        if (sg.dst_pos != 0 && t < sg.n_recompute) flags[p] |= pic::kAttnSink;
+        if (source != PIC_ATTEND_FUSED) continue;
+        if (sg.kind == pic::kRunPool) {
+          rows[p] = static_cast<int32_t>(sg.src_tok + t);
+          flags[p] &= ~pic::kAttnFromCache;
+          deltas[p] = sg.delta;
+        } else if (sg.kind == pic::kRunBlocks) {
+          rows[p] = sg.src_blocks[t / bs] * bs + t % bs;
+          deltas[p] = sg.delta;
+        } else if (!pl->applied) {  // mapped chunk whose keys have not moved yet
+          deltas[p] = sg.delta;
+        }
+      }
+    }
+    int32_t p = 0;
+    while (p < pl->total_tokens) {
+      pic::AttnTile T{};
+      T.req = r;
+      T.first_pos = p;
+      T.tok_off = n_toks;
+      while (p < pl->total_tokens && T.n_tok < pic::kAttnTileTokens) {
+        int32_t slot = -1;
+        for (int32_t k = 0; k < T.n_slots; ++k)
+          if (T.deltas[k] == deltas[p]) slot = k;
+        if (slot < 0) {
+          if (T.n_slots == max_slots) break;
+          slot = T.n_slots++;
+          T.deltas[slot] = deltas[p];
+        }
+        if (toks) toks->push_back(pic::AttnTok{rows[p], flags[p] | slot});
+        ++T.n_tok;
+        ++n_toks;
+        ++p;
+      }
+      if (tiles) tiles->push_back(T);
+      ++n_tiles;
+    }
+  }
+  if (req_tile_begin) (*req_tile_begin)[n_req] = n_tiles;
+  if (!tiles && !toks && req_tile_begin) return;
+  (void)n_toks;
+}
+
+AttnLayout attend_layout(const pic_ctx* ctx, int32_t n_tiles, int32_t n_toks, int32_t n_req, int32_t num_q_heads,
+                         int32_t num_layers) {
+  AttnLayout w;
+  w.n_tiles = n_tiles;
+  w.n_toks = n_toks;
+  w.freq_off = pic::align_up(sizeof(WsHeader), pic::kWsAlign);
+  w.tiles_off = pic::align_up(w.freq_off + ctx->freq_turns.size() * sizeof(float2), pic::kWsAlign);
+  w.toks_off = pic::align_up(w.tiles_off + static_cast<size_t>(n_tiles) * sizeof(pic::AttnTile), pic::kWsAlign);
+  w.reqt_off = pic::align_up(w.toks_off + static_cast<size_t>(n_toks) * sizeof(pic::AttnTok), pic::kWsAlign);
+  w.partial_off = pic::align_up(w.reqt_off + (static_cast<size_t>(n_req) + 1) * sizeof(int32_t), pic::kWsAlign);
+  const size_t partial = static_cast<size_t>(num_layers) * n_tiles * num_q_heads * (ctx->model.head_dim + 2) * sizeof(float);
+  w.total = pic::align_up(w.partial_off + partial, pic::kWsAlign);
+  return w;
+}
+
 }  // namespace
 
 // ======================================================================= API
@@ -1210,6 +1297,112 @@ pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n,
   e = pic::launch_cossin(d_deltas, n, static_cast<const float2*>(d_ws),
                          static_cast<int32_t>(ctx->freq_turns.size()), d_out, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cos/sin launch");
+  return ok(ctx);
+}
+
+// ------------------------------------------------------- decode attention
+
+size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                                  int32_t num_q_heads, int32_t num_layers) {
+  if (!ctx || n_req < 0 || (n_req > 0 && !plans) || num_q_heads <= 0 || num_layers <= 0) return 0;
+  int64_t toks = 0;
+  for (int32_t r = 0; r < n_req; ++r) {
+    if (!plans[r]) return 0;
+    toks += plans[r]->total_tokens;
+  }
+  const int32_t slots = pic::attn_slots(num_q_heads / std::max(1, ctx->model.num_kv_heads));
+  std::vector<pic::AttnTile> tiles;
+  attend_tokens(ctx, plans, n_req, PIC_ATTEND_FUSED, slots, &tiles, nullptr, nullptr);
+  std::vector<pic::AttnTile> tiles_c;
+  attend_tokens(ctx, plans, n_req, PIC_ATTEND_CACHE, slots, &tiles_c, nullptr, nullptr);
+  const int32_t nt = static_cast<int32_t>(std::max(tiles.size(), tiles_c.size()));
+  return attend_layout(ctx, nt, static_cast<int32_t>(toks), n_req, num_q_heads, num_layers).total;
+}
+
+pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
+                             const void* q, int32_t num_q_heads, float softmax_scale, float sink_bias,
+                             const void* k_pool, const void* v_pool, int64_t pool_ls, const void* k_cache,
+                             const void* v_cache, int64_t cache_ls, int32_t layer_begin, int32_t num_layers,
+                             float* out, float* lse, void* d_ws, size_t ws_bytes, pic_stream_t stream) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  const pic_model_desc& m = ctx->model;
+  if (m.kind != PIC_KIND_GQA || (m.head_dim != 64 && m.head_dim != 128))
+    return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention covers GQA heads of 64 or 128 dims");
+  if (source != PIC_ATTEND_FUSED && source != PIC_ATTEND_CACHE) return fail(ctx, PIC_ERR_INVALID_ARG, "bad source");
+  if (n_req <= 0 || !plans) return fail(ctx, PIC_ERR_INVALID_ARG, "no requests");
+  for (int32_t r = 0; r < n_req; ++r)
+    if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
+  if (num_q_heads <= 0 || num_q_heads % m.num_kv_heads != 0)
+    return fail(ctx, PIC_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  const int32_t group = num_q_heads / m.num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8)
+    return fail(ctx, PIC_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8");
+  if (layer_begin < 0 || num_layers <= 0 || layer_begin + num_layers > m.num_layers)
+    return fail(ctx, PIC_ERR_RANGE, "layer range outside the model");
+  if (!q || !out || !d_ws || !k_cache || !v_cache) return fail(ctx, PIC_ERR_INVALID_ARG, "null q, out, cache or workspace");
+  if (source == PIC_ATTEND_FUSED && (!k_pool || !v_pool))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "fused attention reads the pool: pass k_pool and v_pool");
+  if (!vectorized_bytes_ok(k_cache) || !vectorized_bytes_ok(v_cache) || (cache_ls & 15) ||
+      (k_pool && !vectorized_bytes_ok(k_pool)) || (v_pool && !vectorized_bytes_ok(v_pool)) || (pool_ls & 15) ||
+      !vectorized_bytes_ok(d_ws))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "pools, caches, strides and workspace must be 16-byte aligned");
+  std::vector<pic::AttnTile> tiles;
+  std::vector<pic::AttnTok> toks;
+  std::vector<int32_t> reqt(static_cast<size_t>(n_req) + 1);
+  attend_tokens(ctx, plans, n_req, source, pic::attn_slots(group), &tiles, &toks, &reqt);
+  for (int32_t r = 0; r < n_req; ++r)
+    if (plans[r]->total_tokens == 0) return fail(ctx, PIC_ERR_RANGE, "plans[%d] has no context to attend", r);
+  const AttnLayout w = attend_layout(ctx, static_cast<int32_t>(tiles.size()), static_cast<int32_t>(toks.size()), n_req,
+                                     num_q_heads, num_layers);
+  if (ws_bytes < w.total) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+
+  DeviceInfo di;
+  pic_status st = current_device(ctx, di);
+  if (st != PIC_OK) return st;
+  const void* bufs[4] = {k_pool, v_pool, k_cache, v_cache};
+  for (int i = 0; i < 4; ++i)
+    if (bufs[i] && residency(bufs[i]) != 0)
+      return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention reads pools and caches from device memory only");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t image = w.partial_off;  // everything before the partial results
+  StagingSlot* sl = nullptr;
+  st = acquire_staging(ctx, di.device, image, &sl);
+  if (st != PIC_OK) return st;
+  uint8_t* base = sl->host;
+  std::memcpy(base + w.freq_off, ctx->freq_turns.data(), ctx->freq_turns.size() * sizeof(float2));
+  std::memcpy(base + w.tiles_off, tiles.data(), tiles.size() * sizeof(pic::AttnTile));
+  std::memcpy(base + w.toks_off, toks.data(), toks.size() * sizeof(pic::AttnTok));
+  std::memcpy(base + w.reqt_off, reqt.data(), reqt.size() * sizeof(int32_t));
+  st = upload_staging(ctx, sl, d_ws, image, s);
+  if (st != PIC_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  pic::AttnParams p{};
+  p.tiles = reinterpret_cast<const pic::AttnTile*>(ws + w.tiles_off);
+  p.n_tiles = static_cast<int32_t>(tiles.size());
+  p.toks = reinterpret_cast<const pic::AttnTok*>(ws + w.toks_off);
+  p.req_tile_begin = reinterpret_cast<const int32_t*>(ws + w.reqt_off);
+  p.n_req = n_req;
+  p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
+  p.q = static_cast<const uint16_t*>(q);
+  p.num_q_heads = num_q_heads;
+  p.n_kv_heads = m.num_kv_heads;
+  p.n_layers = num_layers;
+  p.layer_begin = layer_begin;
+  p.scale = softmax_scale;
+  p.sink_bias = sink_bias;
+  p.k_pool = static_cast<const uint8_t*>(k_pool);
+  p.v_pool = static_cast<const uint8_t*>(v_pool);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.pool_layer_stride = pool_ls;
+  p.cache_layer_stride = cache_ls;
+  p.row_bytes = static_cast<int32_t>(row_bytes_of(m));
+  p.partial = reinterpret_cast<float*>(ws + w.partial_off);
+  p.out = out;
+  p.lse = lse;
+  const cudaError_t e = pic::launch_attend(p, m.pairing, m.head_dim, group, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "attention launch");
   return ok(ctx);
 }
 

@@ -94,6 +94,60 @@ size_t tma_smem_bytes(const TmaConfig& c);
 cudaError_t launch_tma(const KernelParams& p, const TmaConfig& c, int mode, int pairing, int rope_dim,
                        int grid, cudaStream_t stream);
 
+// ---- decode attention over a stitched context (pic_attention.cu)
+constexpr int kAttnTileTokens = 128;   // positions per tile (one thread each)
+constexpr int kAttnMaxSlots = 16;      // distinct deltas per tile (8 when G = 8)
+// Distinct deltas a tile may hold for G query heads per KV head: the rotated
+// queries of all of them stay in static shared memory (<= 48 KB).
+__host__ __device__ constexpr int attn_slots(int group) { return group >= 8 ? 8 : kAttnMaxSlots; }
+constexpr int kAttnMaxCombine = 1024;  // tiles whose weights the combine keeps on chip
+constexpr int32_t kAttnFromCache = 1 << 8;  // AttnTok.flags: row is a paged-cache row
+constexpr int32_t kAttnSink = 1 << 9;       // AttnTok.flags: LegoLink pseudo-sink position
+
+struct AttnTile {
+  int32_t req;
+  int32_t first_pos;
+  int32_t n_tok;
+  int32_t n_slots;
+  int32_t tok_off;
+  int32_t pad[3];
+  int32_t deltas[kAttnMaxSlots];
+};
+static_assert(sizeof(AttnTile) == 96, "AttnTile layout");
+
+struct AttnTok {
+  int32_t row;    // pool token row or absolute cache row (block * bs + row)
+  int32_t flags;  // delta slot (low 8 bits) | kAttnFromCache | kAttnSink
+};
+
+struct AttnParams {
+  const AttnTile* tiles;
+  int32_t n_tiles;
+  const AttnTok* toks;
+  const int32_t* req_tile_begin;  // [n_req + 1]
+  int32_t n_req;
+  const float2* freq;
+  const uint16_t* q;              // bf16 [n_layers][n_req][num_q_heads][D]
+  int32_t num_q_heads;
+  int32_t n_kv_heads;
+  int32_t n_layers;
+  int32_t layer_begin;
+  float scale;
+  float sink_bias;
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  int64_t pool_layer_stride;
+  int64_t cache_layer_stride;
+  int32_t row_bytes;
+  float* partial;                 // [n_layers][n_tiles][n_kv_heads][group][D + 2]
+  float* out;                     // [n_layers][n_req][num_q_heads][D]
+  float* lse;                     // [n_layers][n_req][num_q_heads] or null
+};
+
+cudaError_t launch_attend(const AttnParams& p, int pairing, int head_dim, int group, cudaStream_t stream);
+
 // Launchers; each returns the launch's cudaError_t.  `grid` is the number of
 // CTAs (persistent, grid-stride over units).
 cudaError_t launch_stitch_gqa(const KernelParams& p, int pairing, int head_dim, int grid,

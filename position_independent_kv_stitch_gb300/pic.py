@@ -31,6 +31,7 @@ PIC_DEV_BAD_BLOCK = 0x1
 PIC_DEV_TIMEOUT = 0x2
 PIC_VARIANT_REGISTERS, PIC_VARIANT_BULK_PIPELINE = 0, 1
 PIC_SEG_COPY_POOL, PIC_SEG_COPY_BLOCKS, PIC_SEG_MAPPED = 0, 1, 2
+PIC_ATTEND_FUSED, PIC_ATTEND_CACHE = 0, 1
 
 
 class PicError(RuntimeError):
@@ -99,6 +100,10 @@ _SIGNATURES = {
     "pic_recompute_indices": (ctypes.c_int, [_P(_c_void_p), _i32, _P(_i32), _P(_i32), _i64, _P(_i64)]),
     "pic_query_device_status": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _P(_u32)]),
     "pic_kernel_variant": (_i32, [_c_void_p, _i32]),
+    "pic_attend_workspace_bytes": (_sz, [_c_void_p, _P(_c_void_p), _i32, _i32, _i32]),
+    "pic_attend_decode": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _i32, _c_void_p, _i32, ctypes.c_float,
+                                         ctypes.c_float, _c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p, _i64,
+                                         _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "pic_rotation_cossin": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _sz, _c_void_p]),
 }
 
@@ -431,6 +436,28 @@ def pic_query_device_status(ctx, workspace, stream=None) -> int:
     if st != PIC_OK:
         raise PicError(st, load().pic_last_error(ctx).decode())
     return out.value
+
+
+def pic_attend_workspace_bytes(ctx, plans, num_q_heads: int, num_layers: int) -> int:
+    return int(load().pic_attend_workspace_bytes(ctx, _plan_array(plans), len(plans), int(num_q_heads),
+                                                 int(num_layers)))
+
+
+def pic_attend_decode(ctx, plans, source, q, softmax_scale, k_pool, v_pool, k_cache, v_cache, out, lse=None,
+                      workspace=None, sink_bias=0.0, layer_begin=0, stream=None):
+    """One decode step of attention over each plan's context.  q: CUDA bf16
+    [num_layers][n_req][num_q_heads][head_dim]; out: CUDA float32 of the same
+    shape; lse: CUDA float32 [num_layers][n_req][num_q_heads] or None."""
+    num_layers, n_req, hq = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    if n_req != len(plans):
+        raise ValueError("q holds one row per plan")
+    st = load().pic_attend_decode(ctx, _plan_array(plans), len(plans), int(source), _ptr(q), hq,
+                                  float(softmax_scale), float(sink_bias), _ptr(k_pool), _ptr(v_pool),
+                                  _layer_stride_bytes(k_pool), _ptr(k_cache), _ptr(v_cache),
+                                  _layer_stride_bytes(k_cache), int(layer_begin), num_layers, _ptr(out), _ptr(lse),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+    _check(st, ctx)
 
 
 def pic_kernel_variant(ctx, mode: int) -> int:
