@@ -412,12 +412,13 @@ size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* pla
  *   s_t = softmax_scale * q . k_t + (sink_bias if t is a pseudo-sink),
  *   out = sum_t softmax(s)_t v_t,  lse = log sum_t exp(s_t).
  * PIC_ATTEND_FUSED reads chunk tokens where the chunk lives (pool rows, or the
- * blocks of a block-resident chunk) and applies R(delta) to each key on the
- * way from HBM into registers, so the context needs no stitched copy
- * ([Irminsul] 2.2: the delta-rotation "fused into the FlashMLA kernel",
- * 4. "fused into the HBM-to-SRAM load path, avoiding extra HBM bandwidth");
- * positions no chunk covers (inline tokens) and mapped chunks whose rotation
- * already ran are read from the paged cache through the plan's block table.
+ * blocks of a block-resident chunk) and applies the chunk's R(delta) on the
+ * way from HBM to the SMs, so the context needs no stitched copy ([Irminsul]
+ * 2.2 and 4: the rotation belongs in the attention kernel's load path, where
+ * it costs no HBM traffic).  The kernel rotates the query by R(-delta) once
+ * per delta instead of every key, which gives the same scores.  Positions no
+ * chunk covers (inline tokens) and mapped chunks whose rotation already ran
+ * are read from the paged cache through the plan's block table.
  * PIC_ATTEND_CACHE reads every position from the paged cache (a stitched
  * context).  A pseudo-sink is one of the first k_nonleading tokens of a chunk
  * not at position 0, the positions pic_recompute_indices lists for it
@@ -425,12 +426,19 @@ size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* pla
  * adds -15 to those logits); sink_bias 0 disables it.
  *   q      device bf16 [num_layers][n_req][num_q_heads][head_dim], already
  *          rotated to the query's position; query head g reads KV head
- *          g / (num_q_heads / num_kv_heads).
+ *          g / (num_q_heads / num_kv_heads).  16-byte aligned.
  *   out    device float [num_layers][n_req][num_q_heads][head_dim].
  *   lse    device float [num_layers][n_req][num_q_heads] or NULL.
- * GQA models with head_dim 64 or 128 and 1, 2, 4 or 8 query heads per KV
- * head; pools and caches in device memory.  The cache's block tables are the
- * plans' (as pic_build_block_table returned them).
+ * GQA models with head_dim 64 or 128, at most 8 KV heads or a multiple of 8,
+ * and 1, 2, 4 or 8 query heads per KV head; pools and caches in device
+ * memory, 16-byte aligned.  The cache's block tables are the plans' (as
+ * pic_build_block_table returned them).  Two launches: a persistent kernel
+ * streams the context through shared memory and leaves per-range softmax
+ * records in the workspace, a second merges them into out and lse.  Errors:
+ * PIC_ERR_UNSUPPORTED for other geometries or host-resident buffers,
+ * PIC_ERR_RANGE for an empty context or a layer range outside the model,
+ * PIC_ERR_CAPACITY for a short workspace; a bounded wait that gave up on the
+ * device sets PIC_DEV_TIMEOUT in the workspace's status word.
  */
 pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
                              const void* q, int32_t num_q_heads, float softmax_scale, float sink_bias,

@@ -1,309 +1,569 @@
 // Decode attention over a stitched context, with the delta-rotation fused into
-// the key loads (GQA, sm_103a).
+// the key path (GQA, sm_103a).
 //
 // Irminsul: MLA-Native Position-Independent Caching for Agentic LLM Serving,
 // 2.2 "delta-Rotation Rule" and 4. Results: the rotation R(delta) k can be
-// applied on the HBM -> on-chip load path of attention instead of writing a
-// rotated copy, so no extra HBM traffic is spent.  Here every context
-// position is read from where it lives -- a chunk token from its source rows
-// (pool, or the blocks of a block-resident chunk) with its key rotated by the
-// chunk's delta in registers, an inline token from the request's paged cache
-// -- and one decode step of attention runs over them:
+// applied on the HBM -> on-chip path of attention instead of writing a rotated
+// copy, so no extra HBM traffic is spent.  Every context position is read from
+// where it lives -- a chunk token from its source rows (pool, or the blocks of
+// a block-resident chunk), an inline token from the request's paged cache --
+// and one decode step of attention runs over them:
 //   scores = scale * q . R(delta) k + bias,  p = softmax,  out = sum p v
 // (bias: LegoLink's pseudo-sink suppression, EPIC Guide: Position-Independent
 // Caching for LLM Serving, LegoLink "1. Identifying and Neutralizing
 // Pseudo-Sinks" -- the first k tokens of every chunk not at position 0 get a
-// negative logit offset).
+// negative logit offset).  q . R(delta) k = (R(-delta) q) . k because R is
+// orthogonal, so the query is rotated once per delta and keys are used as
+// stored.
 //
-// Flash-decoding split: one CTA per (tile of <= 128 positions, KV head,
-// layer) computes the tile's max, sum of exponentials and weighted value sum
-// for the query heads of its group; a second kernel merges the tiles.  The work is memory-bound (one pass over K and V, a few FMAs per
-// byte) and runs on CUDA cores; tensor cores would idle on a 1-token query.
+// Structure (one pass over K and V: HBM-bound):
+//   * Persistent CTAs, each owning a contiguous range of (layer, stage)
+//     units; a stage is <= 16 consecutive positions of one request that share
+//     one delta.  Warp HB (the producer) copies every position's K and V rows
+//     (all heads of the group) into a ring of shared-memory slots with
+//     cp.async.bulk, one row per copy into a row pitch padded by 16 bytes (so
+//     the eight rows an ldmatrix reads fall in distinct banks), tracked by
+//     mbarriers; its descriptor loads run two stages ahead.
+//   * Warp h < HB (a consumer) owns KV head h and keeps an online softmax per
+//     query head across the CTA's stages of one key (request x head group),
+//     flushed to a record when the range leaves the key; a second kernel
+//     merges the records of each key (flash-decoding).
+//   * The two products of a stage are small matrix products, run on the
+//     tensor cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate):
+//     S = Q K^T (rows: query heads, 16 positions) and O += P V.  Tensor cores
+//     are used here to cut the instruction count per byte (a 16-position
+//     stage costs ~150 instructions per warp instead of ~1,000 FMA-path
+//     ones), not for their FLOPs.  Q and P are fp32 values; each is split
+//     into bf16 hi + lo parts placed in rows g and g + 8 of the same A tile,
+//     so one product carries both and the sum of the two rows keeps about
+//     16 significant bits (K and V are bf16 already, products accumulate in
+//     fp32).
+// Every mbarrier wait is bounded: on timeout the warp raises PIC_DEV_TIMEOUT,
+// the producer waits (bounded) for the copies it issued, and the CTA exits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cfloat>
 #include <cstdint>
 
+#include "pic_device.cuh"
 #include "pic_internal.h"
 
 namespace pic {
 namespace {
 
-constexpr int kAttnThreads = kAttnTileTokens;  // one thread per position of a tile
+using namespace dev;
 
-__device__ __forceinline__ void shift_cossin(int delta, float2 f, float& c, float& s) {
-  const float d = static_cast<float>(delta);   // exact for |delta| < 2^24
-  const float p = __fmul_rn(d, f.x);
-  const float e = __fmaf_rn(d, f.x, -p);       // d * hi == p + e exactly (TwoProduct)
-  const float r = __fsub_rn(p, rintf(p));      // exact, |r| <= 1/2 turn
-  const float t = __fadd_rn(r, __fmaf_rn(d, f.y, e));
-  sincospif(2.0f * t, &s, &c);
-}
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ uint32_t vword(const uint4& v, int w) {
-  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr size_t kSmemBudget = 227 * 1024;  // dynamic shared memory per CTA on sm_103a
+constexpr int kMetaFirst = 1;               // stage opens its key in this CTA
+constexpr int kMetaLast = 2;                // stage closes its key in this CTA
+
+struct StageMeta {  // written by the producer before the stage's arrive
+  int32_t layer;    // local layer
+  int32_t key;
+  int32_t delta;
+  int32_t n_tok;
+  uint32_t sink_mask;
+  int32_t flags;
+  int32_t pad[2];
+};
+static_assert(sizeof(StageMeta) == 32, "StageMeta layout");
+
+constexpr int ST = kAttnStageTokens;
+
+// The producer's descriptor rings: stage descriptors of units u .. u + 4
+// and token rows of units u .. u + 2, filled by cp.async so that the loads
+// stay in flight several stages ahead without holding registers.
+struct ProdState {
+  AttnStage desc[8];      // unit v at [v & 7]
+  AttnTok tok[4][32];     // unit v at [v & 3], one row per lane
+};
+static_assert(sizeof(ProdState) == 1152, "ProdState layout");
+constexpr int kDescAhead = 4;  // descriptors are requested this many units ahead
+
+// Shared memory: barriers | metas | producer rings | per consumer warp (raw
+// q bf16 [G][D], rotated q fp32 [G][D]) | ring of stages (ST K rows, then ST
+// V rows).
+struct SmemLayout {
+  size_t meta, prod, warp, warp_bytes, qrot, ring, row_pitch, stage_bytes, total;
+};
+__host__ __device__ inline SmemLayout smem_layout(int D, int G, int HB, int ring) {
+  SmemLayout L{};
+  L.meta = 2 * kAttnMaxStages * sizeof(uint64_t);
+  L.prod = L.meta + kAttnMaxStages * sizeof(StageMeta);
+  L.warp = (L.prod + sizeof(ProdState) + 127) / 128 * 128;
+  L.qrot = static_cast<size_t>(G) * D * 2;
+  L.warp_bytes = (L.qrot + static_cast<size_t>(G) * D * 4 + 127) / 128 * 128;
+  L.ring = (L.warp + HB * L.warp_bytes + 127) / 128 * 128;
+  L.row_pitch = static_cast<size_t>(HB) * D * 2 + 16;
+  L.stage_bytes = 2 * ST * L.row_pitch;
+  L.total = L.ring + ring * L.stage_bytes;
+  return L;
 }
 
-// Block-wide max / sum over the threads of the CTA through shared scratch.
-__device__ __forceinline__ float block_max(float x, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-  __syncthreads();
-  float m = red[0];
-#pragma unroll
-  for (int w = 1; w < kAttnThreads / 32; ++w) m = fmaxf(m, red[w]);
-  __syncthreads();
-  return m;
+// ------------------------------------------------------------- tensor cores
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
-__device__ __forceinline__ float block_sum(float x, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-  __syncthreads();
-  float t = 0.0f;
-#pragma unroll
-  for (int w = 0; w < kAttnThreads / 32; ++w) t += red[w];
-  __syncthreads();
-  return t;
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// c += A B for one 16x8x16 tile: A row-major bf16 (4 regs), B column-major bf16 (2 regs)
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (x, y) as bf16 pairs: hi = RN(x, y), lo = RN of what hi left out
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// grid: (tiles, kv heads, layers).  G = query heads per KV head, D = head dim.
-//
-// The rotation is applied to the query, not the keys: q . R(d) k =
-// (R(-d) q) . k, so each tile rotates its G query heads once per distinct
-// delta (<= kAttnMaxSlots) into shared memory and every key is consumed as
-// stored.  Thread t owns token t of the tile: it loads the token's head row
-// (2*D bytes) and dots it with the rotated query of its delta, read as
-// 16-byte broadcasts.  After the tile's softmax statistics, VT = D/8 threads
-// share each value row for the weighted sum.  No shuffle or barrier sits in
-// a divergent region: every thread of the CTA runs the same reductions.
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// unit v's stage descriptor (stage j of its layer; lane 0) and, once that
+// is in shared memory, its token rows (one per lane)
+__device__ __forceinline__ void fetch_desc(const AttnParams& P, ProdState* ps, int64_t v, int j, int lane) {
+  if (lane == 0) cp_async16(&ps->desc[v & 7], P.stages + j);
+}
+__device__ __forceinline__ void fetch_toks(const AttnParams& P, ProdState* ps, int64_t v, int lane) {
+  const AttnStage& d = ps->desc[v & 7];
+  if (lane < d.n_tok) cp_async8(&ps->tok[v & 3][lane], P.toks + d.tok_off + lane);
+}
+// (stage, layer) of the unit k units after (j, layer)
+__device__ __forceinline__ int advance_stage(int j, int k, int n_stages) {
+  j += k;
+  while (j >= n_stages) j -= n_stages;
+  return j;
+}
+
+// grid: persistent CTAs; block: 32 * (HB + 1) threads.
 template <int PAIRING, int D, int G>
-__global__ void __launch_bounds__(kAttnThreads) k_attend_tiles(const AttnParams P) {
+__global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const AttnParams P) {
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr int HALF = D / 2;
-  constexpr int VPR = D / 8;              // 16-B vectors per head row
-  constexpr int VT = VPR;                 // value phase: threads per row
-  constexpr int VG = kAttnThreads / VT;   // value phase: rows handled at once
-  static_assert(kAttnThreads % VT == 0 && 32 % VT == 0, "value threads must tile a warp");
+  constexpr int KS = D / 16;   // k-steps of Q K^T
+  constexpr int NT = D / 8;    // n-tiles of P V
+  constexpr int BLK = attn_block_floats(G, D);
 
-  // The rotated queries are dead once the scores are computed (the softmax
-  // reductions' barriers separate the two uses), so the per-warp value sums
-  // reuse their shared memory.
-  constexpr int QROT = attn_slots(G) * G * D;
-  constexpr int PART = (kAttnThreads / 32) * G * D;
-  __shared__ __align__(16) float buf[QROT > PART ? QROT : PART];
-  float (*q_rot)[G][D] = reinterpret_cast<float (*)[G][D]>(buf);
-  float (*part)[G][D] = reinterpret_cast<float (*)[G][D]>(buf);
-  __shared__ float p_s[kAttnThreads][G];
-  __shared__ AttnTok tok_s[kAttnThreads];
-  __shared__ float red[kAttnThreads / 32];
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int HB = P.heads_per_cta;
+  const int NS = P.ring;
+  const SmemLayout L = smem_layout(D, G, HB, NS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kAttnMaxStages;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
+  uint8_t* ring = smem + L.ring;
+  const size_t srow = static_cast<size_t>(HB) * D * 2;  // bytes of one position's rows
+  const uint32_t pitch = static_cast<uint32_t>(L.row_pitch);
 
-  const int tile = blockIdx.x;
-  const int h = blockIdx.y;
-  const int layer = P.layer_begin + blockIdx.z;
-  const AttnTile T = P.tiles[tile];
-  const int tid = threadIdx.x;
-  const bool have = tid < T.n_tok;
-  if (have) tok_s[tid] = P.toks[T.tok_off + tid];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = P.n_units, N = gridDim.x;
+  const int64_t u_begin = U * blockIdx.x / N, u_end = U * (blockIdx.x + 1) / N;
 
-  // ---- R(-delta) q for every distinct delta of the tile
-  const uint16_t* qg = P.q + ((static_cast<int64_t>(blockIdx.z) * P.n_req + T.req) * P.num_q_heads + h * G) * D;
-  for (int i = tid; i < T.n_slots * G * HALF; i += kAttnThreads) {
-    const int slot = i / (G * HALF), g = (i / HALF) % G, f = i % HALF;
-    const int a = NEOX ? f : 2 * f, b = NEOX ? f + HALF : 2 * f + 1;
-    const float qa = __uint_as_float(static_cast<uint32_t>(qg[g * D + a]) << 16);
-    const float qb = __uint_as_float(static_cast<uint32_t>(qg[g * D + b]) << 16);
-    float c = 1.0f, s = 0.0f;
-    if (T.deltas[slot] != 0) shift_cossin(T.deltas[slot], __ldg(P.freq + f), c, s);
-    q_rot[slot][g][a] = qa * c + qb * s;        // R(-delta): rotate backwards
-    q_rot[slot][g][b] = qb * c - qa * s;
+  // Rows past a stage's positions keep what an earlier stage left there; the
+  // ring starts zeroed so that they always hold finite values (their
+  // probabilities are 0, and 0 * v must stay 0 in the tensor-core sums).
+  for (size_t i = threadIdx.x; i < static_cast<size_t>(NS) * L.stage_bytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], HB);
+    }
+    fence_mbar_init();
   }
+  fence_proxy_async_smem();  // the zeros are ordered before the bulk copies into the ring
   __syncthreads();
 
-  // ---- scores: thread t owns token t of the tile
-  float sc[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) sc[g] = -FLT_MAX;
-  if (have) {
-    const AttnTok tk = tok_s[tid];
-    const bool from_cache = (tk.flags & kAttnFromCache) != 0;
-    const uint8_t* base = from_cache ? P.k_cache + layer * P.cache_layer_stride
-                                     : P.k_pool + layer * P.pool_layer_stride;
-    const uint8_t* row = base + static_cast<int64_t>(tk.row) * P.row_bytes + h * (D * 2);
-    uint4 kv[VPR];
-#pragma unroll
-    for (int v = 0; v < VPR; ++v) kv[v] = *reinterpret_cast<const uint4*>(row + v * 16);
-    const int slot = tk.flags & 0xff;
-    float dot[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) dot[g] = 0.0f;
-#pragma unroll
-    for (int v = 0; v < VPR; ++v) {
-      float kf[8];
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        kf[2 * w] = bf_lo(vword(kv[v], w));
-        kf[2 * w + 1] = bf_hi(vword(kv[v], w));
+  if (warp == HB) {
+    // ------------------------------------------------------------ producer
+    // Descriptors run ahead: each iteration requests unit u + 4's stage and
+    // unit u + 2's token rows (whose stage arrived two iterations ago), and
+    // waits only for the requests of two iterations ago.
+    ProdState* ps = reinterpret_cast<ProdState*>(smem + L.prod);
+    const int n_st = P.n_stages;
+    int j = static_cast<int>(u_begin % n_st);       // stage of unit u within its layer
+    int layer = static_cast<int>(u_begin / n_st);
+    for (int k = 0; k < kDescAhead && u_begin + k < u_end; ++k)
+      fetch_desc(P, ps, u_begin + k, advance_stage(j, k, n_st), lane);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    for (int k = 0; k < 2 && u_begin + k < u_end; ++k) fetch_toks(P, ps, u_begin + k, lane);
+    cp_async_commit();
+    cp_async_wait<0>();
+    // per-layer bases of the four source tensors
+    int base_layer = -1;
+    const uint8_t *kp = nullptr, *vp = nullptr, *kc = nullptr, *vc = nullptr;
+    int prev_layer = -1, prev_key = -1;
+    // Unit u is prepared (its meta, this lane's source rows) before its slot
+    // frees up, so a released slot is refilled with a handful of
+    // instructions.  The unit's rows arrived two iterations ago, the stage
+    // after it three.
+    StageMeta pm{};
+    int pn = 0;
+    const uint8_t* pks = nullptr;
+    const uint8_t* pvs = nullptr;
+    auto prepare = [&](int64_t u) {
+      cp_async_wait<1>();
+      __syncwarp();
+      const AttnStage cur = ps->desc[u & 7];
+      const AttnStage nx = ps->desc[(u + 1) & 7];
+      pm.layer = layer;
+      pm.key = cur.key;
+      pm.delta = cur.delta;
+      pm.n_tok = cur.n_tok;
+      pm.sink_mask = cur.sink_mask;
+      pm.flags = 0;
+      if (layer != prev_layer || cur.key != prev_key) pm.flags |= kMetaFirst;
+      if (u + 1 == u_end || j + 1 == n_st || nx.key != cur.key) pm.flags |= kMetaLast;
+      prev_layer = layer;
+      prev_key = cur.key;
+      if (layer != base_layer) {
+        const int64_t l_abs = P.layer_begin + layer;
+        kp = P.k_pool + l_abs * P.pool_layer_stride;
+        vp = P.v_pool + l_abs * P.pool_layer_stride;
+        kc = P.k_cache + l_abs * P.cache_layer_stride;
+        vc = P.v_cache + l_abs * P.cache_layer_stride;
+        base_layer = layer;
       }
+      pn = cur.n_tok;
+      if (lane < pn) {
+        const AttnTok tok = ps->tok[u & 3][lane];
+        const bool from_cache = (tok.flags & kAttnFromCache) != 0;
+        const int64_t off = static_cast<int64_t>(tok.row) * P.row_bytes +
+                            static_cast<int64_t>(cur.key % P.head_groups) * srow;
+        pks = (from_cache ? kc : kp) + off;
+        pvs = (from_cache ? vc : vp) + off;
+      }
+    };
+    prepare(u_begin);
+    int64_t it = 0;
+    bool failed = false;
+    int slot = 0;
+    uint32_t round = 0;   // how many times the ring has wrapped
+    for (int64_t u = u_begin; u < u_end; ++u, ++it) {
+      // every lane polls; the warp leaves together if any lane gave up
+      if (round > 0 && !__all_sync(kFullMask, mbar_wait_bounded(&empty[slot], (round - 1) & 1u))) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) meta[slot] = pm;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(2 * pn * srow));
+      __syncwarp();
+      if (lane < pn) {
+        // one copy per position and tensor, into the padded row pitch
+        uint8_t* kd = ring + slot * L.stage_bytes + lane * L.row_pitch;
+        bulk_load(kd, pks, static_cast<uint32_t>(srow), &full[slot]);
+        bulk_load(kd + ST * L.row_pitch, pvs, static_cast<uint32_t>(srow), &full[slot]);
+      }
+      // ring entries being refilled held units u - 4 (stage) and u - 2 (rows): both done
+      if (u + kDescAhead < u_end) fetch_desc(P, ps, u + kDescAhead, advance_stage(j, kDescAhead, n_st), lane);
+      if (u + 2 < u_end) fetch_toks(P, ps, u + 2, lane);
+      cp_async_commit();
+      if (j + 1 == n_st) {
+        j = 0;
+        ++layer;
+      } else {
+        ++j;
+      }
+      if (++slot == NS) {
+        slot = 0;
+        ++round;
+      }
+      if (u + 1 < u_end) prepare(u + 1);
+    }
+    if (failed) {
+      if (lane == 0) atomicOr(P.status, kDevTimeout);
+      // wait (bounded) for every copy this warp issued before leaving
+      const int64_t issued = it;
+      for (int64_t k = (issued > NS ? issued - NS : 0); k < issued; ++k)
+        mbar_wait_bounded(&full[k % NS], static_cast<uint32_t>((k / NS) & 1));
+    }
+    cp_async_wait<0>();  // no descriptor copy may outlive the CTA
+    return;
+  }
+  if (warp > HB) return;
+
+  // -------------------------------------------------------------- consumer
+  const int h = warp;              // KV head within the group
+  const int g = lane >> 2;         // query-head row of the fragments (rows g and g + 8)
+  const int tq = lane & 3;         // column pair within the fragments
+  const bool row_live = g < G;
+  uint8_t* wbuf = smem + L.warp + h * L.warp_bytes;
+  uint16_t* q_raw = reinterpret_cast<uint16_t*>(wbuf);
+  float* q_rot = reinterpret_cast<float*>(wbuf + L.qrot);
+  // ldmatrix row addresses of this lane: K (non-transposed) and V (transposed)
+  const int mi = lane >> 3, ri = lane & 7;
+  const uint32_t k_lane = static_cast<uint32_t>((ri + ((mi & 2) ? 8 : 0)) * pitch + h * D * 2 + (mi & 1) * 16);
+  const uint32_t v_lane = static_cast<uint32_t>((ri + ((mi & 1) ? 8 : 0)) * pitch + h * D * 2 + (mi & 2) * 8);
+  const uint32_t ring_u32 = smem_u32(ring);
+
+  float o[NT][4];
+  uint32_t qa[KS][4];
+  float m_run = -FLT_MAX, l_part = 0.0f;
+  int cur_delta = 0;
+  bool have_rot = false;
+  int slot = 0;
+  uint32_t round = 0;
+  for (int64_t u = u_begin; u < u_end; ++u) {
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&full[slot], round & 1u))) {
+      if (lane == 0) atomicOr(P.status, kDevTimeout);
+      return;
+    }
+    const StageMeta m = meta[slot];
+    if (m.flags & kMetaFirst) {
+      m_run = -FLT_MAX;
+      l_part = 0.0f;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float4 q0 = *reinterpret_cast<const float4*>(&q_rot[slot][g][v * 8]);
-        const float4 q1 = *reinterpret_cast<const float4*>(&q_rot[slot][g][v * 8 + 4]);
-        dot[g] += kf[0] * q0.x + kf[1] * q0.y + kf[2] * q0.z + kf[3] * q0.w +
-                  kf[4] * q1.x + kf[5] * q1.y + kf[6] * q1.z + kf[7] * q1.w;
+      for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
+      // this head's G query rows, bf16, contiguous
+      const int hg = m.key % P.head_groups;
+      const int req = m.key / P.head_groups;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(
+          P.q + ((static_cast<int64_t>(m.layer) * P.n_req + req) * P.num_q_heads + (hg * HB + h) * G) * D);
+      for (int i = lane; i < G * D / 8; i += 32) reinterpret_cast<uint4*>(q_raw)[i] = __ldg(qsrc + i);
+      have_rot = false;
+      __syncwarp();
+    }
+    if (!have_rot || m.delta != cur_delta) {
+      // R(-delta) q: each lane takes frequencies f = lane, lane + 32, ...
+      for (int f = lane; f < HALF; f += 32) {
+        float cs = 1.0f, sn = 0.0f;
+        if (m.delta != 0) shift_cossin(m.delta, __ldg(P.freq + f), cs, sn);
+        const int a = NEOX ? f : 2 * f, b = NEOX ? f + HALF : 2 * f + 1;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          const float qa_ = __uint_as_float(static_cast<uint32_t>(q_raw[gg * D + a]) << 16);
+          const float qb_ = __uint_as_float(static_cast<uint32_t>(q_raw[gg * D + b]) << 16);
+          q_rot[gg * D + a] = qa_ * cs + qb_ * sn;
+          q_rot[gg * D + b] = qb_ * cs - qa_ * sn;
+        }
+      }
+      __syncwarp();
+      // A fragments of [q_hi; q_lo]: row g holds hi, row g + 8 lo
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        if (row_live) {
+          const float2 x = *reinterpret_cast<const float2*>(q_rot + g * D + 16 * kk + 2 * tq);
+          const float2 y = *reinterpret_cast<const float2*>(q_rot + g * D + 16 * kk + 8 + 2 * tq);
+          split_bf16x2(x.x, x.y, qa[kk][0], qa[kk][1]);
+          split_bf16x2(y.x, y.y, qa[kk][2], qa[kk][3]);
+        } else {
+          qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
+        }
+      }
+      __syncwarp();
+      cur_delta = m.delta;
+      have_rot = true;
+    }
+
+    const uint32_t kbase = ring_u32 + static_cast<uint32_t>(slot * L.stage_bytes);
+    const uint32_t vbase = kbase + ST * pitch;
+    // ---- S = [q_hi; q_lo] K^T over the stage's 16 positions (two n-tiles)
+    // (even and odd k-steps accumulate separately: two short dependency chains)
+    float s0[2][4] = {}, s1[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kbase + k_lane + kk * 32, b0, b1, b2, b3);
+      mma_bf16(s0[kk & 1], qa[kk], b0, b1);
+      mma_bf16(s1[kk & 1], qa[kk], b2, b3);
+    }
+    // this lane's scores: head g, positions 2tq, 2tq + 1, 8 + 2tq, 9 + 2tq
+    float sc[4] = {(s0[0][0] + s0[0][2]) + (s0[1][0] + s0[1][2]), (s0[0][1] + s0[0][3]) + (s0[1][1] + s0[1][3]),
+                   (s1[0][0] + s1[0][2]) + (s1[1][0] + s1[1][2]), (s1[0][1] + s1[0][3]) + (s1[1][1] + s1[1][3])};
+    float mt = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = (i < 2 ? 0 : 8) + 2 * tq + (i & 1);
+      const bool live = row_live && t < m.n_tok;
+      const float bias = ((m.sink_mask >> t) & 1u) ? P.sink_log2 : 0.0f;
+      sc[i] = live ? sc[i] * P.scale_log2 + bias : -FLT_MAX;
+      mt = fmaxf(mt, sc[i]);
+    }
+    mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 2));
+    const float m_new = fmaxf(m_run, mt);
+    const float alpha = exp2f(m_run - m_new);
+    float p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = sc[i] > -FLT_MAX ? exp2f(sc[i] - m_new) : 0.0f;
+    l_part = l_part * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+    m_run = m_new;
+    // A fragment of [p_hi; p_lo] over the 16 positions
+    uint32_t pa[4];
+    split_bf16x2(p[0], p[1], pa[0], pa[1]);
+    split_bf16x2(p[2], p[3], pa[2], pa[3]);
+
+    // ---- O = alpha O + [p_hi; p_lo] V (alpha is 1 once the running max settles)
+    if (!__all_sync(kFullMask, alpha == 1.0f)) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        o[j][0] *= alpha;
+        o[j][1] *= alpha;
+        o[j][2] *= alpha;
+        o[j][3] *= alpha;
       }
     }
-    const float bias = (tk.flags & kAttnSink) ? P.sink_bias : 0.0f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) sc[g] = dot[g] * P.scale + bias;
-  }
-
-  // ---- tile softmax statistics per query head
-  float m_g[G], l_g[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m_g[g] = block_max(sc[g], red);
-    const float pv = have ? __expf(sc[g] - m_g[g]) : 0.0f;
-    p_s[tid][g] = pv;
-    l_g[g] = block_sum(pv, red);
-  }
-  __syncthreads();
-
-  // ---- weighted value sum: VT threads per row, VG rows at a time
-  const int vv = tid % VT;          // this thread's 16-B vector of the row
-  const int r0 = tid / VT;
-  float acc[G][8];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.0f;
-  for (int t = r0; t < T.n_tok; t += VG) {
-    const AttnTok tk = tok_s[t];
-    const bool from_cache = (tk.flags & kAttnFromCache) != 0;
-    const uint8_t* base = from_cache ? P.v_cache + layer * P.cache_layer_stride
-                                     : P.v_pool + layer * P.pool_layer_stride;
-    const uint4 x = *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(tk.row) * P.row_bytes +
-                                                    h * (D * 2) + vv * 16);
-    float xv[8];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      xv[2 * w] = bf_lo(vword(x, w));
-      xv[2 * w + 1] = bf_hi(vword(x, w));
+    for (int j = 0; j < NT; j += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vbase + v_lane + j * 16, b0, b1, b2, b3);
+      mma_bf16(o[j], pa, b0, b1);
+      mma_bf16(o[j + 1], pa, b2, b3);
     }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float pt = p_s[t][g];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] += pt * xv[e];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == NS) {
+      slot = 0;
+      ++round;
     }
-  }
-  // reduce the VG row groups: lanes of a warp that hold the same vector by
-  // shuffles (every lane takes part), then the warps through shared memory
+
+    if (m.flags & kMetaLast) {
+      // the four lanes of a query head hold its sums over different positions
+      float l_tot = l_part;
+      l_tot += __shfl_xor_sync(kFullMask, l_tot, 1);
+      l_tot += __shfl_xor_sync(kFullMask, l_tot, 2);
+      const AttnKey kk = P.keys[static_cast<int64_t>(m.layer) * P.n_keys + m.key];
+      float* blk = P.records + (static_cast<int64_t>(kk.rec_base + (blockIdx.x - kk.first_cta)) * HB + h) * BLK;
+      if (row_live) {
 #pragma unroll
-  for (int o = VT; o < 32; o <<= 1)
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
-  const int lane = tid & 31, warp = tid >> 5;
-  if (lane < VT) {
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) part[warp][g][vv * 8 + e] = acc[g][e];
-  }
-  __syncthreads();
-  // partial record: [layer][tile][h][g] -> (m, l, acc[D])
-  float* out = P.partial + ((static_cast<int64_t>(blockIdx.z) * gridDim.x + tile) * gridDim.y + h) *
-                               static_cast<int64_t>(G) * (D + 2);
-  for (int i = tid; i < G * D; i += kAttnThreads) {
-    const int g = i / D, d = i % D;
-    float sum = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kAttnThreads / 32; ++w) sum += part[w][g][d];
-    out[g * (D + 2) + 2 + d] = sum;
-  }
-  if (tid == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      out[g * (D + 2)] = m_g[g];
-      out[g * (D + 2) + 1] = l_g[g];
+        for (int j = 0; j < NT; ++j)
+          *reinterpret_cast<float2*>(blk + g * D + 8 * j + 2 * tq) = make_float2(o[j][0] + o[j][2], o[j][1] + o[j][3]);
+        if (tq == 0) {
+          blk[G * D + g] = m_run;
+          blk[G * D + G + g] = l_tot;
+        }
+      }
     }
   }
 }
 
-// One thread block per (request, query head, layer): merges its tiles.
+// One thread block per (request, query head, layer): merges the records of
+// its key.  Statistics are in log2 units.
 template <int D>
-__global__ void __launch_bounds__(128) k_attend_combine(const AttnParams P, int group) {
+__global__ void __launch_bounds__(128) k_attend_merge(const AttnParams P, int group) {
   const int r = blockIdx.x, gq = blockIdx.y, lz = blockIdx.z;
-  const int h = gq / group, g = gq % group;
-  const int t0 = P.req_tile_begin[r], t1 = P.req_tile_begin[r + 1];
-  __shared__ float w_s[kAttnMaxCombine];
-  __shared__ float tot_s;
-  const int64_t stride_tile = static_cast<int64_t>(P.n_kv_heads) * group * (D + 2);
-  const float* base = P.partial + static_cast<int64_t>(lz) * P.n_tiles * stride_tile +
-                      static_cast<int64_t>(h) * group * (D + 2) + static_cast<int64_t>(g) * (D + 2);
+  const int hk = gq / group, g = gq % group;
+  const int HB = P.heads_per_cta;
+  const int hg = hk / HB, h = hk % HB;
+  const int64_t lk = static_cast<int64_t>(lz) * P.n_keys + static_cast<int64_t>(r) * P.head_groups + hg;
+  const int rec0 = P.keys[lk].rec_base, rec1 = P.keys[lk + 1].rec_base;
+  const int BLK = attn_block_floats(group, D);
+  const float* base = P.records + static_cast<int64_t>(h) * BLK;
+  const int64_t stride = static_cast<int64_t>(HB) * BLK;
   float M = -FLT_MAX;
-  for (int t = t0; t < t1; ++t) M = fmaxf(M, base[t * stride_tile]);
-  if (threadIdx.x == 0) {
-    float tot = 0.0f;
-    for (int t = t0; t < t1; ++t) {
-      const float w = __expf(base[t * stride_tile] - M);
-      if (t - t0 < kAttnMaxCombine) w_s[t - t0] = w;
-      tot += w * base[t * stride_tile + 1];
-    }
-    tot_s = tot;
-  }
-  __syncthreads();
-  const float tot = tot_s;
+  for (int k = rec0; k < rec1; ++k) M = fmaxf(M, base[k * stride + group * D + g]);
+  float tot = 0.0f;
+  for (int k = rec0; k < rec1; ++k)
+    tot += exp2f(base[k * stride + group * D + g] - M) * base[k * stride + group * D + group + g];
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
     float s = 0.0f;
-    for (int t = t0; t < t1; ++t) {
-      const float w = (t - t0 < kAttnMaxCombine) ? w_s[t - t0] : __expf(base[t * stride_tile] - M);
-      s += w * base[t * stride_tile + 2 + d];
-    }
+    for (int k = rec0; k < rec1; ++k) s += exp2f(base[k * stride + group * D + g] - M) * base[k * stride + g * D + d];
     P.out[((static_cast<int64_t>(lz) * P.n_req + r) * P.num_q_heads + gq) * D + d] = s / tot;
   }
   if (threadIdx.x == 0 && P.lse != nullptr)
-    P.lse[(static_cast<int64_t>(lz) * P.n_req + r) * P.num_q_heads + gq] = M + logf(tot);
+    P.lse[(static_cast<int64_t>(lz) * P.n_req + r) * P.num_q_heads + gq] = (M + log2f(tot)) * 0.69314718055994531f;
 }
 
 template <int PAIRING, int D, int G>
-cudaError_t launch_tiles(const AttnParams& p, cudaStream_t s) {
-  k_attend_tiles<PAIRING, D, G><<<dim3(p.n_tiles, p.n_kv_heads, p.n_layers), kAttnThreads, 0, s>>>(p);
+cudaError_t launch_g(const AttnParams& p, int grid, size_t smem, cudaStream_t s) {
+  auto kern = k_attend<PAIRING, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 32 * (p.heads_per_cta + 1), smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_attend_merge<D><<<dim3(p.n_req, p.num_q_heads, p.n_layers), D, 0, s>>>(p, G);
   return cudaGetLastError();
 }
 
-template <int PAIRING, int D>
-cudaError_t launch_for_d(const AttnParams& p, int group, cudaStream_t s) {
-  cudaError_t e;
-  switch (group) {
-    case 1: e = launch_tiles<PAIRING, D, 1>(p, s); break;
-    case 2: e = launch_tiles<PAIRING, D, 2>(p, s); break;
-    case 4: e = launch_tiles<PAIRING, D, 4>(p, s); break;
-    case 8: e = launch_tiles<PAIRING, D, 8>(p, s); break;
-    default: return cudaErrorInvalidValue;
-  }
-  if (e != cudaSuccess) return e;
-  k_attend_combine<D><<<dim3(p.n_req, p.num_q_heads, p.n_layers), 128, 0, s>>>(p, group);
-  return cudaGetLastError();
+template <int PAIRING, int D, int G>
+int occupancy_g(int heads_per_cta, size_t smem) {
+  auto kern = k_attend<PAIRING, D, G>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (heads_per_cta + 1), smem) != cudaSuccess) return 0;
+  return n;
 }
+
+// Returns FN<pairing, head_dim, group>(args...) for the runtime triple, FAIL
+// when it has no instance.
+#define PIC_ATTN_DISPATCH(FN, FAIL, ...)                              \
+  do {                                                                \
+    if (pairing == kNeox) {                                           \
+      if (head_dim == 64) {                                           \
+        if (group == 1) return FN<kNeox, 64, 1>(__VA_ARGS__);         \
+        if (group == 2) return FN<kNeox, 64, 2>(__VA_ARGS__);         \
+        if (group == 4) return FN<kNeox, 64, 4>(__VA_ARGS__);         \
+        if (group == 8) return FN<kNeox, 64, 8>(__VA_ARGS__);         \
+      } else if (head_dim == 128) {                                   \
+        if (group == 1) return FN<kNeox, 128, 1>(__VA_ARGS__);        \
+        if (group == 2) return FN<kNeox, 128, 2>(__VA_ARGS__);        \
+        if (group == 4) return FN<kNeox, 128, 4>(__VA_ARGS__);        \
+        if (group == 8) return FN<kNeox, 128, 8>(__VA_ARGS__);        \
+      }                                                               \
+    } else {                                                          \
+      if (head_dim == 64) {                                           \
+        if (group == 1) return FN<kInterleaved, 64, 1>(__VA_ARGS__);  \
+        if (group == 2) return FN<kInterleaved, 64, 2>(__VA_ARGS__);  \
+        if (group == 4) return FN<kInterleaved, 64, 4>(__VA_ARGS__);  \
+        if (group == 8) return FN<kInterleaved, 64, 8>(__VA_ARGS__);  \
+      } else if (head_dim == 128) {                                   \
+        if (group == 1) return FN<kInterleaved, 128, 1>(__VA_ARGS__); \
+        if (group == 2) return FN<kInterleaved, 128, 2>(__VA_ARGS__); \
+        if (group == 4) return FN<kInterleaved, 128, 4>(__VA_ARGS__); \
+        if (group == 8) return FN<kInterleaved, 128, 8>(__VA_ARGS__); \
+      }                                                               \
+    }                                                                 \
+    return FAIL;                                                      \
+  } while (0)
 
 }  // namespace
 
-cudaError_t launch_attend(const AttnParams& p, int pairing, int head_dim, int group, cudaStream_t s) {
-  if (p.n_tiles <= 0 || p.n_layers <= 0) return cudaSuccess;
-  if (pairing == kNeox) {
-    if (head_dim == 64) return launch_for_d<kNeox, 64>(p, group, s);
-    if (head_dim == 128) return launch_for_d<kNeox, 128>(p, group, s);
-  } else {
-    if (head_dim == 64) return launch_for_d<kInterleaved, 64>(p, group, s);
-    if (head_dim == 128) return launch_for_d<kInterleaved, 128>(p, group, s);
-  }
-  return cudaErrorInvalidValue;
+bool attend_config(int head_dim, int group, int heads_per_cta, int* ring, size_t* smem_bytes) {
+  if (heads_per_cta < 1 || heads_per_cta > kAttnMaxHeads) return false;
+  const SmemLayout base = smem_layout(head_dim, group, heads_per_cta, 0);
+  if (base.total + 2 * base.stage_bytes > kSmemBudget) return false;
+  int n = static_cast<int>((kSmemBudget - base.total) / base.stage_bytes);
+  if (n > kAttnMaxStages) n = kAttnMaxStages;
+  *ring = n;
+  *smem_bytes = smem_layout(head_dim, group, heads_per_cta, n).total;
+  return true;
+}
+
+int attend_ctas_per_sm(int pairing, int head_dim, int group, int heads_per_cta, size_t smem_bytes) {
+  PIC_ATTN_DISPATCH(occupancy_g, 0, heads_per_cta, smem_bytes);
+}
+
+cudaError_t launch_attend(const AttnParams& p, int pairing, int head_dim, int group, int grid, size_t smem_bytes,
+                          cudaStream_t s) {
+  if (p.n_units <= 0 || grid <= 0) return cudaSuccess;
+  PIC_ATTN_DISPATCH(launch_g, cudaErrorInvalidValue, p, grid, smem_bytes, s);
 }
 
 }  // namespace pic

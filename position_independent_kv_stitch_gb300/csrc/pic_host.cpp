@@ -617,90 +617,128 @@ void fill_freq(const pic_ctx* ctx, uint8_t* base, const WsLayout& w) {
 }
 
 // Decode attention: every position [0, total) of each request becomes one
-// token descriptor (where its K/V row is and which delta its key needs), and
-// positions are grouped into tiles of <= kAttnTileTokens tokens with <=
-// kAttnMaxSlots distinct deltas.  fused: chunk tokens are read from their
-// sources (pool rows, block-resident chunk rows) and rotated on load; inline
-// positions and mapped chunks already rotated come from the request's paged
-// cache.  cache: every position from the paged cache, no rotation.
-struct AttnLayout {
-  size_t freq_off, tiles_off, toks_off, reqt_off, partial_off, total;
-  int32_t n_tiles, n_toks;
+// token entry (where its K/V row is), and each request's positions are cut
+// into stages of <= kAttnStageTokens consecutive positions sharing one
+// delta.  fused: chunk tokens are read from their sources (pool rows,
+// block-resident chunk rows) and their keys need R(delta); inline positions
+// and mapped chunks already rotated come from the request's paged cache.
+// cache: every position from the paged cache, no rotation.  Stages are listed
+// key-major (key = request * head_groups + head group) for one layer; the
+// kernel walks (layer, stage) units.
+struct AttnPlan {
+  std::vector<pic::AttnStage> stages;
+  std::vector<pic::AttnTok> toks;
+  std::vector<int32_t> key_stage_begin;  // [n_keys + 1]
+  int32_t heads_per_cta = 0, head_groups = 0, n_keys = 0;
 };
 
-void attend_tokens(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
-                   int32_t max_slots, std::vector<pic::AttnTile>* tiles, std::vector<pic::AttnTok>* toks,
-                   std::vector<int32_t>* req_tile_begin) {
+bool attn_heads(const pic_model_desc& m, int32_t* hb, int32_t* groups) {
+  const int32_t H = m.num_kv_heads;
+  if (H >= 1 && H <= pic::kAttnMaxHeads) {
+    *hb = H;
+    *groups = 1;
+    return true;
+  }
+  if (H > 0 && H % pic::kAttnMaxHeads == 0) {
+    *hb = pic::kAttnMaxHeads;
+    *groups = H / pic::kAttnMaxHeads;
+    return true;
+  }
+  return false;
+}
+
+void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source, int32_t group,
+                 AttnPlan* out) {
   const int32_t bs = ctx->model.block_size;
-  int32_t n_tiles = 0, n_toks = 0;
+  const int32_t ST = pic::kAttnStageTokens;
+  attn_heads(ctx->model, &out->heads_per_cta, &out->head_groups);
+  out->n_keys = n_req * out->head_groups;
+  out->key_stage_begin.assign(1, 0);
+  std::vector<pic::AttnStage> req_stages;
   for (int32_t r = 0; r < n_req; ++r) {
     const pic_plan* pl = plans[r];
-    if (req_tile_begin) (*req_tile_begin)[r] = n_tiles;
-    // per-position (row, delta, flags) in order
-    std::vector<int32_t> rows(pl->total_tokens), deltas(pl->total_tokens, 0), flags(pl->total_tokens, 0);
-    for (int32_t p = 0; p < pl->total_tokens; ++p) {
-      rows[p] = pl->table[p / bs] * bs + p % bs;
-      flags[p] = pic::kAttnFromCache;
-    }
+    const int32_t T = pl->total_tokens;
+    const int32_t tok_off = static_cast<int32_t>(out->toks.size());
+    std::vector<int32_t> deltas(T, 0);
+    std::vector<uint8_t> sink(T, 0);
+    out->toks.resize(out->toks.size() + T);
+    pic::AttnTok* tk = out->toks.data() + tok_off;
+    for (int32_t p = 0; p < T; ++p) tk[p] = pic::AttnTok{pl->table[p / bs] * bs + p % bs, pic::kAttnFromCache};
     for (const Segment& sg : pl->segs) {
       for (int32_t t = 0; t < sg.num_tokens; ++t) {
         const int32_t p = sg.dst_pos + t;
-        if (sg.dst_pos != 0 && t < sg.n_recompute) flags[p] |= pic::kAttnSink;
+        if (sg.dst_pos != 0 && t < sg.n_recompute) sink[p] = 1;
         if (source != PIC_ATTEND_FUSED) continue;
         if (sg.kind == pic::kRunPool) {
-          rows[p] = static_cast<int32_t>(sg.src_tok + t);
-          flags[p] &= ~pic::kAttnFromCache;
+          tk[p] = pic::AttnTok{static_cast<int32_t>(sg.src_tok + t), 0};
           deltas[p] = sg.delta;
         } else if (sg.kind == pic::kRunBlocks) {
-          rows[p] = sg.src_blocks[t / bs] * bs + t % bs;
+          tk[p].row = sg.src_blocks[t / bs] * bs + t % bs;
           deltas[p] = sg.delta;
         } else if (!pl->applied) {  // mapped chunk whose keys have not moved yet
           deltas[p] = sg.delta;
         }
       }
     }
-    int32_t p = 0;
-    while (p < pl->total_tokens) {
-      pic::AttnTile T{};
-      T.req = r;
-      T.first_pos = p;
-      T.tok_off = n_toks;
-      while (p < pl->total_tokens && T.n_tok < pic::kAttnTileTokens) {
-        int32_t slot = -1;
-        for (int32_t k = 0; k < T.n_slots; ++k)
-          if (T.deltas[k] == deltas[p]) slot = k;
-        if (slot < 0) {
-          if (T.n_slots == max_slots) break;
-          slot = T.n_slots++;
-          T.deltas[slot] = deltas[p];
-        }
-        if (toks) toks->push_back(pic::AttnTok{rows[p], flags[p] | slot});
-        ++T.n_tok;
-        ++n_toks;
-        ++p;
+    req_stages.clear();
+    for (int32_t p = 0; p < T;) {
+      pic::AttnStage st{};
+      st.tok_off = tok_off + p;
+      st.delta = deltas[p];
+      int32_t n = 0;
+      while (p + n < T && n < ST && deltas[p + n] == st.delta) {
+        if (sink[p + n]) st.sink_mask |= static_cast<uint16_t>(1u << n);
+        ++n;
       }
-      if (tiles) tiles->push_back(T);
-      ++n_tiles;
+      st.n_tok = static_cast<uint16_t>(n);
+      req_stages.push_back(st);
+      p += n;
+    }
+    for (int32_t hg = 0; hg < out->head_groups; ++hg) {
+      for (pic::AttnStage st : req_stages) {
+        st.key = r * out->head_groups + hg;
+        out->stages.push_back(st);
+      }
+      out->key_stage_begin.push_back(static_cast<int32_t>(out->stages.size()));
     }
   }
-  if (req_tile_begin) (*req_tile_begin)[n_req] = n_tiles;
-  if (!tiles && !toks && req_tile_begin) return;
-  (void)n_toks;
 }
 
-AttnLayout attend_layout(const pic_ctx* ctx, int32_t n_tiles, int32_t n_toks, int32_t n_req, int32_t num_q_heads,
-                         int32_t num_layers) {
+struct AttnLayout {
+  size_t freq_off, stages_off, toks_off, keys_off, records_off, total;
+};
+
+AttnLayout attend_layout(const pic_ctx* ctx, size_t n_stages, size_t n_toks, size_t n_key_entries,
+                         size_t n_records, int32_t heads_per_cta, int32_t group) {
   AttnLayout w;
-  w.n_tiles = n_tiles;
-  w.n_toks = n_toks;
   w.freq_off = pic::align_up(sizeof(WsHeader), pic::kWsAlign);
-  w.tiles_off = pic::align_up(w.freq_off + ctx->freq_turns.size() * sizeof(float2), pic::kWsAlign);
-  w.toks_off = pic::align_up(w.tiles_off + static_cast<size_t>(n_tiles) * sizeof(pic::AttnTile), pic::kWsAlign);
-  w.reqt_off = pic::align_up(w.toks_off + static_cast<size_t>(n_toks) * sizeof(pic::AttnTok), pic::kWsAlign);
-  w.partial_off = pic::align_up(w.reqt_off + (static_cast<size_t>(n_req) + 1) * sizeof(int32_t), pic::kWsAlign);
-  const size_t partial = static_cast<size_t>(num_layers) * n_tiles * num_q_heads * (ctx->model.head_dim + 2) * sizeof(float);
-  w.total = pic::align_up(w.partial_off + partial, pic::kWsAlign);
+  w.stages_off = pic::align_up(w.freq_off + ctx->freq_turns.size() * sizeof(float2), pic::kWsAlign);
+  w.toks_off = pic::align_up(w.stages_off + n_stages * sizeof(pic::AttnStage), pic::kWsAlign);
+  w.keys_off = pic::align_up(w.toks_off + n_toks * sizeof(pic::AttnTok), pic::kWsAlign);
+  w.records_off = pic::align_up(w.keys_off + n_key_entries * sizeof(pic::AttnKey), pic::kWsAlign);
+  const size_t rec = static_cast<size_t>(pic::attn_record_floats(group, ctx->model.head_dim, heads_per_cta)) * 4;
+  w.total = pic::align_up(w.records_off + n_records * rec, pic::kWsAlign);
   return w;
+}
+
+// Records of a persistent grid of `ctas` over `layers` x plan.stages units:
+// CTA c owns units [U c / N, U (c + 1) / N); each (layer, key) gets one
+// record per CTA whose range touches it, written at rec_base + (c - first_cta).
+int64_t attend_keys(const AttnPlan& plan, int32_t layers, int64_t ctas, std::vector<pic::AttnKey>* keys) {
+  const int64_t nsl = static_cast<int64_t>(plan.stages.size());
+  const int64_t U = nsl * layers;
+  auto cta_of = [&](int64_t u) { return ((u + 1) * ctas - 1) / U; };
+  int64_t rec = 0;
+  if (keys) keys->clear();
+  for (int32_t l = 0; l < layers; ++l)
+    for (int32_t k = 0; k < plan.n_keys; ++k) {
+      const int64_t a = l * nsl + plan.key_stage_begin[k], b = l * nsl + plan.key_stage_begin[k + 1];
+      const int64_t c0 = cta_of(a), c1 = cta_of(b - 1);
+      if (keys) keys->push_back(pic::AttnKey{static_cast<int32_t>(rec), static_cast<int32_t>(c0)});
+      rec += c1 - c0 + 1;
+    }
+  if (keys) keys->push_back(pic::AttnKey{static_cast<int32_t>(rec), 0});
+  return rec;
 }
 
 }  // namespace
@@ -1305,18 +1343,19 @@ pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n,
 size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
                                   int32_t num_q_heads, int32_t num_layers) {
   if (!ctx || n_req < 0 || (n_req > 0 && !plans) || num_q_heads <= 0 || num_layers <= 0) return 0;
-  int64_t toks = 0;
-  for (int32_t r = 0; r < n_req; ++r) {
+  for (int32_t r = 0; r < n_req; ++r)
     if (!plans[r]) return 0;
-    toks += plans[r]->total_tokens;
-  }
-  const int32_t slots = pic::attn_slots(num_q_heads / std::max(1, ctx->model.num_kv_heads));
-  std::vector<pic::AttnTile> tiles;
-  attend_tokens(ctx, plans, n_req, PIC_ATTEND_FUSED, slots, &tiles, nullptr, nullptr);
-  std::vector<pic::AttnTile> tiles_c;
-  attend_tokens(ctx, plans, n_req, PIC_ATTEND_CACHE, slots, &tiles_c, nullptr, nullptr);
-  const int32_t nt = static_cast<int32_t>(std::max(tiles.size(), tiles_c.size()));
-  return attend_layout(ctx, nt, static_cast<int32_t>(toks), n_req, num_q_heads, num_layers).total;
+  int32_t hb = 0, hgroups = 0;
+  if (!attn_heads(ctx->model, &hb, &hgroups)) return 0;
+  const int32_t group = std::max(1, num_q_heads / std::max(1, ctx->model.num_kv_heads));
+  AttnPlan fused, cache;
+  attend_plan(ctx, plans, n_req, PIC_ATTEND_FUSED, group, &fused);
+  attend_plan(ctx, plans, n_req, PIC_ATTEND_CACHE, group, &cache);
+  const size_t n_stages = std::max(fused.stages.size(), cache.stages.size());
+  // a grid of at most kAttnMaxCtas CTAs adds at most one record per CTA
+  const size_t n_keys = static_cast<size_t>(num_layers) * fused.n_keys;
+  const size_t records = n_keys + pic::kAttnMaxCtas;
+  return attend_layout(ctx, n_stages, fused.toks.size(), n_keys + 1, records, hb, group).total;
 }
 
 pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
@@ -1328,6 +1367,10 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   const pic_model_desc& m = ctx->model;
   if (m.kind != PIC_KIND_GQA || (m.head_dim != 64 && m.head_dim != 128))
     return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention covers GQA heads of 64 or 128 dims");
+  int32_t hb = 0, hgroups = 0;
+  if (!attn_heads(m, &hb, &hgroups))
+    return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention needs <= %d KV heads or a multiple of %d",
+                pic::kAttnMaxHeads, pic::kAttnMaxHeads);
   if (source != PIC_ATTEND_FUSED && source != PIC_ATTEND_CACHE) return fail(ctx, PIC_ERR_INVALID_ARG, "bad source");
   if (n_req <= 0 || !plans) return fail(ctx, PIC_ERR_INVALID_ARG, "no requests");
   for (int32_t r = 0; r < n_req; ++r)
@@ -1342,19 +1385,22 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   if (!q || !out || !d_ws || !k_cache || !v_cache) return fail(ctx, PIC_ERR_INVALID_ARG, "null q, out, cache or workspace");
   if (source == PIC_ATTEND_FUSED && (!k_pool || !v_pool))
     return fail(ctx, PIC_ERR_INVALID_ARG, "fused attention reads the pool: pass k_pool and v_pool");
-  if (!vectorized_bytes_ok(k_cache) || !vectorized_bytes_ok(v_cache) || (cache_ls & 15) ||
-      (k_pool && !vectorized_bytes_ok(k_pool)) || (v_pool && !vectorized_bytes_ok(v_pool)) || (pool_ls & 15) ||
-      !vectorized_bytes_ok(d_ws))
-    return fail(ctx, PIC_ERR_ALIGNMENT, "pools, caches, strides and workspace must be 16-byte aligned");
-  std::vector<pic::AttnTile> tiles;
-  std::vector<pic::AttnTok> toks;
-  std::vector<int32_t> reqt(static_cast<size_t>(n_req) + 1);
-  attend_tokens(ctx, plans, n_req, source, pic::attn_slots(group), &tiles, &toks, &reqt);
+  if (!vectorized_bytes_ok(q) || !vectorized_bytes_ok(out) || !vectorized_bytes_ok(k_cache) ||
+      !vectorized_bytes_ok(v_cache) || (cache_ls & 15) || (k_pool && !vectorized_bytes_ok(k_pool)) ||
+      (v_pool && !vectorized_bytes_ok(v_pool)) || (pool_ls & 15) || !vectorized_bytes_ok(d_ws))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "q, out, pools, caches, strides and workspace must be 16-byte aligned");
   for (int32_t r = 0; r < n_req; ++r)
     if (plans[r]->total_tokens == 0) return fail(ctx, PIC_ERR_RANGE, "plans[%d] has no context to attend", r);
-  const AttnLayout w = attend_layout(ctx, static_cast<int32_t>(tiles.size()), static_cast<int32_t>(toks.size()), n_req,
-                                     num_q_heads, num_layers);
-  if (ws_bytes < w.total) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  int ring = 0;
+  size_t smem = 0;
+  if (!pic::attend_config(m.head_dim, group, hb, &ring, &smem))
+    return fail(ctx, PIC_ERR_UNSUPPORTED, "attention stages do not fit in shared memory");
+
+  AttnPlan plan;
+  attend_plan(ctx, plans, n_req, source, group, &plan);
+  const int64_t units = static_cast<int64_t>(plan.stages.size()) * num_layers;
+  if (units > INT32_MAX || static_cast<int64_t>(plan.toks.size()) > INT32_MAX)
+    return fail(ctx, PIC_ERR_CAPACITY, "attention batch too large");
 
   DeviceInfo di;
   pic_status st = current_device(ctx, di);
@@ -1363,34 +1409,48 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   for (int i = 0; i < 4; ++i)
     if (bufs[i] && residency(bufs[i]) != 0)
       return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention reads pools and caches from device memory only");
+  const int per_sm = pic::attend_ctas_per_sm(m.pairing, m.head_dim, group, hb, smem);
+  if (per_sm <= 0) return fail(ctx, PIC_ERR_CUDA, "attention kernel does not fit on an SM");
+  const int64_t ctas = std::min<int64_t>({units, static_cast<int64_t>(di.sm_count) * per_sm, pic::kAttnMaxCtas});
+  std::vector<pic::AttnKey> keys;
+  const int64_t records = attend_keys(plan, num_layers, ctas, &keys);
+  const AttnLayout w = attend_layout(ctx, plan.stages.size(), plan.toks.size(), keys.size(),
+                                     static_cast<size_t>(records), hb, group);
+  if (ws_bytes < w.total) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t image = w.partial_off;  // everything before the partial results
+  const size_t image = w.records_off;  // everything before the records; the header is zeroed
   StagingSlot* sl = nullptr;
   st = acquire_staging(ctx, di.device, image, &sl);
   if (st != PIC_OK) return st;
   uint8_t* base = sl->host;
   std::memcpy(base + w.freq_off, ctx->freq_turns.data(), ctx->freq_turns.size() * sizeof(float2));
-  std::memcpy(base + w.tiles_off, tiles.data(), tiles.size() * sizeof(pic::AttnTile));
-  std::memcpy(base + w.toks_off, toks.data(), toks.size() * sizeof(pic::AttnTok));
-  std::memcpy(base + w.reqt_off, reqt.data(), reqt.size() * sizeof(int32_t));
+  std::memcpy(base + w.stages_off, plan.stages.data(), plan.stages.size() * sizeof(pic::AttnStage));
+  std::memcpy(base + w.toks_off, plan.toks.data(), plan.toks.size() * sizeof(pic::AttnTok));
+  std::memcpy(base + w.keys_off, keys.data(), keys.size() * sizeof(pic::AttnKey));
   st = upload_staging(ctx, sl, d_ws, image, s);
   if (st != PIC_OK) return st;
 
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  constexpr float kLog2e = 1.4426950408889634f;
   pic::AttnParams p{};
-  p.tiles = reinterpret_cast<const pic::AttnTile*>(ws + w.tiles_off);
-  p.n_tiles = static_cast<int32_t>(tiles.size());
+  p.stages = reinterpret_cast<const pic::AttnStage*>(ws + w.stages_off);
+  p.n_stages = static_cast<int32_t>(plan.stages.size());
   p.toks = reinterpret_cast<const pic::AttnTok*>(ws + w.toks_off);
-  p.req_tile_begin = reinterpret_cast<const int32_t*>(ws + w.reqt_off);
-  p.n_req = n_req;
+  p.keys = reinterpret_cast<const pic::AttnKey*>(ws + w.keys_off);
+  p.n_keys = plan.n_keys;
+  p.n_units = units;
   p.freq = reinterpret_cast<const float2*>(ws + w.freq_off);
   p.q = static_cast<const uint16_t*>(q);
+  p.n_req = n_req;
   p.num_q_heads = num_q_heads;
   p.n_kv_heads = m.num_kv_heads;
+  p.heads_per_cta = hb;
+  p.head_groups = hgroups;
   p.n_layers = num_layers;
   p.layer_begin = layer_begin;
-  p.scale = softmax_scale;
-  p.sink_bias = sink_bias;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.sink_log2 = sink_bias * kLog2e;
   p.k_pool = static_cast<const uint8_t*>(k_pool);
   p.v_pool = static_cast<const uint8_t*>(v_pool);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
@@ -1398,10 +1458,12 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   p.pool_layer_stride = pool_ls;
   p.cache_layer_stride = cache_ls;
   p.row_bytes = static_cast<int32_t>(row_bytes_of(m));
-  p.partial = reinterpret_cast<float*>(ws + w.partial_off);
+  p.ring = ring;
+  p.records = reinterpret_cast<float*>(ws + w.records_off);
   p.out = out;
   p.lse = lse;
-  const cudaError_t e = pic::launch_attend(p, m.pairing, m.head_dim, group, s);
+  p.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  const cudaError_t e = pic::launch_attend(p, m.pairing, m.head_dim, group, static_cast<int>(ctas), smem, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "attention launch");
   return ok(ctx);
 }

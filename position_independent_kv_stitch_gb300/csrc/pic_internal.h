@@ -95,58 +95,85 @@ cudaError_t launch_tma(const KernelParams& p, const TmaConfig& c, int mode, int 
                        int grid, cudaStream_t stream);
 
 // ---- decode attention over a stitched context (pic_attention.cu)
-constexpr int kAttnTileTokens = 128;   // positions per tile (one thread each)
-constexpr int kAttnMaxSlots = 16;      // distinct deltas per tile (8 when G = 8)
-// Distinct deltas a tile may hold for G query heads per KV head: the rotated
-// queries of all of them stay in static shared memory (<= 48 KB).
-__host__ __device__ constexpr int attn_slots(int group) { return group >= 8 ? 8 : kAttnMaxSlots; }
-constexpr int kAttnMaxCombine = 1024;  // tiles whose weights the combine keeps on chip
+//
+// Work is cut into stages: <= kAttnStageTokens consecutive positions of one
+// request that share one delta.  A persistent CTA owns a contiguous range of
+// (layer, stage) units; one consumer warp per KV head keeps an online softmax
+// for the group's query heads while the CTA's range stays on one key
+// (request x head group); each (layer, key) the range leaves becomes one
+// record: per KV head, the max, sum and weighted values of its query heads.
+constexpr int kAttnStageTokens = 16;        // positions per stage (one k-step of P.V)
+constexpr int kAttnMaxHeads = 8;            // KV heads per CTA: one consumer warp each
+constexpr int kAttnMaxStages = 8;           // shared-memory ring depth
+constexpr int kAttnMaxCtas = 1024;          // persistent grid bound (workspace sizing)
 constexpr int32_t kAttnFromCache = 1 << 8;  // AttnTok.flags: row is a paged-cache row
-constexpr int32_t kAttnSink = 1 << 9;       // AttnTok.flags: LegoLink pseudo-sink position
 
-struct AttnTile {
-  int32_t req;
-  int32_t first_pos;
-  int32_t n_tok;
-  int32_t n_slots;
-  int32_t tok_off;
-  int32_t pad[3];
-  int32_t deltas[kAttnMaxSlots];
+struct AttnStage {
+  int32_t tok_off;     // first entry of the stage in the token list
+  int32_t delta;       // every key of the stage is rotated by R(delta)
+  int32_t key;         // request * head_groups + head group
+  uint16_t n_tok;      // 1 .. kAttnStageTokens
+  uint16_t sink_mask;  // bit t: position t is a LegoLink pseudo-sink
 };
-static_assert(sizeof(AttnTile) == 96, "AttnTile layout");
+static_assert(sizeof(AttnStage) == 16, "AttnStage layout");
 
 struct AttnTok {
-  int32_t row;    // pool token row or absolute cache row (block * bs + row)
-  int32_t flags;  // delta slot (low 8 bits) | kAttnFromCache | kAttnSink
+  int32_t row;    // pool token row, or absolute cache row (block * bs + row)
+  int32_t flags;  // kAttnFromCache
+};
+
+struct AttnKey {  // per (layer, key), plus one closing entry
+  int32_t rec_base;   // first record of this (layer, key)
+  int32_t first_cta;  // CTA that writes that record
 };
 
 struct AttnParams {
-  const AttnTile* tiles;
-  int32_t n_tiles;
+  const AttnStage* stages;  // one layer's stages, key-major
+  int32_t n_stages;
   const AttnTok* toks;
-  const int32_t* req_tile_begin;  // [n_req + 1]
+  const AttnKey* keys;      // [n_layers * n_keys + 1]
+  int32_t n_keys;
+  int64_t n_units;          // n_layers * n_stages
+  const float2* freq;       // RoPE frequencies in turns, (hi, lo)
+  const uint16_t* q;        // bf16 [n_layers][n_req][num_q_heads][D]
   int32_t n_req;
-  const float2* freq;
-  const uint16_t* q;              // bf16 [n_layers][n_req][num_q_heads][D]
   int32_t num_q_heads;
   int32_t n_kv_heads;
+  int32_t heads_per_cta;    // HB: KV heads a CTA (and a record) covers
+  int32_t head_groups;      // n_kv_heads / HB
   int32_t n_layers;
   int32_t layer_begin;
-  float scale;
-  float sink_bias;
+  float scale_log2;         // softmax scale * log2(e)
+  float sink_log2;          // sink bias * log2(e)
   const uint8_t* k_pool;
   const uint8_t* v_pool;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   int64_t pool_layer_stride;
   int64_t cache_layer_stride;
-  int32_t row_bytes;
-  float* partial;                 // [n_layers][n_tiles][n_kv_heads][group][D + 2]
-  float* out;                     // [n_layers][n_req][num_q_heads][D]
-  float* lse;                     // [n_layers][n_req][num_q_heads] or null
+  int32_t row_bytes;        // one token, all KV heads
+  int32_t ring;             // stages in the shared-memory ring
+  float* records;           // [records][HB][attn_block_floats(G, D)]
+  float* out;               // [n_layers][n_req][num_q_heads][D]
+  float* lse;               // [n_layers][n_req][num_q_heads] or null
+  uint32_t* status;         // PIC_DEV_* bits
 };
 
-cudaError_t launch_attend(const AttnParams& p, int pairing, int head_dim, int group, cudaStream_t stream);
+// floats of one (record, KV head) block: acc[G][D], m[G], l[G], padded to 16 B
+__host__ __device__ constexpr int attn_block_floats(int group, int head_dim) {
+  return (group * (head_dim + 2) + 3) / 4 * 4;
+}
+// floats of one record: every KV head of the group
+__host__ __device__ constexpr int attn_record_floats(int group, int head_dim, int heads_per_cta) {
+  return heads_per_cta * attn_block_floats(group, head_dim);
+}
+// Ring depth and dynamic shared memory of the attention kernel; false when
+// two stages do not fit.
+bool attend_config(int head_dim, int group, int heads_per_cta, int* ring, size_t* smem_bytes);
+// CTAs of the attention kernel that fit on one SM.
+int attend_ctas_per_sm(int pairing, int head_dim, int group, int heads_per_cta, size_t smem_bytes);
+cudaError_t launch_attend(const AttnParams& p, int pairing, int head_dim, int group, int grid, size_t smem_bytes,
+                          cudaStream_t stream);
 
 // Launchers; each returns the launch's cudaError_t.  `grid` is the number of
 // CTAs (persistent, grid-stride over units).

@@ -32,30 +32,15 @@
 
 #include <cstdint>
 
+#include "pic_device.cuh"
 #include "pic_internal.h"
 
 namespace pic {
 namespace {
 
-constexpr unsigned kDevBadBlock = 0x1u;  // matches PIC_DEV_BAD_BLOCK
+using namespace dev;
 
 // ---------------------------------------------------------------- helpers
-
-__device__ __forceinline__ void shift_cossin(int delta, float2 f, float& c, float& s) {
-  const float d = static_cast<float>(delta);   // exact for |delta| < 2^24
-  const float p = __fmul_rn(d, f.x);
-  const float e = __fmaf_rn(d, f.x, -p);       // d * hi == p + e exactly
-  const float r = __fsub_rn(p, rintf(p));      // exact, |r| <= 1/2 turn
-  const float t = __fadd_rn(r, __fmaf_rn(d, f.y, e));
-  sincospif(2.0f * t, &s, &c);                 // cos / sin of 2 pi t
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 __device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
@@ -68,32 +53,6 @@ __device__ __forceinline__ uint4 ld_plain(const uint8_t* p) {
 }
 __device__ __forceinline__ void st_plain(uint8_t* p, uint4 v) {
   *reinterpret_cast<uint4*>(p) = v;
-}
-
-__device__ __forceinline__ uint32_t& word(uint4& v, int w) {
-  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
-}
-
-// Neox pair-vector: a holds x_a of frequencies f0..f0+7, b holds x_b of the same.
-__device__ __forceinline__ void rotate_neox(uint4& a, uint4& b, const float* c, const float* s) {
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t aw = word(a, w), bw = word(b, w);
-    const float a0 = bf_lo(aw), a1 = bf_hi(aw), b0 = bf_lo(bw), b1 = bf_hi(bw);
-    const float c0 = c[2 * w], s0 = s[2 * w], c1 = c[2 * w + 1], s1 = s[2 * w + 1];
-    word(a, w) = bf_pack(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
-    word(b, w) = bf_pack(a0 * s0 + b0 * c0, a1 * s1 + b1 * c1);
-  }
-}
-
-// Interleaved vector: word w holds the pair (x, y) of frequency f0 + w.
-__device__ __forceinline__ void rotate_interleaved(uint4& v, const float* c, const float* s) {
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t vw = word(v, w);
-    const float x = bf_lo(vw), y = bf_hi(vw);
-    word(v, w) = bf_pack(x * c[w] - y * s[w], x * s[w] + y * c[w]);
-  }
 }
 
 // Resolves a run's destination block; false (and a raised status bit) when

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_util import bits
+from gpu_util import Stitched, bits
 from position_independent_kv_stitch_gb300 import pic
 
 pytestmark = pytest.mark.gpu
@@ -143,3 +143,186 @@ def test_cache_path_over_materialized_stitch():
         assert np.abs(out_f - want).max() < np.abs(out_c - want).max()   # fusing skips one rounding
     finally:
         pic.pic_destroy(S["ctx"])
+
+
+# ---------------------------------------------------------------------------
+# long contexts: many stages per key, CTAs spanning several keys and keys
+# spread over several CTAs, head groups, every query-group size
+# ---------------------------------------------------------------------------
+
+_POOL_LENS = [1, 5, 16, 17, 33, 100, 250, 300, 64, 128, 7, 400]
+_BLOCK_CHUNK = (45, [190, 191, 192], 700)   # tokens, blocks, position its keys sit at
+
+
+def _long_setup(pairing, D, Hkv, G, L, seed, rep=1):
+    bs, nb = 16, 200 + 120 * (rep - 1)
+    m = W.Model("attn-long", "gqa", L, Hkv, D, D, 0, pairing, 1e6, bs)
+    ctx = pic.create_from_spec(pic.model_spec_from(m), nb)
+    offs = [0]
+    for n in _POOL_LENS[:-1]:
+        offs.append(offs[-1] + n)
+    ids, sources = [], {}
+    for c, (o, n) in enumerate(zip(offs, _POOL_LENS)):
+        cid = pic.pic_register_chunk(ctx, W.chunk_key("attn-long", c), o, n)[0]
+        ids.append(cid)
+        sources[cid] = ("pool", o)
+    n_b, blocks, base = _BLOCK_CHUNK
+    bid = pic.pic_register_chunk_blocks(ctx, W.chunk_key("attn-long", 99), blocks, n_b, base)[0]
+    sources[bid] = ("blocks", blocks)
+    g = torch.Generator().manual_seed(seed)
+    P = offs[-1] + _POOL_LENS[-1]
+    k_pool = torch.randn((L, P, Hkv, D), generator=g).to(torch.bfloat16)
+    v_pool = torch.randn((L, P, Hkv, D), generator=g).to(torch.bfloat16)
+    k_cache = torch.randn((L, nb, bs, Hkv, D), generator=g).to(torch.bfloat16)
+    v_cache = torch.randn((L, nb, bs, Hkv, D), generator=g).to(torch.bfloat16)
+
+    def positions(chunks, start, gaps):
+        pos, p = [], start
+        for j, c in enumerate(chunks):
+            p += gaps.get(j, 0)
+            pos.append(p)
+            p += n_b if c == bid else _POOL_LENS[ids.index(c)]
+        return pos, p
+
+    # rep > 1 repeats each request's pool chunks (a chunk may occur more than
+    # once in a request when it is copied) so every CTA owns many stages
+    pool_runs = [ids[9], ids[3], ids[8], ids[0], ids[4], ids[10], ids[6], ids[1]]
+    specs = [([ids[5], ids[11], ids[2], bid, ids[7]] + [ids[7], ids[4]] * (rep - 1), 3, {4: 10}, 6),
+             (pool_runs * rep, 0, {}, 0),
+             ([ids[11], ids[6], ids[5]] * rep, 0, {}, 40)]
+    plans, tables = [], []
+    for chunks, start, gaps, tail in specs:
+        pos, end = positions(chunks, start, gaps)
+        plan, bt = pic.pic_build_block_table(ctx, chunks, 64 * rep, dst_pos=pos, start_pos=start,
+                                             total_tokens=end + tail, k_nonleading=4)
+        plans.append(plan)
+        tables.append(bt)
+    return dict(m=m, ctx=ctx, plans=plans, tables=tables, sources=sources, k_pool=k_pool, v_pool=v_pool,
+                k_cache=k_cache, v_cache=v_cache, bs=bs, L=L, Hq=Hkv * G, D=D)
+
+
+def _context_kv(S, r, layers):
+    """fp64 keys (exactly rotated) and values of request r's context."""
+    m, bs = S["m"], S["bs"]
+    theta = oracle.model_inv_freq(m.rope_dim, m.rope_theta, m.llama3)
+    pairing = oracle.NEOX_HALF if m.pairing == "neox" else oracle.INTERLEAVED
+    plan, table = S["plans"][r], S["tables"][r]
+    T = pic.pic_plan_info(plan)["total_tokens"]
+    pos = np.arange(T)
+    blk_i = torch.as_tensor(np.asarray(table)[pos // bs], dtype=torch.long)
+    row_i = torch.as_tensor(pos % bs, dtype=torch.long)
+    kc, vc = S["k_cache"][layers], S["v_cache"][layers]
+    keys = oracle.bf16_bits_to_f64(bits(kc[:, blk_i, row_i]))
+    vals = oracle.bf16_bits_to_f64(bits(vc[:, blk_i, row_i]))
+    segs = []
+    for j in range(pic.pic_plan_info(plan)["num_segments"]):
+        sg = pic.pic_plan_segment(plan, j)
+        n, p0 = sg["num_tokens"], sg["dst_pos"]
+        kind, where = S["sources"][sg["chunk_id"]]
+        t = np.arange(n)
+        if kind == "pool":
+            src = torch.as_tensor(sg["src_tok"] + t, dtype=torch.long)
+            src_k = S["k_pool"][layers][:, src]
+            src_v = S["v_pool"][layers][:, src]
+        else:   # a block-resident chunk, used from its first token (src_tok is -1 there)
+            loc = t
+            blk = torch.as_tensor(np.asarray(where)[loc // bs], dtype=torch.long)
+            row = torch.as_tensor(loc % bs, dtype=torch.long)
+            src_k = S["k_cache"][layers][:, blk, row]
+            src_v = S["v_cache"][layers][:, blk, row]
+        keys[:, p0:p0 + n] = oracle.rotate(oracle.bf16_bits_to_f64(bits(src_k)), sg["delta"], theta, pairing)
+        vals[:, p0:p0 + n] = oracle.bf16_bits_to_f64(bits(src_v))
+        segs.append(oracle.Segment(sg["chunk_id"], sg["src_tok"], n, p0, sg["delta"]))
+    return keys, vals, segs, T
+
+
+@pytest.mark.parametrize("pairing,D,Hkv,G,L,bias_value,rep", [
+    ("neox", 128, 8, 4, 3, -15.0, 1),
+    ("interleaved", 64, 16, 2, 2, 0.0, 1),
+    ("neox", 64, 8, 8, 2, -15.0, 1),
+    ("neox", 128, 8, 8, 2, 0.0, 1),
+    ("interleaved", 128, 2, 1, 2, -15.0, 1),
+    ("neox", 128, 8, 4, 3, -15.0, 6),
+    ("neox", 64, 8, 8, 2, 0.0, 4),
+    ("interleaved", 128, 2, 1, 2, -15.0, 4),
+    ("interleaved", 64, 16, 2, 2, -15.0, 4),
+])
+def test_fused_attention_long_mixed_contexts(pairing, D, Hkv, G, L, bias_value, rep):
+    """Three requests of 250-1,400 positions (times rep): chunks of 1..400
+    tokens (so stages of every length and delta changes inside a CTA's
+    range), inline gaps and a trailing run of inline tokens, a block-resident
+    chunk read from its blocks; every (layer, request, query head) against
+    the oracle.  With rep > 1 every CTA owns many more stages than its ring
+    has slots, so slots are refilled while the others are in flight."""
+    S = _long_setup(pairing, D, Hkv, G, L, seed=4, rep=rep)
+    try:
+        layers = list(range(L))
+        g = torch.Generator().manual_seed(5)
+        q = torch.randn((L, 3, S["Hq"], D), generator=g).to(torch.bfloat16)
+        out = torch.empty((L, 3, S["Hq"], D), dtype=torch.float32, device=DEV)
+        lse = torch.empty((L, 3, S["Hq"]), dtype=torch.float32, device=DEV)
+        ws = torch.empty(pic.pic_attend_workspace_bytes(S["ctx"], S["plans"], S["Hq"], L), dtype=torch.uint8,
+                         device=DEV)
+        scale = 1.0 / math.sqrt(D)
+        pic.pic_attend_decode(S["ctx"], S["plans"], pic.PIC_ATTEND_FUSED, q.to(DEV), scale, S["k_pool"].to(DEV),
+                              S["v_pool"].to(DEV), S["k_cache"].to(DEV), S["v_cache"].to(DEV), out, lse, ws,
+                              sink_bias=bias_value)
+        assert pic.pic_query_device_status(S["ctx"], ws) == 0
+        out, lse = out.cpu().double().numpy(), lse.cpu().double().numpy()
+        qb = bits(q)
+        for r in range(3):
+            keys, vals, segs, T = _context_kv(S, r, layers)
+            bias = oracle.sink_bias(segs, T, 4, bias_value) if bias_value else None
+            for l in layers:
+                o, s = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[l, r]), keys[l], vals[l], scale, bias)
+                np.testing.assert_allclose(out[l, r], o, atol=2e-3, rtol=0)
+                np.testing.assert_allclose(lse[l, r], s, atol=2e-3, rtol=0)
+    finally:
+        pic.pic_destroy(S["ctx"])
+
+
+def test_llama_full_launch_sampled_layers():
+    """The benchmark's launch (Llama-3.1-8B shapes, 32 layers, 32 query heads,
+    10,368 positions, sink bias -15) in one call; layers 0, 17 and 31 against
+    the oracle, and the cache path over the stitched copy against the fused
+    result everywhere."""
+    wl = W.llama31_8b_rag()
+    st = Stitched(wl).run()
+    try:
+        m = wl.model
+        Hq, L = 32, m.num_layers
+        g = torch.Generator(device=DEV)
+        g.manual_seed(11)
+        q = torch.empty((L, 1, Hq, 128), dtype=torch.bfloat16, device=DEV).normal_(0.0, 1.0, generator=g)
+        scale = 1.0 / math.sqrt(128)
+        ws = torch.empty(pic.pic_attend_workspace_bytes(st.ctx, st.plans, Hq, L), dtype=torch.uint8, device=DEV)
+        res = {}
+        for src in (pic.PIC_ATTEND_FUSED, pic.PIC_ATTEND_CACHE):
+            out = torch.empty((L, 1, Hq, 128), dtype=torch.float32, device=DEV)
+            lse = torch.empty((L, 1, Hq), dtype=torch.float32, device=DEV)
+            pic.pic_attend_decode(st.ctx, st.plans, src, q, scale, st.k_pool, st.v_pool, st.k_cache, st.v_cache,
+                                  out, lse, ws, sink_bias=-15.0)
+            assert pic.pic_query_device_status(st.ctx, ws) == 0
+            res[src] = (out.cpu().double().numpy(), lse.cpu().double().numpy())
+        out, lse = res[pic.PIC_ATTEND_FUSED]
+        layers = [0, 17, 31]
+        sources = {}
+        for c, off in enumerate(wl.pool_offsets):
+            sources[pic.pic_lookup_chunk(st.ctx, W.chunk_key(wl.name, c))] = ("pool", off)
+        S = dict(m=m, plans=st.plans, tables=st.tables, sources=sources, bs=m.block_size,
+                 k_pool=st.k_pool[layers].cpu(), v_pool=st.v_pool[layers].cpu(),
+                 k_cache=st.k_cache[layers].cpu(), v_cache=st.v_cache[layers].cpu())
+        keys, vals, segs, T = _context_kv(S, 0, list(range(len(layers))))
+        assert T == 10368
+        bias = oracle.sink_bias(segs, T, 4, -15.0)
+        qb = bits(q)
+        for i, l in enumerate(layers):
+            o, s = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[l, 0]), keys[i], vals[i], scale, bias)
+            np.testing.assert_allclose(out[l, 0], o, atol=2e-3, rtol=0)
+            np.testing.assert_allclose(lse[l, 0], s, atol=2e-3, rtol=0)
+        out_c, lse_c = res[pic.PIC_ATTEND_CACHE]
+        np.testing.assert_allclose(out_c, out, atol=3e-2, rtol=0)
+        np.testing.assert_allclose(lse_c, lse, atol=3e-2, rtol=0)
+    finally:
+        st.close()
+        torch.cuda.empty_cache()
