@@ -44,8 +44,29 @@ Pin status of each function (what outside fact each is checked against is in
 * ``map_request`` / ``apply_mapped`` (virtual block mapping) pinned against the
                          block ids printed on the EPIC runtime figure and
                          against forward RoPE at the mapped positions.
+* ``gear_hashes``        pinned (the explicit 64-token window sum, the closed
+                         form of a constant stream, the window length itself)
+* ``cdc_chunk_ends``     pinned (cuts exactly where the hash is below the
+                         threshold; boundaries follow content when a prefix
+                         shifts a document; min/max length invariants)
+* ``xxh64``              pinned against the system xxHash library (libxxhash)
+                         when it is installed
+* ``s1_windows``         pinned (brute force)
 """
 
+from .cdc_oracle import (  # noqa: F401
+    GEAR_WINDOW,
+    S1_WINDOW,
+    gear_hashes,
+    gear_hashes_window,
+    cdc_chunk_ends,
+    threshold_for_mean,
+    xxh64,
+    fingerprint,
+    registry_key,
+    s1_windows,
+    chunk_document,
+)
 from .pic_oracle import (  # noqa: F401
     NEOX_HALF,
     INTERLEAVED,

@@ -9,7 +9,9 @@ no shifts, no block tables, no recompute lists.  It only draws
 * each request's chunk sequence (which chunk ids, in what order, how many
   tokens taken from the last one);
 * the new positions of the in-place shift workload;
-* the bfloat16 K / V / latent values (N(0, 1)).
+* the bfloat16 K / V / latent values (N(0, 1));
+* token-id documents and the Gear table (one 64-bit random value per
+  vocabulary id) for content-defined chunking.
 
 Random structure comes from splitmix64 (Steele, Lea & Flood, "Fast
 splittable pseudorandom number generators", OOPSLA 2014), one stream per
@@ -29,6 +31,8 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass, field
 from itertools import accumulate
+
+import numpy as np
 
 MASK64 = (1 << 64) - 1
 
@@ -318,3 +322,65 @@ def fill_random_bf16(t, seed: int, purpose: str):
     for i in range(flat.shape[0]):
         flat[i].normal_(0.0, 1.0, generator=g)
     return t
+
+
+# ---------------------------------------------------------------------------
+# token documents for content-defined chunking
+# ---------------------------------------------------------------------------
+
+_GOLDEN_GAMMA = 0x9E3779B97F4A7C15
+
+
+def u64_array(seed: int, purpose: str, n: int) -> np.ndarray:
+    """The first n outputs of Stream(seed, purpose), vectorised (uint64).
+
+    splitmix64 is counter-based: output i is mix(state0 + (i + 1) * gamma),
+    so a whole array is drawn at once and equals the sequential stream."""
+    s0 = np.uint64(Stream(seed, purpose).state)
+    with np.errstate(over="ignore"):
+        z = s0 + np.uint64(_GOLDEN_GAMMA) * np.arange(1, n + 1, dtype=np.uint64)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        return z ^ (z >> np.uint64(31))
+
+
+@dataclass
+class Corpus:
+    """Token-id documents stored back to back (int32), with the Gear table."""
+    name: str
+    vocab: int
+    tokens: np.ndarray        # int32 [n_tokens]
+    offsets: np.ndarray       # int64 [n_docs + 1]
+    gear: np.ndarray          # uint64 [vocab]
+
+    @property
+    def n_docs(self) -> int:
+        return len(self.offsets) - 1
+
+    def doc(self, i: int) -> np.ndarray:
+        return self.tokens[self.offsets[i]:self.offsets[i + 1]]
+
+
+def gear_table(seed: int, vocab: int) -> np.ndarray:
+    """One random 64-bit value per vocabulary id."""
+    return u64_array(seed, "cdc/gear", vocab)
+
+
+def random_tokens(seed: int, purpose: str, n: int, vocab: int) -> np.ndarray:
+    """n token ids, uniform over [0, vocab) (modulo of 64 random bits)."""
+    return (u64_array(seed, purpose, n) % np.uint64(vocab)).astype(np.int32)
+
+
+def corpus_from_lengths(name: str, seed: int, lengths, vocab: int) -> Corpus:
+    offsets = np.zeros(len(lengths) + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    tokens = random_tokens(seed, name + "/tokens", int(offsets[-1]), vocab)
+    return Corpus(name, vocab, tokens, offsets, gear_table(seed, vocab))
+
+
+def rag_corpus(seed: int = 0, n_docs: int = 8192, lo: int = 512, hi: int = 16384, vocab: int = 128256) -> Corpus:
+    """Multi-document RAG corpus: n_docs documents of round(exp(U[ln lo, ln
+    hi])) tokens (mean ~4k), token ids uniform over a Llama-3-sized vocabulary."""
+    st = Stream(seed, "cdc/lengths")
+    lengths = [st.log_uniform_int(lo, hi) for _ in range(n_docs)]
+    return corpus_from_lengths("rag_corpus", seed, lengths, vocab)
