@@ -486,6 +486,162 @@ def run_e2e(rig, steps, warmup):
     return ms, h2d, d2h
 
 
+# ------------------------------------------------- content-defined chunking
+
+CDC_TEXT = ("rag_corpus: 8,192 documents of log-uniform 512-16,384 tokens (37.6M int32 token ids, uniform over a "
+            "128,256-id vocabulary), Gear hash over 64-token windows, xxHash64 fingerprints")
+
+
+def cdc_oracle_sample(corpus, thr, min_len, max_len, budget_s=12.0):
+    """The oracle as it stands, on whole documents until about budget_s seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    n_tok = n_chunks = 0
+    d = 0
+    while d < corpus.n_docs and time.perf_counter() - t0 < budget_s:
+        doc = corpus.doc(d)
+        ends, _ = oracle.chunk_document(list(doc), corpus.gear, thr, min_len, max_len)
+        n_tok += len(doc)
+        n_chunks += len(ends)
+        d += 1
+    return d, n_tok, n_chunks, time.perf_counter() - t0
+
+
+def run_cdc(args):
+    """One step = content-defined chunking of the whole corpus: every kernel
+    of pic_cdc_chunk (offset checks, Gear hash + cut bits, [length rules],
+    counts, scan, chunk ends, fingerprints)."""
+    import torch
+    import torch.distributed as dist
+    import oracle
+    from position_independent_kv_stitch_gb300 import pic
+    from position_independent_kv_stitch_gb300.sharding import max_over_ranks
+    pic.load()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    corpus = W.rag_corpus()
+    thr = oracle.threshold_for_mean(args.cdc_mean) if args.cdc_mean > 0 else 0
+    n_tok, n_docs = len(corpus.tokens), corpus.n_docs
+    tokens = torch.from_numpy(corpus.tokens).to(dev)
+    offsets = torch.from_numpy(corpus.offsets).to(dev)
+    gear = torch.from_numpy(corpus.gear.view(np.int64)).to(dev)
+    cap = n_tok // 4 + n_docs   # room for chunks of 4 tokens on average
+    indptr = torch.empty(n_docs + 1, dtype=torch.int64, device=dev)
+    ends = torch.empty(cap, dtype=torch.int64, device=dev)
+    fps = torch.empty(cap, dtype=torch.int64, device=dev)
+    ws = torch.empty(pic.pic_cdc_workspace_bytes(n_tok), dtype=torch.uint8, device=dev)
+
+    def step(toks=tokens):
+        pic.pic_cdc_chunk(toks, offsets, gear, thr, indptr, ends, fps, args.cdc_min, args.cdc_max, 0, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pic.pic_query_device_status(None, ws) != 0:
+        raise RuntimeError("chunking reported a device error")
+    n_chunks = int(indptr[-1].item())
+    if n_chunks > cap:
+        raise RuntimeError("chunk capacity too small")
+
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    t0.record()
+    for i in range(args.steps):
+        evs[i][0].record()
+        step()
+        evs[i][1].record()
+    t1.record()
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    pic.pic_query_device_status(None, ws)
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, dev)
+    kms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # algorithmic bytes: token ids read once, offsets read, CSR offsets + ends + fingerprints written
+    algo = 4 * n_tok + 8 * (n_docs + 1) * 2 + 16 * n_chunks
+    peak, peak_kind = measured_peak()
+    value = world * algo / (ms * 1e-3) / 1e9
+
+    # end to end: token ids from pinned host memory, chunk ends and fingerprints back
+    htok = torch.from_numpy(corpus.tokens).pin_memory()
+    hends = torch.empty(cap, dtype=torch.int64).pin_memory()
+    hfps = torch.empty(cap, dtype=torch.int64).pin_memory()
+    hind = torch.empty(n_docs + 1, dtype=torch.int64).pin_memory()
+    dtok = torch.empty_like(tokens)
+
+    def e2e_step():
+        dtok.copy_(htok, non_blocking=True)
+        step(dtok)
+        hind.copy_(indptr, non_blocking=True)
+        hends[:n_chunks].copy_(ends[:n_chunks], non_blocking=True)
+        hfps[:n_chunks].copy_(fps[:n_chunks], non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        k = max(3, min(args.steps, 20))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(k):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        ems = max_over_ranks(a.elapsed_time(b) / k, dev)
+        e2e = {"value": world * algo / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": 4 * n_tok, "d2h_bytes_per_step": 8 * (n_docs + 1) + 16 * n_chunks,
+               "how": "token ids copied from pinned host memory, chunk offsets, ends and fingerprints copied back"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        d, ntk, nch, el = cdc_oracle_sample(corpus, thr, args.cdc_min, args.cdc_max)
+        cpu_algo = 4 * ntk + 16 * nch + 16 * (d + 1)
+        cpu = {"value": cpu_algo / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {d} documents ({ntk} tokens, {nch} chunks, {el:.1f} s, Python, single thread)",
+               "tokens_per_s": ntk / el}
+
+    line = {
+        "metric": "CDC token GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u64", "data": "synthetic",
+        "config": {"workload": CDC_TEXT, "mode": "cdc", "threshold_mean_len": args.cdc_mean,
+                   "min_len": args.cdc_min, "max_len": args.cdc_max, "tokens_per_step_per_gpu": n_tok,
+                   "documents": n_docs, "chunks": n_chunks, "algorithmic_bytes_per_step_per_gpu": algo,
+                   "l2": "no flush: the 150 MB of token ids exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world} (independent corpora per GPU, no collective)"},
+        "tokens_per_s": world * n_tok / (ms * 1e-3),
+        "pct_hbm_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "hbm", "kernel": "pic_cdc_chunk (all launches; k_cdc_hash dominant)",
+                     "achieved": algo / (kms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": algo / (kms * 1e-3) / 1e9 / peak, "peak_source": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": algo, "launch_ms": kms},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (7 if (args.cdc_min > 1 or args.cdc_max > 0) else 6),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,7 +649,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pic", choices=["pic", "reference"])
     ap.add_argument("--workload", default="llama31_8b_rag", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--mode", default="stitch", choices=["stitch", "inplace", "mapped", "attend", "attend_cache"])
+    ap.add_argument("--mode", default="stitch",
+                    choices=["stitch", "inplace", "mapped", "attend", "attend_cache", "cdc"])
+    ap.add_argument("--cdc-mean", type=int, default=64, help="cdc mode: mean chunk length the threshold aims at")
+    ap.add_argument("--cdc-min", type=int, default=0, help="cdc mode: minimum chunk length (0: none)")
+    ap.add_argument("--cdc-max", type=int, default=0, help="cdc mode: maximum chunk length (0: none)")
     ap.add_argument("--q-heads", type=int, default=0, help="query heads for the attend modes (default 4 per KV head)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling captures only)")
@@ -514,6 +674,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, wl)
+        return
+    if args.mode == "cdc":
+        run_cdc(args)
         return
 
     import torch

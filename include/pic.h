@@ -89,6 +89,10 @@ enum { PIC_SCALING_NONE = 0, PIC_SCALING_LLAMA3 = 1 };
 /* Device status word bits (pic_query_device_status). */
 #define PIC_DEV_BAD_BLOCK 0x1u /* a block-table entry was < 0 or >= num_cache_blocks */
 #define PIC_DEV_TIMEOUT 0x2u   /* a bounded wait inside a kernel gave up (never expected) */
+#define PIC_DEV_BAD_TOKEN 0x4u /* chunking: a token id outside [0, vocab); its Gear value taken as 0 */
+#define PIC_DEV_BAD_DOCS 0x8u  /* chunking: document offsets not non-decreasing within [0, n_tokens] */
+#define PIC_DEV_CAPACITY 0x10u /* chunking: more chunks than capacity; the rest were not written */
+#define PIC_DEV_BAD_SPAN 0x20u /* fingerprints: a span outside [0, n_tokens] or with end < start */
 
 /*
  * Model geometry and RoPE settings.
@@ -447,12 +451,83 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
                              int32_t layer_begin, int32_t num_layers, float* out, float* lse,
                              void* d_workspace, size_t workspace_bytes, pic_stream_t stream);
 
+/* ------------------------------------------- content-defined chunking */
+
+/*
+ * Chunk keys from content ([Irminsul] 2.2 "Content-Hash Keying with CDC":
+ * boundaries from a rolling Gear hash over 64-token windows, a chunk ends
+ * where the hash falls below a threshold, each chunk keyed by its xxHash64
+ * fingerprint).  Document d is tokens [offsets[d], offsets[d + 1]) of
+ * d_tokens; documents are chunked independently:
+ *   h_i = 2 h_{i-1} + gear[t_i] (mod 2^64), h = 0 before the document's first
+ *   token (so h_i depends on the 64 tokens t_{i-63} .. t_i only);
+ *   a chunk ends after token i when h_i < threshold -- with min_len > 1 only
+ *   once it holds min_len tokens, with max_len > 0 always once it holds
+ *   max_len -- and the document's last token ends its last chunk.
+ *   fingerprint = XXH64 (published specification) of the chunk's token ids as
+ *   little-endian int32 bytes, with `seed`.  A registry key (pic_register_chunk)
+ *   is the fingerprint's 8 bytes little-endian, zero-padded to 32.
+ *   d_tokens       device int32 [n_tokens], 16-byte aligned.
+ *   d_doc_offsets  device int64 [n_docs + 1]; checked on the device: offsets
+ *                  that are not non-decreasing inside [0, n_tokens] raise
+ *                  PIC_DEV_BAD_DOCS and every count comes out 0.
+ *   d_gear         device uint64 [vocab]: one random 64-bit value per token id.
+ *                  A token outside [0, vocab) counts as Gear value 0 and
+ *                  raises PIC_DEV_BAD_TOKEN.
+ *   threshold      e.g. 2^64 / mean_len for chunks of mean_len tokens on average.
+ * Outputs (device, 8-byte aligned), in document order:
+ *   d_chunk_indptr int64 [n_docs + 1]: document d owns chunks
+ *                  [indptr[d], indptr[d + 1]); indptr[n_docs] is the total,
+ *                  also when it exceeds capacity.
+ *   d_chunk_ends   int64 [capacity]: one past each chunk's last token (a
+ *                  chunk starts where the previous one of its document ended,
+ *                  the first at offsets[d]).
+ *   d_fingerprints uint64 [capacity], or NULL for no fingerprints.
+ * Chunks past capacity are not written and raise PIC_DEV_CAPACITY; read the
+ * total from indptr[n_docs] and call again with a larger buffer.
+ * d_workspace: pic_cdc_workspace_bytes(n_tokens) bytes, 256-byte aligned; its
+ * status word (PIC_DEV_* bits) is read with pic_query_device_status(NULL, ...).
+ * Host-side argument errors return before anything is enqueued.
+ */
+size_t pic_cdc_workspace_bytes(int64_t n_tokens);
+pic_status pic_cdc_chunk(const int32_t* d_tokens, int64_t n_tokens, const int64_t* d_doc_offsets,
+                         int32_t n_docs, const uint64_t* d_gear, int32_t vocab, uint64_t threshold,
+                         int32_t min_len, int32_t max_len, uint64_t seed, int64_t* d_chunk_indptr,
+                         int64_t* d_chunk_ends, uint64_t* d_fingerprints, int64_t capacity,
+                         void* d_workspace, size_t workspace_bytes, pic_stream_t stream);
+
+/*
+ * XXH64 of arbitrary token spans: d_out[k] = XXH64(token ids [d_starts[k],
+ * d_ends[k]) as little-endian int32 bytes, seed) -- the fingerprint
+ * pic_cdc_chunk computes, for spans the caller chooses (the S1 windows of a
+ * chunk that missed the registry, [Irminsul] "Hybrid Strategies (S1/S2)").
+ *   d_tokens  device int32 [n_tokens], 4-byte aligned.
+ *   d_starts, d_ends  device int64 [n_spans]; d_out device uint64 [n_spans].
+ *   d_status  device uint32, set to 0 and then OR-ed with PIC_DEV_BAD_SPAN for
+ *             a span outside [0, n_tokens] or with end < start (its digest
+ *             is written as 0).
+ */
+pic_status pic_fingerprint_spans(const int32_t* d_tokens, int64_t n_tokens, const int64_t* d_starts,
+                                 const int64_t* d_ends, int64_t n_spans, uint64_t seed, uint64_t* d_out,
+                                 uint32_t* d_status, pic_stream_t stream);
+
+/*
+ * S1 fallback windows of a chunk [begin, end) that missed the registry
+ * ([Irminsul] "Hybrid Strategies (S1/S2)", S1: fixed 128-token windows):
+ * window k is [begin + window*k, min(begin + window*(k + 1), end)).  Host
+ * arrays; *count receives the number of windows; starts and ends may both be
+ * NULL to query it; PIC_ERR_CAPACITY when count > capacity.
+ */
+pic_status pic_s1_windows(int64_t begin, int64_t end, int32_t window, int64_t* starts, int64_t* ends,
+                          int64_t capacity, int64_t* count);
+
 /* ---------------------------------------------------------- diagnostics */
 
 /*
  * Synchronizes `stream`, then reads and clears nothing: returns the device
  * status word the last launch that used d_workspace left (0 = clean) in
- * *status_out, and PIC_ERR_DEVICE_CHECK when it is non-zero.
+ * *status_out, and PIC_ERR_DEVICE_CHECK when it is non-zero.  ctx may be NULL
+ * (a chunking workspace); the message then goes to the calling thread.
  */
 pic_status pic_query_device_status(pic_ctx* ctx, const void* d_workspace, pic_stream_t stream,
                                    uint32_t* status_out);

@@ -1,6 +1,6 @@
 """Builds libpic.so in-tree for GB300 (sm_103a) with nvcc.
 
-Two translation units (host C++ and CUDA kernels) are compiled in parallel and
+The translation units (host C++ and the CUDA kernel files) are compiled in parallel and
 linked against the shared CUDA runtime, so the process uses one runtime with
 PyTorch.  The library is written under a temporary name and renamed into
 place, so a concurrent reader never sees a half-written file.
@@ -23,7 +23,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libpic.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["pic_host.cpp", "pic_kernels.cu", "pic_kernels_tma.cu", "pic_attention.cu", "pic_noalloc.cu"]
+SOURCES = ["pic_host.cpp", "pic_kernels.cu", "pic_kernels_tma.cu", "pic_attention.cu", "pic_noalloc.cu",
+           "pic_cdc.cu"]
 HEADERS = [os.path.join(CSRC, "pic_internal.h"), os.path.join(INCLUDE, "pic.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

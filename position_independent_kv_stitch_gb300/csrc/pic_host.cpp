@@ -1299,7 +1299,6 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
 
 pic_status pic_query_device_status(pic_ctx* ctx, const void* d_ws, pic_stream_t stream,
                                    uint32_t* status_out) {
-  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
   if (!d_ws) return fail(ctx, PIC_ERR_INVALID_ARG, "null workspace");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
@@ -1311,7 +1310,8 @@ pic_status pic_query_device_status(pic_ctx* ctx, const void* d_ws, pic_stream_t 
   if (h.status != 0)
     return fail(ctx, PIC_ERR_DEVICE_CHECK,
                 "kernel reported device status 0x%x (bit 0x1: block-table entry outside the cache, table row %u, "
-                "position %u; bit 0x2: a bounded wait gave up)",
+                "position %u; bit 0x2: a bounded wait gave up; 0x4: token id outside the Gear table; "
+                "0x8: bad document offsets; 0x10: more chunks than capacity; 0x20: bad span)",
                 h.status, h.bad_req, h.bad_pos);
   return ok(ctx);
 }

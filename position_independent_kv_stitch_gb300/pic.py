@@ -29,6 +29,10 @@ PIC_SCALING_NONE, PIC_SCALING_LLAMA3 = 0, 1
 PIC_KEY_BYTES = 32
 PIC_DEV_BAD_BLOCK = 0x1
 PIC_DEV_TIMEOUT = 0x2
+PIC_DEV_BAD_TOKEN = 0x4
+PIC_DEV_BAD_DOCS = 0x8
+PIC_DEV_CAPACITY = 0x10
+PIC_DEV_BAD_SPAN = 0x20
 PIC_VARIANT_REGISTERS, PIC_VARIANT_BULK_PIPELINE = 0, 1
 PIC_SEG_COPY_POOL, PIC_SEG_COPY_BLOCKS, PIC_SEG_MAPPED = 0, 1, 2
 PIC_ATTEND_FUSED, PIC_ATTEND_CACHE = 0, 1
@@ -105,6 +109,13 @@ _SIGNATURES = {
                                          ctypes.c_float, _c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p, _i64,
                                          _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "pic_rotation_cossin": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "pic_cdc_workspace_bytes": (_sz, [_i64]),
+    "pic_cdc_chunk": (ctypes.c_int, [_c_void_p, _i64, _c_void_p, _i32, _c_void_p, _i32, ctypes.c_uint64, _i32,
+                                     _i32, ctypes.c_uint64, _c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _sz,
+                                     _c_void_p]),
+    "pic_fingerprint_spans": (ctypes.c_int, [_c_void_p, _i64, _c_void_p, _c_void_p, _i64, ctypes.c_uint64,
+                                             _c_void_p, _c_void_p, _c_void_p]),
+    "pic_s1_windows": (ctypes.c_int, [_i64, _i64, _i32, _P(_i64), _P(_i64), _i64, _P(_i64)]),
 }
 
 _lib = None
@@ -428,14 +439,97 @@ def pic_rerotate_inplace(ctx, k_cache, block_tables, segs, workspace, stream=Non
     _check(st, ctx)
 
 
-def pic_query_device_status(ctx, workspace, stream=None) -> int:
+def pic_query_device_status(ctx, workspace, stream=None, raise_on_device_error: bool = True) -> int:
     """Synchronizes the stream; returns the device status word (raises on a
-    non-zero word with PIC_ERR_DEVICE_CHECK)."""
+    non-zero word with PIC_ERR_DEVICE_CHECK unless raise_on_device_error is
+    False).  ctx may be None for a chunking workspace."""
     out = ctypes.c_uint32()
     st = load().pic_query_device_status(ctx, _ptr(workspace), _stream_handle(stream), ctypes.byref(out))
+    if st == 9 and not raise_on_device_error:   # PIC_ERR_DEVICE_CHECK
+        return out.value
     if st != PIC_OK:
         raise PicError(st, load().pic_last_error(ctx).decode())
     return out.value
+
+
+# ------------------------------------------------- content-defined chunking
+
+def pic_cdc_workspace_bytes(n_tokens: int) -> int:
+    return int(load().pic_cdc_workspace_bytes(int(n_tokens)))
+
+
+def _check_device(t, dtype, name, allow_none=False):
+    import torch
+    if t is None:
+        if allow_none:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def pic_cdc_chunk(tokens, doc_offsets, gear, threshold: int, chunk_indptr, chunk_ends, fingerprints=None,
+                  min_len: int = 0, max_len: int = 0, seed: int = 0, workspace=None, stream=None):
+    """Content-defined chunking of the documents [offsets[d], offsets[d + 1]) of
+    ``tokens`` (CUDA int32); ``doc_offsets`` CUDA int64 [n_docs + 1]; ``gear``
+    CUDA uint64 (or int64 holding the same bits) [vocab].  Writes
+    ``chunk_indptr`` (int64 [n_docs + 1]), ``chunk_ends`` (int64 [capacity])
+    and ``fingerprints`` (int64/uint64 [capacity], optional).  The workspace
+    is allocated here if not given.  Returns the workspace (its status word is
+    read with pic_query_device_status(None, workspace))."""
+    import torch
+    _check_device(tokens, torch.int32, "tokens")
+    _check_device(doc_offsets, torch.int64, "doc_offsets")
+    if gear.dtype not in (torch.int64, torch.uint64) or not gear.is_cuda or not gear.is_contiguous():
+        raise ValueError("gear must be a contiguous CUDA 64-bit integer tensor")
+    _check_device(chunk_indptr, torch.int64, "chunk_indptr")
+    _check_device(chunk_ends, torch.int64, "chunk_ends")
+    if fingerprints is not None and (fingerprints.dtype not in (torch.int64, torch.uint64) or not fingerprints.is_cuda
+                                     or not fingerprints.is_contiguous()):
+        raise ValueError("fingerprints must be a contiguous CUDA 64-bit integer tensor")
+    n_docs = doc_offsets.numel() - 1
+    if n_docs < 0 or chunk_indptr.numel() < n_docs + 1:
+        raise ValueError("doc_offsets needs n_docs + 1 entries and chunk_indptr as many")
+    cap = chunk_ends.numel()
+    if fingerprints is not None and fingerprints.numel() < cap:
+        raise ValueError("fingerprints must hold as many entries as chunk_ends")
+    if workspace is None:
+        workspace = torch.empty(max(1, pic_cdc_workspace_bytes(tokens.numel())), dtype=torch.uint8,
+                                device=tokens.device)
+    st = load().pic_cdc_chunk(_ptr(tokens), tokens.numel(), _ptr(doc_offsets), n_docs, _ptr(gear), gear.numel(),
+                              int(threshold) & ((1 << 64) - 1), int(min_len), int(max_len),
+                              int(seed) & ((1 << 64) - 1), _ptr(chunk_indptr), _ptr(chunk_ends),
+                              _ptr(fingerprints), cap, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, None)
+    return workspace
+
+
+def pic_fingerprint_spans(tokens, starts, ends, out, status, seed: int = 0, stream=None):
+    """XXH64 of token spans [starts[k], ends[k]) into ``out`` (CUDA 64-bit
+    integers); ``status`` is a CUDA 32-bit tensor that receives PIC_DEV_BAD_SPAN."""
+    import torch
+    _check_device(tokens, torch.int32, "tokens")
+    _check_device(starts, torch.int64, "starts")
+    _check_device(ends, torch.int64, "ends")
+    n = starts.numel()
+    if ends.numel() != n or out.numel() < n or out.element_size() != 8 or not out.is_cuda:
+        raise ValueError("starts, ends and out must hold one 64-bit entry per span")
+    if not status.is_cuda or status.element_size() != 4:
+        raise ValueError("status must be a CUDA 32-bit tensor")
+    st = load().pic_fingerprint_spans(_ptr(tokens), tokens.numel(), _ptr(starts), _ptr(ends), n,
+                                      int(seed) & ((1 << 64) - 1), _ptr(out), _ptr(status), _stream_handle(stream))
+    _check(st, None)
+
+
+def pic_s1_windows(begin: int, end: int, window: int = 128):
+    """(starts, ends) of the fixed windows covering [begin, end), as lists."""
+    lib_ = load()
+    n = ctypes.c_int64()
+    _check(lib_.pic_s1_windows(int(begin), int(end), int(window), None, None, 0, ctypes.byref(n)), None)
+    a = (ctypes.c_int64 * max(1, n.value))()
+    b = (ctypes.c_int64 * max(1, n.value))()
+    _check(lib_.pic_s1_windows(int(begin), int(end), int(window), a, b, n.value, ctypes.byref(n)), None)
+    return list(a[:n.value]), list(b[:n.value])
 
 
 def pic_attend_workspace_bytes(ctx, plans, num_q_heads: int, num_layers: int) -> int:
