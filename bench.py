@@ -65,24 +65,24 @@ def measured_peak():
 KERNEL_SOURCES = ("pic_kernels.cu", "pic_kernels_tma.cu", "pic_host.cpp", "pic_internal.h")
 
 
-def kernel_source_hash():
+def kernel_source_hash(names=KERNEL_SOURCES):
     """Hash of the kernel and launch-schedule sources a traffic record was taken on."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "position_independent_kv_stitch_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload, mode):
+def recorded_traffic(key):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel source as it is now."""
+    the sources (the record's own list) as they are now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d.get(f"{workload}/{mode}")
-        if e and e.get("kernel_source_sha256_16") == kernel_source_hash():
+        e = d.get(key)
+        if e and e.get("kernel_source_sha256_16") == kernel_source_hash(tuple(e.get("sources", KERNEL_SOURCES))):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -629,11 +629,12 @@ def run_cdc(args):
         "pct_hbm_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "hbm", "kernel": "pic_cdc_chunk (all launches; k_cdc_hash dominant)",
                      "achieved": algo / (kms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": algo / (kms * 1e-3) / 1e9 / peak, "peak_source": peak_kind, "traffic": None,
+                     "frac": algo / (kms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
+                     "traffic": recorded_traffic("rag_corpus/cdc" if not (args.cdc_min or args.cdc_max) else "-"),
                      "algorithmic_bytes_per_launch": algo, "launch_ms": kms},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (7 if (args.cdc_min > 1 or args.cdc_max > 0) else 6),
+        "gpu_launches": args.steps * (7 if (args.cdc_min > 1 or args.cdc_max > 0) else 5),
         "clocks": clk,
     }
     if rank == 0:
@@ -734,7 +735,7 @@ def main():
     peak, peak_kind = measured_peak()
     value = world * algo_bytes / (ms * 1e-3) / 1e9
     achieved = algo_bytes / (kms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name, args.mode)
+    traffic = recorded_traffic(f"{wl.name}/{args.mode}")
 
     e2e = None
     if not args.no_e2e and args.mode == "stitch":
@@ -756,8 +757,8 @@ def main():
     else:
         kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
                  "mapped": "k_rotate_rows<stitch, mapped chunks in place>",
-                 "attend": "k_attend_tiles + k_attend_combine (fused delta-rotation)",
-                 "attend_cache": "k_rotate_rows<stitch> then k_attend_tiles + k_attend_combine",
+                 "attend": "k_attend + k_attend_merge (fused delta-rotation)",
+                 "attend_cache": "k_rotate_rows<stitch> then k_attend + k_attend_merge",
                  "inplace": "k_rotate_rows<in place>"}[args.mode]
     line = {
         "metric": "stitched KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

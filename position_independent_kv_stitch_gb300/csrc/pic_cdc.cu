@@ -23,14 +23,19 @@
 //   k_cdc_docs   checks the document offsets; for every 8192-token tile finds
 //                the first document boundary its hash window can see.
 //   k_cdc_hash   one CTA per tile: token ids by 16-byte loads, one Gear
-//                gather per token, every position's hash, one cut bit each.
+//                gather per token, every position's hash, one cut bit each,
+//                and the tile's cut count.
 //   k_cdc_walk   (min_len > 1 or max_len > 0 only) one warp per document
-//                walks its cut candidates and applies the length rules.
-//   k_cdc_count  one warp per document: its chunk count.
-//   k_cdc_scan   one CTA: counts -> chunk CSR offsets.
-//   k_cdc_emit   one warp per document: chunk ends in document order (the
-//                chunk starts are parked in the fingerprint buffer).
+//                walks its cut candidates and applies the length rules; then
+//                k_cdc_tile_count recounts the tiles.
+//   k_cdc_scan   one CTA: tile counts -> each tile's first chunk index.
+//   k_cdc_emit   one CTA per tile: chunk ends, numbered in position order,
+//                and the CSR offset of every document starting in the tile.
 //   k_xxh64      four lanes per chunk: XXH64 of the chunk's token bytes.
+// Documents are contiguous and each one's last token ends a chunk, so chunks
+// numbered in position order are in document order, document d's first
+// chunk index is the number of cuts before offsets[d], and chunk c starts
+// where chunk c - 1 ends (chunk 0 at offsets[0]).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -63,8 +68,9 @@ constexpr uint64_t kP4 = 0x85EBCA77C2B2AE63ull;
 constexpr uint64_t kP5 = 0x27D4EB2F165667C5ull;
 
 struct CdcLayout {
-  size_t first_doc;  // int32 per tile
-  size_t bits;       // uint32 cut words, kTileWords per tile
+  size_t first_doc;   // int32 per tile
+  size_t tile_count;  // int64 per tile + 1: cut counts, then each tile's first chunk index and the total
+  size_t bits;        // uint32 cut words, kTileWords per tile
   size_t total;
 };
 
@@ -72,7 +78,8 @@ CdcLayout cdc_layout(int64_t n_tokens) {
   const int64_t n_tiles = (n_tokens + kTile - 1) / kTile;
   CdcLayout l;
   l.first_doc = kWsAlign;
-  l.bits = l.first_doc + align_up(static_cast<size_t>(n_tiles) * 4, kWsAlign);
+  l.tile_count = l.first_doc + align_up(static_cast<size_t>(n_tiles) * 4, kWsAlign);
+  l.bits = l.tile_count + align_up(static_cast<size_t>(n_tiles + 1) * 8, kWsAlign);
   l.total = l.bits + align_up(static_cast<size_t>(n_tiles) * kTileWords * 4, kWsAlign);
   return l;
 }
@@ -113,7 +120,8 @@ __device__ __forceinline__ bool docs_bad(const WsHeader* h) {
 // owns the tiles whose window start falls in (offsets[d - 1], offsets[d]],
 // with offsets[-1] = -inf and offsets[n_docs + 1] = +inf.
 __global__ void k_cdc_docs(const int64_t* __restrict__ offsets, int32_t n_docs, int64_t n_tokens,
-                           int32_t* __restrict__ first_doc, int64_t n_tiles, WsHeader* hdr) {
+                           int32_t* __restrict__ first_doc, int64_t* __restrict__ tile_count, int64_t n_tiles,
+                           WsHeader* hdr) {
   const int64_t n = static_cast<int64_t>(n_docs) + 2;
   for (int64_t d = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; d < n;
        d += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -129,7 +137,10 @@ __global__ void k_cdc_docs(const int64_t* __restrict__ offsets, int32_t n_docs, 
     if (d > 0 && prev + kHalo < 0) k_lo = 0;
     int64_t k_hi = d == n_docs + 1 ? n_tiles - 1 : (cur + kHalo) / kTile;
     if (k_hi > n_tiles - 1) k_hi = n_tiles - 1;
-    for (int64_t k = k_lo; k <= k_hi; ++k) first_doc[k] = static_cast<int32_t>(d);
+    for (int64_t k = k_lo; k <= k_hi; ++k) {
+      first_doc[k] = static_cast<int32_t>(d);
+      tile_count[k] = 0;
+    }
   }
 }
 
@@ -147,8 +158,8 @@ __global__ void k_cdc_docs(const int64_t* __restrict__ offsets, int32_t n_docs, 
 __global__ void __launch_bounds__(kHashThreads, 2)
 k_cdc_hash(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* __restrict__ offsets,
            int32_t n_docs, const uint64_t* __restrict__ gear, uint32_t vocab, uint64_t threshold,
-           const int32_t* __restrict__ first_doc, uint32_t* __restrict__ bits, int64_t n_tiles,
-           WsHeader* hdr) {
+           const int32_t* __restrict__ first_doc, uint32_t* __restrict__ bits,
+           unsigned long long* __restrict__ tile_count, int64_t n_tiles, WsHeader* hdr) {
   __shared__ int32_t s_tok[kTokPad];
   __shared__ uint32_t s_bnd[kBndWords];
   __shared__ uint64_t s_part[kHashThreads + 2];  // B_j at index j + 2; halo blocks -2, -1 at 0, 1
@@ -254,7 +265,10 @@ k_cdc_hash(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* 
     const int64_t b = in_hi - p0 < 0 ? 0 : (in_hi - p0 > 32 ? 32 : in_hi - p0);
     uint32_t inside = 0;
     if (b > a) inside = (b == 32 ? kFull : ((1u << b) - 1u)) & ~((1u << a) - 1u);
-    bits[tile * kTileWords + tid] = (cut | ends) & inside;
+    const uint32_t word = (cut | ends) & inside;
+    bits[tile * kTileWords + tid] = word;
+    const unsigned n_cut = __reduce_add_sync(kFull, static_cast<unsigned>(__popc(word)));
+    if (lane == 0 && n_cut) atomicAdd(&tile_count[tile], static_cast<unsigned long long>(n_cut));
   }
   if (__syncthreads_or(bad_token) && tid == 0) atomicOr(&hdr->status, PIC_DEV_BAD_TOKEN);
 }
@@ -320,48 +334,46 @@ k_cdc_walk(const int64_t* __restrict__ offsets, int32_t n_docs, uint32_t* bits, 
 
 // ---------------------------------------------------------------- counts, scan
 
+// One warp per tile: its cut count (after the length rules rewrote the bits).
 __global__ void __launch_bounds__(kWarpThreads)
-k_cdc_count(const int64_t* __restrict__ offsets, int32_t n_docs, const uint32_t* __restrict__ bits,
-            int64_t* __restrict__ indptr, const WsHeader* hdr) {
-  const bool bad = docs_bad(hdr);
+k_cdc_tile_count(const uint32_t* __restrict__ bits, int64_t* __restrict__ tile_count, int64_t n_tiles,
+                 const WsHeader* hdr) {
+  if (docs_bad(hdr)) return;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t d = warp; d < n_docs; d += n_warps) {
-    int64_t count = 0;
-    if (!bad) {
-      const int64_t ds = offsets[d], de = offsets[d + 1];
-      if (ds < de) {
-        const int64_t w_last = (de - 1) >> 5;
-        for (int64_t w = (ds >> 5) + lane; w <= w_last; w += 32)
-          count += __popc(bits[w] & word_mask(w, ds, de));
-      }
+  for (int64_t t = warp; t < n_tiles; t += n_warps) {
+    unsigned c = 0;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) count += __shfl_xor_sync(kFull, count, o);
-    }
-    if (lane == 0) indptr[d + 1] = count;
+    for (int k = 0; k < kTileWords / 32; ++k) c += __popc(bits[t * kTileWords + k * 32 + lane]);
+    c = __reduce_add_sync(kFull, c);
+    if (lane == 0) tile_count[t] = c;
   }
 }
 
-// Single CTA: indptr[d + 1] holds document d's count on entry and the running
-// total through document d on exit; indptr[0] = 0.
+// Single CTA: tile_count[k] holds tile k's cut count on entry and the number
+// of cuts before tile k on exit; tile_count[n_tiles] receives the total.
+// With bad offsets it writes indptr = 0 instead; with no tiles (no tokens)
+// every offset is 0 and so is every indptr entry.
 __global__ void __launch_bounds__(kScanThreads)
-k_cdc_scan(int64_t* __restrict__ indptr, int32_t n_docs, int64_t capacity, WsHeader* hdr) {
+k_cdc_scan(int64_t* __restrict__ tile_count, int64_t n_tiles, int64_t* __restrict__ indptr, int32_t n_docs,
+           int64_t capacity, WsHeader* hdr) {
   __shared__ int64_t s_warp[kScanThreads / 32];
   __shared__ int64_t s_carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == 0) {
-    s_carry = 0;
-    indptr[0] = 0;
+  if (docs_bad(hdr) || n_tiles == 0) {
+    for (int64_t d = tid; d <= n_docs; d += kScanThreads) indptr[d] = 0;
+    return;
   }
+  if (tid == 0) s_carry = 0;
   __syncthreads();
-  for (int64_t base = 0; base < n_docs; base += kScanThreads * kScanPerThread) {
+  for (int64_t base = 0; base < n_tiles; base += kScanThreads * kScanPerThread) {
     int64_t v[kScanPerThread];
     int64_t sum = 0;
 #pragma unroll
     for (int k = 0; k < kScanPerThread; ++k) {
       const int64_t i = base + tid * kScanPerThread + k;
-      v[k] = i < n_docs ? indptr[i + 1] : 0;
+      v[k] = i < n_tiles ? tile_count[i] : 0;
       sum += v[k];
     }
     int64_t incl = sum;
@@ -386,158 +398,219 @@ k_cdc_scan(int64_t* __restrict__ indptr, int32_t n_docs, int64_t capacity, WsHea
 #pragma unroll
     for (int k = 0; k < kScanPerThread; ++k) {
       const int64_t i = base + tid * kScanPerThread + k;
+      if (i < n_tiles) tile_count[i] = run;
       run += v[k];
-      if (i < n_docs) indptr[i + 1] = run;
     }
     __syncthreads();
     if (tid == 0) s_carry += s_warp[kScanThreads / 32 - 1];
     __syncthreads();
   }
-  if (tid == 0 && s_carry > capacity) atomicOr(&hdr->status, PIC_DEV_CAPACITY);
+  if (tid == 0) {
+    tile_count[n_tiles] = s_carry;
+    if (s_carry > capacity) atomicOr(&hdr->status, PIC_DEV_CAPACITY);
+  }
 }
 
 // ---------------------------------------------------------------- emission
 
-// One warp per document: chunk c of the document (global index indptr[d] + c)
-// gets ends[c] = one past its last token and starts[c] = its first token.
-// Nothing past `capacity` is written.
-__global__ void __launch_bounds__(kWarpThreads)
+// One CTA per tile, one thread per cut word.  Chunk index = cuts before the
+// tile + rank inside it; ends[index] = one past the cut token.  Every document
+// offset inside the tile (offsets[n_docs] included) gets indptr = the number
+// of cuts before it.  Nothing at or past `capacity` is written to ends.
+__global__ void __launch_bounds__(kHashThreads)
 k_cdc_emit(const int64_t* __restrict__ offsets, int32_t n_docs, const uint32_t* __restrict__ bits,
-           const int64_t* __restrict__ indptr, int64_t* __restrict__ ends, int64_t* starts,
-           int64_t capacity, const WsHeader* hdr) {
+           const int64_t* __restrict__ tile_first, const int32_t* __restrict__ first_doc, int64_t n_tiles,
+           int64_t* __restrict__ ends, int64_t capacity, int64_t* __restrict__ indptr, const WsHeader* hdr) {
+  __shared__ int32_t s_warp[kHashThreads / 32];
+  __shared__ int32_t s_pref[kTileWords];
+  __shared__ uint32_t s_word[kTileWords];
   if (docs_bad(hdr)) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t d = warp; d < n_docs; d += n_warps) {
-    const int64_t ds = offsets[d], de = offsets[d + 1];
-    if (ds >= de) continue;
-    int64_t base = indptr[d];
-    if (base >= capacity) continue;
-    int64_t next_start = ds;  // first token of the next chunk
-    const int64_t w_last = (de - 1) >> 5;
-    for (int64_t wb = ds >> 5; wb <= w_last; wb += 32) {
-      const int64_t w = wb + lane;
-      const uint32_t m = w <= w_last ? (bits[w] & word_mask(w, ds, de)) : 0u;
-      const int n = __popc(m);
-      int incl = n;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t t0 = tile * kTile;
+    const uint32_t word = bits[tile * kTileWords + tid];
+    const int n = __popc(word);
+    int incl = n;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += t;
-      }
-      // end of the last chunk closed by this lane's word, max-scanned over lanes
-      int64_t last_end = m ? (w << 5) + 32 - __clz(m) : -1;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    __syncthreads();  // the previous tile is done with shared memory
+    if (lane == 31) s_warp[wid] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t t = __shfl_up_sync(kFull, last_end, o);
-        if (lane >= o && t > last_end) last_end = t;
+    for (int k = 0; k < kHashThreads / 32; ++k) {
+      const int c = s_warp[k];
+      before += k < wid ? c : 0;
+      total += c;
+    }
+    const int excl = before + incl - n;
+    s_pref[tid] = excl;
+    s_word[tid] = word;
+    const int64_t base = tile_first[tile];
+    int64_t idx = base + excl;
+    uint32_t m = word;
+    while (m) {
+      const int b = __ffs(m) - 1;
+      m &= m - 1u;
+      if (idx < capacity) ends[idx] = t0 + 32 * tid + b + 1;
+      ++idx;
+    }
+    __syncthreads();  // s_pref, s_word complete
+    const bool last = tile == n_tiles - 1;
+    for (int64_t d = static_cast<int64_t>(first_doc[tile]) + tid; d <= n_docs; d += kHashThreads) {
+      const int64_t o = offsets[d];
+      if (o < t0) continue;  // seen by the tile's hash window, but lies in the tile before
+      if (o >= t0 + kTile) {
+        if (!last) break;    // offsets are non-decreasing
+        indptr[d] = base + total;  // o == n_tokens at the end of the last tile
+        continue;
       }
-      int64_t prev = __shfl_up_sync(kFull, last_end, 1);
-      if (lane == 0) prev = -1;
-      int64_t s = prev >= 0 ? prev : next_start;
-      int64_t idx = base + incl - n;
-      uint32_t mm = m;
-      while (mm) {
-        const int bpos = __ffs(mm) - 1;
-        mm &= mm - 1u;
-        const int64_t e = (w << 5) + bpos + 1;
-        if (idx < capacity) {
-          ends[idx] = e;
-          if (starts) starts[idx] = s;
-        }
-        s = e;
-        ++idx;
-      }
-      base += __shfl_sync(kFull, incl, 31);
-      const int64_t le = __shfl_sync(kFull, last_end, 31);
-      if (le >= 0) next_start = le;
+      const int r = static_cast<int>(o - t0);
+      const int w = r >> 5, bit = r & 31;
+      indptr[d] = base + s_pref[w] + __popc(s_word[w] & ((1u << bit) - 1u));
     }
   }
 }
 
 // ---------------------------------------------------------------- XXH64
 
-// Four lanes per span: lane j runs accumulator j over the span's 32-byte
-// stripes (bytes 8j .. 8j + 7 of each), lane 0 merges them and hashes the
-// tail.  `starts` may alias `out` (each span's start is read by its own lanes
-// before its digest is written), so neither is __restrict__.  The span count
-// is *n_dev (clamped to cap) when n_dev is given, else n_host.
+// XXH64 of spans of token ids, in two phases per CTA batch of spans:
+//   A: a 4-lane group runs the four stripe accumulators of one span (lane j
+//      takes bytes 8j .. 8j + 7 of every 32-byte stripe) and parks them in
+//      shared memory; groups take the batch's spans from a shared counter, so
+//      long and short spans keep every group busy.
+//   B: one thread per span merges the accumulators, hashes the tail (at most
+//      seven tokens), adds the length and applies the avalanche.
+// Every lane of phase B runs the same code, so the serial finishing steps do
+// not leave three of four lanes idle.  Each CTA owns a contiguous range of
+// spans.
+//   starts == nullptr: span c starts where span c - 1 ends (span 0 at
+//   *first_start): the chunks of pic_cdc_chunk.
+//   n_dev != nullptr: the span count is *n_dev, clamped to cap.
+constexpr int kXxhBatch = 1024;             // spans per CTA batch
+constexpr int kXxhGroups = kXxhThreads / 4; // 4-lane groups per CTA
+constexpr int kXxhU = 8;                    // stripes per group step
+
+struct SpanInfo {
+  const int32_t* p;
+  int64_t ntok;
+  bool bad;
+};
+
+__device__ __forceinline__ SpanInfo span_info(const int32_t* tokens, int64_t n_tokens, const int64_t* starts,
+                                              const int64_t* first_start, const int64_t* ends, int64_t c) {
+  const int64_t e = ends[c];
+  const int64_t s = starts ? starts[c] : (c > 0 ? ends[c - 1] : *first_start);
+  SpanInfo r;
+  r.bad = s < 0 || e < s || e > n_tokens;
+  r.ntok = r.bad ? 0 : e - s;
+  r.p = tokens + (r.bad ? 0 : s);
+  return r;
+}
+
 __global__ void __launch_bounds__(kXxhThreads)
-k_xxh64(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* starts,
-        const int64_t* __restrict__ ends, const int64_t* __restrict__ n_dev, int64_t n_host, int64_t cap,
-        uint64_t seed, uint64_t* out, uint32_t* status, const WsHeader* hdr) {
+k_xxh64(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* __restrict__ starts,
+        const int64_t* __restrict__ first_start, const int64_t* __restrict__ ends,
+        const int64_t* __restrict__ n_dev, int64_t n_host, int64_t cap, uint64_t seed, uint64_t* __restrict__ out,
+        uint32_t* status, const WsHeader* hdr) {
+  __shared__ uint64_t s_acc[4][kXxhBatch];
+  __shared__ int s_next;
   if (hdr && docs_bad(hdr)) return;
   int64_t n = n_host;
   if (n_dev) {
     n = *n_dev;
     if (n > cap) n = cap;
   }
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
   const int j = lane & 3;
-  const unsigned gmask = 0xfu << (lane & ~3);
-  const int64_t group = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 2;
-  const int64_t n_groups = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 2;
-  for (int64_t c = group; c < n; c += n_groups) {
-    const int64_t s = starts[c], e = ends[c];
-    if (s < 0 || e < s || e > n_tokens) {
-      __syncwarp(gmask);
-      if (j == 0) {
-        out[c] = 0;
-        atomicOr(status, PIC_DEV_BAD_SPAN);
-      }
-      continue;
+  const int g0 = lane & ~3;
+  const unsigned gmask = 0xfu << g0;
+  uint64_t v_init = seed;
+  if (j == 0) v_init = seed + kP1 + kP2;
+  else if (j == 1) v_init = seed + kP2;
+  else if (j == 3) v_init = seed - kP1;
+  const int64_t c_lo = n * blockIdx.x / gridDim.x, c_hi = n * (blockIdx.x + 1) / gridDim.x;
+
+  for (int64_t b0 = c_lo; b0 < c_hi; b0 += kXxhBatch) {
+    const int nb = static_cast<int>(c_hi - b0 < kXxhBatch ? c_hi - b0 : kXxhBatch);
+    if (tid == 0) s_next = kXxhGroups;
+    __syncthreads();
+    // phase A: stripes.  One flat loop: every iteration advances each group's
+    // span by up to kXxhU stripes; a group whose span is done parks its
+    // accumulators and takes the next span in the same iteration, so the
+    // warp never waits at a loop exit for its longest span.
+    int k = tid >> 2;
+    const int32_t* q = tokens;
+    int64_t left = 0;  // stripes still to run on span k
+    uint64_t v = v_init;
+    if (k < nb) {
+      const SpanInfo sp = span_info(tokens, n_tokens, starts, first_start, ends, b0 + k);
+      left = sp.ntok >> 3;  // 32 bytes = 8 tokens
+      q = sp.p + 2 * j;
     }
-    const int64_t ntok = e - s;
-    const int32_t* p = tokens + s;
-    const int64_t stripes = ntok >> 3;  // 32 bytes = 8 tokens
-    uint64_t acc;
-    if (stripes > 0) {
-      uint64_t v = seed;
-      if (j == 0) v = seed + kP1 + kP2;
-      else if (j == 1) v = seed + kP2;
-      else if (j == 3) v = seed - kP1;
-      const int32_t* q = p + 2 * j;
-      int64_t st = 0;
-      for (; st + 4 <= stripes; st += 4) {
-        uint32_t lo[4], hi[4];
+    while (__any_sync(kFull, k < nb)) {
+      if (k < nb && left > 0) {
+        const int m = left < kXxhU ? static_cast<int>(left) : kXxhU;
+        uint32_t lo[kXxhU], hi[kXxhU];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          lo[u] = static_cast<uint32_t>(__ldg(q + 8 * (st + u)));
-          hi[u] = static_cast<uint32_t>(__ldg(q + 8 * (st + u) + 1));
+        for (int u = 0; u < kXxhU; ++u) {
+          lo[u] = 0u;
+          hi[u] = 0u;
+          if (u < m) {
+            lo[u] = static_cast<uint32_t>(__ldg(q + 8 * u));
+            hi[u] = static_cast<uint32_t>(__ldg(q + 8 * u + 1));
+          }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v = xxh_round(v, lo[u] | (static_cast<uint64_t>(hi[u]) << 32));
+        for (int u = 0; u < kXxhU; ++u)
+          if (u < m) v = xxh_round(v, lo[u] | (static_cast<uint64_t>(hi[u]) << 32));
+        left -= m;
+        q += 8 * m;
       }
-      for (; st < stripes; ++st) {
-        const uint32_t lo = static_cast<uint32_t>(__ldg(q + 8 * st));
-        const uint32_t hi = static_cast<uint32_t>(__ldg(q + 8 * st + 1));
-        v = xxh_round(v, lo | (static_cast<uint64_t>(hi) << 32));
+      if (k < nb && left == 0) {
+        s_acc[j][k] = v;
+        int nk = 0;
+        if (j == 0) nk = atomicAdd(&s_next, 1);
+        k = __shfl_sync(gmask, nk, g0);
+        v = v_init;
+        if (k < nb) {
+          const SpanInfo sp = span_info(tokens, n_tokens, starts, first_start, ends, b0 + k);
+          left = sp.ntok >> 3;
+          q = sp.p + 2 * j;
+        }
       }
-      const int g0 = lane & ~3;
-      const uint64_t v1 = __shfl_sync(gmask, v, g0);
-      const uint64_t v2 = __shfl_sync(gmask, v, g0 + 1);
-      const uint64_t v3 = __shfl_sync(gmask, v, g0 + 2);
-      const uint64_t v4 = __shfl_sync(gmask, v, g0 + 3);
-      acc = rotl64(v1, 1) + rotl64(v2, 7) + rotl64(v3, 12) + rotl64(v4, 18);
-      acc = xxh_merge(acc, v1);
-      acc = xxh_merge(acc, v2);
-      acc = xxh_merge(acc, v3);
-      acc = xxh_merge(acc, v4);
-    } else {
-      acc = seed + kP5;
     }
-    if (j == 0) {
-      acc += static_cast<uint64_t>(ntok) * 4u;
+    __syncthreads();
+    // phase B: one thread per span
+    for (int k = tid; k < nb; k += kXxhThreads) {
+      const int64_t c = b0 + k;
+      const SpanInfo sp = span_info(tokens, n_tokens, starts, first_start, ends, c);
+      const int64_t stripes = sp.ntok >> 3;
+      uint64_t acc;
+      if (stripes > 0) {
+        const uint64_t v1 = s_acc[0][k], v2 = s_acc[1][k], v3 = s_acc[2][k], v4 = s_acc[3][k];
+        acc = rotl64(v1, 1) + rotl64(v2, 7) + rotl64(v3, 12) + rotl64(v4, 18);
+        acc = xxh_merge(acc, v1);
+        acc = xxh_merge(acc, v2);
+        acc = xxh_merge(acc, v3);
+        acc = xxh_merge(acc, v4);
+      } else {
+        acc = seed + kP5;
+      }
+      acc += static_cast<uint64_t>(sp.ntok) * 4u;
       int64_t t = stripes << 3;
-      for (; t + 2 <= ntok; t += 2) {
-        const uint64_t k = static_cast<uint32_t>(__ldg(p + t)) |
-                           (static_cast<uint64_t>(static_cast<uint32_t>(__ldg(p + t + 1))) << 32);
-        acc ^= xxh_round(0, k);
+      for (; t + 2 <= sp.ntok; t += 2) {
+        const uint64_t w = static_cast<uint32_t>(__ldg(sp.p + t)) |
+                           (static_cast<uint64_t>(static_cast<uint32_t>(__ldg(sp.p + t + 1))) << 32);
+        acc ^= xxh_round(0, w);
         acc = rotl64(acc, 27) * kP1 + kP4;
       }
-      if (t < ntok) {
-        acc ^= static_cast<uint64_t>(static_cast<uint32_t>(__ldg(p + t))) * kP1;
+      if (t < sp.ntok) {
+        acc ^= static_cast<uint64_t>(static_cast<uint32_t>(__ldg(sp.p + t))) * kP1;
         acc = rotl64(acc, 23) * kP2 + kP3;
       }
       acc ^= acc >> 33;
@@ -545,9 +618,13 @@ k_xxh64(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* sta
       acc ^= acc >> 29;
       acc *= kP3;
       acc ^= acc >> 32;
+      if (sp.bad) {
+        acc = 0;
+        atomicOr(status, PIC_DEV_BAD_SPAN);
+      }
+      out[c] = acc;
     }
-    __syncwarp(gmask);  // every lane of the group has read starts[c]
-    if (j == 0) out[c] = acc;
+    __syncthreads();  // the next batch reuses s_acc and s_next
   }
 }
 
@@ -612,6 +689,7 @@ extern "C" pic_status pic_cdc_chunk(const int32_t* d_tokens, int64_t n_tokens, c
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   int32_t* first_doc = reinterpret_cast<int32_t*>(ws + lay.first_doc);
+  int64_t* tile_count = reinterpret_cast<int64_t*>(ws + lay.tile_count);
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws + lay.bits);
   const int64_t n_tiles = (n_tokens + kTile - 1) / kTile;
   const int sms = sm_count();
@@ -623,27 +701,28 @@ extern "C" pic_status pic_cdc_chunk(const int32_t* d_tokens, int64_t n_tokens, c
     int64_t grid = (work + 255) / 256;
     if (grid > static_cast<int64_t>(sms) * 4) grid = static_cast<int64_t>(sms) * 4;
     k_cdc_docs<<<static_cast<int>(grid < 1 ? 1 : grid), 256, 0, s>>>(d_doc_offsets, n_docs, n_tokens, first_doc,
-                                                                      n_tiles, hdr);
+                                                                      tile_count, n_tiles, hdr);
   }
   if (n_tiles > 0) {
-    int64_t grid = n_tiles < static_cast<int64_t>(sms) * 2 ? n_tiles : static_cast<int64_t>(sms) * 2;
-    k_cdc_hash<<<static_cast<int>(grid), kHashThreads, 0, s>>>(d_tokens, n_tokens, d_doc_offsets, n_docs, d_gear,
-                                                               static_cast<uint32_t>(vocab), threshold, first_doc,
-                                                               bits, n_tiles, hdr);
-  }
-  const int wgrid = warp_grid(n_docs, sms);
-  if (n_docs > 0 && (min_len > 1 || max_len > 0))
-    k_cdc_walk<<<wgrid, kWarpThreads, 0, s>>>(d_doc_offsets, n_docs, bits, min_len, max_len, hdr);
-  if (n_docs > 0) k_cdc_count<<<wgrid, kWarpThreads, 0, s>>>(d_doc_offsets, n_docs, bits, d_chunk_indptr, hdr);
-  k_cdc_scan<<<1, kScanThreads, 0, s>>>(d_chunk_indptr, n_docs, capacity, hdr);
-  if (n_docs > 0 && capacity > 0) {
-    int64_t* starts = reinterpret_cast<int64_t*>(d_fingerprints);  // parked there until hashed
-    k_cdc_emit<<<wgrid, kWarpThreads, 0, s>>>(d_doc_offsets, n_docs, bits, d_chunk_indptr, d_chunk_ends, starts,
-                                               capacity, hdr);
-    if (d_fingerprints) {
-      k_xxh64<<<sms * 8, kXxhThreads, 0, s>>>(d_tokens, n_tokens, starts, d_chunk_ends, d_chunk_indptr + n_docs, 0,
-                                              capacity, seed, d_fingerprints, &hdr->status, hdr);
+    const int grid = static_cast<int>(n_tiles < static_cast<int64_t>(sms) * 2 ? n_tiles : static_cast<int64_t>(sms) * 2);
+    k_cdc_hash<<<grid, kHashThreads, 0, s>>>(d_tokens, n_tokens, d_doc_offsets, n_docs, d_gear,
+                                             static_cast<uint32_t>(vocab), threshold, first_doc, bits,
+                                             reinterpret_cast<unsigned long long*>(tile_count), n_tiles, hdr);
+    if (n_docs > 0 && (min_len > 1 || max_len > 0)) {
+      k_cdc_walk<<<warp_grid(n_docs, sms), kWarpThreads, 0, s>>>(d_doc_offsets, n_docs, bits, min_len, max_len,
+                                                                  hdr);
+      k_cdc_tile_count<<<warp_grid(n_tiles, sms), kWarpThreads, 0, s>>>(bits, tile_count, n_tiles, hdr);
     }
+  }
+  k_cdc_scan<<<1, kScanThreads, 0, s>>>(tile_count, n_tiles, d_chunk_indptr, n_docs, capacity, hdr);
+  if (n_tiles > 0) {
+    const int grid = static_cast<int>(n_tiles < static_cast<int64_t>(sms) * 4 ? n_tiles : static_cast<int64_t>(sms) * 4);
+    k_cdc_emit<<<grid, kHashThreads, 0, s>>>(d_doc_offsets, n_docs, bits, tile_count, first_doc, n_tiles,
+                                             d_chunk_ends, capacity, d_chunk_indptr, hdr);
+    if (d_fingerprints && capacity > 0)
+      k_xxh64<<<sms * 4, kXxhThreads, 0, s>>>(d_tokens, n_tokens, nullptr, d_doc_offsets, d_chunk_ends,
+                                              tile_count + n_tiles, 0, capacity, seed, d_fingerprints, &hdr->status,
+                                              hdr);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "chunking launch");
@@ -667,10 +746,10 @@ extern "C" pic_status pic_fingerprint_spans(const int32_t* d_tokens, int64_t n_t
   }
   if (n_spans == 0) return set_error(nullptr, PIC_OK, "");
   const int sms = sm_count();
-  int64_t grid = (n_spans * 4 + kXxhThreads - 1) / kXxhThreads;
-  if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
-  k_xxh64<<<static_cast<int>(grid), kXxhThreads, 0, s>>>(d_tokens, n_tokens, d_starts, d_ends, nullptr, n_spans,
-                                                          n_spans, seed, d_out, d_status, nullptr);
+  int64_t grid = (n_spans + kXxhBatch - 1) / kXxhBatch;
+  if (grid > static_cast<int64_t>(sms) * 4) grid = static_cast<int64_t>(sms) * 4;
+  k_xxh64<<<static_cast<int>(grid), kXxhThreads, 0, s>>>(d_tokens, n_tokens, d_starts, nullptr, d_ends, nullptr,
+                                                          n_spans, n_spans, seed, d_out, d_status, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "fingerprint launch");
   return set_error(nullptr, PIC_OK, "");
