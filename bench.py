@@ -219,6 +219,49 @@ def cpu_baseline(wl, budget_s=12.0):
             "tokens_layers_per_s": tl / el}
 
 
+def cpu_baseline_attend(wl, hq, budget_s=12.0):
+    """Oracle decode attention on a bounded sample: the fused-path definition
+    (chunk keys rotated in fp64 from the pool) over the whole context of every
+    request, one layer at a time, until about budget_s seconds have passed."""
+    import oracle
+    m = wl.model
+    theta = oracle.model_inv_freq(m.rope_dim, m.rope_theta, m.llama3)
+    pairing = oracle.NEOX_HALF if m.pairing == "neox" else oracle.INTERLEAVED
+    chunks = [oracle.Chunk(off, n, 0) for off, n in zip(wl.pool_offsets, wl.chunk_lens)]
+    mla = m.kind == "mla"
+    vdim = m.head_dim - m.rope_dim if mla else m.head_dim
+    kb = oracle.bf16_bits_to_f64(host_pool_bits(wl, "k", [0]))[0]
+    vb = kb[..., :vdim] if mla else oracle.bf16_bits_to_f64(host_pool_bits(wl, "v", [0]))[0]
+    rng = np.random.default_rng(0)
+    scale = 1.0 / (192 ** 0.5) if mla else 1.0 / (m.head_dim ** 0.5)
+    t0 = time.perf_counter()
+    layers = token_layers = 0
+    while layers < m.num_layers and (layers == 0 or time.perf_counter() - t0 < budget_s):
+        for req in wl.requests:
+            segs = oracle.compose(chunks, [c for c, _ in req], take=[t for _, t in req])
+            T = segs[-1].dst_pos + segs[-1].length
+            rows = kb.reshape(kb.shape[0], -1, m.head_dim)
+            keys = np.empty((T,) + rows.shape[1:])
+            vals = np.empty((T, rows.shape[1], vdim))
+            for sg in segs:
+                src = rows[sg.src_tok:sg.src_tok + sg.length]
+                keys[sg.dst_pos:sg.dst_pos + sg.length] = oracle.rotate_rows(src, sg.delta, theta, pairing,
+                                                                            m.rope_offset, m.rope_dim)
+                vals[sg.dst_pos:sg.dst_pos + sg.length] = vb.reshape(vb.shape[0], -1, vdim)[
+                    sg.src_tok:sg.src_tok + sg.length]
+            bias = oracle.sink_bias(segs, T, wl.k_nonleading, -15.0)
+            oracle.attention_decode(rng.standard_normal((hq, m.head_dim)), keys, vals, scale, bias)
+            token_layers += T
+        layers += 1
+    el = time.perf_counter() - t0
+    row = m.num_kv_heads * m.head_dim * 2
+    gbs = token_layers * row * (1 if mla else 2) / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{layers} layer(s) x all {sum(wl.request_tokens)} positions, {hq} query heads "
+                      f"({token_layers} token-layers, {el:.1f} s, fp64 numpy, single thread)",
+            "tokens_layers_per_s": token_layers / el}
+
+
 def run_reference(args, wl):
     """Reference arm: the fp64 oracle timed on the host, one layer of the whole
     workload per step."""
@@ -254,7 +297,7 @@ def run_reference(args, wl):
 class Rig:
     """Everything one rank needs to run steps of a workload through the C ABI."""
 
-    def __init__(self, wl, device, mode):
+    def __init__(self, wl, device, mode, q_heads=0):
         import torch
         from position_independent_kv_stitch_gb300 import pic
         self.torch, self.pic = torch, pic
@@ -304,7 +347,10 @@ class Rig:
         self.shift_segs = None
         self.attn = None
         if mode in ("attend", "attend_cache"):
-            hq = 4 * m.num_kv_heads
+            # GQA: 4 query heads per KV head (Llama-3.1-8B: 32 over 8); MLA: 16
+            # query heads over the latent (DeepSeek-V3's 128 split over 8 GPUs)
+            hq = q_heads or (16 if m.kind == "mla" else 4 * m.num_kv_heads)
+            vdim = m.head_dim - m.rope_dim if m.kind == "mla" else m.head_dim
             g = torch.Generator(device=device)
             g.manual_seed(11)
             q = torch.empty((m.num_layers, len(wl.requests), hq, m.head_dim), dtype=torch.bfloat16, device=device)
@@ -313,8 +359,9 @@ class Rig:
             aws = pic.pic_attend_workspace_bytes(self.ctx, plans, hq, m.num_layers)
             self.free(plans)
             self.attn = {
-                "q": q, "hq": hq, "scale": 1.0 / (m.head_dim ** 0.5),
-                "out": torch.empty((m.num_layers, len(wl.requests), hq, m.head_dim), dtype=torch.float32, device=device),
+                "q": q, "hq": hq,
+                "scale": 1.0 / (192 ** 0.5) if m.kind == "mla" else 1.0 / (m.head_dim ** 0.5),
+                "out": torch.empty((m.num_layers, len(wl.requests), hq, vdim), dtype=torch.float32, device=device),
                 "lse": torch.empty((m.num_layers, len(wl.requests), hq), dtype=torch.float32, device=device),
                 "ws": torch.empty(aws, dtype=torch.uint8, device=device),
             }
@@ -690,7 +737,7 @@ def main():
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
 
-    rig = Rig(wl, dev, args.mode)
+    rig = Rig(wl, dev, args.mode, args.q_heads)
     for _ in range(args.warmup):
         rig.step()
     torch.cuda.synchronize()
@@ -724,10 +771,12 @@ def main():
         algo_bytes = rig.moved / args.steps           # bytes actually moved per step
         bpt = algo_bytes / tl
     elif args.mode in ("attend", "attend_cache"):
-        # attention reads every context K and V row once; the cache path also
-        # stitches first (pool read + cache write)
+        # attention reads every context K and V row once (MLA: the one latent
+        # row serves as both); the cache path also stitches first (pool read +
+        # cache write)
         row = wl.model.num_kv_heads * wl.model.head_dim * 2
-        bpt = 2 * row + (4 * row if args.mode == "attend_cache" else 0)
+        tensors = 1 if wl.model.kind == "mla" else 2
+        bpt = tensors * row + (2 * tensors * row if args.mode == "attend_cache" else 0)
         algo_bytes = tl * bpt
     else:
         bpt = bytes_per_token_layer(wl.model, args.mode)
@@ -748,7 +797,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(wl)
+        cpu = cpu_baseline_attend(wl, rig.attn["hq"]) if args.mode == "attend" else cpu_baseline(wl)
 
     bulk = pic.pic_kernel_variant(rig.ctx, 1 if args.mode == "inplace" else 0) == pic.PIC_VARIANT_BULK_PIPELINE
     if bulk and args.mode not in ("attend", "attend_cache"):
@@ -757,8 +806,9 @@ def main():
     else:
         kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
                  "mapped": "k_rotate_rows<stitch, mapped chunks in place>",
-                 "attend": "k_attend + k_attend_merge (fused delta-rotation)",
-                 "attend_cache": "k_rotate_rows<stitch> then k_attend + k_attend_merge",
+                 "attend": ("k_attend_mla" if wl.model.kind == "mla" else "k_attend")
+                 + " + k_attend_merge (fused delta-rotation)",
+                 "attend_cache": "stitch, then decode attention over the cache",
                  "inplace": "k_rotate_rows<in place>"}[args.mode]
     line = {
         "metric": "stitched KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

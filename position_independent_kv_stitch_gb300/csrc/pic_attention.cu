@@ -543,6 +543,448 @@ int occupancy_g(int heads_per_cta, size_t smem) {
     return FAIL;                                                      \
   } while (0)
 
+
+// ------------------------------------------------------------------ MLA
+
+// Decode attention for MLA models (Irminsul 2.1-2.2): every query head
+// attends to the same latent rows, row_t = [cKV_t (512) | k_r,t (64)], with
+// the query already absorbed into the latent space, q_h = [q_nope,h (512) |
+// q_rope,h (64)]:
+//   s_h,t = scale * (q_nope,h . cKV_t + q_rope,h . R(delta) k_r,t) + bias_t
+//         = scale * [q_nope,h | R(-delta) q_rope,h] . row_t + bias_t,
+//   out_h = sum_t softmax(s_h)_t cKV_t     (512 dims, before the up-projection).
+// Only the 64-d rope part of the query is rotated (once per delta); the
+// latent is used as stored, as Irminsul's delta-rotation requires.
+//
+// One latent row per position: the producer warp copies each position's
+// 1,152-byte row once (it serves as key and, its first 512 dims, as value).
+// The score tile of 16 heads x 16 positions and the 16 x 512 output are
+// shared by four consumer warps: warp quarter q computes the partial scores
+// over k-steps [9q, 9q + 9) of the 36 and owns output dims [128q, 128q + 128).
+// Partial scores meet in shared memory (two buffers, by stage parity) behind
+// an mbarrier per head group, waited on with a bound like every other wait;
+// each warp then runs the same softmax on the summed scores.
+constexpr int kMlaLatent = 512;
+constexpr int kMlaRopeDims = 64;
+constexpr int kMlaRow = kMlaLatent + kMlaRopeDims;  // 576 dims per latent row
+constexpr int kMlaQKS = kMlaRow / 16 / 4;           // k-steps of Q K^T per warp quarter (9)
+constexpr int kMlaRopeKS0 = kMlaLatent / 16;        // first rope k-step (32)
+constexpr int kMlaQNT = kMlaLatent / 8 / 4;         // n-tiles of P V per warp quarter (16)
+constexpr int kMlaHeadsPerGroup = 16;
+constexpr int kMlaMaxStages = 12;                   // ring depth bound (smaller stages than GQA's)
+
+struct MlaLayout {
+  size_t meta, gbar, prod, sbuf, ring, row_pitch, stage_bytes, total;
+};
+__host__ __device__ inline MlaLayout mla_layout(int ng, int ring) {
+  MlaLayout L{};
+  L.meta = 2 * kMlaMaxStages * sizeof(uint64_t);
+  L.gbar = L.meta + kMlaMaxStages * sizeof(StageMeta);
+  L.prod = (L.gbar + 8 * sizeof(uint64_t) + 127) / 128 * 128;
+  L.sbuf = (L.prod + sizeof(ProdState) + 127) / 128 * 128;
+  // per head group: 2 stage parities x 4 quarters x 16 heads x 16 positions
+  L.ring = (L.sbuf + static_cast<size_t>(ng) * 2 * 4 * 256 * sizeof(float) + 127) / 128 * 128;
+  L.row_pitch = kMlaRow * 2 + 16;  // +16 bytes: the 8 rows an ldmatrix reads fall in distinct banks
+  L.stage_bytes = ST * L.row_pitch;
+  L.total = L.ring + ring * L.stage_bytes;
+  return L;
+}
+
+// grid: persistent CTAs; block: 32 * (4 NG + 1) threads (NG groups of 16 heads).
+template <int PAIRING, int NG>
+__global__ void __launch_bounds__(32 * (4 * NG + 1), 1) k_attend_mla(const AttnParams P) {
+  constexpr bool NEOX = (PAIRING == kNeox);
+  constexpr int NCW = 4 * NG;                          // consumer warps
+  constexpr int HC = kMlaHeadsPerGroup * NG;           // query heads per CTA (and per record)
+  const int BLK = attn_block_floats(HC, kMlaLatent);   // floats of one record
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int NS = P.ring;
+  const MlaLayout L = mla_layout(NG, NS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMlaMaxStages;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
+  uint64_t* gbar = reinterpret_cast<uint64_t*>(smem + L.gbar);
+  float* sbuf = reinterpret_cast<float*>(smem + L.sbuf);
+  uint8_t* ring = smem + L.ring;
+  const uint32_t pitch = static_cast<uint32_t>(L.row_pitch);
+  const uint32_t rowb = static_cast<uint32_t>(P.row_bytes);  // 1,152
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = P.n_units, N = gridDim.x;
+  const int64_t u_begin = U * blockIdx.x / N, u_end = U * (blockIdx.x + 1) / N;
+
+  for (size_t i = threadIdx.x; i < static_cast<size_t>(NS) * L.stage_bytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NCW);
+    }
+    for (int gi = 0; gi < NG; ++gi) mbar_init(&gbar[gi], 4);
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    ProdState* ps = reinterpret_cast<ProdState*>(smem + L.prod);
+    const int n_st = P.n_stages;
+    int j = static_cast<int>(u_begin % n_st);
+    int layer = static_cast<int>(u_begin / n_st);
+    for (int k = 0; k < kDescAhead && u_begin + k < u_end; ++k)
+      fetch_desc(P, ps, u_begin + k, advance_stage(j, k, n_st), lane);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    for (int k = 0; k < 2 && u_begin + k < u_end; ++k) fetch_toks(P, ps, u_begin + k, lane);
+    cp_async_commit();
+    cp_async_wait<0>();
+    int base_layer = -1;
+    const uint8_t *kp = nullptr, *kc = nullptr;
+    int prev_layer = -1, prev_key = -1;
+    StageMeta pm{};
+    int pn = 0;
+    const uint8_t* pks = nullptr;
+    auto prepare = [&](int64_t u) {
+      cp_async_wait<1>();
+      __syncwarp();
+      const AttnStage cur = ps->desc[u & 7];
+      const AttnStage nx = ps->desc[(u + 1) & 7];
+      pm.layer = layer;
+      pm.key = cur.key;
+      pm.delta = cur.delta;
+      pm.n_tok = cur.n_tok;
+      pm.sink_mask = cur.sink_mask;
+      pm.flags = 0;
+      if (layer != prev_layer || cur.key != prev_key) pm.flags |= kMetaFirst;
+      if (u + 1 == u_end || j + 1 == n_st || nx.key != cur.key) pm.flags |= kMetaLast;
+      prev_layer = layer;
+      prev_key = cur.key;
+      if (layer != base_layer) {
+        const int64_t l_abs = P.layer_begin + layer;
+        kp = P.k_pool + l_abs * P.pool_layer_stride;
+        kc = P.k_cache + l_abs * P.cache_layer_stride;
+        base_layer = layer;
+      }
+      pn = cur.n_tok;
+      if (lane < pn) {
+        const AttnTok tok = ps->tok[u & 3][lane];
+        pks = ((tok.flags & kAttnFromCache) ? kc : kp) + static_cast<int64_t>(tok.row) * P.row_bytes;
+      }
+    };
+    prepare(u_begin);
+    int64_t it = 0;
+    bool failed = false;
+    int slot = 0;
+    uint32_t round = 0;
+    for (int64_t u = u_begin; u < u_end; ++u, ++it) {
+      if (round > 0 && !__all_sync(kFullMask, mbar_wait_bounded(&empty[slot], (round - 1) & 1u))) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) meta[slot] = pm;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(pn) * rowb);
+      __syncwarp();
+      if (lane < pn) bulk_load(ring + slot * L.stage_bytes + lane * L.row_pitch, pks, rowb, &full[slot]);
+      if (u + kDescAhead < u_end) fetch_desc(P, ps, u + kDescAhead, advance_stage(j, kDescAhead, n_st), lane);
+      if (u + 2 < u_end) fetch_toks(P, ps, u + 2, lane);
+      cp_async_commit();
+      if (j + 1 == n_st) {
+        j = 0;
+        ++layer;
+      } else {
+        ++j;
+      }
+      if (++slot == NS) {
+        slot = 0;
+        ++round;
+      }
+      if (u + 1 < u_end) prepare(u + 1);
+    }
+    if (failed) {
+      if (lane == 0) atomicOr(P.status, kDevTimeout);
+      const int64_t issued = it;
+      for (int64_t k = (issued > NS ? issued - NS : 0); k < issued; ++k)
+        mbar_wait_bounded(&full[k % NS], static_cast<uint32_t>((k / NS) & 1));
+    }
+    cp_async_wait<0>();
+    return;
+  }
+  if (warp > NCW) return;
+
+  // -------------------------------------------------------------- consumer
+  const int grp = warp >> 2;        // head group within the CTA: heads 16 grp .. 16 grp + 15
+  const int qr = warp & 3;          // quarter: k-steps [9 qr, 9 qr + 9), output dims [128 qr, 128 qr + 128)
+  const int g = lane >> 2, tq = lane & 3;
+  const int mi = lane >> 3, ri = lane & 7;
+  const uint32_t k_lane = static_cast<uint32_t>((ri + ((mi & 2) ? 8 : 0)) * pitch + (mi & 1) * 16);
+  const uint32_t v_lane =
+      static_cast<uint32_t>((ri + ((mi & 1) ? 8 : 0)) * pitch + (mi & 2) * 8 + qr * (kMlaLatent / 4) * 2);
+  const uint32_t ring_u32 = smem_u32(ring);
+  float* my_sbuf = sbuf + grp * (2 * 4 * 256);
+
+  float o[kMlaQNT][4];
+  uint32_t qa[kMlaQKS][4];  // A fragments of q; quarter 3 keeps its raw rope q in entries 5..8
+  uint32_t qh[4][4], ql[4][4];  // quarter 3: rotated rope q, bf16 hi and lo parts
+  float m_run[2] = {-FLT_MAX, -FLT_MAX}, l_part[2] = {0.0f, 0.0f};
+  int cur_delta = 0;
+  bool have_rot = false;
+  int slot = 0;
+  uint32_t round = 0;
+  uint32_t gphase = 0;
+  for (int64_t u = u_begin; u < u_end; ++u) {
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&full[slot], round & 1u))) {
+      if (lane == 0) atomicOr(P.status, kDevTimeout);
+      return;
+    }
+    const StageMeta m = meta[slot];
+    if (m.flags & kMetaFirst) {
+      m_run[0] = m_run[1] = -FLT_MAX;
+      l_part[0] = l_part[1] = 0.0f;
+#pragma unroll
+      for (int jn = 0; jn < kMlaQNT; ++jn) o[jn][0] = o[jn][1] = o[jn][2] = o[jn][3] = 0.0f;
+      const int hg = m.key % P.head_groups;
+      const int req = m.key / P.head_groups;
+      const uint16_t* qh0 = P.q + ((static_cast<int64_t>(m.layer) * P.n_req + req) * P.num_q_heads + hg * HC +
+                                   grp * kMlaHeadsPerGroup) * kMlaRow;
+#pragma unroll
+      for (int kk = 0; kk < kMlaQKS; ++kk) {
+        const int d0 = 16 * (kMlaQKS * qr + kk) + 2 * tq;
+        qa[kk][0] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + g * kMlaRow + d0));
+        qa[kk][1] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + (g + 8) * kMlaRow + d0));
+        qa[kk][2] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + g * kMlaRow + d0 + 8));
+        qa[kk][3] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + (g + 8) * kMlaRow + d0 + 8));
+      }
+      have_rot = false;
+    }
+    if (qr == 3 && (!have_rot || m.delta != cur_delta)) {
+      // R(-delta) on the rope part: the lane holds both members of each of
+      // its pairs (interleaved: the two halves of one register; neox: the
+      // same register of rope k-steps r and r + 2).
+      constexpr int R0 = kMlaRopeKS0 - kMlaQKS * 3;  // entry of the first rope k-step (5)
+      float x[4][8];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w = qa[R0 + r][i];
+          x[r][2 * i] = __uint_as_float(w << 16);
+          x[r][2 * i + 1] = __uint_as_float(w & 0xffff0000u);
+        }
+      if (m.delta != 0) {
+        if (NEOX) {
+          // rope dim of (k-step r, register i, half e): 16 r + (i >= 2 ? 8 : 0) + 2 tq + e; pairs (f, f + 32)
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int f = 16 * r + ((i >> 1) ? 8 : 0) + 2 * tq + e;
+                float cs, sn;
+                shift_cossin(m.delta, __ldg(P.freq + f), cs, sn);
+                const float a = x[r][2 * i + e], b = x[r + 2][2 * i + e];
+                x[r][2 * i + e] = a * cs + b * sn;
+                x[r + 2][2 * i + e] = b * cs - a * sn;
+              }
+        } else {
+          // pair (2f, 2f + 1) = the two halves of one register, f = 8 r + (i >= 2 ? 4 : 0) + tq
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int f = 8 * r + 4 * half + tq;
+              float cs, sn;
+              shift_cossin(m.delta, __ldg(P.freq + f), cs, sn);
+#pragma unroll
+              for (int i = 2 * half; i < 2 * half + 2; ++i) {
+                const float a = x[r][2 * i], b = x[r][2 * i + 1];
+                x[r][2 * i] = a * cs + b * sn;
+                x[r][2 * i + 1] = b * cs - a * sn;
+              }
+            }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_bf16x2(x[r][2 * i], x[r][2 * i + 1], qh[r][i], ql[r][i]);
+      cur_delta = m.delta;
+      have_rot = true;
+    }
+
+    const uint32_t kbase = ring_u32 + static_cast<uint32_t>(slot * L.stage_bytes);
+    // ---- partial S over this quarter's k-steps (two n-tiles of 8 positions)
+    float s[2][4] = {};
+    if (qr < 3) {
+#pragma unroll
+      for (int kk = 0; kk < kMlaQKS; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + k_lane + (kMlaQKS * qr + kk) * 32, b0, b1, b2, b3);
+        mma_bf16(s[0], qa[kk], b0, b1);
+        mma_bf16(s[1], qa[kk], b2, b3);
+      }
+    } else {
+      constexpr int R0 = kMlaRopeKS0 - kMlaQKS * 3;
+#pragma unroll
+      for (int kk = 0; kk < R0; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + k_lane + (kMlaQKS * 3 + kk) * 32, b0, b1, b2, b3);
+        mma_bf16(s[0], qa[kk], b0, b1);
+        mma_bf16(s[1], qa[kk], b2, b3);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + k_lane + (kMlaRopeKS0 + r) * 32, b0, b1, b2, b3);
+        mma_bf16(s[0], qh[r], b0, b1);
+        mma_bf16(s[1], qh[r], b2, b3);
+        mma_bf16(s[0], ql[r], b0, b1);
+        mma_bf16(s[1], ql[r], b2, b3);
+      }
+    }
+    // ---- exchange partial scores within the head group
+    float* part = my_sbuf + (gphase & 1) * (4 * 256);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      *reinterpret_cast<float2*>(part + qr * 256 + g * 16 + 8 * nt + 2 * tq) = make_float2(s[nt][0], s[nt][1]);
+      *reinterpret_cast<float2*>(part + qr * 256 + (g + 8) * 16 + 8 * nt + 2 * tq) = make_float2(s[nt][2], s[nt][3]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&gbar[grp]);
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&gbar[grp], gphase & 1u))) {
+      if (lane == 0) atomicOr(P.status, kDevTimeout);
+      return;
+    }
+    ++gphase;
+    float sc[2][4];  // [row g / g + 8][positions 2tq, 2tq + 1, 8 + 2tq, 9 + 2tq]
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const float2 v = *reinterpret_cast<const float2*>(part + qq * 256 + (g + 8 * rr) * 16 + 8 * nt + 2 * tq);
+          acc.x += v.x;
+          acc.y += v.y;
+        }
+        sc[rr][2 * nt] = acc.x;
+        sc[rr][2 * nt + 1] = acc.y;
+      }
+    // ---- online softmax per head (rows g and g + 8), identical in the four quarters
+    float p[2][4], alpha[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      float mt = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = (i < 2 ? 0 : 8) + 2 * tq + (i & 1);
+        const bool live = t < m.n_tok;
+        const float bias = ((m.sink_mask >> t) & 1u) ? P.sink_log2 : 0.0f;
+        sc[rr][i] = live ? sc[rr][i] * P.scale_log2 + bias : -FLT_MAX;
+        mt = fmaxf(mt, sc[rr][i]);
+      }
+      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 2));
+      const float m_new = fmaxf(m_run[rr], mt);
+      alpha[rr] = exp2f(m_run[rr] - m_new);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[rr][i] = sc[rr][i] > -FLT_MAX ? exp2f(sc[rr][i] - m_new) : 0.0f;
+      l_part[rr] = l_part[rr] * alpha[rr] + ((p[rr][0] + p[rr][1]) + (p[rr][2] + p[rr][3]));
+      m_run[rr] = m_new;
+    }
+    if (!__all_sync(kFullMask, alpha[0] == 1.0f && alpha[1] == 1.0f)) {
+#pragma unroll
+      for (int jn = 0; jn < kMlaQNT; ++jn) {
+        o[jn][0] *= alpha[0];
+        o[jn][1] *= alpha[0];
+        o[jn][2] *= alpha[1];
+        o[jn][3] *= alpha[1];
+      }
+    }
+    // A fragments of P (rows: heads g, g + 8; cols: the 16 positions), hi and lo parts
+    uint32_t ph[4], pl[4];
+    split_bf16x2(p[0][0], p[0][1], ph[0], pl[0]);
+    split_bf16x2(p[1][0], p[1][1], ph[1], pl[1]);
+    split_bf16x2(p[0][2], p[0][3], ph[2], pl[2]);
+    split_bf16x2(p[1][2], p[1][3], ph[3], pl[3]);
+    // ---- O += P V over this quarter's 128 latent dims
+#pragma unroll
+    for (int jn = 0; jn < kMlaQNT; jn += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(kbase + v_lane + jn * 16, b0, b1, b2, b3);
+      mma_bf16(o[jn], ph, b0, b1);
+      mma_bf16(o[jn], pl, b0, b1);
+      mma_bf16(o[jn + 1], ph, b2, b3);
+      mma_bf16(o[jn + 1], pl, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == NS) {
+      slot = 0;
+      ++round;
+    }
+
+    if (m.flags & kMetaLast) {
+      const AttnKey kk = P.keys[static_cast<int64_t>(m.layer) * P.n_keys + m.key];
+      float* blk = P.records + static_cast<int64_t>(kk.rec_base + (blockIdx.x - kk.first_cta)) * BLK;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int hrow = grp * kMlaHeadsPerGroup + g + 8 * rr;  // head within the record
+#pragma unroll
+        for (int jn = 0; jn < kMlaQNT; ++jn)
+          *reinterpret_cast<float2*>(blk + hrow * kMlaLatent + qr * (kMlaLatent / 4) + 8 * jn + 2 * tq) =
+              make_float2(o[jn][2 * rr], o[jn][2 * rr + 1]);
+        float l_tot = l_part[rr];
+        l_tot += __shfl_xor_sync(kFullMask, l_tot, 1);
+        l_tot += __shfl_xor_sync(kFullMask, l_tot, 2);
+        if (qr == 0 && tq == 0) {
+          blk[HC * kMlaLatent + hrow] = m_run[rr];
+          blk[HC * kMlaLatent + HC + hrow] = l_tot;
+        }
+      }
+    }
+  }
+}
+
+template <int PAIRING, int NG>
+cudaError_t launch_mla_g(const AttnParams& p, int grid, size_t smem, cudaStream_t s) {
+  auto kern = k_attend_mla<PAIRING, NG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 32 * (4 * NG + 1), smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_attend_merge<kMlaLatent><<<dim3(p.n_req, p.num_q_heads, p.n_layers), 128, 0, s>>>(p, kMlaHeadsPerGroup * NG);
+  return cudaGetLastError();
+}
+
+template <int PAIRING, int NG>
+int occupancy_mla_g(size_t smem) {
+  auto kern = k_attend_mla<PAIRING, NG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (4 * NG + 1), smem) != cudaSuccess) return 0;
+  return n;
+}
+
+#define PIC_MLA_DISPATCH(FN, FAIL, ...)                                     \
+  do {                                                                      \
+    if (pairing == kNeox) {                                                 \
+      if (ng == 1) return FN<kNeox, 1>(__VA_ARGS__);                        \
+      if (ng == 2) return FN<kNeox, 2>(__VA_ARGS__);                        \
+    } else {                                                                \
+      if (ng == 1) return FN<kInterleaved, 1>(__VA_ARGS__);                 \
+      if (ng == 2) return FN<kInterleaved, 2>(__VA_ARGS__);                 \
+    }                                                                       \
+    return FAIL;                                                            \
+  } while (0)
+
 }  // namespace
 
 bool attend_config(int head_dim, int group, int heads_per_cta, int* ring, size_t* smem_bytes) {
@@ -564,6 +1006,31 @@ cudaError_t launch_attend(const AttnParams& p, int pairing, int head_dim, int gr
                           cudaStream_t s) {
   if (p.n_units <= 0 || grid <= 0) return cudaSuccess;
   PIC_ATTN_DISPATCH(launch_g, cudaErrorInvalidValue, p, grid, smem_bytes, s);
+}
+
+}  // namespace pic
+
+namespace pic {
+
+bool attend_mla_config(int ng, int* ring, size_t* smem_bytes) {
+  if (ng != 1 && ng != 2) return false;
+  const MlaLayout base = mla_layout(ng, 0);
+  if (base.total + 2 * base.stage_bytes > kSmemBudget) return false;
+  int n = static_cast<int>((kSmemBudget - base.total) / base.stage_bytes);
+  if (n > kMlaMaxStages) n = kMlaMaxStages;
+  *ring = n;
+  *smem_bytes = mla_layout(ng, n).total;
+  return true;
+}
+
+int attend_mla_ctas_per_sm(int pairing, int ng, size_t smem_bytes) {
+  PIC_MLA_DISPATCH(occupancy_mla_g, 0, smem_bytes);
+}
+
+cudaError_t launch_attend_mla(const AttnParams& p, int pairing, int ng, int grid, size_t smem_bytes,
+                              cudaStream_t s) {
+  if (p.n_units <= 0 || grid <= 0) return cudaSuccess;
+  PIC_MLA_DISPATCH(launch_mla_g, cudaErrorInvalidValue, p, grid, smem_bytes, s);
 }
 
 }  // namespace pic

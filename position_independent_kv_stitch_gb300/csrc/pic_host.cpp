@@ -647,11 +647,41 @@ bool attn_heads(const pic_model_desc& m, int32_t* hb, int32_t* groups) {
   return false;
 }
 
-void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source, int32_t group,
-                 AttnPlan* out) {
+// How one decode attention maps heads onto CTAs and records.
+//   GQA: hb KV heads per CTA (head_groups groups of them per request), group
+//        query heads per KV head, values of head_dim dims.
+//   MLA: every query head reads the one latent row; a CTA (and a record)
+//        covers group = min(H, 32) query heads, 16 per mla_ng quarter-warp
+//        set, head_groups = H / group per request; values are the 512 latent
+//        dims.
+struct AttnHeads {
+  int32_t hb = 0, head_groups = 0, group = 0, vdim = 0, mla_ng = 0;
+};
+
+bool attn_layout_heads(const pic_model_desc& m, int32_t num_q_heads, AttnHeads* h) {
+  if (m.kind == PIC_KIND_MLA) {
+    if (num_q_heads != 16 && num_q_heads != 32 && num_q_heads != 64 && num_q_heads != 128) return false;
+    h->hb = 1;
+    h->group = std::min<int32_t>(num_q_heads, 32);
+    h->head_groups = num_q_heads / h->group;
+    h->vdim = m.head_dim - m.rope_dim;
+    h->mla_ng = h->group / 16;
+    return true;
+  }
+  if (!attn_heads(m, &h->hb, &h->head_groups)) return false;
+  if (m.num_kv_heads <= 0 || num_q_heads % m.num_kv_heads != 0) return false;
+  h->group = num_q_heads / m.num_kv_heads;
+  h->vdim = m.head_dim;
+  h->mla_ng = 0;
+  return true;
+}
+
+void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
+                 const AttnHeads& heads, AttnPlan* out) {
   const int32_t bs = ctx->model.block_size;
   const int32_t ST = pic::kAttnStageTokens;
-  attn_heads(ctx->model, &out->heads_per_cta, &out->head_groups);
+  out->heads_per_cta = heads.hb;
+  out->head_groups = heads.head_groups;
   out->n_keys = n_req * out->head_groups;
   out->key_stage_begin.assign(1, 0);
   std::vector<pic::AttnStage> req_stages;
@@ -709,14 +739,14 @@ struct AttnLayout {
 };
 
 AttnLayout attend_layout(const pic_ctx* ctx, size_t n_stages, size_t n_toks, size_t n_key_entries,
-                         size_t n_records, int32_t heads_per_cta, int32_t group) {
+                         size_t n_records, const AttnHeads& heads) {
   AttnLayout w;
   w.freq_off = pic::align_up(sizeof(WsHeader), pic::kWsAlign);
   w.stages_off = pic::align_up(w.freq_off + ctx->freq_turns.size() * sizeof(float2), pic::kWsAlign);
   w.toks_off = pic::align_up(w.stages_off + n_stages * sizeof(pic::AttnStage), pic::kWsAlign);
   w.keys_off = pic::align_up(w.toks_off + n_toks * sizeof(pic::AttnTok), pic::kWsAlign);
   w.records_off = pic::align_up(w.keys_off + n_key_entries * sizeof(pic::AttnKey), pic::kWsAlign);
-  const size_t rec = static_cast<size_t>(pic::attn_record_floats(group, ctx->model.head_dim, heads_per_cta)) * 4;
+  const size_t rec = static_cast<size_t>(pic::attn_record_floats(heads.group, heads.vdim, heads.hb)) * 4;
   w.total = pic::align_up(w.records_off + n_records * rec, pic::kWsAlign);
   return w;
 }
@@ -1345,17 +1375,16 @@ size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* pla
   if (!ctx || n_req < 0 || (n_req > 0 && !plans) || num_q_heads <= 0 || num_layers <= 0) return 0;
   for (int32_t r = 0; r < n_req; ++r)
     if (!plans[r]) return 0;
-  int32_t hb = 0, hgroups = 0;
-  if (!attn_heads(ctx->model, &hb, &hgroups)) return 0;
-  const int32_t group = std::max(1, num_q_heads / std::max(1, ctx->model.num_kv_heads));
+  AttnHeads heads;
+  if (!attn_layout_heads(ctx->model, num_q_heads, &heads)) return 0;
   AttnPlan fused, cache;
-  attend_plan(ctx, plans, n_req, PIC_ATTEND_FUSED, group, &fused);
-  attend_plan(ctx, plans, n_req, PIC_ATTEND_CACHE, group, &cache);
+  attend_plan(ctx, plans, n_req, PIC_ATTEND_FUSED, heads, &fused);
+  attend_plan(ctx, plans, n_req, PIC_ATTEND_CACHE, heads, &cache);
   const size_t n_stages = std::max(fused.stages.size(), cache.stages.size());
   // a grid of at most kAttnMaxCtas CTAs adds at most one record per CTA
   const size_t n_keys = static_cast<size_t>(num_layers) * fused.n_keys;
   const size_t records = n_keys + pic::kAttnMaxCtas;
-  return attend_layout(ctx, n_stages, fused.toks.size(), n_keys + 1, records, hb, group).total;
+  return attend_layout(ctx, n_stages, fused.toks.size(), n_keys + 1, records, heads).total;
 }
 
 pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
@@ -1365,39 +1394,55 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
                              float* out, float* lse, void* d_ws, size_t ws_bytes, pic_stream_t stream) {
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
   const pic_model_desc& m = ctx->model;
-  if (m.kind != PIC_KIND_GQA || (m.head_dim != 64 && m.head_dim != 128))
-    return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention covers GQA heads of 64 or 128 dims");
-  int32_t hb = 0, hgroups = 0;
-  if (!attn_heads(m, &hb, &hgroups))
-    return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention needs <= %d KV heads or a multiple of %d",
-                pic::kAttnMaxHeads, pic::kAttnMaxHeads);
+  const bool mla = m.kind == PIC_KIND_MLA;
+  AttnHeads heads;
+  if (mla) {
+    if (m.head_dim != 576 || m.rope_dim != 64 || m.rope_offset != 512)
+      return fail(ctx, PIC_ERR_UNSUPPORTED, "MLA decode attention covers 512-dim latents with a 64-dim rope key");
+    if (!attn_layout_heads(m, num_q_heads, &heads))
+      return fail(ctx, PIC_ERR_UNSUPPORTED, "MLA decode attention takes 16, 32, 64 or 128 query heads");
+  } else {
+    if (m.head_dim != 64 && m.head_dim != 128)
+      return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention covers GQA heads of 64 or 128 dims");
+    int32_t hb = 0, hgroups = 0;
+    if (!attn_heads(m, &hb, &hgroups))
+      return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention needs <= %d KV heads or a multiple of %d",
+                  pic::kAttnMaxHeads, pic::kAttnMaxHeads);
+    if (num_q_heads <= 0 || num_q_heads % m.num_kv_heads != 0)
+      return fail(ctx, PIC_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+    const int32_t group = num_q_heads / m.num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8)
+      return fail(ctx, PIC_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8");
+    attn_layout_heads(m, num_q_heads, &heads);
+  }
   if (source != PIC_ATTEND_FUSED && source != PIC_ATTEND_CACHE) return fail(ctx, PIC_ERR_INVALID_ARG, "bad source");
   if (n_req <= 0 || !plans) return fail(ctx, PIC_ERR_INVALID_ARG, "no requests");
   for (int32_t r = 0; r < n_req; ++r)
     if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
-  if (num_q_heads <= 0 || num_q_heads % m.num_kv_heads != 0)
-    return fail(ctx, PIC_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
-  const int32_t group = num_q_heads / m.num_kv_heads;
-  if (group != 1 && group != 2 && group != 4 && group != 8)
-    return fail(ctx, PIC_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8");
   if (layer_begin < 0 || num_layers <= 0 || layer_begin + num_layers > m.num_layers)
     return fail(ctx, PIC_ERR_RANGE, "layer range outside the model");
-  if (!q || !out || !d_ws || !k_cache || !v_cache) return fail(ctx, PIC_ERR_INVALID_ARG, "null q, out, cache or workspace");
-  if (source == PIC_ATTEND_FUSED && (!k_pool || !v_pool))
-    return fail(ctx, PIC_ERR_INVALID_ARG, "fused attention reads the pool: pass k_pool and v_pool");
+  if (!q || !out || !d_ws || !k_cache || (!mla && !v_cache))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "null q, out, cache or workspace");
+  if (source == PIC_ATTEND_FUSED && (!k_pool || (!mla && !v_pool)))
+    return fail(ctx, PIC_ERR_INVALID_ARG, "fused attention reads the pool: pass k_pool (and v_pool for GQA)");
+  if (mla) {
+    v_pool = nullptr;  // the latent serves as value
+    v_cache = nullptr;
+  }
   if (!vectorized_bytes_ok(q) || !vectorized_bytes_ok(out) || !vectorized_bytes_ok(k_cache) ||
-      !vectorized_bytes_ok(v_cache) || (cache_ls & 15) || (k_pool && !vectorized_bytes_ok(k_pool)) ||
+      (v_cache && !vectorized_bytes_ok(v_cache)) || (cache_ls & 15) || (k_pool && !vectorized_bytes_ok(k_pool)) ||
       (v_pool && !vectorized_bytes_ok(v_pool)) || (pool_ls & 15) || !vectorized_bytes_ok(d_ws))
     return fail(ctx, PIC_ERR_ALIGNMENT, "q, out, pools, caches, strides and workspace must be 16-byte aligned");
   for (int32_t r = 0; r < n_req; ++r)
     if (plans[r]->total_tokens == 0) return fail(ctx, PIC_ERR_RANGE, "plans[%d] has no context to attend", r);
   int ring = 0;
   size_t smem = 0;
-  if (!pic::attend_config(m.head_dim, group, hb, &ring, &smem))
-    return fail(ctx, PIC_ERR_UNSUPPORTED, "attention stages do not fit in shared memory");
+  const bool fits = mla ? pic::attend_mla_config(heads.mla_ng, &ring, &smem)
+                        : pic::attend_config(m.head_dim, heads.group, heads.hb, &ring, &smem);
+  if (!fits) return fail(ctx, PIC_ERR_UNSUPPORTED, "attention stages do not fit in shared memory");
 
   AttnPlan plan;
-  attend_plan(ctx, plans, n_req, source, group, &plan);
+  attend_plan(ctx, plans, n_req, source, heads, &plan);
   const int64_t units = static_cast<int64_t>(plan.stages.size()) * num_layers;
   if (units > INT32_MAX || static_cast<int64_t>(plan.toks.size()) > INT32_MAX)
     return fail(ctx, PIC_ERR_CAPACITY, "attention batch too large");
@@ -1409,13 +1454,14 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   for (int i = 0; i < 4; ++i)
     if (bufs[i] && residency(bufs[i]) != 0)
       return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention reads pools and caches from device memory only");
-  const int per_sm = pic::attend_ctas_per_sm(m.pairing, m.head_dim, group, hb, smem);
+  const int per_sm = mla ? pic::attend_mla_ctas_per_sm(m.pairing, heads.mla_ng, smem)
+                         : pic::attend_ctas_per_sm(m.pairing, m.head_dim, heads.group, heads.hb, smem);
   if (per_sm <= 0) return fail(ctx, PIC_ERR_CUDA, "attention kernel does not fit on an SM");
   const int64_t ctas = std::min<int64_t>({units, static_cast<int64_t>(di.sm_count) * per_sm, pic::kAttnMaxCtas});
   std::vector<pic::AttnKey> keys;
   const int64_t records = attend_keys(plan, num_layers, ctas, &keys);
   const AttnLayout w = attend_layout(ctx, plan.stages.size(), plan.toks.size(), keys.size(),
-                                     static_cast<size_t>(records), hb, group);
+                                     static_cast<size_t>(records), heads);
   if (ws_bytes < w.total) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1445,8 +1491,8 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   p.n_req = n_req;
   p.num_q_heads = num_q_heads;
   p.n_kv_heads = m.num_kv_heads;
-  p.heads_per_cta = hb;
-  p.head_groups = hgroups;
+  p.heads_per_cta = heads.hb;
+  p.head_groups = heads.head_groups;
   p.n_layers = num_layers;
   p.layer_begin = layer_begin;
   p.scale_log2 = softmax_scale * kLog2e;
@@ -1463,7 +1509,8 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   p.out = out;
   p.lse = lse;
   p.status = &reinterpret_cast<WsHeader*>(ws)->status;
-  const cudaError_t e = pic::launch_attend(p, m.pairing, m.head_dim, group, static_cast<int>(ctas), smem, s);
+  const cudaError_t e = mla ? pic::launch_attend_mla(p, m.pairing, heads.mla_ng, static_cast<int>(ctas), smem, s)
+                            : pic::launch_attend(p, m.pairing, m.head_dim, heads.group, static_cast<int>(ctas), smem, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "attention launch");
   return ok(ctx);
 }

@@ -175,6 +175,14 @@ int attend_ctas_per_sm(int pairing, int head_dim, int group, int heads_per_cta, 
 cudaError_t launch_attend(const AttnParams& p, int pairing, int head_dim, int group, int grid, size_t smem_bytes,
                           cudaStream_t stream);
 
+// MLA decode attention (same plan, stages and records; one latent row per
+// position, query heads in groups of 16, ng groups per CTA).
+constexpr int kAttnMlaLatent = 512;
+bool attend_mla_config(int ng, int* ring, size_t* smem_bytes);
+int attend_mla_ctas_per_sm(int pairing, int ng, size_t smem_bytes);
+cudaError_t launch_attend_mla(const AttnParams& p, int pairing, int ng, int grid, size_t smem_bytes,
+                              cudaStream_t stream);
+
 // Launchers; each returns the launch's cudaError_t.  `grid` is the number of
 // CTAs (persistent, grid-stride over units).
 cudaError_t launch_stitch_gqa(const KernelParams& p, int pairing, int head_dim, int grid,

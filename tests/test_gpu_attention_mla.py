@@ -1,0 +1,181 @@
+"""GPU parity of decode attention for MLA models (Irminsul 2.1-2.2): every
+query head reads the same latent rows, row = [cKV (512) | k_r (64)]; a chunk's
+k_r is rotated by its delta on the way in, the latent is used as stored and is
+the value.  Against the fp64 oracle's attention over exactly rotated rows."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import bits
+from position_independent_kv_stitch_gb300 import pic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+LATENT, ROPE = 512, 64
+ROW = LATENT + ROPE
+
+_POOL_LENS = [1, 5, 16, 17, 33, 100, 250, 300, 64, 128, 7, 400]
+_BLOCK_CHUNK = (45, [190, 191, 192], 700)   # tokens, blocks, position its keys sit at
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pic.load(build_if_missing=True)
+
+
+def _setup(pairing, L, seed, rep=1):
+    bs, nb = 16, 200 + 120 * (rep - 1)
+    m = W.Model("attn-mla", "mla", L, 1, ROW, ROPE, LATENT, pairing, 1e4, bs)
+    ctx = pic.create_from_spec(pic.model_spec_from(m), nb)
+    offs = [0]
+    for n in _POOL_LENS[:-1]:
+        offs.append(offs[-1] + n)
+    ids, sources = [], {}
+    for c, (o, n) in enumerate(zip(offs, _POOL_LENS)):
+        cid = pic.pic_register_chunk(ctx, W.chunk_key("attn-mla", c), o, n)[0]
+        ids.append(cid)
+        sources[cid] = ("pool", o)
+    n_b, blocks, base = _BLOCK_CHUNK
+    bid = pic.pic_register_chunk_blocks(ctx, W.chunk_key("attn-mla", 99), blocks, n_b, base)[0]
+    sources[bid] = ("blocks", blocks)
+    g = torch.Generator().manual_seed(seed)
+    P = offs[-1] + _POOL_LENS[-1]
+    pool = torch.randn((L, P, ROW), generator=g).to(torch.bfloat16)
+    cache = torch.randn((L, nb, bs, ROW), generator=g).to(torch.bfloat16)
+
+    def positions(chunks, start, gaps):
+        pos, p = [], start
+        for j, c in enumerate(chunks):
+            p += gaps.get(j, 0)
+            pos.append(p)
+            p += n_b if c == bid else _POOL_LENS[ids.index(c)]
+        return pos, p
+
+    pool_runs = [ids[9], ids[3], ids[8], ids[0], ids[4], ids[10], ids[6], ids[1]]
+    specs = [([ids[5], ids[11], ids[2], bid, ids[7]] + [ids[7], ids[4]] * (rep - 1), 3, {4: 10}, 6),
+             (pool_runs * rep, 0, {}, 0),
+             ([ids[11], ids[6], ids[5]] * rep, 0, {}, 40)]
+    plans, tables = [], []
+    for chunks, start, gaps, tail in specs:
+        pos, end = positions(chunks, start, gaps)
+        plan, bt = pic.pic_build_block_table(ctx, chunks, 64 * rep, dst_pos=pos, start_pos=start,
+                                             total_tokens=end + tail, k_nonleading=4)
+        plans.append(plan)
+        tables.append(bt)
+    return dict(m=m, ctx=ctx, plans=plans, tables=tables, sources=sources, pool=pool, cache=cache, bs=bs, L=L)
+
+
+def _context_rows(S, r):
+    """fp64 latent rows of request r's context, rope slice exactly rotated."""
+    m, bs = S["m"], S["bs"]
+    theta = oracle.model_inv_freq(ROPE, m.rope_theta, None)
+    pairing = oracle.NEOX_HALF if m.pairing == "neox" else oracle.INTERLEAVED
+    plan, table = S["plans"][r], S["tables"][r]
+    T = pic.pic_plan_info(plan)["total_tokens"]
+    pos = np.arange(T)
+    blk_i = torch.as_tensor(np.asarray(table)[pos // bs], dtype=torch.long)
+    row_i = torch.as_tensor(pos % bs, dtype=torch.long)
+    rows = oracle.bf16_bits_to_f64(bits(S["cache"][:, blk_i, row_i]))
+    segs = []
+    for j in range(pic.pic_plan_info(plan)["num_segments"]):
+        sg = pic.pic_plan_segment(plan, j)
+        n, p0 = sg["num_tokens"], sg["dst_pos"]
+        kind, where = S["sources"][sg["chunk_id"]]
+        t = np.arange(n)
+        if kind == "pool":
+            src = S["pool"][:, torch.as_tensor(sg["src_tok"] + t, dtype=torch.long)]
+        else:
+            blk = torch.as_tensor(np.asarray(where)[t // bs], dtype=torch.long)
+            src = S["cache"][:, blk, torch.as_tensor(t % bs, dtype=torch.long)]
+        rows[:, p0:p0 + n] = oracle.rotate_rows(oracle.bf16_bits_to_f64(bits(src)), sg["delta"], theta, pairing,
+                                                LATENT, ROPE)
+        segs.append(oracle.Segment(sg["chunk_id"], sg["src_tok"], n, p0, sg["delta"]))
+    return rows, segs, T
+
+
+def _attend(S, H, source, bias_value, pool=None, cache=None):
+    L = S["L"]
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn((L, 3, H, ROW), generator=g).to(torch.bfloat16)
+    out = torch.empty((L, 3, H, LATENT), dtype=torch.float32, device=DEV)
+    lse = torch.empty((L, 3, H), dtype=torch.float32, device=DEV)
+    ws = torch.empty(pic.pic_attend_workspace_bytes(S["ctx"], S["plans"], H, L), dtype=torch.uint8, device=DEV)
+    scale = 1.0 / math.sqrt(192)
+    pool = S["pool"].to(DEV) if pool is None else pool
+    cache = S["cache"].to(DEV) if cache is None else cache
+    pic.pic_attend_decode(S["ctx"], S["plans"], source, q.to(DEV), scale, pool, None, cache, None, out, lse, ws,
+                          sink_bias=bias_value)
+    assert pic.pic_query_device_status(S["ctx"], ws) == 0
+    return q, out.cpu().double().numpy(), lse.cpu().double().numpy(), scale
+
+
+def _check_against_oracle(S, q, out, lse, scale, bias_value, atol):
+    qb = bits(q)
+    for r in range(3):
+        rows, segs, T = _context_rows(S, r)
+        bias = oracle.sink_bias(segs, T, 4, bias_value) if bias_value else None
+        for l in range(S["L"]):
+            keys = rows[l][:, None, :]
+            vals = rows[l][:, None, :LATENT]
+            o, s = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[l, r]), keys, vals, scale, bias)
+            np.testing.assert_allclose(out[l, r], o, atol=atol, rtol=0)
+            np.testing.assert_allclose(lse[l, r], s, atol=atol, rtol=0)
+
+
+@pytest.mark.parametrize("pairing,H,L,bias_value,rep", [
+    ("interleaved", 16, 2, -15.0, 1),
+    ("interleaved", 16, 2, 0.0, 4),
+    ("neox", 16, 2, -15.0, 1),
+    ("interleaved", 32, 2, 0.0, 1),
+    ("neox", 32, 2, -15.0, 3),
+    ("interleaved", 64, 1, -15.0, 1),
+    ("interleaved", 128, 1, 0.0, 1),
+])
+def test_fused_mla_attention_matches_oracle(pairing, H, L, bias_value, rep):
+    """Three requests of 250-1,400 positions (times rep): chunks of 1..400
+    tokens, inline gaps and a trailing run of inline tokens, a block-resident
+    chunk read from its blocks, delta 0 and nonzero; every (layer, request,
+    query head) against the oracle.  64 and 128 heads run as 2 and 4 head
+    groups of 32 per request."""
+    S = _setup(pairing, L, seed=4, rep=rep)
+    try:
+        q, out, lse, scale = _attend(S, H, pic.PIC_ATTEND_FUSED, bias_value)
+        _check_against_oracle(S, q, out, lse, scale, bias_value, 2e-3)
+    finally:
+        pic.pic_destroy(S["ctx"])
+
+
+def test_mla_cache_path_over_materialized_stitch():
+    """Stitch the requests into the cache (MLA stitch: latent copied, rope
+    rotated, rounded to bf16 once), then attend from the cache: the oracle's
+    result up to that rounding, and the fused path closer to it."""
+    S = _setup("interleaved", 2, seed=6)
+    try:
+        ctx = S["ctx"]
+        cache = S["cache"].to(DEV)
+        pool = S["pool"].to(DEV)
+        d_bt = torch.from_numpy(np.stack(S["tables"])).to(DEV)
+        ws = torch.empty(pic.pic_workspace_bytes(ctx, S["plans"]), dtype=torch.uint8, device=DEV)
+        pic.pic_stitch(ctx, S["plans"], pool, None, cache, None, d_bt, None, None, ws)
+        assert pic.pic_query_device_status(ctx, ws) == 0
+        q, out_c, lse_c, scale = _attend(S, 16, pic.PIC_ATTEND_CACHE, -15.0, pool, cache)
+        _, out_f, lse_f, _ = _attend(S, 16, pic.PIC_ATTEND_FUSED, -15.0, pool, cache)
+        _check_against_oracle(S, q, out_f, lse_f, scale, -15.0, 2e-3)
+        _check_against_oracle(S, q, out_c, lse_c, scale, -15.0, 3e-2)
+    finally:
+        pic.pic_destroy(S["ctx"])
+
+
+def test_mla_rejects_unsupported_head_counts():
+    S = _setup("interleaved", 1, seed=7)
+    try:
+        with pytest.raises(pic.PicError) as e:
+            _attend(S, 24, pic.PIC_ATTEND_FUSED, 0.0)
+        assert e.value.status_name == "PIC_ERR_UNSUPPORTED"
+    finally:
+        pic.pic_destroy(S["ctx"])

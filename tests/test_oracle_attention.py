@@ -65,3 +65,24 @@ def test_sink_bias_follows_the_listing_boundary_loop():
     want[10:13] = -15.0        # chunk 1 is only 3 tokens long
     want[13:17] = -15.0        # chunk 2: its first 4 tokens
     np.testing.assert_array_equal(b, want)       # chunk 0 (global token 0) untouched
+
+
+def test_mla_absorbed_attention_equals_per_head_attention():
+    """Irminsul 2.1 (MLA decomposition): a head's key is [W_UK c | k_r] and its
+    value W_UV c.  With the query absorbed, q_abs = [W_UK^T q_nope | q_rope],
+    attention over the shared latent rows [c | k_r] gives the same scores, and
+    W_UV applied to its latent output gives the head's output -- the form the
+    MLA decode attention computes (values = the latent)."""
+    rng = np.random.default_rng(35)
+    T, dc, dr, dn, dv = 9, 16, 4, 6, 5
+    w_uk, w_uv = rng.standard_normal((dn, dc)), rng.standard_normal((dv, dc))
+    c, k_r = rng.standard_normal((T, dc)), rng.standard_normal((T, dr))
+    q_nope, q_rope = rng.standard_normal(dn), rng.standard_normal(dr)
+    keys = np.concatenate([c @ w_uk.T, k_r], axis=1)[:, None, :]
+    vals = (c @ w_uv.T)[:, None, :]
+    want, want_lse = oracle.attention_decode(np.concatenate([q_nope, q_rope])[None], keys, vals, 0.3)
+    rows = np.concatenate([c, k_r], axis=1)[:, None, :]
+    q_abs = np.concatenate([w_uk.T @ q_nope, q_rope])[None]
+    lat, lse = oracle.attention_decode(q_abs, rows, c[:, None, :], 0.3)
+    np.testing.assert_allclose(lat @ w_uv.T, want, atol=1e-12)
+    np.testing.assert_allclose(lse, want_lse, atol=1e-12)
