@@ -435,7 +435,16 @@ size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* pla
  *   lse    device float [num_layers][n_req][num_q_heads] or NULL.
  * GQA models with head_dim 64 or 128, at most 8 KV heads or a multiple of 8,
  * and 1, 2, 4 or 8 query heads per KV head; pools and caches in device
- * memory, 16-byte aligned.  The cache's block tables are the plans' (as
+ * memory, 16-byte aligned.
+ * MLA models ([Irminsul] 2.1: 512-dim latent + 64-dim rope key per row):
+ * every query head attends to the shared latent rows with its query absorbed
+ * into the latent space, q = [q_nope (512) | q_rope (64)] (head_dim 576), so
+ *   s_t = softmax_scale * (q_nope . cKV_t + q_rope . R(delta) k_r,t) + bias,
+ *   out = sum_t softmax(s)_t cKV_t   (out: [num_layers][n_req][num_q_heads][512]);
+ * only the rope part is rotated (the kernel rotates q_rope by R(-delta)),
+ * the latent is used as stored and serves as the value.  16, 32, 64 or 128
+ * query heads (64 and 128 run as 2 and 4 groups of 32 that each read the
+ * rows); v_pool and v_cache are ignored and may be NULL.  The cache's block tables are the plans' (as
  * pic_build_block_table returned them).  Two launches: a persistent kernel
  * streams the context through shared memory and leaves per-range softmax
  * records in the workspace, a second merges them into out and lse.  Errors:

@@ -572,9 +572,13 @@ constexpr int kMlaRopeKS0 = kMlaLatent / 16;        // first rope k-step (32)
 constexpr int kMlaQNT = kMlaLatent / 8 / 4;         // n-tiles of P V per warp quarter (16)
 constexpr int kMlaHeadsPerGroup = 16;
 constexpr int kMlaMaxStages = 12;                   // ring depth bound (smaller stages than GQA's)
+constexpr size_t kMlaSmemHalf = 112 * 1024;         // shared memory per CTA when two share an SM
+
+constexpr int kMlaQPitch = kMlaQKS * 16 * 2 + 16;  // bytes per head row of a warp's q slice (304)
+constexpr int kMlaRopePitch = kMlaRopeDims * 2 + 16; // bytes per head row of a rotated rope tile (144)
 
 struct MlaLayout {
-  size_t meta, gbar, prod, sbuf, ring, row_pitch, stage_bytes, total;
+  size_t meta, gbar, prod, sbuf, qs, rope, ring, row_pitch, stage_bytes, total;
 };
 __host__ __device__ inline MlaLayout mla_layout(int ng, int ring) {
   MlaLayout L{};
@@ -583,7 +587,11 @@ __host__ __device__ inline MlaLayout mla_layout(int ng, int ring) {
   L.prod = (L.gbar + 8 * sizeof(uint64_t) + 127) / 128 * 128;
   L.sbuf = (L.prod + sizeof(ProdState) + 127) / 128 * 128;
   // per head group: 2 stage parities x 4 quarters x 16 heads x 16 positions
-  L.ring = (L.sbuf + static_cast<size_t>(ng) * 2 * 4 * 256 * sizeof(float) + 127) / 128 * 128;
+  L.qs = (L.sbuf + static_cast<size_t>(ng) * 2 * 4 * 256 * sizeof(float) + 127) / 128 * 128;
+  // per consumer warp: its q slice, 16 heads x 144 dims (bf16)
+  L.rope = L.qs + static_cast<size_t>(ng) * 4 * 16 * kMlaQPitch;
+  // per head group: the rotated rope part of q as bf16 hi and lo tiles, 16 heads x 64 dims each
+  L.ring = (L.rope + static_cast<size_t>(ng) * 2 * 16 * kMlaRopePitch + 127) / 128 * 128;
   L.row_pitch = kMlaRow * 2 + 16;  // +16 bytes: the 8 rows an ldmatrix reads fall in distinct banks
   L.stage_bytes = ST * L.row_pitch;
   L.total = L.ring + ring * L.stage_bytes;
@@ -592,7 +600,7 @@ __host__ __device__ inline MlaLayout mla_layout(int ng, int ring) {
 
 // grid: persistent CTAs; block: 32 * (4 NG + 1) threads (NG groups of 16 heads).
 template <int PAIRING, int NG>
-__global__ void __launch_bounds__(32 * (4 * NG + 1), 1) k_attend_mla(const AttnParams P) {
+__global__ void __launch_bounds__(32 * (4 * NG + 1), NG == 1 ? 2 : 1) k_attend_mla(const AttnParams P) {
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr int NCW = 4 * NG;                          // consumer warps
   constexpr int HC = kMlaHeadsPerGroup * NG;           // query heads per CTA (and per record)
@@ -725,10 +733,16 @@ __global__ void __launch_bounds__(32 * (4 * NG + 1), 1) k_attend_mla(const AttnP
       static_cast<uint32_t>((ri + ((mi & 1) ? 8 : 0)) * pitch + (mi & 2) * 8 + qr * (kMlaLatent / 4) * 2);
   const uint32_t ring_u32 = smem_u32(ring);
   float* my_sbuf = sbuf + grp * (2 * 4 * 256);
+  // this warp's q slice (16 heads x its 144 dims) and the group's rotated rope tiles
+  uint8_t* qs = smem + L.qs + static_cast<size_t>(warp) * 16 * kMlaQPitch;
+  uint8_t* rope_hl = smem + L.rope + static_cast<size_t>(grp) * 2 * 16 * kMlaRopePitch;
+  // ldmatrix row address of this lane for an A tile (16 rows x 16 cols)
+  const uint32_t a_lane = static_cast<uint32_t>((ri + ((mi & 1) ? 8 : 0)) * kMlaQPitch + ((mi & 2) ? 16 : 0));
+  const uint32_t r_lane = static_cast<uint32_t>((ri + ((mi & 1) ? 8 : 0)) * kMlaRopePitch + ((mi & 2) ? 16 : 0));
+  const uint32_t qs_u32 = smem_u32(qs), rope_u32 = smem_u32(rope_hl);
+  constexpr int R0 = kMlaRopeKS0 - kMlaQKS * 3;  // first rope k-step within quarter 3's slice (5)
 
   float o[kMlaQNT][4];
-  uint32_t qa[kMlaQKS][4];  // A fragments of q; quarter 3 keeps its raw rope q in entries 5..8
-  uint32_t qh[4][4], ql[4][4];  // quarter 3: rotated rope q, bf16 hi and lo parts
   float m_run[2] = {-FLT_MAX, -FLT_MAX}, l_part[2] = {0.0f, 0.0f};
   int cur_delta = 0;
   bool have_rot = false;
@@ -749,103 +763,83 @@ __global__ void __launch_bounds__(32 * (4 * NG + 1), 1) k_attend_mla(const AttnP
       const int hg = m.key % P.head_groups;
       const int req = m.key / P.head_groups;
       const uint16_t* qh0 = P.q + ((static_cast<int64_t>(m.layer) * P.n_req + req) * P.num_q_heads + hg * HC +
-                                   grp * kMlaHeadsPerGroup) * kMlaRow;
-#pragma unroll
-      for (int kk = 0; kk < kMlaQKS; ++kk) {
-        const int d0 = 16 * (kMlaQKS * qr + kk) + 2 * tq;
-        qa[kk][0] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + g * kMlaRow + d0));
-        qa[kk][1] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + (g + 8) * kMlaRow + d0));
-        qa[kk][2] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + g * kMlaRow + d0 + 8));
-        qa[kk][3] = __ldg(reinterpret_cast<const uint32_t*>(qh0 + (g + 8) * kMlaRow + d0 + 8));
+                                   grp * kMlaHeadsPerGroup) * kMlaRow + kMlaQKS * 16 * qr;
+      __syncwarp();  // the slice's previous readers are done
+      // 16 heads x 144 dims = 16 x 18 chunks of 16 bytes
+      for (int i = lane; i < 16 * kMlaQKS * 2; i += 32) {
+        const int row = i / (kMlaQKS * 2), c = i % (kMlaQKS * 2);
+        *reinterpret_cast<uint4*>(qs + row * kMlaQPitch + c * 16) =
+            __ldg(reinterpret_cast<const uint4*>(qh0 + row * kMlaRow) + c);
       }
+      __syncwarp();
       have_rot = false;
     }
     if (qr == 3 && (!have_rot || m.delta != cur_delta)) {
-      // R(-delta) on the rope part: the lane holds both members of each of
-      // its pairs (interleaved: the two halves of one register; neox: the
-      // same register of rope k-steps r and r + 2).
-      constexpr int R0 = kMlaRopeKS0 - kMlaQKS * 3;  // entry of the first rope k-step (5)
-      float x[4][8];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w = qa[R0 + r][i];
-          x[r][2 * i] = __uint_as_float(w << 16);
-          x[r][2 * i + 1] = __uint_as_float(w & 0xffff0000u);
-        }
-      if (m.delta != 0) {
-        if (NEOX) {
-          // rope dim of (k-step r, register i, half e): 16 r + (i >= 2 ? 8 : 0) + 2 tq + e; pairs (f, f + 32)
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int f = 16 * r + ((i >> 1) ? 8 : 0) + 2 * tq + e;
-                float cs, sn;
-                shift_cossin(m.delta, __ldg(P.freq + f), cs, sn);
-                const float a = x[r][2 * i + e], b = x[r + 2][2 * i + e];
-                x[r][2 * i + e] = a * cs + b * sn;
-                x[r + 2][2 * i + e] = b * cs - a * sn;
-              }
-        } else {
-          // pair (2f, 2f + 1) = the two halves of one register, f = 8 r + (i >= 2 ? 4 : 0) + tq
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int f = 8 * r + 4 * half + tq;
-              float cs, sn;
-              shift_cossin(m.delta, __ldg(P.freq + f), cs, sn);
-#pragma unroll
-              for (int i = 2 * half; i < 2 * half + 2; ++i) {
-                const float a = x[r][2 * i], b = x[r][2 * i + 1];
-                x[r][2 * i] = a * cs + b * sn;
-                x[r][2 * i + 1] = b * cs - a * sn;
-              }
-            }
-        }
+      // R(-delta) on the rope part: lane f takes frequency f for all 16 heads
+      // (pairs (2f, 2f + 1) interleaved, (f, f + 32) neox)
+      const int f = lane;
+      const int ia = NEOX ? f : 2 * f, ib = NEOX ? f + 32 : 2 * f + 1;
+      float cs = 1.0f, sn = 0.0f;
+      if (m.delta != 0) shift_cossin(m.delta, __ldg(P.freq + f), cs, sn);
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(qs) + R0 * 16;
+#pragma unroll 4
+      for (int row = 0; row < 16; ++row) {
+        const uint16_t* qrow = src + row * (kMlaQPitch / 2);
+        const float a = __uint_as_float(static_cast<uint32_t>(qrow[ia]) << 16);
+        const float b = __uint_as_float(static_cast<uint32_t>(qrow[ib]) << 16);
+        const float ra = a * cs + b * sn, rb = b * cs - a * sn;
+        const __nv_bfloat16 ha = __float2bfloat16_rn(ra), hb = __float2bfloat16_rn(rb);
+        const __nv_bfloat16 la = __float2bfloat16_rn(ra - __bfloat162float(ha));
+        const __nv_bfloat16 lb = __float2bfloat16_rn(rb - __bfloat162float(hb));
+        __nv_bfloat16* hi_row = reinterpret_cast<__nv_bfloat16*>(rope_hl + row * kMlaRopePitch);
+        __nv_bfloat16* lo_row = reinterpret_cast<__nv_bfloat16*>(rope_hl + (16 + row) * kMlaRopePitch);
+        hi_row[ia] = ha;
+        hi_row[ib] = hb;
+        lo_row[ia] = la;
+        lo_row[ib] = lb;
       }
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) split_bf16x2(x[r][2 * i], x[r][2 * i + 1], qh[r][i], ql[r][i]);
+      __syncwarp();
       cur_delta = m.delta;
       have_rot = true;
     }
 
     const uint32_t kbase = ring_u32 + static_cast<uint32_t>(slot * L.stage_bytes);
-    // ---- partial S over this quarter's k-steps (two n-tiles of 8 positions)
-    float s[2][4] = {};
-    if (qr < 3) {
+    // ---- partial S over this quarter's k-steps (two n-tiles of 8 positions;
+    // even and odd k-steps accumulate separately: two short dependency chains)
+    float s[2][4] = {}, s2[2][4] = {};
+    const int nope_ks = qr < 3 ? kMlaQKS : R0;
 #pragma unroll
-      for (int kk = 0; kk < kMlaQKS; ++kk) {
-        uint32_t b0, b1, b2, b3;
+    for (int kk = 0; kk < kMlaQKS; ++kk) {
+      if (kk < nope_ks) {
+        uint32_t a[4], b0, b1, b2, b3;
+        ldsm_x4(qs_u32 + a_lane + kk * 32, a[0], a[1], a[2], a[3]);
         ldsm_x4(kbase + k_lane + (kMlaQKS * qr + kk) * 32, b0, b1, b2, b3);
-        mma_bf16(s[0], qa[kk], b0, b1);
-        mma_bf16(s[1], qa[kk], b2, b3);
-      }
-    } else {
-      constexpr int R0 = kMlaRopeKS0 - kMlaQKS * 3;
-#pragma unroll
-      for (int kk = 0; kk < R0; ++kk) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + k_lane + (kMlaQKS * 3 + kk) * 32, b0, b1, b2, b3);
-        mma_bf16(s[0], qa[kk], b0, b1);
-        mma_bf16(s[1], qa[kk], b2, b3);
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + k_lane + (kMlaRopeKS0 + r) * 32, b0, b1, b2, b3);
-        mma_bf16(s[0], qh[r], b0, b1);
-        mma_bf16(s[1], qh[r], b2, b3);
-        mma_bf16(s[0], ql[r], b0, b1);
-        mma_bf16(s[1], ql[r], b2, b3);
+        if (kk & 1) {
+          mma_bf16(s2[0], a, b0, b1);
+          mma_bf16(s2[1], a, b2, b3);
+        } else {
+          mma_bf16(s[0], a, b0, b1);
+          mma_bf16(s[1], a, b2, b3);
+        }
       }
     }
+    if (qr == 3) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        uint32_t ah[4], al[4], b0, b1, b2, b3;
+        ldsm_x4(rope_u32 + r_lane + r * 32, ah[0], ah[1], ah[2], ah[3]);
+        ldsm_x4(rope_u32 + 16 * kMlaRopePitch + r_lane + r * 32, al[0], al[1], al[2], al[3]);
+        ldsm_x4(kbase + k_lane + (kMlaRopeKS0 + r) * 32, b0, b1, b2, b3);
+        mma_bf16(s[0], ah, b0, b1);
+        mma_bf16(s[1], ah, b2, b3);
+        mma_bf16(s2[0], al, b0, b1);
+        mma_bf16(s2[1], al, b2, b3);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
     // ---- exchange partial scores within the head group
     float* part = my_sbuf + (gphase & 1) * (4 * 256);
 #pragma unroll
@@ -1014,9 +1008,12 @@ namespace pic {
 
 bool attend_mla_config(int ng, int* ring, size_t* smem_bytes) {
   if (ng != 1 && ng != 2) return false;
+  // one group of 16 heads: two CTAs per SM (half the shared memory each, so
+  // eight consumer warps share an SM); two groups: one CTA
+  const size_t budget = ng == 1 ? kMlaSmemHalf : kSmemBudget;
   const MlaLayout base = mla_layout(ng, 0);
-  if (base.total + 2 * base.stage_bytes > kSmemBudget) return false;
-  int n = static_cast<int>((kSmemBudget - base.total) / base.stage_bytes);
+  if (base.total + 3 * base.stage_bytes > budget) return false;
+  int n = static_cast<int>((budget - base.total) / base.stage_bytes);
   if (n > kMlaMaxStages) n = kMlaMaxStages;
   *ring = n;
   *smem_bytes = mla_layout(ng, n).total;

@@ -541,7 +541,8 @@ def pic_attend_decode(ctx, plans, source, q, softmax_scale, k_pool, v_pool, k_ca
                       workspace=None, sink_bias=0.0, layer_begin=0, stream=None):
     """One decode step of attention over each plan's context.  q: CUDA bf16
     [num_layers][n_req][num_q_heads][head_dim]; out: CUDA float32 of the same
-    shape; lse: CUDA float32 [num_layers][n_req][num_q_heads] or None."""
+    shape (MLA: [..][512], the latent); lse: CUDA float32
+    [num_layers][n_req][num_q_heads] or None.  MLA: v_pool and v_cache are None."""
     num_layers, n_req, hq = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
     if n_req != len(plans):
         raise ValueError("q holds one row per plan")
