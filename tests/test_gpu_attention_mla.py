@@ -179,3 +179,48 @@ def test_mla_rejects_unsupported_head_counts():
         assert e.value.status_name == "PIC_ERR_UNSUPPORTED"
     finally:
         pic.pic_destroy(S["ctx"])
+
+
+def test_deepseek_full_launch_sampled_layers():
+    """The benchmark's launch (DeepSeek-V3 MLA shapes: 61 layers, 65,536
+    positions of 16-128-token chunks behind a 32-token leading chunk, 16 query
+    heads) in one call; layers 0, 30 and 60 against the oracle, and the cache
+    path over the stitched copy against the fused result everywhere."""
+    from gpu_util import Stitched
+    wl = W.deepseek_v3_mla()
+    st = Stitched(wl).run()
+    try:
+        m = wl.model
+        H, L = 16, m.num_layers
+        g = torch.Generator(device=DEV)
+        g.manual_seed(11)
+        q = torch.empty((L, 1, H, ROW), dtype=torch.bfloat16, device=DEV).normal_(0.0, 1.0, generator=g)
+        scale = 1.0 / math.sqrt(192)
+        ws = torch.empty(pic.pic_attend_workspace_bytes(st.ctx, st.plans, H, L), dtype=torch.uint8, device=DEV)
+        res = {}
+        for src in (pic.PIC_ATTEND_FUSED, pic.PIC_ATTEND_CACHE):
+            out = torch.empty((L, 1, H, LATENT), dtype=torch.float32, device=DEV)
+            lse = torch.empty((L, 1, H), dtype=torch.float32, device=DEV)
+            pic.pic_attend_decode(st.ctx, st.plans, src, q, scale, st.k_pool, None, st.k_cache, None, out, lse, ws)
+            assert pic.pic_query_device_status(st.ctx, ws) == 0
+            res[src] = (out.cpu().double().numpy(), lse.cpu().double().numpy())
+        out, lse = res[pic.PIC_ATTEND_FUSED]
+        layers = [0, 30, 60]
+        sources = {pic.pic_lookup_chunk(st.ctx, W.chunk_key(wl.name, c)): ("pool", off)
+                   for c, off in enumerate(wl.pool_offsets)}
+        S = dict(m=m, plans=st.plans, tables=list(st.tables), sources=sources, bs=m.block_size,
+                 pool=st.k_pool[layers].cpu(), cache=st.k_cache[layers].cpu())
+        rows, segs, T = _context_rows(S, 0)
+        assert T == 65536
+        qb = bits(q)
+        for i, l in enumerate(layers):
+            o, s = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[l, 0]), rows[i][:, None, :],
+                                           rows[i][:, None, :LATENT], scale, None)
+            np.testing.assert_allclose(out[l, 0], o, atol=2e-3, rtol=0)
+            np.testing.assert_allclose(lse[l, 0], s, atol=2e-3, rtol=0)
+        out_c, lse_c = res[pic.PIC_ATTEND_CACHE]
+        np.testing.assert_allclose(out_c, out, atol=3e-2, rtol=0)
+        np.testing.assert_allclose(lse_c, lse, atol=3e-2, rtol=0)
+    finally:
+        st.close()
+        torch.cuda.empty_cache()
