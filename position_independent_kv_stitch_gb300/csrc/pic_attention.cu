@@ -90,9 +90,9 @@ struct SmemLayout {
 };
 __host__ __device__ inline SmemLayout smem_layout(int D, int G, int HB, int ring) {
   SmemLayout L{};
-  L.meta = 2 * kAttnMaxStages * sizeof(uint64_t);
+  L.meta = 4 * kAttnMaxStages * sizeof(uint64_t);  // full and empty barriers of the K and V halves
   L.prod = L.meta + kAttnMaxStages * sizeof(StageMeta);
-  L.warp = (L.prod + sizeof(ProdState) + 127) / 128 * 128;
+  L.warp = (L.prod + 2 * sizeof(ProdState) + 127) / 128 * 128;  // one descriptor ring per producer
   L.qrot = static_cast<size_t>(G) * D * 2;
   L.warp_bytes = (L.qrot + static_cast<size_t>(G) * D * 4 + 127) / 128 * 128;
   L.ring = (L.warp + HB * L.warp_bytes + 127) / 128 * 128;
@@ -157,9 +157,9 @@ __device__ __forceinline__ int advance_stage(int j, int k, int n_stages) {
   return j;
 }
 
-// grid: persistent CTAs; block: 32 * (HB + 1) threads.
+// grid: persistent CTAs; block: 32 * (HB + 2) threads (HB consumers, a K and a V producer).
 template <int PAIRING, int D, int G>
-__global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const AttnParams P) {
+__global__ void __launch_bounds__(32 * (kAttnMaxHeads + 2), 1) k_attend(const AttnParams P) {
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr int HALF = D / 2;
   constexpr int KS = D / 16;   // k-steps of Q K^T
@@ -170,8 +170,13 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
   const int HB = P.heads_per_cta;
   const int NS = P.ring;
   const SmemLayout L = smem_layout(D, G, HB, NS);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kAttnMaxStages;
+  // Each ring slot holds a stage's K rows then its V rows; the halves have
+  // their own barriers, so a slot's K half is refilled as soon as every
+  // consumer has its scores, while its V half is still being read.
+  uint64_t* full_k = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* full_v = full_k + kAttnMaxStages;
+  uint64_t* empty_k = full_v + kAttnMaxStages;
+  uint64_t* empty_v = empty_k + kAttnMaxStages;
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
   uint8_t* ring = smem + L.ring;
   const size_t srow = static_cast<size_t>(HB) * D * 2;  // bytes of one position's rows
@@ -188,20 +193,27 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
     reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], HB);
+      mbar_init(&full_k[s], 1);
+      mbar_init(&full_v[s], 1);
+      mbar_init(&empty_k[s], HB);
+      mbar_init(&empty_v[s], HB);
     }
     fence_mbar_init();
   }
   fence_proxy_async_smem();  // the zeros are ordered before the bulk copies into the ring
   __syncthreads();
 
-  if (warp == HB) {
-    // ------------------------------------------------------------ producer
+  if (warp >= HB) {
+    // ----------------------------------------------------------- producers
+    // Warp HB fills the K halves of the slots (and writes each stage's
+    // meta), warp HB + 1 the V halves; each walks every unit of the CTA.
     // Descriptors run ahead: each iteration requests unit u + 4's stage and
     // unit u + 2's token rows (whose stage arrived two iterations ago), and
     // waits only for the requests of two iterations ago.
-    ProdState* ps = reinterpret_cast<ProdState*>(smem + L.prod);
+    const bool vq = warp == HB + 1;
+    uint64_t* fb = vq ? full_v : full_k;
+    uint64_t* eb = vq ? empty_v : empty_k;
+    ProdState* ps = reinterpret_cast<ProdState*>(smem + L.prod) + (vq ? 1 : 0);
     const int n_st = P.n_stages;
     int j = static_cast<int>(u_begin % n_st);       // stage of unit u within its layer
     int layer = static_cast<int>(u_begin / n_st);
@@ -265,19 +277,18 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
     uint32_t round = 0;   // how many times the ring has wrapped
     for (int64_t u = u_begin; u < u_end; ++u, ++it) {
       // every lane polls; the warp leaves together if any lane gave up
-      if (round > 0 && !__all_sync(kFullMask, mbar_wait_bounded(&empty[slot], (round - 1) & 1u))) {
+      if (round > 0 && !__all_sync(kFullMask, mbar_wait_bounded(&eb[slot], (round - 1) & 1u))) {
         failed = true;
         break;
       }
-      if (lane == 0) meta[slot] = pm;
+      if (!vq && lane == 0) meta[slot] = pm;
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(2 * pn * srow));
+      if (lane == 0) mbar_arrive_expect_tx(&fb[slot], static_cast<uint32_t>(pn * srow));
       __syncwarp();
       if (lane < pn) {
-        // one copy per position and tensor, into the padded row pitch
-        uint8_t* kd = ring + slot * L.stage_bytes + lane * L.row_pitch;
-        bulk_load(kd, pks, static_cast<uint32_t>(srow), &full[slot]);
-        bulk_load(kd + ST * L.row_pitch, pvs, static_cast<uint32_t>(srow), &full[slot]);
+        // one copy per position, into the padded row pitch of this half
+        uint8_t* d = ring + slot * L.stage_bytes + (vq ? ST * L.row_pitch : 0) + lane * L.row_pitch;
+        bulk_load(d, vq ? pvs : pks, static_cast<uint32_t>(srow), &fb[slot]);
       }
       // ring entries being refilled held units u - 4 (stage) and u - 2 (rows): both done
       if (u + kDescAhead < u_end) fetch_desc(P, ps, u + kDescAhead, advance_stage(j, kDescAhead, n_st), lane);
@@ -300,12 +311,11 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
       // wait (bounded) for every copy this warp issued before leaving
       const int64_t issued = it;
       for (int64_t k = (issued > NS ? issued - NS : 0); k < issued; ++k)
-        mbar_wait_bounded(&full[k % NS], static_cast<uint32_t>((k / NS) & 1));
+        mbar_wait_bounded(&fb[k % NS], static_cast<uint32_t>((k / NS) & 1));
     }
     cp_async_wait<0>();  // no descriptor copy may outlive the CTA
     return;
   }
-  if (warp > HB) return;
 
   // -------------------------------------------------------------- consumer
   const int h = warp;              // KV head within the group
@@ -329,7 +339,7 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
   int slot = 0;
   uint32_t round = 0;
   for (int64_t u = u_begin; u < u_end; ++u) {
-    if (!__all_sync(kFullMask, mbar_wait_bounded(&full[slot], round & 1u))) {
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&full_k[slot], round & 1u))) {
       if (lane == 0) atomicOr(P.status, kDevTimeout);
       return;
     }
@@ -392,6 +402,9 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
       mma_bf16(s0[kk & 1], qa[kk], b0, b1);
       mma_bf16(s1[kk & 1], qa[kk], b2, b3);
     }
+    // the K half is free for the next stage as soon as every consumer has its scores
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_k[slot]);
     // this lane's scores: head g, positions 2tq, 2tq + 1, 8 + 2tq, 9 + 2tq
     float sc[4] = {(s0[0][0] + s0[0][2]) + (s0[1][0] + s0[1][2]), (s0[0][1] + s0[0][3]) + (s0[1][1] + s0[1][3]),
                    (s1[0][0] + s1[0][2]) + (s1[1][0] + s1[1][2]), (s1[0][1] + s1[0][3]) + (s1[1][1] + s1[1][3])};
@@ -418,6 +431,10 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
     split_bf16x2(p[0], p[1], pa[0], pa[1]);
     split_bf16x2(p[2], p[3], pa[2], pa[3]);
 
+    if (!__all_sync(kFullMask, mbar_wait_bounded(&full_v[slot], round & 1u))) {
+      if (lane == 0) atomicOr(P.status, kDevTimeout);
+      return;
+    }
     // ---- O = alpha O + [p_hi; p_lo] V (alpha is 1 once the running max settles)
     if (!__all_sync(kFullMask, alpha == 1.0f)) {
 #pragma unroll
@@ -436,7 +453,7 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 1), 1) k_attend(const At
       mma_bf16(o[j + 1], pa, b2, b3);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (lane == 0) mbar_arrive(&empty_v[slot]);
     if (++slot == NS) {
       slot = 0;
       ++round;
@@ -494,7 +511,7 @@ cudaError_t launch_g(const AttnParams& p, int grid, size_t smem, cudaStream_t s)
   auto kern = k_attend<PAIRING, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, 32 * (p.heads_per_cta + 1), smem, s>>>(p);
+  kern<<<grid, 32 * (p.heads_per_cta + 2), smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_attend_merge<D><<<dim3(p.n_req, p.num_q_heads, p.n_layers), D, 0, s>>>(p, G);
@@ -507,7 +524,7 @@ int occupancy_g(int heads_per_cta, size_t smem) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (heads_per_cta + 1), smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (heads_per_cta + 2), smem) != cudaSuccess) return 0;
   return n;
 }
 
