@@ -13,7 +13,11 @@ namespace dev {
 
 constexpr unsigned kDevBadBlock = 0x1u;   // PIC_DEV_BAD_BLOCK
 constexpr unsigned kDevTimeout = 0x2u;    // PIC_DEV_TIMEOUT
-constexpr uint32_t kMaxSpins = 1u << 22;  // tries of one bounded mbarrier wait
+// Tries of one bounded mbarrier wait.  An unfinished try_wait suspends the
+// thread for a few microseconds (about 4 us per try measured on GB300), so a
+// wait gives up after about a second; a copy the kernel issued lands within
+// microseconds.
+constexpr uint32_t kMaxSpins = 1u << 18;
 
 // cos / sin of delta * theta_i.  The host gives f_i = theta_i / (2 pi) as a
 // float pair hi + lo; delta * hi is split exactly into p + e with one FMA
@@ -90,9 +94,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// true when the phase completed, false after kMaxSpins tries
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMaxSpins; ++i)
+// true when the phase completed, false after max_spins tries
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t max_spins = kMaxSpins) {
+  for (uint32_t i = 0; i < max_spins; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }

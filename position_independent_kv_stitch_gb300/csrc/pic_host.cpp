@@ -176,6 +176,9 @@ struct pic_ctx {
   StagingSlot staging[kStagingSlots];
   int staging_next = 0;
   int staging_device = -1;
+  // pic_debug_stall_next_launch: consumed by the next pic_stitch
+  int32_t debug_stall = 0;   // tile + 1, 0 = off
+  uint32_t debug_spins = 0;  // 0 = the default wait bound
   pic_ctx(int32_t nb) : num_cache_blocks(nb), alloc(nb) {}
 };
 
@@ -1242,6 +1245,10 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
   pic::KernelParams p{};
   fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_ws), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
                      v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
+  p.debug_stall = ctx->debug_stall;
+  p.max_spins = ctx->debug_spins;
+  ctx->debug_stall = 0;
+  ctx->debug_spins = 0;
   const cudaError_t e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0, mostly_in_place(plans, n_req));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
   for (int32_t r = 0; r < n_req; ++r) const_cast<pic_plan*>(plans[r])->applied = true;
@@ -1343,6 +1350,13 @@ pic_status pic_query_device_status(pic_ctx* ctx, const void* d_ws, pic_stream_t 
                 "position %u; bit 0x2: a bounded wait gave up; 0x4: token id outside the Gear table; "
                 "0x8: bad document offsets; 0x10: more chunks than capacity; 0x20: bad span)",
                 h.status, h.bad_req, h.bad_pos);
+  return ok(ctx);
+}
+
+pic_status pic_debug_stall_next_launch(pic_ctx* ctx, int32_t stall_tile, uint32_t max_spins) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  ctx->debug_stall = stall_tile >= 0 ? stall_tile + 1 : 0;
+  ctx->debug_spins = stall_tile >= 0 ? max_spins : 0;
   return ok(ctx);
 }
 

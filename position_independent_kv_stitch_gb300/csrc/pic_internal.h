@@ -77,6 +77,11 @@ struct KernelParams {
   int32_t* indptr_dst;      // recompute CSR offsets output (may be null)
   int32_t n_indptr;
   WsHeader* header;
+  // Test hook of the bulk pipeline's failure path (pic_debug_stall_next_launch):
+  // debug_stall = t + 1 makes CTA 0 skip tile t's copies and barrier arrival;
+  // max_spins bounds every mbarrier wait (0: the default bound).
+  int32_t debug_stall;
+  uint32_t max_spins;
 };
 
 // Shared-memory pipeline shape of the bulk-copy kernels.

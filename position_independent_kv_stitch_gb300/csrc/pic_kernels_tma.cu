@@ -169,6 +169,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
     m.has_v = has_v ? 1 : 0;
     m.dst_k = P.k_dst + l * P.dst_layer_stride + dst_off;
     m.dst_v = HAS_V ? P.v_dst + l * P.dst_layer_stride + dst_off : nullptr;
+    // test hook (pic_debug_stall_next_launch): this tile's barrier never
+    // completes, so the waits for it run out and take the failure path below
+    if (P.debug_stall != 0 && blockIdx.x == 0 && t == P.debug_stall - 1) return;
     if (!valid || ntok == 0) {
       mbar_arrive(&bars[s]);  // nothing to copy: complete the phase
       return;
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
     }
   };
 
+  const uint32_t spins = P.max_spins != 0 ? P.max_spins : kMaxSpins;
   int issued = 0;
   if (tid == 0) {
     const int pre = min(C.stages - 1, n_tiles);
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
   for (; t < n_tiles; ++t) {
     const int sidx = t % C.stages;
     const uint32_t parity = static_cast<uint32_t>(t / C.stages) & 1u;
-    const bool ok = mbar_wait_bounded(&bars[sidx], parity);
+    const bool ok = mbar_wait_bounded(&bars[sidx], parity, spins);
     if (__syncthreads_or(!ok)) {
       aborted = true;
       break;
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
       atomicOr(&P.header->status, kDevTimeout);
       // wait (bounded) for loads this CTA started but nobody consumed
       for (int u = t; u < issued; ++u)
-        mbar_wait_bounded(&bars[u % C.stages], static_cast<uint32_t>(u / C.stages) & 1u);
+        mbar_wait_bounded(&bars[u % C.stages], static_cast<uint32_t>(u / C.stages) & 1u, spins);
     }
     bulk_wait_all();
   }

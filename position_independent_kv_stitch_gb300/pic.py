@@ -116,6 +116,7 @@ _SIGNATURES = {
     "pic_fingerprint_spans": (ctypes.c_int, [_c_void_p, _i64, _c_void_p, _c_void_p, _i64, ctypes.c_uint64,
                                              _c_void_p, _c_void_p, _c_void_p]),
     "pic_s1_windows": (ctypes.c_int, [_i64, _i64, _i32, _P(_i64), _P(_i64), _i64, _P(_i64)]),
+    "pic_debug_stall_next_launch": (ctypes.c_int, [_c_void_p, _i32, _u32]),
 }
 
 _lib = None
@@ -553,6 +554,13 @@ def pic_attend_decode(ctx, plans, source, q, softmax_scale, k_pool, v_pool, k_ca
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream_handle(stream))
     _check(st, ctx)
+
+
+def pic_debug_stall_next_launch(ctx, stall_tile: int, max_spins: int = 0):
+    """Test hook: the next bulk-pipeline stitch on ctx leaves tile stall_tile
+    of its first CTA without copies, so its bounded waits run out and raise
+    PIC_DEV_TIMEOUT (see include/pic.h)."""
+    _check(load().pic_debug_stall_next_launch(ctx, int(stall_tile), int(max_spins)), ctx)
 
 
 def pic_kernel_variant(ctx, mode: int) -> int:

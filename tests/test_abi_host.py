@@ -274,3 +274,14 @@ def test_workspace_sizes_grow_with_runs():
         assert pic.pic_rerotate_workspace_bytes(ctx, [(0, 3, 40, 7)]) > pic.pic_rerotate_workspace_bytes(ctx, [(0, 3, 40, 0)])
     finally:
         pic.pic_destroy(ctx)
+
+
+def test_debug_stall_hook_checks_its_context():
+    L = pic.load()
+    assert pic.STATUS_NAMES[L.pic_debug_stall_next_launch(None, 2, 1000)] == "PIC_ERR_INVALID_ARG"
+    ctx = _gqa_ctx(nb=8)
+    try:
+        pic.pic_debug_stall_next_launch(ctx, 2, 1000)
+        pic.pic_debug_stall_next_launch(ctx, -1)
+    finally:
+        pic.pic_destroy(ctx)
