@@ -489,20 +489,25 @@ class Rig:
         self.pic.pic_query_device_status(self.ctx, ws)
 
 
-def run_e2e(rig, steps, warmup):
-    """Same metric end to end through the public API with HOST buffers: the
-    chunk pool and the paged cache live in pinned host memory, which the
-    stitch kernel reads and writes directly over the host link (on GB300,
-    NVLink-C2C to Grace memory) -- the pool's bytes cross host->device and the
-    stitched cache's bytes device->host inside the timed region, every step.
-    Each step also plans, uploads the block table and reads the recompute
-    list back to the host."""
+def run_e2e(rig, steps, warmup, cache_on_host=False):
+    """Same metric end to end through the public API with the chunk pool in
+    HOST memory: the pool lives in pinned host memory (a host-side chunk
+    store), which the stitch kernel reads directly over the host link (on
+    GB300, NVLink-C2C to Grace memory), so the pool's bytes cross
+    host->device inside the timed region every step.  The paged cache is in
+    HBM, where decode attention reads it (cache_on_host: in pinned host
+    memory too, so the stitched bytes also cross device->host).  Each step
+    also plans, uploads the block table and reads the recompute list back to
+    the host."""
     torch = rig.torch
     pic = rig.pic
     hk = rig.k_pool.cpu().pin_memory()
     hv = rig.v_pool.cpu().pin_memory() if rig.v_pool is not None else None
-    hkc = torch.empty(rig.k_cache.shape, dtype=rig.k_cache.dtype).pin_memory()
-    hvc = torch.empty(rig.v_cache.shape, dtype=rig.v_cache.dtype).pin_memory() if rig.v_cache is not None else None
+    if cache_on_host:
+        hkc = torch.empty(rig.k_cache.shape, dtype=rig.k_cache.dtype).pin_memory()
+        hvc = torch.empty(rig.v_cache.shape, dtype=rig.v_cache.dtype).pin_memory() if rig.v_cache is not None else None
+    else:
+        hkc, hvc = rig.k_cache, rig.v_cache
     oi = torch.empty_like(rig.ridx, device="cpu").pin_memory()
     op = torch.empty_like(rig.indptr, device="cpu").pin_memory()
 
@@ -529,7 +534,7 @@ def run_e2e(rig, steps, warmup):
     rows = wl.token_layers * rig.m.num_kv_heads * rig.m.head_dim * 2   # bytes of K rows moved
     tensors = 2 if hv is not None else 1
     h2d = rows * tensors + rig.d_bt.numel() * 4 + rig.ws_bytes
-    d2h = rows * tensors + oi.numel() * 4 + op.numel() * 4
+    d2h = (rows * tensors if cache_on_host else 0) + oi.numel() * 4 + op.numel() * 4
     return ms, h2d, d2h
 
 
@@ -706,6 +711,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling captures only)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-cache-on-host", action="store_true",
+                    help="end-to-end leg: keep the paged cache in pinned host memory too")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -788,12 +795,14 @@ def main():
 
     e2e = None
     if not args.no_e2e and args.mode == "stitch":
-        ems, h2d, d2h = run_e2e(rig, max(3, min(args.steps, 10)), 3)
+        ems, h2d, d2h = run_e2e(rig, max(3, min(args.steps, 10)), 3, args.e2e_cache_on_host)
         ems = max_over_ranks(ems, dev)
+        where = "pool and cache" if args.e2e_cache_on_host else "pool"
         e2e = {"value": world * algo_bytes / (ems * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ems,
-               "how": "pool and cache in pinned host memory, streamed by the kernel over NVLink-C2C; "
-                      "block table up, recompute list down"}
+               "how": f"{where} in pinned host memory, streamed by the kernel over NVLink-C2C"
+                      + ("" if args.e2e_cache_on_host else ", cache written to HBM")
+                      + "; block table up, recompute list down"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:

@@ -54,7 +54,10 @@ struct StageMeta {
 
 // MODE 0: GQA/MLA stitch with values (K + V tiles); 1: stitch without values
 // (MLA rows); 2: in place (K rows of the cache, read and written back).
-template <int PAIRING, int RD, int MODE>
+// HOOK: the instance launched only under pic_debug_stall_next_launch (the
+// stall test hook and a launch-specific wait bound); the production
+// instances carry neither.
+template <int PAIRING, int RD, int MODE, bool HOOK = false>
 __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelParams P, const TmaConfig C) {
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr bool HAS_V = (MODE == 0);
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
     m.dst_v = HAS_V ? P.v_dst + l * P.dst_layer_stride + dst_off : nullptr;
     // test hook (pic_debug_stall_next_launch): this tile's barrier never
     // completes, so the waits for it run out and take the failure path below
-    if (P.debug_stall != 0 && blockIdx.x == 0 && t == P.debug_stall - 1) return;
+    if (HOOK && P.debug_stall != 0 && blockIdx.x == 0 && t == P.debug_stall - 1) return;
     if (!valid || ntok == 0) {
       mbar_arrive(&bars[s]);  // nothing to copy: complete the phase
       return;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma_pipeline(const KernelPar
     }
   };
 
-  const uint32_t spins = P.max_spins != 0 ? P.max_spins : kMaxSpins;
+  const uint32_t spins = HOOK && P.max_spins != 0 ? P.max_spins : kMaxSpins;
   int issued = 0;
   if (tid == 0) {
     const int pre = min(C.stages - 1, n_tiles);
@@ -289,6 +292,16 @@ size_t tma_smem_bytes(const TmaConfig& c) {
 cudaError_t launch_tma(const KernelParams& p, const TmaConfig& c, int mode, int pairing, int rope_dim, int grid,
                        cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
+  if (p.debug_stall != 0 || p.max_spins != 0) {  // test hook: stitch modes only
+#define PIC_TMA_HOOK(MODE_, PAIR_, RD_)                                             \
+  if (mode == MODE_ && pairing == PAIR_ && rope_dim == RD_)                         \
+    return launch_one(k_tma_pipeline<PAIR_, RD_, MODE_, true>, p, c, grid, stream);
+    PIC_TMA_HOOK(0, kNeox, 64) PIC_TMA_HOOK(0, kNeox, 128) PIC_TMA_HOOK(0, kNeox, 256)
+    PIC_TMA_HOOK(0, kInterleaved, 64) PIC_TMA_HOOK(0, kInterleaved, 128) PIC_TMA_HOOK(0, kInterleaved, 256)
+    PIC_TMA_HOOK(1, kNeox, 64) PIC_TMA_HOOK(1, kInterleaved, 64)
+#undef PIC_TMA_HOOK
+    return cudaErrorInvalidValue;
+  }
 #define PIC_TMA_CASE(MODE_, PAIR_, RD_)                                             \
   if (mode == MODE_ && pairing == PAIR_ && rope_dim == RD_)                         \
     return launch_one(k_tma_pipeline<PAIR_, RD_, MODE_>, p, c, grid, stream);
