@@ -480,9 +480,30 @@ __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 2), 1) k_attend(const At
 }
 
 // One thread block per (request, query head, layer): merges the records of
-// its key.  Statistics are in log2 units.
+// its key (flash-decoding).  Statistics are in log2 units.  The records'
+// maxima and sums are reduced across the block's threads; each record's
+// weight exp2(m_k - M) is kept in shared memory for the weighted sum over
+// the output dims.
+constexpr int kMergeThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(kFullMask, v, o);
+    v = is_max ? fmaxf(v, w) : v + w;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red is free
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = red[0];
+  for (int w = 1; w < kMergeThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+  return v;
+}
+
 template <int D>
-__global__ void __launch_bounds__(128) k_attend_merge(const AttnParams P, int group) {
+__global__ void __launch_bounds__(kMergeThreads) k_attend_merge(const AttnParams P, int group) {
+  __shared__ float s_e[kAttnMaxCtas];  // exp2(m_k - M) per record
+  __shared__ float s_red[kMergeThreads / 32];
   const int r = blockIdx.x, gq = blockIdx.y, lz = blockIdx.z;
   const int hk = gq / group, g = gq % group;
   const int HB = P.heads_per_cta;
@@ -492,15 +513,21 @@ __global__ void __launch_bounds__(128) k_attend_merge(const AttnParams P, int gr
   const int BLK = attn_block_floats(group, D);
   const float* base = P.records + static_cast<int64_t>(h) * BLK;
   const int64_t stride = static_cast<int64_t>(HB) * BLK;
-  float M = -FLT_MAX;
-  for (int k = rec0; k < rec1; ++k) M = fmaxf(M, base[k * stride + group * D + g]);
-  float tot = 0.0f;
-  for (int k = rec0; k < rec1; ++k)
-    tot += exp2f(base[k * stride + group * D + g] - M) * base[k * stride + group * D + group + g];
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float s = 0.0f;
-    for (int k = rec0; k < rec1; ++k) s += exp2f(base[k * stride + group * D + g] - M) * base[k * stride + g * D + d];
-    P.out[((static_cast<int64_t>(lz) * P.n_req + r) * P.num_q_heads + gq) * D + d] = s / tot;
+  float mloc = -FLT_MAX;
+  for (int k = rec0 + threadIdx.x; k < rec1; k += kMergeThreads) mloc = fmaxf(mloc, base[k * stride + group * D + g]);
+  const float M = block_reduce(mloc, true, s_red);
+  float tloc = 0.0f;
+  for (int k = rec0 + threadIdx.x; k < rec1; k += kMergeThreads) {
+    const float e = exp2f(base[k * stride + group * D + g] - M);
+    s_e[k - rec0] = e;
+    tloc += e * base[k * stride + group * D + group + g];
+  }
+  const float tot = block_reduce(tloc, false, s_red);  // its barriers also publish s_e
+  const float inv = 1.0f / tot;
+  for (int d = threadIdx.x; d < D; d += kMergeThreads) {
+    float acc = 0.0f;
+    for (int k = rec0; k < rec1; ++k) acc += s_e[k - rec0] * base[k * stride + g * D + d];
+    P.out[((static_cast<int64_t>(lz) * P.n_req + r) * P.num_q_heads + gq) * D + d] = acc * inv;
   }
   if (threadIdx.x == 0 && P.lse != nullptr)
     P.lse[(static_cast<int64_t>(lz) * P.n_req + r) * P.num_q_heads + gq] = (M + log2f(tot)) * 0.69314718055994531f;
@@ -514,7 +541,7 @@ cudaError_t launch_g(const AttnParams& p, int grid, size_t smem, cudaStream_t s)
   kern<<<grid, 32 * (p.heads_per_cta + 2), smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_attend_merge<D><<<dim3(p.n_req, p.num_q_heads, p.n_layers), D, 0, s>>>(p, G);
+  k_attend_merge<D><<<dim3(p.n_req, p.num_q_heads, p.n_layers), kMergeThreads, 0, s>>>(p, G);
   return cudaGetLastError();
 }
 
@@ -970,7 +997,8 @@ cudaError_t launch_mla_g(const AttnParams& p, int grid, size_t smem, cudaStream_
   kern<<<grid, 32 * (4 * NG + 1), smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_attend_merge<kMlaLatent><<<dim3(p.n_req, p.num_q_heads, p.n_layers), 128, 0, s>>>(p, kMlaHeadsPerGroup * NG);
+  k_attend_merge<kMlaLatent><<<dim3(p.n_req, p.num_q_heads, p.n_layers), kMergeThreads, 0, s>>>(
+      p, kMlaHeadsPerGroup * NG);
   return cudaGetLastError();
 }
 
