@@ -791,7 +791,8 @@ def main():
     peak, peak_kind = measured_peak()
     value = world * algo_bytes / (ms * 1e-3) / 1e9
     achieved = algo_bytes / (kms * 1e-3) / 1e9
-    traffic = recorded_traffic(f"{wl.name}/{args.mode}")
+    # the recorded DRAM bytes are for the workload at full size, default heads
+    traffic = recorded_traffic(f"{wl.name}/{args.mode}") if not (args.layers or args.q_heads) else None
 
     e2e = None
     if not args.no_e2e and args.mode == "stitch":
