@@ -76,7 +76,7 @@ typedef enum pic_status {
   PIC_ERR_ALIGNMENT = 7,     /* pointer or stride not a multiple of 16 bytes         */
   PIC_ERR_CUDA = 8,          /* a CUDA runtime call or launch failed                 */
   PIC_ERR_DEVICE_CHECK = 9,  /* a kernel found a bad block-table entry               */
-  PIC_ERR_UNSUPPORTED = 10,  /* geometry this build has no kernel for                */
+  PIC_ERR_UNSUPPORTED = 10,  /* geometry the library has no kernel for               */
   PIC_ERR_BUSY = 11          /* chunk is mapped by a live request, or in use         */
 } pic_status;
 

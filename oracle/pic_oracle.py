@@ -394,8 +394,8 @@ def map_request(chunks, chunk_ids, block_size, pool: BlockPool, req_id, start_po
 
     EPIC Guide, runtime figure: step 1 "Virtual Block Mapping" (the request
     reuses the chunk's physical blocks) and step 2 (the keys are rotated in
-    place by dp; values untouched).  Rules (readings):
-    a block-resident chunk is mapped when aliasing is on, it starts on a
+    place by dp; values untouched).  The figure states no conditions; the
+    rules taken here: a block-resident chunk is mapped when aliasing is on, it starts on a
     block boundary, it occurs once in the request and no other live request
     uses it; otherwise it is copied out of its blocks.  A chunk mapped by a
     live request may not be used by any other (BusyError).  delta is always
