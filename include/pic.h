@@ -563,10 +563,18 @@ pic_status pic_debug_stall_next_launch(pic_ctx* ctx, int32_t stall_tile, uint32_
  * loads and stores through registers) or PIC_VARIANT_BULK_PIPELINE (bulk
  * async copies through a shared-memory ring).  The bulk pipeline is used when
  * one work unit fits a stage, unless the environment variable PIC_KERNEL was
- * "regs" at pic_create.  Both compute the same result.  -1 on bad arguments.
+ * "regs" at pic_create.  Both compute the same result.
+ * Mode 2 (pic_attend_decode): PIC_VARIANT_TENSOR_CORE_TMEM (MLA models:
+ * tcgen05 products with TMEM accumulators, rows loaded by TMA tensor copies;
+ * chosen unless PIC_ATTEND_KERNEL was "mma" at pic_create) or
+ * PIC_VARIANT_WARP_MMA (warp-level mma.sync products; GQA models, and MLA
+ * when so chosen).  Both compute the same result to rounding.
+ * -1 on bad arguments.
  */
 #define PIC_VARIANT_REGISTERS 0
 #define PIC_VARIANT_BULK_PIPELINE 1
+#define PIC_VARIANT_TENSOR_CORE_TMEM 2
+#define PIC_VARIANT_WARP_MMA 3
 int32_t pic_kernel_variant(const pic_ctx* ctx, int32_t mode);
 
 /*

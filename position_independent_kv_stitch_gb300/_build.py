@@ -23,8 +23,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libpic.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["pic_host.cpp", "pic_kernels.cu", "pic_kernels_tma.cu", "pic_attention.cu", "pic_noalloc.cu",
-           "pic_cdc.cu"]
+SOURCES = ["pic_host.cpp", "pic_kernels.cu", "pic_kernels_tma.cu", "pic_attention.cu", "pic_attention_tc.cu",
+           "pic_noalloc.cu", "pic_cdc.cu"]
 HEADERS = [os.path.join(CSRC, "pic_internal.h"), os.path.join(INCLUDE, "pic.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1075,4 +1075,9 @@ cudaError_t launch_attend_mla(const AttnParams& p, int pairing, int ng, int grid
   PIC_MLA_DISPATCH(launch_mla_g, cudaErrorInvalidValue, p, grid, smem_bytes, s);
 }
 
+cudaError_t launch_attend_merge_mla(const AttnParams& p, int heads_per_record, cudaStream_t s) {
+  k_attend_merge<kMlaLatent><<<dim3(p.n_req, p.num_q_heads, p.n_layers), kMergeThreads, 0, s>>>(p, heads_per_record);
+  return cudaGetLastError();
+}
+
 }  // namespace pic

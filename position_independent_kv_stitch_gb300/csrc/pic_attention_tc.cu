@@ -1,0 +1,836 @@
+// MLA decode attention on the fifth-generation tensor cores (tcgen05 with
+// TMEM accumulators), fed by TMA tensor copies, sm_103a.
+//
+// Irminsul: MLA-Native Position-Independent Caching for Agentic LLM Serving,
+// 2.1-2.2: every query head h attends to the shared latent rows
+// row_t = [cKV_t (512) | k_r,t (64)], with the query absorbed into the latent
+// space, q_h = [q_nope,h (512) | q_rope,h (64)].  A chunk token's rope key is
+// used as stored and the query's rope part is rotated by R(-delta) instead
+// (q . R(delta) k = (R(-delta) q) . k, R orthogonal), so no rotated copy is
+// written:
+//   s_h,t = scale * [q_nope,h | R(-delta_t) q_rope,h] . row_t + bias_t,
+//   out_h = sum_t softmax(s_h)_t cKV_t      (512 dims, before W_UV).
+// bias: LegoLink's pseudo-sink suppression (EPIC Guide: Position-Independent
+// Caching for LLM Serving, LegoLink "1. Identifying and Neutralizing
+// Pseudo-Sinks"): a constant logit offset on the first k tokens of every
+// chunk not at position 0.
+//
+// A tile is up to four plan stages (16 consecutive positions each, read from
+// consecutive rows of one source, one delta) of one (layer, key): 64
+// positions, the M of the score product.  Per tile, with warps by role:
+//   * the producer forms the tile (its delta entries, whether it opens or
+//     closes its key) and loads its rows into a ring of two tiles with 3-D
+//     TMA tile copies, one per 64-dim plane (128-byte swizzle) and per run
+//     of stages that read consecutive rows (boxes of 16 to 64 rows);
+//   * the query warp writes the query operands: q_nope on a key change, and
+//     for each new delta of the tile R(-delta) q_rope as bf16 hi and lo rows
+//     (NE delta entries, so stages with different deltas share a tile);
+//   * score issuers (one thread each) issue S = rows [q_nope | rope parts]^T
+//     into TMEM: M = 64, 32 k-steps over the latent, 4 over the rope plane;
+//   * a value issuer issues O^T += V^T P^T once P is written: M = 128
+//     latent dims (four M-tiles), N = 32 (16 heads: P's hi and lo rows side
+//     by side; 32 heads: each part in turn), K = the 16 positions of a
+//     stage; V^T is the same shared planes read as an MN-major operand;
+//   * softmax warps 0-7: warp w owns stage w's positions (TMEM lanes
+//     32 (w % 4) .. + 15 of the M = 64 scores) for half of the heads.  It
+//     adds the nope partial sums and its delta's hi and lo rope columns,
+//     keeps a running max per head that is raised only when a score passes
+//     it by more than kTcLazy (log2 units; O and l are then rescaled), writes
+//     P = exp2(s - m) as bf16 hi and lo rows, and at the key's last tile in
+//     this CTA writes the record (O, m, l) that k_attend_merge combines.
+// The hi + lo splits keep about 16 significant bits of the rotated query and
+// of P; rows and q_nope are bf16 already and every product accumulates in
+// fp32 in TMEM.  Every wait is bounded: a wait that runs out raises
+// PIC_DEV_TIMEOUT and tells the other roles to stop, and the CTA frees its
+// TMEM before it leaves.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "pic_device.cuh"
+#include "pic_internal.h"
+
+namespace pic {
+namespace {
+
+using namespace dev;
+
+constexpr int kMlaLatentDims = 512;
+constexpr int kMlaRowDims = 576;                           // latent + 64-d rope key
+constexpr int kTcStagesPerTile = 4;
+constexpr int kTcPlanes = 9;                               // 8 latent planes + the rope plane
+constexpr int kTcPlaneBytes = 64 * 128;                    // 64 rows x 64 dims x bf16
+constexpr int kTcTileBytes = kTcPlanes * kTcPlaneBytes;    // 73,728
+constexpr int kTcStageBytes = 16 * 128;                    // one stage's rows in one plane
+constexpr uint32_t kTcStageTx = kTcStageBytes * kTcPlanes; // bytes a stage's copies deliver
+constexpr float kTcLazy = 8.0f;
+// warps 0-7 softmax (warp w: TMEM lane quadrant w % 4, heads of half w / 4),
+// then the producer, the score-product issuer (it also holds the TMEM
+// allocation), the query warp, the value-product issuer and, for 16 heads, a
+// second score-product issuer.  One thread issues a small tcgen05.mma about
+// every 70 cycles whatever its shape, so the products are spread over
+// threads; 32 heads need the registers the extra warp would take.
+constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcProducer = 8, kTcMma = 9, kTcQuery = 10, kTcPv = 11, kTcMma2 = 12;
+__host__ __device__ constexpr int tc_score_issuers(int hc) { return hc == 16 ? 2 : 1; }
+__host__ __device__ constexpr int tc_threads(int hc) { return 32 * (11 + tc_score_issuers(hc)); }
+constexpr uint32_t kTcCols = 512;                          // TMEM columns held by the CTA
+// TMEM columns: two score buffers of kTcSCols (the latent score as partial
+// sums over interleaved k-steps, NP x HC columns, then the rope columns),
+// then O^T: four M-tiles of 32 columns (16 heads: the hi and lo parts of P
+// in columns 0-15 and 16-31; 32 heads: both parts summed in place).
+constexpr uint32_t kTcSCols = 192;
+constexpr uint32_t kTcOCol = 2 * kTcSCols;
+constexpr uint32_t kTcOColsPerTile = 32;
+constexpr int kTcFirst = 1, kTcLast = 2, kTcEnd = 4;       // tile flags
+
+struct TcTile {
+  int32_t ns;      // stages present
+  int32_t layer;   // local layer
+  int32_t key;
+  int32_t flags;   // kTcFirst: first tile of the key in this CTA; kTcLast: its last; kTcEnd: the CTA's last
+  int32_t n_tok[kTcStagesPerTile];
+  int32_t sink[kTcStagesPerTile];
+  int32_t entry[kTcStagesPerTile];  // delta entry of the stage's rope operand
+  int32_t fresh;                    // entries this tile (re)writes
+  int32_t ent_delta[kTcStagesPerTile];
+  int32_t pad[3];
+};
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+template <int HC>
+struct TcLayout {
+  static constexpr int NE = HC == 16 ? 4 : 2;                   // delta entries per tile
+  static constexpr int kRing = 0;                               // 2 tiles
+  static constexpr int kQn = kRing + 2 * kTcTileBytes;          // q_nope: 8 planes x HC rows x 128 B
+  static constexpr int kQnPlane = HC * 128;
+  static constexpr int kRope = kQn + 8 * kQnPlane;              // NE x (HC hi + HC lo) rows x 128 B
+  static constexpr int kPt = kRope + NE * 2 * HC * 128;         // P^T: 2 buffers x (HC hi + HC lo) rows
+  static constexpr int kPtBytes = 2 * HC * 128;
+  static constexpr int kQsrc = kPt + 2 * kPtBytes;              // q_rope as loaded: HC x 64 bf16
+  static constexpr int kWmax = kQsrc + HC * 64 * 2;             // float [2][4][HC]
+  static constexpr int kLred = kWmax + 2 * 4 * HC * 4;          // float [4][HC]
+  static constexpr int kTiles = kLred + 4 * HC * 4;             // TcTile [2]
+  static constexpr int kBars = kTiles + 2 * static_cast<int>(sizeof(TcTile));
+  // full[2] empty[2] meta[2] rope_full[2] s_full[2] p_full[2] pv_done[2] done[3]
+  static constexpr int kNumBars = 17;
+  static constexpr int kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kAlloc = kTotal + 1024;                  // room to align the base
+  static_assert(kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 && kPtBytes % 1024 == 0,
+                "operands sit on 1024-byte swizzle atoms");
+};
+
+// byte offset of element (row r, col c) of a 128B-swizzled tile of 128-byte rows
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + (((c >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+
+// tcgen05 shared-memory matrix descriptor: start, leading / stride byte
+// offsets, version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// instruction descriptor of kind::f16: bf16 A and B, fp32 D, M x N, A K- or MN-major
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc ? 1u : 0u));
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
+// N columns (8, or a multiple of 16) of this warp's TMEM lanes
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
+  if constexpr (N == 8) {
+    tmem_ld8(taddr, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; j += 16) tmem_ld16(taddr + j, v + j);
+  }
+}
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float* v) {
+  if constexpr (N == 8) {
+    tmem_st8(taddr, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; j += 16) tmem_st16(taddr + j, v + j);
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// bounded wait that also gives up once another role has aborted
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kMaxSpins; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  return false;
+}
+
+// named barrier 1 over the eight softmax warps (256 threads), returning the
+// OR of every thread's predicate
+__device__ __forceinline__ bool softmax_bar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(x);
+  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// grid: persistent CTAs, CTA c owns units [U c / G, U (c + 1) / G) of the
+// (layer, stage) list; block: 224 threads (4 softmax warps, producer, MMA,
+// query).
+template <int PAIRING, int HC>
+__global__ void __launch_bounds__(tc_threads(HC), 1)
+    k_attend_mla_tc(const AttnParams P, const __grid_constant__ TcMaps maps) {
+  using L = TcLayout<HC>;
+  constexpr int NE = L::NE;
+  constexpr bool NEOX = (PAIRING == kNeox);
+  constexpr uint32_t kIdS = idesc(64, HC, 0);
+  constexpr uint32_t kIdR = idesc(64, NE * 2 * HC, 0);
+  constexpr uint32_t kIdPV = idesc(128, 32, 1);
+  constexpr int kPvParts = HC == 16 ? 1 : 2;  // value products per stage and M-tile (N = 32 each)
+  constexpr int kSI = tc_score_issuers(HC);
+  // the latent score accumulates in NP independent partial sums (k-steps
+  // interleaved), so consecutive small products do not wait on one another
+  constexpr int NP = HC == 16 ? 4 : 2;
+  constexpr uint32_t kRopeCol = NP * HC;
+  static_assert(NE * 2 * HC == 128 && kRopeCol + NE * 2 * HC <= kTcSCols, "rope columns");
+  static_assert(kTcOCol + 4 * kTcOColsPerTile <= kTcCols, "TMEM columns");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t base_u32 = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint64_t* full = bars + 0;        // a tile's rows landed (by tile parity, as below)
+  uint64_t* empty = bars + 2;       // its value product finished: the ring slot is free
+  uint64_t* meta_ready = bars + 4;  // its metadata is written
+  uint64_t* rope_full = bars + 6;   // its query operands are written
+  uint64_t* s_full = bars + 8;      // its score product finished
+  uint64_t* p_full = bars + 10;     // its P is written
+  uint64_t* pv_done = bars + 12;    // its value product finished
+  uint64_t* done = bars + 14;       // each issuer's products all finished
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  TcTile* tiles = reinterpret_cast<TcTile*>(smem + L::kTiles);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = P.n_units, G = gridDim.x;
+  const int64_t u_begin = U * blockIdx.x / G, u_end = U * (blockIdx.x + 1) / G;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], 1);
+      mbar_init(&meta_ready[b], 1);
+      mbar_init(&rope_full[b], 1);
+      mbar_init(&s_full[b], kSI);  // every score issuer commits
+      mbar_init(&p_full[b], kTcSoftmaxWarps);
+      mbar_init(&pv_done[b], 1);
+    }
+    for (int b = 0; b < 3; ++b) mbar_init(&done[b], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTcMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                 "r"(kTcCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  auto fail = [&]() {
+    atomicOr(P.status, kDevTimeout);
+    *abort_flag = 1;
+  };
+  const bool has_work = u_begin < u_end;
+
+  if (warp == kTcProducer && has_work) {
+    // ------------------------------------------------------------ producer
+    // Forms the tiles and starts their copies.  The next tile's plan stages
+    // (lanes 0-4; the fifth tells whether the key goes on) are read while
+    // the current slot drains, and consecutive stages that read consecutive
+    // rows of one source share one TMA box of 16, 32, 48 or 64 rows.
+    const int n_st = P.n_stages;
+    auto stage_at = [&](int64_t v) -> const AttnStage* {
+      const int lv = static_cast<int>(v / n_st);
+      return P.stages + (v - static_cast<int64_t>(lv) * n_st);
+    };
+    int64_t u = u_begin;
+    int4 cw = make_int4(0, 0, 0, 0);
+    if (lane <= kTcStagesPerTile && u + lane < u_end) cw = __ldg(reinterpret_cast<const int4*>(stage_at(u + lane)));
+    int i = 0;
+    int prev_layer = -1, prev_key = -1;
+    int ent_delta[NE];
+    uint32_t ent_valid = 0;
+#pragma unroll
+    for (int e = 0; e < NE; ++e) ent_delta[e] = 0;
+    bool failed = false;
+    int issued = 0;
+    while (u < u_end) {
+      const int rt = i & 1;
+      AttnTok tk{0, 0};  // first row of this lane's stage
+      if (lane < kTcStagesPerTile && u + lane < u_end) tk = P.toks[cw.x];
+      // the tile is formed (registers only) while its slot drains
+      const int layer = static_cast<int>(u / n_st);
+      const int j = static_cast<int>(u - static_cast<int64_t>(layer) * n_st);
+      TcTile t{};
+      const int key = __shfl_sync(0xffffffffu, cw.z, 0);
+      const bool key_change = layer != prev_layer || key != prev_key;
+      if (key_change) ent_valid = 0;
+      uint32_t used = 0, fresh = 0;
+      int ns = 0;
+#pragma unroll
+      for (int k = 0; k < kTcStagesPerTile; ++k) {
+        const int c_delta = __shfl_sync(0xffffffffu, cw.y, k);
+        const int c_key = __shfl_sync(0xffffffffu, cw.z, k), c_nw = __shfl_sync(0xffffffffu, cw.w, k);
+        if (ns != k) continue;  // the tile already ended
+        if (k > 0 && (j + k >= n_st || u + k >= u_end || c_key != key)) continue;
+        int e = -1;
+#pragma unroll
+        for (int x = 0; x < NE; ++x)
+          if (((ent_valid >> x) & 1u) && ent_delta[x] == c_delta) e = x;
+        if (e < 0) {  // a free entry: not valid, else any this tile does not use
+#pragma unroll
+          for (int x = NE - 1; x >= 0; --x)
+            if (!((used >> x) & 1u) && !((ent_valid >> x) & 1u)) e = x;
+          if (e < 0) {
+#pragma unroll
+            for (int x = NE - 1; x >= 0; --x)
+              if (!((used >> x) & 1u)) e = x;
+          }
+          if (e < 0) continue;  // more distinct deltas than entries: the tile ends here
+          ent_delta[e] = c_delta;
+          ent_valid |= 1u << e;
+          fresh |= 1u << e;
+        }
+        used |= 1u << e;
+        t.n_tok[k] = c_nw & 0xffff;
+        t.sink[k] = static_cast<int>(static_cast<uint32_t>(c_nw) >> 16);
+        t.entry[k] = e;
+        ++ns;
+      }
+      t.ns = ns;
+      t.layer = layer;
+      t.key = key;
+      t.fresh = static_cast<int>(fresh);
+#pragma unroll
+      for (int e = 0; e < NE; ++e) t.ent_delta[e] = ent_delta[e];
+      t.flags = key_change ? kTcFirst : 0;
+      const int64_t un = u + ns;
+      const int next_key = __shfl_sync(0xffffffffu, cw.z, ns);  // candidate ns starts the next tile
+      if (un >= u_end) {
+        t.flags |= kTcLast | kTcEnd;
+      } else if (j + ns >= n_st || next_key != key) {
+        t.flags |= kTcLast;
+      }
+      // the slot's previous tile (i - 2) must be done before its metadata and rows are replaced
+      if (i >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&empty[rt], ((i >> 1) - 1) & 1, abort_flag))) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        tiles[rt] = t;
+        mbar_arrive(&meta_ready[rt]);
+        mbar_arrive_expect_tx(&full[rt], static_cast<uint32_t>(ns) * kTcStageTx);
+      }
+      __syncwarp();
+      // stage k continues stage k - 1's box when that stage is full and its rows go on
+      const int prow = __shfl_up_sync(0xffffffffu, tk.row, 1);
+      const int pflags = __shfl_up_sync(0xffffffffu, tk.flags, 1);
+      const int pn = __shfl_up_sync(0xffffffffu, cw.w & 0xffff, 1);
+      const bool cont = lane > 0 && lane < ns && pn == 16 && pflags == tk.flags && tk.row == prow + 16;
+      const uint32_t cmask = __ballot_sync(0xffffffffu, cont);
+      const bool leader = lane < ns && !cont;
+      const uint32_t lmask = __ballot_sync(0xffffffffu, leader);
+      const int ngroups = __popc(lmask);
+      const int my_len = leader ? __ffs(~(cmask >> (lane + 1))) : 0;  // this stage and the ones continuing it
+      const int z = P.layer_begin + layer;
+      // one (box, plane) copy per lane: lane q takes copy q and q + 32 of the 9 per box
+#pragma unroll
+      for (int round = 0; round < 2; ++round) {
+        const int q = lane + 32 * round;
+        const int g = q / kTcPlanes, pl = q - g * kTcPlanes;
+        uint32_t m = lmask;
+        for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
+        const int src = m ? __ffs(m) - 1 : 0;
+        const int row = __shfl_sync(0xffffffffu, tk.row, src), fl = __shfl_sync(0xffffffffu, tk.flags, src);
+        const int len = __shfl_sync(0xffffffffu, my_len, src);
+        if (g < ngroups) {
+          const CUtensorMap* map = (fl & kAttnFromCache) ? &maps.cache[len - 1] : &maps.pool[len - 1];
+          tma_load_3d(base_u32 + L::kRing + rt * kTcTileBytes + src * kTcStageBytes + pl * kTcPlaneBytes, map,
+                      64 * pl, row, z, &full[rt]);
+        }
+      }
+      issued = i + 1;
+      cw = make_int4(0, 0, 0, 0);
+      if (lane <= kTcStagesPerTile && un + lane < u_end) cw = __ldg(reinterpret_cast<const int4*>(stage_at(un + lane)));
+      prev_layer = layer;
+      prev_key = key;
+      u = un;
+      ++i;
+    }
+    if (failed) {
+      if (lane == 0) fail();
+      // wait (bounded) for the copies of the last two tiles issued
+      if (lane == 0)
+        for (int k = (issued > 2 ? issued - 2 : 0); k < issued; ++k) mbar_wait_bounded(&full[k & 1], (k >> 1) & 1);
+    }
+  } else if (warp == kTcQuery && has_work) {
+    // --------------------------------------------------------------- query
+    // Writes each tile's query operands: q_nope on a key change, and for each
+    // fresh delta entry R(-delta) q_rope as bf16 hi and lo rows; the previous
+    // tile's score product must be done reading them.
+    float qa[HC], qb[HC];  // this lane's rope pair of every head (lane f: frequency f)
+#pragma unroll
+    for (int h = 0; h < HC; ++h) qa[h] = qb[h] = 0.0f;
+    const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
+    for (int i = 0;; ++i) {
+      const int rt = i & 1;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&meta_ready[rt], (i >> 1) & 1, abort_flag))) {
+        if (lane == 0) fail();
+        break;
+      }
+      const TcTile t = tiles[rt];
+      const bool key_change = (t.flags & kTcFirst) != 0;
+      if (key_change || t.fresh) {
+        if (i >= 1 && !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag))) {
+          if (lane == 0) fail();
+          break;
+        }
+        if (key_change) {
+          const int req = t.key / P.head_groups, hg = t.key - req * P.head_groups;
+          const uint16_t* qh = P.q + ((static_cast<int64_t>(t.layer) * P.n_req + req) * P.num_q_heads + hg * HC) *
+                                         static_cast<int64_t>(kMlaRowDims);
+          for (int c = lane; c < HC * 64; c += 32) {
+            const int h = c >> 6, ch = c & 63;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + h * kMlaRowDims) + ch);
+            *reinterpret_cast<uint4*>(smem + L::kQn + (ch >> 3) * L::kQnPlane + sw128(h, (ch & 7) * 8)) = v;
+          }
+#pragma unroll
+          for (int h = 0; h < HC; ++h) {
+            qa[h] = __uint_as_float(static_cast<uint32_t>(__ldg(qh + h * kMlaRowDims + kMlaLatentDims + ia)) << 16);
+            qb[h] = __uint_as_float(static_cast<uint32_t>(__ldg(qh + h * kMlaRowDims + kMlaLatentDims + ib)) << 16);
+          }
+        }
+        // lane f rotates frequency f of every head: pairs (2f, 2f + 1) interleaved, (f, f + 32) neox
+        uint8_t* rp = smem + L::kRope;
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+          if (!((t.fresh >> e) & 1)) continue;
+          float cs = 1.0f, sn = 0.0f;
+          if (t.ent_delta[e] != 0) shift_cossin(t.ent_delta[e], __ldg(P.freq + lane), cs, sn);
+#pragma unroll
+          for (int h = 0; h < HC; ++h) {
+            __nv_bfloat16 ah, al, bh, bl;
+            split_bf16(qa[h] * cs + qb[h] * sn, ah, al);
+            split_bf16(qb[h] * cs - qa[h] * sn, bh, bl);
+            const int rh = e * 2 * HC + h, rl = rh + HC;
+            if (NEOX) {
+              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ia)) = ah;
+              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ib)) = bh;
+              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rl, ia)) = al;
+              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rl, ib)) = bl;
+            } else {  // (2f, 2f + 1) are adjacent: one 4-byte store per part
+              *reinterpret_cast<__nv_bfloat162*>(rp + sw128(rh, ia)) = __halves2bfloat162(ah, bh);
+              *reinterpret_cast<__nv_bfloat162*>(rp + sw128(rl, ia)) = __halves2bfloat162(al, bl);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rope_full[rt]);
+      if (t.flags & kTcEnd) break;
+    }
+  } else if ((warp == kTcMma || warp == kTcMma2 || warp == kTcPv) && has_work) {
+    // --------------------------------------------------- MMA issuers
+    if (lane == 0) {
+      const uint32_t ring = base_u32 + L::kRing;
+      // A descriptor is affine in its start address (start / 16 sits in the
+      // low bits, and no start here reaches 256 KB), so each product builds
+      // its base descriptors once and steps them by constants.
+      if (warp == kTcMma || warp == kTcMma2) {
+        // S of tile i once its rows and query operands are in and its TMEM
+        // buffer is free (the softmax of tile i - 2 has written P, so it is
+        // done reading that buffer).  With two issuers the first takes the
+        // even latent k-steps and the rope plane, the second the odd k-steps;
+        // each writes its own partial sums (k-step mod NP).
+        const int par = warp == kTcMma ? 0 : 1;
+        const uint64_t dq = sdesc(base_u32 + L::kQn, 16, 1024), dr = sdesc(base_u32 + L::kRope, 16, 1024);
+        for (int i = 0;; ++i) {
+          const int rt = i & 1;
+          if (!wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag) ||
+              !wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag) ||
+              (i >= 2 && !wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag))) {
+            fail();
+            break;
+          }
+          const int flags = tiles[rt].flags;
+          tc_fence_after();
+          const uint64_t da = sdesc(ring + rt * kTcTileBytes, 16, 1024);
+          const uint32_t d = tmem + rt * kTcSCols;
+#pragma unroll
+          for (int k2 = 0; k2 < 32 / kSI; ++k2) {
+            const int ks = kSI * k2 + par;
+            tc_mma(d + (ks % NP) * HC, da + (((ks >> 2) * kTcPlaneBytes + (ks & 3) * 32) >> 4),
+                   dq + (((ks >> 2) * L::kQnPlane + (ks & 3) * 32) >> 4), kIdS, ks >= NP);
+          }
+          if (par == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);
+          }
+          tc_commit(&s_full[rt]);
+          if (flags & kTcEnd) break;
+        }
+        tc_commit(&done[par]);
+        mbar_wait_bounded(&done[par], 0);
+      } else {
+        // O^T += V^T P^T of tile i once its P is written; its metadata stays
+        // in the slot until this product ends
+        const uint32_t pt = base_u32 + L::kPt;
+        for (int i = 0;; ++i) {
+          const int rt = i & 1;
+          if (!wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag)) {
+            fail();
+            break;
+          }
+          const TcTile t = tiles[rt];
+          tc_fence_after();
+          const uint64_t dv = sdesc(ring + rt * kTcTileBytes, kTcPlaneBytes, 1024);
+          const uint64_t dp = sdesc(pt + rt * L::kPtBytes, 16, 1024);
+          const bool first = (t.flags & kTcFirst) != 0;
+          // the four latent M-tiles are independent accumulators: innermost
+#pragma unroll
+          for (int w = 0; w < kTcStagesPerTile; ++w) {
+            if (w >= t.ns) break;
+#pragma unroll
+            for (int part = 0; part < kPvParts; ++part) {
+              const uint64_t bd = dp + ((part * 32 * 128 + w * 32) >> 4);
+#pragma unroll
+              for (int mt = 0; mt < 4; ++mt)
+                tc_mma(tmem + kTcOCol + mt * kTcOColsPerTile, dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4),
+                       bd, kIdPV, !(first && w == 0 && part == 0));
+            }
+          }
+          tc_commit(&empty[rt]);
+          tc_commit(&pv_done[rt]);
+          if (t.flags & kTcEnd) break;
+        }
+        tc_commit(&done[2]);
+        mbar_wait_bounded(&done[2], 0);
+      }
+    }
+  } else if (warp < kTcSoftmaxWarps && has_work) {
+    // ------------------------------------------------------------ softmax
+    // Warp (w, half): stage w's 16 positions (TMEM lanes 32w .. 32w + 15 of
+    // the M = 64 scores), heads [h0, h0 + HH); O^T lanes 32w .. 32w + 31.
+    constexpr int HH = HC / 2;
+    const int w = warp & 3, half = warp >> 2, h0 = half * HH;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * w) << 16);
+    float* wmax = reinterpret_cast<float*>(smem + L::kWmax);
+    float* lred = reinterpret_cast<float*>(smem + L::kLred);
+    float m_run[HH], l_part[HH];
+#pragma unroll
+    for (int h = 0; h < HH; ++h) {
+      m_run[h] = -INFINITY;
+      l_part[h] = 0.0f;
+    }
+    // this warp's O^T columns of M-tile mt: both parts of P (16 heads), or the sum (32 heads)
+    auto o_load = [&](int mt, float* o) {
+      const uint32_t c = tl + kTcOCol + mt * kTcOColsPerTile + h0;
+      tmem_ld<HH>(c, o);
+      if constexpr (kPvParts == 1) tmem_ld<HH>(c + HC, o + HH);
+    };
+    auto o_store = [&](int mt, const float* o) {
+      const uint32_t c = tl + kTcOCol + mt * kTcOColsPerTile + h0;
+      tmem_st<HH>(c, o);
+      if constexpr (kPvParts == 1) tmem_st<HH>(c + HC, o + HH);
+    };
+    constexpr int kOLoad = kPvParts == 1 ? 2 * HH : HH;
+    for (int i = 0;; ++i) {
+      const int rt = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      // every softmax warp reaches each barrier reduction below, so a wait
+      // that runs out in one warp ends all eight together
+      const bool got = wait_or_abort(&full[rt], ph, abort_flag) && wait_or_abort(&s_full[rt], ph, abort_flag);
+      if (softmax_bar_or(!got)) {
+        if (lane == 0 && !got) fail();
+        break;
+      }
+      tc_fence_after();
+      const TcTile t = tiles[rt];
+      if (t.flags & kTcFirst) {
+#pragma unroll
+        for (int h = 0; h < HH; ++h) {
+          m_run[h] = -INFINITY;
+          l_part[h] = 0.0f;
+        }
+      }
+      const bool present = w < t.ns;
+      const int n_tok = present ? t.n_tok[w] : 0;
+      const int entry = present ? t.entry[w] : 0;
+      float sp[NP][HH], rh[HH], rl[HH];
+      const uint32_t sc = tl + rt * kTcSCols + h0;
+      tmem_ld<HH>(sc + kRopeCol + entry * 2 * HC, rh);
+      tmem_ld<HH>(sc + kRopeCol + entry * 2 * HC + HC, rl);
+#pragma unroll
+      for (int pp = 0; pp < NP; ++pp) tmem_ld<HH>(sc + pp * HC, sp[pp]);
+      tmem_wait_ld();
+      const bool live = lane < n_tok;
+      const float bias = (live && ((t.sink[w] >> lane) & 1)) ? P.sink_log2 : 0.0f;
+      float s[HH];
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < HH; ++h) {
+        float v = sp[0][h];
+#pragma unroll
+        for (int pp = 1; pp < NP; ++pp) v += sp[pp][h];
+        s[h] = live ? ((v + rh[h]) + rl[h]) * P.scale_log2 + bias : -INFINITY;
+        need |= s[h] > m_run[h] + kTcLazy;
+      }
+      // does any position raise a head's running max?
+      if (softmax_bar_or(need)) {
+        float* wm = wmax + (rt * 4 + w) * HC + h0;
+#pragma unroll
+        for (int h = 0; h < HH; ++h) {
+          float v = s[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          if (lane == 0) wm[h] = v;
+        }
+        softmax_bar_or(false);
+        const volatile float* vm = wmax + rt * 4 * HC + h0;
+        float alpha[HH];
+        bool rescale = false;
+#pragma unroll
+        for (int h = 0; h < HH; ++h) {
+          const float tm = fmaxf(fmaxf(vm[h], vm[HC + h]), fmaxf(vm[2 * HC + h], vm[3 * HC + h]));
+          const float mn = fmaxf(m_run[h], tm);
+          alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m_run[h] - mn);
+          rescale |= alpha[h] != 1.0f;
+          m_run[h] = mn;
+          l_part[h] *= alpha[h];
+        }
+        // every warp takes the same branch: the barrier below is reached by all or none
+        const bool rescale_any = softmax_bar_or(rescale);
+        if (!(t.flags & kTcFirst) && rescale_any) {
+          // O holds this key's earlier tiles: wait for the last product into it, then scale in place
+          const bool landed = wait_or_abort(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag);
+          if (softmax_bar_or(!landed)) {
+            if (lane == 0 && !landed) fail();
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            float o[kOLoad];
+            o_load(mt, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < kOLoad; ++c) o[c] *= alpha[c % HH];
+            o_store(mt, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      float p[HH];
+#pragma unroll
+      for (int h = 0; h < HH; ++h) {
+        p[h] = live ? exp2f(s[h] - m_run[h]) : 0.0f;
+        l_part[h] += p[h];
+      }
+      if (present) {
+        uint8_t* ring_t = smem + L::kRing + rt * kTcTileBytes;
+        // rows past the stage's tokens may hold anything: zero their values (planes
+        // 4 half .. 4 half + 3) so that P = 0 meets finite V
+        const int dead = 16 - n_tok;
+        for (int c = lane; c < dead * 32; c += 32) {
+          const int r = 16 * w + n_tok + (c >> 5), pl = 4 * half + ((c >> 3) & 3), ch = c & 7;
+          *reinterpret_cast<uint4*>(ring_t + pl * kTcPlaneBytes + (r >> 3) * 1024 + (r & 7) * 128 +
+                                    ((ch ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        if (lane < 16) {
+          uint8_t* ptb = smem + L::kPt + rt * L::kPtBytes;
+          const int col = 16 * w + lane;
+#pragma unroll
+          for (int h = 0; h < HH; ++h) {
+            __nv_bfloat16 hi, lo;
+            split_bf16(p[h], hi, lo);
+            *reinterpret_cast<__nv_bfloat16*>(ptb + sw128(h0 + h, col)) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(ptb + sw128(HC + h0 + h, col)) = lo;
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[rt]);
+
+      if (t.flags & kTcLast) {
+        // the key's last tile in this CTA: write its record (O, m, l)
+        const bool landed = wait_or_abort(&pv_done[rt], ph, abort_flag);
+        if (softmax_bar_or(!landed)) {
+          if (lane == 0 && !landed) fail();
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < HH; ++h) {
+          float v = l_part[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) lred[w * HC + h0 + h] = v;
+        }
+        softmax_bar_or(false);
+        const AttnKey kk = P.keys[static_cast<int64_t>(t.layer) * P.n_keys + t.key];
+        const int blk_floats = attn_block_floats(HC, kMlaLatentDims);
+        float* blk =
+            P.records + static_cast<int64_t>(kk.rec_base + (static_cast<int>(blockIdx.x) - kk.first_cta)) * blk_floats;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          float o[kOLoad];
+          o_load(mt, o);
+          tmem_wait_ld();
+          const int d = mt * 128 + 32 * w + lane;
+#pragma unroll
+          for (int h = 0; h < HH; ++h)
+            blk[(h0 + h) * kMlaLatentDims + d] = kPvParts == 1 ? o[h] + o[HH + h] : o[h];
+        }
+        if (w == 0 && lane < HH) {
+          float mv = 0.0f;
+#pragma unroll
+          for (int h = 0; h < HH; ++h)
+            if (lane == h) mv = m_run[h];
+          const volatile float* vl = lred + h0;
+          blk[HC * kMlaLatentDims + h0 + lane] = mv;
+          blk[HC * kMlaLatentDims + HC + h0 + lane] =
+              (vl[lane] + vl[HC + lane]) + (vl[2 * HC + lane] + vl[3 * HC + lane]);
+        }
+        tc_fence_before();
+      }
+      if (t.flags & kTcEnd) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMma) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols) : "memory");
+  }
+}
+
+template <int PAIRING, int HC>
+cudaError_t launch_tc(const AttnParams& p, const TcMaps& maps, int grid, size_t smem, cudaStream_t s) {
+  auto kern = k_attend_mla_tc<PAIRING, HC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, tc_threads(HC), smem, s>>>(p, maps);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_attend_merge_mla(p, HC, s);
+}
+
+}  // namespace
+
+bool attend_mla_tc_config(int hc, size_t* smem_bytes) {
+  if (hc == 16) {
+    *smem_bytes = TcLayout<16>::kAlloc;
+  } else if (hc == 32) {
+    *smem_bytes = TcLayout<32>::kAlloc;
+  } else {
+    return false;
+  }
+  return *smem_bytes <= 227 * 1024;
+}
+
+cudaError_t launch_attend_mla_tc(const AttnParams& p, const TcMaps& maps, int pairing, int hc, int grid,
+                                 size_t smem_bytes, cudaStream_t s) {
+  if (p.n_units <= 0 || grid <= 0) return cudaSuccess;
+  if (pairing == kNeox) {
+    if (hc == 16) return launch_tc<kNeox, 16>(p, maps, grid, smem_bytes, s);
+    if (hc == 32) return launch_tc<kNeox, 32>(p, maps, grid, smem_bytes, s);
+  } else {
+    if (hc == 16) return launch_tc<kInterleaved, 16>(p, maps, grid, smem_bytes, s);
+    if (hc == 32) return launch_tc<kInterleaved, 32>(p, maps, grid, smem_bytes, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pic

@@ -173,6 +173,9 @@ struct pic_ctx {
   bool tma_inplace = false;
   pic::TmaConfig tma_stitch_cfg{};
   pic::TmaConfig tma_inplace_cfg{};
+  // MLA decode attention on tcgen05 tensor cores (16 or 32 heads per CTA);
+  // PIC_ATTEND_KERNEL=mma at pic_create selects the warp-level mma kernel
+  bool attend_tc = false;
   StagingSlot staging[kStagingSlots];
   int staging_next = 0;
   int staging_device = -1;
@@ -683,6 +686,7 @@ void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req
                  const AttnHeads& heads, AttnPlan* out) {
   const int32_t bs = ctx->model.block_size;
   const int32_t ST = pic::kAttnStageTokens;
+  const bool mla = ctx->model.kind == PIC_KIND_MLA;
   out->heads_per_cta = heads.hb;
   out->head_groups = heads.head_groups;
   out->n_keys = n_req * out->head_groups;
@@ -719,7 +723,9 @@ void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req
       st.tok_off = tok_off + p;
       st.delta = deltas[p];
       int32_t n = 0;
-      while (p + n < T && n < ST && deltas[p + n] == st.delta) {
+      // MLA stages also read consecutive rows of one source (one TMA box)
+      while (p + n < T && n < ST && deltas[p + n] == st.delta &&
+             (!mla || n == 0 || (tk[p + n].flags == tk[p].flags && tk[p + n].row == tk[p].row + n))) {
         if (sink[p + n]) st.sink_mask |= static_cast<uint16_t>(1u << n);
         ++n;
       }
@@ -740,6 +746,39 @@ void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req
 struct AttnLayout {
   size_t freq_off, stages_off, toks_off, keys_off, records_off, total;
 };
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
+// driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// A view of MLA rows as [layers][rows][576] bf16, read in boxes of box_rows
+// rows x 64 dims with 128-byte swizzle; rows past `rows` read as zeros.
+bool encode_mla_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t layers, int64_t layer_stride,
+                     uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc || !base || rows <= 0 || layers <= 0 || (layer_stride & 15) || rows > (int64_t{1} << 32)) return false;
+  if (layers > 1 && layer_stride < rows * 1152) return false;
+  const cuuint64_t dims[3] = {576, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(layers)};
+  const cuuint64_t strides[2] = {1152, static_cast<cuuint64_t>(layers > 1 ? layer_stride : rows * 1152)};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 AttnLayout attend_layout(const pic_ctx* ctx, size_t n_stages, size_t n_toks, size_t n_key_entries,
                          size_t n_records, const AttnHeads& heads) {
@@ -882,6 +921,8 @@ pic_status pic_create(const pic_model_desc* m, int32_t num_cache_blocks, pic_ctx
     if (bulk_all && m->kind == PIC_KIND_GQA) {
       ctx->tma_inplace = tma_config_for(row, m->block_size, 1, tile_bytes, ctx->tma_inplace_cfg);
     }
+    const char* ak = std::getenv("PIC_ATTEND_KERNEL");
+    ctx->attend_tc = m->kind == PIC_KIND_MLA && !(ak && std::strcmp(ak, "mma") == 0);
   }
   ctx->model.inv_freq = nullptr;
   ctx->theta = theta;
@@ -1361,7 +1402,8 @@ pic_status pic_debug_stall_next_launch(pic_ctx* ctx, int32_t stall_tile, uint32_
 }
 
 int32_t pic_kernel_variant(const pic_ctx* ctx, int32_t mode) {
-  if (!ctx || (mode != 0 && mode != 1)) return -1;
+  if (!ctx || mode < 0 || mode > 2) return -1;
+  if (mode == 2) return ctx->attend_tc ? PIC_VARIANT_TENSOR_CORE_TMEM : PIC_VARIANT_WARP_MMA;
   const bool bulk = mode == 0 ? ctx->tma_stitch : ctx->tma_inplace;
   return bulk ? PIC_VARIANT_BULK_PIPELINE : PIC_VARIANT_REGISTERS;
 }
@@ -1449,14 +1491,31 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
     return fail(ctx, PIC_ERR_ALIGNMENT, "q, out, pools, caches, strides and workspace must be 16-byte aligned");
   for (int32_t r = 0; r < n_req; ++r)
     if (plans[r]->total_tokens == 0) return fail(ctx, PIC_ERR_RANGE, "plans[%d] has no context to attend", r);
-  int ring = 0;
-  size_t smem = 0;
-  const bool fits = mla ? pic::attend_mla_config(heads.mla_ng, &ring, &smem)
-                        : pic::attend_config(m.head_dim, heads.group, heads.hb, &ring, &smem);
-  if (!fits) return fail(ctx, PIC_ERR_UNSUPPORTED, "attention stages do not fit in shared memory");
-
   AttnPlan plan;
   attend_plan(ctx, plans, n_req, source, heads, &plan);
+
+  // MLA on tcgen05 when the pool and cache can be described as TMA tensors
+  int ring = 0;
+  size_t smem = 0;
+  pic::TcMaps maps;
+  bool tc = mla && ctx->attend_tc && pic::attend_mla_tc_config(heads.group, &smem);
+  if (tc) {
+    // the pool view spans the rows the plan reads; the cache view every cache row
+    int64_t pool_rows = 0;
+    for (const pic::AttnTok& t : plan.toks)
+      if (!(t.flags & pic::kAttnFromCache)) pool_rows = std::max<int64_t>(pool_rows, int64_t{t.row} + 1);
+    const int64_t layers = static_cast<int64_t>(layer_begin) + num_layers;
+    for (int g = 0; g < 4 && tc; ++g) {
+      const uint32_t box = 16u * static_cast<uint32_t>(g + 1);
+      tc = encode_mla_rows(&maps.cache[g], k_cache, static_cast<int64_t>(ctx->num_cache_blocks) * m.block_size,
+                           layers, cache_ls, box);
+      if (tc && pool_rows > 0) tc = encode_mla_rows(&maps.pool[g], k_pool, pool_rows, layers, pool_ls, box);
+      if (tc && pool_rows == 0) maps.pool[g] = maps.cache[g];  // nothing is read from the pool
+    }
+  }
+  const bool fits = tc || (mla ? pic::attend_mla_config(heads.mla_ng, &ring, &smem)
+                               : pic::attend_config(m.head_dim, heads.group, heads.hb, &ring, &smem));
+  if (!fits) return fail(ctx, PIC_ERR_UNSUPPORTED, "attention stages do not fit in shared memory");
   const int64_t units = static_cast<int64_t>(plan.stages.size()) * num_layers;
   if (units > INT32_MAX || static_cast<int64_t>(plan.toks.size()) > INT32_MAX)
     return fail(ctx, PIC_ERR_CAPACITY, "attention batch too large");
@@ -1468,7 +1527,8 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   for (int i = 0; i < 4; ++i)
     if (bufs[i] && residency(bufs[i]) != 0)
       return fail(ctx, PIC_ERR_UNSUPPORTED, "decode attention reads pools and caches from device memory only");
-  const int per_sm = mla ? pic::attend_mla_ctas_per_sm(m.pairing, heads.mla_ng, smem)
+  const int per_sm = tc ? 1
+                   : mla ? pic::attend_mla_ctas_per_sm(m.pairing, heads.mla_ng, smem)
                          : pic::attend_ctas_per_sm(m.pairing, m.head_dim, heads.group, heads.hb, smem);
   if (per_sm <= 0) return fail(ctx, PIC_ERR_CUDA, "attention kernel does not fit on an SM");
   const int64_t ctas = std::min<int64_t>({units, static_cast<int64_t>(di.sm_count) * per_sm, pic::kAttnMaxCtas});
@@ -1523,8 +1583,13 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   p.out = out;
   p.lse = lse;
   p.status = &reinterpret_cast<WsHeader*>(ws)->status;
-  const cudaError_t e = mla ? pic::launch_attend_mla(p, m.pairing, heads.mla_ng, static_cast<int>(ctas), smem, s)
-                            : pic::launch_attend(p, m.pairing, m.head_dim, heads.group, static_cast<int>(ctas), smem, s);
+  cudaError_t e;
+  if (tc) {
+    e = pic::launch_attend_mla_tc(p, maps, m.pairing, heads.group, static_cast<int>(ctas), smem, s);
+  } else {
+    e = mla ? pic::launch_attend_mla(p, m.pairing, heads.mla_ng, static_cast<int>(ctas), smem, s)
+            : pic::launch_attend(p, m.pairing, m.head_dim, heads.group, static_cast<int>(ctas), smem, s);
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "attention launch");
   return ok(ctx);
 }

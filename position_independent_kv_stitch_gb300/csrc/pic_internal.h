@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "pic.h"
@@ -187,6 +188,21 @@ bool attend_mla_config(int ng, int* ring, size_t* smem_bytes);
 int attend_mla_ctas_per_sm(int pairing, int ng, size_t smem_bytes);
 cudaError_t launch_attend_mla(const AttnParams& p, int pairing, int ng, int grid, size_t smem_bytes,
                               cudaStream_t stream);
+// Combines the per-CTA records of an MLA attention into out / lse.
+cudaError_t launch_attend_merge_mla(const AttnParams& p, int heads_per_record, cudaStream_t stream);
+
+// MLA decode attention on tcgen05 tensor cores with TMA tensor loads (same
+// plan and records; hc = 16 or 32 query heads per CTA).  The maps view the
+// pool and the paged cache as [layers][rows][576] bf16 with 128-byte swizzle
+// and a box of 64 dims x 16 (g + 1) rows for map g; every stage of the plan
+// reads consecutive rows of one of them.
+struct TcMaps {
+  CUtensorMap pool[4];
+  CUtensorMap cache[4];
+};
+bool attend_mla_tc_config(int hc, size_t* smem_bytes);
+cudaError_t launch_attend_mla_tc(const AttnParams& p, const TcMaps& maps, int pairing, int hc, int grid,
+                                 size_t smem_bytes, cudaStream_t stream);
 
 // Launchers; each returns the launch's cudaError_t.  `grid` is the number of
 // CTAs (persistent, grid-stride over units).

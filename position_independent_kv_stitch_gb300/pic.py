@@ -34,6 +34,7 @@ PIC_DEV_BAD_DOCS = 0x8
 PIC_DEV_CAPACITY = 0x10
 PIC_DEV_BAD_SPAN = 0x20
 PIC_VARIANT_REGISTERS, PIC_VARIANT_BULK_PIPELINE = 0, 1
+PIC_VARIANT_TENSOR_CORE_TMEM, PIC_VARIANT_WARP_MMA = 2, 3
 PIC_SEG_COPY_POOL, PIC_SEG_COPY_BLOCKS, PIC_SEG_MAPPED = 0, 1, 2
 PIC_ATTEND_FUSED, PIC_ATTEND_CACHE = 0, 1
 
@@ -564,7 +565,10 @@ def pic_debug_stall_next_launch(ctx, stall_tile: int, max_spins: int = 0):
 
 
 def pic_kernel_variant(ctx, mode: int) -> int:
-    """0 = register kernel, 1 = bulk-copy pipeline; mode 0 stitch, 1 in-place shift."""
+    """Kernel a context launches.  Modes 0 (stitch) and 1 (in-place shift):
+    PIC_VARIANT_REGISTERS or PIC_VARIANT_BULK_PIPELINE.  Mode 2 (decode
+    attention): PIC_VARIANT_TENSOR_CORE_TMEM (MLA on tcgen05) or
+    PIC_VARIANT_WARP_MMA."""
     return int(load().pic_kernel_variant(ctx, int(mode)))
 
 

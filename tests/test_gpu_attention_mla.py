@@ -4,6 +4,7 @@ k_r is rotated by its delta on the way in, the latent is used as stored and is
 the value.  Against the fp64 oracle's attention over exactly rotated rows."""
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -28,10 +29,24 @@ def _lib():
     pic.load(build_if_missing=True)
 
 
+@pytest.fixture(params=["tc", "mma"], autouse=True)
+def attend_kernel(request, monkeypatch):
+    """Every case runs on both MLA attention kernels, chosen at pic_create:
+    tcgen05 with TMEM accumulators (the default) and warp-level mma.sync."""
+    monkeypatch.setenv("PIC_ATTEND_KERNEL", request.param)
+    return request.param
+
+
+def _check_variant(ctx, kernel):
+    want = pic.PIC_VARIANT_TENSOR_CORE_TMEM if kernel == "tc" else pic.PIC_VARIANT_WARP_MMA
+    assert pic.pic_kernel_variant(ctx, 2) == want
+
+
 def _setup(pairing, L, seed, rep=1):
     bs, nb = 16, 200 + 120 * (rep - 1)
     m = W.Model("attn-mla", "mla", L, 1, ROW, ROPE, LATENT, pairing, 1e4, bs)
     ctx = pic.create_from_spec(pic.model_spec_from(m), nb)
+    _check_variant(ctx, os.environ["PIC_ATTEND_KERNEL"])
     offs = [0]
     for n in _POOL_LENS[:-1]:
         offs.append(offs[-1] + n)
@@ -190,6 +205,7 @@ def test_deepseek_full_launch_sampled_layers():
     wl = W.deepseek_v3_mla()
     st = Stitched(wl).run()
     try:
+        _check_variant(st.ctx, os.environ["PIC_ATTEND_KERNEL"])
         m = wl.model
         H, L = 16, m.num_layers
         g = torch.Generator(device=DEV)
