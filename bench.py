@@ -814,9 +814,11 @@ def main():
         kname = "k_tma_pipeline<" + ("stitch K+V" if wl.model.kind == "gqa" else "stitch MLA rows") \
             + ">" if args.mode != "inplace" else "k_tma_pipeline<in place>"
     else:
+        tc = pic.pic_kernel_variant(rig.ctx, 2) == pic.PIC_VARIANT_TENSOR_CORE_TMEM
         kname = {"stitch": "k_stitch_mla" if wl.model.kind == "mla" else "k_rotate_rows<stitch>",
                  "mapped": "k_rotate_rows<stitch, mapped chunks in place>",
-                 "attend": ("k_attend_mla" if wl.model.kind == "mla" else "k_attend")
+                 "attend": ("k_attend_mla_tc (tcgen05, TMEM, TMA tensor loads)" if tc
+                            else "k_attend_mla" if wl.model.kind == "mla" else "k_attend")
                  + " + k_attend_merge (fused delta-rotation)",
                  "attend_cache": "stitch, then decode attention over the cache",
                  "inplace": "k_rotate_rows<in place>"}[args.mode]

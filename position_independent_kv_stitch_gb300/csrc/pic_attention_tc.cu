@@ -65,18 +65,23 @@ constexpr int kTcPlanes = 9;                               // 8 latent planes + 
 constexpr int kTcPlaneBytes = 64 * 128;                    // 64 rows x 64 dims x bf16
 constexpr int kTcTileBytes = kTcPlanes * kTcPlaneBytes;    // 73,728
 constexpr int kTcStageBytes = 16 * 128;                    // one stage's rows in one plane
-constexpr uint32_t kTcStageTx = kTcStageBytes * kTcPlanes; // bytes a stage's copies deliver
 constexpr float kTcLazy = 8.0f;
 // warps 0-7 softmax (warp w: TMEM lane quadrant w % 4, heads of half w / 4),
-// then the producer, the score-product issuer (it also holds the TMEM
+// then a producer, the score-product issuer (it also holds the TMEM
 // allocation), the query warp, the value-product issuer and, for 16 heads, a
-// second score-product issuer.  One thread issues a small tcgen05.mma about
-// every 70 cycles whatever its shape, so the products are spread over
-// threads; 32 heads need the registers the extra warp would take.
+// second score-product issuer, two more producers and a second value-product
+// issuer.  One thread issues a small tcgen05.mma about every 70 cycles
+// whatever its shape, and one warp issues TMA copies one lane after another
+// (~35 ns each), so both are spread over warps; 32 heads need the registers
+// the extra warps would take.
 constexpr int kTcSoftmaxWarps = 8;
-constexpr int kTcProducer = 8, kTcMma = 9, kTcQuery = 10, kTcPv = 11, kTcMma2 = 12;
+constexpr int kTcProducer = 8, kTcMma = 9, kTcQuery = 10, kTcPv = 11, kTcMma2 = 12, kTcProducer2 = 13, kTcPv2 = 15;
 __host__ __device__ constexpr int tc_score_issuers(int hc) { return hc == 16 ? 2 : 1; }
-__host__ __device__ constexpr int tc_threads(int hc) { return 32 * (11 + tc_score_issuers(hc)); }
+__host__ __device__ constexpr int tc_producers(int hc) { return hc == 16 ? 3 : 1; }
+__host__ __device__ constexpr int tc_value_issuers(int hc) { return hc == 16 ? 2 : 1; }
+__host__ __device__ constexpr int tc_threads(int hc) {
+  return 32 * (9 + tc_score_issuers(hc) + tc_producers(hc) + tc_value_issuers(hc));
+}
 constexpr uint32_t kTcCols = 512;                          // TMEM columns held by the CTA
 // TMEM columns: two score buffers of kTcSCols (the latent score as partial
 // sums over interleaved k-steps, NP x HC columns, then the rope columns),
@@ -115,8 +120,8 @@ struct TcLayout {
   static constexpr int kLred = kWmax + 2 * 4 * HC * 4;          // float [4][HC]
   static constexpr int kTiles = kLred + 4 * HC * 4;             // TcTile [2]
   static constexpr int kBars = kTiles + 2 * static_cast<int>(sizeof(TcTile));
-  // full[2] empty[2] meta[2] rope_full[2] s_full[2] p_full[2] pv_done[2] done[3]
-  static constexpr int kNumBars = 17;
+  // full[2] empty[2] meta[2] rope_full[2] s_full[2] p_full[2] pv_done[2] done[4]
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;                  // room to align the base
@@ -262,6 +267,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   constexpr uint32_t kIdPV = idesc(128, 32, 1);
   constexpr int kPvParts = HC == 16 ? 1 : 2;  // value products per stage and M-tile (N = 32 each)
   constexpr int kSI = tc_score_issuers(HC);
+  constexpr int kNP = tc_producers(HC);
+  constexpr int kVI = tc_value_issuers(HC);
   // the latent score accumulates in NP independent partial sums (k-steps
   // interleaved), so consecutive small products do not wait on one another
   constexpr int NP = HC == 16 ? 4 : 2;
@@ -291,15 +298,15 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&full[b], 1);
-      mbar_init(&empty[b], 1);
+      mbar_init(&full[b], kNP);  // each producer warp arrives with the bytes of its copies
+      mbar_init(&empty[b], kVI);  // every value issuer commits
       mbar_init(&meta_ready[b], 1);
       mbar_init(&rope_full[b], 1);
       mbar_init(&s_full[b], kSI);  // every score issuer commits
       mbar_init(&p_full[b], kTcSoftmaxWarps);
-      mbar_init(&pv_done[b], 1);
+      mbar_init(&pv_done[b], kVI);
     }
-    for (int b = 0; b < 3; ++b) mbar_init(&done[b], 1);
+    for (int b = 0; b < 4; ++b) mbar_init(&done[b], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -319,7 +326,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   };
   const bool has_work = u_begin < u_end;
 
-  if (warp == kTcProducer && has_work) {
+  const int prod = warp == kTcProducer ? 0 : (warp >= kTcProducer2 && warp < kTcProducer2 + kNP - 1) ? warp - kTcProducer2 + 1 : -1;
+  if (prod >= 0 && has_work) {
     // ------------------------------------------------------------ producer
     // Forms the tiles and starts their copies.  The next tile's plan stages
     // (lanes 0-4; the fifth tells whether the key goes on) are read while
@@ -403,12 +411,10 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         failed = true;
         break;
       }
-      if (lane == 0) {
+      if (prod == 0 && lane == 0) {
         tiles[rt] = t;
         mbar_arrive(&meta_ready[rt]);
-        mbar_arrive_expect_tx(&full[rt], static_cast<uint32_t>(ns) * kTcStageTx);
       }
-      __syncwarp();
       // stage k continues stage k - 1's box when that stage is full and its rows go on
       const int prow = __shfl_up_sync(0xffffffffu, tk.row, 1);
       const int pflags = __shfl_up_sync(0xffffffffu, tk.flags, 1);
@@ -420,20 +426,54 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const int ngroups = __popc(lmask);
       const int my_len = leader ? __ffs(~(cmask >> (lane + 1))) : 0;  // this stage and the ones continuing it
       const int z = P.layer_begin + layer;
-      // one (box, plane) copy per lane: lane q takes copy q and q + 32 of the 9 per box
+      if constexpr (kNP == 1) {
+        // one producer: it announces the whole tile, then lane q issues copies q and q + 32
+        if (lane == 0) mbar_arrive_expect_tx(&full[rt], static_cast<uint32_t>(ns) * kTcStageBytes * kTcPlanes);
+        __syncwarp();
 #pragma unroll
-      for (int round = 0; round < 2; ++round) {
-        const int q = lane + 32 * round;
-        const int g = q / kTcPlanes, pl = q - g * kTcPlanes;
-        uint32_t m = lmask;
-        for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
-        const int src = m ? __ffs(m) - 1 : 0;
-        const int row = __shfl_sync(0xffffffffu, tk.row, src), fl = __shfl_sync(0xffffffffu, tk.flags, src);
-        const int len = __shfl_sync(0xffffffffu, my_len, src);
-        if (g < ngroups) {
-          const CUtensorMap* map = (fl & kAttnFromCache) ? &maps.cache[len - 1] : &maps.pool[len - 1];
-          tma_load_3d(base_u32 + L::kRing + rt * kTcTileBytes + src * kTcStageBytes + pl * kTcPlaneBytes, map,
-                      64 * pl, row, z, &full[rt]);
+        for (int round = 0; round < 2; ++round) {
+          const int q = lane + 32 * round;
+          const int g = q / kTcPlanes, pl = q - g * kTcPlanes;
+          uint32_t m = lmask;
+          for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
+          const int src = m ? __ffs(m) - 1 : 0;
+          const int row = __shfl_sync(0xffffffffu, tk.row, src), fl = __shfl_sync(0xffffffffu, tk.flags, src);
+          const int len = __shfl_sync(0xffffffffu, my_len, src);
+          if (g < ngroups) {
+            const CUtensorMap* map = (fl & kAttnFromCache) ? &maps.cache[len - 1] : &maps.pool[len - 1];
+            tma_load_3d(base_u32 + L::kRing + rt * kTcTileBytes + src * kTcStageBytes + pl * kTcPlaneBytes, map,
+                        64 * pl, row, z, &full[rt]);
+          }
+        }
+      } else {
+        // copy q (box q / 9, plane q % 9; at most 36) goes to producer warp
+        // q % kNP, lane (q / kNP) % 32; this warp announces its bytes first
+        constexpr int kRounds = (4 * kTcPlanes + 32 * kNP - 1) / (32 * kNP);
+        int cp_row[kRounds], cp_fl[kRounds], cp_len[kRounds], cp_src[kRounds], cp_pl[kRounds];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+          const int q = prod + kNP * (lane + 32 * r);
+          const int g = q / kTcPlanes;
+          uint32_t m = lmask;
+          for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
+          cp_src[r] = m ? __ffs(m) - 1 : 0;
+          cp_row[r] = __shfl_sync(0xffffffffu, tk.row, cp_src[r]);
+          cp_fl[r] = __shfl_sync(0xffffffffu, tk.flags, cp_src[r]);
+          cp_len[r] = __shfl_sync(0xffffffffu, my_len, cp_src[r]);
+          cp_pl[r] = g < ngroups ? q - g * kTcPlanes : kTcPlanes;
+          bytes += cp_pl[r] < kTcPlanes ? static_cast<uint32_t>(cp_len[r]) * kTcStageBytes : 0u;
+        }
+        bytes = __reduce_add_sync(0xffffffffu, bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[rt], bytes);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+          if (cp_pl[r] < kTcPlanes) {
+            const CUtensorMap* map = (cp_fl[r] & kAttnFromCache) ? &maps.cache[cp_len[r] - 1] : &maps.pool[cp_len[r] - 1];
+            tma_load_3d(base_u32 + L::kRing + rt * kTcTileBytes + cp_src[r] * kTcStageBytes + cp_pl[r] * kTcPlaneBytes,
+                        map, 64 * cp_pl[r], cp_row[r], z, &full[rt]);
+          }
         }
       }
       issued = i + 1;
@@ -517,7 +557,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       if (lane == 0) mbar_arrive(&rope_full[rt]);
       if (t.flags & kTcEnd) break;
     }
-  } else if ((warp == kTcMma || warp == kTcMma2 || warp == kTcPv) && has_work) {
+  } else if ((warp == kTcMma || warp == kTcMma2 || warp == kTcPv || warp == kTcPv2) && has_work) {
     // --------------------------------------------------- MMA issuers
     if (lane == 0) {
       const uint32_t ring = base_u32 + L::kRing;
@@ -562,8 +602,10 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         mbar_wait_bounded(&done[par], 0);
       } else {
         // O^T += V^T P^T of tile i once its P is written; its metadata stays
-        // in the slot until this product ends
+        // in the slot until this product ends.  With two issuers each takes
+        // two of the four latent M-tiles.
         const uint32_t pt = base_u32 + L::kPt;
+        const int vi = warp == kTcPv ? 0 : 1;
         for (int i = 0;; ++i) {
           const int rt = i & 1;
           if (!wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag)) {
@@ -583,17 +625,19 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             for (int part = 0; part < kPvParts; ++part) {
               const uint64_t bd = dp + ((part * 32 * 128 + w * 32) >> 4);
 #pragma unroll
-              for (int mt = 0; mt < 4; ++mt)
+              for (int m4 = 0; m4 < 4 / kVI; ++m4) {
+                const int mt = vi * (4 / kVI) + m4;
                 tc_mma(tmem + kTcOCol + mt * kTcOColsPerTile, dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4),
                        bd, kIdPV, !(first && w == 0 && part == 0));
+              }
             }
           }
           tc_commit(&empty[rt]);
           tc_commit(&pv_done[rt]);
           if (t.flags & kTcEnd) break;
         }
-        tc_commit(&done[2]);
-        mbar_wait_bounded(&done[2], 0);
+        tc_commit(&done[2 + vi]);
+        mbar_wait_bounded(&done[2 + vi], 0);
       }
     }
   } else if (warp < kTcSoftmaxWarps && has_work) {
