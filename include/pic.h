@@ -542,18 +542,22 @@ pic_status pic_query_device_status(pic_ctx* ctx, const void* d_workspace, pic_st
                                    uint32_t* status_out);
 
 /*
- * Test hook for the failure path of the bulk-copy pipeline.  The next
- * pic_stitch on ctx that runs the bulk pipeline (pic_kernel_variant(ctx, 0) ==
- * PIC_VARIANT_BULK_PIPELINE) makes its first CTA skip the copies and the
- * barrier arrival of its tile stall_tile, and bounds every barrier wait of
- * that launch at max_spins tries (0: the library's default bound).  The wait
- * for that tile then runs out: the launch raises PIC_DEV_TIMEOUT in the
- * workspace status word, every thread of the CTA leaves after bounded waits
- * for the copies it did start, and the context stays usable.  Nothing
- * faults or hangs; the other CTAs complete their tiles.  The setting is used
- * by exactly one pic_stitch (whichever kernel it runs) and then cleared;
- * stall_tile < 0 clears it at once.  The pages have no counterpart: this
- * exists to test the library's own failure detection.
+ * Test hook for the failure paths of the kernels that wait on their own
+ * copies: the bulk-copy pipeline of pic_stitch (pic_kernel_variant(ctx, 0) ==
+ * PIC_VARIANT_BULK_PIPELINE) and the tcgen05 MLA attention of
+ * pic_attend_decode (pic_kernel_variant(ctx, 2) ==
+ * PIC_VARIANT_TENSOR_CORE_TMEM).  The next of those calls on ctx makes its
+ * first CTA skip the copies and the barrier arrival of its tile stall_tile,
+ * and bounds every barrier wait of that launch at max_spins tries (0: the
+ * library's default bound).  The wait for that tile then runs out: the
+ * launch raises PIC_DEV_TIMEOUT in the workspace status word, every thread
+ * of the CTA leaves after bounded waits for the copies and products it did
+ * start (the attention CTA also frees its tensor memory), and the context
+ * stays usable.  Nothing faults or hangs; the other CTAs complete their
+ * tiles.  The setting is used by exactly one pic_stitch or pic_attend_decode
+ * (whichever kernel it runs) and then cleared; stall_tile < 0 clears it at
+ * once.  The pages have no counterpart: this exists to test the library's
+ * own failure detection.
  */
 pic_status pic_debug_stall_next_launch(pic_ctx* ctx, int32_t stall_tile, uint32_t max_spins);
 

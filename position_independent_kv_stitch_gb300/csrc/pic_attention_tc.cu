@@ -228,8 +228,9 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 }
 
 // bounded wait that also gives up once another role has aborted
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kMaxSpins; ++i) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
+                                              uint32_t spins) {
+  for (uint32_t i = 0; i < spins; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
   }
@@ -324,6 +325,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     atomicOr(P.status, kDevTimeout);
     *abort_flag = 1;
   };
+  const uint32_t spins = P.max_spins != 0 ? P.max_spins : kMaxSpins;
   const bool has_work = u_begin < u_end;
 
   const int prod = warp == kTcProducer ? 0 : (warp >= kTcProducer2 && warp < kTcProducer2 + kNP - 1) ? warp - kTcProducer2 + 1 : -1;
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         t.flags |= kTcLast;
       }
       // the slot's previous tile (i - 2) must be done before its metadata and rows are replaced
-      if (i >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&empty[rt], ((i >> 1) - 1) & 1, abort_flag))) {
+      if (i >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&empty[rt], ((i >> 1) - 1) & 1, abort_flag, spins))) {
         failed = true;
         break;
       }
@@ -426,7 +428,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const int ngroups = __popc(lmask);
       const int my_len = leader ? __ffs(~(cmask >> (lane + 1))) : 0;  // this stage and the ones continuing it
       const int z = P.layer_begin + layer;
-      if constexpr (kNP == 1) {
+      // test hook (pic_debug_stall_next_launch): CTA 0 leaves this tile's rows
+      // unrequested, so the waits for them run out and take the failure path
+      const bool stalled = P.debug_stall != 0 && blockIdx.x == 0 && i == P.debug_stall - 1;
+      if (stalled) {
+        // no arrival, no copies
+      } else if constexpr (kNP == 1) {
         // one producer: it announces the whole tile, then lane q issues copies q and q + 32
         if (lane == 0) mbar_arrive_expect_tx(&full[rt], static_cast<uint32_t>(ns) * kTcStageBytes * kTcPlanes);
         __syncwarp();
@@ -488,7 +495,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       if (lane == 0) fail();
       // wait (bounded) for the copies of the last two tiles issued
       if (lane == 0)
-        for (int k = (issued > 2 ? issued - 2 : 0); k < issued; ++k) mbar_wait_bounded(&full[k & 1], (k >> 1) & 1);
+        for (int k = (issued > 2 ? issued - 2 : 0); k < issued; ++k) mbar_wait_bounded(&full[k & 1], (k >> 1) & 1, spins);
     }
   } else if (warp == kTcQuery && has_work) {
     // --------------------------------------------------------------- query
@@ -501,14 +508,14 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
     for (int i = 0;; ++i) {
       const int rt = i & 1;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&meta_ready[rt], (i >> 1) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(&meta_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
         if (lane == 0) fail();
         break;
       }
       const TcTile t = tiles[rt];
       const bool key_change = (t.flags & kTcFirst) != 0;
       if (key_change || t.fresh) {
-        if (i >= 1 && !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag))) {
+        if (i >= 1 && !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins))) {
           if (lane == 0) fail();
           break;
         }
@@ -574,9 +581,9 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         const uint64_t dq = sdesc(base_u32 + L::kQn, 16, 1024), dr = sdesc(base_u32 + L::kRope, 16, 1024);
         for (int i = 0;; ++i) {
           const int rt = i & 1;
-          if (!wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag) ||
-              !wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag) ||
-              (i >= 2 && !wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag))) {
+          if (!wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag, spins) ||
+              !wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins) ||
+              (i >= 2 && !wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag, spins))) {
             fail();
             break;
           }
@@ -608,7 +615,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         const int vi = warp == kTcPv ? 0 : 1;
         for (int i = 0;; ++i) {
           const int rt = i & 1;
-          if (!wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag)) {
+          if (!wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag, spins)) {
             fail();
             break;
           }
@@ -672,7 +679,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const uint32_t ph = (i >> 1) & 1;
       // every softmax warp reaches each barrier reduction below, so a wait
       // that runs out in one warp ends all eight together
-      const bool got = wait_or_abort(&full[rt], ph, abort_flag) && wait_or_abort(&s_full[rt], ph, abort_flag);
+      const bool got = wait_or_abort(&full[rt], ph, abort_flag, spins) && wait_or_abort(&s_full[rt], ph, abort_flag, spins);
       if (softmax_bar_or(!got)) {
         if (lane == 0 && !got) fail();
         break;
@@ -735,7 +742,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         const bool rescale_any = softmax_bar_or(rescale);
         if (!(t.flags & kTcFirst) && rescale_any) {
           // O holds this key's earlier tiles: wait for the last product into it, then scale in place
-          const bool landed = wait_or_abort(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag);
+          const bool landed = wait_or_abort(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins);
           if (softmax_bar_or(!landed)) {
             if (lane == 0 && !landed) fail();
             break;
@@ -788,7 +795,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
 
       if (t.flags & kTcLast) {
         // the key's last tile in this CTA: write its record (O, m, l)
-        const bool landed = wait_or_abort(&pv_done[rt], ph, abort_flag);
+        const bool landed = wait_or_abort(&pv_done[rt], ph, abort_flag, spins);
         if (softmax_bar_or(!landed)) {
           if (lane == 0 && !landed) fail();
           break;

@@ -179,7 +179,7 @@ struct pic_ctx {
   StagingSlot staging[kStagingSlots];
   int staging_next = 0;
   int staging_device = -1;
-  // pic_debug_stall_next_launch: consumed by the next pic_stitch
+  // pic_debug_stall_next_launch: consumed by the next pic_stitch or pic_attend_decode
   int32_t debug_stall = 0;   // tile + 1, 0 = off
   uint32_t debug_spins = 0;  // 0 = the default wait bound
   pic_ctx(int32_t nb) : num_cache_blocks(nb), alloc(nb) {}
@@ -1583,6 +1583,10 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   p.out = out;
   p.lse = lse;
   p.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  p.debug_stall = ctx->debug_stall;
+  p.max_spins = ctx->debug_spins;
+  ctx->debug_stall = 0;
+  ctx->debug_spins = 0;
   cudaError_t e;
   if (tc) {
     e = pic::launch_attend_mla_tc(p, maps, m.pairing, heads.group, static_cast<int>(ctas), smem, s);

@@ -163,6 +163,11 @@ struct AttnParams {
   float* out;               // [n_layers][n_req][num_q_heads][D]
   float* lse;               // [n_layers][n_req][num_q_heads] or null
   uint32_t* status;         // PIC_DEV_* bits
+  // Test hook (pic_debug_stall_next_launch; the tcgen05 MLA kernel only):
+  // debug_stall = t + 1 makes CTA 0 skip tile t's copies and barrier
+  // arrivals; max_spins bounds every wait of the launch (0: the default).
+  int32_t debug_stall;
+  uint32_t max_spins;
 };
 
 // floats of one (record, KV head) block: acc[G][D], m[G], l[G], padded to 16 B
