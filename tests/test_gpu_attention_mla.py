@@ -186,6 +186,36 @@ def test_mla_cache_path_over_materialized_stitch():
         pic.pic_destroy(S["ctx"])
 
 
+def test_mla_attention_over_a_layer_window():
+    """Layers [1, 3) of a 3-layer model in one call: q, out and lse hold the
+    window's layers only, while the pool and cache rows are read from
+    absolute layers 1 and 2 (the tcgen05 kernel's TMA layer coordinate and
+    its query indexing differ by layer_begin)."""
+    S = _setup("interleaved", 3, seed=8)
+    try:
+        H, lb, nl = 16, 1, 2
+        g = torch.Generator().manual_seed(9)
+        q = torch.randn((nl, 3, H, ROW), generator=g).to(torch.bfloat16)
+        out = torch.empty((nl, 3, H, LATENT), dtype=torch.float32, device=DEV)
+        lse = torch.empty((nl, 3, H), dtype=torch.float32, device=DEV)
+        ws = torch.empty(pic.pic_attend_workspace_bytes(S["ctx"], S["plans"], H, nl), dtype=torch.uint8, device=DEV)
+        scale = 1.0 / math.sqrt(192)
+        pic.pic_attend_decode(S["ctx"], S["plans"], pic.PIC_ATTEND_FUSED, q.to(DEV), scale, S["pool"].to(DEV), None,
+                              S["cache"].to(DEV), None, out, lse, ws, sink_bias=-15.0, layer_begin=lb)
+        assert pic.pic_query_device_status(S["ctx"], ws) == 0
+        out, lse, qb = out.cpu().double().numpy(), lse.cpu().double().numpy(), bits(q)
+        for r in range(3):
+            rows, segs, T = _context_rows(S, r)
+            bias = oracle.sink_bias(segs, T, 4, -15.0)
+            for l in range(nl):
+                o, sv = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[l, r]), rows[lb + l][:, None, :],
+                                                rows[lb + l][:, None, :LATENT], scale, bias)
+                np.testing.assert_allclose(out[l, r], o, atol=2e-3, rtol=0)
+                np.testing.assert_allclose(lse[l, r], sv, atol=2e-3, rtol=0)
+    finally:
+        pic.pic_destroy(S["ctx"])
+
+
 def test_mla_rejects_unsupported_head_counts():
     S = _setup("interleaved", 1, seed=7)
     try:
