@@ -270,9 +270,9 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   constexpr int kSI = tc_score_issuers(HC);
   constexpr int kNP = tc_producers(HC);
   constexpr int kVI = tc_value_issuers(HC);
-  // the latent score accumulates in NP independent partial sums (k-steps
-  // interleaved), so consecutive small products do not wait on one another
-  constexpr int NP = HC == 16 ? 4 : 2;
+  // the latent score accumulates in NP partial sums (k-step mod NP; with two
+  // score issuers, one each)
+  constexpr int NP = 2;
   constexpr uint32_t kRopeCol = NP * HC;
   static_assert(NE * 2 * HC == 128 && kRopeCol + NE * 2 * HC <= kTcSCols, "rope columns");
   static_assert(kTcOCol + 4 * kTcOColsPerTile <= kTcCols, "TMEM columns");
