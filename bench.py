@@ -840,7 +840,8 @@ def main():
                      "launch_ms": kms},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        # per step: the stitch or shift kernel; attention adds its merge kernel
+        "gpu_launches": args.steps * {"stitch": 1, "mapped": 1, "inplace": 1, "attend": 2, "attend_cache": 3}[args.mode],
         "clocks": clk,
     }
     if rank == 0:
