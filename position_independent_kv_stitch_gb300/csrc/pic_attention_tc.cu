@@ -83,10 +83,12 @@ __host__ __device__ constexpr int tc_threads(int hc) {
   return 32 * (9 + tc_score_issuers(hc) + tc_producers(hc) + tc_value_issuers(hc));
 }
 constexpr uint32_t kTcCols = 512;                          // TMEM columns held by the CTA
-// TMEM columns: two score buffers of kTcSCols (the latent score as partial
-// sums over interleaved k-steps, NP x HC columns, then the rope columns),
-// then O^T: four M-tiles of 32 columns (16 heads: the hi and lo parts of P
-// in columns 0-15 and 16-31; 32 heads: both parts summed in place).
+// TMEM columns: two score buffers of kTcSCols (the latent score as NP partial
+// sums, NP x HC columns, then the rope columns), then O^T: four M-tiles of
+// 32 columns (16 heads: the hi and lo parts of P in columns 0-15 and 16-31;
+// 32 heads: both parts summed in place).  An M = 64 score puts rows
+// 16 q .. 16 q + 15 in lanes 0-15 of lane quadrant q; an M = 128 product row r
+// in lane r.
 constexpr uint32_t kTcSCols = 192;
 constexpr uint32_t kTcOCol = 2 * kTcSCols;
 constexpr uint32_t kTcOColsPerTile = 32;
@@ -621,6 +623,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           }
           const TcTile t = tiles[rt];
           tc_fence_after();
+          // V^T as an MN-major A: 64 latent dims per 128-byte row, rows 1,024
+          // bytes per 8 positions (SBO), the next 64 dims one plane on (LBO)
           const uint64_t dv = sdesc(ring + rt * kTcTileBytes, kTcPlaneBytes, 1024);
           const uint64_t dp = sdesc(pt + rt * L::kPtBytes, 16, 1024);
           const bool first = (t.flags & kTcFirst) != 0;
