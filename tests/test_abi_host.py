@@ -285,3 +285,28 @@ def test_debug_stall_hook_checks_its_context():
         pic.pic_debug_stall_next_launch(ctx, -1)
     finally:
         pic.pic_destroy(ctx)
+
+
+def test_kernel_variant_of_decode_attention(monkeypatch):
+    """Mode 2 reports the decode-attention kernel chosen at pic_create: tcgen05
+    for MLA models unless PIC_ATTEND_KERNEL=mma, warp-level mma for GQA."""
+    mla = W.deepseek_v3_mla(context_tokens=256, num_layers=1).model
+    monkeypatch.delenv("PIC_ATTEND_KERNEL", raising=False)
+    ctx = pic.create_from_spec(pic.model_spec_from(mla), 32)
+    try:
+        assert pic.pic_kernel_variant(ctx, 2) == pic.PIC_VARIANT_TENSOR_CORE_TMEM
+        assert pic.pic_kernel_variant(ctx, 3) == -1
+    finally:
+        pic.pic_destroy(ctx)
+    monkeypatch.setenv("PIC_ATTEND_KERNEL", "mma")
+    ctx = pic.create_from_spec(pic.model_spec_from(mla), 32)
+    try:
+        assert pic.pic_kernel_variant(ctx, 2) == pic.PIC_VARIANT_WARP_MMA
+    finally:
+        pic.pic_destroy(ctx)
+    monkeypatch.delenv("PIC_ATTEND_KERNEL")
+    ctx = _gqa_ctx(nb=8)
+    try:
+        assert pic.pic_kernel_variant(ctx, 2) == pic.PIC_VARIANT_WARP_MMA
+    finally:
+        pic.pic_destroy(ctx)
