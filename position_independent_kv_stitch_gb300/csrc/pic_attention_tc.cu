@@ -117,8 +117,7 @@ struct TcLayout {
   static constexpr int kRope = kQn + 8 * kQnPlane;              // NE x (HC hi + HC lo) rows x 128 B
   static constexpr int kPt = kRope + NE * 2 * HC * 128;         // P^T: 2 buffers x (HC hi + HC lo) rows
   static constexpr int kPtBytes = 2 * HC * 128;
-  static constexpr int kQsrc = kPt + 2 * kPtBytes;              // q_rope as loaded: HC x 64 bf16
-  static constexpr int kWmax = kQsrc + HC * 64 * 2;             // float [2][4][HC]
+  static constexpr int kWmax = kPt + 2 * kPtBytes;              // float [2][4][HC]
   static constexpr int kLred = kWmax + 2 * 4 * HC * 4;          // float [4][HC]
   static constexpr int kTiles = kLred + 4 * HC * 4;             // TcTile [2]
   static constexpr int kBars = kTiles + 2 * static_cast<int>(sizeof(TcTile));
@@ -257,8 +256,7 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
 }
 
 // grid: persistent CTAs, CTA c owns units [U c / G, U (c + 1) / G) of the
-// (layer, stage) list; block: 224 threads (4 softmax warps, producer, MMA,
-// query).
+// (layer, stage) list; block: tc_threads(HC) threads (the warp roles above).
 template <int PAIRING, int HC>
 __global__ void __launch_bounds__(tc_threads(HC), 1)
     k_attend_mla_tc(const AttnParams P, const __grid_constant__ TcMaps maps) {
