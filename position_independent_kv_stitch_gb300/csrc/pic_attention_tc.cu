@@ -25,7 +25,7 @@
 //   * the query warp writes the query operands: q_nope on a key change, and
 //     for each new delta of the tile R(-delta) q_rope as bf16 hi and lo rows
 //     (NE delta entries, so stages with different deltas share a tile);
-//   * score issuers (one thread each) issue S = rows [q_nope | rope parts]^T
+//   * score issuers (one warp each) issue S = rows [q_nope | rope parts]^T
 //     into TMEM: M = 64, 32 k-steps over the latent, 4 over the rope plane;
 //   * a value issuer issues O^T += V^T P^T once P is written: M = 128
 //     latent dims (four M-tiles), N = 32 (16 heads: P's hi and lo rows side
@@ -70,10 +70,11 @@ constexpr float kTcLazy = 8.0f;
 // then a producer, the score-product issuer (it also holds the TMEM
 // allocation), the query warp, the value-product issuer and, for 16 heads, a
 // second score-product issuer, two more producers and a second value-product
-// issuer.  One thread issues a small tcgen05.mma about every 70 cycles
-// whatever its shape, and one warp issues TMA copies one lane after another
-// (~35 ns each), so both are spread over warps; 32 heads need the registers
-// the extra warps would take.
+// issuer.  A thread issuing alone puts out a small tcgen05.mma about every
+// 55-70 cycles whatever its shape (a converged warp issuing from its elected
+// lane, about every 29), and one warp issues TMA copies one lane after
+// another (~35 ns each), so both are spread over warps; 32 heads need the
+// registers the extra warps would take.
 constexpr int kTcSoftmaxWarps = 8;
 constexpr int kTcProducer = 8, kTcMma = 9, kTcQuery = 10, kTcPv = 11, kTcMma2 = 12, kTcProducer2 = 13, kTcPv2 = 15;
 __host__ __device__ constexpr int tc_score_issuers(int hc) { return hc == 16 ? 2 : 1; }
@@ -147,6 +148,7 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
+// one thread issues / commits
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -156,6 +158,47 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+// Both run on a whole converged warp and issue from its elected lane (the
+// same lane every time, as the commit tracks that thread's products).  Issued
+// this way, from operands the warp holds in common, a 64 x 16 product goes out
+// about twice as often as from a branch taken by one lane.
+__device__ __forceinline__ void tc_mma_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc ? 1u : 0u));
+}
+__device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// the issue form of a role: E, the whole warp and its elected lane; else one thread
+template <bool E>
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
+  if constexpr (E) {
+    tc_mma_elect(d, a, b, id, acc);
+  } else {
+    tc_mma(d, a, b, id, acc);
+  }
+}
+template <bool E>
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  if constexpr (E) {
+    tc_commit_elect(bar);
+  } else {
+    tc_commit(bar);
+  }
+}
+template <bool E>
+__device__ __forceinline__ bool agree(bool ok) {
+  if constexpr (E) {
+    return __all_sync(0xffffffffu, ok);
+  } else {
+    return ok;
+  }
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -270,6 +313,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   constexpr int kSI = tc_score_issuers(HC);
   constexpr int kNP = tc_producers(HC);
   constexpr int kVI = tc_value_issuers(HC);
+  // How each issuer role issues (see the MMA issuers below).  Measured on
+  // the 61-layer, 65,536-position workload: at 16 heads the elected-lane form
+  // for both roles is the fastest (1.064 ms; score only 1.080, value only
+  // 1.138), at 32 heads the single-thread form for both (1.656 ms; 1.699 and
+  // 1.784 with either role elected, slower still with both).
+  constexpr bool kElectS = HC == 16, kElectV = HC == 16;
   // the latent score accumulates in NP partial sums (k-step mod NP; with two
   // score issuers, one each)
   constexpr int NP = 2;
@@ -566,88 +615,92 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     }
   } else if ((warp == kTcMma || warp == kTcMma2 || warp == kTcPv || warp == kTcPv2) && has_work) {
     // --------------------------------------------------- MMA issuers
-    if (lane == 0) {
-      const uint32_t ring = base_u32 + L::kRing;
-      // A descriptor is affine in its start address (start / 16 sits in the
-      // low bits, and no start here reaches 256 KB), so each product builds
-      // its base descriptors once and steps them by constants.
-      if (warp == kTcMma || warp == kTcMma2) {
-        // S of tile i once its rows and query operands are in and its TMEM
-        // buffer is free (the softmax of tile i - 2 has written P, so it is
-        // done reading that buffer).  With two issuers the first takes the
-        // even latent k-steps and the rope plane, the second the odd k-steps;
-        // each writes its own partial sums (k-step mod NP).
-        const int par = warp == kTcMma ? 0 : 1;
-        const uint64_t dq = sdesc(base_u32 + L::kQn, 16, 1024), dr = sdesc(base_u32 + L::kRope, 16, 1024);
-        for (int i = 0;; ++i) {
-          const int rt = i & 1;
-          if (!wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag, spins) ||
-              !wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins) ||
-              (i >= 2 && !wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag, spins))) {
-            fail();
-            break;
-          }
-          const int flags = tiles[rt].flags;
-          tc_fence_after();
-          const uint64_t da = sdesc(ring + rt * kTcTileBytes, 16, 1024);
-          const uint32_t d = tmem + rt * kTcSCols;
-#pragma unroll
-          for (int k2 = 0; k2 < 32 / kSI; ++k2) {
-            const int ks = kSI * k2 + par;
-            tc_mma(d + (ks % NP) * HC, da + (((ks >> 2) * kTcPlaneBytes + (ks & 3) * 32) >> 4),
-                   dq + (((ks >> 2) * L::kQnPlane + (ks & 3) * 32) >> 4), kIdS, ks >= NP);
-          }
-          if (par == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc_mma(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);
-          }
-          tc_commit(&s_full[rt]);
-          if (flags & kTcEnd) break;
+    // A role with E set runs its loop on the whole warp (the waits, the
+    // operand addresses) and issues the products and commits from the elected
+    // lane; otherwise lane 0 alone runs it.
+    const uint32_t ring = base_u32 + L::kRing;
+    // A descriptor is affine in its start address (start / 16 sits in the
+    // low bits, and no start here reaches 256 KB), so each product builds its
+    // base descriptors once and steps them by constants.
+    if ((warp == kTcMma || warp == kTcMma2) && (kElectS || lane == 0)) {
+      constexpr bool E = kElectS;
+      // S of tile i once its rows and query operands are in and its TMEM
+      // buffer is free (the softmax of tile i - 2 has written P, so it is
+      // done reading that buffer).  With two issuers the first takes the even
+      // latent k-steps and the rope plane, the second the odd k-steps; each
+      // writes its own partial sums (k-step mod NP).
+      const int par = warp == kTcMma ? 0 : 1;
+      const uint64_t dq = sdesc(base_u32 + L::kQn, 16, 1024), dr = sdesc(base_u32 + L::kRope, 16, 1024);
+      for (int i = 0;; ++i) {
+        const int rt = i & 1;
+        const bool ok = wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag, spins) &&
+                        wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins) &&
+                        (i < 2 || wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag, spins));
+        if (!agree<E>(ok)) {
+          if (lane == 0) fail();
+          break;
         }
-        tc_commit(&done[par]);
-        mbar_wait_bounded(&done[par], 0);
-      } else {
-        // O^T += V^T P^T of tile i once its P is written; its metadata stays
-        // in the slot until this product ends.  With two issuers each takes
-        // two of the four latent M-tiles.
-        const uint32_t pt = base_u32 + L::kPt;
-        const int vi = warp == kTcPv ? 0 : 1;
-        for (int i = 0;; ++i) {
-          const int rt = i & 1;
-          if (!wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag, spins)) {
-            fail();
-            break;
-          }
-          const TcTile t = tiles[rt];
-          tc_fence_after();
-          // V^T as an MN-major A: 64 latent dims per 128-byte row, rows 1,024
-          // bytes per 8 positions (SBO), the next 64 dims one plane on (LBO)
-          const uint64_t dv = sdesc(ring + rt * kTcTileBytes, kTcPlaneBytes, 1024);
-          const uint64_t dp = sdesc(pt + rt * L::kPtBytes, 16, 1024);
-          const bool first = (t.flags & kTcFirst) != 0;
-          // the four latent M-tiles are independent accumulators: innermost
+        const int flags = tiles[rt].flags;
+        tc_fence_after();
+        const uint64_t da = sdesc(ring + rt * kTcTileBytes, 16, 1024);
+        const uint32_t d = tmem + rt * kTcSCols;
 #pragma unroll
-          for (int w = 0; w < kTcStagesPerTile; ++w) {
-            if (w >= t.ns) break;
+        for (int k2 = 0; k2 < 32 / kSI; ++k2) {
+          const int ks = kSI * k2 + par;
+          mma<E>(d + (ks % NP) * HC, da + (((ks >> 2) * kTcPlaneBytes + (ks & 3) * 32) >> 4),
+              dq + (((ks >> 2) * L::kQnPlane + (ks & 3) * 32) >> 4), kIdS, ks >= NP);
+        }
+        if (par == 0) {
 #pragma unroll
-            for (int part = 0; part < kPvParts; ++part) {
-              const uint64_t bd = dp + ((part * 32 * 128 + w * 32) >> 4);
+          for (int ks = 0; ks < 4; ++ks)
+            mma<E>(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);
+        }
+        commit<E>(&s_full[rt]);
+        if (flags & kTcEnd) break;
+      }
+      commit<E>(&done[par]);
+      mbar_wait_bounded(&done[par], 0);
+    } else if ((warp == kTcPv || warp == kTcPv2) && (kElectV || lane == 0)) {
+      constexpr bool E = kElectV;
+      // O^T += V^T P^T of tile i once its P is written; its metadata stays in
+      // the slot until this product ends.  With two issuers each takes two of
+      // the four latent M-tiles.
+      const uint32_t pt = base_u32 + L::kPt;
+      const int vi = warp == kTcPv ? 0 : 1;
+      for (int i = 0;; ++i) {
+        const int rt = i & 1;
+        if (!agree<E>(wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag, spins))) {
+          if (lane == 0) fail();
+          break;
+        }
+        const int t_ns = tiles[rt].ns, t_flags = tiles[rt].flags;
+        tc_fence_after();
+        // V^T as an MN-major A: 64 latent dims per 128-byte row, rows 1,024
+        // bytes per 8 positions (SBO), the next 64 dims one plane on (LBO)
+        const uint64_t dv = sdesc(ring + rt * kTcTileBytes, kTcPlaneBytes, 1024);
+        const uint64_t dp = sdesc(pt + rt * L::kPtBytes, 16, 1024);
+        const bool first = (t_flags & kTcFirst) != 0;
+        // the four latent M-tiles are independent accumulators: innermost
 #pragma unroll
-              for (int m4 = 0; m4 < 4 / kVI; ++m4) {
-                const int mt = vi * (4 / kVI) + m4;
-                tc_mma(tmem + kTcOCol + mt * kTcOColsPerTile, dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4),
-                       bd, kIdPV, !(first && w == 0 && part == 0));
-              }
+        for (int w = 0; w < kTcStagesPerTile; ++w) {
+          if (w >= t_ns) break;
+#pragma unroll
+          for (int part = 0; part < kPvParts; ++part) {
+            const uint64_t bd = dp + ((part * 32 * 128 + w * 32) >> 4);
+#pragma unroll
+            for (int m4 = 0; m4 < 4 / kVI; ++m4) {
+              const int mt = vi * (4 / kVI) + m4;
+              mma<E>(tmem + kTcOCol + mt * kTcOColsPerTile, dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4),
+                  bd, kIdPV, !(first && w == 0 && part == 0));
             }
           }
-          tc_commit(&empty[rt]);
-          tc_commit(&pv_done[rt]);
-          if (t.flags & kTcEnd) break;
         }
-        tc_commit(&done[2 + vi]);
-        mbar_wait_bounded(&done[2 + vi], 0);
+        commit<E>(&empty[rt]);
+        commit<E>(&pv_done[rt]);
+        if (t_flags & kTcEnd) break;
       }
+      commit<E>(&done[2 + vi]);
+      mbar_wait_bounded(&done[2 + vi], 0);
     }
   } else if (warp < kTcSoftmaxWarps && has_work) {
     // ------------------------------------------------------------ softmax
