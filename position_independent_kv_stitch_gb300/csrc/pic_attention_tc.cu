@@ -115,7 +115,8 @@ struct TcLayout {
   static constexpr int kRing = 0;                               // 2 tiles
   static constexpr int kQn = kRing + 2 * kTcTileBytes;          // q_nope: 8 planes x HC rows x 128 B
   static constexpr int kQnPlane = HC * 128;
-  static constexpr int kRope = kQn + 8 * kQnPlane;              // NE x (HC hi + HC lo) rows x 128 B
+  // NE entries x 2 halves of the heads x (HC / 2 hi + HC / 2 lo) rows x 128 B
+  static constexpr int kRope = kQn + 8 * kQnPlane;
   static constexpr int kPt = kRope + NE * 2 * HC * 128;         // P^T: 2 buffers x (HC hi + HC lo) rows
   static constexpr int kPtBytes = 2 * HC * 128;
   static constexpr int kWmax = kPt + 2 * kPtBytes;              // float [2][4][HC]
@@ -457,16 +458,9 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       } else if (j + ns >= n_st || next_key != key) {
         t.flags |= kTcLast;
       }
-      // the slot's previous tile (i - 2) must be done before its metadata and rows are replaced
-      if (i >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&empty[rt], ((i >> 1) - 1) & 1, abort_flag, spins))) {
-        failed = true;
-        break;
-      }
-      if (prod == 0 && lane == 0) {
-        tiles[rt] = t;
-        mbar_arrive(&meta_ready[rt]);
-      }
-      // stage k continues stage k - 1's box when that stage is full and its rows go on
+      // The copies are planned before the slot is free, so that once it is
+      // only the announcements and the copies themselves remain.  Stage k
+      // continues stage k - 1's box when that stage is full and its rows go on.
       const int prow = __shfl_up_sync(0xffffffffu, tk.row, 1);
       const int pflags = __shfl_up_sync(0xffffffffu, tk.flags, 1);
       const int pn = __shfl_up_sync(0xffffffffu, cw.w & 0xffff, 1);
@@ -477,60 +471,48 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const int ngroups = __popc(lmask);
       const int my_len = leader ? __ffs(~(cmask >> (lane + 1))) : 0;  // this stage and the ones continuing it
       const int z = P.layer_begin + layer;
+      // copy q (box q / 9, plane q % 9; at most 36) goes to producer warp
+      // q % kNP, lane (q / kNP) % 32; each warp announces its own bytes
+      constexpr int kRounds = (4 * kTcPlanes + 32 * kNP - 1) / (32 * kNP);
+      int cp_row[kRounds], cp_len[kRounds], cp_pl[kRounds];
+      uint32_t cp_dst[kRounds];
+      const CUtensorMap* cp_map[kRounds];
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int r = 0; r < kRounds; ++r) {
+        const int q = prod + kNP * (lane + 32 * r);
+        const int g = q / kTcPlanes;
+        uint32_t m = lmask;
+        for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
+        const int src = m ? __ffs(m) - 1 : 0;
+        cp_row[r] = __shfl_sync(0xffffffffu, tk.row, src);
+        const int fl = __shfl_sync(0xffffffffu, tk.flags, src);
+        cp_len[r] = __shfl_sync(0xffffffffu, my_len, src);
+        cp_pl[r] = g < ngroups ? q - g * kTcPlanes : kTcPlanes;
+        cp_dst[r] = base_u32 + L::kRing + rt * kTcTileBytes + src * kTcStageBytes + cp_pl[r] * kTcPlaneBytes;
+        cp_map[r] = cp_pl[r] < kTcPlanes ? ((fl & kAttnFromCache) ? &maps.cache[cp_len[r] - 1] : &maps.pool[cp_len[r] - 1])
+                                         : nullptr;
+        bytes += cp_pl[r] < kTcPlanes ? static_cast<uint32_t>(cp_len[r]) * kTcStageBytes : 0u;
+      }
+      bytes = __reduce_add_sync(0xffffffffu, bytes);
+      // the slot's previous tile (i - 2) must be done before its metadata and rows are replaced
+      if (i >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&empty[rt], ((i >> 1) - 1) & 1, abort_flag, spins))) {
+        failed = true;
+        break;
+      }
+      if (prod == 0 && lane == 0) {
+        tiles[rt] = t;
+        mbar_arrive(&meta_ready[rt]);
+      }
       // test hook (pic_debug_stall_next_launch): CTA 0 leaves this tile's rows
       // unrequested, so the waits for them run out and take the failure path
       const bool stalled = P.debug_stall != 0 && blockIdx.x == 0 && i == P.debug_stall - 1;
-      if (stalled) {
-        // no arrival, no copies
-      } else if constexpr (kNP == 1) {
-        // one producer: it announces the whole tile, then lane q issues copies q and q + 32
-        if (lane == 0) mbar_arrive_expect_tx(&full[rt], static_cast<uint32_t>(ns) * kTcStageBytes * kTcPlanes);
-        __syncwarp();
-#pragma unroll
-        for (int round = 0; round < 2; ++round) {
-          const int q = lane + 32 * round;
-          const int g = q / kTcPlanes, pl = q - g * kTcPlanes;
-          uint32_t m = lmask;
-          for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
-          const int src = m ? __ffs(m) - 1 : 0;
-          const int row = __shfl_sync(0xffffffffu, tk.row, src), fl = __shfl_sync(0xffffffffu, tk.flags, src);
-          const int len = __shfl_sync(0xffffffffu, my_len, src);
-          if (g < ngroups) {
-            const CUtensorMap* map = (fl & kAttnFromCache) ? &maps.cache[len - 1] : &maps.pool[len - 1];
-            tma_load_3d(base_u32 + L::kRing + rt * kTcTileBytes + src * kTcStageBytes + pl * kTcPlaneBytes, map,
-                        64 * pl, row, z, &full[rt]);
-          }
-        }
-      } else {
-        // copy q (box q / 9, plane q % 9; at most 36) goes to producer warp
-        // q % kNP, lane (q / kNP) % 32; this warp announces its bytes first
-        constexpr int kRounds = (4 * kTcPlanes + 32 * kNP - 1) / (32 * kNP);
-        int cp_row[kRounds], cp_fl[kRounds], cp_len[kRounds], cp_src[kRounds], cp_pl[kRounds];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int r = 0; r < kRounds; ++r) {
-          const int q = prod + kNP * (lane + 32 * r);
-          const int g = q / kTcPlanes;
-          uint32_t m = lmask;
-          for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
-          cp_src[r] = m ? __ffs(m) - 1 : 0;
-          cp_row[r] = __shfl_sync(0xffffffffu, tk.row, cp_src[r]);
-          cp_fl[r] = __shfl_sync(0xffffffffu, tk.flags, cp_src[r]);
-          cp_len[r] = __shfl_sync(0xffffffffu, my_len, cp_src[r]);
-          cp_pl[r] = g < ngroups ? q - g * kTcPlanes : kTcPlanes;
-          bytes += cp_pl[r] < kTcPlanes ? static_cast<uint32_t>(cp_len[r]) * kTcStageBytes : 0u;
-        }
-        bytes = __reduce_add_sync(0xffffffffu, bytes);
+      if (!stalled) {
         if (lane == 0) mbar_arrive_expect_tx(&full[rt], bytes);
         __syncwarp();
 #pragma unroll
-        for (int r = 0; r < kRounds; ++r) {
-          if (cp_pl[r] < kTcPlanes) {
-            const CUtensorMap* map = (cp_fl[r] & kAttnFromCache) ? &maps.cache[cp_len[r] - 1] : &maps.pool[cp_len[r] - 1];
-            tma_load_3d(base_u32 + L::kRing + rt * kTcTileBytes + cp_src[r] * kTcStageBytes + cp_pl[r] * kTcPlaneBytes,
-                        map, 64 * cp_pl[r], cp_row[r], z, &full[rt]);
-          }
-        }
+        for (int r = 0; r < kRounds; ++r)
+          if (cp_pl[r] < kTcPlanes) tma_load_3d(cp_dst[r], cp_map[r], 64 * cp_pl[r], cp_row[r], z, &full[rt]);
       }
       issued = i + 1;
       cw = make_int4(0, 0, 0, 0);
@@ -595,7 +577,9 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             __nv_bfloat16 ah, al, bh, bl;
             split_bf16(qa[h] * cs + qb[h] * sn, ah, al);
             split_bf16(qb[h] * cs - qa[h] * sn, bh, bl);
-            const int rh = e * 2 * HC + h, rl = rh + HC;
+            // per entry and half of the heads: the half's hi rows, then its lo rows
+            constexpr int HH = HC / 2;
+            const int rh = e * 2 * HC + (h / HH) * 2 * HH + h % HH, rl = rh + HH;
             if (NEOX) {
               *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ia)) = ah;
               *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ib)) = bh;
@@ -740,26 +724,29 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         break;
       }
       tc_fence_after();
-      const TcTile t = tiles[rt];
-      if (t.flags & kTcFirst) {
+      // this warp's fields of the tile record (read now: the slot's record is
+      // replaced once the tile's value product has finished)
+      const TcTile& tr = tiles[rt];
+      const int t_flags = tr.flags, t_layer = tr.layer, t_key = tr.key;
+      const bool present = w < tr.ns;
+      const int n_tok = present ? tr.n_tok[w] : 0;
+      const int entry = present ? tr.entry[w] : 0;
+      const int sink = present ? tr.sink[w] : 0;
+      if (t_flags & kTcFirst) {
 #pragma unroll
         for (int h = 0; h < HH; ++h) {
           m_run[h] = -INFINITY;
           l_part[h] = 0.0f;
         }
       }
-      const bool present = w < t.ns;
-      const int n_tok = present ? t.n_tok[w] : 0;
-      const int entry = present ? t.entry[w] : 0;
-      float sp[NP][HH], rh[HH], rl[HH];
+      float sp[NP][HH], rr[2 * HH];  // latent partial sums; the rope hi then lo columns
       const uint32_t sc = tl + rt * kTcSCols + h0;
-      tmem_ld<HH>(sc + kRopeCol + entry * 2 * HC, rh);
-      tmem_ld<HH>(sc + kRopeCol + entry * 2 * HC + HC, rl);
+      tmem_ld<2 * HH>(sc + kRopeCol + entry * 2 * HC + h0, rr);
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) tmem_ld<HH>(sc + pp * HC, sp[pp]);
       tmem_wait_ld();
       const bool live = lane < n_tok;
-      const float bias = (live && ((t.sink[w] >> lane) & 1)) ? P.sink_log2 : 0.0f;
+      const float bias = (live && ((sink >> lane) & 1)) ? P.sink_log2 : 0.0f;
       float s[HH];
       bool need = false;
 #pragma unroll
@@ -767,7 +754,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         float v = sp[0][h];
 #pragma unroll
         for (int pp = 1; pp < NP; ++pp) v += sp[pp][h];
-        s[h] = live ? ((v + rh[h]) + rl[h]) * P.scale_log2 + bias : -INFINITY;
+        s[h] = live ? ((v + rr[h]) + rr[HH + h]) * P.scale_log2 + bias : -INFINITY;
         need |= s[h] > m_run[h] + kTcLazy;
       }
       // does any position raise a head's running max?
@@ -795,7 +782,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         }
         // every warp takes the same branch: the barrier below is reached by all or none
         const bool rescale_any = softmax_bar_or(rescale);
-        if (!(t.flags & kTcFirst) && rescale_any) {
+        if (!(t_flags & kTcFirst) && rescale_any) {
           // O holds this key's earlier tiles: wait for the last product into it, then scale in place
           const bool landed = wait_or_abort(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins);
           if (softmax_bar_or(!landed)) {
@@ -848,7 +835,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[rt]);
 
-      if (t.flags & kTcLast) {
+      if (t_flags & kTcLast) {
         // the key's last tile in this CTA: write its record (O, m, l)
         const bool landed = wait_or_abort(&pv_done[rt], ph, abort_flag, spins);
         if (softmax_bar_or(!landed)) {
@@ -864,7 +851,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           if (lane == 0) lred[w * HC + h0 + h] = v;
         }
         softmax_bar_or(false);
-        const AttnKey kk = P.keys[static_cast<int64_t>(t.layer) * P.n_keys + t.key];
+        const AttnKey kk = P.keys[static_cast<int64_t>(t_layer) * P.n_keys + t_key];
         const int blk_floats = attn_block_floats(HC, kMlaLatentDims);
         float* blk =
             P.records + static_cast<int64_t>(kk.rec_base + (static_cast<int>(blockIdx.x) - kk.first_cta)) * blk_floats;
@@ -890,7 +877,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         }
         tc_fence_before();
       }
-      if (t.flags & kTcEnd) break;
+      if (t_flags & kTcEnd) break;
     }
   }
 
