@@ -264,6 +264,33 @@ __device__ __forceinline__ void tmem_st(uint32_t taddr, const float* v) {
   }
 }
 
+// 16 TMEM lanes from a lane quadrant's base, G groups of 8 columns (shape
+// 16x256b).  Per group g, thread t gets lanes t / 4 and t / 4 + 8 at columns
+// 8 g + 2 (t % 4) and + 1, as v[4 g .. 4 g + 3] = (t / 4, c), (t / 4, c + 1),
+// (t / 4 + 8, c), (t / 4 + 8, c + 1) (the layout measured on GB300).
+template <int G>
+__device__ __forceinline__ void tmem_ld16x256(uint32_t taddr, float* v) {
+  uint32_t r[4 * G];
+  if constexpr (G == 1) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+  } else if constexpr (G == 2) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+  } else {
+    static_assert(G == 4, "16x256b groups");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+  }
+#pragma unroll
+  for (int j = 0; j < 4 * G; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -690,16 +717,24 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     // ------------------------------------------------------------ softmax
     // Warp (w, half): stage w's 16 positions (TMEM lanes 32w .. 32w + 15 of
     // the M = 64 scores), heads [h0, h0 + HH); O^T lanes 32w .. 32w + 31.
+    // The scores are read with the 16x256b shape, so every thread holds two
+    // positions (q0 and q0 + 8) of NH of the warp's heads: its value r is
+    // position q0 + 8 ((r >> 1) & 1) of head slot 2 (r >> 2) + (r & 1), and
+    // slot j is head 8 (j >> 1) + c0 + (j & 1) of the warp's HH.
     constexpr int HH = HC / 2;
+    constexpr int NG = HH / 8;  // 8-column groups of the warp's heads
+    constexpr int NR = 4 * NG;  // scores a thread holds
+    constexpr int NH = 2 * NG;  // heads a thread holds
     const int w = warp & 3, half = warp >> 2, h0 = half * HH;
+    const int q0 = lane >> 2, c0 = 2 * (lane & 3);
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * w) << 16);
     float* wmax = reinterpret_cast<float*>(smem + L::kWmax);
     float* lred = reinterpret_cast<float*>(smem + L::kLred);
-    float m_run[HH], l_part[HH];
+    float m_run[NH], l_part[NH];
 #pragma unroll
-    for (int h = 0; h < HH; ++h) {
-      m_run[h] = -INFINITY;
-      l_part[h] = 0.0f;
+    for (int j = 0; j < NH; ++j) {
+      m_run[j] = -INFINITY;
+      l_part[j] = 0.0f;
     }
     // this warp's O^T columns of M-tile mt: both parts of P (16 heads), or the sum (32 heads)
     auto o_load = [&](int mt, float* o) {
@@ -734,51 +769,54 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const int sink = present ? tr.sink[w] : 0;
       if (t_flags & kTcFirst) {
 #pragma unroll
-        for (int h = 0; h < HH; ++h) {
-          m_run[h] = -INFINITY;
-          l_part[h] = 0.0f;
+        for (int j = 0; j < NH; ++j) {
+          m_run[j] = -INFINITY;
+          l_part[j] = 0.0f;
         }
       }
-      float sp[NP][HH], rr[2 * HH];  // latent partial sums; the rope hi then lo columns
+      float sp[NP][NR], rr[2 * NR];  // latent partial sums; the rope hi then lo columns
       const uint32_t sc = tl + rt * kTcSCols + h0;
-      tmem_ld<2 * HH>(sc + kRopeCol + entry * 2 * HC + h0, rr);
+      tmem_ld16x256<2 * NG>(sc + kRopeCol + entry * 2 * HC + h0, rr);
 #pragma unroll
-      for (int pp = 0; pp < NP; ++pp) tmem_ld<HH>(sc + pp * HC, sp[pp]);
+      for (int pp = 0; pp < NP; ++pp) tmem_ld16x256<NG>(sc + pp * HC, sp[pp]);
       tmem_wait_ld();
-      const bool live = lane < n_tok;
-      const float bias = (live && ((sink >> lane) & 1)) ? P.sink_log2 : 0.0f;
-      float s[HH];
+      float s[NR];
       bool need = false;
 #pragma unroll
-      for (int h = 0; h < HH; ++h) {
-        float v = sp[0][h];
+      for (int r = 0; r < NR; ++r) {
+        const int q = q0 + 8 * ((r >> 1) & 1);
+        const bool live = q < n_tok;
+        const float bias = (live && ((sink >> q) & 1)) ? P.sink_log2 : 0.0f;
+        float v = sp[0][r];
 #pragma unroll
-        for (int pp = 1; pp < NP; ++pp) v += sp[pp][h];
-        s[h] = live ? ((v + rr[h]) + rr[HH + h]) * P.scale_log2 + bias : -INFINITY;
-        need |= s[h] > m_run[h] + kTcLazy;
+        for (int pp = 1; pp < NP; ++pp) v += sp[pp][r];
+        s[r] = live ? ((v + rr[r]) + rr[NR + r]) * P.scale_log2 + bias : -INFINITY;
+        need |= s[r] > m_run[2 * (r >> 2) + (r & 1)] + kTcLazy;
       }
       // does any position raise a head's running max?
       if (softmax_bar_or(need)) {
         float* wm = wmax + (rt * 4 + w) * HC + h0;
 #pragma unroll
-        for (int h = 0; h < HH; ++h) {
-          float v = s[h];
+        for (int j = 0; j < NH; ++j) {
+          const int r = 4 * (j >> 1) + (j & 1);
+          float v = fmaxf(s[r], s[r + 2]);
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-          if (lane == 0) wm[h] = v;
+          for (int o = 4; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          if (q0 == 0) wm[8 * (j >> 1) + c0 + (j & 1)] = v;
         }
         softmax_bar_or(false);
         const volatile float* vm = wmax + rt * 4 * HC + h0;
-        float alpha[HH];
+        float alpha[NH];
         bool rescale = false;
 #pragma unroll
-        for (int h = 0; h < HH; ++h) {
+        for (int j = 0; j < NH; ++j) {
+          const int h = 8 * (j >> 1) + c0 + (j & 1);
           const float tm = fmaxf(fmaxf(vm[h], vm[HC + h]), fmaxf(vm[2 * HC + h], vm[3 * HC + h]));
-          const float mn = fmaxf(m_run[h], tm);
-          alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m_run[h] - mn);
-          rescale |= alpha[h] != 1.0f;
-          m_run[h] = mn;
-          l_part[h] *= alpha[h];
+          const float mn = fmaxf(m_run[j], tm);
+          alpha[j] = (mn == -INFINITY) ? 1.0f : exp2f(m_run[j] - mn);
+          rescale |= alpha[j] != 1.0f;
+          m_run[j] = mn;
+          l_part[j] *= alpha[j];
         }
         // every warp takes the same branch: the barrier below is reached by all or none
         const bool rescale_any = softmax_bar_or(rescale);
@@ -789,6 +827,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             if (lane == 0 && !landed) fail();
             break;
           }
+          // every lane scales all HH heads of its O^T rows: head h's factor is
+          // held by lane (h % 8) / 2 in slot 2 (h / 8) + (h & 1)
+          float alpha_all[HH];
+#pragma unroll
+          for (int h = 0; h < HH; ++h)
+            alpha_all[h] = __shfl_sync(0xffffffffu, alpha[2 * (h >> 3) + (h & 1)], (h & 7) >> 1);
           tc_fence_after();
 #pragma unroll
           for (int mt = 0; mt < 4; ++mt) {
@@ -796,17 +840,19 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             o_load(mt, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < kOLoad; ++c) o[c] *= alpha[c % HH];
+            for (int c = 0; c < kOLoad; ++c) o[c] *= alpha_all[c % HH];
             o_store(mt, o);
           }
           tmem_wait_st();
         }
       }
-      float p[HH];
+      float p[NR];
 #pragma unroll
-      for (int h = 0; h < HH; ++h) {
-        p[h] = live ? exp2f(s[h] - m_run[h]) : 0.0f;
-        l_part[h] += p[h];
+      for (int r = 0; r < NR; ++r) {
+        const int q = q0 + 8 * ((r >> 1) & 1);
+        const int j = 2 * (r >> 2) + (r & 1);
+        p[r] = q < n_tok ? exp2f(s[r] - m_run[j]) : 0.0f;
+        l_part[j] += p[r];
       }
       if (present) {
         uint8_t* ring_t = smem + L::kRing + rt * kTcTileBytes;
@@ -818,16 +864,14 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           *reinterpret_cast<uint4*>(ring_t + pl * kTcPlaneBytes + (r >> 3) * 1024 + (r & 7) * 128 +
                                     ((ch ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
         }
-        if (lane < 16) {
-          uint8_t* ptb = smem + L::kPt + rt * L::kPtBytes;
-          const int col = 16 * w + lane;
+        uint8_t* ptb = smem + L::kPt + rt * L::kPtBytes;
 #pragma unroll
-          for (int h = 0; h < HH; ++h) {
-            __nv_bfloat16 hi, lo;
-            split_bf16(p[h], hi, lo);
-            *reinterpret_cast<__nv_bfloat16*>(ptb + sw128(h0 + h, col)) = hi;
-            *reinterpret_cast<__nv_bfloat16*>(ptb + sw128(HC + h0 + h, col)) = lo;
-          }
+        for (int r = 0; r < NR; ++r) {
+          const int row = h0 + 8 * (r >> 2) + c0 + (r & 1), col = 16 * w + q0 + 8 * ((r >> 1) & 1);
+          __nv_bfloat16 hi, lo;
+          split_bf16(p[r], hi, lo);
+          *reinterpret_cast<__nv_bfloat16*>(ptb + sw128(row, col)) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(ptb + sw128(HC + row, col)) = lo;
         }
         fence_proxy_async_smem();
       }
@@ -844,11 +888,11 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < HH; ++h) {
-          float v = l_part[h];
+        for (int j = 0; j < NH; ++j) {
+          float v = l_part[j];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0) lred[w * HC + h0 + h] = v;
+          for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (q0 == 0) lred[w * HC + h0 + 8 * (j >> 1) + c0 + (j & 1)] = v;
         }
         softmax_bar_or(false);
         const AttnKey kk = P.keys[static_cast<int64_t>(t_layer) * P.n_keys + t_key];
@@ -865,15 +909,20 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           for (int h = 0; h < HH; ++h)
             blk[(h0 + h) * kMlaLatentDims + d] = kPvParts == 1 ? o[h] + o[HH + h] : o[h];
         }
-        if (w == 0 && lane < HH) {
+        if (w == 0) {
+          // lane h < HH writes head h0 + h: its running max from the lane that holds it
           float mv = 0.0f;
 #pragma unroll
-          for (int h = 0; h < HH; ++h)
-            if (lane == h) mv = m_run[h];
-          const volatile float* vl = lred + h0;
-          blk[HC * kMlaLatentDims + h0 + lane] = mv;
-          blk[HC * kMlaLatentDims + HC + h0 + lane] =
-              (vl[lane] + vl[HC + lane]) + (vl[2 * HC + lane] + vl[3 * HC + lane]);
+          for (int h = 0; h < HH; ++h) {
+            const float v = __shfl_sync(0xffffffffu, m_run[2 * (h >> 3) + (h & 1)], (h & 7) >> 1);
+            if (lane == h) mv = v;
+          }
+          if (lane < HH) {
+            const volatile float* vl = lred + h0;
+            blk[HC * kMlaLatentDims + h0 + lane] = mv;
+            blk[HC * kMlaLatentDims + HC + h0 + lane] =
+                (vl[lane] + vl[HC + lane]) + (vl[2 * HC + lane] + vl[3 * HC + lane]);
+          }
         }
         tc_fence_before();
       }
