@@ -68,18 +68,17 @@ constexpr int kTcStageBytes = 16 * 128;                    // one stage's rows i
 constexpr float kTcLazy = 8.0f;
 // warps 0-7 softmax (warp w: TMEM lane quadrant w % 4, heads of half w / 4),
 // then a producer, the score-product issuer (it also holds the TMEM
-// allocation), the query warp, the value-product issuer and, for 16 heads, a
-// second score-product issuer, two more producers and a second value-product
+// allocation), the query warp, the value-product issuer, a second
+// score-product issuer, two more producers and a second value-product
 // issuer.  A thread issuing alone puts out a small tcgen05.mma about every
 // 55-70 cycles whatever its shape (a converged warp issuing from its elected
 // lane, about every 29), and one warp issues TMA copies one lane after
-// another (~35 ns each), so both are spread over warps; 32 heads need the
-// registers the extra warps would take.
+// another (~35 ns each), so both are spread over warps.
 constexpr int kTcSoftmaxWarps = 8;
 constexpr int kTcProducer = 8, kTcMma = 9, kTcQuery = 10, kTcPv = 11, kTcMma2 = 12, kTcProducer2 = 13, kTcPv2 = 15;
-__host__ __device__ constexpr int tc_score_issuers(int hc) { return hc == 16 ? 2 : 1; }
-__host__ __device__ constexpr int tc_producers(int hc) { return hc == 16 ? 3 : 1; }
-__host__ __device__ constexpr int tc_value_issuers(int hc) { return hc == 16 ? 2 : 1; }
+__host__ __device__ constexpr int tc_score_issuers(int) { return 2; }
+__host__ __device__ constexpr int tc_producers(int) { return 3; }
+__host__ __device__ constexpr int tc_value_issuers(int) { return 2; }
 __host__ __device__ constexpr int tc_threads(int hc) {
   return 32 * (9 + tc_score_issuers(hc) + tc_producers(hc) + tc_value_issuers(hc));
 }
@@ -149,17 +148,6 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
-// one thread issues / commits
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(id), "r"(acc ? 1u : 0u));
-}
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
 // Both run on a whole converged warp and issue from its elected lane (the
 // same lane every time, as the commit tracks that thread's products).  Issued
 // this way, from operands the warp holds in common, a 64 x 16 product goes out
@@ -175,31 +163,6 @@ __device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
-}
-// the issue form of a role: E, the whole warp and its elected lane; else one thread
-template <bool E>
-__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
-  if constexpr (E) {
-    tc_mma_elect(d, a, b, id, acc);
-  } else {
-    tc_mma(d, a, b, id, acc);
-  }
-}
-template <bool E>
-__device__ __forceinline__ void commit(uint64_t* bar) {
-  if constexpr (E) {
-    tc_commit_elect(bar);
-  } else {
-    tc_commit(bar);
-  }
-}
-template <bool E>
-__device__ __forceinline__ bool agree(bool ok) {
-  if constexpr (E) {
-    return __all_sync(0xffffffffu, ok);
-  } else {
-    return ok;
-  }
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -341,12 +304,6 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   constexpr int kSI = tc_score_issuers(HC);
   constexpr int kNP = tc_producers(HC);
   constexpr int kVI = tc_value_issuers(HC);
-  // How each issuer role issues (see the MMA issuers below).  Measured on
-  // the 61-layer, 65,536-position workload: at 16 heads the elected-lane form
-  // for both roles is the fastest (1.064 ms; score only 1.080, value only
-  // 1.138), at 32 heads the single-thread form for both (1.656 ms; 1.699 and
-  // 1.784 with either role elected, slower still with both).
-  constexpr bool kElectS = HC == 16, kElectV = HC == 16;
   // the latent score accumulates in NP partial sums (k-step mod NP; with two
   // score issuers, one each)
   constexpr int NP = 2;
@@ -626,15 +583,13 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     }
   } else if ((warp == kTcMma || warp == kTcMma2 || warp == kTcPv || warp == kTcPv2) && has_work) {
     // --------------------------------------------------- MMA issuers
-    // A role with E set runs its loop on the whole warp (the waits, the
-    // operand addresses) and issues the products and commits from the elected
-    // lane; otherwise lane 0 alone runs it.
+    // Each issuer runs its loop on the whole warp (the waits, the operand
+    // addresses) and issues the products and commits from the elected lane.
     const uint32_t ring = base_u32 + L::kRing;
     // A descriptor is affine in its start address (start / 16 sits in the
     // low bits, and no start here reaches 256 KB), so each product builds its
     // base descriptors once and steps them by constants.
-    if ((warp == kTcMma || warp == kTcMma2) && (kElectS || lane == 0)) {
-      constexpr bool E = kElectS;
+    if (warp == kTcMma || warp == kTcMma2) {
       // S of tile i once its rows and query operands are in and its TMEM
       // buffer is free (the softmax of tile i - 2 has written P, so it is
       // done reading that buffer).  With two issuers the first takes the even
@@ -647,7 +602,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         const bool ok = wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag, spins) &&
                         wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins) &&
                         (i < 2 || wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag, spins));
-        if (!agree<E>(ok)) {
+        if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) fail();
           break;
         }
@@ -658,21 +613,20 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
 #pragma unroll
         for (int k2 = 0; k2 < 32 / kSI; ++k2) {
           const int ks = kSI * k2 + par;
-          mma<E>(d + (ks % NP) * HC, da + (((ks >> 2) * kTcPlaneBytes + (ks & 3) * 32) >> 4),
-              dq + (((ks >> 2) * L::kQnPlane + (ks & 3) * 32) >> 4), kIdS, ks >= NP);
+          tc_mma_elect(d + (ks % NP) * HC, da + (((ks >> 2) * kTcPlaneBytes + (ks & 3) * 32) >> 4),
+                       dq + (((ks >> 2) * L::kQnPlane + (ks & 3) * 32) >> 4), kIdS, ks >= NP);
         }
         if (par == 0) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma<E>(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);
+            tc_mma_elect(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);
         }
-        commit<E>(&s_full[rt]);
+        tc_commit_elect(&s_full[rt]);
         if (flags & kTcEnd) break;
       }
-      commit<E>(&done[par]);
+      tc_commit_elect(&done[par]);
       mbar_wait_bounded(&done[par], 0);
-    } else if ((warp == kTcPv || warp == kTcPv2) && (kElectV || lane == 0)) {
-      constexpr bool E = kElectV;
+    } else {
       // O^T += V^T P^T of tile i once its P is written; its metadata stays in
       // the slot until this product ends.  With two issuers each takes two of
       // the four latent M-tiles.
@@ -680,7 +634,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const int vi = warp == kTcPv ? 0 : 1;
       for (int i = 0;; ++i) {
         const int rt = i & 1;
-        if (!agree<E>(wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag, spins))) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&p_full[rt], (i >> 1) & 1, abort_flag, spins))) {
           if (lane == 0) fail();
           break;
         }
@@ -701,16 +655,17 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
 #pragma unroll
             for (int m4 = 0; m4 < 4 / kVI; ++m4) {
               const int mt = vi * (4 / kVI) + m4;
-              mma<E>(tmem + kTcOCol + mt * kTcOColsPerTile, dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4),
-                  bd, kIdPV, !(first && w == 0 && part == 0));
+              tc_mma_elect(tmem + kTcOCol + mt * kTcOColsPerTile,
+                           dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4), bd, kIdPV,
+                           !(first && w == 0 && part == 0));
             }
           }
         }
-        commit<E>(&empty[rt]);
-        commit<E>(&pv_done[rt]);
+        tc_commit_elect(&empty[rt]);
+        tc_commit_elect(&pv_done[rt]);
         if (t_flags & kTcEnd) break;
       }
-      commit<E>(&done[2 + vi]);
+      tc_commit_elect(&done[2 + vi]);
       mbar_wait_bounded(&done[2 + vi], 0);
     }
   } else if (warp < kTcSoftmaxWarps && has_work) {
