@@ -75,7 +75,7 @@ constexpr float kTcLazy = 8.0f;
 // lane, about every 29), and one warp issues TMA copies one lane after
 // another (~35 ns each), so both are spread over warps.
 constexpr int kTcSoftmaxWarps = 8;
-constexpr int kTcProducer = 8, kTcMma = 9, kTcQuery = 10, kTcPv = 11, kTcMma2 = 12, kTcProducer2 = 13, kTcPv2 = 15;
+constexpr int kTcProducer = 8, kTcMma = 9, kTcQuery = 10, kTcPv = 11, kTcMma2 = 12, kTcPv2 = 13, kTcProducer2 = 14;
 __host__ __device__ constexpr int tc_score_issuers(int) { return 2; }
 __host__ __device__ constexpr int tc_producers(int) { return 3; }
 __host__ __device__ constexpr int tc_value_issuers(int) { return 2; }
@@ -708,48 +708,53 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const uint32_t ph = (i >> 1) & 1;
       // every softmax warp reaches each barrier reduction below, so a wait
       // that runs out in one warp ends all eight together
-      const bool got = wait_or_abort(&full[rt], ph, abort_flag, spins) && wait_or_abort(&s_full[rt], ph, abort_flag, spins);
-      if (softmax_bar_or(!got)) {
-        if (lane == 0 && !got) fail();
-        break;
-      }
-      tc_fence_after();
+      const bool got = __all_sync(0xffffffffu, wait_or_abort(&full[rt], ph, abort_flag, spins) &&
+                                                    wait_or_abort(&s_full[rt], ph, abort_flag, spins));
       // this warp's fields of the tile record (read now: the slot's record is
-      // replaced once the tile's value product has finished)
+      // replaced once the tile's value product has finished; after a wait
+      // that ran out they are not used) and its scores
       const TcTile& tr = tiles[rt];
       const int t_flags = tr.flags, t_layer = tr.layer, t_key = tr.key;
       const bool present = w < tr.ns;
       const int n_tok = present ? tr.n_tok[w] : 0;
       const int entry = present ? tr.entry[w] : 0;
       const int sink = present ? tr.sink[w] : 0;
-      if (t_flags & kTcFirst) {
-#pragma unroll
-        for (int j = 0; j < NH; ++j) {
-          m_run[j] = -INFINITY;
-          l_part[j] = 0.0f;
-        }
-      }
-      float sp[NP][NR], rr[2 * NR];  // latent partial sums; the rope hi then lo columns
-      const uint32_t sc = tl + rt * kTcSCols + h0;
-      tmem_ld16x256<2 * NG>(sc + kRopeCol + entry * 2 * HC + h0, rr);
-#pragma unroll
-      for (int pp = 0; pp < NP; ++pp) tmem_ld16x256<NG>(sc + pp * HC, sp[pp]);
-      tmem_wait_ld();
       float s[NR];
       bool need = false;
+      if (got) {
+        tc_fence_after();
+        if (t_flags & kTcFirst) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const int q = q0 + 8 * ((r >> 1) & 1);
-        const bool live = q < n_tok;
-        const float bias = (live && ((sink >> q) & 1)) ? P.sink_log2 : 0.0f;
-        float v = sp[0][r];
+          for (int j = 0; j < NH; ++j) {
+            m_run[j] = -INFINITY;
+            l_part[j] = 0.0f;
+          }
+        }
+        float sp[NP][NR], rr[2 * NR];  // latent partial sums; the rope hi then lo columns
+        const uint32_t sc = tl + rt * kTcSCols + h0;
+        tmem_ld16x256<2 * NG>(sc + kRopeCol + entry * 2 * HC + h0, rr);
 #pragma unroll
-        for (int pp = 1; pp < NP; ++pp) v += sp[pp][r];
-        s[r] = live ? ((v + rr[r]) + rr[NR + r]) * P.scale_log2 + bias : -INFINITY;
-        need |= s[r] > m_run[2 * (r >> 2) + (r & 1)] + kTcLazy;
+        for (int pp = 0; pp < NP; ++pp) tmem_ld16x256<NG>(sc + pp * HC, sp[pp]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          const int q = q0 + 8 * ((r >> 1) & 1);
+          const bool live = q < n_tok;
+          const float bias = (live && ((sink >> q) & 1)) ? P.sink_log2 : 0.0f;
+          float v = sp[0][r];
+#pragma unroll
+          for (int pp = 1; pp < NP; ++pp) v += sp[pp][r];
+          s[r] = live ? ((v + rr[r]) + rr[NR + r]) * P.scale_log2 + bias : -INFINITY;
+          need |= s[r] > m_run[2 * (r >> 2) + (r & 1)] + kTcLazy;
+        }
       }
-      // does any position raise a head's running max?
-      if (softmax_bar_or(need)) {
+      // One reduction carries both rare events, a wait that ran out and a
+      // score that raises a head's running max; a second one tells them apart.
+      if (softmax_bar_or(!got || need)) {
+        if (softmax_bar_or(!got)) {
+          if (lane == 0 && !got) fail();
+          break;
+        }
         float* wm = wmax + (rt * 4 + w) * HC + h0;
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
