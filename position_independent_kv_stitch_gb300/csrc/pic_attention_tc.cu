@@ -418,7 +418,9 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
               if (!((used >> x) & 1u)) e = x;
           }
           if (e < 0) continue;  // more distinct deltas than entries: the tile ends here
-          ent_delta[e] = c_delta;
+#pragma unroll
+          for (int x = 0; x < NE; ++x)
+            if (x == e) ent_delta[x] = c_delta;  // a constant index keeps the entries in registers
           ent_valid |= 1u << e;
           fresh |= 1u << e;
         }
