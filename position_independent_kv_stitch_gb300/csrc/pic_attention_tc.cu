@@ -18,21 +18,23 @@
 // A tile is up to four plan stages (16 consecutive positions each, read from
 // consecutive rows of one source, one delta) of one (layer, key): 64
 // positions, the M of the score product.  Per tile, with warps by role:
-//   * the producer forms the tile (its delta entries, whether it opens or
-//     closes its key) and loads its rows into a ring of two tiles with 3-D
-//     TMA tile copies, one per 64-dim plane (128-byte swizzle) and per run
-//     of stages that read consecutive rows (boxes of 16 to 64 rows);
+//   * three producer warps form the tile (its delta entries, whether it
+//     opens or closes its key) and load its rows into a ring of two tiles
+//     with 3-D TMA tile copies, one per 64-dim plane (128-byte swizzle) and
+//     per run of stages that read consecutive rows (boxes of 16 to 64 rows);
 //   * the query warp writes the query operands: q_nope on a key change, and
 //     for each new delta of the tile R(-delta) q_rope as bf16 hi and lo rows
 //     (NE delta entries, so stages with different deltas share a tile);
-//   * score issuers (one warp each) issue S = rows [q_nope | rope parts]^T
-//     into TMEM: M = 64, 32 k-steps over the latent, 4 over the rope plane;
-//   * a value issuer issues O^T += V^T P^T once P is written: M = 128
-//     latent dims (four M-tiles), N = 32 (16 heads: P's hi and lo rows side
-//     by side; 32 heads: each part in turn), K = the 16 positions of a
-//     stage; V^T is the same shared planes read as an MN-major operand;
+//   * two score issuers (one warp each) issue S = rows [q_nope | rope
+//     parts]^T into TMEM: M = 64, 32 k-steps over the latent (even and odd
+//     into separate partial sums), 4 over the rope plane;
+//   * two value issuers issue O^T += V^T P^T once P is written: M = 128
+//     latent dims (four M-tiles, two each), N = 32 (16 heads: P's hi and lo
+//     rows side by side; 32 heads: each part in turn), K = the 16 positions
+//     of a stage; V^T is the same shared planes read as an MN-major operand;
 //   * softmax warps 0-7: warp w owns stage w's positions (TMEM lanes
-//     32 (w % 4) .. + 15 of the M = 64 scores) for half of the heads.  It
+//     32 (w % 4) .. + 15 of the M = 64 scores) for half of the heads, read
+//     with the 16x256b shape so that each thread holds two positions.  It
 //     adds the nope partial sums and its delta's hi and lo rope columns,
 //     keeps a running max per head that is raised only when a score passes
 //     it by more than kTcLazy (log2 units; O and l are then rescaled), writes
@@ -129,6 +131,7 @@ struct TcLayout {
   static constexpr int kAlloc = kTotal + 1024;                  // room to align the base
   static_assert(kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 && kPtBytes % 1024 == 0,
                 "operands sit on 1024-byte swizzle atoms");
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
 // byte offset of element (row r, col c) of a 128B-swizzled tile of 128-byte rows
