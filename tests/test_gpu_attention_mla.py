@@ -42,7 +42,7 @@ def _check_variant(ctx, kernel):
     assert pic.pic_kernel_variant(ctx, 2) == want
 
 
-def _setup(pairing, L, seed, rep=1):
+def _setup(pairing, L, seed, rep=1, row_scale=None):
     bs, nb = 16, 200 + 120 * (rep - 1)
     m = W.Model("attn-mla", "mla", L, 1, ROW, ROPE, LATENT, pairing, 1e4, bs)
     ctx = pic.create_from_spec(pic.model_spec_from(m), nb)
@@ -60,7 +60,10 @@ def _setup(pairing, L, seed, rep=1):
     sources[bid] = ("blocks", blocks)
     g = torch.Generator().manual_seed(seed)
     P = offs[-1] + _POOL_LENS[-1]
-    pool = torch.randn((L, P, ROW), generator=g).to(torch.bfloat16)
+    pool = torch.randn((L, P, ROW), generator=g)
+    for c, f in (row_scale or {}).items():  # chunk index -> factor on its pool rows
+        pool[:, offs[c]:offs[c] + _POOL_LENS[c]] *= f
+    pool = pool.to(torch.bfloat16)
     cache = torch.randn((L, nb, bs, ROW), generator=g).to(torch.bfloat16)
 
     def positions(chunks, start, gaps):
@@ -161,6 +164,25 @@ def test_fused_mla_attention_matches_oracle(pairing, H, L, bias_value, rep):
     try:
         q, out, lse, scale = _attend(S, H, pic.PIC_ATTEND_FUSED, bias_value)
         _check_against_oracle(S, q, out, lse, scale, bias_value, 2e-3)
+    finally:
+        pic.pic_destroy(S["ctx"])
+
+
+@pytest.mark.parametrize("H", [16, 32])
+def test_mla_running_max_rises_in_a_later_tile(H):
+    """Rows of chunks 6 and 11 scaled by 6 and of chunks 9, 3 and 8 by 1/4,
+    in contexts 16 times the base case (about 1,700 stages, so each of the
+    152 CTAs takes about 11 and several tiles of a key): where a CTA's range
+    runs from small rows into scaled ones, a later tile's scores pass the
+    running max by far more than the lazy threshold (8 in log2 units), and
+    the O and l already accumulated are rescaled (about 150 such tiles in a
+    CPU model of the split; random rows of one scale never get there).
+    Outputs reach about 6 in magnitude."""
+    S = _setup("interleaved", 1, seed=12, rep=16, row_scale={6: 6.0, 11: 6.0, 9: 0.25, 3: 0.25, 8: 0.25})
+    try:
+        q, out, lse, scale = _attend(S, H, pic.PIC_ATTEND_FUSED, -15.0)
+        assert np.abs(out).max() > 2.0  # the scaled rows dominate
+        _check_against_oracle(S, q, out, lse, scale, -15.0, 4e-3)
     finally:
         pic.pic_destroy(S["ctx"])
 
