@@ -213,7 +213,9 @@ pic_status pic_register_chunk(pic_ctx* ctx, const uint8_t* key, int64_t pool_tok
  * ceil(num_tokens / block_size), holds its tokens [j*bs, (j+1)*bs) in rows
  * 0.. of the block (the last block partly), keys rotated for position
  * base_pos.  The blocks must be free in the allocator; they are taken out of
- * it and belong to the chunk until pic_unregister_chunk.
+ * it and belong to the chunk until pic_unregister_chunk.  A chunk needing
+ * more blocks than the cache holds fails with PIC_ERR_RANGE before blocks[]
+ * is read.
  *
  * Such a chunk can be served to a request without moving its values: the
  * EPIC runtime ([EPIC] "Algorithmic Architecture", runtime figure step 1
@@ -395,7 +397,8 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_layer
  * Carve-Out).  idx_out / indptr_out are host arrays (indptr_out has n_req + 1
  * entries); *count receives the total even when capacity is too small
  * (PIC_ERR_CAPACITY, nothing written to idx_out then).  idx_out may be NULL to
- * query the count.
+ * query the count.  A total above 2^31 - 1 entries (the CSR offsets are
+ * int32) fails with PIC_ERR_RANGE, *count still set, nothing written.
  */
 pic_status pic_recompute_indices(const pic_plan* const* plans, int32_t n_req, int32_t* idx_out,
                                  int32_t* indptr_out, int64_t capacity, int64_t* count);

@@ -538,6 +538,9 @@ pic_status check_stitch_args(pic_ctx* ctx, const pic_plan* const* plans, int32_t
     return fail(ctx, PIC_ERR_RANGE, "cache layer stride smaller than num_cache_blocks * block_size rows");
   int64_t n_rec = 0;
   for (int32_t r = 0; r < n_req; ++r) n_rec += plans[r]->n_recompute;
+  if (d_ridx && n_rec > std::numeric_limits<int32_t>::max())
+    return fail(ctx, PIC_ERR_RANGE, "recompute list of %lld entries: CSR offsets are int32",
+                static_cast<long long>(n_rec));
   if (d_ridx && n_rec > recompute_capacity)
     return fail(ctx, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
                 static_cast<long long>(n_rec), static_cast<long long>(recompute_capacity));
@@ -982,8 +985,13 @@ pic_status pic_register_chunk_blocks(pic_ctx* ctx, const uint8_t* key, const int
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
   if (!key || !chunk_id || !blocks) return fail(ctx, PIC_ERR_INVALID_ARG, "null key, blocks or chunk_id");
   if (num_tokens <= 0 || base_pos < 0) return fail(ctx, PIC_ERR_RANGE, "num_tokens must be > 0 and base_pos >= 0");
-  const int32_t bs = ctx->model.block_size;
-  const int32_t nb = (num_tokens + bs - 1) / bs;
+  const int64_t bs = ctx->model.block_size;
+  const int64_t nb64 = (static_cast<int64_t>(num_tokens) + bs - 1) / bs;
+  // Checked before blocks[] is read: a chunk cannot hold more blocks than the cache has.
+  if (nb64 > ctx->num_cache_blocks)
+    return fail(ctx, PIC_ERR_RANGE, "chunk of %d tokens needs %lld blocks, the cache has %d", num_tokens,
+                static_cast<long long>(nb64), ctx->num_cache_blocks);
+  const int32_t nb = static_cast<int32_t>(nb64);
   std::vector<int32_t> ids(blocks, blocks + nb);
   std::array<uint8_t, PIC_KEY_BYTES> k;
   std::memcpy(k.data(), key, PIC_KEY_BYTES);
@@ -1228,6 +1236,9 @@ pic_status pic_recompute_indices(const pic_plan* const* plans, int32_t n_req, in
     total += plans[r]->n_recompute;
   }
   if (count) *count = total;
+  if (total > std::numeric_limits<int32_t>::max())
+    return fail(nullptr, PIC_ERR_RANGE, "recompute list of %lld entries: CSR offsets are int32",
+                static_cast<long long>(total));
   if (!idx_out) return ok(nullptr);
   if (total > capacity) return fail(nullptr, PIC_ERR_CAPACITY, "recompute list has %lld entries, capacity %lld",
                                     static_cast<long long>(total), static_cast<long long>(capacity));

@@ -210,6 +210,35 @@ def test_explicit_positions_total_tokens_and_recompute():
         pic.pic_destroy(ctx)
 
 
+def test_recompute_list_beyond_int32_offsets_is_refused():
+    # One request of 2^30 + 1 tokens whose chunk (at position 1) is all
+    # recompute tokens; the same plan listed three times holds 3 * 2^30
+    # entries, more than the int32 CSR offsets address.
+    bs, n = 256, 2**30
+    nb = n // bs + 1
+    ctx = pic.pic_create(pic.PIC_KIND_GQA, 1, 1, 64, 64, 0, pic.PIC_PAIRING_NEOX_HALF, bs, 1e4, nb)
+    try:
+        cid, _ = pic.pic_register_chunk(ctx, W.chunk_key("big", 0), 0, n)
+        plan, _ = pic.pic_build_block_table(ctx, [cid], nb, start_pos=1, k_nonleading=n)
+        assert pic.pic_plan_info(plan)["num_recompute"] == n
+        count = ctypes.c_int64()
+        one = pic._plan_array([plan])
+        assert pic.load().pic_recompute_indices(one, 1, None, None, 0, ctypes.byref(count)) == 0
+        assert count.value == n
+        with pytest.raises(PicError) as e:
+            pic.pic_recompute_indices([plan] * 3)
+        assert e.value.status_name == "PIC_ERR_RANGE"
+        # the stitch's device CSR has the same limit; refused on the host
+        # (fake, aligned pointers that never reach a launch)
+        good = ctypes.c_void_p(0x10000)
+        st = pic.load().pic_stitch(ctx, pic._plan_array([plan] * 3), 3, good, good, 0, good, good, 0, good, nb,
+                                   good, good, 1 << 40, good, 1 << 40, None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_RANGE"
+        pic.pic_free_request(ctx, plan)
+    finally:
+        pic.pic_destroy(ctx)
+
+
 def test_stitch_argument_checks_need_no_gpu():
     """Validation fails before anything is enqueued (no GPU needed to see it).
     Every call here must fail a host check: the pointers are fake."""

@@ -125,6 +125,12 @@ def test_register_blocks_validation():
         with pytest.raises(PicError) as e:        # listed twice
             pic.pic_register_chunk_blocks(ctx, W.chunk_key("v", 3), [5, 5], 6)
         assert e.value.status_name == "PIC_ERR_INVALID_ARG"
+        # more blocks than the cache holds (9 > 8; and 2^31 - 1 tokens, whose
+        # block count once overflowed int32): refused before blocks[] is read
+        for n in (33, 2**31 - 1):
+            with pytest.raises(PicError) as e:
+                pic.pic_register_chunk_blocks(ctx, W.chunk_key("v", 4), [6], n)
+            assert e.value.status_name == "PIC_ERR_RANGE"
         # same key, same blocks: the existing id
         assert pic.pic_register_chunk_blocks(ctx, W.chunk_key("v", 0), [1, 2], 8) == (0, False)
         # the chunk's blocks are out of the allocator: a 6-block request gets 0, 3..7
