@@ -1335,6 +1335,8 @@ pic_status pic_rerotate_inplace(pic_ctx* ctx, void* k_cache, int64_t cache_ls,
     if (g.start_pos < 0 || g.num_tokens < 0) return fail(ctx, PIC_ERR_RANGE, "segs[%d] has a negative range", i);
     if (static_cast<int64_t>(g.start_pos) + g.num_tokens > static_cast<int64_t>(max_blocks) * bs)
       return fail(ctx, PIC_ERR_RANGE, "segs[%d] ends past the block table", i);
+    if (static_cast<int64_t>(g.start_pos) + g.num_tokens > std::numeric_limits<int32_t>::max())
+      return fail(ctx, PIC_ERR_RANGE, "segs[%d] ends past int32 positions", i);
     if (g.delta > PIC_MAX_ABS_DELTA || g.delta < -PIC_MAX_ABS_DELTA)
       return fail(ctx, PIC_ERR_RANGE, "segs[%d].delta exceeds 2^24 - 1", i);
   }

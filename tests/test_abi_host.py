@@ -288,6 +288,10 @@ def test_stitch_argument_checks_need_no_gpu():
         segs = pic._shift_array([(0, 60, 5, 5)])  # ends past 4 blocks of 16
         st = L.pic_rerotate_inplace(ctx, good, ls, good, 1, 4, segs, 1, good, 1 << 20, None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_RANGE"
+        # within a (claimed) 2^27-block table, but ending past int32 positions
+        segs = pic._shift_array([(0, 2**31 - 8, 16, 5)])
+        st = L.pic_rerotate_inplace(ctx, good, ls, good, 1, 2**27, segs, 1, good, 1 << 20, None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_RANGE"
     finally:
         pic.pic_destroy(ctx)
 
