@@ -1488,7 +1488,7 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   if (n_req <= 0 || !plans) return fail(ctx, PIC_ERR_INVALID_ARG, "no requests");
   for (int32_t r = 0; r < n_req; ++r)
     if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
-  if (layer_begin < 0 || num_layers <= 0 || layer_begin + num_layers > m.num_layers)
+  if (layer_begin < 0 || num_layers <= 0 || static_cast<int64_t>(layer_begin) + num_layers > m.num_layers)
     return fail(ctx, PIC_ERR_RANGE, "layer range outside the model");
   if (!q || !out || !d_ws || !k_cache || (!mla && !v_cache))
     return fail(ctx, PIC_ERR_INVALID_ARG, "null q, out, cache or workspace");

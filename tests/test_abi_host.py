@@ -296,6 +296,40 @@ def test_stitch_argument_checks_need_no_gpu():
         pic.pic_destroy(ctx)
 
 
+def test_attend_argument_checks_need_no_gpu():
+    """pic_attend_decode refuses bad arguments before any CUDA call (fake,
+    aligned pointers that never reach a launch)."""
+    ctx = _gqa_ctx(nb=8)  # 2 layers, 2 KV heads of 128 dims
+    L = pic.load()
+    try:
+        pic.pic_register_chunk(ctx, W.chunk_key("a", 0), 0, 20)
+        plan, _ = pic.pic_build_block_table(ctx, [0], 4)
+        arr = pic._plan_array([plan])
+        g, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+        ls = 8 * 16 * 512
+
+        def call(source=pic.PIC_ATTEND_FUSED, q=g, hq=4, lb=0, nl=2, plans=arr, n=1):
+            st = L.pic_attend_decode(ctx, plans, n, source, q, hq, 0.1, 0.0, g, g, ls, g, g, ls, lb, nl,
+                                     g, None, g, 1 << 20, None)
+            return pic.STATUS_NAMES[st]
+
+        assert call(source=7) == "PIC_ERR_INVALID_ARG"
+        assert call(hq=6) == "PIC_ERR_UNSUPPORTED"          # 3 query heads per KV head
+        assert call(hq=3) == "PIC_ERR_INVALID_ARG"          # not a multiple of the KV heads
+        assert call(lb=1, nl=2) == "PIC_ERR_RANGE"
+        assert call(lb=2**31 - 1, nl=1) == "PIC_ERR_RANGE"  # the sum once wrapped past int32
+        assert call(nl=0) == "PIC_ERR_RANGE"
+        assert call(q=None) == "PIC_ERR_INVALID_ARG"
+        assert call(q=odd) == "PIC_ERR_ALIGNMENT"
+        assert call(n=0) == "PIC_ERR_INVALID_ARG"
+        empty, _ = pic.pic_build_block_table(ctx, [], 4)
+        assert call(plans=pic._plan_array([empty])) == "PIC_ERR_RANGE"  # no context to attend
+        pic.pic_free_request(ctx, empty)
+        pic.pic_free_request(ctx, plan)
+    finally:
+        pic.pic_destroy(ctx)
+
+
 def test_workspace_sizes_grow_with_runs():
     ctx = _gqa_ctx(nb=64)
     try:
