@@ -57,6 +57,24 @@ def test_llama3_invariants():
     assert np.all(np.diff(sc) <= 0)
 
 
+def test_llama3_continuous_at_both_regime_boundaries():
+    """The blend meets the kept frequencies at wavelength orig/high and the
+    divided ones at orig/low; between them theta'/theta is affine in theta
+    (s is linear in orig/lambda).  A swapped low/high, a sign slip in s or a
+    blend weighted the wrong way round breaks one of these."""
+    orig, factor, low, high = 8192, 8.0, 1.0, 4.0
+    for lam, left, right in ((orig / high, 1.0, 1.0), (orig / low, 1.0 / factor, 1.0 / factor)):
+        for eps in (1e-6, 1e-9):
+            th = np.array([2 * math.pi / (lam * (1 - eps)), 2 * math.pi / (lam * (1 + eps))])
+            sc = oracle.llama3_inv_freq(th, factor, low, high, orig) / th
+            assert abs(sc[0] - left) < 10 * eps and abs(sc[1] - right) < 10 * eps
+    th = 2 * math.pi / np.linspace(orig / high * 1.01, orig / low * 0.99, 9)
+    ratio = oracle.llama3_inv_freq(th, factor, low, high, orig) / th
+    slope = np.diff(ratio) / np.diff(th)
+    np.testing.assert_allclose(slope, slope[0], rtol=1e-9)
+    assert slope[0] > 0  # higher frequency, less division
+
+
 # ------------------------------------------------------------ rotation basics
 
 @pytest.mark.parametrize("pairing", [NEOX_HALF, INTERLEAVED])
