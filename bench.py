@@ -756,8 +756,16 @@ def main():
                         wl.requests, wl.k_nonleading, wl.k_leading, wl.new_pos)
 
     if args.impl == "reference":
-        if rank == 0:
-            run_reference(args, wl)
+        if rank != 0:
+            return
+        if args.mode != "stitch":
+            # only the stitch has a reference arm; every mode's own line
+            # carries an oracle timing in its cpu_baseline field
+            print(json.dumps({"impl": "reference", "unavailable": f"only --mode stitch has a reference arm (the oracle's "
+                              f"stitch); the --mode {args.mode} line carries an oracle timing in cpu_baseline"}),
+                  flush=True)
+            return
+        run_reference(args, wl)
         return
     if args.mode == "cdc":
         run_cdc(args)
