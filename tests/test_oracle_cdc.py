@@ -154,3 +154,33 @@ def test_s1_windows(b, e):
     assert covered == list(range(b, e))
     assert all(hi - lo == 128 for lo, hi in w[:-1])
     assert all(lo == b + 128 * k for k, (lo, _) in enumerate(w))
+
+
+def test_chunk_document_extreme_thresholds():
+    """Threshold 0 never cuts: one chunk, the document's own XXH64 (checked
+    against the system library when it is installed).  Threshold 2^64 - 1
+    cuts after every token whose hash is below it (all but a 2^-64 chance):
+    one-token chunks.  An empty document has no chunks."""
+    gear = _gear()
+    doc = [int(t) for t in W.random_tokens(7, "pin/doc-ext", 300, 1000)]
+    ends, fps = oracle.chunk_document(doc, gear, 0)
+    assert ends == [len(doc)] and fps == [oracle.fingerprint(doc)]
+    lib = _libxxhash()
+    if lib is not None:
+        raw = np.asarray(doc, dtype="<i4").tobytes()
+        assert fps[0] == lib.XXH64(raw, len(raw), 0)
+    ends, fps = oracle.chunk_document(doc, gear, MASK64, seed=9)
+    assert ends == list(range(1, len(doc) + 1))
+    assert fps == [oracle.fingerprint([t], 9) for t in doc]
+    assert oracle.chunk_document([], gear, 1 << 60) == ([], [])
+
+
+def test_chunk_document_tiles_the_document():
+    gear = _gear()
+    doc = [int(t) for t in W.random_tokens(8, "pin/doc-tile", 3000, 1000)]
+    for lo, hi in ((0, 0), (16, 128), (50, 50)):
+        ends, fps = oracle.chunk_document(doc, gear, oracle.threshold_for_mean(64), lo, hi)
+        starts = [0] + ends[:-1]
+        assert ends[-1] == len(doc) and all(b > a for a, b in zip(starts, ends))
+        assert sum((doc[s:e] for s, e in zip(starts, ends)), []) == doc
+        assert len(fps) == len(ends)

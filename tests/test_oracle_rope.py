@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 
 import oracle
+import workloads as W
 from oracle import INTERLEAVED, NEOX_HALF
 
 
@@ -73,6 +74,35 @@ def test_llama3_continuous_at_both_regime_boundaries():
     slope = np.diff(ratio) / np.diff(th)
     np.testing.assert_allclose(slope, slope[0], rtol=1e-9)
     assert slope[0] > 0  # higher frequency, less division
+
+
+def test_model_table_end_entries_closed_forms():
+    """theta_0 = b^0 = 1 in every table; Llama-3.1's highest frequency has a
+    wavelength of 2 pi < 8192/4 and is kept, its lowest (wavelength about
+    3.3e5 > 8192) is divided by the factor 8."""
+    plain = oracle.model_inv_freq(128, 5e5)
+    sc = oracle.model_inv_freq(128, 5e5, W.LLAMA3_SCALING)
+    assert plain[0] == 1.0 and sc[0] == 1.0
+    assert math.isclose(plain[-1], 5e5 ** (-126 / 128), rel_tol=1e-14)
+    assert math.isclose(sc[-1], 5e5 ** (-126 / 128) / 8.0, rel_tol=1e-14)
+    assert len(sc) == 64
+
+
+@pytest.mark.parametrize("pairing", [NEOX_HALF, INTERLEAVED])
+def test_expected_row_identity_and_quarter_turn(pairing):
+    """An MLA-shaped row (576 dims, rope slice at 512..575): delta 0 returns
+    the bf16 values exactly; with every frequency pi/2 a shift of 1 maps each
+    rope pair (x, y) to (-y, x) and leaves the latent alone."""
+    rng = np.random.default_rng(3)
+    bits = (rng.standard_normal(576).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    x = oracle.bf16_bits_to_f64(bits)
+    th = np.full(32, math.pi / 2)
+    np.testing.assert_array_equal(oracle.expected_row(bits, 0, th, pairing, 512, 64), x)
+    got = oracle.expected_row(bits, 1, th, pairing, 512, 64)
+    np.testing.assert_array_equal(got[:512], x[:512])
+    a, b = oracle.rope_pairs(64, pairing)
+    np.testing.assert_allclose(got[512 + a], -x[512 + b], atol=1e-15)
+    np.testing.assert_allclose(got[512 + b], x[512 + a], atol=1e-15)
 
 
 # ------------------------------------------------------------ rotation basics
