@@ -199,3 +199,82 @@ def test_mapped_chunk_moves_again_by_the_difference():
         pic.pic_free_request(ctx, plan)
     finally:
         pic.pic_destroy(res["ctx"])
+
+
+def test_llama_full_size_mapped_in_two_orders():
+    """The mapped benchmark's launch at full size (Llama-3.1-8B RAG workload,
+    32 layers, llama3-scaled theta): every chunk sits in its own cache blocks
+    at position 0 and is mapped into the request (EPIC runtime figure, steps 1
+    and 2: its blocks reused, its keys rotated in place, its values never
+    moved).  Then the request is built again in a second order, so each chunk
+    after the system prompt moves by the difference of its two positions.
+    After each step, layers 0, 13 and 31 of every chunk are compared with
+    the oracle's rotation of that layer's keys as they were before the step
+    (one bf16 rounding per step); values, the request's own blocks, block
+    tables and recompute lists must match bit for bit."""
+    wl = W.llama31_8b_rag()
+    m = wl.model
+    bs = m.block_size
+    theta = oracle.model_inv_freq(m.rope_dim, m.rope_theta, m.llama3)
+    own_blocks = -(-wl.request_tokens[0] // bs)
+    nblk = [-(-n // bs) for n in wl.chunk_lens]
+    nb = own_blocks + sum(nblk)
+    ctx = pic.create_from_spec(pic.model_spec_from(m), nb)
+    try:
+        k_pool = W.make_pool(wl, "k", device=DEV)
+        v_pool = W.make_pool(wl, "v", device=DEV)
+        shape = (m.num_layers, nb, bs) + tuple(m.row_shape)
+        k_cache = torch.zeros(shape, dtype=torch.bfloat16, device=DEV)
+        v_cache = torch.zeros(shape, dtype=torch.bfloat16, device=DEV)
+        ids, blocks, first = [], [], own_blocks
+        for c, (off, n) in enumerate(zip(wl.pool_offsets, wl.chunk_lens)):
+            blks = list(range(first, first + nblk[c]))
+            first += nblk[c]
+            for j, b in enumerate(blks):
+                t0, t1 = j * bs, min(n, (j + 1) * bs)
+                k_cache[:, b, :t1 - t0] = k_pool[:, off + t0:off + t1]
+                v_cache[:, b, :t1 - t0] = v_pool[:, off + t0:off + t1]
+            ids.append(pic.pic_register_chunk_blocks(ctx, W.chunk_key(wl.name, c), blks, n, 0)[0])
+            blocks.append(blks)
+        v_before = v_cache.clone()
+        head, rest = wl.requests[0][:1], list(wl.requests[0][1:])
+        perm = W.Stream(1, "mapped/order/0").permutation(len(rest))
+        orders = [wl.requests[0], head + [rest[i] for i in perm]]
+        assert orders[0] != orders[1]
+        layers = [0, 13, 31]
+        pos_now = [0] * len(ids)  # where each chunk's keys sit
+        for order in orders:
+            plan, bt = pic.pic_build_block_table(ctx, [ids[c] for c, _ in order], own_blocks,
+                                                 take_tokens=[t for _, t in order],
+                                                 k_nonleading=wl.k_nonleading, k_leading=wl.k_leading, alias=True)
+            # block-aligned chunks taken whole: all mapped, no fresh block
+            assert bt.tolist() == [b for c, _ in order for b in blocks[c]]
+            p, new_pos, rec = 0, {}, []
+            for j, (c, n) in enumerate(order):
+                assert pic.pic_plan_segment_mode(plan, j) == pic.PIC_SEG_MAPPED
+                assert pic.pic_plan_segment(plan, j)["delta"] == p - pos_now[c]
+                new_pos[c] = p
+                rec += list(range(p, p + min(wl.k_leading if p == 0 else wl.k_nonleading, n)))
+                p += n
+            before = bits(k_cache[layers])
+            ridx = torch.full((len(rec),), -7, dtype=torch.int32, device=DEV)
+            indptr = torch.empty(2, dtype=torch.int32, device=DEV)
+            ws = torch.empty(pic.pic_workspace_bytes(ctx, [plan]), dtype=torch.uint8, device=DEV)
+            pic.pic_stitch(ctx, [plan], k_pool, v_pool, k_cache, v_cache, torch.from_numpy(bt).to(DEV).view(1, -1),
+                           ridx, indptr, ws)
+            assert pic.pic_query_device_status(ctx, ws) == 0
+            assert ridx.cpu().tolist() == rec and indptr.cpu().tolist() == [0, len(rec)]
+            after = k_cache[layers]
+            for c, n in order:
+                got = f64(after[:, blocks[c]].reshape(len(layers), -1, *m.row_shape)[:, :n])
+                old = oracle.bf16_bits_to_f64(before[:, blocks[c]].reshape(len(layers), -1, *m.row_shape)[:, :n])
+                assert_k_close(got, oracle.rotate(old, new_pos[c] - pos_now[c], theta, oracle.NEOX_HALF), f"K {c}")
+            assert torch.equal(v_cache.view(torch.int16), v_before.view(torch.int16))
+            assert not k_cache[:, :own_blocks].view(torch.int16).any()
+            pic.pic_free_request(ctx, plan)
+            for c in new_pos:
+                pos_now[c] = new_pos[c]
+                assert pic.pic_chunk_info(ctx, ids[c])[2] == new_pos[c]
+    finally:
+        pic.pic_destroy(ctx)
+        torch.cuda.empty_cache()
