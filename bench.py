@@ -167,6 +167,25 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle
+#
+# The oracle runs as it stands, on every host core: one spawned process per
+# core (spawned, not forked: a child forked after the first CUDA call can
+# hang), each running whole units of the sample it is handed.  A unit is one
+# request x one layer (stitch, attention) or one document (chunking).  The
+# pool layer the units read is drawn once and shared through a file every
+# process maps read-only.  Time is the wall clock from handing out a sample
+# until the last core has finished its share.
+
+_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
 
 def run_oracle_sample(wl, pool_k_bits, pool_v_bits, layers):
     """The oracle as it stands, on the given pool layers of every request."""
@@ -188,41 +207,10 @@ def run_oracle_sample(wl, pool_k_bits, pool_v_bits, layers):
                         m.rope_offset, m.rope_dim, layers=layers)
 
 
-def host_pool_bits(wl, which, layers):
-    """bf16 bits of the given pool layers, drawn on the host (the oracle's own inputs)."""
-    import torch
-    t = W.make_pool(W.Workload(wl.name, W.Model(**{**wl.model.__dict__, "num_layers": len(layers)}),
-                               wl.chunk_lens, wl.requests, wl.k_nonleading, wl.k_leading), which, "cpu")
-    return t.view(torch.int16).numpy().view(np.uint16)
-
-
-def cpu_baseline(wl, budget_s=12.0):
-    """Oracle GB/s on a bounded sample: whole requests, as many layers as fit
-    in about budget_s seconds of one host core."""
-    m = wl.model
-    kb = host_pool_bits(wl, "k", [0])
-    vb = host_pool_bits(wl, "v", [0]) if m.kind == "gqa" else None
-    t0 = time.perf_counter()
-    run_oracle_sample(wl, kb, vb, [0])
-    t1 = time.perf_counter() - t0
-    n = int(max(1, min(m.num_layers - 1, budget_s / max(t1, 1e-3) - 1)))
-    kb = np.repeat(kb, n, axis=0)
-    vb = np.repeat(vb, n, axis=0) if vb is not None else None
-    t0 = time.perf_counter()
-    run_oracle_sample(wl, kb, vb, list(range(n)))
-    el = time.perf_counter() - t0
-    tl = sum(wl.request_tokens) * n
-    gbs = tl * bytes_per_token_layer(m, "stitch") / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} layer(s) x all {sum(wl.request_tokens)} tokens of the workload "
-                      f"({tl} token-layers, {el:.1f} s, fp64 numpy, single thread)",
-            "tokens_layers_per_s": tl / el}
-
-
-def cpu_baseline_attend(wl, hq, budget_s=12.0):
-    """Oracle decode attention on a bounded sample: the fused-path definition
-    (chunk keys rotated in fp64 from the pool) over the whole context of every
-    request, one layer at a time, until about budget_s seconds have passed."""
+def run_oracle_attend(wl, r, kb, vb, hq, rng):
+    """The oracle's decode attention for request r over one layer: chunk keys
+    rotated in fp64 from the pool (the fused path's definition), the sink
+    bias on the recompute positions, then attention_decode."""
     import oracle
     m = wl.model
     theta = oracle.model_inv_freq(m.rope_dim, m.rope_theta, m.llama3)
@@ -230,92 +218,250 @@ def cpu_baseline_attend(wl, hq, budget_s=12.0):
     chunks = [oracle.Chunk(off, n, 0) for off, n in zip(wl.pool_offsets, wl.chunk_lens)]
     mla = m.kind == "mla"
     vdim = m.head_dim - m.rope_dim if mla else m.head_dim
-    kb = oracle.bf16_bits_to_f64(host_pool_bits(wl, "k", [0]))[0]
-    vb = kb[..., :vdim] if mla else oracle.bf16_bits_to_f64(host_pool_bits(wl, "v", [0]))[0]
-    rng = np.random.default_rng(0)
     scale = 1.0 / (192 ** 0.5) if mla else 1.0 / (m.head_dim ** 0.5)
-    t0 = time.perf_counter()
-    layers = token_layers = 0
-    while layers < m.num_layers and (layers == 0 or time.perf_counter() - t0 < budget_s):
-        for req in wl.requests:
-            segs = oracle.compose(chunks, [c for c, _ in req], take=[t for _, t in req])
-            T = segs[-1].dst_pos + segs[-1].length
-            rows = kb.reshape(kb.shape[0], -1, m.head_dim)
-            keys = np.empty((T,) + rows.shape[1:])
-            vals = np.empty((T, rows.shape[1], vdim))
-            for sg in segs:
-                src = rows[sg.src_tok:sg.src_tok + sg.length]
-                keys[sg.dst_pos:sg.dst_pos + sg.length] = oracle.rotate_rows(src, sg.delta, theta, pairing,
-                                                                            m.rope_offset, m.rope_dim)
-                vals[sg.dst_pos:sg.dst_pos + sg.length] = vb.reshape(vb.shape[0], -1, vdim)[
-                    sg.src_tok:sg.src_tok + sg.length]
-            bias = oracle.sink_bias(segs, T, wl.k_nonleading, -15.0)
-            oracle.attention_decode(rng.standard_normal((hq, m.head_dim)), keys, vals, scale, bias)
-            token_layers += T
-        layers += 1
-    el = time.perf_counter() - t0
-    row = m.num_kv_heads * m.head_dim * 2
-    gbs = token_layers * row * (1 if mla else 2) / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{layers} layer(s) x all {sum(wl.request_tokens)} positions, {hq} query heads "
-                      f"({token_layers} token-layers, {el:.1f} s, fp64 numpy, single thread)",
-            "tokens_layers_per_s": token_layers / el}
+    req = wl.requests[r]
+    segs = oracle.compose(chunks, [c for c, _ in req], take=[t for _, t in req])
+    T = segs[-1].dst_pos + segs[-1].length
+    keys = np.empty((T, m.num_kv_heads, m.head_dim))
+    vals = np.empty((T, m.num_kv_heads, vdim))
+    for sg in segs:
+        src = oracle.bf16_bits_to_f64(kb[sg.src_tok:sg.src_tok + sg.length]).reshape(sg.length, -1, m.head_dim)
+        keys[sg.dst_pos:sg.dst_pos + sg.length] = oracle.rotate_rows(src, sg.delta, theta, pairing,
+                                                                    m.rope_offset, m.rope_dim)
+        if mla:
+            vals[sg.dst_pos:sg.dst_pos + sg.length] = src[..., :vdim]
+        else:
+            vals[sg.dst_pos:sg.dst_pos + sg.length] = oracle.bf16_bits_to_f64(
+                vb[sg.src_tok:sg.src_tok + sg.length]).reshape(sg.length, -1, vdim)
+    bias = oracle.sink_bias(segs, T, wl.k_nonleading, -15.0)
+    oracle.attention_decode(rng.standard_normal((hq, m.head_dim)), keys, vals, scale, bias)
 
 
-def prefix_sample(wl, frac):
-    """The workload with every request cut to about its first frac of tokens
-    (whole chunks, the last one taken in part)."""
-    reqs = []
-    for req in wl.requests:
-        want = max(1, int(round(frac * sum(t for _, t in req))))
-        cut = []
-        for c, t in req:
-            if want <= 0:
+def _oracle_worker(conn, job):
+    """One host core: maps the shared inputs, then runs each share it is sent
+    (a list of unit ids) and answers with its busy seconds."""
+    import traceback
+    try:
+        import oracle
+        kind = job["kind"]
+        if kind == "cdc":
+            tokens = np.load(job["tokens"], mmap_mode="r")
+            offsets = np.load(job["offsets"])
+            gear = np.load(job["gear"])
+        else:
+            wl = job["wl"]
+            kb = np.load(job["k"], mmap_mode="r")[0]
+            vb = np.load(job["v"], mmap_mode="r")[0] if job["v"] else None
+            rng = np.random.default_rng(0)
+        conn.send(("ready", None))
+        while True:
+            share = conn.recv()
+            if share is None:
                 break
-            cut.append((c, min(t, want)))
-            want -= t
-        reqs.append(cut)
-    return W.Workload(wl.name, wl.model, wl.chunk_lens, reqs, wl.k_nonleading, wl.k_leading)
+            t0 = time.perf_counter()
+            produced = 0
+            for u in share:
+                if kind == "stitch":
+                    sub = W.Workload(wl.name, wl.model, wl.chunk_lens, [wl.requests[u]], wl.k_nonleading,
+                                     wl.k_leading)
+                    run_oracle_sample(sub, kb[None], None if vb is None else vb[None], [0])
+                elif kind == "attend":
+                    run_oracle_attend(wl, u, kb, vb, job["hq"], rng)
+                else:
+                    doc = tokens[offsets[u]:offsets[u + 1]]
+                    ends, _ = oracle.chunk_document(list(doc), gear, job["thr"], job["min_len"], job["max_len"])
+                    produced += len(ends)
+            conn.send(("done", (time.perf_counter() - t0, produced)))
+    except Exception:
+        conn.send(("error", traceback.format_exc()))
 
 
-def run_reference(args, wl, budget_s=120.0):
-    """Reference arm: the fp64 oracle timed on the host.  A step is one layer
-    of every request; when K + W such steps would take more than about
-    budget_s seconds of one core, a step takes a prefix of every request
-    instead (segments and tokens both shrink, so the rate stays that of the
-    whole layer), and the bytes counted are the sample's."""
-    m = wl.model
-    kb = host_pool_bits(wl, "k", [0])
-    vb = host_pool_bits(wl, "v", [0]) if m.kind == "gqa" else None
-    # Two whole-layer calls count as the first two warm-up steps; the second,
-    # free of the first call's one-time set-up, sizes the sample.
-    run_oracle_sample(wl, kb, vb, [0])
-    t0 = time.perf_counter()
-    run_oracle_sample(wl, kb, vb, [0])
-    t1 = time.perf_counter() - t0
-    sub = wl
-    if (args.steps + args.warmup) * t1 > budget_s:
-        sub = prefix_sample(wl, budget_s / ((args.steps + args.warmup) * t1))
-    for _ in range(max(0, args.warmup - 2)):
-        run_oracle_sample(sub, kb, vb, [0])
-    times = []
-    for _ in range(args.steps):
+def balance(weights, n):
+    """Split unit ids 0..len(weights)-1 over n cores: heaviest first, each to
+    the least loaded core (ties to the lowest core).  Returns n lists."""
+    shares = [[] for _ in range(n)]
+    load = [0] * n
+    for u in sorted(range(len(weights)), key=lambda u: (-weights[u], u)):
+        c = min(range(n), key=lambda i: (load[i], i))
+        shares[c].append(u)
+        load[c] += weights[u]
+    return shares
+
+
+class OracleCores:
+    """One spawned oracle process per host core."""
+
+    def __init__(self, job, n=None):
+        import multiprocessing as mp
+        self.n = n or host_cores()
+        ctx = mp.get_context("spawn")
+        saved = {k: os.environ.get(k) for k in _THREAD_VARS}
+        for k in _THREAD_VARS:       # one thread per process: the cores are the parallelism
+            os.environ[k] = "1"
+        self.procs, self.conns = [], []
+        try:
+            for _ in range(self.n):
+                a, b = ctx.Pipe()
+                p = ctx.Process(target=_oracle_worker, args=(b, job), daemon=True)
+                p.start()
+                self.procs.append(p)
+                self.conns.append(a)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for c in self.conns:
+            self._answer(c)
+
+    @staticmethod
+    def _answer(conn):
+        tag, val = conn.recv()
+        if tag == "error":
+            raise RuntimeError("oracle process failed:\n" + val)
+        return val
+
+    def run(self, units, weights):
+        """Runs the given units (ids) spread over the cores; returns (wall
+        seconds, cores that got work, what the units produced in all: chunks
+        for chunking, else 0)."""
+        shares = balance([weights[u] for u in units], self.n)
+        shares = [[units[i] for i in s] for s in shares]
         t0 = time.perf_counter()
-        run_oracle_sample(sub, kb, vb, [0])
-        times.append(time.perf_counter() - t0)
+        for c, s in zip(self.conns, shares):
+            c.send(s)
+        produced = sum(self._answer(c)[1] for c in self.conns)
+        return time.perf_counter() - t0, sum(1 for s in shares if s), produced
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except Exception:
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
+            if p.is_alive():
+                p.terminate()
+
+
+def host_pool_bits(wl, which):
+    """bf16 bits of pool layer 0, drawn on the host (the oracle's own inputs)."""
+    import torch
+    t = W.make_pool(W.Workload(wl.name, W.Model(**{**wl.model.__dict__, "num_layers": 1}),
+                               wl.chunk_lens, wl.requests, wl.k_nonleading, wl.k_leading), which, "cpu")
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+class OracleRun:
+    """The oracle's stitch (kind "stitch") or decode attention ("attend") of a
+    workload on all host cores.  Every unit reads pool layer 0: the oracle's
+    cost per unit does not depend on the layer's values."""
+
+    def __init__(self, wl, kind, hq=0, n=None):
+        self.wl, self.kind = wl, kind
+        self.dir = tempfile.mkdtemp(prefix="pic_oracle_")
+        paths = {"k": os.path.join(self.dir, "k.npy"), "v": None}
+        np.save(paths["k"], host_pool_bits(wl, "k"))
+        if wl.model.kind == "gqa":
+            paths["v"] = os.path.join(self.dir, "v.npy")
+            np.save(paths["v"], host_pool_bits(wl, "v"))
+        self.cores = OracleCores({"kind": kind, "wl": wl, "hq": hq, **paths}, n)
+        # units, layer-major: every request of layer 0, then of layer 1, ...
+        R = len(wl.requests)
+        self.units = [r for _ in range(wl.model.num_layers) for r in range(R)]
+        self.weights = {r: t for r, t in enumerate(wl.request_tokens)}
+
+    def sample(self, wall_s):
+        """The first units (layer-major) that keep every core busy for about
+        wall_s seconds: a whole number of units per core, at least one,
+        sized by two runs of one unit per core (the first warms the cores up)
+        and at most the whole workload.  Returns the number of units."""
+        n = self.cores.n
+        first = self.units[:n]
+        for _ in range(2):
+            el, _, _ = self.cores.run(first, self.weights)
+        rate = sum(self.weights[u] for u in first) / max(el, 1e-6)   # token-layers/s, all cores
+        want = rate * wall_s
+        k, acc = 0, 0
+        while k < len(self.units) and (k < n or acc < want):
+            acc += self.weights[self.units[k]]
+            k += 1
+        return min(len(self.units), -(-k // n) * n)
+
+    def run(self, k):
+        """Runs the first k units; returns (wall seconds, token-layers, cores used)."""
+        units = self.units[:k]
+        el, used, _ = self.cores.run(units, self.weights)
+        return el, sum(self.weights[u] for u in units), used
+
+    def describe(self, k):
+        wl = self.wl
+        R, L = len(wl.requests), wl.model.num_layers
+        if k == R * L:
+            return f"the whole workload ({R} request(s) x {L} layers)"
+        return (f"{k} of the workload's {R * L} (request, layer) units, layer-major "
+                f"({k // R} whole layer(s) of every request" + (f" + {k % R} request(s)" if k % R else "") + ")")
+
+    def close(self):
+        self.cores.close()
+        import shutil
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+
+def cpu_baseline(wl, mode="stitch", hq=0, cpu_seconds=24.0):
+    """Oracle rate on a bounded sample spread over all host cores: about
+    cpu_seconds of CPU work in all (whole units, layer-major)."""
+    run = OracleRun(wl, mode, hq)
+    try:
+        k = run.sample(cpu_seconds / run.cores.n)
+        el, tl, used = run.run(k)
+    finally:
+        run.close()
+    m = wl.model
+    if mode == "attend":
+        row = m.num_kv_heads * m.head_dim * 2
+        bpt = row * (1 if m.kind == "mla" else 2)
+    else:
+        bpt = bytes_per_token_layer(m, "stitch")
+    what = f"{hq} query heads, " if mode == "attend" else ""
+    return {"value": tl * bpt / el / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
+            "sample": f"{run.describe(k)}: {tl} token-layers, {what}{el:.2f} s wall on {used} host cores "
+                      f"(fp64 numpy, one process per core)",
+            "tokens_layers_per_s": tl / el}
+
+
+def run_reference(args, wl, budget_s=None):
+    """Reference arm: the fp64 oracle timed on all host cores.  A step is the
+    whole workload when K + W of them fit in about budget_s seconds, else the
+    first (request, layer) units, layer-major, that do; the bytes counted are
+    the sample's."""
+    budget_s = args.ref_seconds if budget_s is None else budget_s
+    run = OracleRun(wl, "stitch")
+    try:
+        k = run.sample(budget_s / (args.steps + args.warmup))
+        for _ in range(args.warmup):
+            run.run(k)
+        times, used = [], 0
+        for _ in range(args.steps):
+            el, tl, used = run.run(k)
+            times.append(el)
+    finally:
+        run.close()
     el = sum(times)
-    tl = sum(sub.request_tokens) * args.steps
-    gbs = tl * bytes_per_token_layer(m, "stitch") / el / 1e9
-    sample_txt = (f", the first {sum(sub.request_tokens)} of {sum(wl.request_tokens)} tokens" if sub is not wl else "")
+    tl_all = tl * args.steps
+    gbs = tl_all * bytes_per_token_layer(wl.model, "stitch") / el / 1e9
+    sample = run.describe(k)
     line = {
         "impl": "reference", "metric": "stitched KV GB/s", "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {WORKLOAD_TEXT.get(wl.name, '')}",
-                   "step": f"one layer of every request{sample_txt} (bounded sample)"},
-        "tokens_layers_per_s": tl / el,
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"1 layer of every request{sample_txt} per step"},
+                   "step": f"{sample} ({tl} token-layers), bounded sample"},
+        "tokens_layers_per_s": tl_all / el,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": f"{sample} per step, on {used} host cores (fp64 numpy, one process per core)"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -530,8 +676,13 @@ def run_e2e(rig, steps, warmup, cache_on_host=False):
     the host."""
     torch = rig.torch
     pic = rig.pic
-    hk = rig.k_pool.cpu().pin_memory()
-    hv = rig.v_pool.cpu().pin_memory() if rig.v_pool is not None else None
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    hk = pinned_copy(rig.k_pool)
+    hv = pinned_copy(rig.v_pool) if rig.v_pool is not None else None
     if cache_on_host:
         hkc = torch.empty(rig.k_cache.shape, dtype=rig.k_cache.dtype).pin_memory()
         hvc = torch.empty(rig.v_cache.shape, dtype=rig.v_cache.dtype).pin_memory() if rig.v_cache is not None else None
@@ -573,19 +724,31 @@ CDC_TEXT = ("rag_corpus: 8,192 documents of log-uniform 512-16,384 tokens (37.6M
             "128,256-id vocabulary), Gear hash over 64-token windows, xxHash64 fingerprints")
 
 
-def cdc_oracle_sample(corpus, thr, min_len, max_len, budget_s=12.0):
-    """The oracle as it stands, on whole documents until about budget_s seconds."""
-    import oracle
-    t0 = time.perf_counter()
-    n_tok = n_chunks = 0
-    d = 0
-    while d < corpus.n_docs and time.perf_counter() - t0 < budget_s:
-        doc = corpus.doc(d)
-        ends, _ = oracle.chunk_document(list(doc), corpus.gear, thr, min_len, max_len)
-        n_tok += len(doc)
-        n_chunks += len(ends)
-        d += 1
-    return d, n_tok, n_chunks, time.perf_counter() - t0
+def cdc_oracle_sample(corpus, thr, min_len, max_len, cpu_seconds=24.0):
+    """The oracle as it stands, on all host cores: whole documents in corpus
+    order, about cpu_seconds of CPU work in all (sized by a run of one
+    document per core).  Returns (documents, tokens, chunks, wall s, cores)."""
+    d = tempfile.mkdtemp(prefix="pic_cdc_oracle_")
+    paths = {k: os.path.join(d, k + ".npy") for k in ("tokens", "offsets", "gear")}
+    np.save(paths["tokens"], corpus.tokens)
+    np.save(paths["offsets"], corpus.offsets)
+    np.save(paths["gear"], corpus.gear)
+    cores = OracleCores({"kind": "cdc", "thr": thr, "min_len": min_len, "max_len": max_len, **paths})
+    try:
+        lens = np.diff(corpus.offsets).tolist()
+        first = list(range(min(cores.n, corpus.n_docs)))
+        el, _, _ = cores.run(first, lens)
+        want = sum(lens[u] for u in first) / max(el, 1e-6) * cpu_seconds / cores.n
+        k, acc = 0, 0
+        while k < corpus.n_docs and (k == 0 or acc < want):
+            acc += lens[k]
+            k += 1
+        el, used, n_chunks = cores.run(list(range(k)), lens)
+    finally:
+        cores.close()
+        import shutil
+        shutil.rmtree(d, ignore_errors=True)
+    return k, int(sum(lens[:k])), n_chunks, el, used
 
 
 def run_cdc(args):
@@ -621,9 +784,15 @@ def run_cdc(args):
     def step(toks=tokens):
         pic.pic_cdc_chunk(toks, offsets, gear, thr, indptr, ends, fps, args.cdc_min, args.cdc_max, 0, workspace=ws)
 
-    for _ in range(args.warmup):
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        if i == args.warmup - 1:
+            w0.record()
         step()
+    w1.record()
     torch.cuda.synchronize()
+    if args.steps is None:
+        args.steps = auto_steps(w0.elapsed_time(w1), dev)
     if pic.pic_query_device_status(None, ws) != 0:
         raise RuntimeError("chunking reported a device error")
     n_chunks = int(indptr[-1].item())
@@ -691,10 +860,11 @@ def run_cdc(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        d, ntk, nch, el = cdc_oracle_sample(corpus, thr, args.cdc_min, args.cdc_max)
+        d, ntk, nch, el, used = cdc_oracle_sample(corpus, thr, args.cdc_min, args.cdc_max)
         cpu_algo = 4 * ntk + 16 * nch + 16 * (d + 1)
-        cpu = {"value": cpu_algo / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {d} documents ({ntk} tokens, {nch} chunks, {el:.1f} s, Python, single thread)",
+        cpu = {"value": cpu_algo / el / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
+               "sample": f"first {d} documents ({ntk} tokens, {nch} chunks), {el:.2f} s wall on {used} host "
+                         f"cores (Python, one process per core)",
                "tokens_per_s": ntk / el}
 
     line = {
@@ -724,13 +894,22 @@ def run_cdc(args):
         dist.destroy_process_group()
 
 
+def auto_steps(step_ms, dev):
+    """Timed steps when --steps is not given: about 10 s of steps, 20 to 1000,
+    the same on every rank (sized by the slowest rank's last warm-up step)."""
+    from position_independent_kv_stitch_gb300.sharding import max_over_ranks
+    ms = max_over_ranks(step_ms, dev)
+    return int(min(1000, max(20, 10000.0 / max(ms, 1e-3))))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about 10 s of GPU steps, 20 to 1000; 20 for the reference arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pic", choices=["pic", "reference"])
-    ap.add_argument("--workload", default="llama31_8b_rag", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="serving_stress", choices=sorted(W.WORKLOADS))
     ap.add_argument("--mode", default="stitch",
                     choices=["stitch", "inplace", "mapped", "attend", "attend_cache", "cdc"])
     ap.add_argument("--cdc-mean", type=int, default=64, help="cdc mode: mean chunk length the threshold aims at")
@@ -743,6 +922,8 @@ def main():
     ap.add_argument("--e2e-cache-on-host", action="store_true",
                     help="end-to-end leg: keep the paged cache in pinned host memory too")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: about how long all its steps (warm-up and timed) may take")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -758,6 +939,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
+        if args.steps is None:
+            args.steps = 20
         if args.mode != "stitch":
             # only the stitch has a reference arm; every mode's own line
             # carries an oracle timing in its cpu_baseline field
@@ -782,10 +965,16 @@ def main():
     dev = torch.device("cuda", local_rank)
 
     rig = Rig(wl, dev, args.mode, args.q_heads)
-    for _ in range(args.warmup):
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        if i == args.warmup - 1:
+            w0.record()
         rig.step()
+    w1.record()
     torch.cuda.synchronize()
     rig.check_status()
+    if args.steps is None:
+        args.steps = auto_steps(w0.elapsed_time(w1), dev)
 
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
@@ -844,7 +1033,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline_attend(wl, rig.attn["hq"]) if args.mode == "attend" else cpu_baseline(wl)
+        cpu = cpu_baseline(wl, "attend", rig.attn["hq"]) if args.mode == "attend" else cpu_baseline(wl)
 
     bulk = pic.pic_kernel_variant(rig.ctx, 1 if args.mode == "inplace" else 0) == pic.PIC_VARIANT_BULK_PIPELINE
     if bulk and args.mode not in ("attend", "attend_cache"):

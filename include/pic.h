@@ -335,9 +335,9 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
  *
  * Some callers cannot allocate device memory where they stitch: an engine
  * that gave (nearly) all of HBM to its own KV-cache pool, a framework that
- * hands a plugin only the tensors it reads and writes, or a latency-bound
- * loop that cannot pay for cudaMalloc / cudaFree (cudaFree synchronizes the
- * whole device).  This call runs the same kernel and computes the same result
+ * hands a plugin only the tensors it reads and writes, or a loop that must
+ * not pay for cudaMalloc / cudaFree (cudaFree synchronizes the whole
+ * device).  This call runs the same kernel and computes the same result
  * as pic_stitch, with the same arguments minus the workspace; it allocates no
  * memory of any kind.  Its scratch (run list, frequency table, status word)
  * is a fixed 4 MiB array of device memory inside the library, which every GPU
@@ -349,6 +349,11 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
  *   - Set-up: the first call on a device (with that device current) looks up
  *     the array's device address; make that first call before any stream
  *     capture.
+ *   - Host wait: the scratch image is uploaded from an ordinary (pageable)
+ *     host array inside the library, and the CUDA runtime may hold such a
+ *     copy, and so this call, until the work already queued on the stream
+ *     has finished.  Unlike pic_stitch, the call is therefore not always
+ *     asynchronous with respect to the host.
  *   - Sharing: every call uses the same array and leaves its contents behind;
  *     each call rewrites what it needs, including a zeroed status word.  Calls
  *     that overlap on the GPU (different streams) race on it, and calls from

@@ -1617,8 +1617,10 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
 //
 // Used only by the no-alloc entry point.  Same checks, workspace image and
 // launch as pic_stitch, but the image is written straight into a
-// caller-owned host buffer and uploaded with a plain (pageable) copy into a
-// caller-owned device buffer, so nothing is allocated here.
+// caller-owned host buffer and uploaded with a plain copy from that
+// (pageable) buffer into a caller-owned device buffer, so nothing is
+// allocated here.  A copy from pageable memory may make the host wait until
+// the stream's earlier work has finished.
 
 namespace pic {
 
@@ -1660,6 +1662,11 @@ pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32
   KernelParams p{};
   fill_stitch_params(ctx, p, static_cast<uint8_t*>(d_scratch), w, n_runs, n_req, k_pool, v_pool, pool_ls, k_cache,
                      v_cache, cache_ls, d_bt, max_blocks, d_ridx, d_indptr);
+  // The failure-test hook applies to this launch exactly as to pic_stitch's.
+  p.debug_stall = ctx->debug_stall;
+  p.max_spins = ctx->debug_spins;
+  ctx->debug_stall = 0;
+  ctx->debug_spins = 0;
   e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0, mostly_in_place(plans, n_req));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
   for (int32_t r = 0; r < n_req; ++r) const_cast<pic_plan*>(plans[r])->applied = true;

@@ -3,13 +3,13 @@
 // Some callers cannot allocate GPU memory where they stitch: a serving
 // engine that has already handed (nearly) all of HBM to its own KV-cache
 // block pool and forbids other allocations, a host framework that gives a
-// plugin only the tensors it reads and writes, or a latency-critical loop
-// that cannot afford cudaMalloc / cudaFree (cudaFree synchronizes the whole
-// device).  For them this entry point runs the same stitch kernel as
-// pic_stitch, but its scratch (the per-launch run list, frequency table and
-// status word) lives in a fixed array of device memory that belongs to this
-// library, declared below, instead of a caller workspace.  The caller still
-// passes every input and output buffer.
+// plugin only the tensors it reads and writes, or a loop that must not pay
+// for cudaMalloc / cudaFree (cudaFree synchronizes the whole device).  For
+// them this entry point runs the same stitch kernel as pic_stitch, but its
+// scratch (the per-launch run list, frequency table and status word) lives
+// in a fixed array of device memory that belongs to this library, declared
+// below, instead of a caller workspace.  The caller still passes every input
+// and output buffer.
 //
 // The array is a file-scope __device__ variable: each GPU that loads the
 // library holds kScratchBytes of it until the process exits.  Host code may
@@ -35,7 +35,8 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-// Host image of one launch's scratch, uploaded with a pageable copy.  Static
+// Host image of one launch's scratch, uploaded with a pageable copy (which
+// the runtime may hold until the stream's earlier work is done).  Static
 // too, so nothing is allocated per call.
 alignas(256) unsigned char g_host_image[kScratchBytes];
 

@@ -1,8 +1,9 @@
 """GPU parity of decode attention over a stitched context: the fused path
 (chunk keys rotated on their way from the pool into registers) against the
 fp64 oracle over exactly rotated keys, with and without LegoLink's sink bias;
-the paged-cache path over a materialized stitch against the same oracle
-(looser: its keys were rounded to bf16 once)."""
+the paged-cache path over a materialized stitch against the oracle over the
+stitched bf16 keys it reads (same tolerance), and against the exact-key
+oracle (looser: its keys were rounded to bf16 once)."""
 
 import math
 
@@ -93,6 +94,33 @@ def _oracle(S, q, scale, bias_value):
     return np.stack(outs, axis=1), np.stack(lses, axis=1)
 
 
+def _oracle_over_cache(S, k_cache_bits, v_cache_bits, q, scale, bias_value):
+    """The oracle's attention over the keys and values as a stitch left them
+    in the paged cache (bf16, already rotated): what the cache path reads."""
+    m, bs = S["m"], S["bs"]
+    kc, vc = oracle.bf16_bits_to_f64(k_cache_bits), oracle.bf16_bits_to_f64(v_cache_bits)
+    outs, lses = [], []
+    for r, plan in enumerate(S["plans"]):
+        info = pic.pic_plan_info(plan)
+        T = info["total_tokens"]
+        table = S["tables"][r]
+        keys = np.stack([kc[:, table[p // bs], p % bs] for p in range(T)], axis=1)
+        vals = np.stack([vc[:, table[p // bs], p % bs] for p in range(T)], axis=1)
+        segs = []
+        for j in range(info["num_segments"]):
+            sg = pic.pic_plan_segment(plan, j)
+            segs.append(oracle.Segment(sg["chunk_id"], sg["src_tok"], sg["num_tokens"], sg["dst_pos"], sg["delta"]))
+        bias = oracle.sink_bias(segs, T, 4, bias_value) if bias_value else None
+        o_l, s_l = [], []
+        for l in range(S["L"]):
+            o, s_ = oracle.attention_decode(oracle.bf16_bits_to_f64(q[l, r]), keys[l], vals[l], scale, bias)
+            o_l.append(o)
+            s_l.append(s_)
+        outs.append(np.stack(o_l))
+        lses.append(np.stack(s_l))
+    return np.stack(outs, axis=1), np.stack(lses, axis=1)
+
+
 def _run(S, source, bias_value=0.0, k_cache=None, v_cache=None):
     L, Hq, D = S["L"], S["Hq"], S["D"]
     g = torch.Generator().manual_seed(9)
@@ -136,6 +164,13 @@ def test_cache_path_over_materialized_stitch():
         assert pic.pic_query_device_status(ctx, ws) == 0
         q, out_c, lse_c, scale = _run(S, pic.PIC_ATTEND_CACHE, -15.0, kc, vc)
         _, out_f, lse_f, _ = _run(S, pic.PIC_ATTEND_FUSED, -15.0, kc, vc)
+        # the cache path against the oracle over the very keys it reads
+        # (the GPU-stitched bf16 rows), at the attention tolerance
+        want_c, want_c_lse = _oracle_over_cache(S, bits(kc), bits(vc), bits(q), scale, -15.0)
+        np.testing.assert_allclose(out_c, want_c, atol=2e-3, rtol=0)
+        np.testing.assert_allclose(lse_c, want_c_lse, atol=2e-3, rtol=0)
+        # both paths against the oracle over exactly rotated keys: the cache
+        # path differs by the one bf16 rounding of its stitched keys
         want, want_lse = _oracle(S, bits(q), scale, -15.0)
         np.testing.assert_allclose(out_f, want, atol=2e-3, rtol=0)
         np.testing.assert_allclose(out_c, want, atol=3e-2, rtol=0)

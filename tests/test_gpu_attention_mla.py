@@ -116,6 +116,24 @@ def _context_rows(S, r):
     return rows, segs, T
 
 
+def _check_over_cache(S, cache, q, out, lse, scale, bias_value, atol):
+    """Against the oracle over the rows as the cache holds them after a
+    stitch (bf16, rope slices already rotated): what the cache path reads."""
+    qb, bs = bits(q), S["bs"]
+    cb = oracle.bf16_bits_to_f64(bits(cache))
+    for r in range(3):
+        _, segs, T = _context_rows(S, r)
+        table = np.asarray(S["tables"][r])
+        pos = np.arange(T)
+        rows = cb[:, table[pos // bs], pos % bs]
+        bias = oracle.sink_bias(segs, T, 4, bias_value) if bias_value else None
+        for l in range(S["L"]):
+            o, sv = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[l, r]), rows[l][:, None, :],
+                                            rows[l][:, None, :LATENT], scale, bias)
+            np.testing.assert_allclose(out[l, r], o, atol=atol, rtol=0)
+            np.testing.assert_allclose(lse[l, r], sv, atol=atol, rtol=0)
+
+
 def _attend(S, H, source, bias_value, pool=None, cache=None):
     L = S["L"]
     g = torch.Generator().manual_seed(5)
@@ -189,8 +207,9 @@ def test_mla_running_max_rises_in_a_later_tile(H):
 
 def test_mla_cache_path_over_materialized_stitch():
     """Stitch the requests into the cache (MLA stitch: latent copied, rope
-    rotated, rounded to bf16 once), then attend from the cache: the oracle's
-    result up to that rounding, and the fused path closer to it."""
+    rotated, rounded to bf16 once), then attend from the cache: the oracle
+    over the stitched rows at the attention tolerance, the oracle over
+    exactly rotated rows up to that rounding, and the fused path closer."""
     S = _setup("interleaved", 2, seed=6)
     try:
         ctx = S["ctx"]
@@ -202,6 +221,9 @@ def test_mla_cache_path_over_materialized_stitch():
         assert pic.pic_query_device_status(ctx, ws) == 0
         q, out_c, lse_c, scale = _attend(S, 16, pic.PIC_ATTEND_CACHE, -15.0, pool, cache)
         _, out_f, lse_f, _ = _attend(S, 16, pic.PIC_ATTEND_FUSED, -15.0, pool, cache)
+        # the cache path against the oracle over the GPU-stitched rows it reads
+        _check_over_cache(S, cache, q, out_c, lse_c, scale, -15.0, 2e-3)
+        # both against exactly rotated rows; the cache path's rows were rounded once
         _check_against_oracle(S, q, out_f, lse_f, scale, -15.0, 2e-3)
         _check_against_oracle(S, q, out_c, lse_c, scale, -15.0, 3e-2)
     finally:

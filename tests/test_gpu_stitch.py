@@ -5,6 +5,8 @@ in fp32 and rounded once to bf16).  Values, MLA latents, block tables and
 recompute lists: bit-exact.  Destinations are pre-filled with a NaN sentinel
 so rows written where nothing belongs, or left unwritten, are caught."""
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -64,6 +66,63 @@ def test_cossin_matches_fp64(rope_dim, base, llama3):
         phi = deltas[:, None].astype(np.float64) * theta[None, :]
         err = max(np.abs(got[..., 0] - np.cos(phi)).max(), np.abs(got[..., 1] - np.sin(phi)).max())
         assert err < 1e-6, err
+    finally:
+        pic.pic_destroy(ctx)
+
+
+def _library_theta(ctx, half):
+    """The frequencies the kernels use, read back through
+    pic_rotation_cossin: each theta_i is refined over shifts 1, 2, 4, ...
+    up to the last one that turns it by less than 3 radians (no wrap), so
+    the angle error of about 1e-6 is at most 1e-6 relative."""
+    deltas = np.array([1 << k for k in range(24)], dtype=np.int32)
+    out = torch.empty((len(deltas), half, 2), dtype=torch.float32, device=DEV)
+    ws = torch.empty(4096, dtype=torch.uint8, device=DEV)
+    pic.pic_rotation_cossin(ctx, torch.from_numpy(deltas).to(DEV), out, ws)
+    o = out.cpu().double().numpy()
+    ang = np.arctan2(o[..., 1], o[..., 0])
+    theta = ang[0].copy()                      # shift 1: theta_i <= 1 < pi
+    for k in range(1, len(deltas)):
+        grow = theta * deltas[k] < 3.0
+        theta[grow] = ang[k][grow] / deltas[k]
+    return theta
+
+
+def test_library_llama3_table_hand_derived():
+    """The library's own Llama-3.1 rescaling, tied to hand-derived values
+    rather than to the oracle: (1) Llama-3.1-8B's table keeps frequencies
+    0-28, divides 35-63 by 8 and blends 29-34 strictly between; (2) one
+    frequency placed by the choice of base at each hand-picked wavelength
+    (test_oracle_rope.LLAMA3_HAND: s = 0, 1/4, 1/2, 3/4, 1 and both outer
+    regimes) comes out at the hand-derived ratio; (3) factor 1 changes
+    nothing."""
+    from test_oracle_rope import LLAMA3_HAND
+    ctx = pic.pic_create(pic.PIC_KIND_GQA, 1, 8, 128, 128, 0, pic.PIC_PAIRING_NEOX_HALF, 16, 5e5, 4,
+                         llama3=W.LLAMA3_SCALING)
+    try:
+        r = _library_theta(ctx, 64) / oracle.rope_inv_freq(128, 5e5)
+    finally:
+        pic.pic_destroy(ctx)
+    np.testing.assert_allclose(r[:29], 1.0, rtol=1e-5)
+    np.testing.assert_allclose(r[35:], 0.125, rtol=1e-5)
+    assert np.all((r[29:35] > 0.13) & (r[29:35] < 0.99))
+
+    for lam, ratio in LLAMA3_HAND:
+        # head_dim 64: theta_16 = b^(-1/2), so b = (lambda / 2 pi)^2 puts
+        # frequency 16 at wavelength lambda
+        b = (lam / (2 * math.pi)) ** 2
+        ctx = pic.pic_create(pic.PIC_KIND_GQA, 1, 1, 64, 64, 0, pic.PIC_PAIRING_NEOX_HALF, 16, b, 4,
+                             llama3=W.LLAMA3_SCALING)
+        try:
+            th16 = _library_theta(ctx, 32)[16]
+        finally:
+            pic.pic_destroy(ctx)
+        assert abs(th16 / (2 * math.pi / lam) - ratio) <= 1e-5 * ratio, (lam, th16 / (2 * math.pi / lam), ratio)
+
+    one = dict(W.LLAMA3_SCALING, factor=1.0)
+    ctx = pic.pic_create(pic.PIC_KIND_GQA, 1, 8, 128, 128, 0, pic.PIC_PAIRING_NEOX_HALF, 16, 5e5, 4, llama3=one)
+    try:
+        np.testing.assert_allclose(_library_theta(ctx, 64) / oracle.rope_inv_freq(128, 5e5), 1.0, rtol=1e-5)
     finally:
         pic.pic_destroy(ctx)
 
@@ -422,8 +481,9 @@ def test_inplace_parity(kind, pairing, variant):
 def test_serving_stress_full_size_stitch_then_shift():
     """Serving stress at full size (64 x 16,384 tokens, Zipf reuse, 256-chunk
     pool, Llama-3.1-8B shapes): stitch, check a sample; then shift every chunk
-    in place to a new position up to 128k and check against R(delta + delta')
-    of the pool row (EPIC guide: angles add)."""
+    in place to a new position up to 128k and check the sampled rows against
+    the oracle's in-place rotation of their own pre-shift bits, per element,
+    and against R(delta + delta') of the pool row (EPIC guide: angles add)."""
     wl = W.serving_stress()
     st = Stitched(wl).run()
     try:
@@ -437,10 +497,21 @@ def test_serving_stress_full_size_stitch_then_shift():
         shift = [[wl.new_pos[r][j] - s.dst_pos for j, s in enumerate(segs[r])] for r in range(len(segs))]
         shift_segs = [(r, s.dst_pos, s.length, shift[r][j]) for r in range(len(segs))
                       for j, s in enumerate(segs[r])]
+        # the rows the checks sample, with their bits before the shift
+        l_idx, blk, row, _, d_stitch = _sample_rows(st, segs, tables, 6000, 4)
+        _, _, _, _, d_total = _sample_rows(st, segs, tables, 6000, 4, shift=shift)
+        pre = bits(st.k_cache[l_idx, blk, row])
         ws = torch.empty(pic.pic_rerotate_workspace_bytes(st.ctx, shift_segs), dtype=torch.uint8, device=DEV)
         pic.pic_rerotate_inplace(st.ctx, st.k_cache, st.d_bt, shift_segs, ws)
         assert pic.pic_query_device_status(st.ctx, ws) == 0
         assert max(abs(d) for _, _, _, d in shift_segs) > 100000
+        # (1) the contract: the oracle's in-place rotation R(delta') of the
+        # cache's own bits before the shift, per element
+        theta, pairing = theta_of(st.m), pairing_of(st.m)
+        want = np.stack([oracle.expected_row(pre[i], d_total[i] - d_stitch[i], theta, pairing, 0, 128)
+                         for i in range(len(pre))])
+        assert_k_close(f64(st.k_cache[l_idx, blk, row]), want, "in place, from the cache's own bits")
+        # (2) the composition R(delta') R(delta) = R(delta + delta') of the pool row
         _check_sampled(st, segs, tables, 6000, 4, shift=shift)
     finally:
         st.close()

@@ -76,6 +76,50 @@ def test_llama3_continuous_at_both_regime_boundaries():
     assert slope[0] > 0  # higher frequency, less division
 
 
+# Hand-derived values of the Llama-3.1 rule with orig 8192, low 1, high 4,
+# factor 8.  At wavelength lambda, s = (8192 / lambda - 1) / 3 and
+# theta' / theta = (1 - s) / 8 + s.  Choosing 8192 / lambda = 1.75, 2.5 and
+# 3.25 puts s at exactly 1/4, 1/2 and 3/4:
+#   s = 1/4: 3/32 + 8/32 = 11/32 = 0.34375
+#   s = 1/2: 1/16 + 8/16 =  9/16 = 0.5625
+#   s = 3/4: 1/32 + 24/32 = 25/32 = 0.78125
+# lambda = 8192 gives s = 0 (1/8) and lambda = 2048 gives s = 1 (1), so the
+# blend meets both outer regimes; lambda = 2000 (< 8192 / 4) keeps theta and
+# lambda = 9000 (> 8192 / 1) divides it by 8.  A swapped low/high keeps
+# theta at 8192/3.25 ~ 2521 (ratio 1, not 25/32); a blend weighted the wrong
+# way round gives 25/32 at s = 1/4.
+LLAMA3_HAND = [(2000.0, 1.0), (2048.0, 1.0), (8192 / 3.25, 0.78125), (8192 / 2.5, 0.5625),
+               (8192 / 1.75, 0.34375), (8192.0, 0.125), (9000.0, 0.125)]
+
+
+def test_llama3_hand_derived_ratios():
+    lam = np.array([w for w, _ in LLAMA3_HAND])
+    want = np.array([r for _, r in LLAMA3_HAND])
+    th = 2 * math.pi / lam
+    got = oracle.llama3_inv_freq(th, 8.0, 1.0, 4.0, 8192) / th
+    np.testing.assert_allclose(got, want, rtol=1e-12)
+
+
+def test_llama3_factor_one_is_the_identity():
+    """With factor 1 every regime gives theta back: theta/1, or
+    (1 - s) theta + s theta."""
+    th = oracle.rope_inv_freq(128, 5e5)
+    np.testing.assert_allclose(oracle.llama3_inv_freq(th, 1.0, 1.0, 4.0, 8192), th, rtol=1e-15)
+
+
+def test_llama3_regimes_of_the_llama31_table():
+    """Llama-3.1-8B's table (base 5e5, d = 128): lambda_i = 2 pi 5e5^(i/64).
+    By hand, ln 5e5 = 13.1224, so lambda_28 = 2 pi e^5.741 = 1956 < 2048,
+    lambda_29 = 2 pi e^5.946 = 2402 > 2048, lambda_34 = 2 pi e^6.971 = 6695
+    < 8192 and lambda_35 = 2 pi e^7.176 = 8219 > 8192: frequencies 0-28 are
+    kept, 35-63 divided by 8, and 29-34 blended, strictly between."""
+    th = oracle.rope_inv_freq(128, 5e5)
+    r = oracle.model_inv_freq(128, 5e5, W.LLAMA3_SCALING) / th
+    np.testing.assert_array_equal(r[:29], 1.0)
+    np.testing.assert_allclose(r[35:], 0.125, rtol=1e-15)
+    assert np.all((r[29:35] > 0.125) & (r[29:35] < 1.0))
+
+
 def test_model_table_end_entries_closed_forms():
     """theta_0 = b^0 = 1 in every table; Llama-3.1's highest frequency has a
     wavelength of 2 pi < 8192/4 and is kept, its lowest (wavelength about
