@@ -62,15 +62,28 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("pic_kernels.cu", "pic_kernels_tma.cu", "pic_host.cpp", "pic_internal.h")
+KERNEL_SOURCES = ("pic_kernels.cu", "pic_kernels_tma.cu", "pic_host.cpp#stitch-schedule",
+                  "pic_internal.h#stitch-schedule")
+
+
+def source_text(name):
+    """A source file's bytes, or with "file#region" only the lines between
+    its "region <name>" and "end region <name>" comments."""
+    fname, _, region = name.partition("#")
+    with open(os.path.join(ROOT, "position_independent_kv_stitch_gb300", "csrc", fname), "rb") as f:
+        data = f.read()
+    if not region:
+        return data
+    begin = data.index(f"// region {region}:".encode())
+    end = data.index(f"// end region {region}".encode(), begin)
+    return data[begin:end]
 
 
 def kernel_source_hash(names=KERNEL_SOURCES):
     """Hash of the kernel and launch-schedule sources a traffic record was taken on."""
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(ROOT, "position_independent_kv_stitch_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        h.update(source_text(name))
     return h.hexdigest()[:16]
 
 

@@ -230,6 +230,9 @@ bool plan_valid(const pic_ctx* ctx, const pic_plan* p) {
   return p != nullptr && ctx->plans.count(const_cast<pic_plan*>(p)) != 0;
 }
 
+// region stitch-schedule: run lists, workspace layout, grids and launches of
+// the stitch and in-place kernels (a measurement record names this region).
+
 // Calls f(t, cnt, src) for each run of a segment: at most `cap` tokens that
 // land in one destination block and, for copies out of a block-resident
 // chunk, come from one of its blocks.  src is the run's first source row
@@ -569,6 +572,8 @@ void fill_stitch_params(const pic_ctx* ctx, pic::KernelParams& p, uint8_t* ws, c
   p.n_indptr = n_req + 1;
   p.header = reinterpret_cast<WsHeader*>(ws);
 }
+
+// end region stitch-schedule
 
 void release_staging(pic_ctx* ctx) {
   for (StagingSlot& sl : ctx->staging) {

@@ -12,6 +12,9 @@
 
 namespace pic {
 
+// region stitch-schedule: what the stitch and in-place kernels share with the
+// host (a measurement record names this region).
+
 // One run: up to block_size consecutive tokens of one segment that land in
 // one paged block.  Runs are layer-independent; a kernel work unit is a run
 // times a group of consecutive layers.  32 bytes, read once per unit.
@@ -99,6 +102,8 @@ size_t tma_smem_bytes(const TmaConfig& c);
 // mode 0: stitch with values, 1: stitch without values (MLA), 2: in place.
 cudaError_t launch_tma(const KernelParams& p, const TmaConfig& c, int mode, int pairing, int rope_dim,
                        int grid, cudaStream_t stream);
+
+// end region stitch-schedule
 
 // ---- decode attention over a stitched context (pic_attention.cu)
 //
