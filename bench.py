@@ -543,9 +543,12 @@ class Rig:
             g.manual_seed(11)
             q = torch.empty((m.num_layers, len(wl.requests), hq, m.head_dim), dtype=torch.bfloat16, device=device)
             q.normal_(0.0, 1.0, generator=g)
-            plans, _ = self.plan()
+            # A decode loop attends to the same composed requests every step:
+            # the plans and block tables are built once and kept.
+            plans, bt = self.plan()
+            self.attn_plans = plans
+            self.d_bt.copy_(torch.from_numpy(bt))
             aws = pic.pic_attend_workspace_bytes(self.ctx, plans, hq, m.num_layers)
-            self.free(plans)
             self.attn = {
                 "q": q, "hq": hq,
                 "scale": 1.0 / (192 ** 0.5) if m.kind == "mla" else 1.0 / (m.head_dim ** 0.5),
@@ -646,11 +649,27 @@ class Rig:
         self.slot ^= 1
 
     def step(self, kernel_events=None):
-        """One step: plan + table upload + one launch; returns nothing."""
+        """One step: plan + table upload + one launch (in place: one shift
+        launch; attend modes: one decode step over the plans built at set-up,
+        stitched first for attend_cache); returns nothing."""
         if self.mode == "inplace":
             if kernel_events:
                 kernel_events[0].record()
             self.pic.pic_rerotate_inplace(self.ctx, self.k_cache, self.d_bt, self.shift_segs, self.ws_shift)
+            if kernel_events:
+                kernel_events[1].record()
+            return
+        if self.attn is not None:
+            # one decode step over the kept plans (attend_cache: stitched first)
+            plans, a = self.attn_plans, self.attn
+            if kernel_events:
+                kernel_events[0].record()
+            if self.mode == "attend_cache":
+                self.pic.pic_stitch(self.ctx, plans, self.k_pool, self.v_pool, self.k_cache, self.v_cache,
+                                    self.d_bt, self.ridx, self.indptr, self.ws)
+            src = self.pic.PIC_ATTEND_FUSED if self.mode == "attend" else self.pic.PIC_ATTEND_CACHE
+            self.pic.pic_attend_decode(self.ctx, plans, src, a["q"], a["scale"], self.k_pool, self.v_pool,
+                                       self.k_cache, self.v_cache, a["out"], a["lse"], a["ws"], sink_bias=-15.0)
             if kernel_events:
                 kernel_events[1].record()
             return
@@ -660,14 +679,8 @@ class Rig:
         self.upload_tables(bt)
         if kernel_events:
             kernel_events[0].record()
-        if self.mode != "attend":
-            self.pic.pic_stitch(self.ctx, plans, self.k_pool, self.v_pool, self.k_cache, self.v_cache, self.d_bt,
-                                self.ridx, self.indptr, self.ws)
-        if self.attn is not None:
-            a = self.attn
-            src = self.pic.PIC_ATTEND_FUSED if self.mode == "attend" else self.pic.PIC_ATTEND_CACHE
-            self.pic.pic_attend_decode(self.ctx, plans, src, a["q"], a["scale"], self.k_pool, self.v_pool,
-                                       self.k_cache, self.v_cache, a["out"], a["lse"], a["ws"], sink_bias=-15.0)
+        self.pic.pic_stitch(self.ctx, plans, self.k_pool, self.v_pool, self.k_cache, self.v_cache, self.d_bt,
+                            self.ridx, self.indptr, self.ws)
         if kernel_events:
             kernel_events[1].record()
         self.free(plans)
@@ -675,6 +688,8 @@ class Rig:
     def check_status(self):
         ws = self.ws_shift if self.mode == "inplace" else self.ws
         self.pic.pic_query_device_status(self.ctx, ws)
+        if self.attn is not None:
+            self.pic.pic_query_device_status(self.ctx, self.attn["ws"])
 
 
 def run_e2e(rig, steps, warmup, cache_on_host=False):

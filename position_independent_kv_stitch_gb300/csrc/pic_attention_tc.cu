@@ -15,10 +15,14 @@
 // Pseudo-Sinks"): a constant logit offset on the first k tokens of every
 // chunk not at position 0.
 //
-// A tile is up to four plan stages (16 consecutive positions each, read from
-// consecutive rows of one source, one delta) of one (layer, key): 64
-// positions, the M of the score product.  Per tile, with warps by role:
-//   * three producer warps form the tile (its delta entries, whether it
+// A tile is up to four plan stages of one (layer, key), one per 16-row slot:
+// 64 positions, the M of the score product.  A stage is up to 16 consecutive
+// positions read from consecutive rows of one source, with at most two
+// deltas (positions from its split on take the second), so a stage of
+// consecutive rows runs across a chunk boundary.  Per tile, with warps by
+// role:
+//   * three producer warps read the tile's record (formed on the host, the
+//     same in every layer: its stages, their delta entries, whether it
 //     opens or closes its key) and load its rows into a ring of two tiles
 //     with 3-D TMA tile copies, one per 64-dim plane (128-byte swizzle) and
 //     per run of stages that read consecutive rows (boxes of 16 to 64 rows);
@@ -35,7 +39,8 @@
 //   * softmax warps 0-7: warp w owns stage w's positions (TMEM lanes
 //     32 (w % 4) .. + 15 of the M = 64 scores) for half of the heads, read
 //     with the 16x256b shape so that each thread holds two positions.  It
-//     adds the nope partial sums and its delta's hi and lo rope columns,
+//     adds the nope partial sums and each position's delta's hi and lo rope
+//     columns,
 //     keeps a running max per head that is raised only when a score passes
 //     it by more than kTcLazy (log2 units; O and l are then rescaled), writes
 //     P = exp2(s - m) as bf16 hi and lo rows, and at the key's last tile in
@@ -101,10 +106,12 @@ struct TcTile {
   int32_t layer;   // local layer
   int32_t key;
   int32_t flags;   // kTcFirst: first tile of the key in this CTA; kTcLast: its last; kTcEnd: the CTA's last
-  int32_t n_tok[kTcStagesPerTile];
-  int32_t sink[kTcStagesPerTile];
-  int32_t entry[kTcStagesPerTile];  // delta entry of the stage's rope operand
-  int32_t fresh;                    // entries this tile (re)writes
+  int32_t n_tok[kTcStagesPerTile];   // positions of each stage
+  int32_t sink[kTcStagesPerTile];    // their sink bits
+  int32_t entry[kTcStagesPerTile];   // delta entry of the stage's positions [0, split)
+  int32_t entry2[kTcStagesPerTile];  // and of [split, n_tok)
+  int32_t split[kTcStagesPerTile];
+  int32_t fresh;                     // entries this tile (re)writes
   int32_t ent_delta[kTcStagesPerTile];
   int32_t pad[3];
 };
@@ -293,7 +300,7 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
 }
 
 // grid: persistent CTAs, CTA c owns units [U c / G, U (c + 1) / G) of the
-// (layer, stage) list; block: tc_threads(HC) threads (the warp roles above).
+// (layer, tile) list; block: tc_threads(HC) threads (the warp roles above).
 template <int PAIRING, int HC>
 __global__ void __launch_bounds__(tc_threads(HC), 1)
     k_attend_mla_tc(const AttnParams P, const __grid_constant__ TcMaps maps) {
@@ -368,92 +375,54 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   const int prod = warp == kTcProducer ? 0 : (warp >= kTcProducer2 && warp < kTcProducer2 + kNP - 1) ? warp - kTcProducer2 + 1 : -1;
   if (prod >= 0 && has_work) {
     // ------------------------------------------------------------ producer
-    // Forms the tiles and starts their copies.  The next tile's plan stages
-    // (lanes 0-4; the fifth tells whether the key goes on) are read while
-    // the current slot drains, and consecutive stages that read consecutive
-    // rows of one source share one TMA box of 16, 32, 48 or 64 rows.
-    const int n_st = P.n_stages;
-    auto stage_at = [&](int64_t v) -> const AttnStage* {
-      const int lv = static_cast<int>(v / n_st);
-      return P.stages + (v - static_cast<int64_t>(lv) * n_st);
+    // Starts the copies of the CTA's tiles, which the host formed (TcTileRec,
+    // the same in every layer): the next tile's record is read while the
+    // current slot drains, and consecutive stages that read consecutive rows
+    // of one source share one TMA box of 16, 32, 48 or 64 rows.
+    const int tpl = P.tc_tiles_per_layer;
+    const int32_t* recs = reinterpret_cast<const int32_t*>(P.tc_tiles);
+    constexpr int kRecInts = static_cast<int>(sizeof(TcTileRec) / 4);  // 36: lane l reads ints l and 32 + l
+    auto load_rec = [&](int64_t ti, int& a, int& b) {
+      a = 0;
+      b = 0;
+      if (ti < u_end) {
+        const int64_t k = ti - (ti / tpl) * tpl;
+        a = __ldg(recs + k * kRecInts + lane);
+        if (lane < kRecInts - 32) b = __ldg(recs + k * kRecInts + 32 + lane);
+      }
     };
-    int64_t u = u_begin;
-    int4 cw = make_int4(0, 0, 0, 0);
-    if (lane <= kTcStagesPerTile && u + lane < u_end) cw = __ldg(reinterpret_cast<const int4*>(stage_at(u + lane)));
+    int ra, rb;  // the current tile's record
+    load_rec(u_begin, ra, rb);
     int i = 0;
-    int prev_layer = -1, prev_key = -1;
-    int ent_delta[NE];
-    uint32_t ent_valid = 0;
-#pragma unroll
-    for (int e = 0; e < NE; ++e) ent_delta[e] = 0;
     bool failed = false;
     int issued = 0;
-    while (u < u_end) {
+    for (int64_t ti = u_begin; ti < u_end; ++ti, ++i) {
       const int rt = i & 1;
-      AttnTok tk{0, 0};  // first row of this lane's stage
-      if (lane < kTcStagesPerTile && u + lane < u_end) tk = P.toks[cw.x];
-      // the tile is formed (registers only) while its slot drains
-      const int layer = static_cast<int>(u / n_st);
-      const int j = static_cast<int>(u - static_cast<int64_t>(layer) * n_st);
-      TcTile t{};
-      const int key = __shfl_sync(0xffffffffu, cw.z, 0);
-      const bool key_change = layer != prev_layer || key != prev_key;
-      if (key_change) ent_valid = 0;
-      uint32_t used = 0, fresh = 0;
-      int ns = 0;
-#pragma unroll
-      for (int k = 0; k < kTcStagesPerTile; ++k) {
-        const int c_delta = __shfl_sync(0xffffffffu, cw.y, k);
-        const int c_key = __shfl_sync(0xffffffffu, cw.z, k), c_nw = __shfl_sync(0xffffffffu, cw.w, k);
-        if (ns != k) continue;  // the tile already ended
-        if (k > 0 && (j + k >= n_st || u + k >= u_end || c_key != key)) continue;
-        int e = -1;
-#pragma unroll
-        for (int x = 0; x < NE; ++x)
-          if (((ent_valid >> x) & 1u) && ent_delta[x] == c_delta) e = x;
-        if (e < 0) {  // a free entry: not valid, else any this tile does not use
-#pragma unroll
-          for (int x = NE - 1; x >= 0; --x)
-            if (!((used >> x) & 1u) && !((ent_valid >> x) & 1u)) e = x;
-          if (e < 0) {
-#pragma unroll
-            for (int x = NE - 1; x >= 0; --x)
-              if (!((used >> x) & 1u)) e = x;
-          }
-          if (e < 0) continue;  // more distinct deltas than entries: the tile ends here
-#pragma unroll
-          for (int x = 0; x < NE; ++x)
-            if (x == e) ent_delta[x] = c_delta;  // a constant index keeps the entries in registers
-          ent_valid |= 1u << e;
-          fresh |= 1u << e;
-        }
-        used |= 1u << e;
-        t.n_tok[k] = c_nw & 0xffff;
-        t.sink[k] = static_cast<int>(static_cast<uint32_t>(c_nw) >> 16);
-        t.entry[k] = e;
-        ++ns;
-      }
-      t.ns = ns;
-      t.layer = layer;
-      t.key = key;
-      t.fresh = static_cast<int>(fresh);
-#pragma unroll
-      for (int e = 0; e < NE; ++e) t.ent_delta[e] = ent_delta[e];
-      t.flags = key_change ? kTcFirst : 0;
-      const int64_t un = u + ns;
-      const int next_key = __shfl_sync(0xffffffffu, cw.z, ns);  // candidate ns starts the next tile
-      if (un >= u_end) {
-        t.flags |= kTcLast | kTcEnd;
-      } else if (j + ns >= n_st || next_key != key) {
-        t.flags |= kTcLast;
-      }
+      int na, nb;
+      load_rec(ti + 1, na, nb);  // the next tile's, used in the next iteration
+      const int layer = static_cast<int>(ti / tpl);
+      const int ns = __shfl_sync(0xffffffffu, ra, 0), key = __shfl_sync(0xffffffffu, ra, 1);
+      const int rflags = __shfl_sync(0xffffffffu, ra, 2), rfresh = __shfl_sync(0xffffffffu, ra, 3);
+      // lane s < 4 holds stage s (lanes 4-31 a copy of stage lane % 4)
+      const int s4 = lane & 3;
+      const int my_n = __shfl_sync(0xffffffffu, ra, 4 + s4), my_sink = __shfl_sync(0xffffffffu, ra, 8 + s4);
+      const int my_e0 = __shfl_sync(0xffffffffu, ra, 12 + s4), my_e1 = __shfl_sync(0xffffffffu, ra, 16 + s4);
+      const int my_split = __shfl_sync(0xffffffffu, ra, 20 + s4), my_row = __shfl_sync(0xffffffffu, ra, 24 + s4);
+      const int my_src = __shfl_sync(0xffffffffu, ra, 28 + s4), my_ed = __shfl_sync(0xffffffffu, rb, s4);
+      const bool first = ti == u_begin || (rflags & kTcRecKeyFirst);
+      const bool end = ti == u_end - 1;
+      const int flags = (first ? kTcFirst : 0) | ((end || (rflags & kTcRecKeyLast)) ? kTcLast : 0) | (end ? kTcEnd : 0);
+      // at the CTA's first tile every entry it uses is new to the query warp
+      uint32_t used = lane < ns ? ((1u << my_e0) | (my_split < my_n ? (1u << my_e1) : 0u)) : 0u;
+      used = __reduce_or_sync(0xffffffffu, used);
+      const int fresh = ti == u_begin ? static_cast<int>(used) : rfresh;
       // The copies are planned before the slot is free, so that once it is
       // only the announcements and the copies themselves remain.  Stage k
       // continues stage k - 1's box when that stage is full and its rows go on.
-      const int prow = __shfl_up_sync(0xffffffffu, tk.row, 1);
-      const int pflags = __shfl_up_sync(0xffffffffu, tk.flags, 1);
-      const int pn = __shfl_up_sync(0xffffffffu, cw.w & 0xffff, 1);
-      const bool cont = lane > 0 && lane < ns && pn == 16 && pflags == tk.flags && tk.row == prow + 16;
+      const int prow = __shfl_up_sync(0xffffffffu, my_row, 1);
+      const int pflags = __shfl_up_sync(0xffffffffu, my_src, 1);
+      const int pn = __shfl_up_sync(0xffffffffu, my_n, 1);
+      const bool cont = lane > 0 && lane < ns && pn == 16 && pflags == my_src && my_row == prow + 16;
       const uint32_t cmask = __ballot_sync(0xffffffffu, cont);
       const bool leader = lane < ns && !cont;
       const uint32_t lmask = __ballot_sync(0xffffffffu, leader);
@@ -474,8 +443,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         uint32_t m = lmask;
         for (int x = 0; x < g && m; ++x) m &= m - 1;  // drop the first g leaders
         const int src = m ? __ffs(m) - 1 : 0;
-        cp_row[r] = __shfl_sync(0xffffffffu, tk.row, src);
-        const int fl = __shfl_sync(0xffffffffu, tk.flags, src);
+        cp_row[r] = __shfl_sync(0xffffffffu, my_row, src);
+        const int fl = __shfl_sync(0xffffffffu, my_src, src);
         cp_len[r] = __shfl_sync(0xffffffffu, my_len, src);
         cp_pl[r] = g < ngroups ? q - g * kTcPlanes : kTcPlanes;
         cp_dst[r] = base_u32 + L::kRing + rt * kTcTileBytes + src * kTcStageBytes + cp_pl[r] * kTcPlaneBytes;
@@ -489,9 +458,25 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         failed = true;
         break;
       }
-      if (prod == 0 && lane == 0) {
-        tiles[rt] = t;
-        mbar_arrive(&meta_ready[rt]);
+      if (prod == 0) {
+        TcTile& t = tiles[rt];
+        if (lane < 4) {
+          t.n_tok[lane] = my_n;
+          t.sink[lane] = my_sink;
+          t.entry[lane] = my_e0;
+          t.entry2[lane] = my_e1;
+          t.split[lane] = my_split;
+          t.ent_delta[lane] = my_ed;
+        }
+        if (lane == 0) {
+          t.ns = ns;
+          t.layer = layer;
+          t.key = key;
+          t.flags = flags;
+          t.fresh = fresh;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta_ready[rt]);
       }
       // test hook (pic_debug_stall_next_launch): CTA 0 leaves this tile's rows
       // unrequested, so the waits for them run out and take the failure path
@@ -504,12 +489,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           if (cp_pl[r] < kTcPlanes) tma_load_3d(cp_dst[r], cp_map[r], 64 * cp_pl[r], cp_row[r], z, &full[rt]);
       }
       issued = i + 1;
-      cw = make_int4(0, 0, 0, 0);
-      if (lane <= kTcStagesPerTile && un + lane < u_end) cw = __ldg(reinterpret_cast<const int4*>(stage_at(un + lane)));
-      prev_layer = layer;
-      prev_key = key;
-      u = un;
-      ++i;
+      ra = na;
+      rb = nb;
     }
     if (failed) {
       if (lane == 0) fail();
@@ -723,6 +704,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const bool present = w < tr.ns;
       const int n_tok = present ? tr.n_tok[w] : 0;
       const int entry = present ? tr.entry[w] : 0;
+      const int entry2 = present ? tr.entry2[w] : 0;
+      const int split = present ? tr.split[w] : 16;
       const int sink = present ? tr.sink[w] : 0;
       float s[NR];
       bool need = false;
@@ -735,7 +718,10 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             l_part[j] = 0.0f;
           }
         }
-        float sp[NP][NR], rr[2 * NR];  // latent partial sums; the rope hi then lo columns
+        // latent partial sums; the rope hi then lo columns of the slot's first
+        // delta and then, when the slot holds a second one from position split
+        // on, of that one (read into the same registers)
+        float sp[NP][NR], rr[2 * NR], nope[NR];
         const uint32_t sc = tl + rt * kTcSCols + h0;
         tmem_ld16x256<2 * NG>(sc + kRopeCol + entry * 2 * HC + h0, rr);
 #pragma unroll
@@ -743,13 +729,24 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         tmem_wait_ld();
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
+          nope[r] = sp[0][r];
+#pragma unroll
+          for (int pp = 1; pp < NP; ++pp) nope[r] += sp[pp][r];
+          s[r] = (nope[r] + rr[r]) + rr[NR + r];
+        }
+        if (split < n_tok) {  // the same for the whole warp
+          tmem_ld16x256<2 * NG>(sc + kRopeCol + entry2 * 2 * HC + h0, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < NR; ++r)
+            if (q0 + 8 * ((r >> 1) & 1) >= split) s[r] = (nope[r] + rr[r]) + rr[NR + r];
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
           const int q = q0 + 8 * ((r >> 1) & 1);
           const bool live = q < n_tok;
           const float bias = (live && ((sink >> q) & 1)) ? P.sink_log2 : 0.0f;
-          float v = sp[0][r];
-#pragma unroll
-          for (int pp = 1; pp < NP; ++pp) v += sp[pp][r];
-          s[r] = live ? ((v + rr[r]) + rr[NR + r]) * P.scale_log2 + bias : -INFINITY;
+          s[r] = live ? s[r] * P.scale_log2 + bias : -INFINITY;
           need |= s[r] > m_run[2 * (r >> 2) + (r & 1)] + kTcLazy;
         }
       }

@@ -22,6 +22,7 @@
 #include <set>
 #include <string>
 #include <unordered_map>
+#include <memory>
 #include <vector>
 
 #include "pic_internal.h"
@@ -135,6 +136,7 @@ int vectorized_bytes_ok(const void* p) { return (reinterpret_cast<uintptr_t>(p) 
 
 struct pic_plan {
   pic_ctx* owner;
+  uint64_t serial = 0;          // unique within the context: names this plan in caches
   std::vector<Segment> segs;
   std::vector<int32_t> table;   // the request's block table (mapped + fresh blocks)
   std::vector<int32_t> fresh;   // blocks this plan took from the allocator
@@ -182,6 +184,12 @@ struct pic_ctx {
   // pic_debug_stall_next_launch: consumed by the next pic_stitch or pic_attend_decode
   int32_t debug_stall = 0;   // tile + 1, 0 = off
   uint32_t debug_spins = 0;  // 0 = the default wait bound
+  uint64_t plan_serial = 0;  // last serial given to a plan
+  // The last decode-attention plan of each stage form (one delta per stage,
+  // or up to two), reused while the same plans (by serial and in-place
+  // state), source and head layout come back: a decode loop attends to the
+  // same composed requests every step.
+  std::shared_ptr<void> attn_cache[2];
   pic_ctx(int32_t nb) : num_cache_blocks(nb), alloc(nb) {}
 };
 
@@ -641,6 +649,7 @@ void fill_freq(const pic_ctx* ctx, uint8_t* base, const WsLayout& w) {
 // kernel walks (layer, stage) units.
 struct AttnPlan {
   std::vector<pic::AttnStage> stages;
+  std::vector<int4> ext;  // per stage: first token's {row, flags}, second delta, split (16: none)
   std::vector<pic::AttnTok> toks;
   std::vector<int32_t> key_stage_begin;  // [n_keys + 1]
   int32_t heads_per_cta = 0, head_groups = 0, n_keys = 0;
@@ -690,8 +699,10 @@ bool attn_layout_heads(const pic_model_desc& m, int32_t num_q_heads, AttnHeads* 
   return true;
 }
 
+// two_deltas (MLA on tcgen05): a stage of consecutive rows may go on across
+// one change of delta; the positions from its split on take the second delta.
 void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
-                 const AttnHeads& heads, AttnPlan* out) {
+                 const AttnHeads& heads, bool two_deltas, AttnPlan* out) {
   const int32_t bs = ctx->model.block_size;
   const int32_t ST = pic::kAttnStageTokens;
   const bool mla = ctx->model.kind == PIC_KIND_MLA;
@@ -700,6 +711,7 @@ void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req
   out->n_keys = n_req * out->head_groups;
   out->key_stage_begin.assign(1, 0);
   std::vector<pic::AttnStage> req_stages;
+  std::vector<int4> req_ext;
   for (int32_t r = 0; r < n_req; ++r) {
     const pic_plan* pl = plans[r];
     const int32_t T = pl->total_tokens;
@@ -726,19 +738,31 @@ void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req
       }
     }
     req_stages.clear();
+    req_ext.clear();
     for (int32_t p = 0; p < T;) {
       pic::AttnStage st{};
       st.tok_off = tok_off + p;
       st.delta = deltas[p];
-      int32_t n = 0;
+      int32_t n = 0, split = ST, d2 = 0;
       // MLA stages also read consecutive rows of one source (one TMA box)
-      while (p + n < T && n < ST && deltas[p + n] == st.delta &&
+      while (p + n < T && n < ST &&
              (!mla || n == 0 || (tk[p + n].flags == tk[p].flags && tk[p + n].row == tk[p].row + n))) {
+        const int32_t d = deltas[p + n];
+        if (split == ST) {
+          if (d != st.delta) {
+            if (!two_deltas) break;
+            split = n;  // the one change of delta a stage may hold
+            d2 = d;
+          }
+        } else if (d != d2) {
+          break;
+        }
         if (sink[p + n]) st.sink_mask |= static_cast<uint16_t>(1u << n);
         ++n;
       }
       st.n_tok = static_cast<uint16_t>(n);
       req_stages.push_back(st);
+      req_ext.push_back(make_int4(tk[p].row, tk[p].flags, d2, split));
       p += n;
     }
     for (int32_t hg = 0; hg < out->head_groups; ++hg) {
@@ -746,13 +770,129 @@ void attend_plan(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req
         st.key = r * out->head_groups + hg;
         out->stages.push_back(st);
       }
+      out->ext.insert(out->ext.end(), req_ext.begin(), req_ext.end());
       out->key_stage_begin.push_back(static_cast<int32_t>(out->stages.size()));
     }
   }
 }
 
+// The attention plan of a call, from the context's one-entry cache when the
+// same plans (serials and in-place state), source and head layout were
+// planned last; pool_rows: one past the last pool row the plan reads.
+struct AttnPlanCache {
+  std::vector<uint64_t> key;
+  AttnPlan plan;
+  int64_t pool_rows = 0;
+  // two-delta plans (MLA on tcgen05): one layer's tiles and each key's first
+  // tile (n_keys + 1 entries)
+  std::vector<pic::TcTileRec> tiles;
+  std::vector<int32_t> key_tile_begin;
+};
+
+// The tiles of the tcgen05 MLA attention for one layer (every layer has the
+// same stages).  Within a key, stages fill tiles of up to four in order.  Each
+// delta of a stage takes an entry of rotated query rows: the entry that holds
+// it, else a free one (holding nothing), else one the tile does not use; a
+// stage that finds no entry starts the next tile.  Entries start empty at each
+// key.
+void tc_tiles(const AttnPlan& plan, int ne, std::vector<pic::TcTileRec>* tiles, std::vector<int32_t>* key_tile_begin) {
+  tiles->clear();
+  key_tile_begin->assign(1, 0);
+  for (int32_t k = 0; k < plan.n_keys; ++k) {
+    const int32_t end = plan.key_stage_begin[k + 1];
+    int32_t ent_delta[4] = {0, 0, 0, 0};
+    uint32_t valid = 0;
+    bool first = true;
+    for (int32_t j = plan.key_stage_begin[k]; j < end;) {
+      pic::TcTileRec t{};
+      t.key = k;
+      uint32_t used = 0, fresh = 0;
+      auto find = [&](int32_t d, uint32_t skip) {
+        for (int x = 0; x < ne; ++x)
+          if (((valid >> x) & 1u) && !((skip >> x) & 1u) && ent_delta[x] == d) return x;
+        return -1;
+      };
+      auto pick = [&](uint32_t busy) {
+        for (int x = 0; x < ne; ++x)
+          if (!((busy >> x) & 1u) && !((valid >> x) & 1u)) return x;
+        for (int x = 0; x < ne; ++x)
+          if (!((busy >> x) & 1u)) return x;
+        return -1;
+      };
+      while (t.ns < 4 && j < end) {
+        const pic::AttnStage& st = plan.stages[j];
+        const int4 x = plan.ext[j];
+        const bool two = x.w < st.n_tok;
+        uint32_t busy = used;
+        int e1 = find(st.delta, 0u);
+        const bool new1 = e1 < 0;
+        if (new1) e1 = pick(busy);
+        if (e1 < 0) break;
+        busy |= 1u << e1;
+        int e2 = e1;
+        bool new2 = false;
+        if (two) {
+          e2 = find(x.z, new1 ? (1u << e1) : 0u);  // an entry just taken no longer holds what it held
+          new2 = e2 < 0;
+          if (new2) e2 = pick(busy);
+          if (e2 < 0) break;
+          busy |= 1u << e2;
+        }
+        if (new1) ent_delta[e1] = st.delta;
+        if (new2) ent_delta[e2] = x.z;
+        const uint32_t took = (new1 ? (1u << e1) : 0u) | (new2 ? (1u << e2) : 0u);
+        valid |= took;
+        fresh |= took;
+        used = busy;
+        const int s4 = t.ns;
+        t.n_tok[s4] = st.n_tok;
+        t.sink[s4] = st.sink_mask;
+        t.entry[s4] = e1;
+        t.entry2[s4] = e2;
+        t.split[s4] = two ? x.w : 16;
+        t.row[s4] = x.x;
+        t.src[s4] = x.y;
+        ++t.ns;
+        ++j;
+      }
+      t.fresh = static_cast<int32_t>(fresh);
+      for (int e = 0; e < 4; ++e) t.ent_delta[e] = ent_delta[e];
+      t.flags = (first ? pic::kTcRecKeyFirst : 0) | (j >= end ? pic::kTcRecKeyLast : 0);
+      first = false;
+      tiles->push_back(t);
+    }
+    key_tile_begin->push_back(static_cast<int32_t>(tiles->size()));
+  }
+}
+
+const AttnPlanCache& attend_plan_cached(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
+                                        const AttnHeads& heads, bool two_deltas) {
+  std::vector<uint64_t> key;
+  key.reserve(2 * static_cast<size_t>(n_req) + 5);
+  for (int32_t r = 0; r < n_req; ++r) {
+    key.push_back(plans[r]->serial);
+    key.push_back(plans[r]->applied ? 1u : 0u);
+  }
+  key.push_back(static_cast<uint64_t>(source));
+  key.push_back(static_cast<uint64_t>(heads.hb));
+  key.push_back(static_cast<uint64_t>(heads.head_groups));
+  key.push_back(static_cast<uint64_t>(heads.group));
+  key.push_back(two_deltas ? 1u : 0u);
+  std::shared_ptr<void>& slot = ctx->attn_cache[two_deltas ? 1 : 0];
+  auto* c = static_cast<AttnPlanCache*>(slot.get());
+  if (c && c->key == key) return *c;
+  auto fresh = std::make_shared<AttnPlanCache>();
+  attend_plan(ctx, plans, n_req, source, heads, two_deltas, &fresh->plan);
+  for (const pic::AttnTok& t : fresh->plan.toks)
+    if (!(t.flags & pic::kAttnFromCache)) fresh->pool_rows = std::max<int64_t>(fresh->pool_rows, int64_t{t.row} + 1);
+  if (two_deltas) tc_tiles(fresh->plan, heads.group == 16 ? 4 : 2, &fresh->tiles, &fresh->key_tile_begin);
+  fresh->key = std::move(key);
+  slot = fresh;
+  return *fresh;
+}
+
 struct AttnLayout {
-  size_t freq_off, stages_off, toks_off, keys_off, records_off, total;
+  size_t freq_off, stages_off, tiles_off, toks_off, keys_off, records_off, total;
 };
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
@@ -788,12 +928,13 @@ bool encode_mla_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t l
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-AttnLayout attend_layout(const pic_ctx* ctx, size_t n_stages, size_t n_toks, size_t n_key_entries,
+AttnLayout attend_layout(const pic_ctx* ctx, size_t n_stages, size_t n_tiles, size_t n_toks, size_t n_key_entries,
                          size_t n_records, const AttnHeads& heads) {
   AttnLayout w;
   w.freq_off = pic::align_up(sizeof(WsHeader), pic::kWsAlign);
   w.stages_off = pic::align_up(w.freq_off + ctx->freq_turns.size() * sizeof(float2), pic::kWsAlign);
-  w.toks_off = pic::align_up(w.stages_off + n_stages * sizeof(pic::AttnStage), pic::kWsAlign);
+  w.tiles_off = pic::align_up(w.stages_off + n_stages * sizeof(pic::AttnStage), pic::kWsAlign);
+  w.toks_off = pic::align_up(w.tiles_off + n_tiles * sizeof(pic::TcTileRec), pic::kWsAlign);
   w.keys_off = pic::align_up(w.toks_off + n_toks * sizeof(pic::AttnTok), pic::kWsAlign);
   w.records_off = pic::align_up(w.keys_off + n_key_entries * sizeof(pic::AttnKey), pic::kWsAlign);
   const size_t rec = static_cast<size_t>(pic::attn_record_floats(heads.group, heads.vdim, heads.hb)) * 4;
@@ -804,6 +945,27 @@ AttnLayout attend_layout(const pic_ctx* ctx, size_t n_stages, size_t n_toks, siz
 // Records of a persistent grid of `ctas` over `layers` x plan.stages units:
 // CTA c owns units [U c / N, U (c + 1) / N); each (layer, key) gets one
 // record per CTA whose range touches it, written at rec_base + (c - first_cta).
+// The same for a grid over (layer, tile) units: key k of a layer covers its
+// tiles [key_tile_begin[k], key_tile_begin[k + 1]).
+int64_t attend_keys_tiles(const std::vector<int32_t>& key_tile_begin, int32_t layers, int64_t ctas,
+                          std::vector<pic::AttnKey>* keys) {
+  const int32_t n_keys = static_cast<int32_t>(key_tile_begin.size()) - 1;
+  const int64_t tpl = key_tile_begin.back();
+  const int64_t U = tpl * layers;
+  auto cta_of = [&](int64_t u) { return ((u + 1) * ctas - 1) / U; };
+  int64_t rec = 0;
+  if (keys) keys->clear();
+  for (int32_t l = 0; l < layers; ++l)
+    for (int32_t k = 0; k < n_keys; ++k) {
+      const int64_t a = l * tpl + key_tile_begin[k], b = l * tpl + key_tile_begin[k + 1];
+      const int64_t c0 = cta_of(a), c1 = cta_of(b - 1);
+      if (keys) keys->push_back(pic::AttnKey{static_cast<int32_t>(rec), static_cast<int32_t>(c0)});
+      rec += c1 - c0 + 1;
+    }
+  if (keys) keys->push_back(pic::AttnKey{static_cast<int32_t>(rec), 0});
+  return rec;
+}
+
 int64_t attend_keys(const AttnPlan& plan, int32_t layers, int64_t ctas, std::vector<pic::AttnKey>* keys) {
   const int64_t nsl = static_cast<int64_t>(plan.stages.size());
   const int64_t U = nsl * layers;
@@ -1161,6 +1323,7 @@ pic_status pic_build_block_table(pic_ctx* ctx, const pic_request_desc* rq, int32
   for (size_t i = 0, f = 0; i < table.size(); ++i)
     if (table[i] < 0) table[i] = plan->fresh[f++];
   plan->owner = ctx;
+  plan->serial = ++ctx->plan_serial;
   plan->table = std::move(table);
   plan->segs = std::move(segs);
   plan->total_tokens = static_cast<int32_t>(total);
@@ -1451,14 +1614,16 @@ size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* pla
     if (!plans[r]) return 0;
   AttnHeads heads;
   if (!attn_layout_heads(ctx->model, num_q_heads, &heads)) return 0;
+  const bool mla = ctx->model.kind == PIC_KIND_MLA;
   AttnPlan fused, cache;
-  attend_plan(ctx, plans, n_req, PIC_ATTEND_FUSED, heads, &fused);
-  attend_plan(ctx, plans, n_req, PIC_ATTEND_CACHE, heads, &cache);
+  attend_plan(ctx, plans, n_req, PIC_ATTEND_FUSED, heads, false, &fused);  // two-delta stages are never more
+  attend_plan(ctx, plans, n_req, PIC_ATTEND_CACHE, heads, false, &cache);
   const size_t n_stages = std::max(fused.stages.size(), cache.stages.size());
   // a grid of at most kAttnMaxCtas CTAs adds at most one record per CTA
   const size_t n_keys = static_cast<size_t>(num_layers) * fused.n_keys;
   const size_t records = n_keys + pic::kAttnMaxCtas;
-  return attend_layout(ctx, n_stages, fused.toks.size(), n_keys + 1, records, heads).total;
+  // the tcgen05 kernel's tiles: at most one per stage
+  return attend_layout(ctx, n_stages, mla ? n_stages : 0, fused.toks.size(), n_keys + 1, records, heads).total;
 }
 
 pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t source,
@@ -1509,19 +1674,17 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
     return fail(ctx, PIC_ERR_ALIGNMENT, "q, out, pools, caches, strides and workspace must be 16-byte aligned");
   for (int32_t r = 0; r < n_req; ++r)
     if (plans[r]->total_tokens == 0) return fail(ctx, PIC_ERR_RANGE, "plans[%d] has no context to attend", r);
-  AttnPlan plan;
-  attend_plan(ctx, plans, n_req, source, heads, &plan);
-
-  // MLA on tcgen05 when the pool and cache can be described as TMA tensors
+  // MLA on tcgen05 when the pool and cache can be described as TMA tensors;
+  // its stages may hold two deltas, the other kernels' one
   int ring = 0;
   size_t smem = 0;
   pic::TcMaps maps;
-  bool tc = mla && ctx->attend_tc && pic::attend_mla_tc_config(heads.group, &smem);
+  const bool tc_fits = mla && ctx->attend_tc && pic::attend_mla_tc_config(heads.group, &smem);
+  const AttnPlanCache* cached = &attend_plan_cached(ctx, plans, n_req, source, heads, tc_fits);
+  bool tc = tc_fits;
   if (tc) {
     // the pool view spans the rows the plan reads; the cache view every cache row
-    int64_t pool_rows = 0;
-    for (const pic::AttnTok& t : plan.toks)
-      if (!(t.flags & pic::kAttnFromCache)) pool_rows = std::max<int64_t>(pool_rows, int64_t{t.row} + 1);
+    const int64_t pool_rows = cached->pool_rows;
     const int64_t layers = static_cast<int64_t>(layer_begin) + num_layers;
     for (int g = 0; g < 4 && tc; ++g) {
       const uint32_t box = 16u * static_cast<uint32_t>(g + 1);
@@ -1531,10 +1694,13 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
       if (tc && pool_rows == 0) maps.pool[g] = maps.cache[g];  // nothing is read from the pool
     }
   }
+  if (tc_fits && !tc) cached = &attend_plan_cached(ctx, plans, n_req, source, heads, false);
+  const AttnPlan& plan = cached->plan;
   const bool fits = tc || (mla ? pic::attend_mla_config(heads.mla_ng, &ring, &smem)
                                : pic::attend_config(m.head_dim, heads.group, heads.hb, &ring, &smem));
   if (!fits) return fail(ctx, PIC_ERR_UNSUPPORTED, "attention stages do not fit in shared memory");
-  const int64_t units = static_cast<int64_t>(plan.stages.size()) * num_layers;
+  // units: (layer, stage), or (layer, tile) for the tcgen05 kernel
+  const int64_t units = static_cast<int64_t>(tc ? cached->tiles.size() : plan.stages.size()) * num_layers;
   if (units > INT32_MAX || static_cast<int64_t>(plan.toks.size()) > INT32_MAX)
     return fail(ctx, PIC_ERR_CAPACITY, "attention batch too large");
 
@@ -1551,8 +1717,9 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   if (per_sm <= 0) return fail(ctx, PIC_ERR_CUDA, "attention kernel does not fit on an SM");
   const int64_t ctas = std::min<int64_t>({units, static_cast<int64_t>(di.sm_count) * per_sm, pic::kAttnMaxCtas});
   std::vector<pic::AttnKey> keys;
-  const int64_t records = attend_keys(plan, num_layers, ctas, &keys);
-  const AttnLayout w = attend_layout(ctx, plan.stages.size(), plan.toks.size(), keys.size(),
+  const int64_t records = tc ? attend_keys_tiles(cached->key_tile_begin, num_layers, ctas, &keys)
+                            : attend_keys(plan, num_layers, ctas, &keys);
+  const AttnLayout w = attend_layout(ctx, plan.stages.size(), tc ? cached->tiles.size() : 0, plan.toks.size(), keys.size(),
                                      static_cast<size_t>(records), heads);
   if (ws_bytes < w.total) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
 
@@ -1564,6 +1731,7 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   uint8_t* base = sl->host;
   std::memcpy(base + w.freq_off, ctx->freq_turns.data(), ctx->freq_turns.size() * sizeof(float2));
   std::memcpy(base + w.stages_off, plan.stages.data(), plan.stages.size() * sizeof(pic::AttnStage));
+  if (tc) std::memcpy(base + w.tiles_off, cached->tiles.data(), cached->tiles.size() * sizeof(pic::TcTileRec));
   std::memcpy(base + w.toks_off, plan.toks.data(), plan.toks.size() * sizeof(pic::AttnTok));
   std::memcpy(base + w.keys_off, keys.data(), keys.size() * sizeof(pic::AttnKey));
   st = upload_staging(ctx, sl, d_ws, image, s);
@@ -1575,6 +1743,8 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   p.stages = reinterpret_cast<const pic::AttnStage*>(ws + w.stages_off);
   p.n_stages = static_cast<int32_t>(plan.stages.size());
   p.toks = reinterpret_cast<const pic::AttnTok*>(ws + w.toks_off);
+  p.tc_tiles = reinterpret_cast<const pic::TcTileRec*>(ws + w.tiles_off);
+  p.tc_tiles_per_layer = tc ? static_cast<int32_t>(cached->tiles.size()) : 0;
   p.keys = reinterpret_cast<const pic::AttnKey*>(ws + w.keys_off);
   p.n_keys = plan.n_keys;
   p.n_units = units;

@@ -121,7 +121,8 @@ constexpr int32_t kAttnFromCache = 1 << 8;  // AttnTok.flags: row is a paged-cac
 
 struct AttnStage {
   int32_t tok_off;     // first entry of the stage in the token list
-  int32_t delta;       // every key of the stage is rotated by R(delta)
+  int32_t delta;       // every key of the stage is rotated by R(delta) (MLA on tcgen05: the keys
+                       // before the stage's split; see TcTileRec)
   int32_t key;         // request * head_groups + head group
   uint16_t n_tok;      // 1 .. kAttnStageTokens
   uint16_t sink_mask;  // bit t: position t is a LegoLink pseudo-sink
@@ -142,6 +143,8 @@ struct AttnParams {
   const AttnStage* stages;  // one layer's stages, key-major
   int32_t n_stages;
   const AttnTok* toks;
+  const struct TcTileRec* tc_tiles;  // MLA on tcgen05: one layer's tiles (the same in every layer)
+  int32_t tc_tiles_per_layer;        // n_units then counts (layer, tile) units
   const AttnKey* keys;      // [n_layers * n_keys + 1]
   int32_t n_keys;
   int64_t n_units;          // n_layers * n_stages
@@ -206,6 +209,30 @@ cudaError_t launch_attend_merge_mla(const AttnParams& p, int heads_per_record, c
 // pool and the paged cache as [layers][rows][576] bf16 with 128-byte swizzle
 // and a box of 64 dims x 16 (g + 1) rows for map g; every stage of the plan
 // reads consecutive rows of one of them.
+// One tile of the tcgen05 MLA attention, formed on the host: up to four plan
+// stages of one key, one per 16-row slot of the shared-memory ring.  A stage
+// is up to 16 positions read from consecutive rows of one source and holds
+// one or two deltas (positions from split on take the second); each delta
+// uses one of the tile's entries of rotated query rows (at most 4 entries at
+// 16 heads per CTA, 2 at 32).  Every layer has the same tiles.
+constexpr int kTcRecKeyFirst = 1;  // the key's first tile in the layer
+constexpr int kTcRecKeyLast = 2;   // its last
+struct TcTileRec {
+  int32_t ns;            // stages
+  int32_t key;
+  int32_t flags;         // kTcRecKeyFirst | kTcRecKeyLast
+  int32_t fresh;         // entries first used (or given a new delta) since the key's previous tile
+  int32_t n_tok[4];
+  int32_t sink[4];       // bit t: position t is a LegoLink pseudo-sink
+  int32_t entry[4];      // entry of the stage's positions [0, split)
+  int32_t entry2[4];     // entry of [split, n_tok)
+  int32_t split[4];      // 16: one delta
+  int32_t row[4];        // first source row of the stage
+  int32_t src[4];        // its source (kAttnFromCache or 0)
+  int32_t ent_delta[4];  // the delta each entry holds after this tile
+};
+static_assert(sizeof(TcTileRec) == 144, "TcTileRec layout: 36 ints");
+
 struct TcMaps {
   CUtensorMap pool[4];
   CUtensorMap cache[4];

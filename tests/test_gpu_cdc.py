@@ -77,9 +77,10 @@ def _assert_same(got, want, cap=None):
 EDGE_LENGTHS = [0, 1, 31, 32, 33, 63, 64, 65, 0, 0, 127, 8191, 2, 8192, 8193, 20000, 1, 300, 0, 5000]
 
 
-@pytest.mark.parametrize("mean", [16, 64, 256])
+@pytest.mark.parametrize("mean", [16, 24, 32, 64, 256])
 def test_edge_lengths_match_oracle(pic, mean):
-    """Empty, tiny and tile-straddling documents (tiles are 8192 tokens)."""
+    """Empty, tiny and tile-straddling documents (tiles are 8192 tokens),
+    from about 512 chunks a tile (mean 16) down to about 32 (mean 256)."""
     tokens, offsets, gear = _corpus(EDGE_LENGTHS)
     thr = oracle.threshold_for_mean(mean)
     got = _gpu(pic, tokens, offsets, gear, thr)
