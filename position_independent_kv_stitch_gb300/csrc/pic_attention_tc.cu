@@ -501,9 +501,10 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   } else if (warp == kTcQuery && has_work) {
     // --------------------------------------------------------------- query
     // Writes each tile's query operands: q_nope on a key change, and for each
-    // fresh delta entry R(-delta) q_rope as bf16 hi and lo rows; the previous
-    // tile's score product must be done reading them.
+    // fresh delta entry R(-delta) q_rope as bf16 hi and lo rows, once no
+    // earlier score product still reads what they replace.
     float qa[HC], qb[HC];  // this lane's rope pair of every head (lane f: frequency f)
+    uint32_t used_prev = 0;  // entries the previous tile read
 #pragma unroll
     for (int h = 0; h < HC; ++h) qa[h] = qb[h] = 0.0f;
     const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
@@ -515,8 +516,17 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       }
       const TcTile t = tiles[rt];
       const bool key_change = (t.flags & kTcFirst) != 0;
+      uint32_t used = 0;  // entries this tile reads
+#pragma unroll
+      for (int st = 0; st < kTcStagesPerTile; ++st)
+        if (st < t.ns) used |= (1u << t.entry[st]) | (t.split[st] < t.n_tok[st] ? (1u << t.entry2[st]) : 0u);
       if (key_change || t.fresh) {
-        if (i >= 1 && !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins))) {
+        // Tile i - 2's score product is done (its value product freed the
+        // slot tile i loads into); tile i - 1's may still read q_nope and its
+        // entries, so wait for it when either is about to be rewritten.
+        const bool clash = key_change || (static_cast<uint32_t>(t.fresh) & used_prev) != 0u;
+        if (i >= 1 && clash &&
+            !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins))) {
           if (lane == 0) fail();
           break;
         }
@@ -565,6 +575,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rope_full[rt]);
+      used_prev = used;
       if (t.flags & kTcEnd) break;
     }
   } else if ((warp == kTcMma || warp == kTcMma2 || warp == kTcPv || warp == kTcPv2) && has_work) {
@@ -576,23 +587,28 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     // low bits, and no start here reaches 256 KB), so each product builds its
     // base descriptors once and steps them by constants.
     if (warp == kTcMma || warp == kTcMma2) {
-      // S of tile i once its rows and query operands are in and its TMEM
-      // buffer is free (the softmax of tile i - 2 has written P, so it is
-      // done reading that buffer).  With two issuers the first takes the even
-      // latent k-steps and the rope plane, the second the odd k-steps; each
-      // writes its own partial sums (k-step mod NP).
+      // S of tile i once its rows are in and its TMEM buffer is free (the
+      // softmax of tile i - 2 has written P, so it is done reading that
+      // buffer); the latent k-steps also wait for the query operands at a
+      // key's first tile (q_nope changes), the rope k-steps always.  With two
+      // issuers the first takes the even latent k-steps and the rope plane,
+      // the second the odd k-steps; each writes its own partial sums (k-step
+      // mod NP).
       const int par = warp == kTcMma ? 0 : 1;
       const uint64_t dq = sdesc(base_u32 + L::kQn, 16, 1024), dr = sdesc(base_u32 + L::kRope, 16, 1024);
       for (int i = 0;; ++i) {
         const int rt = i & 1;
-        const bool ok = wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag, spins) &&
-                        wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins) &&
-                        (i < 2 || wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag, spins));
+        bool ok = wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag, spins) &&
+                  (i < 2 || wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag, spins));
+        const int flags = ok ? tiles[rt].flags : 0;
+        // q_nope changes at a key's first tile; otherwise only the rope
+        // k-steps wait for the query warp's rotated rows
+        const bool q_new = (flags & kTcFirst) != 0;
+        if (ok && q_new) ok = wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins);
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) fail();
           break;
         }
-        const int flags = tiles[rt].flags;
         tc_fence_after();
         const uint64_t da = sdesc(ring + rt * kTcTileBytes, 16, 1024);
         const uint32_t d = tmem + rt * kTcSCols;
@@ -603,6 +619,13 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
                        dq + (((ks >> 2) * L::kQnPlane + (ks & 3) * 32) >> 4), kIdS, ks >= NP);
         }
         if (par == 0) {
+          if (!q_new) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins))) {
+              if (lane == 0) fail();
+              break;
+            }
+            tc_fence_after();
+          }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             tc_mma_elect(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);

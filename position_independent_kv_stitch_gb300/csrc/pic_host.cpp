@@ -792,16 +792,17 @@ struct AttnPlanCache {
 // The tiles of the tcgen05 MLA attention for one layer (every layer has the
 // same stages).  Within a key, stages fill tiles of up to four in order.  Each
 // delta of a stage takes an entry of rotated query rows: the entry that holds
-// it, else a free one (holding nothing), else one the tile does not use; a
-// stage that finds no entry starts the next tile.  Entries start empty at each
-// key.
+// it, else a free one (holding nothing), else one neither this tile nor the
+// previous one uses (its rewrite need not wait for the previous tile's score
+// product), else one this tile does not use; a stage that finds no entry
+// starts the next tile.  Entries start empty at each key.
 void tc_tiles(const AttnPlan& plan, int ne, std::vector<pic::TcTileRec>* tiles, std::vector<int32_t>* key_tile_begin) {
   tiles->clear();
   key_tile_begin->assign(1, 0);
   for (int32_t k = 0; k < plan.n_keys; ++k) {
     const int32_t end = plan.key_stage_begin[k + 1];
     int32_t ent_delta[4] = {0, 0, 0, 0};
-    uint32_t valid = 0;
+    uint32_t valid = 0, prev_used = 0;
     bool first = true;
     for (int32_t j = plan.key_stage_begin[k]; j < end;) {
       pic::TcTileRec t{};
@@ -815,6 +816,8 @@ void tc_tiles(const AttnPlan& plan, int ne, std::vector<pic::TcTileRec>* tiles, 
       auto pick = [&](uint32_t busy) {
         for (int x = 0; x < ne; ++x)
           if (!((busy >> x) & 1u) && !((valid >> x) & 1u)) return x;
+        for (int x = 0; x < ne; ++x)
+          if (!((busy >> x) & 1u) && !((prev_used >> x) & 1u)) return x;
         for (int x = 0; x < ne; ++x)
           if (!((busy >> x) & 1u)) return x;
         return -1;
@@ -859,6 +862,7 @@ void tc_tiles(const AttnPlan& plan, int ne, std::vector<pic::TcTileRec>* tiles, 
       for (int e = 0; e < 4; ++e) t.ent_delta[e] = ent_delta[e];
       t.flags = (first ? pic::kTcRecKeyFirst : 0) | (j >= end ? pic::kTcRecKeyLast : 0);
       first = false;
+      prev_used = used;
       tiles->push_back(t);
     }
     key_tile_begin->push_back(static_cast<int32_t>(tiles->size()));
