@@ -5,10 +5,11 @@
 // 2.1-2.2: every query head h attends to the shared latent rows
 // row_t = [cKV_t (512) | k_r,t (64)], with the query absorbed into the latent
 // space, q_h = [q_nope,h (512) | q_rope,h (64)].  A chunk token's rope key is
-// used as stored and the query's rope part is rotated by R(-delta) instead
-// (q . R(delta) k = (R(-delta) q) . k, R orthogonal), so no rotated copy is
-// written:
-//   s_h,t = scale * [q_nope,h | R(-delta_t) q_rope,h] . row_t + bias_t,
+// used rotated by its chunk's delta, which needs no rotated copy: either the
+// query's rope part is rotated by R(-delta) instead (q . R(delta) k =
+// (R(-delta) q) . k, R orthogonal), or the stored key is rotated on its way
+// through shared memory:
+//   s_h,t = scale * [q_nope,h | q_rope,h] . [cKV_t | R(delta_t) k_r,t] + bias_t,
 //   out_h = sum_t softmax(s_h)_t cKV_t      (512 dims, before W_UV).
 // bias: LegoLink's pseudo-sink suppression (EPIC Guide: Position-Independent
 // Caching for LLM Serving, LegoLink "1. Identifying and Neutralizing
@@ -22,31 +23,42 @@
 // consecutive rows runs across a chunk boundary.  Per tile, with warps by
 // role:
 //   * three producer warps read the tile's record (formed on the host, the
-//     same in every layer: its stages, their delta entries, whether it
-//     opens or closes its key) and load its rows into a ring of two tiles
-//     with 3-D TMA tile copies, one per 64-dim plane (128-byte swizzle) and
-//     per run of stages that read consecutive rows (boxes of 16 to 64 rows);
-//   * the query warp writes the query operands: q_nope on a key change, and
-//     for each new delta of the tile R(-delta) q_rope as bf16 hi and lo rows
-//     (NE delta entries, so stages with different deltas share a tile);
-//   * two score issuers (one warp each) issue S = rows [q_nope | rope
-//     parts]^T into TMEM: M = 64, 32 k-steps over the latent (even and odd
-//     into separate partial sums), 4 over the rope plane;
+//     same in every layer) and load its rows into a ring of two tiles with
+//     3-D TMA tile copies, one per 64-dim plane (128-byte swizzle) and per run
+//     of stages that read consecutive rows (boxes of 16 to 64 rows);
+//   * the query warp writes the query operands: q_nope at each key's first
+//     tile, and the rope part --
+//       16 heads per CTA: for each delta new to the tile's four entries,
+//       R(-delta) q_rope as bf16 hi and lo rows;
+//       32 heads: q_rope as given, at the key's first tile;
+//   * (32 heads) softmax warps 0-7 first rotate the rope keys: warp w takes
+//     8 rows of stage w % 4, rotates each row's 64-dim k_r by its delta in
+//     fp32 and writes it back as bf16 hi and lo rows (the rope plane and a
+//     second plane);
+//   * two score issuers (one warp each) issue S = rows [q_nope | rope]^T into
+//     TMEM: M = 64, 32 k-steps over the latent (even and odd into separate
+//     partial sums), then the rope k-steps: 16 heads, 4 over the rope plane
+//     against every entry's hi and lo rows; 32 heads, 4 over the rotated hi
+//     plane and 4 over the lo plane into one column per head;
 //   * two value issuers issue O^T += V^T P^T once P is written: M = 128
-//     latent dims (four M-tiles, two each), N = 32 (16 heads: P's hi and lo
-//     rows side by side; 32 heads: each part in turn), K = the 16 positions
-//     of a stage; V^T is the same shared planes read as an MN-major operand;
-//   * softmax warps 0-7: warp w owns stage w's positions (TMEM lanes
-//     32 (w % 4) .. + 15 of the M = 64 scores) for half of the heads, read
-//     with the 16x256b shape so that each thread holds two positions.  It
-//     adds the nope partial sums and each position's delta's hi and lo rope
-//     columns,
-//     keeps a running max per head that is raised only when a score passes
-//     it by more than kTcLazy (log2 units; O and l are then rescaled), writes
-//     P = exp2(s - m) as bf16 hi and lo rows, and at the key's last tile in
-//     this CTA writes the record (O, m, l) that k_attend_merge combines.
-// The hi + lo splits keep about 16 significant bits of the rotated query and
-// of P; rows and q_nope are bf16 already and every product accumulates in
+//     latent dims (four M-tiles, two each), N = 2 x heads (P's hi and lo rows
+//     side by side), K = the 16 positions of a stage; V^T is the same shared
+//     planes read as an MN-major operand;
+//   * softmax warp w, for stage w % 4's positions (TMEM lanes
+//     32 (w % 4) .. + 15 of the M = 64 scores) and half of the heads, read
+//     with the 16x256b shape so that each thread holds two positions, adds
+//     the nope partial sums and the rope columns (16 heads: of each
+//     position's entry), keeps a running max per head that is raised only
+//     when a score passes it by more than kTcLazy (log2 units; O and l are
+//     then rescaled), writes P = exp2(s - m) as bf16 hi and lo rows, and at
+//     the key's last tile in this CTA writes the record (O, m, l) that
+//     k_attend_merge combines.
+// Rotating the query costs one pass over the heads per new delta and keeps
+// the key path untouched: the better trade at 16 heads.  At 32 heads that
+// pass is twice as long and sits on the score product's chain, and rotating
+// the keys (a fixed 64 rows per tile, spread over the softmax warps) wins.
+// The hi + lo splits keep about 16 significant bits of the rotated operand
+// and of P; rows and q are bf16 already and every product accumulates in
 // fp32 in TMEM.  Every wait is bounded: a wait that runs out raises
 // PIC_DEV_TIMEOUT and tells the other roles to stop, and the CTA frees its
 // TMEM before it leaves.
@@ -64,6 +76,7 @@ namespace pic {
 namespace {
 
 using namespace dev;
+
 
 constexpr int kMlaLatentDims = 512;
 constexpr int kMlaRowDims = 576;                           // latent + 64-d rope key
@@ -89,16 +102,18 @@ __host__ __device__ constexpr int tc_value_issuers(int) { return 2; }
 __host__ __device__ constexpr int tc_threads(int hc) {
   return 32 * (9 + tc_score_issuers(hc) + tc_producers(hc) + tc_value_issuers(hc));
 }
-constexpr uint32_t kTcCols = 512;                          // TMEM columns held by the CTA
-// TMEM columns: two score buffers of kTcSCols (the latent score as NP partial
-// sums, NP x HC columns, then the rope columns), then O^T: four M-tiles of
-// 32 columns (16 heads: the hi and lo parts of P in columns 0-15 and 16-31;
-// 32 heads: both parts summed in place).  An M = 64 score puts rows
-// 16 q .. 16 q + 15 in lanes 0-15 of lane quadrant q; an M = 128 product row r
-// in lane r.
-constexpr uint32_t kTcSCols = 192;
-constexpr uint32_t kTcOCol = 2 * kTcSCols;
-constexpr uint32_t kTcOColsPerTile = 32;
+// TMEM columns: two score buffers of tc_score_cols(HC) (the latent score as
+// NP = 2 partial sums, 2 HC columns, then the rope columns: HC, or with
+// rotated queries NE x 2 x HC), then O^T: four
+// M-tiles of 2 HC columns (the hi and lo parts of P side by side).  An M = 64
+// score puts rows 16 q .. 16 q + 15 in lanes 0-15 of lane quadrant q; an
+// M = 128 product row r in lane r.
+// 16 heads per CTA rotate the query (NE entries), 32 the rope keys.
+__host__ __device__ constexpr bool tc_rot_keys(int hc) { return hc >= 32; }
+__host__ __device__ constexpr uint32_t tc_score_cols(int hc) {
+  return tc_rot_keys(hc) ? 3u * static_cast<uint32_t>(hc) : 192u;
+}
+__host__ __device__ constexpr uint32_t tc_tmem_cols(int) { return 512u; }
 constexpr int kTcFirst = 1, kTcLast = 2, kTcEnd = 4;       // tile flags
 
 struct TcTile {
@@ -108,9 +123,11 @@ struct TcTile {
   int32_t flags;   // kTcFirst: first tile of the key in this CTA; kTcLast: its last; kTcEnd: the CTA's last
   int32_t n_tok[kTcStagesPerTile];   // positions of each stage
   int32_t sink[kTcStagesPerTile];    // their sink bits
-  int32_t entry[kTcStagesPerTile];   // delta entry of the stage's positions [0, split)
+  int32_t split[kTcStagesPerTile];   // first position of the stage's second delta (16: none)
+  int32_t delta[kTcStagesPerTile];   // rotated keys: shift of the stage's positions [0, split)
+  int32_t delta2[kTcStagesPerTile];  // and of [split, n_tok)
+  int32_t entry[kTcStagesPerTile];   // rotated queries: entry of [0, split)
   int32_t entry2[kTcStagesPerTile];  // and of [split, n_tok)
-  int32_t split[kTcStagesPerTile];
   int32_t fresh;                     // entries this tile (re)writes
   int32_t ent_delta[kTcStagesPerTile];
   int32_t pad[3];
@@ -119,24 +136,29 @@ struct TcTile {
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 template <int HC>
 struct TcLayout {
-  static constexpr int NE = HC == 16 ? 4 : 2;                   // delta entries per tile
+  static constexpr bool kKeys = tc_rot_keys(HC);
+  static constexpr int NE = kKeys ? 1 : 4;                      // entries of rotated query rows
   static constexpr int kRing = 0;                               // 2 tiles
-  static constexpr int kQn = kRing + 2 * kTcTileBytes;          // q_nope: 8 planes x HC rows x 128 B
+  static constexpr int kRopeLo = kRing + 2 * kTcTileBytes;      // rotated keys: each tile's rope lo plane
+  static constexpr int kQn = kRopeLo + (kKeys ? 2 * kTcPlaneBytes : 0);  // q_nope: 8 planes x HC rows x 128 B
   static constexpr int kQnPlane = HC * 128;
-  // NE entries x 2 halves of the heads x (HC / 2 hi + HC / 2 lo) rows x 128 B
+  // the rope B operand: rotated keys, q_rope (HC rows); rotated queries, NE
+  // entries x 2 halves of the heads x (HC / 2 hi + HC / 2 lo) rows; 128 B a row
   static constexpr int kRope = kQn + 8 * kQnPlane;
-  static constexpr int kPt = kRope + NE * 2 * HC * 128;         // P^T: 2 buffers x (HC hi + HC lo) rows
+  static constexpr int kRopeBytes = kKeys ? (HC * 128 < 1024 ? 1024 : HC * 128) : NE * 2 * HC * 128;
+  static constexpr int kPt = kRope + kRopeBytes;                // P^T: 2 buffers x (HC hi + HC lo) rows
   static constexpr int kPtBytes = 2 * HC * 128;
   static constexpr int kWmax = kPt + 2 * kPtBytes;              // float [2][4][HC]
   static constexpr int kLred = kWmax + 2 * 4 * HC * 4;          // float [4][HC]
   static constexpr int kTiles = kLred + 4 * HC * 4;             // TcTile [2]
   static constexpr int kBars = kTiles + 2 * static_cast<int>(sizeof(TcTile));
-  // full[2] empty[2] meta[2] rope_full[2] s_full[2] p_full[2] pv_done[2] done[4]
-  static constexpr int kNumBars = 18;
+  // full[2] empty[2] meta[2] q_ready[2] rot_done[2] s_full[2] p_full[2] pv_done[2] done[4]
+  static constexpr int kNumBars = 20;
   static constexpr int kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;                  // room to align the base
-  static_assert(kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 && kPtBytes % 1024 == 0,
+  static_assert(kRopeLo % 1024 == 0 && kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 &&
+                    kPtBytes % 1024 == 0,
                 "operands sit on 1024-byte swizzle atoms");
   static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
@@ -305,21 +327,25 @@ template <int PAIRING, int HC>
 __global__ void __launch_bounds__(tc_threads(HC), 1)
     k_attend_mla_tc(const AttnParams P, const __grid_constant__ TcMaps maps) {
   using L = TcLayout<HC>;
-  constexpr int NE = L::NE;
   constexpr bool NEOX = (PAIRING == kNeox);
-  constexpr uint32_t kIdS = idesc(64, HC, 0);
-  constexpr uint32_t kIdR = idesc(64, NE * 2 * HC, 0);
-  constexpr uint32_t kIdPV = idesc(128, 32, 1);
-  constexpr int kPvParts = HC == 16 ? 1 : 2;  // value products per stage and M-tile (N = 32 each)
+  constexpr bool KEYS = L::kKeys;  // rotate the rope keys (else the query)
+  constexpr int NE = L::NE;
+  constexpr uint32_t kIdS = idesc(64, HC, 0);       // scores: latent k-steps (and rope ones, rotated keys)
+  constexpr uint32_t kIdR = idesc(64, NE * 2 * HC, 0);  // rope k-steps against every entry (rotated queries)
+  constexpr uint32_t kIdPV = idesc(128, 2 * HC, 1);  // O^T += V^T P^T, P's hi and lo rows side by side
   constexpr int kSI = tc_score_issuers(HC);
   constexpr int kNP = tc_producers(HC);
   constexpr int kVI = tc_value_issuers(HC);
   // the latent score accumulates in NP partial sums (k-step mod NP; with two
-  // score issuers, one each)
+  // score issuers, one each), then one rope column per head
   constexpr int NP = 2;
+  constexpr uint32_t kSCols = tc_score_cols(HC);
   constexpr uint32_t kRopeCol = NP * HC;
-  static_assert(NE * 2 * HC == 128 && kRopeCol + NE * 2 * HC <= kTcSCols, "rope columns");
-  static_assert(kTcOCol + 4 * kTcOColsPerTile <= kTcCols, "TMEM columns");
+  constexpr uint32_t kOCol = 2 * kSCols;
+  constexpr uint32_t kOColsPerTile = 2 * HC;
+  constexpr uint32_t kCols = tc_tmem_cols(HC);
+  static_assert(kRopeCol + (KEYS ? HC : NE * 2 * HC) <= kSCols && kOCol + 4 * kOColsPerTile <= kCols, "TMEM columns");
+  static_assert(KEYS || NE * 2 * HC == 128, "rope entry columns");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -328,11 +354,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   uint64_t* full = bars + 0;        // a tile's rows landed (by tile parity, as below)
   uint64_t* empty = bars + 2;       // its value product finished: the ring slot is free
   uint64_t* meta_ready = bars + 4;  // its metadata is written
-  uint64_t* rope_full = bars + 6;   // its query operands are written
-  uint64_t* s_full = bars + 8;      // its score product finished
-  uint64_t* p_full = bars + 10;     // its P is written
-  uint64_t* pv_done = bars + 12;    // its value product finished
-  uint64_t* done = bars + 14;       // each issuer's products all finished
+  uint64_t* q_ready = bars + 6;     // its query operands are written
+  uint64_t* rot_done = bars + 8;    // its rope keys are rotated
+  uint64_t* s_full = bars + 10;     // its score product finished
+  uint64_t* p_full = bars + 12;     // its P is written
+  uint64_t* pv_done = bars + 14;    // its value product finished
+  uint64_t* done = bars + 16;       // each issuer's products all finished
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   TcTile* tiles = reinterpret_cast<TcTile*>(smem + L::kTiles);
@@ -346,7 +373,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       mbar_init(&full[b], kNP);  // each producer warp arrives with the bytes of its copies
       mbar_init(&empty[b], kVI);  // every value issuer commits
       mbar_init(&meta_ready[b], 1);
-      mbar_init(&rope_full[b], 1);
+      mbar_init(&q_ready[b], 1);
+      mbar_init(&rot_done[b], kTcSoftmaxWarps);
       mbar_init(&s_full[b], kSI);  // every score issuer commits
       mbar_init(&p_full[b], kTcSoftmaxWarps);
       mbar_init(&pv_done[b], kVI);
@@ -357,7 +385,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   }
   if (warp == kTcMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
-                 "r"(kTcCols)
+                 "r"(kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -381,7 +409,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     // of one source share one TMA box of 16, 32, 48 or 64 rows.
     const int tpl = P.tc_tiles_per_layer;
     const int32_t* recs = reinterpret_cast<const int32_t*>(P.tc_tiles);
-    constexpr int kRecInts = static_cast<int>(sizeof(TcTileRec) / 4);  // 36: lane l reads ints l and 32 + l
+    constexpr int kRecInts = static_cast<int>(sizeof(TcTileRec) / 4);  // 44: lane l reads ints l and 32 + l
     auto load_rec = [&](int64_t ti, int& a, int& b) {
       a = 0;
       b = 0;
@@ -403,16 +431,17 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       const int layer = static_cast<int>(ti / tpl);
       const int ns = __shfl_sync(0xffffffffu, ra, 0), key = __shfl_sync(0xffffffffu, ra, 1);
       const int rflags = __shfl_sync(0xffffffffu, ra, 2), rfresh = __shfl_sync(0xffffffffu, ra, 3);
-      // lane s < 4 holds stage s (lanes 4-31 a copy of stage lane % 4)
+      // lane s < 4 holds stage s (lanes 4-31 a copy of stage lane % 4) and entry s
       const int s4 = lane & 3;
       const int my_n = __shfl_sync(0xffffffffu, ra, 4 + s4), my_sink = __shfl_sync(0xffffffffu, ra, 8 + s4);
       const int my_e0 = __shfl_sync(0xffffffffu, ra, 12 + s4), my_e1 = __shfl_sync(0xffffffffu, ra, 16 + s4);
       const int my_split = __shfl_sync(0xffffffffu, ra, 20 + s4), my_row = __shfl_sync(0xffffffffu, ra, 24 + s4);
       const int my_src = __shfl_sync(0xffffffffu, ra, 28 + s4), my_ed = __shfl_sync(0xffffffffu, rb, s4);
+      const int my_d = __shfl_sync(0xffffffffu, rb, 4 + s4), my_d2 = __shfl_sync(0xffffffffu, rb, 8 + s4);
       const bool first = ti == u_begin || (rflags & kTcRecKeyFirst);
       const bool end = ti == u_end - 1;
       const int flags = (first ? kTcFirst : 0) | ((end || (rflags & kTcRecKeyLast)) ? kTcLast : 0) | (end ? kTcEnd : 0);
-      // at the CTA's first tile every entry it uses is new to the query warp
+      // rotated queries: at the CTA's first tile every entry it uses is new to the query warp
       uint32_t used = lane < ns ? ((1u << my_e0) | (my_split < my_n ? (1u << my_e1) : 0u)) : 0u;
       used = __reduce_or_sync(0xffffffffu, used);
       const int fresh = ti == u_begin ? static_cast<int>(used) : rfresh;
@@ -463,9 +492,11 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         if (lane < 4) {
           t.n_tok[lane] = my_n;
           t.sink[lane] = my_sink;
+          t.split[lane] = my_split;
+          t.delta[lane] = my_d;
+          t.delta2[lane] = my_d2;
           t.entry[lane] = my_e0;
           t.entry2[lane] = my_e1;
-          t.split[lane] = my_split;
           t.ent_delta[lane] = my_ed;
         }
         if (lane == 0) {
@@ -499,84 +530,120 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         for (int k = (issued > 2 ? issued - 2 : 0); k < issued; ++k) mbar_wait_bounded(&full[k & 1], (k >> 1) & 1, spins);
     }
   } else if (warp == kTcQuery && has_work) {
-    // --------------------------------------------------------------- query
-    // Writes each tile's query operands: q_nope on a key change, and for each
-    // fresh delta entry R(-delta) q_rope as bf16 hi and lo rows, once no
-    // earlier score product still reads what they replace.
-    float qa[HC], qb[HC];  // this lane's rope pair of every head (lane f: frequency f)
-    uint32_t used_prev = 0;  // entries the previous tile read
-#pragma unroll
-    for (int h = 0; h < HC; ++h) qa[h] = qb[h] = 0.0f;
-    const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
-    for (int i = 0;; ++i) {
-      const int rt = i & 1;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&meta_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
-        if (lane == 0) fail();
-        break;
-      }
-      const TcTile t = tiles[rt];
-      const bool key_change = (t.flags & kTcFirst) != 0;
-      uint32_t used = 0;  // entries this tile reads
-#pragma unroll
-      for (int st = 0; st < kTcStagesPerTile; ++st)
-        if (st < t.ns) used |= (1u << t.entry[st]) | (t.split[st] < t.n_tok[st] ? (1u << t.entry2[st]) : 0u);
-      if (key_change || t.fresh) {
-        // Tile i - 2's score product is done (its value product freed the
-        // slot tile i loads into); tile i - 1's may still read q_nope and its
-        // entries, so wait for it when either is about to be rewritten.
-        const bool clash = key_change || (static_cast<uint32_t>(t.fresh) & used_prev) != 0u;
-        if (i >= 1 && clash &&
-            !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins))) {
+    if constexpr (KEYS) {
+      // --------------------------------------------------------------- query
+      // Writes the query operands, q_nope (8 planes) and q_rope (one plane),
+      // at each key's first tile in this CTA, once the previous tile's score
+      // product no longer reads them; arrives on every tile.
+      for (int i = 0;; ++i) {
+        const int rt = i & 1;
+        if (!__all_sync(0xffffffffu, wait_or_abort(&meta_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
           if (lane == 0) fail();
           break;
         }
-        if (key_change) {
-          const int req = t.key / P.head_groups, hg = t.key - req * P.head_groups;
-          const uint16_t* qh = P.q + ((static_cast<int64_t>(t.layer) * P.n_req + req) * P.num_q_heads + hg * HC) *
+        const int t_flags = tiles[rt].flags, t_layer = tiles[rt].layer, t_key = tiles[rt].key;
+        if (t_flags & kTcFirst) {
+          if (i >= 1 &&
+              !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins))) {
+            if (lane == 0) fail();
+            break;
+          }
+          const int req = t_key / P.head_groups, hg = t_key - req * P.head_groups;
+          const uint16_t* qh = P.q + ((static_cast<int64_t>(t_layer) * P.n_req + req) * P.num_q_heads + hg * HC) *
                                          static_cast<int64_t>(kMlaRowDims);
-          for (int c = lane; c < HC * 64; c += 32) {
-            const int h = c >> 6, ch = c & 63;
+          // 72 16-byte pieces per head: 64 of q_nope, 8 of q_rope
+          for (int c = lane; c < HC * 72; c += 32) {
+            const int h = c / 72, ch = c - h * 72;
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + h * kMlaRowDims) + ch);
-            *reinterpret_cast<uint4*>(smem + L::kQn + (ch >> 3) * L::kQnPlane + sw128(h, (ch & 7) * 8)) = v;
+            const int off = ch < 64 ? L::kQn + (ch >> 3) * L::kQnPlane : L::kRope;
+            *reinterpret_cast<uint4*>(smem + off + sw128(h, (ch & 7) * 8)) = v;
           }
-#pragma unroll
-          for (int h = 0; h < HC; ++h) {
-            qa[h] = __uint_as_float(static_cast<uint32_t>(__ldg(qh + h * kMlaRowDims + kMlaLatentDims + ia)) << 16);
-            qb[h] = __uint_as_float(static_cast<uint32_t>(__ldg(qh + h * kMlaRowDims + kMlaLatentDims + ib)) << 16);
-          }
+          fence_proxy_async_smem();
         }
-        // lane f rotates frequency f of every head: pairs (2f, 2f + 1) interleaved, (f, f + 32) neox
-        uint8_t* rp = smem + L::kRope;
-#pragma unroll
-        for (int e = 0; e < NE; ++e) {
-          if (!((t.fresh >> e) & 1)) continue;
-          float cs = 1.0f, sn = 0.0f;
-          if (t.ent_delta[e] != 0) shift_cossin(t.ent_delta[e], __ldg(P.freq + lane), cs, sn);
-#pragma unroll
-          for (int h = 0; h < HC; ++h) {
-            __nv_bfloat16 ah, al, bh, bl;
-            split_bf16(qa[h] * cs + qb[h] * sn, ah, al);
-            split_bf16(qb[h] * cs - qa[h] * sn, bh, bl);
-            // per entry and half of the heads: the half's hi rows, then its lo rows
-            constexpr int HH = HC / 2;
-            const int rh = e * 2 * HC + (h / HH) * 2 * HH + h % HH, rl = rh + HH;
-            if (NEOX) {
-              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ia)) = ah;
-              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ib)) = bh;
-              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rl, ia)) = al;
-              *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rl, ib)) = bl;
-            } else {  // (2f, 2f + 1) are adjacent: one 4-byte store per part
-              *reinterpret_cast<__nv_bfloat162*>(rp + sw128(rh, ia)) = __halves2bfloat162(ah, bh);
-              *reinterpret_cast<__nv_bfloat162*>(rp + sw128(rl, ia)) = __halves2bfloat162(al, bl);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_ready[rt]);
+        if (t_flags & kTcEnd) break;
+      }
+    } else {
+      // --------------------------------------------------------------- query
+      // Writes each tile's query operands: q_nope on a key change, and for each
+      // fresh delta entry R(-delta) q_rope as bf16 hi and lo rows, once no
+      // earlier score product still reads what they replace.
+      float qa[HC], qb[HC];  // this lane's rope pair of every head (lane f: frequency f)
+      uint32_t used_prev = 0;  // entries the previous tile read
+  #pragma unroll
+      for (int h = 0; h < HC; ++h) qa[h] = qb[h] = 0.0f;
+      const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
+      for (int i = 0;; ++i) {
+        const int rt = i & 1;
+        if (!__all_sync(0xffffffffu, wait_or_abort(&meta_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
+          if (lane == 0) fail();
+          break;
+        }
+        const TcTile t = tiles[rt];
+        const bool key_change = (t.flags & kTcFirst) != 0;
+        uint32_t used = 0;  // entries this tile reads
+  #pragma unroll
+        for (int st = 0; st < kTcStagesPerTile; ++st)
+          if (st < t.ns) used |= (1u << t.entry[st]) | (t.split[st] < t.n_tok[st] ? (1u << t.entry2[st]) : 0u);
+        if (key_change || t.fresh) {
+          // Tile i - 2's score product is done (its value product freed the
+          // slot tile i loads into); tile i - 1's may still read q_nope and its
+          // entries, so wait for it when either is about to be rewritten.
+          const bool clash = key_change || (static_cast<uint32_t>(t.fresh) & used_prev) != 0u;
+          if (i >= 1 && clash &&
+              !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins))) {
+            if (lane == 0) fail();
+            break;
+          }
+          if (key_change) {
+            const int req = t.key / P.head_groups, hg = t.key - req * P.head_groups;
+            const uint16_t* qh = P.q + ((static_cast<int64_t>(t.layer) * P.n_req + req) * P.num_q_heads + hg * HC) *
+                                           static_cast<int64_t>(kMlaRowDims);
+            for (int c = lane; c < HC * 64; c += 32) {
+              const int h = c >> 6, ch = c & 63;
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + h * kMlaRowDims) + ch);
+              *reinterpret_cast<uint4*>(smem + L::kQn + (ch >> 3) * L::kQnPlane + sw128(h, (ch & 7) * 8)) = v;
+            }
+  #pragma unroll
+            for (int h = 0; h < HC; ++h) {
+              qa[h] = __uint_as_float(static_cast<uint32_t>(__ldg(qh + h * kMlaRowDims + kMlaLatentDims + ia)) << 16);
+              qb[h] = __uint_as_float(static_cast<uint32_t>(__ldg(qh + h * kMlaRowDims + kMlaLatentDims + ib)) << 16);
             }
           }
+          // lane f rotates frequency f of every head: pairs (2f, 2f + 1) interleaved, (f, f + 32) neox
+          uint8_t* rp = smem + L::kRope;
+  #pragma unroll
+          for (int e = 0; e < NE; ++e) {
+            if (!((t.fresh >> e) & 1)) continue;
+            float cs = 1.0f, sn = 0.0f;
+            if (t.ent_delta[e] != 0) shift_cossin(t.ent_delta[e], __ldg(P.freq + lane), cs, sn);
+  #pragma unroll
+            for (int h = 0; h < HC; ++h) {
+              __nv_bfloat16 ah, al, bh, bl;
+              split_bf16(qa[h] * cs + qb[h] * sn, ah, al);
+              split_bf16(qb[h] * cs - qa[h] * sn, bh, bl);
+              // per entry and half of the heads: the half's hi rows, then its lo rows
+              constexpr int HH = HC / 2;
+              const int rh = e * 2 * HC + (h / HH) * 2 * HH + h % HH, rl = rh + HH;
+              if (NEOX) {
+                *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ia)) = ah;
+                *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rh, ib)) = bh;
+                *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rl, ia)) = al;
+                *reinterpret_cast<__nv_bfloat16*>(rp + sw128(rl, ib)) = bl;
+              } else {  // (2f, 2f + 1) are adjacent: one 4-byte store per part
+                *reinterpret_cast<__nv_bfloat162*>(rp + sw128(rh, ia)) = __halves2bfloat162(ah, bh);
+                *reinterpret_cast<__nv_bfloat162*>(rp + sw128(rl, ia)) = __halves2bfloat162(al, bl);
+              }
+            }
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_ready[rt]);
+        used_prev = used;
+        if (t.flags & kTcEnd) break;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&rope_full[rt]);
-      used_prev = used;
-      if (t.flags & kTcEnd) break;
     }
   } else if ((warp == kTcMma || warp == kTcMma2 || warp == kTcPv || warp == kTcPv2) && has_work) {
     // --------------------------------------------------- MMA issuers
@@ -589,11 +656,13 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     if (warp == kTcMma || warp == kTcMma2) {
       // S of tile i once its rows are in and its TMEM buffer is free (the
       // softmax of tile i - 2 has written P, so it is done reading that
-      // buffer); the latent k-steps also wait for the query operands at a
-      // key's first tile (q_nope changes), the rope k-steps always.  With two
-      // issuers the first takes the even latent k-steps and the rope plane,
-      // the second the odd k-steps; each writes its own partial sums (k-step
-      // mod NP).
+      // buffer); at a key's first tile also once the query operands are
+      // written.  The first issuer takes the even latent k-steps and then the
+      // rope k-steps: rotated keys, once the softmax warps have rotated them,
+      // over the hi and the lo plane (one accumulator); rotated queries, once
+      // the query warp has written this tile's entries, over the rope plane
+      // against every entry.  The second issuer takes the odd latent k-steps.
+      // Each writes its own latent partial sums (k-step mod NP).
       const int par = warp == kTcMma ? 0 : 1;
       const uint64_t dq = sdesc(base_u32 + L::kQn, 16, 1024), dr = sdesc(base_u32 + L::kRope, 16, 1024);
       for (int i = 0;; ++i) {
@@ -601,17 +670,14 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         bool ok = wait_or_abort(&full[rt], (i >> 1) & 1, abort_flag, spins) &&
                   (i < 2 || wait_or_abort(&p_full[rt], ((i - 2) >> 1) & 1, abort_flag, spins));
         const int flags = ok ? tiles[rt].flags : 0;
-        // q_nope changes at a key's first tile; otherwise only the rope
-        // k-steps wait for the query warp's rotated rows
-        const bool q_new = (flags & kTcFirst) != 0;
-        if (ok && q_new) ok = wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins);
+        if (ok && (flags & kTcFirst)) ok = wait_or_abort(&q_ready[rt], (i >> 1) & 1, abort_flag, spins);
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) fail();
           break;
         }
         tc_fence_after();
         const uint64_t da = sdesc(ring + rt * kTcTileBytes, 16, 1024);
-        const uint32_t d = tmem + rt * kTcSCols;
+        const uint32_t d = tmem + rt * kSCols;
 #pragma unroll
         for (int k2 = 0; k2 < 32 / kSI; ++k2) {
           const int ks = kSI * k2 + par;
@@ -619,16 +685,31 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
                        dq + (((ks >> 2) * L::kQnPlane + (ks & 3) * 32) >> 4), kIdS, ks >= NP);
         }
         if (par == 0) {
-          if (!q_new) {
-            if (!__all_sync(0xffffffffu, wait_or_abort(&rope_full[rt], (i >> 1) & 1, abort_flag, spins))) {
+          if constexpr (KEYS) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(&rot_done[rt], (i >> 1) & 1, abort_flag, spins))) {
               if (lane == 0) fail();
               break;
             }
             tc_fence_after();
-          }
+            const uint64_t dlo = sdesc(base_u32 + L::kRopeLo + rt * kTcPlaneBytes, 16, 1024);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_elect(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_elect(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdS, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_elect(d + kRopeCol, dlo + ((ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdS, true);
+          } else {
+            if (!(flags & kTcFirst)) {
+              if (!__all_sync(0xffffffffu, wait_or_abort(&q_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
+                if (lane == 0) fail();
+                break;
+              }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_elect(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdR, ks > 0);
+          }
         }
         tc_commit_elect(&s_full[rt]);
         if (flags & kTcEnd) break;
@@ -658,16 +739,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
 #pragma unroll
         for (int w = 0; w < kTcStagesPerTile; ++w) {
           if (w >= t_ns) break;
+          const uint64_t bd = dp + ((w * 32) >> 4);
 #pragma unroll
-          for (int part = 0; part < kPvParts; ++part) {
-            const uint64_t bd = dp + ((part * 32 * 128 + w * 32) >> 4);
-#pragma unroll
-            for (int m4 = 0; m4 < 4 / kVI; ++m4) {
-              const int mt = vi * (4 / kVI) + m4;
-              tc_mma_elect(tmem + kTcOCol + mt * kTcOColsPerTile,
-                           dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4), bd, kIdPV,
-                           !(first && w == 0 && part == 0));
-            }
+          for (int m4 = 0; m4 < 4 / kVI; ++m4) {
+            const int mt = vi * (4 / kVI) + m4;
+            tc_mma_elect(tmem + kOCol + mt * kOColsPerTile, dv + ((2 * mt * kTcPlaneBytes + w * kTcStageBytes) >> 4),
+                         bd, kIdPV, !(first && w == 0));
           }
         }
         tc_commit_elect(&empty[rt]);
@@ -700,25 +777,64 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       m_run[j] = -INFINITY;
       l_part[j] = 0.0f;
     }
-    // this warp's O^T columns of M-tile mt: both parts of P (16 heads), or the sum (32 heads)
-    auto o_load = [&](int mt, float* o) {
-      const uint32_t c = tl + kTcOCol + mt * kTcOColsPerTile + h0;
-      tmem_ld<HH>(c, o);
-      if constexpr (kPvParts == 1) tmem_ld<HH>(c + HC, o + HH);
-    };
-    auto o_store = [&](int mt, const float* o) {
-      const uint32_t c = tl + kTcOCol + mt * kTcOColsPerTile + h0;
-      tmem_st<HH>(c, o);
-      if constexpr (kPvParts == 1) tmem_st<HH>(c + HC, o + HH);
-    };
-    constexpr int kOLoad = kPvParts == 1 ? 2 * HH : HH;
+    // this warp's O^T columns of M-tile mt: part 0 the product of P's hi rows, part 1 of its lo rows
+    auto o_col = [&](int mt, int part) { return tl + kOCol + mt * kOColsPerTile + part * HC + h0; };
+    // the rope keys this warp rotates: rows 8 half .. 8 half + 7 of stage w,
+    // lane f taking frequency f (pair (2f, 2f + 1) interleaved, (f, f + 32) neox)
+    const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
+    const float2 fq = __ldg(P.freq + lane);
     for (int i = 0;; ++i) {
       const int rt = i & 1;
       const uint32_t ph = (i >> 1) & 1;
       // every softmax warp reaches each barrier reduction below, so a wait
       // that runs out in one warp ends all eight together
-      const bool got = __all_sync(0xffffffffu, wait_or_abort(&full[rt], ph, abort_flag, spins) &&
-                                                    wait_or_abort(&s_full[rt], ph, abort_flag, spins));
+      const bool landed_rows = __all_sync(0xffffffffu, wait_or_abort(&full[rt], ph, abort_flag, spins));
+      if (KEYS && landed_rows) {
+        // rotate this warp's rope keys by their stage's delta: R(delta) k_r
+        // in fp32, written back as bf16 hi (the rope plane) and lo rows
+        const TcTile& tr0 = tiles[rt];
+        if (w < tr0.ns) {
+          const int n0 = tr0.n_tok[w], sp0 = tr0.split[w], d1 = tr0.delta[w], d2 = tr0.delta2[w];
+          float c1 = 1.0f, s1 = 0.0f, c2 = 1.0f, s2 = 0.0f;
+          if (d1 != 0) shift_cossin(d1, fq, c1, s1);
+          if (sp0 < n0 && d2 != 0) shift_cossin(d2, fq, c2, s2);
+          uint8_t* rope_hi = smem + L::kRing + rt * kTcTileBytes + 8 * kTcPlaneBytes;
+          uint8_t* rope_lo = smem + L::kRopeLo + rt * kTcPlaneBytes;
+#pragma unroll 2
+          for (int k = 0; k < 8; ++k) {
+            const int q = 8 * half + k;  // position within the stage
+            if (q >= n0) continue;
+            const int row = 16 * w + q;
+            const bool second = q >= sp0;
+            const float cs = second ? c2 : c1, sn = second ? s2 : s1;
+            float a, b;
+            if (NEOX) {
+              a = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rope_hi + sw128(row, ia)));
+              b = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rope_hi + sw128(row, ib)));
+            } else {  // (2f, 2f + 1) are adjacent: one 4-byte access
+              const float2 ab = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(rope_hi + sw128(row, ia)));
+              a = ab.x;
+              b = ab.y;
+            }
+            __nv_bfloat16 ah, al, bh, bl;
+            split_bf16(a * cs - b * sn, ah, al);
+            split_bf16(a * sn + b * cs, bh, bl);
+            if (NEOX) {
+              *reinterpret_cast<__nv_bfloat16*>(rope_hi + sw128(row, ia)) = ah;
+              *reinterpret_cast<__nv_bfloat16*>(rope_hi + sw128(row, ib)) = bh;
+              *reinterpret_cast<__nv_bfloat16*>(rope_lo + sw128(row, ia)) = al;
+              *reinterpret_cast<__nv_bfloat16*>(rope_lo + sw128(row, ib)) = bl;
+            } else {
+              *reinterpret_cast<__nv_bfloat162*>(rope_hi + sw128(row, ia)) = __halves2bfloat162(ah, bh);
+              *reinterpret_cast<__nv_bfloat162*>(rope_lo + sw128(row, ia)) = __halves2bfloat162(al, bl);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rot_done[rt]);
+      }
+      const bool got = landed_rows && __all_sync(0xffffffffu, wait_or_abort(&s_full[rt], ph, abort_flag, spins));
       // this warp's fields of the tile record (read now: the slot's record is
       // replaced once the tile's value product has finished; after a wait
       // that ran out they are not used) and its scores
@@ -741,28 +857,45 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             l_part[j] = 0.0f;
           }
         }
-        // latent partial sums; the rope hi then lo columns of the slot's first
-        // delta and then, when the slot holds a second one from position split
-        // on, of that one (read into the same registers)
-        float sp[NP][NR], rr[2 * NR], nope[NR];
-        const uint32_t sc = tl + rt * kTcSCols + h0;
-        tmem_ld16x256<2 * NG>(sc + kRopeCol + entry * 2 * HC + h0, rr);
-#pragma unroll
-        for (int pp = 0; pp < NP; ++pp) tmem_ld16x256<NG>(sc + pp * HC, sp[pp]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          nope[r] = sp[0][r];
-#pragma unroll
-          for (int pp = 1; pp < NP; ++pp) nope[r] += sp[pp][r];
-          s[r] = (nope[r] + rr[r]) + rr[NR + r];
-        }
-        if (split < n_tok) {  // the same for the whole warp
-          tmem_ld16x256<2 * NG>(sc + kRopeCol + entry2 * 2 * HC + h0, rr);
+        if constexpr (KEYS) {
+          // the latent partial sums and the rope column of the warp's heads
+          float sp[NP][NR], rr[NR];
+          const uint32_t sc = tl + rt * kSCols + h0;
+          tmem_ld16x256<NG>(sc + kRopeCol, rr);
+  #pragma unroll
+          for (int pp = 0; pp < NP; ++pp) tmem_ld16x256<NG>(sc + pp * HC, sp[pp]);
           tmem_wait_ld();
-#pragma unroll
-          for (int r = 0; r < NR; ++r)
-            if (q0 + 8 * ((r >> 1) & 1) >= split) s[r] = (nope[r] + rr[r]) + rr[NR + r];
+  #pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            float v = sp[0][r];
+  #pragma unroll
+            for (int pp = 1; pp < NP; ++pp) v += sp[pp][r];
+            s[r] = v + rr[r];
+          }
+        } else {
+          // latent partial sums; the rope hi then lo columns of the slot's first
+          // delta and then, when the slot holds a second one from position split
+          // on, of that one (read into the same registers)
+          float sp[NP][NR], rr[2 * NR], nope[NR];
+          const uint32_t sc = tl + rt * kSCols + h0;
+          tmem_ld16x256<2 * NG>(sc + kRopeCol + entry * 2 * HC + h0, rr);
+  #pragma unroll
+          for (int pp = 0; pp < NP; ++pp) tmem_ld16x256<NG>(sc + pp * HC, sp[pp]);
+          tmem_wait_ld();
+  #pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            nope[r] = sp[0][r];
+  #pragma unroll
+            for (int pp = 1; pp < NP; ++pp) nope[r] += sp[pp][r];
+            s[r] = (nope[r] + rr[r]) + rr[NR + r];
+          }
+          if (split < n_tok) {  // the same for the whole warp
+            tmem_ld16x256<2 * NG>(sc + kRopeCol + entry2 * 2 * HC + h0, rr);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int r = 0; r < NR; ++r)
+              if (q0 + 8 * ((r >> 1) & 1) >= split) s[r] = (nope[r] + rr[r]) + rr[NR + r];
+          }
         }
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
@@ -821,12 +954,15 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           tc_fence_after();
 #pragma unroll
           for (int mt = 0; mt < 4; ++mt) {
-            float o[kOLoad];
-            o_load(mt, o);
-            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < kOLoad; ++c) o[c] *= alpha_all[c % HH];
-            o_store(mt, o);
+            for (int part = 0; part < 2; ++part) {
+              float o[HH];
+              tmem_ld<HH>(o_col(mt, part), o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < HH; ++c) o[c] *= alpha_all[c];
+              tmem_st<HH>(o_col(mt, part), o);
+            }
           }
           tmem_wait_st();
         }
@@ -886,13 +1022,13 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             P.records + static_cast<int64_t>(kk.rec_base + (static_cast<int>(blockIdx.x) - kk.first_cta)) * blk_floats;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
-          float o[kOLoad];
-          o_load(mt, o);
+          float o[HH], ol[HH];
+          tmem_ld<HH>(o_col(mt, 0), o);
+          tmem_ld<HH>(o_col(mt, 1), ol);
           tmem_wait_ld();
           const int d = mt * 128 + 32 * w + lane;
 #pragma unroll
-          for (int h = 0; h < HH; ++h)
-            blk[(h0 + h) * kMlaLatentDims + d] = kPvParts == 1 ? o[h] + o[HH + h] : o[h];
+          for (int h = 0; h < HH; ++h) blk[(h0 + h) * kMlaLatentDims + d] = o[h] + ol[h];
         }
         if (w == 0) {
           // lane h < HH writes head h0 + h: its running max from the lane that holds it
@@ -919,7 +1055,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   __syncthreads();
   if (warp == kTcMma) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
   }
 }
 

@@ -790,12 +790,14 @@ struct AttnPlanCache {
 };
 
 // The tiles of the tcgen05 MLA attention for one layer (every layer has the
-// same stages).  Within a key, stages fill tiles of up to four in order.  Each
-// delta of a stage takes an entry of rotated query rows: the entry that holds
-// it, else a free one (holding nothing), else one neither this tile nor the
-// previous one uses (its rewrite need not wait for the previous tile's score
-// product), else one this tile does not use; a stage that finds no entry
-// starts the next tile.  Entries start empty at each key.
+// same stages).  Within a key, stages fill tiles of up to four in order.
+// With ne > 0 entries of rotated query rows (16 heads per CTA) each delta of
+// a stage takes an entry: the entry that holds it, else a free one (holding
+// nothing), else one neither this tile nor the previous one uses (its rewrite
+// need not wait for the previous tile's score product), else one this tile
+// does not use; a stage that finds no entry starts the next tile, and entries
+// start empty at each key.  With ne = 0 (the kernel rotates the keys) tiles
+// end only at four stages or at the key's end.
 void tc_tiles(const AttnPlan& plan, int ne, std::vector<pic::TcTileRec>* tiles, std::vector<int32_t>* key_tile_begin) {
   tiles->clear();
   key_tile_begin->assign(1, 0);
@@ -826,27 +828,30 @@ void tc_tiles(const AttnPlan& plan, int ne, std::vector<pic::TcTileRec>* tiles, 
         const pic::AttnStage& st = plan.stages[j];
         const int4 x = plan.ext[j];
         const bool two = x.w < st.n_tok;
-        uint32_t busy = used;
-        int e1 = find(st.delta, 0u);
-        const bool new1 = e1 < 0;
-        if (new1) e1 = pick(busy);
-        if (e1 < 0) break;
-        busy |= 1u << e1;
-        int e2 = e1;
-        bool new2 = false;
-        if (two) {
-          e2 = find(x.z, new1 ? (1u << e1) : 0u);  // an entry just taken no longer holds what it held
-          new2 = e2 < 0;
-          if (new2) e2 = pick(busy);
-          if (e2 < 0) break;
-          busy |= 1u << e2;
+        int e1 = 0, e2 = 0;
+        if (ne > 0) {
+          uint32_t busy = used;
+          e1 = find(st.delta, 0u);
+          const bool new1 = e1 < 0;
+          if (new1) e1 = pick(busy);
+          if (e1 < 0) break;
+          busy |= 1u << e1;
+          e2 = e1;
+          bool new2 = false;
+          if (two) {
+            e2 = find(x.z, new1 ? (1u << e1) : 0u);  // an entry just taken no longer holds what it held
+            new2 = e2 < 0;
+            if (new2) e2 = pick(busy);
+            if (e2 < 0) break;
+            busy |= 1u << e2;
+          }
+          if (new1) ent_delta[e1] = st.delta;
+          if (new2) ent_delta[e2] = x.z;
+          const uint32_t took = (new1 ? (1u << e1) : 0u) | (new2 ? (1u << e2) : 0u);
+          valid |= took;
+          fresh |= took;
+          used = busy;
         }
-        if (new1) ent_delta[e1] = st.delta;
-        if (new2) ent_delta[e2] = x.z;
-        const uint32_t took = (new1 ? (1u << e1) : 0u) | (new2 ? (1u << e2) : 0u);
-        valid |= took;
-        fresh |= took;
-        used = busy;
         const int s4 = t.ns;
         t.n_tok[s4] = st.n_tok;
         t.sink[s4] = st.sink_mask;
@@ -855,6 +860,8 @@ void tc_tiles(const AttnPlan& plan, int ne, std::vector<pic::TcTileRec>* tiles, 
         t.split[s4] = two ? x.w : 16;
         t.row[s4] = x.x;
         t.src[s4] = x.y;
+        t.delta[s4] = st.delta;
+        t.delta2[s4] = two ? x.z : st.delta;
         ++t.ns;
         ++j;
       }
@@ -889,7 +896,8 @@ const AttnPlanCache& attend_plan_cached(pic_ctx* ctx, const pic_plan* const* pla
   attend_plan(ctx, plans, n_req, source, heads, two_deltas, &fresh->plan);
   for (const pic::AttnTok& t : fresh->plan.toks)
     if (!(t.flags & pic::kAttnFromCache)) fresh->pool_rows = std::max<int64_t>(fresh->pool_rows, int64_t{t.row} + 1);
-  if (two_deltas) tc_tiles(fresh->plan, heads.group == 16 ? 4 : 2, &fresh->tiles, &fresh->key_tile_begin);
+  // 16 heads per CTA: four entries of rotated query rows; more: rotated keys
+  if (two_deltas) tc_tiles(fresh->plan, heads.group == 16 ? 4 : 0, &fresh->tiles, &fresh->key_tile_begin);
   fresh->key = std::move(key);
   slot = fresh;
   return *fresh;

@@ -212,16 +212,18 @@ cudaError_t launch_attend_merge_mla(const AttnParams& p, int heads_per_record, c
 // One tile of the tcgen05 MLA attention, formed on the host: up to four plan
 // stages of one key, one per 16-row slot of the shared-memory ring.  A stage
 // is up to 16 positions read from consecutive rows of one source and holds
-// one or two deltas (positions from split on take the second); each delta
-// uses one of the tile's entries of rotated query rows (at most 4 entries at
-// 16 heads per CTA, 2 at 32).  Every layer has the same tiles.
+// one or two deltas (positions from split on take the second).  Every layer
+// has the same tiles.  With 16 query heads per CTA the kernel rotates the
+// query's rope part, once per delta, into one of four entries of rotated
+// query rows (entry, entry2, fresh, ent_delta); with 32 it rotates the rope
+// keys themselves (delta, delta2).
 constexpr int kTcRecKeyFirst = 1;  // the key's first tile in the layer
 constexpr int kTcRecKeyLast = 2;   // its last
 struct TcTileRec {
   int32_t ns;            // stages
   int32_t key;
   int32_t flags;         // kTcRecKeyFirst | kTcRecKeyLast
-  int32_t fresh;         // entries first used (or given a new delta) since the key's previous tile
+  int32_t fresh;         // entries given a new delta since the key's previous tile
   int32_t n_tok[4];
   int32_t sink[4];       // bit t: position t is a LegoLink pseudo-sink
   int32_t entry[4];      // entry of the stage's positions [0, split)
@@ -230,8 +232,10 @@ struct TcTileRec {
   int32_t row[4];        // first source row of the stage
   int32_t src[4];        // its source (kAttnFromCache or 0)
   int32_t ent_delta[4];  // the delta each entry holds after this tile
+  int32_t delta[4];      // shift of the stage's positions [0, split)
+  int32_t delta2[4];     // and of [split, n_tok)
 };
-static_assert(sizeof(TcTileRec) == 144, "TcTileRec layout: 36 ints");
+static_assert(sizeof(TcTileRec) == 176, "TcTileRec layout: 44 ints");
 
 struct TcMaps {
   CUtensorMap pool[4];
