@@ -30,16 +30,18 @@
 //     tile, and the rope part --
 //       16 heads per CTA: for each delta new to the tile's four entries,
 //       R(-delta) q_rope as bf16 hi and lo rows;
-//       32 heads: q_rope as given, at the key's first tile;
+//       32 heads: q_rope as given, at the key's first tile, and for every
+//       tile the cos / sin of its stage deltas (lane f: frequency f);
 //   * (32 heads) softmax warps 0-7 first rotate the rope keys: warp w takes
 //     8 rows of stage w % 4, rotates each row's 64-dim k_r by its delta in
-//     fp32 and writes it back as bf16 hi and lo rows (the rope plane and a
-//     second plane);
+//     fp32 and writes it as bf16 hi and lo rows of one 128-row operand
+//     (stage s's hi rows at row 32 s, its lo rows at 32 s + 16);
 //   * two score issuers (one warp each) issue S = rows [q_nope | rope]^T into
 //     TMEM: M = 64, 32 k-steps over the latent (even and odd into separate
 //     partial sums), then the rope k-steps: 16 heads, 4 over the rope plane
-//     against every entry's hi and lo rows; 32 heads, 4 over the rotated hi
-//     plane and 4 over the lo plane into one column per head;
+//     against every entry's hi and lo rows; 32 heads, 4 of M = 128 over the
+//     rotated-key operand into one column per head, the hi rows' part in
+//     lanes 0-15 of each lane quadrant and the lo rows' in lanes 16-31;
 //   * two value issuers issue O^T += V^T P^T once P is written: M = 128
 //     latent dims (four M-tiles, two each), N = 2 x heads (P's hi and lo rows
 //     side by side), K = the 16 positions of a stage; V^T is the same shared
@@ -48,7 +50,7 @@
 //     32 (w % 4) .. + 15 of the M = 64 scores) and half of the heads, read
 //     with the 16x256b shape so that each thread holds two positions, adds
 //     the nope partial sums and the rope columns (16 heads: of each
-//     position's entry), keeps a running max per head that is raised only
+//     position's entry; 32 heads: both lane halves), keeps a running max per head that is raised only
 //     when a score passes it by more than kTcLazy (log2 units; O and l are
 //     then rescaled), writes P = exp2(s - m) as bf16 hi and lo rows, and at
 //     the key's last tile in this CTA writes the record (O, m, l) that
@@ -139,8 +141,10 @@ struct TcLayout {
   static constexpr bool kKeys = tc_rot_keys(HC);
   static constexpr int NE = kKeys ? 1 : 4;                      // entries of rotated query rows
   static constexpr int kRing = 0;                               // 2 tiles
-  static constexpr int kRopeLo = kRing + 2 * kTcTileBytes;      // rotated keys: each tile's rope lo plane
-  static constexpr int kQn = kRopeLo + (kKeys ? 2 * kTcPlaneBytes : 0);  // q_nope: 8 planes x HC rows x 128 B
+  // rotated keys: the rotated rope keys of the tile being scored, an A operand
+  // of 128 rows (stage w's bf16 hi rows at 32 w, its lo rows at 32 w + 16)
+  static constexpr int kRopeK = kRing + 2 * kTcTileBytes;
+  static constexpr int kQn = kRopeK + (kKeys ? 2 * kTcPlaneBytes : 0);  // q_nope: 8 planes x HC rows x 128 B
   static constexpr int kQnPlane = HC * 128;
   // the rope B operand: rotated keys, q_rope (HC rows); rotated queries, NE
   // entries x 2 halves of the heads x (HC / 2 hi + HC / 2 lo) rows; 128 B a row
@@ -150,14 +154,16 @@ struct TcLayout {
   static constexpr int kPtBytes = 2 * HC * 128;
   static constexpr int kWmax = kPt + 2 * kPtBytes;              // float [2][4][HC]
   static constexpr int kLred = kWmax + 2 * 4 * HC * 4;          // float [4][HC]
-  static constexpr int kTiles = kLred + 4 * HC * 4;             // TcTile [2]
+  // rotated keys: cos / sin of each slot's stage deltas, float2 [2][4][2][32]
+  static constexpr int kCs = kLred + 4 * HC * 4;
+  static constexpr int kTiles = kCs + (kKeys ? 2 * 4 * 2 * 32 * 8 : 0);  // TcTile [2]
   static constexpr int kBars = kTiles + 2 * static_cast<int>(sizeof(TcTile));
   // full[2] empty[2] meta[2] q_ready[2] rot_done[2] s_full[2] p_full[2] pv_done[2] done[4]
   static constexpr int kNumBars = 20;
   static constexpr int kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;                  // room to align the base
-  static_assert(kRopeLo % 1024 == 0 && kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 &&
+  static_assert(kRopeK % 1024 == 0 && kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 &&
                     kPtBytes % 1024 == 0,
                 "operands sit on 1024-byte swizzle atoms");
   static_assert(kAlloc <= 227 * 1024, "shared memory");
@@ -320,6 +326,11 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
   hi = __float2bfloat16_rn(x);
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
+// the same for a pair, packed: x in the low halves, y in the high
+__device__ __forceinline__ void split2_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+  hi = bf_pack(x, y);
+  lo = bf_pack(x - bf_lo(hi), y - bf_hi(hi));
+}
 
 // grid: persistent CTAs, CTA c owns units [U c / G, U (c + 1) / G) of the
 // (layer, tile) list; block: tc_threads(HC) threads (the warp roles above).
@@ -330,7 +341,8 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr bool KEYS = L::kKeys;  // rotate the rope keys (else the query)
   constexpr int NE = L::NE;
-  constexpr uint32_t kIdS = idesc(64, HC, 0);       // scores: latent k-steps (and rope ones, rotated keys)
+  constexpr uint32_t kIdS = idesc(64, HC, 0);       // scores: latent k-steps
+  constexpr uint32_t kIdK = idesc(128, HC, 0);      // rope k-steps over the rotated keys' hi and lo rows
   constexpr uint32_t kIdR = idesc(64, NE * 2 * HC, 0);  // rope k-steps against every entry (rotated queries)
   constexpr uint32_t kIdPV = idesc(128, 2 * HC, 1);  // O^T += V^T P^T, P's hi and lo rows side by side
   constexpr int kSI = tc_score_issuers(HC);
@@ -532,9 +544,13 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   } else if (warp == kTcQuery && has_work) {
     if constexpr (KEYS) {
       // --------------------------------------------------------------- query
-      // Writes the query operands, q_nope (8 planes) and q_rope (one plane),
-      // at each key's first tile in this CTA, once the previous tile's score
-      // product no longer reads them; arrives on every tile.
+      // For every tile, cos / sin of its stage deltas for the softmax warps'
+      // key rotation (lane f: frequency f), written while the rows are still
+      // on their way.  At each key's first tile in this CTA it also writes
+      // the query operands, q_nope (8 planes) and q_rope (one plane), once
+      // the previous tile's score product no longer reads them.  Arrives on
+      // every tile.
+      const float2 fq = __ldg(P.freq + lane);
       for (int i = 0;; ++i) {
         const int rt = i & 1;
         if (!__all_sync(0xffffffffu, wait_or_abort(&meta_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
@@ -542,6 +558,21 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           break;
         }
         const int t_flags = tiles[rt].flags, t_layer = tiles[rt].layer, t_key = tiles[rt].key;
+        // the slot's previous tile (i - 2) was rotated before its softmax,
+        // which ended before this tile's metadata was written
+        float2* cs = reinterpret_cast<float2*>(smem + L::kCs) + rt * 256;
+        for (int st = 0; st < tiles[rt].ns; ++st) {
+          const int d1 = tiles[rt].delta[st], d2 = tiles[rt].delta2[st];
+          float c = 1.0f, sn = 0.0f;
+          if (d1 != 0) shift_cossin(d1, fq, c, sn);
+          cs[st * 64 + lane] = make_float2(c, sn);
+          if (tiles[rt].split[st] < tiles[rt].n_tok[st]) {
+            c = 1.0f;
+            sn = 0.0f;
+            if (d2 != 0) shift_cossin(d2, fq, c, sn);
+            cs[st * 64 + 32 + lane] = make_float2(c, sn);
+          }
+        }
         if (t_flags & kTcFirst) {
           if (i >= 1 &&
               !__all_sync(0xffffffffu, wait_or_abort(&s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, spins))) {
@@ -691,13 +722,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
               break;
             }
             tc_fence_after();
-            const uint64_t dlo = sdesc(base_u32 + L::kRopeLo + rt * kTcPlaneBytes, 16, 1024);
+            // one M = 128 product per k-step: the hi rows' partial score lands in
+            // lanes 32 w .. 32 w + 15, the lo rows' in lanes 32 w + 16 .. 32 w + 31
+            const uint64_t dk = sdesc(base_u32 + L::kRopeK, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              tc_mma_elect(d + kRopeCol, da + ((8 * kTcPlaneBytes + ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdS, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc_mma_elect(d + kRopeCol, dlo + ((ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdS, true);
+              tc_mma_elect(d + kRopeCol, dk + ((ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdK, ks > 0);
           } else {
             if (!(flags & kTcFirst)) {
               if (!__all_sync(0xffffffffu, wait_or_abort(&q_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
@@ -782,51 +812,63 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     // the rope keys this warp rotates: rows 8 half .. 8 half + 7 of stage w,
     // lane f taking frequency f (pair (2f, 2f + 1) interleaved, (f, f + 32) neox)
     const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
-    const float2 fq = __ldg(P.freq + lane);
     for (int i = 0;; ++i) {
       const int rt = i & 1;
       const uint32_t ph = (i >> 1) & 1;
       // every softmax warp reaches each barrier reduction below, so a wait
       // that runs out in one warp ends all eight together
-      const bool landed_rows = __all_sync(0xffffffffu, wait_or_abort(&full[rt], ph, abort_flag, spins));
+      // rotated keys: also the tile's cos / sin table (the query warp)
+      const bool landed_rows =
+          __all_sync(0xffffffffu, wait_or_abort(&full[rt], ph, abort_flag, spins) &&
+                                      (!KEYS || wait_or_abort(&q_ready[rt], ph, abort_flag, spins)));
       if (KEYS && landed_rows) {
         // rotate this warp's rope keys by their stage's delta: R(delta) k_r
-        // in fp32, written back as bf16 hi (the rope plane) and lo rows
+        // in fp32, written as bf16 hi and lo rows of the rotated-key operand
+        // (free: this warp has seen the previous tile's scores, so its rope
+        // product, the operand's last reader, has ended)
         const TcTile& tr0 = tiles[rt];
         if (w < tr0.ns) {
-          const int n0 = tr0.n_tok[w], sp0 = tr0.split[w], d1 = tr0.delta[w], d2 = tr0.delta2[w];
-          float c1 = 1.0f, s1 = 0.0f, c2 = 1.0f, s2 = 0.0f;
-          if (d1 != 0) shift_cossin(d1, fq, c1, s1);
-          if (sp0 < n0 && d2 != 0) shift_cossin(d2, fq, c2, s2);
-          uint8_t* rope_hi = smem + L::kRing + rt * kTcTileBytes + 8 * kTcPlaneBytes;
-          uint8_t* rope_lo = smem + L::kRopeLo + rt * kTcPlaneBytes;
-#pragma unroll 2
-          for (int k = 0; k < 8; ++k) {
-            const int q = 8 * half + k;  // position within the stage
-            if (q >= n0) continue;
-            const int row = 16 * w + q;
-            const bool second = q >= sp0;
-            const float cs = second ? c2 : c1, sn = second ? s2 : s1;
-            float a, b;
-            if (NEOX) {
-              a = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rope_hi + sw128(row, ia)));
-              b = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rope_hi + sw128(row, ib)));
-            } else {  // (2f, 2f + 1) are adjacent: one 4-byte access
-              const float2 ab = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(rope_hi + sw128(row, ia)));
-              a = ab.x;
-              b = ab.y;
+          const int n0 = tr0.n_tok[w], sp0 = tr0.split[w];
+          const uint8_t* rope = smem + L::kRing + rt * kTcTileBytes + 8 * kTcPlaneBytes;
+          uint8_t* rope_k = smem + L::kRopeK;
+          const float2* cs = reinterpret_cast<const float2*>(smem + L::kCs) + rt * 256 + w * 64;
+          const float2 cs1 = cs[lane], cs2 = sp0 < n0 ? cs[32 + lane] : cs1;
+          // two rounds of four rows: a round's loads all go out before any of
+          // them is used, so the warp waits out two shared-memory latencies
+#pragma unroll 1
+          for (int k0 = 0; k0 < 8; k0 += 4) {
+            uint32_t v[4];  // each row's pair as bf16: a in the low half, b in the high
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int q = 8 * half + k0 + k, row = 16 * w + q;
+              v[k] = 0u;
+              if (q < n0) {
+                if (NEOX) {
+                  v[k] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rope + sw128(row, ia))) |
+                         (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rope + sw128(row, ib))) << 16);
+                } else {  // (2f, 2f + 1) are adjacent: one 4-byte access
+                  v[k] = *reinterpret_cast<const uint32_t*>(rope + sw128(row, ia));
+                }
+              }
             }
-            __nv_bfloat16 ah, al, bh, bl;
-            split_bf16(a * cs - b * sn, ah, al);
-            split_bf16(a * sn + b * cs, bh, bl);
-            if (NEOX) {
-              *reinterpret_cast<__nv_bfloat16*>(rope_hi + sw128(row, ia)) = ah;
-              *reinterpret_cast<__nv_bfloat16*>(rope_hi + sw128(row, ib)) = bh;
-              *reinterpret_cast<__nv_bfloat16*>(rope_lo + sw128(row, ia)) = al;
-              *reinterpret_cast<__nv_bfloat16*>(rope_lo + sw128(row, ib)) = bl;
-            } else {
-              *reinterpret_cast<__nv_bfloat162*>(rope_hi + sw128(row, ia)) = __halves2bfloat162(ah, bh);
-              *reinterpret_cast<__nv_bfloat162*>(rope_lo + sw128(row, ia)) = __halves2bfloat162(al, bl);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int q = 8 * half + k0 + k;
+              if (q >= n0) continue;
+              const int rh = 32 * w + q, rl = rh + 16;  // operand rows of the hi and lo parts
+              const float2 c = q >= sp0 ? cs2 : cs1;
+              const float a = bf_lo(v[k]), b = bf_hi(v[k]);
+              uint32_t hi, lo;
+              split2_bf16(a * c.x - b * c.y, a * c.y + b * c.x, hi, lo);
+              if (NEOX) {
+                *reinterpret_cast<uint16_t*>(rope_k + sw128(rh, ia)) = static_cast<uint16_t>(hi);
+                *reinterpret_cast<uint16_t*>(rope_k + sw128(rh, ib)) = static_cast<uint16_t>(hi >> 16);
+                *reinterpret_cast<uint16_t*>(rope_k + sw128(rl, ia)) = static_cast<uint16_t>(lo);
+                *reinterpret_cast<uint16_t*>(rope_k + sw128(rl, ib)) = static_cast<uint16_t>(lo >> 16);
+              } else {
+                *reinterpret_cast<uint32_t*>(rope_k + sw128(rh, ia)) = hi;
+                *reinterpret_cast<uint32_t*>(rope_k + sw128(rl, ia)) = lo;
+              }
             }
           }
           fence_proxy_async_smem();
@@ -858,10 +900,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           }
         }
         if constexpr (KEYS) {
-          // the latent partial sums and the rope column of the warp's heads
-          float sp[NP][NR], rr[NR];
+          // the latent partial sums and the rope column of the warp's heads:
+          // the hi rows' part in lanes 0-15 of the quadrant, the lo rows' in 16-31
+          float sp[NP][NR], rr[NR], rl[NR];
           const uint32_t sc = tl + rt * kSCols + h0;
           tmem_ld16x256<NG>(sc + kRopeCol, rr);
+          tmem_ld16x256<NG>(sc + kRopeCol + (16u << 16), rl);
   #pragma unroll
           for (int pp = 0; pp < NP; ++pp) tmem_ld16x256<NG>(sc + pp * HC, sp[pp]);
           tmem_wait_ld();
@@ -870,7 +914,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             float v = sp[0][r];
   #pragma unroll
             for (int pp = 1; pp < NP; ++pp) v += sp[pp][r];
-            s[r] = v + rr[r];
+            s[r] = v + (rr[r] + rl[r]);
           }
         } else {
           // latent partial sums; the rope hi then lo columns of the slot's first
