@@ -270,18 +270,20 @@ def test_mla_rejects_unsupported_head_counts():
         pic.pic_destroy(S["ctx"])
 
 
-def test_deepseek_full_launch_sampled_layers():
+@pytest.mark.parametrize("H", [16, 32])
+def test_deepseek_full_launch_sampled_layers(H):
     """The benchmark's launch (DeepSeek-V3 MLA shapes: 61 layers, 65,536
-    positions of 16-128-token chunks behind a 32-token leading chunk, 16 query
-    heads) in one call; layers 0, 30 and 60 against the oracle, and the cache
-    path over the stitched copy against the fused result everywhere."""
+    positions of 16-128-token chunks behind a 32-token leading chunk, 16 or
+    32 query heads: the query-rotating and the key-rotating kernel) in one
+    call; layers 0, 30 and 60 against the oracle, and the cache path over the
+    stitched copy against the fused result everywhere."""
     from gpu_util import Stitched
     wl = W.deepseek_v3_mla()
     st = Stitched(wl).run()
     try:
         _check_variant(st.ctx, os.environ["PIC_ATTEND_KERNEL"])
         m = wl.model
-        H, L = 16, m.num_layers
+        L = m.num_layers
         g = torch.Generator(device=DEV)
         g.manual_seed(11)
         q = torch.empty((L, 1, H, ROW), dtype=torch.bfloat16, device=DEV).normal_(0.0, 1.0, generator=g)
