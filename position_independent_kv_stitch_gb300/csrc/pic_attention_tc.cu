@@ -32,16 +32,19 @@
 //       R(-delta) q_rope as bf16 hi and lo rows;
 //       32 heads: q_rope as given, at the key's first tile, and for every
 //       tile the cos / sin of its stage deltas (lane f: frequency f);
-//   * (32 heads) softmax warps 0-7 first rotate the rope keys: warp w takes
-//     8 rows of stage w % 4, rotates each row's 64-dim k_r by its delta in
-//     fp32 and writes it as bf16 hi and lo rows of one 128-row operand
-//     (stage s's hi rows at row 32 s, its lo rows at 32 s + 16);
+//   * (32 heads) softmax warps 0-7 first rotate the rope keys: the two warps
+//     of lane quadrant s take stage s, half of the dims each; thread t rotates
+//     row t % 16's k_r by its delta in fp32 and writes its bf16 hi (t < 16)
+//     or lo part (t >= 16) into TMEM, so that the quadrant's lanes hold an
+//     A operand of 128 rows (stage s's hi rows in lanes 32 s .. + 15, its lo
+//     rows in lanes 32 s + 16 .. + 31, two dims per column);
 //   * two score issuers (one warp each) issue S = rows [q_nope | rope]^T into
 //     TMEM: M = 64, 32 k-steps over the latent (even and odd into separate
 //     partial sums), then the rope k-steps: 16 heads, 4 over the rope plane
-//     against every entry's hi and lo rows; 32 heads, 4 of M = 128 over the
-//     rotated-key operand into one column per head, the hi rows' part in
-//     lanes 0-15 of each lane quadrant and the lo rows' in lanes 16-31;
+//     against every entry's hi and lo rows; 32 heads, 4 of M = 128 with A
+//     the rotated-key operand in TMEM, into one column per head, the hi
+//     rows' part in lanes 0-15 of each lane quadrant and the lo rows' in
+//     lanes 16-31;
 //   * two value issuers issue O^T += V^T P^T once P is written: M = 128
 //     latent dims (four M-tiles, two each), N = 2 x heads (P's hi and lo rows
 //     side by side), K = the 16 positions of a stage; V^T is the same shared
@@ -141,10 +144,7 @@ struct TcLayout {
   static constexpr bool kKeys = tc_rot_keys(HC);
   static constexpr int NE = kKeys ? 1 : 4;                      // entries of rotated query rows
   static constexpr int kRing = 0;                               // 2 tiles
-  // rotated keys: the rotated rope keys of the tile being scored, an A operand
-  // of 128 rows (stage w's bf16 hi rows at 32 w, its lo rows at 32 w + 16)
-  static constexpr int kRopeK = kRing + 2 * kTcTileBytes;
-  static constexpr int kQn = kRopeK + (kKeys ? 2 * kTcPlaneBytes : 0);  // q_nope: 8 planes x HC rows x 128 B
+  static constexpr int kQn = kRing + 2 * kTcTileBytes;         // q_nope: 8 planes x HC rows x 128 B
   static constexpr int kQnPlane = HC * 128;
   // the rope B operand: rotated keys, q_rope (HC rows); rotated queries, NE
   // entries x 2 halves of the heads x (HC / 2 hi + HC / 2 lo) rows; 128 B a row
@@ -163,7 +163,7 @@ struct TcLayout {
   static constexpr int kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;                  // room to align the base
-  static_assert(kRopeK % 1024 == 0 && kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 &&
+  static_assert(kQn % 1024 == 0 && kRope % 1024 == 0 && kPt % 1024 == 0 &&
                     kPtBytes % 1024 == 0,
                 "operands sit on 1024-byte swizzle atoms");
   static_assert(kAlloc <= 227 * 1024, "shared memory");
@@ -195,6 +195,13 @@ __device__ __forceinline__ void tc_mma_elect(uint32_t d, uint64_t a, uint64_t b,
       "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(id), "r"(acc ? 1u : 0u));
+}
+// the same with A in TMEM (M rows in lanes, two 16-bit elements per column)
+__device__ __forceinline__ void tc_mma_tmem_a_elect(uint32_t d, uint32_t a, uint64_t b, uint32_t id, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(id), "r"(acc ? 1u : 0u));
 }
 __device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
   asm volatile(
@@ -356,7 +363,10 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
   constexpr uint32_t kOCol = 2 * kSCols;
   constexpr uint32_t kOColsPerTile = 2 * HC;
   constexpr uint32_t kCols = tc_tmem_cols(HC);
+  // rotated keys: their A operand after O^T, 128 lanes x 32 columns (64 bf16 dims)
+  constexpr uint32_t kRopeACol = kOCol + 4 * kOColsPerTile;
   static_assert(kRopeCol + (KEYS ? HC : NE * 2 * HC) <= kSCols && kOCol + 4 * kOColsPerTile <= kCols, "TMEM columns");
+  static_assert(!KEYS || kRopeACol + 32 <= kCols, "TMEM columns: rotated-key operand");
   static_assert(KEYS || NE * 2 * HC == 128, "rope entry columns");
 
   extern __shared__ uint8_t smem_raw[];
@@ -722,12 +732,12 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
               break;
             }
             tc_fence_after();
-            // one M = 128 product per k-step: the hi rows' partial score lands in
-            // lanes 32 w .. 32 w + 15, the lo rows' in lanes 32 w + 16 .. 32 w + 31
-            const uint64_t dk = sdesc(base_u32 + L::kRopeK, 16, 1024);
+            // one M = 128 product per k-step, A from TMEM (8 columns a k-step):
+            // the hi rows' partial score lands in lanes 32 w .. 32 w + 15, the
+            // lo rows' in lanes 32 w + 16 .. 32 w + 31
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              tc_mma_elect(d + kRopeCol, dk + ((ks * 32) >> 4), dr + ((ks * 32) >> 4), kIdK, ks > 0);
+              tc_mma_tmem_a_elect(d + kRopeCol, tmem + kRopeACol + 8 * ks, dr + ((ks * 32) >> 4), kIdK, ks > 0);
           } else {
             if (!(flags & kTcFirst)) {
               if (!__all_sync(0xffffffffu, wait_or_abort(&q_ready[rt], (i >> 1) & 1, abort_flag, spins))) {
@@ -809,9 +819,6 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
     }
     // this warp's O^T columns of M-tile mt: part 0 the product of P's hi rows, part 1 of its lo rows
     auto o_col = [&](int mt, int part) { return tl + kOCol + mt * kOColsPerTile + part * HC + h0; };
-    // the rope keys this warp rotates: rows 8 half .. 8 half + 7 of stage w,
-    // lane f taking frequency f (pair (2f, 2f + 1) interleaved, (f, f + 32) neox)
-    const int ia = NEOX ? lane : 2 * lane, ib = NEOX ? lane + 32 : 2 * lane + 1;
     for (int i = 0;; ++i) {
       const int rt = i & 1;
       const uint32_t ph = (i >> 1) & 1;
@@ -822,57 +829,66 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
           __all_sync(0xffffffffu, wait_or_abort(&full[rt], ph, abort_flag, spins) &&
                                       (!KEYS || wait_or_abort(&q_ready[rt], ph, abort_flag, spins)));
       if (KEYS && landed_rows) {
-        // rotate this warp's rope keys by their stage's delta: R(delta) k_r
-        // in fp32, written as bf16 hi and lo rows of the rotated-key operand
-        // (free: this warp has seen the previous tile's scores, so its rope
-        // product, the operand's last reader, has ended)
+        // rotate stage w's rope keys by their deltas, R(delta) k_r in fp32,
+        // into the rotated-key operand in TMEM: an A operand of 128 rows whose
+        // lanes 32 w .. + 15 hold the stage's keys as bf16 hi parts and lanes
+        // 32 w + 16 .. + 31 the lo parts, two dims per column; warp half h
+        // writes dims 32 h .. 32 h + 31.  Thread t takes row t % 16.  The
+        // operand is free: this warp has seen the previous tile's scores, so
+        // its rope product, the operand's last reader, has ended.
         const TcTile& tr0 = tiles[rt];
         if (w < tr0.ns) {
           const int n0 = tr0.n_tok[w], sp0 = tr0.split[w];
-          const uint8_t* rope = smem + L::kRing + rt * kTcTileBytes + 8 * kTcPlaneBytes;
-          uint8_t* rope_k = smem + L::kRopeK;
-          const float2* cs = reinterpret_cast<const float2*>(smem + L::kCs) + rt * 256 + w * 64;
-          const float2 cs1 = cs[lane], cs2 = sp0 < n0 ? cs[32 + lane] : cs1;
-          // two rounds of four rows: a round's loads all go out before any of
-          // them is used, so the warp waits out two shared-memory latencies
-#pragma unroll 1
-          for (int k0 = 0; k0 < 8; k0 += 4) {
-            uint32_t v[4];  // each row's pair as bf16: a in the low half, b in the high
+          const int j = lane & 15, row = 16 * w + j, x7 = row & 7;
+          const bool lo_part = lane >= 16, live = j < n0;
+          const uint8_t* rope =
+              smem + L::kRing + rt * kTcTileBytes + 8 * kTcPlaneBytes + (row >> 3) * 1024 + x7 * 128;
+          const float4* cs = reinterpret_cast<const float4*>(reinterpret_cast<const float2*>(smem + L::kCs) +
+                                                             rt * 256 + w * 64 + (j >= sp0 ? 32 : 0));
+          uint32_t out[16];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int q = 8 * half + k0 + k, row = 16 * w + q;
-              v[k] = 0u;
-              if (q < n0) {
-                if (NEOX) {
-                  v[k] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rope + sw128(row, ia))) |
-                         (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rope + sw128(row, ib))) << 16);
-                } else {  // (2f, 2f + 1) are adjacent: one 4-byte access
-                  v[k] = *reinterpret_cast<const uint32_t*>(rope + sw128(row, ia));
+          for (int c = 0; c < 4; ++c) {  // output dims 32 half + 8 c .. + 7: columns 4 c .. 4 c + 3
+            float o[8];
+            if (NEOX) {
+              // frequency d pairs dims (d, d + 32): half 0 writes d, half 1 d + 32, d = 8 c .. 8 c + 7
+              uint4 xa = *reinterpret_cast<const uint4*>(rope + ((c ^ x7) << 4));
+              uint4 xb = *reinterpret_cast<const uint4*>(rope + (((4 + c) ^ x7) << 4));
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float4 cc = cs[4 * c + k];  // (cos, sin) of frequencies 8 c + 2 k, 8 c + 2 k + 1
+                const float2 a = bf_pair(word(xa, k)), b = bf_pair(word(xb, k));
+                o[2 * k] = half ? a.x * cc.y + b.x * cc.x : a.x * cc.x - b.x * cc.y;
+                o[2 * k + 1] = half ? a.y * cc.w + b.y * cc.z : a.y * cc.z - b.y * cc.w;
+              }
+            } else {
+              // dims (2 f, 2 f + 1) pair, frequency f = 16 half + 4 c + k
+              uint4 x = *reinterpret_cast<const uint4*>(rope + (((4 * half + c) ^ x7) << 4));
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const float4 cc = cs[8 * half + 2 * c + k2];  // (cos, sin) of two frequencies
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const float2 ab = bf_pair(word(x, 2 * k2 + e));
+                  const float cf = e ? cc.z : cc.x, sf = e ? cc.w : cc.y;
+                  o[4 * k2 + 2 * e] = ab.x * cf - ab.y * sf;
+                  o[4 * k2 + 2 * e + 1] = ab.x * sf + ab.y * cf;
                 }
               }
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const int q = 8 * half + k0 + k;
-              if (q >= n0) continue;
-              const int rh = 32 * w + q, rl = rh + 16;  // operand rows of the hi and lo parts
-              const float2 c = q >= sp0 ? cs2 : cs1;
-              const float a = bf_lo(v[k]), b = bf_hi(v[k]);
               uint32_t hi, lo;
-              split2_bf16(a * c.x - b * c.y, a * c.y + b * c.x, hi, lo);
-              if (NEOX) {
-                *reinterpret_cast<uint16_t*>(rope_k + sw128(rh, ia)) = static_cast<uint16_t>(hi);
-                *reinterpret_cast<uint16_t*>(rope_k + sw128(rh, ib)) = static_cast<uint16_t>(hi >> 16);
-                *reinterpret_cast<uint16_t*>(rope_k + sw128(rl, ia)) = static_cast<uint16_t>(lo);
-                *reinterpret_cast<uint16_t*>(rope_k + sw128(rl, ib)) = static_cast<uint16_t>(lo >> 16);
-              } else {
-                *reinterpret_cast<uint32_t*>(rope_k + sw128(rh, ia)) = hi;
-                *reinterpret_cast<uint32_t*>(rope_k + sw128(rl, ia)) = lo;
-              }
+              split2_bf16(o[2 * k], o[2 * k + 1], hi, lo);
+              out[4 * c + k] = live ? (lo_part ? lo : hi) : 0u;
             }
           }
-          fence_proxy_async_smem();
+          float outf[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) outf[k] = __uint_as_float(out[k]);
+          tmem_st16(tmem + (static_cast<uint32_t>(32 * w) << 16) + kRopeACol + 16 * half, outf);
+          tmem_wait_st();
         }
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&rot_done[rt]);
       }

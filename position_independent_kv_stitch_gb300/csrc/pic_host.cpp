@@ -638,6 +638,9 @@ void fill_freq(const pic_ctx* ctx, uint8_t* base, const WsLayout& w) {
   std::memcpy(base + w.freq_off, ctx->freq_turns.data(), ctx->freq_turns.size() * sizeof(float2));
 }
 
+// region attend-plan: stages, tiles, records and tensor maps of the decode
+// attention (a measurement record names this region).
+
 // Decode attention: every position [0, total) of each request becomes one
 // token entry (where its K/V row is), and each request's positions are cut
 // into stages of <= kAttnStageTokens consecutive positions sharing one
@@ -994,6 +997,8 @@ int64_t attend_keys(const AttnPlan& plan, int32_t layers, int64_t ctas, std::vec
   if (keys) keys->push_back(pic::AttnKey{static_cast<int32_t>(rec), 0});
   return rec;
 }
+
+// end region attend-plan
 
 }  // namespace
 
@@ -1618,6 +1623,8 @@ pic_status pic_rotation_cossin(pic_ctx* ctx, const int32_t* d_deltas, int32_t n,
 }
 
 // ------------------------------------------------------- decode attention
+// region attend-launch: workspace and launches of the decode attention (a
+// measurement record names this region).
 
 size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
                                   int32_t num_q_heads, int32_t num_layers) {
@@ -1797,6 +1804,8 @@ pic_status pic_attend_decode(pic_ctx* ctx, const pic_plan* const* plans, int32_t
   if (e != cudaSuccess) return cuda_fail(ctx, e, "attention launch");
   return ok(ctx);
 }
+
+// end region attend-launch
 
 }  // extern "C"
 

@@ -105,6 +105,9 @@ cudaError_t launch_tma(const KernelParams& p, const TmaConfig& c, int mode, int 
 
 // end region stitch-schedule
 
+// region attend-params: what the decode attention kernels share with the host
+// (a measurement record names this region).
+
 // ---- decode attention over a stitched context (pic_attention.cu)
 //
 // Work is cut into stages: <= kAttnStageTokens consecutive positions of one
@@ -244,6 +247,8 @@ struct TcMaps {
 bool attend_mla_tc_config(int hc, size_t* smem_bytes);
 cudaError_t launch_attend_mla_tc(const AttnParams& p, const TcMaps& maps, int pairing, int hc, int grid,
                                  size_t smem_bytes, cudaStream_t stream);
+
+// end region attend-params
 
 // Launchers; each returns the launch's cudaError_t.  `grid` is the number of
 // CTAs (persistent, grid-stride over units).
