@@ -62,7 +62,7 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("pic_kernels.cu", "pic_kernels_tma.cu", "pic_host.cpp#stitch-schedule",
+KERNEL_SOURCES = ("pic_kernels.cu", "pic_kernels_tma.cu", "pic_device.cuh", "pic_host.cpp#stitch-schedule",
                   "pic_internal.h#stitch-schedule")
 
 
