@@ -28,8 +28,11 @@ Pin status of each function (what outside fact each is checked against is in
 * ``rotate``             pinned (identity, quarter-turn closed forms,
                          complex-product and rotate-half forward RoPE,
                          composition brute force, norms, relative position)
-* ``llama3_inv_freq``    parity unpinned: the Llama-3.1 frequency rule is not
-                         on the pages; only its invariants are tested.
+* ``llama3_inv_freq``    pinned by values derived by hand from the public
+                         Llama-3.1 rule (not on the pages): blend weights of
+                         exactly 1/4, 1/2 and 3/4, both regime edges, the
+                         outer regimes, factor 1, and the regimes of
+                         Llama-3.1-8B's own table.
 * ``compose``            pinned (offsets printed on the EPIC guide's figures
                          and client request)
 * ``BlockPool``          pinned (brute force on tiny requests)

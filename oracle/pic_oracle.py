@@ -58,8 +58,11 @@ def llama3_inv_freq(theta: np.ndarray, factor: float, low_freq_factor: float,
                     high_freq_factor: float, orig_max_pos: int) -> np.ndarray:
     """Llama-3.1 long-context rescaling of the RoPE frequencies.
 
-    PARITY UNPINNED: this rule is not on the pages; it is the public
-    Llama-3.1 rule, stated as math.  With wavelength lambda_i = 2 pi / theta_i:
+    This rule is not on the pages; it is the public Llama-3.1 rule, stated
+    as math, and pinned by values derived from it by hand (wavelengths placed
+    so that the blend weight below is exactly 1/4, 1/2 or 3/4, the regime
+    edges, factor 1, and Llama-3.1-8B's own table), not by a second
+    transcription.  With wavelength lambda_i = 2 pi / theta_i:
     lambda_i < orig/high keeps theta_i; lambda_i > orig/low uses
     theta_i/factor; in between the two are blended linearly in
     s = (orig/lambda_i - low) / (high - low):
