@@ -449,13 +449,23 @@ size_t pic_attend_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* pla
  * into the latent space, q = [q_nope (512) | q_rope (64)] (head_dim 576), so
  *   s_t = softmax_scale * (q_nope . cKV_t + q_rope . R(delta) k_r,t) + bias,
  *   out = sum_t softmax(s)_t cKV_t   (out: [num_layers][n_req][num_q_heads][512]);
- * only the rope part is rotated (the kernel rotates q_rope by R(-delta)),
- * the latent is used as stored and serves as the value.  16, 32, 64 or 128
+ * only the rope part is rotated (with 16 heads per CTA the kernel rotates
+ * q_rope by R(-delta); with 32 and more it rotates the rope keys on their way
+ * through the SM), the latent is used as stored and serves as the value.  16, 32, 64 or 128
  * query heads (64 and 128 run as 2 and 4 groups of 32 that each read the
  * rows); v_pool and v_cache are ignored and may be NULL.  The cache's block tables are the plans' (as
  * pic_build_block_table returned them).  Two launches: a persistent kernel
  * streams the context through shared memory and leaves per-range softmax
- * records in the workspace, a second merges them into out and lse.  Errors:
+ * records in the workspace, a second merges them into out and lse.
+ * Device memory: the context keeps a device copy of the plan's read-only
+ * image (stages, token rows, record keys: at most about 10 bytes per context
+ * position, plus 8 per layer and request) for the last plan of each of two
+ * kinds (one delta per stage, or up to two), and uploads
+ * it again only when the plans, the layer count or the grid change, so a
+ * decode loop over the same plans uploads nothing but a zeroed status word.
+ * It is allocated stream-ordered on the call's stream and freed by
+ * pic_destroy; a call that replaces it first waits (on the device) for
+ * launches on any stream that still read it.  Errors:
  * PIC_ERR_UNSUPPORTED for other geometries or host-resident buffers,
  * PIC_ERR_RANGE for an empty context or a layer range outside the model,
  * PIC_ERR_CAPACITY for a short workspace; a bounded wait that gave up on the

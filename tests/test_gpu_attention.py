@@ -361,3 +361,58 @@ def test_llama_full_launch_sampled_layers():
     finally:
         st.close()
         torch.cuda.empty_cache()
+
+
+def test_plan_image_kept_on_device_follows_plans_layers_and_workspaces():
+    """The context keeps each cached attention plan's read-only image (stages,
+    token rows, record keys) on the device and uploads it again only when the
+    plans, the layer count or the grid change; each call zeroes its own
+    workspace's status word.  One context alternates two plan sets, two layer
+    windows, two workspaces and two streams: every call must equal the first
+    call of the same configuration bit for bit, and that one the oracle."""
+    S = _setup("neox", 128, 2, 4, 2)
+    try:
+        ctx, L, Hq, D = S["ctx"], S["L"], S["Hq"], S["D"]
+        g = torch.Generator().manual_seed(5)
+        q = torch.randn((L, 2, Hq, D), generator=g).to(torch.bfloat16).to(DEV)
+        scale = 1.0 / math.sqrt(D)
+        kp, vp = S["k_pool"].to(DEV), S["v_pool"].to(DEV)
+        kc, vc = S["k_cache"].to(DEV), S["v_cache"].to(DEV)
+        nbytes = pic.pic_attend_workspace_bytes(ctx, S["plans"], Hq, L)
+        wss = [torch.full((nbytes,), 0xAB, dtype=torch.uint8, device=DEV) for _ in range(2)]
+        side = torch.cuda.Stream()
+        configs = {
+            "both": (S["plans"], slice(0, 2), 0, L),
+            "second": ([S["plans"][1]], slice(1, 2), 0, L),
+            "both, layer 1": (S["plans"], slice(0, 2), 1, 1),
+        }
+        first = {}
+        order = ["both", "second", "both", "both, layer 1", "second", "both, layer 1", "both", "second"]
+        for i, name in enumerate(order):
+            plans, rq, lb, nl = configs[name]
+            qq = q[lb:lb + nl, rq].contiguous()
+            out = torch.full((nl, len(plans), Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+            lse = torch.full((nl, len(plans), Hq), float("nan"), dtype=torch.float32, device=DEV)
+            ws = wss[i % 2]
+            stream = side if i % 3 == 2 else None
+            if stream is not None:
+                side.wait_stream(torch.cuda.current_stream())
+            pic.pic_attend_decode(ctx, plans, pic.PIC_ATTEND_FUSED, qq, scale, kp, vp, kc, vc, out, lse, ws,
+                                  sink_bias=-15.0, layer_begin=lb, stream=stream)
+            torch.cuda.synchronize()
+            assert pic.pic_query_device_status(ctx, ws) == 0, (i, name)
+            got = (out.cpu().numpy(), lse.cpu().numpy())
+            if name not in first:
+                first[name] = got
+            else:
+                assert np.array_equal(got[0], first[name][0]) and np.array_equal(got[1], first[name][1]), (i, name)
+        want, want_lse = _oracle(S, bits(q.cpu()), scale, -15.0)
+        out, lse = first["both"]
+        np.testing.assert_allclose(out, want, atol=2e-3, rtol=0)
+        np.testing.assert_allclose(lse, want_lse, atol=2e-3, rtol=0)
+        out, lse = first["both, layer 1"]
+        np.testing.assert_allclose(out, want[1:2], atol=2e-3, rtol=0)
+        out, lse = first["second"]
+        np.testing.assert_allclose(out, want[:, 1:2], atol=2e-3, rtol=0)
+    finally:
+        pic.pic_destroy(S["ctx"])
