@@ -33,9 +33,10 @@
 //       32 heads: q_rope as given, at the key's first tile, and for every
 //       tile the cos / sin of its stage deltas (lane f: frequency f);
 //   * (32 heads) softmax warps 0-7 first rotate the rope keys: the two warps
-//     of lane quadrant s take stage s, half of the dims each; thread t rotates
-//     row t % 16's k_r by its delta in fp32 and writes its bf16 hi (t < 16)
-//     or lo part (t >= 16) into TMEM, so that the quadrant's lanes hold an
+//     of lane quadrant s take stage s, half of the dims each; threads t and
+//     t + 16 rotate half of row t % 16's k_r each by its delta in fp32, swap
+//     halves, and write its bf16 hi (t < 16) or lo part (t >= 16) into TMEM,
+//     so that the quadrant's lanes hold an
 //     A operand of 128 rows (stage s's hi rows in lanes 32 s .. + 15, its lo
 //     rows in lanes 32 s + 16 .. + 31, two dims per column);
 //   * two score issuers (one warp each) issue S = rows [q_nope | rope]^T into
@@ -840,14 +841,19 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         if (w < tr0.ns) {
           const int n0 = tr0.n_tok[w], sp0 = tr0.split[w];
           const int j = lane & 15, row = 16 * w + j, x7 = row & 7;
-          const bool lo_part = lane >= 16, live = j < n0;
+          const bool live = j < n0;
           const uint8_t* rope =
               smem + L::kRing + rt * kTcTileBytes + 8 * kTcPlaneBytes + (row >> 3) * 1024 + x7 * 128;
           const float4* cs = reinterpret_cast<const float4*>(reinterpret_cast<const float2*>(smem + L::kCs) +
                                                              rt * 256 + w * 64 + (j >= sp0 ? 32 : 0));
-          uint32_t out[16];
+          // Threads t and t + 16 share row t % 16: each rotates half of the
+          // warp's 16 columns (thread part p = t / 16 takes columns 8 p ..
+          // 8 p + 7) and hands the other thread the part that one writes.
+          const int p = lane >> 4;
+          uint32_t own[8], other[8];  // this thread's part, and the partner's part, of columns 8 p + m
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // output dims 32 half + 8 c .. + 7: columns 4 c .. 4 c + 3
+          for (int cc2 = 0; cc2 < 2; ++cc2) {
+            const int c = 2 * p + cc2;  // output dims 32 half + 8 c .. + 7: columns 4 c .. 4 c + 3
             float o[8];
             if (NEOX) {
               // frequency d pairs dims (d, d + 32): half 0 writes d, half 1 d + 32, d = 8 c .. 8 c + 7
@@ -879,8 +885,16 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
             for (int k = 0; k < 4; ++k) {
               uint32_t hi, lo;
               split2_bf16(o[2 * k], o[2 * k + 1], hi, lo);
-              out[4 * c + k] = live ? (lo_part ? lo : hi) : 0u;
+              own[4 * cc2 + k] = p ? lo : hi;
+              other[4 * cc2 + k] = p ? hi : lo;
             }
+          }
+          uint32_t out[16];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, other[m], 16);  // the partner's columns, this part
+            out[m] = live ? (p ? got : own[m]) : 0u;
+            out[8 + m] = live ? (p ? own[m] : got) : 0u;
           }
           float outf[16];
 #pragma unroll
