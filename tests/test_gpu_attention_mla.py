@@ -316,3 +316,44 @@ def test_deepseek_full_launch_sampled_layers(H):
     finally:
         st.close()
         torch.cuda.empty_cache()
+
+
+def test_mla_plan_image_kept_on_device_across_head_counts_and_layer_windows():
+    """One context alternates 16 and 32 query heads (the query-rotating and
+    the key-rotating tiles, each its own cached plan and device image) and
+    two layer windows, on two workspaces: every call must equal the first
+    call of the same configuration bit for bit, and that one the oracle."""
+    S = _setup("interleaved", 2, seed=6)
+    try:
+        ctx, L = S["ctx"], S["L"]
+        g = torch.Generator().manual_seed(8)
+        q_all = torch.randn((L, 3, 32, ROW), generator=g).to(torch.bfloat16).to(DEV)
+        scale = 1.0 / math.sqrt(192)
+        pool, cache = S["pool"].to(DEV), S["cache"].to(DEV)
+        nbytes = max(pic.pic_attend_workspace_bytes(ctx, S["plans"], H, L) for H in (16, 32))
+        wss = [torch.full((nbytes,), 0xCD, dtype=torch.uint8, device=DEV) for _ in range(2)]
+        first = {}
+        order = [(16, 0, 2), (32, 0, 2), (16, 1, 1), (32, 0, 2), (16, 0, 2), (32, 1, 1), (16, 1, 1), (32, 1, 1)]
+        for i, (H, lb, nl) in enumerate(order):
+            q = q_all[lb:lb + nl, :, :H].contiguous()
+            out = torch.full((nl, 3, H, LATENT), float("nan"), dtype=torch.float32, device=DEV)
+            lse = torch.full((nl, 3, H), float("nan"), dtype=torch.float32, device=DEV)
+            ws = wss[i % 2]
+            pic.pic_attend_decode(ctx, S["plans"], pic.PIC_ATTEND_FUSED, q, scale, pool, None, cache, None, out, lse,
+                                  ws, sink_bias=-15.0, layer_begin=lb)
+            torch.cuda.synchronize()
+            assert pic.pic_query_device_status(ctx, ws) == 0, (i, H, lb)
+            got = (out.cpu().numpy(), lse.cpu().numpy())
+            key = (H, lb, nl)
+            if key not in first:
+                first[key] = got
+            else:
+                assert np.array_equal(got[0], first[key][0]) and np.array_equal(got[1], first[key][1]), (i, key)
+        for H in (16, 32):
+            q = q_all[:, :, :H].cpu()
+            out, lse = first[(H, 0, 2)]
+            _check_against_oracle(S, q, out.astype(np.float64), lse.astype(np.float64), scale, -15.0, 2e-3)
+            out1, _ = first[(H, 1, 1)]
+            np.testing.assert_allclose(out1, out[1:2], atol=1e-4, rtol=0)
+    finally:
+        pic.pic_destroy(S["ctx"])
