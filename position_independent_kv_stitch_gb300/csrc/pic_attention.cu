@@ -160,6 +160,9 @@ __device__ __forceinline__ int advance_stage(int j, int k, int n_stages) {
 // grid: persistent CTAs; block: 32 * (HB + 2) threads (HB consumers, a K and a V producer).
 template <int PAIRING, int D, int G>
 __global__ void __launch_bounds__(32 * (kAttnMaxHeads + 2), 1) k_attend(const AttnParams P) {
+  // the merge that reads this kernel's records may be scheduled from now on
+  // (it waits for this grid's completion before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr int HALF = D / 2;
   constexpr int KS = D / 16;   // k-steps of Q K^T
@@ -504,6 +507,9 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads) k_attend_merge(const AttnParams P, int group) {
   __shared__ float s_e[kAttnMaxCtas];  // exp2(m_k - M) per record
   __shared__ float s_red[kMergeThreads / 32];
+  // launched as a programmatic dependent of the attention kernel: wait until
+  // that grid has completed and its records are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int r = blockIdx.x, gq = blockIdx.y, lz = blockIdx.z;
   const int hk = gq / group, g = gq % group;
   const int HB = P.heads_per_cta;
@@ -533,6 +539,26 @@ __global__ void __launch_bounds__(kMergeThreads) k_attend_merge(const AttnParams
     P.lse[(static_cast<int64_t>(lz) * P.n_req + r) * P.num_q_heads + gq] = (M + log2f(tot)) * 0.69314718055994531f;
 }
 
+// The merge after an attention kernel, as its programmatic dependent: the
+// merge's CTAs may be scheduled while the attention kernel's last CTAs still
+// run (each attention CTA allows it once it has started), so the launch
+// latency hides behind the attention kernel's tail; the merge's first
+// instruction waits for that kernel's completion and memory.
+template <int D>
+cudaError_t launch_merge(const AttnParams& p, int group, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_req, p.num_q_heads, p.n_layers);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attend_merge<D>, p, group);
+}
+
 template <int PAIRING, int D, int G>
 cudaError_t launch_g(const AttnParams& p, int grid, size_t smem, cudaStream_t s) {
   auto kern = k_attend<PAIRING, D, G>;
@@ -541,8 +567,7 @@ cudaError_t launch_g(const AttnParams& p, int grid, size_t smem, cudaStream_t s)
   kern<<<grid, 32 * (p.heads_per_cta + 2), smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_attend_merge<D><<<dim3(p.n_req, p.num_q_heads, p.n_layers), kMergeThreads, 0, s>>>(p, G);
-  return cudaGetLastError();
+  return launch_merge<D>(p, G, s);
 }
 
 template <int PAIRING, int D, int G>
@@ -645,6 +670,9 @@ __host__ __device__ inline MlaLayout mla_layout(int ng, int ring) {
 // grid: persistent CTAs; block: 32 * (4 NG + 1) threads (NG groups of 16 heads).
 template <int PAIRING, int NG>
 __global__ void __launch_bounds__(32 * (4 * NG + 1), NG == 1 ? 2 : 1) k_attend_mla(const AttnParams P) {
+  // the merge that reads this kernel's records may be scheduled from now on
+  // (it waits for this grid's completion before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr int NCW = 4 * NG;                          // consumer warps
   constexpr int HC = kMlaHeadsPerGroup * NG;           // query heads per CTA (and per record)
@@ -997,9 +1025,7 @@ cudaError_t launch_mla_g(const AttnParams& p, int grid, size_t smem, cudaStream_
   kern<<<grid, 32 * (4 * NG + 1), smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_attend_merge<kMlaLatent><<<dim3(p.n_req, p.num_q_heads, p.n_layers), kMergeThreads, 0, s>>>(
-      p, kMlaHeadsPerGroup * NG);
-  return cudaGetLastError();
+  return launch_merge<kMlaLatent>(p, kMlaHeadsPerGroup * NG, s);
 }
 
 template <int PAIRING, int NG>
@@ -1076,8 +1102,7 @@ cudaError_t launch_attend_mla(const AttnParams& p, int pairing, int ng, int grid
 }
 
 cudaError_t launch_attend_merge_mla(const AttnParams& p, int heads_per_record, cudaStream_t s) {
-  k_attend_merge<kMlaLatent><<<dim3(p.n_req, p.num_q_heads, p.n_layers), kMergeThreads, 0, s>>>(p, heads_per_record);
-  return cudaGetLastError();
+  return launch_merge<kMlaLatent>(p, heads_per_record, s);
 }
 
 }  // namespace pic

@@ -345,6 +345,9 @@ __device__ __forceinline__ void split2_bf16(float x, float y, uint32_t& hi, uint
 template <int PAIRING, int HC>
 __global__ void __launch_bounds__(tc_threads(HC), 1)
     k_attend_mla_tc(const AttnParams P, const __grid_constant__ TcMaps maps) {
+  // the merge that reads this kernel's records may be scheduled from now on
+  // (it waits for this grid's completion before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;");
   using L = TcLayout<HC>;
   constexpr bool NEOX = (PAIRING == kNeox);
   constexpr bool KEYS = L::kKeys;  // rotate the rope keys (else the query)
