@@ -20,9 +20,12 @@
  *
  * Conventions for every function:
  *   - Ownership: the caller owns every device buffer (pools, caches, block
- *     tables, index outputs, workspaces).  The library never allocates device
- *     memory.  It owns its host-side registry, block allocator and pic_plan
- *     objects.
+ *     tables, index outputs, workspaces).  The library owns its host-side
+ *     registry, block allocator and pic_plan objects, and only two pieces of
+ *     device memory: the fixed scratch array of pic_stitch_noalloc, and the
+ *     device copy of the decode attention's plan image that pic_attend_decode
+ *     keeps per context (freed by pic_destroy).
+ *   - Threads: a context is used by one host thread at a time.
  *   - Streams: all device work is enqueued on the caller's stream and is
  *     asynchronous; host arguments may be reused as soon as a call returns.
  *   - Errors: every call returns a pic_status; on failure nothing was
