@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
       // buffer); at a key's first tile also once the query operands are
       // written.  The first issuer takes the even latent k-steps and then the
       // rope k-steps: rotated keys, once the softmax warps have rotated them,
-      // over the hi and the lo plane (one accumulator); rotated queries, once
+      // four of M = 128 with A their hi and lo rows in TMEM; rotated queries, once
       // the query warp has written this tile's entries, over the rope plane
       // against every entry.  The second issuer takes the odd latent k-steps.
       // Each writes its own latent partial sums (k-step mod NP).
@@ -837,7 +837,7 @@ __global__ void __launch_bounds__(tc_threads(HC), 1)
         // into the rotated-key operand in TMEM: an A operand of 128 rows whose
         // lanes 32 w .. + 15 hold the stage's keys as bf16 hi parts and lanes
         // 32 w + 16 .. + 31 the lo parts, two dims per column; warp half h
-        // writes dims 32 h .. 32 h + 31.  Thread t takes row t % 16.  The
+        // writes dims 32 h .. 32 h + 31.  Thread t writes lane 32 w + t.  The
         // operand is free: this warp has seen the previous tile's scores, so
         // its rope product, the operand's last reader, has ended.
         const TcTile& tr0 = tiles[rt];

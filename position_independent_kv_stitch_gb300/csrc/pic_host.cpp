@@ -611,6 +611,9 @@ void release_staging(pic_ctx* ctx) {
 }
 
 void release_attn_resident(pic_ctx* ctx) {
+  bool any = false;
+  for (const AttnResident& r : ctx->attn_res) any |= r.dev != nullptr || r.last_use != nullptr;
+  if (!any) return;
   int cur = -1;
   cudaGetDevice(&cur);
   for (AttnResident& r : ctx->attn_res) {
