@@ -381,7 +381,7 @@ def test_plan_image_kept_on_device_follows_plans_layers_and_workspaces():
         nbytes = pic.pic_attend_workspace_bytes(ctx, S["plans"], Hq, L)
         wss = [torch.full((nbytes,), 0xAB, dtype=torch.uint8, device=DEV) for _ in range(2)]
         side = torch.cuda.Stream()
-        configs = {
+        cases = {
             "both": (S["plans"], slice(0, 2), 0, L),
             "second": ([S["plans"][1]], slice(1, 2), 0, L),
             "both, layer 1": (S["plans"], slice(0, 2), 1, 1),
@@ -389,7 +389,7 @@ def test_plan_image_kept_on_device_follows_plans_layers_and_workspaces():
         first = {}
         order = ["both", "second", "both", "both, layer 1", "second", "both, layer 1", "both", "second"]
         for i, name in enumerate(order):
-            plans, rq, lb, nl = configs[name]
+            plans, rq, lb, nl = cases[name]
             qq = q[lb:lb + nl, rq].contiguous()
             out = torch.full((nl, len(plans), Hq, D), float("nan"), dtype=torch.float32, device=DEV)
             lse = torch.full((nl, len(plans), Hq), float("nan"), dtype=torch.float32, device=DEV)
