@@ -190,6 +190,66 @@ def test_gqa_geometries_ragged(pairing, D, H, bs, variant):
         st.close()
 
 
+def _random_workload(seed):
+    """A seeded small batch: GQA or MLA, either pairing, 1-4 layers, odd head
+    counts and block sizes, 2-9 chunks of 1-150 tokens, 1-3 requests that
+    truncate and repeat chunks, k of 0-6 and a leading carve-out of 0-8."""
+    rng = np.random.default_rng(1000 + seed)
+    kind = "gqa" if seed % 3 else "mla"
+    pairing = ["neox", "interleaved"][int(rng.integers(2))]
+    L = int(rng.integers(1, 5))
+    H = int(rng.choice([1, 2, 3, 8]))
+    D = int(rng.choice([64, 128, 256]))
+    bs = int(rng.choice([1, 5, 8, 16, 33]))
+    lens = [int(x) for x in rng.integers(1, 151, size=int(rng.integers(2, 10)))]
+    reqs = []
+    for _ in range(int(rng.integers(1, 4))):
+        req = []
+        for _ in range(int(rng.integers(1, 7))):
+            c = int(rng.integers(len(lens)))
+            take = lens[c] if rng.random() < 0.7 else int(rng.integers(0, lens[c] + 1))
+            req.append((c, take))
+        if sum(t for _, t in req) == 0:
+            req[0] = (req[0][0], lens[req[0][0]])
+        reqs.append(req)
+    k = (int(rng.integers(0, 7)), int(rng.integers(0, 9)))
+    return _custom_workload(f"rand-{seed}", kind, L, H, D, pairing, bs, lens, reqs,
+                            theta=float(rng.choice([1e4, 5e5, 1e6])), k=k)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_small_batches_match_oracle(seed, variant):
+    """Seeded random batches (geometry, chunk lengths, truncation, repeats,
+    recompute widths) against the oracle: K within the contract tolerance, V
+    and the MLA latent bit for bit, untouched rows left as they were, block
+    tables and recompute lists exact."""
+    wl = _random_workload(seed)
+    m = wl.model
+    st = Stitched(wl, pool_device="cpu", spare_blocks=2).run()
+    try:
+        segs, tables, rec = oracle_side(wl, st.nb)
+        for r in range(len(tables)):
+            assert st.tables[r][:len(tables[r])].tolist() == tables[r]
+        want_k, want_v = oracle.stitch_paged(bits(st.k_pool), None if st.v_pool is None else bits(st.v_pool), segs,
+                                             tables, st.nb, st.bs, theta_of(m), pairing_of(m), m.rope_offset,
+                                             m.rope_dim)
+        got = f64(st.k_cache)
+        if m.kind == "gqa":
+            assert_k_close(got, want_k, "K")
+            np.testing.assert_array_equal(bits(st.v_cache), want_v)
+        else:
+            written = ~np.isnan(want_k[..., 0])
+            wb = np.where(np.isnan(want_k), 0, want_k)
+            assert np.array_equal(got[..., :512][written], wb[..., :512][written])
+            assert_k_close(got[..., 512:], want_k[..., 512:], "k_r")
+        assert np.all(bits(st.k_cache)[np.isnan(want_k)] == 0xFFFF)
+        indptr, idx = oracle.recompute_csr(rec)
+        assert st.indptr.cpu().tolist() == indptr.tolist()
+        assert st.ridx.cpu().numpy()[:st.n_rec].tolist() == idx.tolist()
+    finally:
+        st.close()
+
+
 def test_explicit_positions_base_pos_and_extreme_delta(variant):
     """Chunks cached at a non-zero base position (negative delta up to
     -(2^24 - 4)), explicit positions with inline gaps, a delta-0 chunk (bit
