@@ -849,6 +849,8 @@ def run_cdc(args):
     pic.pic_query_device_status(None, ws)
     ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, dev)
     kms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    dev_props = torch.cuda.get_device_properties(dev)
+    gather_mhz = (clk or {}).get("sm_mhz") or 2070.0  # the GB300's maximum SM clock when unsampled
 
     # algorithmic bytes: token ids read once, offsets read, CSR offsets + ends + fingerprints written
     algo = 4 * n_tok + 8 * (n_docs + 1) * 2 + 16 * n_chunks
@@ -911,6 +913,15 @@ def run_cdc(args):
                      "frac": algo / (kms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
                      "traffic": recorded_traffic("rag_corpus/cdc" if not (args.cdc_min or args.cdc_max) else "-"),
                      "algorithmic_bytes_per_launch": algo, "launch_ms": kms},
+        # The bound that binds here is not HBM: every token costs one random
+        # 8-byte Gear load, one L1TEX request of its own (a warp's 32 loads
+        # are 32 requests), and an SM takes about one request per cycle.
+        "roofline_gather": {"bound": "l1tex requests", "kernel": "pic_cdc_chunk (all launches)",
+                            "achieved": n_tok / (kms * 1e-3), "unit": "requests/s",
+                            "peak": dev_props.multi_processor_count * gather_mhz * 1e6,
+                            "frac": n_tok / (kms * 1e-3) / (dev_props.multi_processor_count * gather_mhz * 1e6),
+                            "peak_source": f"one request per SM per cycle at {gather_mhz:.0f} MHz "
+                                           f"(the median SM clock of the timed region)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * (7 if (args.cdc_min > 1 or args.cdc_max > 0) else 5),
