@@ -720,7 +720,8 @@ extern "C" pic_status pic_cdc_chunk(const int32_t* d_tokens, int64_t n_tokens, c
     k_cdc_emit<<<grid, kHashThreads, 0, s>>>(d_doc_offsets, n_docs, bits, tile_count, first_doc, n_tiles,
                                              d_chunk_ends, capacity, d_chunk_indptr, hdr);
     if (d_fingerprints && capacity > 0)
-      k_xxh64<<<sms * 5, kXxhThreads, 0, s>>>(  // 5 CTAs of 45 registers fill an SMd_tokens, n_tokens, nullptr, d_doc_offsets, d_chunk_ends,
+      // five CTAs per SM: its 45 registers allow them, and the extra warps hide the rounds' latency
+      k_xxh64<<<sms * 5, kXxhThreads, 0, s>>>(d_tokens, n_tokens, nullptr, d_doc_offsets, d_chunk_ends,
                                               tile_count + n_tiles, 0, capacity, seed, d_fingerprints, &hdr->status,
                                               hdr);
   }
