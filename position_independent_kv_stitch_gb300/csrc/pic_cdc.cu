@@ -107,6 +107,15 @@ __device__ __forceinline__ uint32_t word_mask(int64_t w, int64_t lo, int64_t hi)
   return upto & ~((1u << a) - 1u);
 }
 
+// The kernels of one call run back to back: each after the first is
+// launched as a programmatic dependent of the one before it.  A kernel lets
+// the next be scheduled once all its CTAs run, and waits for the previous
+// kernel's completion (and memory) before it reads anything.
+__device__ __forceinline__ void after_previous_kernel() {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ bool docs_bad(const WsHeader* h) {
   return (*reinterpret_cast<const volatile uint32_t*>(&h->status) & PIC_DEV_BAD_DOCS) != 0;
 }
@@ -122,6 +131,7 @@ __device__ __forceinline__ bool docs_bad(const WsHeader* h) {
 __global__ void k_cdc_docs(const int64_t* __restrict__ offsets, int32_t n_docs, int64_t n_tokens,
                            int32_t* __restrict__ first_doc, int64_t* __restrict__ tile_count, int64_t n_tiles,
                            WsHeader* hdr) {
+  asm volatile("griddepcontrol.launch_dependents;");  // the hash pass may be scheduled from now on
   const int64_t n = static_cast<int64_t>(n_docs) + 2;
   for (int64_t d = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; d < n;
        d += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -164,6 +174,7 @@ k_cdc_hash(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* 
   __shared__ uint32_t s_bnd[kBndWords];
   __shared__ uint64_t s_part[kHashThreads + 2];  // B_j at index j + 2; halo blocks -2, -1 at 0, 1
 
+  after_previous_kernel();
   if (docs_bad(hdr)) return;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -284,6 +295,7 @@ k_cdc_hash(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* 
 __global__ void __launch_bounds__(kWarpThreads)
 k_cdc_walk(const int64_t* __restrict__ offsets, int32_t n_docs, uint32_t* bits, int32_t min_len,
            int32_t max_len, const WsHeader* hdr) {
+  after_previous_kernel();
   if (docs_bad(hdr)) return;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -338,6 +350,7 @@ k_cdc_walk(const int64_t* __restrict__ offsets, int32_t n_docs, uint32_t* bits, 
 __global__ void __launch_bounds__(kWarpThreads)
 k_cdc_tile_count(const uint32_t* __restrict__ bits, int64_t* __restrict__ tile_count, int64_t n_tiles,
                  const WsHeader* hdr) {
+  after_previous_kernel();
   if (docs_bad(hdr)) return;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -361,6 +374,7 @@ k_cdc_scan(int64_t* __restrict__ tile_count, int64_t n_tiles, int64_t* __restric
   __shared__ int64_t s_warp[kScanThreads / 32];
   __shared__ int64_t s_carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  after_previous_kernel();
   if (docs_bad(hdr) || n_tiles == 0) {
     for (int64_t d = tid; d <= n_docs; d += kScanThreads) indptr[d] = 0;
     return;
@@ -424,6 +438,7 @@ k_cdc_emit(const int64_t* __restrict__ offsets, int32_t n_docs, const uint32_t* 
   __shared__ int32_t s_warp[kHashThreads / 32];
   __shared__ int32_t s_pref[kTileWords];
   __shared__ uint32_t s_word[kTileWords];
+  after_previous_kernel();
   if (docs_bad(hdr)) return;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
@@ -518,6 +533,7 @@ k_xxh64(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* __r
         uint32_t* status, const WsHeader* hdr) {
   __shared__ uint64_t s_acc[4][kXxhBatch];
   __shared__ int s_next;
+  after_previous_kernel();
   if (hdr && docs_bad(hdr)) return;
   int64_t n = n_host;
   if (n_dev) {
@@ -630,6 +646,23 @@ k_xxh64(const int32_t* __restrict__ tokens, int64_t n_tokens, const int64_t* __r
 
 // ---------------------------------------------------------------- host side
 
+// A kernel launched as a programmatic dependent of the previous one on the
+// stream (see after_previous_kernel).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kern)(KArgs...), int grid, int block, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
@@ -703,29 +736,34 @@ extern "C" pic_status pic_cdc_chunk(const int32_t* d_tokens, int64_t n_tokens, c
     k_cdc_docs<<<static_cast<int>(grid < 1 ? 1 : grid), 256, 0, s>>>(d_doc_offsets, n_docs, n_tokens, first_doc,
                                                                       tile_count, n_tiles, hdr);
   }
-  if (n_tiles > 0) {
+  e = cudaGetLastError();
+  if (n_tiles > 0 && e == cudaSuccess) {
     const int grid = static_cast<int>(n_tiles < static_cast<int64_t>(sms) * 2 ? n_tiles : static_cast<int64_t>(sms) * 2);
-    k_cdc_hash<<<grid, kHashThreads, 0, s>>>(d_tokens, n_tokens, d_doc_offsets, n_docs, d_gear,
-                                             static_cast<uint32_t>(vocab), threshold, first_doc, bits,
-                                             reinterpret_cast<unsigned long long*>(tile_count), n_tiles, hdr);
-    if (n_docs > 0 && (min_len > 1 || max_len > 0)) {
-      k_cdc_walk<<<warp_grid(n_docs, sms), kWarpThreads, 0, s>>>(d_doc_offsets, n_docs, bits, min_len, max_len,
-                                                                  hdr);
-      k_cdc_tile_count<<<warp_grid(n_tiles, sms), kWarpThreads, 0, s>>>(bits, tile_count, n_tiles, hdr);
+    e = launch_after(k_cdc_hash, grid, kHashThreads, s, d_tokens, n_tokens, d_doc_offsets, n_docs, d_gear,
+                     static_cast<uint32_t>(vocab), threshold, static_cast<const int32_t*>(first_doc), bits,
+                     reinterpret_cast<unsigned long long*>(tile_count), n_tiles, hdr);
+    if (e == cudaSuccess && n_docs > 0 && (min_len > 1 || max_len > 0)) {
+      e = launch_after(k_cdc_walk, warp_grid(n_docs, sms), kWarpThreads, s, d_doc_offsets, n_docs, bits, min_len,
+                       max_len, static_cast<const WsHeader*>(hdr));
+      if (e == cudaSuccess)
+        e = launch_after(k_cdc_tile_count, warp_grid(n_tiles, sms), kWarpThreads, s,
+                         static_cast<const uint32_t*>(bits), tile_count, n_tiles, static_cast<const WsHeader*>(hdr));
     }
   }
-  k_cdc_scan<<<1, kScanThreads, 0, s>>>(tile_count, n_tiles, d_chunk_indptr, n_docs, capacity, hdr);
-  if (n_tiles > 0) {
+  if (e == cudaSuccess)
+    e = launch_after(k_cdc_scan, 1, kScanThreads, s, tile_count, n_tiles, d_chunk_indptr, n_docs, capacity, hdr);
+  if (n_tiles > 0 && e == cudaSuccess) {
     const int grid = static_cast<int>(n_tiles < static_cast<int64_t>(sms) * 4 ? n_tiles : static_cast<int64_t>(sms) * 4);
-    k_cdc_emit<<<grid, kHashThreads, 0, s>>>(d_doc_offsets, n_docs, bits, tile_count, first_doc, n_tiles,
-                                             d_chunk_ends, capacity, d_chunk_indptr, hdr);
-    if (d_fingerprints && capacity > 0)
+    e = launch_after(k_cdc_emit, grid, kHashThreads, s, d_doc_offsets, n_docs, static_cast<const uint32_t*>(bits),
+                     static_cast<const int64_t*>(tile_count), static_cast<const int32_t*>(first_doc), n_tiles,
+                     d_chunk_ends, capacity, d_chunk_indptr, static_cast<const WsHeader*>(hdr));
+    if (e == cudaSuccess && d_fingerprints && capacity > 0)
       // five CTAs per SM: its 45 registers allow them, and the extra warps hide the rounds' latency
-      k_xxh64<<<sms * 5, kXxhThreads, 0, s>>>(d_tokens, n_tokens, nullptr, d_doc_offsets, d_chunk_ends,
-                                              tile_count + n_tiles, 0, capacity, seed, d_fingerprints, &hdr->status,
-                                              hdr);
+      e = launch_after(k_xxh64, sms * 5, kXxhThreads, s, d_tokens, n_tokens, static_cast<const int64_t*>(nullptr),
+                       d_doc_offsets, static_cast<const int64_t*>(d_chunk_ends),
+                       static_cast<const int64_t*>(tile_count + n_tiles), static_cast<int64_t>(0), capacity, seed,
+                       d_fingerprints, &hdr->status, static_cast<const WsHeader*>(hdr));
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "chunking launch");
   return set_error(nullptr, PIC_OK, "");
 }
