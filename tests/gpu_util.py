@@ -116,3 +116,66 @@ def theta_of(m):
 
 def pairing_of(m):
     return oracle.NEOX_HALF if m.pairing == "neox" else oracle.INTERLEAVED
+
+
+def random_attend_layout(rng, bs, max_chunk=300, max_req_tokens=2500):
+    """A seeded random decode context, as plain numbers: 2-10 pool chunks of
+    1..max_chunk tokens, maybe one block-resident chunk (1-79 tokens, cached
+    at a random base position), and 1-4 requests of 1-8 chunk occurrences
+    (repeats, some truncated, some to nothing), inline tokens before, between
+    and after them, and a pseudo-sink width k of 0-6.  `nb` is the cache
+    blocks the requests and the block-resident chunk need, plus two."""
+    lens = [int(x) for x in rng.integers(1, max_chunk + 1, size=int(rng.integers(2, 11)))]
+    offs = [0]
+    for n in lens[:-1]:
+        offs.append(offs[-1] + n)
+    block_chunk = (int(rng.integers(1, 80)), int(rng.integers(0, 5000))) if rng.random() < 0.5 else None
+    kinds = len(lens) + (1 if block_chunk else 0)
+    reqs = []
+    for _ in range(int(rng.integers(1, 5))):
+        start = int(rng.integers(0, 21)) if rng.random() < 0.5 else 0
+        chunks, takes, pos, p = [], [], [], start
+        for _ in range(int(rng.integers(1, 9))):
+            c = int(rng.integers(kinds))
+            full = lens[c] if c < len(lens) else block_chunk[0]
+            take = full if rng.random() < 0.8 else int(rng.integers(0, full + 1))
+            gap = int(rng.integers(1, 31)) if rng.random() < 0.3 else 0
+            if p + gap + take > max_req_tokens:
+                break
+            p += gap
+            chunks.append(c)
+            takes.append(take)
+            pos.append(p)
+            p += take
+        tail = int(rng.integers(0, 41)) if rng.random() < 0.5 else 0
+        reqs.append(dict(chunks=chunks, takes=takes, pos=pos, start=start, total=max(1, p + tail)))
+    nb = sum(-(-r["total"] // bs) for r in reqs) + (-(-block_chunk[0] // bs) if block_chunk else 0) + 2
+    return dict(lens=lens, offs=offs, P=sum(lens), block_chunk=block_chunk, reqs=reqs, nb=nb,
+                k=int(rng.integers(0, 7)))
+
+
+def register_attend_layout(ctx, layout, tag, bs):
+    """Registers the layout's chunks with ctx (the block-resident one in the
+    cache's last blocks) and builds its requests.  Returns (plans, block
+    tables, sources), sources mapping a chunk id to ("pool", first token) or
+    ("blocks", block ids)."""
+    ids, sources = [], {}
+    for c, (o, n) in enumerate(zip(layout["offs"], layout["lens"])):
+        cid = pic.pic_register_chunk(ctx, W.chunk_key(tag, c), o, n)[0]
+        ids.append(cid)
+        sources[cid] = ("pool", o)
+    if layout["block_chunk"]:
+        n_b, base = layout["block_chunk"]
+        nblk = -(-n_b // bs)
+        blocks = list(range(layout["nb"] - nblk, layout["nb"]))
+        cid = pic.pic_register_chunk_blocks(ctx, W.chunk_key(tag, 99), blocks, n_b, base)[0]
+        ids.append(cid)
+        sources[cid] = ("blocks", blocks)
+    plans, tables = [], []
+    for r in layout["reqs"]:
+        plan, bt = pic.pic_build_block_table(ctx, [ids[c] for c in r["chunks"]], -(-r["total"] // bs),
+                                             take_tokens=r["takes"], dst_pos=r["pos"], start_pos=r["start"],
+                                             total_tokens=r["total"], k_nonleading=layout["k"])
+        plans.append(plan)
+        tables.append(bt)
+    return plans, tables, sources

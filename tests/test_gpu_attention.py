@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_util import Stitched, bits
+from gpu_util import Stitched, bits, random_attend_layout, register_attend_layout
 from position_independent_kv_stitch_gb300 import pic
 
 pytestmark = pytest.mark.gpu
@@ -312,6 +312,77 @@ def test_fused_attention_long_mixed_contexts(pairing, D, Hkv, G, L, bias_value, 
                 o, s = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[l, r]), keys[l], vals[l], scale, bias)
                 np.testing.assert_allclose(out[l, r], o, atol=2e-3, rtol=0)
                 np.testing.assert_allclose(lse[l, r], s, atol=2e-3, rtol=0)
+    finally:
+        pic.pic_destroy(S["ctx"])
+
+
+def _random_setup(seed):
+    """A seeded random GQA context: either pairing, head_dim 64 or 128, 1-16
+    KV heads (3 and 5 included, 16 as two head groups), 1-8 query heads per
+    KV head, 1-3 layers, block size 1-33, plain or Llama-3.1 frequencies, and
+    the chunk and request mix of random_attend_layout."""
+    rng = np.random.default_rng(3000 + seed)
+    pairing = ["neox", "interleaved"][int(rng.integers(2))]
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2, 3, 5, 8, 16]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    L = int(rng.integers(1, 4))
+    bs = int(rng.choice([1, 4, 16, 33]))
+    theta = float(rng.choice([1e4, 5e5, 1e6]))
+    m = W.Model(f"attn-rand-{seed}", "gqa", L, Hkv, D, D, 0, pairing, theta, bs,
+                W.LLAMA3_SCALING if rng.random() < 0.3 else None)
+    lay = random_attend_layout(rng, bs)
+    ctx = pic.create_from_spec(pic.model_spec_from(m), lay["nb"])
+    plans, tables, sources = register_attend_layout(ctx, lay, m.name, bs)
+    g = torch.Generator().manual_seed(seed)
+    k_pool = torch.randn((L, lay["P"], Hkv, D), generator=g).to(torch.bfloat16)
+    v_pool = torch.randn((L, lay["P"], Hkv, D), generator=g).to(torch.bfloat16)
+    k_cache = torch.randn((L, lay["nb"], bs, Hkv, D), generator=g).to(torch.bfloat16)
+    v_cache = torch.randn((L, lay["nb"], bs, Hkv, D), generator=g).to(torch.bfloat16)
+    return dict(m=m, ctx=ctx, plans=plans, tables=tables, sources=sources, k_pool=k_pool, v_pool=v_pool,
+                k_cache=k_cache, v_cache=v_cache, bs=bs, L=L, Hq=Hkv * G, D=D, k=lay["k"], rng=rng)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_contexts_match_oracle(seed):
+    """Seeded random contexts (geometry, chunk lengths, block-resident chunks,
+    repeats, truncation, inline gaps, pseudo-sink widths, a random layer
+    window), both sources: fused against the oracle over exactly rotated
+    keys, the cache path against the oracle over the cache rows as stored;
+    every (layer, request, query head) within 2e-3."""
+    S = _random_setup(seed)
+    try:
+        rng, ctx, plans = S["rng"], S["ctx"], S["plans"]
+        L, Hq, D, n = S["L"], S["Hq"], S["D"], len(plans)
+        bias_value = -15.0 if rng.random() < 0.5 else 0.0
+        lb = int(rng.integers(0, L))
+        nl = int(rng.integers(1, L - lb + 1))
+        layers = list(range(lb, lb + nl))
+        q = torch.randn((nl, n, Hq, D), generator=torch.Generator().manual_seed(50 + seed)).to(torch.bfloat16)
+        qb = bits(q)
+        scale = 1.0 / math.sqrt(D)
+        dev = {k: S[k].to(DEV) for k in ("k_pool", "v_pool", "k_cache", "v_cache")}
+        ws = torch.empty(pic.pic_attend_workspace_bytes(ctx, plans, Hq, nl), dtype=torch.uint8, device=DEV)
+        bs = S["bs"]
+        for source in (pic.PIC_ATTEND_FUSED, pic.PIC_ATTEND_CACHE):
+            out = torch.full((nl, n, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+            lse = torch.full((nl, n, Hq), float("nan"), dtype=torch.float32, device=DEV)
+            pic.pic_attend_decode(ctx, plans, source, q.to(DEV), scale, dev["k_pool"], dev["v_pool"], dev["k_cache"],
+                                  dev["v_cache"], out, lse, ws, sink_bias=bias_value, layer_begin=lb)
+            assert pic.pic_query_device_status(ctx, ws) == 0
+            out, lse = out.cpu().double().numpy(), lse.cpu().double().numpy()
+            for r in range(n):
+                keys, vals, segs, T = _context_kv(S, r, layers)
+                if source == pic.PIC_ATTEND_CACHE:
+                    pos = np.arange(T)
+                    table = np.asarray(S["tables"][r])
+                    keys = oracle.bf16_bits_to_f64(bits(S["k_cache"][layers]))[:, table[pos // bs], pos % bs]
+                    vals = oracle.bf16_bits_to_f64(bits(S["v_cache"][layers]))[:, table[pos // bs], pos % bs]
+                bias = oracle.sink_bias(segs, T, S["k"], bias_value) if bias_value else None
+                for i in range(nl):
+                    o, s_ = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[i, r]), keys[i], vals[i], scale, bias)
+                    np.testing.assert_allclose(out[i, r], o, atol=2e-3, rtol=0, err_msg=f"source {source} r {r} l {i}")
+                    np.testing.assert_allclose(lse[i, r], s_, atol=2e-3, rtol=0, err_msg=f"source {source} r {r} l {i}")
     finally:
         pic.pic_destroy(S["ctx"])
 

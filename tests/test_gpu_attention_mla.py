@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_util import bits
+from gpu_util import bits, random_attend_layout, register_attend_layout
 from position_independent_kv_stitch_gb300 import pic
 
 pytestmark = pytest.mark.gpu
@@ -226,6 +226,71 @@ def test_mla_cache_path_over_materialized_stitch():
         # both against exactly rotated rows; the cache path's rows were rounded once
         _check_against_oracle(S, q, out_f, lse_f, scale, -15.0, 2e-3)
         _check_against_oracle(S, q, out_c, lse_c, scale, -15.0, 3e-2)
+    finally:
+        pic.pic_destroy(S["ctx"])
+
+
+def _random_setup(seed):
+    """A seeded random MLA context: either pairing, 1-3 layers, block size
+    1-33, rope theta 1e4 or 1e6, and the chunk and request mix of
+    random_attend_layout."""
+    rng = np.random.default_rng(5000 + seed)
+    pairing = ["neox", "interleaved"][int(rng.integers(2))]
+    L = int(rng.integers(1, 4))
+    bs = int(rng.choice([1, 4, 16, 33]))
+    m = W.Model(f"attn-mla-rand-{seed}", "mla", L, 1, ROW, ROPE, LATENT, pairing, float(rng.choice([1e4, 1e6])), bs)
+    lay = random_attend_layout(rng, bs)
+    ctx = pic.create_from_spec(pic.model_spec_from(m), lay["nb"])
+    _check_variant(ctx, os.environ["PIC_ATTEND_KERNEL"])
+    plans, tables, sources = register_attend_layout(ctx, lay, m.name, bs)
+    g = torch.Generator().manual_seed(seed)
+    pool = torch.randn((L, lay["P"], ROW), generator=g).to(torch.bfloat16)
+    cache = torch.randn((L, lay["nb"], bs, ROW), generator=g).to(torch.bfloat16)
+    return dict(m=m, ctx=ctx, plans=plans, tables=tables, sources=sources, pool=pool, cache=cache, bs=bs, L=L,
+                k=lay["k"], rng=rng)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_mla_contexts_match_oracle(seed):
+    """Seeded random contexts (block sizes, chunk lengths, block-resident
+    chunks, repeats, truncation, inline gaps, pseudo-sink widths, 16-128
+    heads, a random layer window) on both MLA kernels: fused against the
+    oracle over exactly rotated rows, the cache path against the oracle over
+    the cache rows as stored; every (layer, request, query head) within
+    2e-3."""
+    S = _random_setup(seed)
+    try:
+        rng, ctx, plans, bs = S["rng"], S["ctx"], S["plans"], S["bs"]
+        L, n = S["L"], len(plans)
+        H = int(rng.choice([16, 32, 64, 128]))
+        bias_value = -15.0 if rng.random() < 0.5 else 0.0
+        lb = int(rng.integers(0, L))
+        nl = int(rng.integers(1, L - lb + 1))
+        q = torch.randn((nl, n, H, ROW), generator=torch.Generator().manual_seed(60 + seed)).to(torch.bfloat16)
+        qb = bits(q)
+        scale = 1.0 / math.sqrt(192)
+        pool, cache = S["pool"].to(DEV), S["cache"].to(DEV)
+        ws = torch.empty(pic.pic_attend_workspace_bytes(ctx, plans, H, nl), dtype=torch.uint8, device=DEV)
+        cache_rows = oracle.bf16_bits_to_f64(bits(S["cache"]))
+        for source in (pic.PIC_ATTEND_FUSED, pic.PIC_ATTEND_CACHE):
+            out = torch.full((nl, n, H, LATENT), float("nan"), dtype=torch.float32, device=DEV)
+            lse = torch.full((nl, n, H), float("nan"), dtype=torch.float32, device=DEV)
+            pic.pic_attend_decode(ctx, plans, source, q.to(DEV), scale, pool, None, cache, None, out, lse, ws,
+                                  sink_bias=bias_value, layer_begin=lb)
+            assert pic.pic_query_device_status(ctx, ws) == 0
+            out, lse = out.cpu().double().numpy(), lse.cpu().double().numpy()
+            for r in range(n):
+                rows, segs, T = _context_rows(S, r)
+                if source == pic.PIC_ATTEND_CACHE:
+                    pos = np.arange(T)
+                    rows = cache_rows[:, np.asarray(S["tables"][r])[pos // bs], pos % bs]
+                bias = oracle.sink_bias(segs, T, S["k"], bias_value) if bias_value else None
+                for i in range(nl):
+                    x = rows[lb + i]
+                    o, sv = oracle.attention_decode(oracle.bf16_bits_to_f64(qb[i, r]), x[:, None, :],
+                                                    x[:, None, :LATENT], scale, bias)
+                    np.testing.assert_allclose(out[i, r], o, atol=2e-3, rtol=0, err_msg=f"source {source} r {r} l {i}")
+                    np.testing.assert_allclose(lse[i, r], sv, atol=2e-3, rtol=0, err_msg=f"source {source} r {r} l {i}")
     finally:
         pic.pic_destroy(S["ctx"])
 
