@@ -372,6 +372,47 @@ pic_status pic_stitch_noalloc(pic_ctx* ctx, const pic_plan* const* plans, int32_
                               int32_t* d_recompute_idx, int32_t* d_recompute_indptr,
                               int64_t recompute_capacity, uint32_t* d_status, pic_stream_t stream);
 
+/* ---------------------------------------------- pools in host memory */
+
+/*
+ * Pool rows a batch reads: *rows_read counts every (segment, token) that
+ * copies a row out of the pool, *distinct_rows the pool rows among them,
+ * each once (chunks placed more than once, or in several requests, read
+ * the same rows).  Block-resident and mapped chunks read no pool rows.  Per
+ * layer; multiply by num_layers and the row bytes (twice for GQA: K and V)
+ * for bytes.  Host only, no device work.  Either output may be NULL.
+ */
+pic_status pic_pool_read_rows(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                              int64_t* distinct_rows, int64_t* rows_read);
+
+/*
+ * pic_stage_pool -- copies the pool rows a batch reads, each once, from a
+ * pool in pinned host memory into a device pool of the same layout.  The
+ * pages keep chunk caches in GPU memory; this call serves a pool kept in
+ * host memory instead.  pic_stitch can read such a pool directly over the
+ * host link, but then a row placed n times crosses the link n times.  After
+ * this call, pic_stitch with dev_k_pool / dev_v_pool as its pool (on the
+ * same stream) reads every row from HBM.
+ *   host_k_pool, host_v_pool   pinned host memory (cudaHostAlloc or
+ *        cudaHostRegister), [num_layers] x host_pool_layer_stride_bytes of
+ *        [pool_tokens][row]; v is NULL for MLA.
+ *   dev_k_pool, dev_v_pool     device memory with the same token rows,
+ *        [num_layers] x dev_pool_layer_stride_bytes; only the rows the plans
+ *        read are written, the others are left as they are.
+ * Each maximal range of pool rows that the plans read takes one
+ * cudaMemcpy2DAsync per pool (all layers of the range), enqueued on
+ * `stream`.  *bytes_copied (may be NULL) receives the bytes enqueued.
+ * Layer strides must hold the highest row read (with more than one layer);
+ * pointers and strides must be multiples of 16 bytes.  Host pointers that are
+ * not pinned, or device pointers that are not device memory, are refused
+ * with PIC_ERR_INVALID_ARG before anything is enqueued; a copy the CUDA
+ * runtime refuses returns PIC_ERR_CUDA with the earlier copies enqueued.
+ */
+pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                          const void* host_k_pool, const void* host_v_pool,
+                          int64_t host_pool_layer_stride_bytes, void* dev_k_pool, void* dev_v_pool,
+                          int64_t dev_pool_layer_stride_bytes, int64_t* bytes_copied, pic_stream_t stream);
+
 /* ------------------------------------------------------- in-place shift */
 
 size_t pic_rerotate_workspace_bytes(const pic_ctx* ctx, const pic_shift_seg* segs,

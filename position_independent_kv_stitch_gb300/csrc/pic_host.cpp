@@ -1528,6 +1528,110 @@ pic_status pic_stitch(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
   return ok(ctx);
 }
 
+// ---------------------------------------------------- pools in host memory
+
+namespace {
+
+// The pool rows [begin, end) the plans' pool segments read, sorted and
+// merged (overlapping or adjacent ranges become one); *rows_read counts
+// every row read, repeats included.
+std::vector<std::pair<int64_t, int64_t>> pool_read_ranges(const pic_plan* const* plans, int32_t n_req,
+                                                          int64_t* rows_read) {
+  std::vector<std::pair<int64_t, int64_t>> v;
+  int64_t read = 0;
+  for (int32_t r = 0; r < n_req; ++r)
+    for (const Segment& sg : plans[r]->segs)
+      if (sg.kind == pic::kRunPool && sg.num_tokens > 0) {
+        v.emplace_back(sg.src_tok, sg.src_tok + sg.num_tokens);
+        read += sg.num_tokens;
+      }
+  std::sort(v.begin(), v.end());
+  std::vector<std::pair<int64_t, int64_t>> merged;
+  for (const auto& x : v) {
+    if (!merged.empty() && x.first <= merged.back().second)
+      merged.back().second = std::max(merged.back().second, x.second);
+    else
+      merged.push_back(x);
+  }
+  if (rows_read) *rows_read = read;
+  return merged;
+}
+
+pic_status check_plan_list(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req) {
+  if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
+  for (int32_t r = 0; r < n_req; ++r)
+    if (!plan_valid(ctx, plans[r])) return fail(ctx, PIC_ERR_INVALID_ARG, "plans[%d] does not belong to this context", r);
+  return PIC_OK;
+}
+
+}  // namespace
+
+pic_status pic_pool_read_rows(const pic_ctx* cctx, const pic_plan* const* plans, int32_t n_req,
+                              int64_t* distinct_rows, int64_t* rows_read) {
+  pic_ctx* ctx = const_cast<pic_ctx*>(cctx);
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  const pic_status st = check_plan_list(ctx, plans, n_req);
+  if (st != PIC_OK) return st;
+  int64_t read = 0, distinct = 0;
+  for (const auto& x : pool_read_ranges(plans, n_req, &read)) distinct += x.second - x.first;
+  if (distinct_rows) *distinct_rows = distinct;
+  if (rows_read) *rows_read = read;
+  return ok(ctx);
+}
+
+pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                          const void* host_k_pool, const void* host_v_pool, int64_t host_ls,
+                          void* dev_k_pool, void* dev_v_pool, int64_t dev_ls, int64_t* bytes_copied,
+                          pic_stream_t stream) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  pic_status st = check_plan_list(ctx, plans, n_req);
+  if (st != PIC_OK) return st;
+  const pic_model_desc& m = ctx->model;
+  const bool gqa = m.kind == PIC_KIND_GQA;
+  if (!host_k_pool || !dev_k_pool) return fail(ctx, PIC_ERR_INVALID_ARG, "null pool");
+  if (gqa && (!host_v_pool || !dev_v_pool)) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs both value pools");
+  if (!gqa && (host_v_pool || dev_v_pool)) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
+  if (!vectorized_bytes_ok(host_k_pool) || !vectorized_bytes_ok(dev_k_pool) ||
+      (gqa && (!vectorized_bytes_ok(host_v_pool) || !vectorized_bytes_ok(dev_v_pool))) || (host_ls & 15) ||
+      (dev_ls & 15))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "pools and layer strides must be 16-byte aligned");
+  int64_t read = 0;
+  const auto ranges = pool_read_ranges(plans, n_req, &read);
+  const int64_t row = row_bytes_of(m);
+  const int64_t top = ranges.empty() ? 0 : ranges.back().second;
+  const int32_t L = m.num_layers;
+  if (L > 1 && (host_ls < top * row || dev_ls < top * row))
+    return fail(ctx, PIC_ERR_RANGE, "a layer stride is smaller than the %lld pool rows the plans reach",
+                static_cast<long long>(top));
+  DeviceInfo di;
+  st = current_device(ctx, di);
+  if (st != PIC_OK) return st;
+  const void* host[2] = {host_k_pool, host_v_pool};
+  void* dev[2] = {dev_k_pool, dev_v_pool};
+  const int tensors = gqa ? 2 : 1;
+  for (int k = 0; k < tensors; ++k) {
+    if (residency(host[k]) != 1)
+      return fail(ctx, PIC_ERR_INVALID_ARG, "host pools must be pinned host memory (cudaHostAlloc / cudaHostRegister)");
+    if (residency(dev[k]) != 0) return fail(ctx, PIC_ERR_INVALID_ARG, "device pools must be device memory");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int64_t bytes = 0;
+  for (const auto& x : ranges) {
+    const size_t width = static_cast<size_t>((x.second - x.first) * row);
+    // one layer: the pitches only need to hold the range
+    const size_t spitch = L > 1 ? static_cast<size_t>(host_ls) : width, dpitch = L > 1 ? static_cast<size_t>(dev_ls) : width;
+    for (int k = 0; k < tensors; ++k) {
+      const cudaError_t e = cudaMemcpy2DAsync(static_cast<uint8_t*>(dev[k]) + x.first * row, dpitch,
+                                              static_cast<const uint8_t*>(host[k]) + x.first * row, spitch, width,
+                                              static_cast<size_t>(L), cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "pool staging copy");
+      bytes += static_cast<int64_t>(width) * L;
+    }
+  }
+  if (bytes_copied) *bytes_copied = bytes;
+  return ok(ctx);
+}
+
 // ------------------------------------------------------------ in-place shift
 
 size_t pic_rerotate_workspace_bytes(const pic_ctx* ctx, const pic_shift_seg* segs, int32_t n) {

@@ -296,6 +296,85 @@ def test_stitch_argument_checks_need_no_gpu():
         pic.pic_destroy(ctx)
 
 
+def test_pool_read_rows_count_repeats_once():
+    """pic_pool_read_rows against the plans' own segments: every pool row a
+    segment reads counts once in the distinct total however many segments
+    read it; block-resident chunks read no pool rows."""
+    ctx = _gqa_ctx(nb=64)
+    try:
+        lens = [20, 7, 33, 16]
+        offs = [0, 20, 27, 60]
+        ids = [pic.pic_register_chunk(ctx, W.chunk_key("rows", c), offs[c], lens[c])[0] for c in range(4)]
+        bid = pic.pic_register_chunk_blocks(ctx, W.chunk_key("rows", 9), [60, 61], 20)[0]
+        plans = [pic.pic_build_block_table(ctx, [ids[0], ids[2], ids[0], bid], 8)[0],
+                 pic.pic_build_block_table(ctx, [ids[2], ids[3]], 8, take_tokens=[10, 16])[0],
+                 pic.pic_build_block_table(ctx, [bid], 4)[0]]
+        rows, read = set(), 0
+        for plan in plans:
+            for j in range(pic.pic_plan_info(plan)["num_segments"]):
+                sg = pic.pic_plan_segment(plan, j)
+                if sg["src_tok"] >= 0:
+                    rows |= set(range(sg["src_tok"], sg["src_tok"] + sg["num_tokens"]))
+                    read += sg["num_tokens"]
+        assert (len(rows), read) == (20 + 33 + 16, 20 + 33 + 20 + 10 + 16)
+        assert pic.pic_pool_read_rows(ctx, plans) == (len(rows), read)
+        assert pic.pic_pool_read_rows(ctx, plans[2:]) == (0, 0)
+        assert pic.pic_pool_read_rows(ctx, []) == (0, 0)
+        ctx2 = _gqa_ctx(nb=8)
+        with pytest.raises(PicError) as e:
+            pic.pic_pool_read_rows(ctx2, plans[:1])
+        assert e.value.status_name == "PIC_ERR_INVALID_ARG"
+        pic.pic_destroy(ctx2)
+    finally:
+        pic.pic_destroy(ctx)
+
+
+def test_stage_pool_argument_checks_need_no_gpu():
+    """pic_stage_pool refuses bad arguments before any CUDA call (fake,
+    aligned pointers that never reach a copy)."""
+    ctx = _gqa_ctx(nb=8)
+    L = pic.load()
+    try:
+        pic.pic_register_chunk(ctx, W.chunk_key("st", 0), 100, 20)
+        plan, _ = pic.pic_build_block_table(ctx, [0], 4)
+        arr = pic._plan_array([plan])
+        good, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+        ls = 120 * 512  # rows 100-119 of 512 bytes (2 heads x 128 dims x bf16) fit
+        n = ctypes.c_int64(-1)
+        # GQA without value pools
+        st = L.pic_stage_pool(ctx, arr, 1, good, None, ls, good, None, ls, ctypes.byref(n), None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
+        # misaligned device pool, then a misaligned stride
+        st = L.pic_stage_pool(ctx, arr, 1, good, good, ls, good, odd, ls, ctypes.byref(n), None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_ALIGNMENT"
+        st = L.pic_stage_pool(ctx, arr, 1, good, good, ls + 8, good, good, ls, ctypes.byref(n), None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_ALIGNMENT"
+        # a layer stride that does not reach row 119 (two layers)
+        st = L.pic_stage_pool(ctx, arr, 1, good, good, ls, good, good, ls - 512, ctypes.byref(n), None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_RANGE"
+        # null context, a bad plan list
+        st = L.pic_stage_pool(None, arr, 1, good, good, ls, good, good, ls, ctypes.byref(n), None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
+        st = L.pic_stage_pool(ctx, None, 1, good, good, ls, good, good, ls, ctypes.byref(n), None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
+        assert n.value == -1
+    finally:
+        pic.pic_destroy(ctx)
+    mla = pic.pic_create(kind=pic.PIC_KIND_MLA, num_layers=1, num_kv_heads=1, head_dim=576, rope_dim=64,
+                         rope_offset=512, pairing=pic.PIC_PAIRING_INTERLEAVED, block_size=16, rope_theta=1e4,
+                         num_cache_blocks=8)
+    try:
+        pic.pic_register_chunk(mla, W.chunk_key("st", 1), 0, 20)
+        plan, _ = pic.pic_build_block_table(mla, [0], 4)
+        arr = pic._plan_array([plan])
+        good = ctypes.c_void_p(0x10000)
+        # MLA rows have no value pools
+        st = L.pic_stage_pool(mla, arr, 1, good, good, 0, good, None, 0, None, None)
+        assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
+    finally:
+        pic.pic_destroy(mla)
+
+
 def test_attend_argument_checks_need_no_gpu():
     """pic_attend_decode refuses bad arguments before any CUDA call (fake,
     aligned pointers that never reach a launch)."""

@@ -62,6 +62,87 @@ def test_host_pool_and_cache_match_device_path_and_oracle(name):
         dev.close()
 
 
+@pytest.mark.parametrize("kind", ["gqa", "mla"])
+def test_staged_pool_copies_each_row_read_once_and_stitches_the_same(kind):
+    """pic_stage_pool from a pinned host pool into a zeroed device pool: the
+    rows the plans read arrive bit for bit, every other row stays zero, and
+    the stitch from the staged pool equals the stitch from the full device
+    pool bit for bit (the same kernel on the same rows), which the oracle
+    checks.  Chunks 1 and 4 are never read; chunk 2 is read three times, in
+    two requests; chunk 3 in part."""
+    lens = [40, 17, 100, 33, 9, 64]
+    reqs = [[(2, 100), (0, 40), (3, 20), (2, 100)], [(5, 64), (2, 50), (0, 40)]]
+    if kind == "gqa":
+        m = W.Model("stage-gqa", "gqa", 3, 2, 128, 128, 0, "neox", 5e5, 16)
+    else:
+        m = W.Model("stage-mla", "mla", 2, 1, 576, 64, 512, "interleaved", 1e4, 16)
+    wl = W.Workload(f"stage-{kind}", m, lens, reqs, 4, 0)
+    ref = Stitched(wl, pool_device="cpu").run()
+    try:
+        hk = ref.k_pool.cpu().pin_memory()
+        hv = ref.v_pool.cpu().pin_memory() if ref.v_pool is not None else None
+        dk = torch.zeros_like(ref.k_pool)
+        dv = torch.zeros_like(ref.v_pool) if ref.v_pool is not None else None
+        distinct, read = pic.pic_pool_read_rows(ref.ctx, ref.plans)
+        assert (distinct, read) == (40 + 100 + 20 + 64, 100 + 40 + 20 + 100 + 64 + 50 + 40)
+        n = pic.pic_stage_pool(ref.ctx, ref.plans, hk, hv, dk, dv)
+        row = hk[0, 0].numel() * 2
+        assert n == distinct * m.num_layers * row * (2 if hv is not None else 1)
+        torch.cuda.synchronize()
+        offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
+        read_rows = np.zeros(sum(lens), dtype=bool)
+        for c, take in {(c, t) for req in reqs for c, t in req}:
+            read_rows[offs[c]:offs[c] + take] = True
+        for host, staged in ((hk, dk), (hv, dv)):
+            if host is None:
+                continue
+            hb, sb = bits(host), bits(staged)
+            assert np.array_equal(sb[:, read_rows], hb[:, read_rows])
+            assert not sb[:, ~read_rows].any()
+        k_cache = torch.empty_like(ref.k_cache)
+        k_cache.view(torch.int16).fill_(-1)
+        v_cache = None
+        if ref.v_cache is not None:
+            v_cache = torch.empty_like(ref.v_cache)
+            v_cache.view(torch.int16).fill_(-1)
+        ridx, indptr = torch.empty_like(ref.ridx), torch.empty_like(ref.indptr)
+        pic.pic_stitch(ref.ctx, ref.plans, dk, dv, k_cache, v_cache, ref.d_bt, ridx, indptr, torch.empty_like(ref.ws))
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(k_cache), bits(ref.k_cache))
+        if v_cache is not None:
+            assert np.array_equal(bits(v_cache), bits(ref.v_cache))
+        assert torch.equal(ridx, ref.ridx) and torch.equal(indptr, ref.indptr)
+        segs, tables, _ = oracle_side(wl, ref.nb)
+        want_k, _ = oracle.stitch_paged(bits(hk), None, segs, tables, ref.nb, ref.bs, theta_of(m), pairing_of(m),
+                                        m.rope_offset, m.rope_dim)
+        assert_k_close(f64(k_cache), want_k, "K from the staged pool")
+    finally:
+        ref.close()
+
+
+def test_stage_pool_refuses_pageable_and_swapped_pointers():
+    lens = [40, 17]
+    m = W.Model("stage-bad", "gqa", 2, 2, 128, 128, 0, "neox", 1e4, 16)
+    wl = W.Workload("stage-bad", m, lens, [[(0, 40), (1, 17)]], 4, 0)
+    ref = Stitched(wl, pool_device="cpu")
+    try:
+        hk = ref.k_pool.cpu().pin_memory()
+        hv = ref.v_pool.cpu().pin_memory()
+        L = pic.load()
+        arr = pic._plan_array(ref.plans)
+        ls = hk.stride(0) * 2
+        pageable = ref.k_pool.cpu()
+        for args in ((pageable, hv, ref.k_pool, ref.v_pool),     # pageable host pool
+                     (ref.k_pool, ref.v_pool, ref.k_pool, ref.v_pool),  # device memory as the host pool
+                     (hk, hv, hk, hv)):                          # host memory as the device pool
+            st = L.pic_stage_pool(ref.ctx, arr, len(ref.plans), ctypes.c_void_p(args[0].data_ptr()),
+                                  ctypes.c_void_p(args[1].data_ptr()), ls, ctypes.c_void_p(args[2].data_ptr()),
+                                  ctypes.c_void_p(args[3].data_ptr()), ls, None, None)
+            assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG", args
+    finally:
+        ref.close()
+
+
 def test_host_cache_in_place_shift():
     m = W.Model("ip-host", "gqa", 2, 2, 128, 128, 0, "neox", 1e4, 16)
     ctx = pic.create_from_spec(pic.model_spec_from(m), 8)
