@@ -378,11 +378,14 @@ pic_status pic_stitch_noalloc(pic_ctx* ctx, const pic_plan* const* plans, int32_
  * Pool rows a batch reads: *rows_read counts every (segment, token) that
  * copies a row out of the pool, *distinct_rows the pool rows among them,
  * each once (chunks placed more than once, or in several requests, read
- * the same rows).  Block-resident and mapped chunks read no pool rows.  Per
- * layer; multiply by num_layers and the row bytes (twice for GQA: K and V)
- * for bytes.  Host only, no device work.  Either output may be NULL.
+ * the same rows), leaving out rows that staged_plans read (may be NULL and
+ * 0; the rows pic_stage_pool would copy with the same lists).
+ * Block-resident and mapped chunks read no pool rows.  Per layer; multiply
+ * by num_layers and the row bytes (twice for GQA: K and V) for bytes.  Host
+ * only, no device work.  Either output may be NULL.
  */
 pic_status pic_pool_read_rows(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                              const pic_plan* const* staged_plans, int32_t n_staged,
                               int64_t* distinct_rows, int64_t* rows_read);
 
 /*
@@ -393,22 +396,30 @@ pic_status pic_pool_read_rows(const pic_ctx* ctx, const pic_plan* const* plans, 
  * host link, but then a row placed n times crosses the link n times.  After
  * this call, pic_stitch with dev_k_pool / dev_v_pool as its pool (on the
  * same stream) reads every row from HBM.
+ *   staged_plans, n_staged     plans whose rows an earlier call already
+ *        staged into the same device pools (may be NULL and 0): their rows are
+ *        skipped.  A caller can so split a batch into groups of requests and
+ *        stage group g + 1 on a copy stream while group g is stitched.
  *   host_k_pool, host_v_pool   pinned host memory (cudaHostAlloc or
  *        cudaHostRegister), [num_layers] x host_pool_layer_stride_bytes of
  *        [pool_tokens][row]; v is NULL for MLA.
  *   dev_k_pool, dev_v_pool     device memory with the same token rows,
  *        [num_layers] x dev_pool_layer_stride_bytes; only the rows the plans
  *        read are written, the others are left as they are.
- * Each maximal range of pool rows that the plans read takes one
- * cudaMemcpy2DAsync per pool (all layers of the range), enqueued on
- * `stream`.  *bytes_copied (may be NULL) receives the bytes enqueued.
+ * The rows are copied by a kernel on `stream` (SM loads over the host link,
+ * one CTA per SM), not by a copy engine: a copy engine serves its queue in
+ * order, so gigabytes of pool copies queued on it would hold back every
+ * small upload behind them, such as a stitch's workspace image on another
+ * stream.  *bytes_copied (may be NULL) receives the bytes the launch copies.
  * Layer strides must hold the highest row read (with more than one layer);
  * pointers and strides must be multiples of 16 bytes.  Host pointers that are
  * not pinned, or device pointers that are not device memory, are refused
- * with PIC_ERR_INVALID_ARG before anything is enqueued; a copy the CUDA
- * runtime refuses returns PIC_ERR_CUDA with the earlier copies enqueued.
+ * with PIC_ERR_INVALID_ARG before anything is enqueued.  A batch of more than
+ * 1,024 row ranges takes one launch per 1,024; a launch the CUDA runtime
+ * refuses returns PIC_ERR_CUDA with the earlier launches enqueued.
  */
 pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                          const pic_plan* const* staged_plans, int32_t n_staged,
                           const void* host_k_pool, const void* host_v_pool,
                           int64_t host_pool_layer_stride_bytes, void* dev_k_pool, void* dev_v_pool,
                           int64_t dev_pool_layer_stride_bytes, int64_t* bytes_copied, pic_stream_t stream);

@@ -24,7 +24,7 @@ LIB_NAME = "libpic.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
 SOURCES = ["pic_host.cpp", "pic_kernels.cu", "pic_kernels_tma.cu", "pic_attention.cu", "pic_attention_tc.cu",
-           "pic_noalloc.cu", "pic_cdc.cu"]
+           "pic_noalloc.cu", "pic_cdc.cu", "pic_stage.cu"]
 HEADERS = [os.path.join(CSRC, "pic_internal.h"), os.path.join(INCLUDE, "pic.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1557,6 +1557,23 @@ std::vector<std::pair<int64_t, int64_t>> pool_read_ranges(const pic_plan* const*
   return merged;
 }
 
+// The rows of `a` outside `b` (both sorted and merged), sorted and merged.
+std::vector<std::pair<int64_t, int64_t>> minus_ranges(const std::vector<std::pair<int64_t, int64_t>>& a,
+                                                      const std::vector<std::pair<int64_t, int64_t>>& b) {
+  std::vector<std::pair<int64_t, int64_t>> out;
+  size_t j = 0;
+  for (const auto& x : a) {
+    int64_t lo = x.first;
+    while (j < b.size() && b[j].second <= lo) ++j;
+    for (size_t k = j; k < b.size() && b[k].first < x.second; ++k) {
+      if (b[k].first > lo) out.emplace_back(lo, b[k].first);
+      lo = std::max(lo, b[k].second);
+    }
+    if (lo < x.second) out.emplace_back(lo, x.second);
+  }
+  return out;
+}
+
 pic_status check_plan_list(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req) {
   if (n_req < 0 || (n_req > 0 && !plans)) return fail(ctx, PIC_ERR_INVALID_ARG, "bad plan list");
   for (int32_t r = 0; r < n_req; ++r)
@@ -1567,24 +1584,31 @@ pic_status check_plan_list(pic_ctx* ctx, const pic_plan* const* plans, int32_t n
 }  // namespace
 
 pic_status pic_pool_read_rows(const pic_ctx* cctx, const pic_plan* const* plans, int32_t n_req,
-                              int64_t* distinct_rows, int64_t* rows_read) {
+                              const pic_plan* const* staged_plans, int32_t n_staged, int64_t* distinct_rows,
+                              int64_t* rows_read) {
   pic_ctx* ctx = const_cast<pic_ctx*>(cctx);
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
-  const pic_status st = check_plan_list(ctx, plans, n_req);
+  pic_status st = check_plan_list(ctx, plans, n_req);
+  if (st != PIC_OK) return st;
+  st = check_plan_list(ctx, staged_plans, n_staged);
   if (st != PIC_OK) return st;
   int64_t read = 0, distinct = 0;
-  for (const auto& x : pool_read_ranges(plans, n_req, &read)) distinct += x.second - x.first;
+  for (const auto& x : minus_ranges(pool_read_ranges(plans, n_req, &read), pool_read_ranges(staged_plans, n_staged, nullptr)))
+    distinct += x.second - x.first;
   if (distinct_rows) *distinct_rows = distinct;
   if (rows_read) *rows_read = read;
   return ok(ctx);
 }
 
 pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                          const pic_plan* const* staged_plans, int32_t n_staged,
                           const void* host_k_pool, const void* host_v_pool, int64_t host_ls,
                           void* dev_k_pool, void* dev_v_pool, int64_t dev_ls, int64_t* bytes_copied,
                           pic_stream_t stream) {
   if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
   pic_status st = check_plan_list(ctx, plans, n_req);
+  if (st != PIC_OK) return st;
+  st = check_plan_list(ctx, staged_plans, n_staged);
   if (st != PIC_OK) return st;
   const pic_model_desc& m = ctx->model;
   const bool gqa = m.kind == PIC_KIND_GQA;
@@ -1596,7 +1620,7 @@ pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_
       (dev_ls & 15))
     return fail(ctx, PIC_ERR_ALIGNMENT, "pools and layer strides must be 16-byte aligned");
   int64_t read = 0;
-  const auto ranges = pool_read_ranges(plans, n_req, &read);
+  const auto ranges = minus_ranges(pool_read_ranges(plans, n_req, &read), pool_read_ranges(staged_plans, n_staged, nullptr));
   const int64_t row = row_bytes_of(m);
   const int64_t top = ranges.empty() ? 0 : ranges.back().second;
   const int32_t L = m.num_layers;
@@ -1615,18 +1639,28 @@ pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_
     if (residency(dev[k]) != 0) return fail(ctx, PIC_ERR_INVALID_ARG, "device pools must be device memory");
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the copy kernel's parameters carry up to kStageMaxSpans ranges per launch
+  auto prm = std::make_unique<pic::StageParams>();
+  for (int k = 0; k < 2; ++k) {
+    prm->src[k] = static_cast<const uint8_t*>(host[k]);
+    prm->dst[k] = static_cast<uint8_t*>(dev[k]);
+  }
+  prm->src_ls = host_ls;
+  prm->dst_ls = dev_ls;
+  prm->layers = L;
+  prm->tensors = tensors;
   int64_t bytes = 0;
-  for (const auto& x : ranges) {
-    const size_t width = static_cast<size_t>((x.second - x.first) * row);
-    // one layer: the pitches only need to hold the range
-    const size_t spitch = L > 1 ? static_cast<size_t>(host_ls) : width, dpitch = L > 1 ? static_cast<size_t>(dev_ls) : width;
-    for (int k = 0; k < tensors; ++k) {
-      const cudaError_t e = cudaMemcpy2DAsync(static_cast<uint8_t*>(dev[k]) + x.first * row, dpitch,
-                                              static_cast<const uint8_t*>(host[k]) + x.first * row, spitch, width,
-                                              static_cast<size_t>(L), cudaMemcpyHostToDevice, s);
-      if (e != cudaSuccess) return cuda_fail(ctx, e, "pool staging copy");
-      bytes += static_cast<int64_t>(width) * L;
+  for (size_t r0 = 0; r0 < ranges.size(); r0 += pic::kStageMaxSpans) {
+    const size_t n = std::min<size_t>(pic::kStageMaxSpans, ranges.size() - r0);
+    for (size_t i = 0; i < n; ++i) {
+      prm->spans[i].off = ranges[r0 + i].first * row;
+      prm->spans[i].bytes = (ranges[r0 + i].second - ranges[r0 + i].first) * row;
+      bytes += prm->spans[i].bytes * L * tensors;
     }
+    prm->n_spans = static_cast<int32_t>(n);
+    const int64_t items = static_cast<int64_t>(n) * L * tensors;
+    const cudaError_t e = pic::launch_stage_rows(*prm, static_cast<int>(std::min<int64_t>(items, di.sm_count)), s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "pool staging launch");
   }
   if (bytes_copied) *bytes_copied = bytes;
   return ok(ctx);

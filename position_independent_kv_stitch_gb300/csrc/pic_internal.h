@@ -276,6 +276,22 @@ pic_status stitch_with_scratch(pic_ctx* ctx, const pic_plan* const* plans, int32
 // Records an error message on ctx (or the calling thread) and returns st.
 pic_status set_error(pic_ctx* ctx, pic_status st, const char* msg);
 
+// Pool staging (pic_stage_pool): spans of pool rows of one layer (byte
+// offset and length, multiples of 16), copied for every layer and tensor.
+struct StageSpan {
+  int64_t off;
+  int64_t bytes;
+};
+constexpr int kStageMaxSpans = 1024;  // per launch: the parameters stay below 32 KB
+struct StageParams {
+  const uint8_t* src[2];  // host pools (K, V)
+  uint8_t* dst[2];        // device pools (K, V)
+  int64_t src_ls, dst_ls;
+  int32_t n_spans, layers, tensors;
+  StageSpan spans[kStageMaxSpans];
+};
+cudaError_t launch_stage_rows(const StageParams& p, int grid, cudaStream_t stream);
+
 // Resident CTAs per SM of the kernel the matching launcher would use.
 int occupancy_stitch_gqa(int pairing, int head_dim);
 int occupancy_stitch_mla(int pairing);

@@ -99,9 +99,9 @@ _SIGNATURES = {
     "pic_stitch_noalloc": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _c_void_p, _c_void_p, _i64,
                                           _c_void_p, _c_void_p, _i64, _c_void_p, _i32, _c_void_p,
                                           _c_void_p, _i64, _c_void_p, _c_void_p]),
-    "pic_pool_read_rows": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _P(_i64), _P(_i64)]),
-    "pic_stage_pool": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _c_void_p, _c_void_p, _i64, _c_void_p,
-                                      _c_void_p, _i64, _P(_i64), _c_void_p]),
+    "pic_pool_read_rows": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _P(_c_void_p), _i32, _P(_i64), _P(_i64)]),
+    "pic_stage_pool": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _P(_c_void_p), _i32, _c_void_p, _c_void_p,
+                                      _i64, _c_void_p, _c_void_p, _i64, _P(_i64), _c_void_p]),
     "pic_rerotate_workspace_bytes": (_sz, [_c_void_p, _P(pic_shift_seg), _i32]),
     "pic_rerotate_inplace": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _i32, _i32,
                                             _P(pic_shift_seg), _i32, _c_void_p, _sz, _c_void_p]),
@@ -360,17 +360,23 @@ def pic_stitch(ctx, plans, k_pool, v_pool, k_cache, v_cache, block_tables, recom
     _check(st, ctx)
 
 
-def pic_pool_read_rows(ctx, plans):
-    """(distinct pool rows, pool rows read) of a batch, per layer."""
+def pic_pool_read_rows(ctx, plans, staged_plans=()):
+    """(distinct pool rows outside those staged_plans read, pool rows read)
+    of a batch, per layer."""
     d, r = ctypes.c_int64(), ctypes.c_int64()
-    _check(load().pic_pool_read_rows(ctx, _plan_array(plans), len(plans), ctypes.byref(d), ctypes.byref(r)), ctx)
+    staged_plans = list(staged_plans)
+    _check(load().pic_pool_read_rows(ctx, _plan_array(plans), len(plans),
+                                     _plan_array(staged_plans) if staged_plans else None, len(staged_plans),
+                                     ctypes.byref(d), ctypes.byref(r)), ctx)
     return d.value, r.value
 
 
-def pic_stage_pool(ctx, plans, host_k_pool, host_v_pool, dev_k_pool, dev_v_pool, stream=None) -> int:
+def pic_stage_pool(ctx, plans, host_k_pool, host_v_pool, dev_k_pool, dev_v_pool, staged_plans=(),
+                   stream=None) -> int:
     """Enqueues the copies of the pool rows the plans read, each once, from
     pinned host pools [L][tokens][...] into device pools of the same shape
-    (v None for MLA).  Returns the bytes enqueued."""
+    (v None for MLA), skipping the rows staged_plans read (staged by an
+    earlier call).  Returns the bytes enqueued."""
     for name, t in (("host_k_pool", host_k_pool), ("host_v_pool", host_v_pool), ("dev_k_pool", dev_k_pool),
                     ("dev_v_pool", dev_v_pool)):
         _check_kv_buffer(t, name)
@@ -380,7 +386,9 @@ def pic_stage_pool(ctx, plans, host_k_pool, host_v_pool, dev_k_pool, dev_v_pool,
     if dev_v_pool is not None and _layer_stride_bytes(dev_v_pool) != dls:
         raise ValueError("dev_k_pool and dev_v_pool must share a layer stride")
     n = ctypes.c_int64()
-    st = load().pic_stage_pool(ctx, _plan_array(plans), len(plans), _ptr(host_k_pool), _ptr(host_v_pool), hls,
+    staged_plans = list(staged_plans)
+    st = load().pic_stage_pool(ctx, _plan_array(plans), len(plans), _plan_array(staged_plans) if staged_plans else None,
+                               len(staged_plans), _ptr(host_k_pool), _ptr(host_v_pool), hls,
                                _ptr(dev_k_pool), _ptr(dev_v_pool), dls, ctypes.byref(n), _stream_handle(stream))
     _check(st, ctx)
     return n.value

@@ -320,6 +320,14 @@ def test_pool_read_rows_count_repeats_once():
         assert pic.pic_pool_read_rows(ctx, plans) == (len(rows), read)
         assert pic.pic_pool_read_rows(ctx, plans[2:]) == (0, 0)
         assert pic.pic_pool_read_rows(ctx, []) == (0, 0)
+        # rows an earlier group staged are left out: plan 1 reads rows 27-36
+        # (of chunk 2, which plan 0 reads whole) and 60-75
+        assert pic.pic_pool_read_rows(ctx, plans[1:2], staged_plans=plans[:1]) == (16, 26)
+        assert pic.pic_pool_read_rows(ctx, plans[:1], staged_plans=plans[1:2]) == (20 + 33 - 10, 73)
+        assert pic.pic_pool_read_rows(ctx, plans, staged_plans=plans) == (0, read)
+        # the groups' distinct rows add up to the batch's
+        assert (pic.pic_pool_read_rows(ctx, plans[:1])[0] + pic.pic_pool_read_rows(ctx, plans[1:], plans[:1])[0]
+                == len(rows))
         ctx2 = _gqa_ctx(nb=8)
         with pytest.raises(PicError) as e:
             pic.pic_pool_read_rows(ctx2, plans[:1])
@@ -342,20 +350,20 @@ def test_stage_pool_argument_checks_need_no_gpu():
         ls = 120 * 512  # rows 100-119 of 512 bytes (2 heads x 128 dims x bf16) fit
         n = ctypes.c_int64(-1)
         # GQA without value pools
-        st = L.pic_stage_pool(ctx, arr, 1, good, None, ls, good, None, ls, ctypes.byref(n), None)
+        st = L.pic_stage_pool(ctx, arr, 1, None, 0, good, None, ls, good, None, ls, ctypes.byref(n), None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
         # misaligned device pool, then a misaligned stride
-        st = L.pic_stage_pool(ctx, arr, 1, good, good, ls, good, odd, ls, ctypes.byref(n), None)
+        st = L.pic_stage_pool(ctx, arr, 1, None, 0, good, good, ls, good, odd, ls, ctypes.byref(n), None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_ALIGNMENT"
-        st = L.pic_stage_pool(ctx, arr, 1, good, good, ls + 8, good, good, ls, ctypes.byref(n), None)
+        st = L.pic_stage_pool(ctx, arr, 1, None, 0, good, good, ls + 8, good, good, ls, ctypes.byref(n), None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_ALIGNMENT"
         # a layer stride that does not reach row 119 (two layers)
-        st = L.pic_stage_pool(ctx, arr, 1, good, good, ls, good, good, ls - 512, ctypes.byref(n), None)
+        st = L.pic_stage_pool(ctx, arr, 1, None, 0, good, good, ls, good, good, ls - 512, ctypes.byref(n), None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_RANGE"
         # null context, a bad plan list
-        st = L.pic_stage_pool(None, arr, 1, good, good, ls, good, good, ls, ctypes.byref(n), None)
+        st = L.pic_stage_pool(None, arr, 1, None, 0, good, good, ls, good, good, ls, ctypes.byref(n), None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
-        st = L.pic_stage_pool(ctx, None, 1, good, good, ls, good, good, ls, ctypes.byref(n), None)
+        st = L.pic_stage_pool(ctx, None, 1, None, 0, good, good, ls, good, good, ls, ctypes.byref(n), None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
         assert n.value == -1
     finally:
@@ -369,7 +377,7 @@ def test_stage_pool_argument_checks_need_no_gpu():
         arr = pic._plan_array([plan])
         good = ctypes.c_void_p(0x10000)
         # MLA rows have no value pools
-        st = L.pic_stage_pool(mla, arr, 1, good, good, 0, good, None, 0, None, None)
+        st = L.pic_stage_pool(mla, arr, 1, None, 0, good, good, 0, good, None, 0, None, None)
         assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG"
     finally:
         pic.pic_destroy(mla)

@@ -69,7 +69,8 @@ def test_staged_pool_copies_each_row_read_once_and_stitches_the_same(kind):
     the stitch from the staged pool equals the stitch from the full device
     pool bit for bit (the same kernel on the same rows), which the oracle
     checks.  Chunks 1 and 4 are never read; chunk 2 is read three times, in
-    two requests; chunk 3 in part."""
+    two requests; chunk 3 in part.  The rows are staged in two calls, the
+    second skipping the rows of the first request."""
     lens = [40, 17, 100, 33, 9, 64]
     reqs = [[(2, 100), (0, 40), (3, 20), (2, 100)], [(5, 64), (2, 50), (0, 40)]]
     if kind == "gqa":
@@ -85,7 +86,10 @@ def test_staged_pool_copies_each_row_read_once_and_stitches_the_same(kind):
         dv = torch.zeros_like(ref.v_pool) if ref.v_pool is not None else None
         distinct, read = pic.pic_pool_read_rows(ref.ctx, ref.plans)
         assert (distinct, read) == (40 + 100 + 20 + 64, 100 + 40 + 20 + 100 + 64 + 50 + 40)
-        n = pic.pic_stage_pool(ref.ctx, ref.plans, hk, hv, dk, dv)
+        # in two calls, as a pipelined caller stages request groups: the
+        # second skips the rows the first staged
+        n = pic.pic_stage_pool(ref.ctx, ref.plans[:1], hk, hv, dk, dv)
+        n += pic.pic_stage_pool(ref.ctx, ref.plans[1:], hk, hv, dk, dv, staged_plans=ref.plans[:1])
         row = hk[0, 0].numel() * 2
         assert n == distinct * m.num_layers * row * (2 if hv is not None else 1)
         torch.cuda.synchronize()
@@ -135,7 +139,7 @@ def test_stage_pool_refuses_pageable_and_swapped_pointers():
         for args in ((pageable, hv, ref.k_pool, ref.v_pool),     # pageable host pool
                      (ref.k_pool, ref.v_pool, ref.k_pool, ref.v_pool),  # device memory as the host pool
                      (hk, hv, hk, hv)):                          # host memory as the device pool
-            st = L.pic_stage_pool(ref.ctx, arr, len(ref.plans), ctypes.c_void_p(args[0].data_ptr()),
+            st = L.pic_stage_pool(ref.ctx, arr, len(ref.plans), None, 0, ctypes.c_void_p(args[0].data_ptr()),
                                   ctypes.c_void_p(args[1].data_ptr()), ls, ctypes.c_void_p(args[2].data_ptr()),
                                   ctypes.c_void_p(args[3].data_ptr()), ls, None, None)
             assert pic.STATUS_NAMES[st] == "PIC_ERR_INVALID_ARG", args
