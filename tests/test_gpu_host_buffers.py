@@ -124,6 +124,30 @@ def test_staged_pool_copies_each_row_read_once_and_stitches_the_same(kind):
         ref.close()
 
 
+def test_stage_pool_over_more_ranges_than_one_launch_takes():
+    """1,100 chunks of 2 tokens, one request taking the first token of each:
+    1,100 separate row ranges, so the copy runs as two launches (1,024 ranges
+    each at most).  Every first row arrives, every second row stays zero."""
+    n = 1100
+    m = W.Model("stage-many", "gqa", 2, 1, 64, 64, 0, "neox", 1e4, 16)
+    wl = W.Workload("stage-many", m, [2] * n, [[(c, 1) for c in range(n)]], 0, 0)
+    ref = Stitched(wl, pool_device="cpu")
+    try:
+        assert pic.pic_pool_read_rows(ref.ctx, ref.plans) == (n, n)
+        hk = ref.k_pool.cpu().pin_memory()
+        hv = ref.v_pool.cpu().pin_memory()
+        dk, dv = torch.zeros_like(ref.k_pool), torch.zeros_like(ref.v_pool)
+        got = pic.pic_stage_pool(ref.ctx, ref.plans, hk, hv, dk, dv)
+        assert got == n * 2 * 128 * 2   # rows x layers x row bytes x (K, V)
+        torch.cuda.synchronize()
+        for host, staged in ((hk, dk), (hv, dv)):
+            hb, sb = bits(host), bits(staged)
+            assert np.array_equal(sb[:, 0::2], hb[:, 0::2])
+            assert not sb[:, 1::2].any()
+    finally:
+        ref.close()
+
+
 def test_stage_pool_refuses_pageable_and_swapped_pointers():
     lens = [40, 17]
     m = W.Model("stage-bad", "gqa", 2, 2, 128, 128, 0, "neox", 1e4, 16)
