@@ -692,16 +692,20 @@ class Rig:
             self.pic.pic_query_device_status(self.ctx, self.attn["ws"])
 
 
+E2E_GROUPS = 8  # request groups of the staged end-to-end leg
+
+
 def run_e2e(rig, steps, warmup, cache_on_host=False, stage=False):
     """Same metric end to end through the public API with the chunk pool in
     HOST memory: the pool lives in pinned host memory (a host-side chunk
     store), so the pool's bytes cross host->device inside the timed region
     every step.  Streamed (stage False): the stitch kernel reads the pool
     over the host link directly (on GB300, NVLink-C2C to Grace memory), a row
-    as often as the batch places it.  Staged: pic_stage_pool first copies
-    every pool row the batch reads, once, into the device pool buffers
-    (cleared before the first step, so only this leg's copies feed the
-    stitch), and the stitch reads them from HBM.  The paged cache is in HBM,
+    as often as the batch places it.  Staged: pic_stitch_staged copies every
+    pool row the batch reads, once, into the device pool buffers (cleared
+    before the first step, so only this leg's copies feed the stitch), in
+    groups of requests, each stitched from HBM while the next is copied.  The
+    paged cache is in HBM,
     where decode attention reads it (cache_on_host: in pinned host memory
     too, so the stitched bytes also cross device->host).  Each step also
     plans, uploads the block table and reads the recompute list back to the
@@ -728,50 +732,23 @@ def run_e2e(rig, steps, warmup, cache_on_host=False, stage=False):
         rig.k_pool.zero_()
         if rig.v_pool is not None:
             rig.v_pool.zero_()
-        # groups of requests, pipelined: group g + 1's rows are staged on a
-        # copy stream while group g is stitched; each group has its own
-        # workspace and recompute outputs (sized on one plan of the batch)
-        n_req = len(rig.wl.requests)
-        G = min(8, n_req)
-        bounds = [n_req * g // G for g in range(G + 1)]
-        copy_stream = torch.cuda.Stream()
         plans0, _ = rig.plan()
-        grp = []
-        for g in range(G):
-            pg = plans0[bounds[g]:bounds[g + 1]]
-            n_rec = sum(pic.pic_plan_info(p)["num_recompute"] for p in pg)
-            ridx = torch.empty(max(1, n_rec), dtype=torch.int32, device=rig.d_bt.device)
-            indptr = torch.empty(len(pg) + 1, dtype=torch.int32, device=rig.d_bt.device)
-            grp.append(dict(ws=torch.empty(pic.pic_workspace_bytes(rig.ctx, pg), dtype=torch.uint8,
-                                           device=rig.d_bt.device),
-                            ridx=ridx, indptr=indptr, oi=torch.empty_like(ridx, device="cpu").pin_memory(),
-                            op=torch.empty_like(indptr, device="cpu").pin_memory()))
+        ws_staged = torch.empty(pic.pic_stitch_staged_workspace_bytes(rig.ctx, plans0, E2E_GROUPS), dtype=torch.uint8,
+                                device=rig.d_bt.device)
         rig.free(plans0)
 
     def one():
         plans, bt = rig.plan()
         rig.upload_tables(bt)
         if stage:
-            cur = torch.cuda.current_stream()
-            # this step's copies start once the work queued before (the last
-            # step's stitches, this table upload) is done
-            copy_stream.wait_stream(cur)
-            n = 0
-            for g in range(G):
-                b0, b1 = bounds[g], bounds[g + 1]
-                n += pic.pic_stage_pool(rig.ctx, plans[b0:b1], hk, hv, rig.k_pool, rig.v_pool,
-                                        staged_plans=plans[:b0], stream=copy_stream)
-                cur.wait_stream(copy_stream)
-                x = grp[g]
-                pic.pic_stitch(rig.ctx, plans[b0:b1], rig.k_pool, rig.v_pool, hkc, hvc, rig.d_bt[b0:b1], x["ridx"],
-                               x["indptr"], x["ws"])
-                x["oi"].copy_(x["ridx"], non_blocking=True)
-                x["op"].copy_(x["indptr"], non_blocking=True)
-            staged[0] = n
+            # request groups staged on the library's copy stream while the
+            # earlier groups stitch, into the device pool buffers
+            staged[0] = pic.pic_stitch_staged(rig.ctx, plans, hk, hv, rig.k_pool, rig.v_pool, hkc, hvc, rig.d_bt,
+                                              rig.ridx, rig.indptr, ws_staged, n_groups=E2E_GROUPS)
         else:
             pic.pic_stitch(rig.ctx, plans, hk, hv, hkc, hvc, rig.d_bt, rig.ridx, rig.indptr, rig.ws)
-            oi.copy_(rig.ridx, non_blocking=True)
-            op.copy_(rig.indptr, non_blocking=True)
+        oi.copy_(rig.ridx, non_blocking=True)
+        op.copy_(rig.indptr, non_blocking=True)
         rig.free(plans)
 
     for _ in range(warmup):
@@ -783,18 +760,14 @@ def run_e2e(rig, steps, warmup, cache_on_host=False, stage=False):
         one()
     e1.record()
     torch.cuda.synchronize()
-    for ws in ([x["ws"] for x in grp] if stage else [rig.ws]):
-        pic.pic_query_device_status(rig.ctx, ws)
+    pic.pic_query_device_status(rig.ctx, ws_staged if stage else rig.ws)
     ms = e0.elapsed_time(e1) / steps
     wl = rig.wl
     rows = wl.token_layers * rig.m.num_kv_heads * rig.m.head_dim * 2   # bytes of K rows moved
     tensors = 2 if hv is not None else 1
-    if stage:
-        h2d = staged[0] + rig.d_bt.numel() * 4 + sum(x["ws"].numel() for x in grp)
-        d2h = sum(x["oi"].numel() * 4 + x["op"].numel() * 4 for x in grp)
-    else:
-        h2d = rows * tensors + rig.d_bt.numel() * 4 + rig.ws_bytes
-        d2h = (rows * tensors if cache_on_host else 0) + oi.numel() * 4 + op.numel() * 4
+    pool = staged[0] if stage else rows * tensors
+    h2d = pool + rig.d_bt.numel() * 4 + (ws_staged.numel() if stage else rig.ws_bytes)
+    d2h = (rows * tensors if cache_on_host else 0) + oi.numel() * 4 + op.numel() * 4
     return ms, h2d, d2h
 
 
@@ -1164,10 +1137,10 @@ def main():
             res[name] = (max_over_ranks(ems, dev), h2d, d2h)
         ems, h2d, d2h = res["staged" if stage else "streamed"]
         where = "pool and cache" if args.e2e_cache_on_host else "pool"
-        how = (f"{where} in pinned host memory; each step pic_stage_pool copies the pool rows the batch reads, "
-               f"each once ({distinct} of the {read} rows read per layer), into the device pool buffers, and the "
-               f"stitch reads them from HBM: up to 8 request groups, group g + 1 staged on a copy stream while group g "
-               f"is stitched" if stage else
+        how = (f"{where} in pinned host memory; each step pic_stitch_staged copies the pool rows the batch reads, "
+               f"each once ({distinct} of the {read} rows read per layer), into the device pool buffers, and "
+               f"stitches from HBM: {E2E_GROUPS} request groups, group g + 1 staged on the library's copy stream while "
+               f"group g is stitched" if stage else
                f"{where} in pinned host memory, streamed by the kernel over NVLink-C2C")
         e2e = {"value": world * algo_bytes / (ems * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ems,

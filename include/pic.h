@@ -24,10 +24,13 @@
  *     registry, block allocator and pic_plan objects, and only two pieces of
  *     device memory: the fixed scratch array of pic_stitch_noalloc, and the
  *     device copy of the decode attention's plan image that pic_attend_decode
- *     keeps per context (freed by pic_destroy).
+ *     keeps per context (freed by pic_destroy).  pic_stitch_staged also keeps
+ *     a CUDA stream and an event per context.
  *   - Threads: a context is used by one host thread at a time.
  *   - Streams: all device work is enqueued on the caller's stream and is
  *     asynchronous; host arguments may be reused as soon as a call returns.
+ *     (pic_stitch_staged runs its copies on its own stream, ordered between
+ *     the caller's earlier and later work.)
  *   - Errors: every call returns a pic_status; on failure nothing was
  *     enqueued and pic_last_error() describes the cause.  CUDA launch
  *     failures are PIC_ERR_CUDA.  Errors a kernel finds on the device (a
@@ -423,6 +426,41 @@ pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_
                           const void* host_k_pool, const void* host_v_pool,
                           int64_t host_pool_layer_stride_bytes, void* dev_k_pool, void* dev_v_pool,
                           int64_t dev_pool_layer_stride_bytes, int64_t* bytes_copied, pic_stream_t stream);
+
+/*
+ * pic_stitch_staged -- pic_stage_pool and pic_stitch in one call, pipelined
+ * over groups of requests, for a chunk pool in pinned host memory.  The
+ * requests are cut into n_groups consecutive groups (at most n_req).  Group
+ * g's pool rows, less those of earlier groups, are copied into the device
+ * pools on a stream the context owns, while group g - 1 is stitched on
+ * `stream`.  So each distinct row crosses the host link once, and the
+ * stitches hide behind the copies.  The outputs equal those of
+ * pic_stage_pool followed by pic_stitch with the device pools, bit for bit:
+ * the cache rows, and one recompute CSR over all requests.
+ *   host_* / dev_* pools   as pic_stage_pool; the device pools then hold the
+ *                          rows the plans read.
+ *   k_cache ... stream     as pic_stitch.
+ *   d_workspace            pic_stitch_staged_workspace_bytes(ctx, plans,
+ *                          n_req, n_groups) bytes.  Its first 256 bytes hold
+ *                          the status word of the whole call, read by
+ *                          pic_query_device_status.
+ *   *bytes_staged          (may be NULL) bytes the copies move.
+ * Stream order: the copies start after the work queued on `stream` before the
+ * call, and every stitch and the work queued on `stream` after the call run
+ * after the copies they need.  The context keeps the copy stream and an event
+ * (created on first use, per device; destroyed by pic_destroy).  Errors as
+ * pic_stitch and pic_stage_pool; n_groups < 1 is PIC_ERR_INVALID_ARG.
+ */
+size_t pic_stitch_staged_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                                         int32_t n_groups);
+pic_status pic_stitch_staged(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t n_groups,
+                             const void* host_k_pool, const void* host_v_pool,
+                             int64_t host_pool_layer_stride_bytes, void* dev_k_pool, void* dev_v_pool,
+                             int64_t dev_pool_layer_stride_bytes, void* k_cache, void* v_cache,
+                             int64_t cache_layer_stride_bytes, const int32_t* d_block_tables, int32_t max_blocks,
+                             int32_t* d_recompute_idx, int32_t* d_recompute_indptr, int64_t recompute_capacity,
+                             void* d_workspace, size_t workspace_bytes, int64_t* bytes_staged,
+                             pic_stream_t stream);
 
 /* ------------------------------------------------------- in-place shift */
 

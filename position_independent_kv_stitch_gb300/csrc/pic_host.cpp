@@ -205,6 +205,11 @@ struct pic_ctx {
   std::shared_ptr<void> attn_cache[2];
   uint64_t attn_serial = 0;  // last serial given to a cached attention plan
   AttnResident attn_res[2];  // one per cache slot
+  // pic_stitch_staged: the stream its pool copies run on, and the event that
+  // orders them against the caller's stream (created on first use, per device)
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t copy_event = nullptr;
+  int copy_device = -1;
   pic_ctx(int32_t nb) : num_cache_blocks(nb), alloc(nb) {}
 };
 
@@ -625,6 +630,23 @@ void release_attn_resident(pic_ctx* ctx) {
     }
     r = AttnResident{};
   }
+  if (cur >= 0) cudaSetDevice(cur);
+}
+
+// Releases the context's copy stream and event.
+void release_copy_stream(pic_ctx* ctx) {
+  if (!ctx->copy_stream && !ctx->copy_event) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  cudaSetDevice(ctx->copy_device);
+  if (ctx->copy_stream) {
+    cudaStreamSynchronize(ctx->copy_stream);
+    cudaStreamDestroy(ctx->copy_stream);
+  }
+  if (ctx->copy_event) cudaEventDestroy(ctx->copy_event);
+  ctx->copy_stream = nullptr;
+  ctx->copy_event = nullptr;
+  ctx->copy_device = -1;
   if (cur >= 0) cudaSetDevice(cur);
 }
 
@@ -1162,6 +1184,7 @@ void pic_destroy(pic_ctx* ctx) {
   if (!ctx) return;
   release_staging(ctx);
   release_attn_resident(ctx);
+  release_copy_stream(ctx);
   for (pic_plan* p : ctx->plans) delete p;
   delete ctx;
 }
@@ -1600,6 +1623,108 @@ pic_status pic_pool_read_rows(const pic_ctx* cctx, const pic_plan* const* plans,
   return ok(ctx);
 }
 
+namespace {
+
+// Host and device pools of a staging call, checked.
+struct StagePools {
+  const void* host[2];
+  void* dev[2];
+  int64_t host_ls, dev_ls;
+  int tensors;
+};
+
+// Checks the pools of a staging call that need no CUDA call (null,
+// GQA/MLA values, alignment, strides reaching row `top`).
+pic_status check_stage_pools(pic_ctx* ctx, const StagePools& sp, int64_t top) {
+  const pic_model_desc& m = ctx->model;
+  const bool gqa = m.kind == PIC_KIND_GQA;
+  if (!sp.host[0] || !sp.dev[0]) return fail(ctx, PIC_ERR_INVALID_ARG, "null pool");
+  if (gqa && (!sp.host[1] || !sp.dev[1])) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs both value pools");
+  if (!gqa && (sp.host[1] || sp.dev[1])) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
+  for (int k = 0; k < sp.tensors; ++k)
+    if (!vectorized_bytes_ok(sp.host[k]) || !vectorized_bytes_ok(sp.dev[k]))
+      return fail(ctx, PIC_ERR_ALIGNMENT, "pools and layer strides must be 16-byte aligned");
+  if ((sp.host_ls & 15) || (sp.dev_ls & 15))
+    return fail(ctx, PIC_ERR_ALIGNMENT, "pools and layer strides must be 16-byte aligned");
+  const int64_t row = row_bytes_of(m);
+  if (m.num_layers > 1 && (sp.host_ls < top * row || sp.dev_ls < top * row))
+    return fail(ctx, PIC_ERR_RANGE, "a layer stride is smaller than the %lld pool rows the plans reach",
+                static_cast<long long>(top));
+  return PIC_OK;
+}
+
+// Where the pools live: pinned host memory and device memory (CUDA calls).
+pic_status check_stage_residency(pic_ctx* ctx, const StagePools& sp) {
+  for (int k = 0; k < sp.tensors; ++k) {
+    if (residency(sp.host[k]) != 1)
+      return fail(ctx, PIC_ERR_INVALID_ARG, "host pools must be pinned host memory (cudaHostAlloc / cudaHostRegister)");
+    if (residency(sp.dev[k]) != 0) return fail(ctx, PIC_ERR_INVALID_ARG, "device pools must be device memory");
+  }
+  return PIC_OK;
+}
+
+// Enqueues the copy kernel over `ranges` (pool rows), every layer and tensor,
+// on stream s: one launch per kStageMaxSpans ranges.  Adds the bytes to *bytes.
+pic_status launch_stage_ranges(pic_ctx* ctx, const StagePools& sp, const std::vector<std::pair<int64_t, int64_t>>& ranges,
+                               int sm_count, cudaStream_t s, int64_t* bytes) {
+  const int64_t row = row_bytes_of(ctx->model);
+  const int32_t L = ctx->model.num_layers;
+  auto prm = std::make_unique<pic::StageParams>();
+  for (int k = 0; k < 2; ++k) {
+    prm->src[k] = static_cast<const uint8_t*>(sp.host[k]);
+    prm->dst[k] = static_cast<uint8_t*>(sp.dev[k]);
+  }
+  prm->src_ls = sp.host_ls;
+  prm->dst_ls = sp.dev_ls;
+  prm->layers = L;
+  prm->tensors = sp.tensors;
+  for (size_t r0 = 0; r0 < ranges.size(); r0 += pic::kStageMaxSpans) {
+    const size_t n = std::min<size_t>(pic::kStageMaxSpans, ranges.size() - r0);
+    for (size_t i = 0; i < n; ++i) {
+      prm->spans[i].off = ranges[r0 + i].first * row;
+      prm->spans[i].bytes = (ranges[r0 + i].second - ranges[r0 + i].first) * row;
+      *bytes += prm->spans[i].bytes * L * sp.tensors;
+    }
+    prm->n_spans = static_cast<int32_t>(n);
+    const int64_t items = static_cast<int64_t>(n) * L * sp.tensors;
+    const cudaError_t e = pic::launch_stage_rows(*prm, static_cast<int>(std::min<int64_t>(items, sm_count)), s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "pool staging launch");
+  }
+  return PIC_OK;
+}
+
+// The request groups of a staged stitch: [bounds[g], bounds[g + 1]).
+std::vector<int32_t> group_bounds(int32_t n_req, int32_t n_groups) {
+  const int32_t G = std::max<int32_t>(1, std::min(n_groups, n_req));
+  std::vector<int32_t> b(G + 1);
+  for (int32_t g = 0; g <= G; ++g) b[g] = static_cast<int32_t>(static_cast<int64_t>(n_req) * g / G);
+  return b;
+}
+
+// A group's workspace layout, its offset in the workspace and its runs.
+struct GroupLayout {
+  WsLayout w;
+  size_t off;
+  size_t runs;
+};
+
+std::vector<GroupLayout> group_layouts(const pic_ctx* ctx, const pic_plan* const* plans, const std::vector<int32_t>& b,
+                                       size_t* total) {
+  std::vector<GroupLayout> out;
+  size_t off = 0;
+  for (size_t g = 0; g + 1 < b.size(); ++g) {
+    const int32_t n = b[g + 1] - b[g];
+    const size_t runs = count_stitch_runs(ctx, plans + b[g], n);
+    const WsLayout w = ws_layout(ctx->freq_turns.size(), static_cast<size_t>(n) + 1, runs);
+    out.push_back(GroupLayout{w, off, runs});
+    off += w.total;
+  }
+  *total = off;
+  return out;
+}
+
+}  // namespace
+
 pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
                           const pic_plan* const* staged_plans, int32_t n_staged,
                           const void* host_k_pool, const void* host_v_pool, int64_t host_ls,
@@ -1610,59 +1735,117 @@ pic_status pic_stage_pool(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_
   if (st != PIC_OK) return st;
   st = check_plan_list(ctx, staged_plans, n_staged);
   if (st != PIC_OK) return st;
-  const pic_model_desc& m = ctx->model;
-  const bool gqa = m.kind == PIC_KIND_GQA;
-  if (!host_k_pool || !dev_k_pool) return fail(ctx, PIC_ERR_INVALID_ARG, "null pool");
-  if (gqa && (!host_v_pool || !dev_v_pool)) return fail(ctx, PIC_ERR_INVALID_ARG, "GQA needs both value pools");
-  if (!gqa && (host_v_pool || dev_v_pool)) return fail(ctx, PIC_ERR_INVALID_ARG, "MLA rows have no separate values (pass NULL)");
-  if (!vectorized_bytes_ok(host_k_pool) || !vectorized_bytes_ok(dev_k_pool) ||
-      (gqa && (!vectorized_bytes_ok(host_v_pool) || !vectorized_bytes_ok(dev_v_pool))) || (host_ls & 15) ||
-      (dev_ls & 15))
-    return fail(ctx, PIC_ERR_ALIGNMENT, "pools and layer strides must be 16-byte aligned");
-  int64_t read = 0;
-  const auto ranges = minus_ranges(pool_read_ranges(plans, n_req, &read), pool_read_ranges(staged_plans, n_staged, nullptr));
-  const int64_t row = row_bytes_of(m);
-  const int64_t top = ranges.empty() ? 0 : ranges.back().second;
-  const int32_t L = m.num_layers;
-  if (L > 1 && (host_ls < top * row || dev_ls < top * row))
-    return fail(ctx, PIC_ERR_RANGE, "a layer stride is smaller than the %lld pool rows the plans reach",
-                static_cast<long long>(top));
+  const StagePools sp{{host_k_pool, host_v_pool}, {dev_k_pool, dev_v_pool}, host_ls, dev_ls,
+                      ctx->model.kind == PIC_KIND_GQA ? 2 : 1};
+  const auto ranges = minus_ranges(pool_read_ranges(plans, n_req, nullptr), pool_read_ranges(staged_plans, n_staged, nullptr));
+  st = check_stage_pools(ctx, sp, ranges.empty() ? 0 : ranges.back().second);
+  if (st != PIC_OK) return st;
   DeviceInfo di;
   st = current_device(ctx, di);
   if (st != PIC_OK) return st;
-  const void* host[2] = {host_k_pool, host_v_pool};
-  void* dev[2] = {dev_k_pool, dev_v_pool};
-  const int tensors = gqa ? 2 : 1;
-  for (int k = 0; k < tensors; ++k) {
-    if (residency(host[k]) != 1)
-      return fail(ctx, PIC_ERR_INVALID_ARG, "host pools must be pinned host memory (cudaHostAlloc / cudaHostRegister)");
-    if (residency(dev[k]) != 0) return fail(ctx, PIC_ERR_INVALID_ARG, "device pools must be device memory");
-  }
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the copy kernel's parameters carry up to kStageMaxSpans ranges per launch
-  auto prm = std::make_unique<pic::StageParams>();
-  for (int k = 0; k < 2; ++k) {
-    prm->src[k] = static_cast<const uint8_t*>(host[k]);
-    prm->dst[k] = static_cast<uint8_t*>(dev[k]);
-  }
-  prm->src_ls = host_ls;
-  prm->dst_ls = dev_ls;
-  prm->layers = L;
-  prm->tensors = tensors;
+  st = check_stage_residency(ctx, sp);
+  if (st != PIC_OK) return st;
   int64_t bytes = 0;
-  for (size_t r0 = 0; r0 < ranges.size(); r0 += pic::kStageMaxSpans) {
-    const size_t n = std::min<size_t>(pic::kStageMaxSpans, ranges.size() - r0);
-    for (size_t i = 0; i < n; ++i) {
-      prm->spans[i].off = ranges[r0 + i].first * row;
-      prm->spans[i].bytes = (ranges[r0 + i].second - ranges[r0 + i].first) * row;
-      bytes += prm->spans[i].bytes * L * tensors;
-    }
-    prm->n_spans = static_cast<int32_t>(n);
-    const int64_t items = static_cast<int64_t>(n) * L * tensors;
-    const cudaError_t e = pic::launch_stage_rows(*prm, static_cast<int>(std::min<int64_t>(items, di.sm_count)), s);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "pool staging launch");
-  }
+  st = launch_stage_ranges(ctx, sp, ranges, di.sm_count, reinterpret_cast<cudaStream_t>(stream), &bytes);
+  if (st != PIC_OK) return st;
   if (bytes_copied) *bytes_copied = bytes;
+  return ok(ctx);
+}
+
+size_t pic_stitch_staged_workspace_bytes(const pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req,
+                                         int32_t n_groups) {
+  if (!ctx || n_req < 0 || (n_req > 0 && !plans) || n_groups < 1) return 0;
+  for (int32_t r = 0; r < n_req; ++r)
+    if (!plans[r]) return 0;
+  size_t total = 0;
+  group_layouts(ctx, plans, group_bounds(n_req, n_groups), &total);
+  return total;
+}
+
+pic_status pic_stitch_staged(pic_ctx* ctx, const pic_plan* const* plans, int32_t n_req, int32_t n_groups,
+                             const void* host_k_pool, const void* host_v_pool, int64_t host_ls,
+                             void* dev_k_pool, void* dev_v_pool, int64_t dev_ls, void* k_cache, void* v_cache,
+                             int64_t cache_ls, const int32_t* d_bt, int32_t max_blocks, int32_t* d_ridx,
+                             int32_t* d_indptr, int64_t recompute_capacity, void* d_ws, size_t ws_bytes,
+                             int64_t* bytes_staged, pic_stream_t stream) {
+  if (!ctx) return fail(nullptr, PIC_ERR_INVALID_ARG, "null ctx");
+  if (n_groups < 1) return fail(ctx, PIC_ERR_INVALID_ARG, "n_groups must be >= 1");
+  pic_status st = check_stitch_args(ctx, plans, n_req, dev_k_pool, dev_v_pool, dev_ls, k_cache, v_cache, cache_ls,
+                                    d_bt, max_blocks, d_ridx, d_indptr, recompute_capacity);
+  if (st != PIC_OK) return st;
+  const StagePools sp{{host_k_pool, host_v_pool}, {dev_k_pool, dev_v_pool}, host_ls, dev_ls,
+                      ctx->model.kind == PIC_KIND_GQA ? 2 : 1};
+  const auto all = pool_read_ranges(plans, n_req, nullptr);
+  st = check_stage_pools(ctx, sp, all.empty() ? 0 : all.back().second);
+  if (st != PIC_OK) return st;
+  if (!d_ws) return fail(ctx, PIC_ERR_INVALID_ARG, "null workspace");
+  if (!vectorized_bytes_ok(d_ws)) return fail(ctx, PIC_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  const std::vector<int32_t> b = group_bounds(n_req, n_groups);
+  size_t need = 0;
+  const auto lay = group_layouts(ctx, plans, b, &need);
+  if (ws_bytes < need) return fail(ctx, PIC_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  for (const GroupLayout& x : lay)
+    if (x.runs > static_cast<size_t>(std::numeric_limits<int32_t>::max())) return fail(ctx, PIC_ERR_RANGE, "too many runs");
+
+  DeviceInfo di;
+  st = current_device(ctx, di);
+  if (st != PIC_OK) return st;
+  st = check_stage_residency(ctx, sp);
+  if (st != PIC_OK) return st;
+  const void* bufs[2] = {k_cache, v_cache};
+  const int host_io = host_buffers(ctx, bufs, 2);
+  if (host_io < 0) return PIC_ERR_INVALID_ARG;
+  if (ctx->copy_device != di.device) {
+    release_copy_stream(ctx);
+    cudaError_t e = cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamCreate (staging)");
+    e = cudaEventCreateWithFlags(&ctx->copy_event, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaEventCreate (staging)");
+    ctx->copy_device = di.device;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream), cs = ctx->copy_stream;
+  // the copies start after the work queued on the caller's stream before this call
+  cudaError_t e = cudaEventRecord(ctx->copy_event, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ctx->copy_event, 0);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "staging stream order");
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  int64_t bytes = 0;
+  int64_t rec_base = 0;  // recompute entries of the groups before
+  for (size_t g = 0; g + 1 < b.size(); ++g) {
+    const int32_t r0 = b[g], n = b[g + 1] - b[g];
+    // group g's rows that no earlier group read, on the copy stream; then the
+    // caller's stream waits for them
+    st = launch_stage_ranges(ctx, sp, minus_ranges(pool_read_ranges(plans + r0, n, nullptr), pool_read_ranges(plans, r0, nullptr)),
+                             di.sm_count, cs, &bytes);
+    if (st != PIC_OK) return st;
+    e = cudaEventRecord(ctx->copy_event, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ctx->copy_event, 0);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "staging stream order");
+    // the group's stitch: its image numbers requests and recompute entries
+    // from 0; the recompute offsets move by the earlier groups' entries, and
+    // the kernel gets the group's block-table rows and CSR slots
+    const WsLayout& w = lay[g].w;
+    StagingSlot* sl = nullptr;
+    st = acquire_staging(ctx, di.device, w.total, &sl);
+    if (st != PIC_OK) return st;
+    build_stitch_image(ctx, plans + r0, n, sl->host, w);
+    int32_t* indptr = reinterpret_cast<int32_t*>(sl->host + w.indptr_off);
+    for (int32_t i = 0; i <= n; ++i) indptr[i] += static_cast<int32_t>(rec_base);
+    RunDesc* runs = reinterpret_cast<RunDesc*>(sl->host + w.runs_off);
+    for (size_t k = 0; k < lay[g].runs; ++k) runs[k].idx_off += static_cast<int32_t>(rec_base);
+    st = upload_staging(ctx, sl, ws + lay[g].off, w.total, s);
+    if (st != PIC_OK) return st;
+    pic::KernelParams p{};
+    fill_stitch_params(ctx, p, ws + lay[g].off, w, lay[g].runs, n, dev_k_pool, dev_v_pool, dev_ls, k_cache, v_cache,
+                       cache_ls, d_bt + static_cast<int64_t>(r0) * max_blocks, max_blocks, d_ridx,
+                       d_indptr ? d_indptr + r0 : nullptr);
+    p.header = reinterpret_cast<WsHeader*>(ws);  // one status word for the whole call: group 0's
+    e = launch_stitch_kernel(ctx, p, di.sm_count, s, host_io != 0, mostly_in_place(plans + r0, n));
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "stitch launch");
+    for (int32_t r = r0; r < r0 + n; ++r) rec_base += plans[r]->n_recompute;
+  }
+  for (int32_t r = 0; r < n_req; ++r) const_cast<pic_plan*>(plans[r])->applied = true;
+  if (bytes_staged) *bytes_staged = bytes;
   return ok(ctx);
 }
 

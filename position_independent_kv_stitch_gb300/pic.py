@@ -102,6 +102,10 @@ _SIGNATURES = {
     "pic_pool_read_rows": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _P(_c_void_p), _i32, _P(_i64), _P(_i64)]),
     "pic_stage_pool": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _P(_c_void_p), _i32, _c_void_p, _c_void_p,
                                       _i64, _c_void_p, _c_void_p, _i64, _P(_i64), _c_void_p]),
+    "pic_stitch_staged_workspace_bytes": (_sz, [_c_void_p, _P(_c_void_p), _i32, _i32]),
+    "pic_stitch_staged": (ctypes.c_int, [_c_void_p, _P(_c_void_p), _i32, _i32, _c_void_p, _c_void_p, _i64, _c_void_p,
+                                         _c_void_p, _i64, _c_void_p, _c_void_p, _i64, _c_void_p, _i32, _c_void_p,
+                                         _c_void_p, _i64, _c_void_p, _sz, _P(_i64), _c_void_p]),
     "pic_rerotate_workspace_bytes": (_sz, [_c_void_p, _P(pic_shift_seg), _i32]),
     "pic_rerotate_inplace": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _i32, _i32,
                                             _P(pic_shift_seg), _i32, _c_void_p, _sz, _c_void_p]),
@@ -390,6 +394,45 @@ def pic_stage_pool(ctx, plans, host_k_pool, host_v_pool, dev_k_pool, dev_v_pool,
     st = load().pic_stage_pool(ctx, _plan_array(plans), len(plans), _plan_array(staged_plans) if staged_plans else None,
                                len(staged_plans), _ptr(host_k_pool), _ptr(host_v_pool), hls,
                                _ptr(dev_k_pool), _ptr(dev_v_pool), dls, ctypes.byref(n), _stream_handle(stream))
+    _check(st, ctx)
+    return n.value
+
+
+def pic_stitch_staged_workspace_bytes(ctx, plans, n_groups: int) -> int:
+    return int(load().pic_stitch_staged_workspace_bytes(ctx, _plan_array(plans), len(plans), int(n_groups)))
+
+
+def pic_stitch_staged(ctx, plans, host_k_pool, host_v_pool, dev_k_pool, dev_v_pool, k_cache, v_cache, block_tables,
+                      recompute_idx=None, recompute_indptr=None, workspace=None, n_groups: int = 8,
+                      stream=None) -> int:
+    """pic_stage_pool + pic_stitch in one call, pipelined over n_groups
+    groups of requests.  Pools as pic_stage_pool, the rest as pic_stitch;
+    workspace >= pic_stitch_staged_workspace_bytes.  Returns the bytes
+    staged."""
+    arr = _plan_array(plans)
+    _check_device_int32(block_tables, "block_tables")
+    if block_tables.dim() != 2 or (len(plans) > 0 and block_tables.shape[0] < len(plans)):
+        raise ValueError("block_tables must be [n_req][max_blocks] with a row per plan")
+    if recompute_indptr is not None:
+        _check_device_int32(recompute_indptr, "recompute_indptr")
+        _check_device_int32(recompute_idx, "recompute_idx")
+        if recompute_indptr.numel() < len(plans) + 1:
+            raise ValueError("recompute_indptr needs n_req + 1 entries")
+    for name, t in (("host_k_pool", host_k_pool), ("host_v_pool", host_v_pool), ("dev_k_pool", dev_k_pool),
+                    ("dev_v_pool", dev_v_pool), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_kv_buffer(t, name)
+    hls, dls, cls = _layer_stride_bytes(host_k_pool), _layer_stride_bytes(dev_k_pool), _layer_stride_bytes(k_cache)
+    for a, b, what in ((host_v_pool, hls, "host pools"), (dev_v_pool, dls, "device pools"), (v_cache, cls, "caches")):
+        if a is not None and _layer_stride_bytes(a) != b:
+            raise ValueError(f"the K and V {what} must share a layer stride")
+    cap = recompute_idx.numel() if recompute_idx is not None else 0
+    n = ctypes.c_int64()
+    st = load().pic_stitch_staged(ctx, arr, len(plans), int(n_groups), _ptr(host_k_pool), _ptr(host_v_pool), hls,
+                                  _ptr(dev_k_pool), _ptr(dev_v_pool), dls, _ptr(k_cache), _ptr(v_cache), cls,
+                                  _ptr(block_tables), int(block_tables.shape[1]), _ptr(recompute_idx),
+                                  _ptr(recompute_indptr), cap, _ptr(workspace),
+                                  workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                                  ctypes.byref(n), _stream_handle(stream))
     _check(st, ctx)
     return n.value
 

@@ -383,6 +383,41 @@ def test_stage_pool_argument_checks_need_no_gpu():
         pic.pic_destroy(mla)
 
 
+def test_staged_stitch_workspace_and_argument_checks_need_no_gpu():
+    """pic_stitch_staged's workspace is one stitch image per request group
+    (one group: pic_stitch's own size); bad arguments are refused before any
+    CUDA call (fake, aligned pointers)."""
+    ctx = _gqa_ctx(nb=32)
+    L = pic.load()
+    try:
+        for c, n in enumerate([20, 7, 33]):
+            pic.pic_register_chunk(ctx, W.chunk_key("sg", c), [0, 20, 27][c], n)
+        plans = [pic.pic_build_block_table(ctx, ids, 6, k_nonleading=4)[0] for ids in ([0, 2], [1, 0], [2], [1])]
+        one = pic.pic_stitch_staged_workspace_bytes(ctx, plans, 1)
+        assert one == pic.pic_workspace_bytes(ctx, plans)
+        per = [pic.pic_workspace_bytes(ctx, [p]) for p in plans]
+        assert pic.pic_stitch_staged_workspace_bytes(ctx, plans, 4) == sum(per)
+        assert pic.pic_stitch_staged_workspace_bytes(ctx, plans, 99) == sum(per)   # clamped to 4 groups
+        assert pic.pic_stitch_staged_workspace_bytes(ctx, plans, 2) == (pic.pic_workspace_bytes(ctx, plans[:2])
+                                                                         + pic.pic_workspace_bytes(ctx, plans[2:]))
+        assert pic.pic_stitch_staged_workspace_bytes(ctx, plans, 0) == 0
+        arr = pic._plan_array(plans)
+        good = ctypes.c_void_p(0x10000)
+        pls = 60 * 512
+        cls = 32 * 16 * 512
+
+        def call(n_groups, ws_bytes, cache=good, pool_ls=pls):
+            return pic.STATUS_NAMES[L.pic_stitch_staged(ctx, arr, 4, n_groups, good, good, pool_ls, good, good, pool_ls,
+                                                        cache, good, cls, good, 6, None, None, 0, good, ws_bytes,
+                                                        None, None)]
+        assert call(0, 1 << 20) == "PIC_ERR_INVALID_ARG"
+        assert call(2, pic.pic_stitch_staged_workspace_bytes(ctx, plans, 2) - 1) == "PIC_ERR_CAPACITY"
+        assert call(2, 1 << 20, cache=ctypes.c_void_p(0x10008)) == "PIC_ERR_ALIGNMENT"
+        assert call(2, 1 << 20, pool_ls=59 * 512) == "PIC_ERR_RANGE"   # rows up to 59 are read
+    finally:
+        pic.pic_destroy(ctx)
+
+
 def test_attend_argument_checks_need_no_gpu():
     """pic_attend_decode refuses bad arguments before any CUDA call (fake,
     aligned pointers that never reach a launch)."""

@@ -124,6 +124,61 @@ def test_staged_pool_copies_each_row_read_once_and_stitches_the_same(kind):
         ref.close()
 
 
+@pytest.mark.parametrize("kind,n_groups", [("gqa", 1), ("gqa", 2), ("gqa", 3), ("gqa", 9), ("mla", 2), ("mla", 5)])
+def test_staged_stitch_equals_the_stitch_from_device_pools(kind, n_groups):
+    """pic_stitch_staged (pinned host pools, groups of requests staged on the
+    context's copy stream while earlier groups stitch) against pic_stitch
+    over the whole pool in device memory: cache rows, recompute list and CSR
+    offsets equal bit for bit, one status word clean; the device pool holds
+    the rows read and zeros elsewhere.  Five requests reuse chunks across
+    groups; 9 groups are clamped to the 5 requests."""
+    lens = [40, 17, 100, 33, 9, 64, 5]
+    reqs = [[(2, 100), (0, 40)], [(3, 20), (2, 100)], [(5, 64), (2, 50), (0, 40)], [(6, 5), (0, 40)],
+            [(3, 33), (5, 64), (6, 5)]]
+    if kind == "gqa":
+        m = W.Model("staged-gqa", "gqa", 3, 2, 128, 128, 0, "neox", 5e5, 16)
+    else:
+        m = W.Model("staged-mla", "mla", 2, 1, 576, 64, 512, "interleaved", 1e4, 16)
+    wl = W.Workload(f"staged-{kind}", m, lens, reqs, 4, 0)
+    ref = Stitched(wl, pool_device="cpu").run()
+    try:
+        hk = ref.k_pool.cpu().pin_memory()
+        hv = ref.v_pool.cpu().pin_memory() if ref.v_pool is not None else None
+        dk = torch.zeros_like(ref.k_pool)
+        dv = torch.zeros_like(ref.v_pool) if ref.v_pool is not None else None
+        k_cache = torch.empty_like(ref.k_cache)
+        k_cache.view(torch.int16).fill_(-1)
+        v_cache = None
+        if ref.v_cache is not None:
+            v_cache = torch.empty_like(ref.v_cache)
+            v_cache.view(torch.int16).fill_(-1)
+        ridx, indptr = torch.full_like(ref.ridx, -7), torch.full_like(ref.indptr, -7)
+        ws = torch.empty(pic.pic_stitch_staged_workspace_bytes(ref.ctx, ref.plans, n_groups), dtype=torch.uint8,
+                         device=DEV)
+        n = pic.pic_stitch_staged(ref.ctx, ref.plans, hk, hv, dk, dv, k_cache, v_cache, ref.d_bt, ridx, indptr, ws,
+                                  n_groups=n_groups)
+        assert pic.pic_query_device_status(ref.ctx, ws) == 0
+        torch.cuda.synchronize()
+        distinct, _ = pic.pic_pool_read_rows(ref.ctx, ref.plans)
+        row = hk[0, 0].numel() * 2
+        assert n == distinct * m.num_layers * row * (2 if hv is not None else 1)
+        assert np.array_equal(bits(k_cache), bits(ref.k_cache))
+        if v_cache is not None:
+            assert np.array_equal(bits(v_cache), bits(ref.v_cache))
+        assert torch.equal(ridx, ref.ridx) and torch.equal(indptr, ref.indptr)
+        offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
+        read_rows = np.zeros(sum(lens), dtype=bool)
+        for c, take in {(c, t) for req in reqs for c, t in req}:
+            read_rows[offs[c]:offs[c] + take] = True
+        assert not read_rows.all()
+        for host, staged in ((hk, dk), (hv, dv)):
+            if host is not None:
+                assert np.array_equal(bits(staged)[:, read_rows], bits(host)[:, read_rows])
+                assert not bits(staged)[:, ~read_rows].any()
+    finally:
+        ref.close()
+
+
 def test_stage_pool_over_more_ranges_than_one_launch_takes():
     """1,100 chunks of 2 tokens, one request taking the first token of each:
     1,100 separate row ranges, so the copy runs as two launches (1,024 ranges
