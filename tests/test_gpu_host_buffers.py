@@ -179,6 +179,42 @@ def test_staged_stitch_equals_the_stitch_from_device_pools(kind, n_groups):
         ref.close()
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_staged_stitch_on_random_batches(seed):
+    """The seeded random batches of the stitch tests (GQA or MLA, either
+    pairing, block sizes 1-33, truncated and repeated chunks, recompute
+    widths 0-6) through pic_stitch_staged with 1-4 request groups: equal to
+    pic_stitch over the device pool, bit for bit."""
+    from test_gpu_stitch import _random_workload
+    wl = _random_workload(seed)
+    ref = Stitched(wl, pool_device="cpu", spare_blocks=2).run()
+    try:
+        hk = ref.k_pool.cpu().pin_memory()
+        hv = ref.v_pool.cpu().pin_memory() if ref.v_pool is not None else None
+        dk = torch.zeros_like(ref.k_pool)
+        dv = torch.zeros_like(ref.v_pool) if ref.v_pool is not None else None
+        k_cache = torch.empty_like(ref.k_cache)
+        k_cache.view(torch.int16).fill_(-1)
+        v_cache = None
+        if ref.v_cache is not None:
+            v_cache = torch.empty_like(ref.v_cache)
+            v_cache.view(torch.int16).fill_(-1)
+        ridx, indptr = torch.full_like(ref.ridx, -7), torch.full_like(ref.indptr, -7)
+        n_groups = 1 + seed % 4
+        ws = torch.empty(pic.pic_stitch_staged_workspace_bytes(ref.ctx, ref.plans, n_groups), dtype=torch.uint8,
+                         device=DEV)
+        pic.pic_stitch_staged(ref.ctx, ref.plans, hk, hv, dk, dv, k_cache, v_cache, ref.d_bt, ridx, indptr, ws,
+                              n_groups=n_groups)
+        assert pic.pic_query_device_status(ref.ctx, ws) == 0
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(k_cache), bits(ref.k_cache))
+        if v_cache is not None:
+            assert np.array_equal(bits(v_cache), bits(ref.v_cache))
+        assert torch.equal(ridx[:ref.n_rec], ref.ridx[:ref.n_rec]) and torch.equal(indptr, ref.indptr)
+    finally:
+        ref.close()
+
+
 def test_stage_pool_over_more_ranges_than_one_launch_takes():
     """1,100 chunks of 2 tokens, one request taking the first token of each:
     1,100 separate row ranges, so the copy runs as two launches (1,024 ranges
