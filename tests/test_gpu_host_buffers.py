@@ -215,6 +215,72 @@ def test_staged_stitch_on_random_batches(seed):
         ref.close()
 
 
+def _mixed_context(m, nb):
+    """Pool chunks 0-2, chunk B resident in cache blocks 40-42 (40 tokens
+    cached at position 300) and chunk C in blocks 44-45 (20 tokens at 50);
+    three requests: B mapped at a block boundary, C copied after an odd
+    offset, and pool chunks only."""
+    ctx = pic.create_from_spec(pic.model_spec_from(m), nb)
+    lens, offs = [40, 17, 100], [0, 40, 57]
+    ids = [pic.pic_register_chunk(ctx, W.chunk_key("mixed", c), offs[c], lens[c])[0] for c in range(3)]
+    b = pic.pic_register_chunk_blocks(ctx, W.chunk_key("mixed", 9), [40, 41, 42], 40, 300)[0]
+    c_ = pic.pic_register_chunk_blocks(ctx, W.chunk_key("mixed", 10), [44, 45], 20, 50)[0]
+    plans, tables = [], []
+    for chunks, alias in (([b, ids[0], ids[2]], True), ([ids[1], c_, ids[0]], False), ([ids[2], ids[1]], False)):
+        plan, bt = pic.pic_build_block_table(ctx, chunks, 12, alias=alias, k_nonleading=4)
+        plans.append(plan)
+        tables.append(bt)
+    return ctx, plans, np.stack(tables), sum(lens)
+
+
+def test_staged_stitch_with_block_resident_and_mapped_chunks():
+    """A block-resident chunk mapped into one request (its keys rotated in
+    place in the cache, nothing staged) and another copied into a second
+    request, beside pool chunks: pic_stitch_staged from a pinned host pool leaves the cache, the
+    recompute list and the CSR offsets bit for bit as pic_stitch from the
+    device pool does, on two contexts built the same way."""
+    m = W.Model("mixed", "gqa", 2, 2, 128, 128, 0, "neox", 1e4, 16)
+    nb = 64
+    g = torch.Generator().manual_seed(21)
+    ctx_a, plans_a, tables, P = _mixed_context(m, nb)
+    ctx_b, plans_b, tables_b, _ = _mixed_context(m, nb)
+    try:
+        assert np.array_equal(tables, tables_b)
+        assert pic.pic_plan_segment_mode(plans_a[0], 0) == pic.PIC_SEG_MAPPED
+        assert pic.pic_plan_segment_mode(plans_a[1], 1) == pic.PIC_SEG_COPY_BLOCKS
+        k_pool = torch.randn((2, P, 2, 128), generator=g).to(torch.bfloat16)
+        v_pool = torch.randn((2, P, 2, 128), generator=g).to(torch.bfloat16)
+        cache_k = torch.randn((2, nb, 16, 2, 128), generator=g).to(torch.bfloat16)
+        cache_v = torch.randn((2, nb, 16, 2, 128), generator=g).to(torch.bfloat16)
+        bt = torch.from_numpy(tables).to(DEV)
+        n_rec = sum(pic.pic_plan_info(p)["num_recompute"] for p in plans_a)
+        outs = []
+        for ctx, plans, staged in ((ctx_a, plans_a, False), (ctx_b, plans_b, True)):
+            kc, vc = cache_k.to(DEV), cache_v.to(DEV)
+            ridx = torch.full((n_rec,), -7, dtype=torch.int32, device=DEV)
+            indptr = torch.full((4,), -7, dtype=torch.int32, device=DEV)
+            if staged:
+                dk, dv = torch.zeros((2, P, 2, 128), dtype=torch.bfloat16, device=DEV), torch.zeros(
+                    (2, P, 2, 128), dtype=torch.bfloat16, device=DEV)
+                ws = torch.empty(pic.pic_stitch_staged_workspace_bytes(ctx, plans, 2), dtype=torch.uint8, device=DEV)
+                pic.pic_stitch_staged(ctx, plans, k_pool.pin_memory(), v_pool.pin_memory(), dk, dv, kc, vc, bt, ridx,
+                                      indptr, ws, n_groups=2)
+            else:
+                ws = torch.empty(pic.pic_workspace_bytes(ctx, plans), dtype=torch.uint8, device=DEV)
+                pic.pic_stitch(ctx, plans, k_pool.to(DEV), v_pool.to(DEV), kc, vc, bt, ridx, indptr, ws)
+            assert pic.pic_query_device_status(ctx, ws) == 0
+            torch.cuda.synchronize()
+            outs.append((bits(kc), bits(vc), ridx.cpu(), indptr.cpu()))
+        (ka, va, ra, ia), (kb, vb, rb, ib) = outs
+        assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+        assert torch.equal(ra, rb) and torch.equal(ia, ib)
+        # the mapped chunk's keys moved in place: blocks 40-42 changed
+        assert not np.array_equal(ka[:, 40:43], bits(cache_k)[:, 40:43])
+    finally:
+        pic.pic_destroy(ctx_a)
+        pic.pic_destroy(ctx_b)
+
+
 def test_stage_pool_over_more_ranges_than_one_launch_takes():
     """1,100 chunks of 2 tokens, one request taking the first token of each:
     1,100 separate row ranges, so the copy runs as two launches (1,024 ranges
