@@ -281,6 +281,46 @@ def test_staged_stitch_with_block_resident_and_mapped_chunks():
         pic.pic_destroy(ctx_b)
 
 
+def test_serving_stress_full_size_staged():
+    """The benchmark's end-to-end launch at full size: the serving-stress pool
+    (61 GB of K and V) in pinned host memory, staged by pic_stitch_staged in
+    32 request groups into a cleared device pool and stitched into the
+    137 GB cache.  Sampled rows against the oracle (keys per element within
+    the contract, values bit for bit), the staged rows equal to the host rows,
+    the recompute list exact, and the staged bytes the distinct rows read."""
+    from test_gpu_stitch import _check_sampled, _sample_rows
+    wl = W.serving_stress()
+    st = Stitched(wl)
+    try:
+        hk = torch.empty(st.k_pool.shape, dtype=st.k_pool.dtype, pin_memory=True)
+        hk.copy_(st.k_pool)
+        hv = torch.empty(st.v_pool.shape, dtype=st.v_pool.dtype, pin_memory=True)
+        hv.copy_(st.v_pool)
+        st.k_pool.zero_()
+        st.v_pool.zero_()
+        ws = torch.empty(pic.pic_stitch_staged_workspace_bytes(st.ctx, st.plans, 32), dtype=torch.uint8, device=DEV)
+        n = pic.pic_stitch_staged(st.ctx, st.plans, hk, hv, st.k_pool, st.v_pool, st.k_cache, st.v_cache, st.d_bt,
+                                  st.ridx, st.indptr, ws, n_groups=32)
+        assert pic.pic_query_device_status(st.ctx, ws) == 0
+        torch.cuda.synchronize()
+        distinct, read = pic.pic_pool_read_rows(st.ctx, st.plans)
+        assert read == wl.token_layers // wl.model.num_layers and distinct < read
+        assert n == distinct * wl.model.num_layers * 2048 * 2
+        segs, tables, rec = oracle_side(wl, st.nb)
+        _check_sampled(st, segs, tables, 6000, 5)
+        l_idx, _, _, src, _ = _sample_rows(st, segs, tables, 6000, 5)
+        li, si = l_idx.cpu(), src.cpu()
+        assert np.array_equal(bits(st.k_pool[l_idx, src]), bits(hk[li, si]))
+        assert np.array_equal(bits(st.v_pool[l_idx, src]), bits(hv[li, si]))
+        indptr, idx = oracle.recompute_csr(rec)
+        assert st.indptr.cpu().tolist() == indptr.tolist()
+        assert st.ridx.cpu().numpy()[:st.n_rec].tolist() == idx.tolist()
+    finally:
+        st.close()
+        del st
+        torch.cuda.empty_cache()
+
+
 def test_stage_pool_over_more_ranges_than_one_launch_takes():
     """1,100 chunks of 2 tokens, one request taking the first token of each:
     1,100 separate row ranges, so the copy runs as two launches (1,024 ranges
